@@ -1,0 +1,233 @@
+/*
+ * kvint2.h -- C ABI of the GB300 2-bit KV-cache hot path (OSCAR-style).
+ *
+ * The method (gist.science explainer "OSCAR: Offline Spectral Covariance-
+ * Aware Rotation for 2-bit KV Cache Quantization", section 2.2 B "Online-
+ * Betriebsphase"; yunpan.plus OSCAR write-up, sections "1. 三段式 Token 池"
+ * and "2. 在线量化与反量化"):
+ *   - each sequence's KV cache has three tiers per KV head: the first 64
+ *     tokens (sink) and the last 256 tokens (recent) in BF16, everything in
+ *     between (history) in INT2;
+ *   - a token leaving the recent window is rotated by a fixed per-head
+ *     orthogonal matrix R (x' = x R), clipped per rotated channel, quantized
+ *     to asymmetric INT2 with an fp16 scale and zero per token and channel
+ *     group, and packed four codes per byte into paged history blocks;
+ *   - decode attention dequantizes the history on the fly, attends over all
+ *     three tiers with one softmax, and rotates the history value
+ *     accumulator back by R^T.
+ *
+ * Conventions for every entry point
+ *   - Pointers named "device" are CUDA device pointers on the pool's device;
+ *     host pointers are named "host".  The caller owns every buffer it
+ *     passes; the pool owns its own storage.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *     default stream) unless stated otherwise, and validates its arguments on
+ *     the host first: on failure it launches nothing and returns
+ *     KV_ERR_INVALID_ARG or KV_ERR_UNSUPPORTED.  A failed launch returns
+ *     KV_ERR_CUDA.
+ *   - Problems only the GPU can see (a page id outside [0, num_pages), a
+ *     length above capacity) are recorded in the pool's device error word and
+ *     the offending work is skipped; no kernel traps.  Read it with
+ *     kv_pool_get_error().
+ *   - Supported: head_dim 128, page_size 16 or 32, group_size 64 or 128,
+ *     num_q_heads / num_kv_heads in {1, 2, 4, 8, 16}.
+ *   - Calls that touch the same pool layer must be ordered on one stream.
+ */
+#ifndef KVINT2_H
+#define KVINT2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KV_OK = 0,
+  KV_ERR_INVALID_ARG = 1,  /* bad pointer, size, index or pool kind          */
+  KV_ERR_OOM = 2,          /* device allocation failed                       */
+  KV_ERR_CUDA = 3,         /* a CUDA call or launch failed                   */
+  KV_ERR_UNSUPPORTED = 4,  /* valid but not implemented (e.g. head_dim 64)   */
+  KV_ERR_DEVICE = 5,       /* kv_pool_get_error: the device recorded an error */
+  KV_ERR_TIMEOUT = 6       /* reserved: a bounded device wait gave up        */
+} kv_status_t;
+
+/* Device error codes reported by kv_pool_get_error(). */
+enum {
+  KV_DEVERR_NONE = 0,
+  KV_DEVERR_PAGE_ID = 1,      /* page table entry outside [0, num_pages)     */
+  KV_DEVERR_LENGTH = 2,       /* a length above the tier / table capacity    */
+  KV_DEVERR_SEQ_RANGE = 3     /* cu_tokens not monotone or history overflow  */
+};
+
+typedef enum { KV_POOL_INT2_3TIER = 0, KV_POOL_BF16 = 1 } kv_pool_kind_t;
+
+typedef struct {
+  int32_t kind;           /* kv_pool_kind_t                                  */
+  int32_t num_layers;
+  int32_t num_q_heads;    /* Hq; GQA group G = Hq / Hkv, q head h -> KV head h / G */
+  int32_t num_kv_heads;   /* Hkv                                             */
+  int32_t head_dim;       /* must be 128                                     */
+  int32_t page_size;      /* tokens per page: 16 or 32                       */
+  int32_t group_size;     /* INT2 channel group: 64 or 128 (INT2 pool only)  */
+  int32_t sink_tokens;    /* 64 for the pages' layout (INT2 pool only)       */
+  int32_t recent_tokens;  /* 256 for the pages' layout (INT2 pool only)      */
+  int32_t max_seqs;       /* sequence slots of the sink / recent tiers       */
+  int64_t num_pages;      /* physical pages per layer                        */
+} kv_pool_config_t;
+
+/* Where the pool keeps its data (device pointers and byte strides), so a
+ * caller can copy tiers in or out.  For layer `l`:
+ *   INT2 history block of (page p, KV head g):
+ *       hist + l*hist_layer_stride + p*hist_page_stride + g*hist_head_stride
+ *     = page_size/16 tiles of tile_bytes each; a tile is
+ *       [K codes 512 B][V codes 512 B][scale/zero records 16 * rec_bytes B]
+ *     rec_bytes = 8 * 128/group_size: per group (s_k, z_k) fp16 pairs, then
+ *     per group (s_v, z_v); record slot 2*(t%8) + t/8 holds token t of the tile.
+ *     Code bit of (m, k, step) with m, k in [0,16), step in [0,8): 16-byte
+ *     lane L = 4*(m%8) + (k%8)/2, 32-bit little-endian word step/2, bit
+ *     16*(k%2) + 2*(4*(step%2) + m/8 + 2*(k/8)); K: m = token, k = channel%16,
+ *     step = channel/16; V: m = channel%16, k = token, step = channel/16.
+ *   sink_k / sink_v:   bf16 [max_seqs][Hkv][sink_tokens][128]
+ *   recent_k/recent_v: bf16 [max_seqs][Hkv][recent_tokens][128] (ring)
+ *   BF16 pool: bf16_k / bf16_v bf16 [num_pages][Hkv][page_size][128]
+ * Pointers that do not apply to the pool kind are NULL. */
+typedef struct {
+  void* hist;
+  size_t hist_layer_stride, hist_page_stride, hist_head_stride, tile_bytes;
+  void* sink_k;
+  void* sink_v;
+  void* recent_k;
+  void* recent_v;
+  size_t tier_layer_stride;      /* bytes between layers of sink_* (and of recent_* below) */
+  size_t recent_layer_stride;
+  void* bf16_k;
+  void* bf16_v;
+  size_t bf16_layer_stride;      /* bytes between layers of bf16_k / bf16_v */
+} kv_pool_layout_t;
+
+typedef struct kv_pool kv_pool_t;   /* opaque; owns all pool device memory */
+
+/* Create a pool on the current CUDA device.  Allocates and zeroes its
+ * storage (synchronously: the call returns when the pool is ready).
+ * Rotations default to identity and clips to +inf until set.
+ * Returns KV_ERR_OOM if the device allocation fails. */
+kv_status_t kv_pool_create(const kv_pool_config_t* cfg, void* stream, kv_pool_t** out);
+
+/* Free the pool's device memory (synchronises the device first). */
+kv_status_t kv_pool_destroy(kv_pool_t* pool);
+
+/* Set the fixed rotation and clip thresholds of one layer (gist.science
+ * explainer section 2.2 A: R_K = U_Q H P_br, R_V = U_S H P_br, per-layer clip
+ * thresholds from rotated calibration data).
+ *   R_k, R_v   device fp32 [Hkv][128][128] row-major; x' = x . R (row vector).
+ *              Must be orthogonal (R R^T = I); the decode uses R^T as inverse.
+ *   clip_k/v   device fp32 [Hkv][128] thresholds c_j > 0 on rotated channels,
+ *              y = min(max(x', -c), c); +inf disables clipping.
+ * The values are copied into the pool (asynchronously on `stream`; the
+ * inputs may be freed once the stream reaches this point). */
+kv_status_t kv_pool_set_rotation(kv_pool_t* pool, int32_t layer, const float* R_k,
+                                 const float* R_v, const float* clip_k, const float* clip_v,
+                                 void* stream);
+
+/* Fill `out` with the pool's device pointers and strides for `layer`. */
+kv_status_t kv_pool_get_layout(const kv_pool_t* pool, int32_t layer, kv_pool_layout_t* out);
+
+/* Read and clear the device error word (synchronous).  *device_error_code
+ * receives a KV_DEVERR_* value; the return is KV_ERR_DEVICE if it was
+ * nonzero, KV_OK otherwise. */
+kv_status_t kv_pool_get_error(kv_pool_t* pool, int32_t* device_error_code);
+
+/* Write BF16 tokens into the sink (tier 0) or recent ring (tier 1) of an
+ * INT2 pool: row i goes to sequence slot seq[i], position slot[i] of that
+ * tier, all KV heads.  k, v: device bf16 [n_rows][Hkv][128]; seq, slot:
+ * device int32 [n_rows].  Out-of-range seq/slot entries are skipped and
+ * flagged (KV_DEVERR_LENGTH). */
+kv_status_t kv_store_tier(kv_pool_t* pool, int32_t layer, int32_t tier, int32_t n_rows,
+                          const void* k, const void* v, const int32_t* seq,
+                          const int32_t* slot, void* stream);
+
+/* Parity entry of the quantizer: clip -> INT2 quantize -> pack for rows that
+ * are already rotated (yunpan.plus write-up section 2: "裁剪 -> 量化 -> 打包";
+ * four 2-bit codes per byte).
+ *   tensor     0 = K (uses clip_k), 1 = V (uses clip_v) of `layer`
+ *   x_rot      device fp32 [n_rows][Hkv][128]
+ *   codes      device uint8 [n_rows][Hkv][32]: byte b holds channels 4b..4b+3,
+ *              channel 4b+j in bits [2j, 2j+2)
+ *   scale_zero device fp16 pairs [n_rows][Hkv][128/group_size][2] = (s, z)
+ * Quantizer (per row, head, group of group_size contiguous channels, fp32):
+ *   s = fp16((max - min) / 3), z = fp16(min), both saturated to +-65504;
+ *   code = s == 0 ? 0 : clamp(rint((y - z) / s), 0, 3), ties to even. */
+kv_status_t kv_quantize_pack_f32(kv_pool_t* pool, int32_t layer, int32_t tensor,
+                                 int64_t n_rows, const float* x_rot, uint8_t* codes,
+                                 void* scale_zero, void* stream);
+
+/* Fused append (the eviction step of the yunpan.plus write-up section 2):
+ * rotate by R_k / R_v, clip, quantize and pack K and V tokens into the INT2
+ * history pages of `layer`.
+ *   k, v        device bf16 [T][Hkv][128], T = cu_tokens[n_seqs]
+ *   cu_tokens   device int32 [n_seqs+1], prefix sums of tokens per sequence
+ *   hist_start  device int32 [n_seqs]: history position of each sequence's
+ *               first appended token (its tokens go to consecutive positions)
+ *   page_table  device int32 [n_seqs][max_pages_per_seq]: history position p
+ *               of sequence i lives in page page_table[i][p / page_size]
+ *   max_tokens_per_seq  host bound on tokens of any one sequence (sizes the
+ *               grid; sequences above it are flagged and truncated)
+ * Tiles partly covered keep the other tokens' bits (appends may continue a
+ * partly filled page).  Rotation runs on tensor cores with R split into two
+ * bf16 terms (about 16 significant bits). */
+kv_status_t kv_append_quantize(kv_pool_t* pool, int32_t layer, int32_t n_seqs,
+                               const void* k, const void* v, const int32_t* cu_tokens,
+                               const int32_t* hist_start, const int32_t* page_table,
+                               int32_t max_pages_per_seq, int32_t max_tokens_per_seq,
+                               void* stream);
+
+/* Bytes of device workspace kv_decode_attention / kv_decode_attention_bf16
+ * need for a batch of B sequences whose history (INT2 pool) or total length
+ * (BF16 pool) is at most max_len tokens.  0 on invalid arguments. */
+size_t kv_decode_workspace_bytes(const kv_pool_t* pool, int32_t B, int32_t max_len);
+
+/* One decode step of one layer for B sequences over the three-tier pool
+ * (gist.science explainer section 2.2 B): rotate q by R_k, attend over sink,
+ * history (INT2, dequantized on the fly in registers) and recent tiers with
+ * one split-K online softmax, rotate the history value accumulator back by
+ * R_v^T, and merge everything into fp32 outputs.
+ *   q            device bf16 [B][Hq][128]; sequence b uses pool slot b
+ *   sink_len     device int32 [B] (<= sink_tokens)
+ *   hist_len     device int32 [B] (<= max_hist_len and the page table's span)
+ *   recent_len   device int32 [B] (<= recent_tokens)
+ *   recent_start device int32 [B]: ring index of the oldest recent token
+ *   page_table   device int32 [B][max_pages_per_seq] (history pages)
+ *   max_hist_len host bound on hist_len (sizes the grid)
+ *   softmax_scale  tau in exp(tau q.k) (1/sqrt(128) for standard attention)
+ *   out          device fp32 [B][Hq][128]
+ *   workspace    device, >= kv_decode_workspace_bytes(pool, B, max_hist_len) */
+kv_status_t kv_decode_attention(kv_pool_t* pool, int32_t layer, int32_t B, const void* q,
+                                const int32_t* sink_len, const int32_t* hist_len,
+                                const int32_t* recent_len, const int32_t* recent_start,
+                                const int32_t* page_table, int32_t max_pages_per_seq,
+                                int32_t max_hist_len, float softmax_scale, float* out,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Append BF16 tokens to an all-BF16 paged pool (the baseline the INT2 path is
+ * compared with).  k, v device bf16 [T][Hkv][128]; token i of sequence s goes
+ * to position start_pos[s] + i, page page_table[s][pos / page_size]. */
+kv_status_t kv_append_bf16(kv_pool_t* pool, int32_t layer, int32_t n_seqs, const void* k,
+                           const void* v, const int32_t* cu_tokens, const int32_t* start_pos,
+                           const int32_t* page_table, int32_t max_pages_per_seq,
+                           int32_t max_tokens_per_seq, void* stream);
+
+/* Decode attention over an all-BF16 paged pool: plain split-K softmax
+ * attention of q [B][Hq][128] over seq_len[b] tokens, fp32 out [B][Hq][128]. */
+kv_status_t kv_decode_attention_bf16(kv_pool_t* pool, int32_t layer, int32_t B, const void* q,
+                                     const int32_t* seq_len, const int32_t* page_table,
+                                     int32_t max_pages_per_seq, int32_t max_seq_len,
+                                     float softmax_scale, float* out, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVINT2_H */
