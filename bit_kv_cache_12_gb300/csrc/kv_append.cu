@@ -1,0 +1,563 @@
+// Append path: rotate -> clip -> asymmetric INT2 quantize -> pack into pages.
+//
+// Method: yunpan.plus OSCAR write-up, "2. 在线量化与反量化" (a token leaving
+// the recent window goes through rotate, clip, quantize and pack, four 2-bit
+// codes per byte, into the INT2 history); gist.science OSCAR explainer,
+// section 2.2 B (history is stored after the fixed rotation and the clip).
+//
+// GPU design: a warp owns one 16-token tile of one KV head and one tensor.
+// The rotation x' = x R runs on the tensor cores (mma.sync m16n8k16 bf16):
+// x is exact in bf16 and R is split into bf16 hi + lo terms, fp32 accumulate.
+// The MMA accumulator layout is arranged so that each lane ends up owning
+// exactly the 64 codes of its own 16-byte slot of the stored tile (K: x R with
+// tokens as rows; V: R^T x^T with channels as rows), so packing is lane-local
+// and every tile is written with one 16-byte store per lane.
+#include "kv_device.cuh"
+#include "kv_internal.h"
+
+namespace kvint2 {
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// parity entry: clip + quantize + canonical pack of already rotated fp32 rows
+// one warp per (row, head); lane owns channels 4*lane .. 4*lane+3 (one byte)
+// ---------------------------------------------------------------------------
+template <int GS>
+__global__ void quantize_pack_kernel(const float* __restrict__ x, const float* __restrict__ clip,
+                                     uint8_t* __restrict__ codes, __half2* __restrict__ sz,
+                                     long long n_items, int Hkv) {
+  const long long item = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (item >= n_items) return;
+  const int lane = threadIdx.x & 31;
+  const int head = (int)(item % Hkv);
+  const float4 v = *reinterpret_cast<const float4*>(x + item * 128 + 4 * lane);
+  const float4 c = *reinterpret_cast<const float4*>(clip + head * 128 + 4 * lane);
+  float y[4] = {clip_to(v.x, c.x), clip_to(v.y, c.y), clip_to(v.z, c.z), clip_to(v.w, c.w)};
+  float mn = fminf(fminf(y[0], y[1]), fminf(y[2], y[3]));
+  float mx = fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
+  constexpr int kLanes = GS / 4;   // lanes per group
+#pragma unroll
+  for (int o = 1; o < kLanes; o <<= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  const ScaleZero q = scale_zero(mn, mx);
+  uint32_t byte = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) byte |= quant_code(y[e], q) << (2 * e);
+  codes[item * 32 + lane] = (uint8_t)byte;
+  if ((lane % kLanes) == 0) sz[item * (128 / GS) + lane / kLanes] = __halves2half2(q.sh, q.zh);
+}
+
+// ---------------------------------------------------------------------------
+// fused append
+// ---------------------------------------------------------------------------
+struct AppendArgs {
+  uint8_t* hist;            // layer base
+  size_t page_bytes, head_block;
+  int tile_bytes, tiles_per_page, P;
+  const uint16_t* k;
+  const uint16_t* v;
+  const int32_t* cu;
+  const int32_t* hist_start;
+  const int32_t* pt;
+  int max_pages, n_seqs, max_tiles, Hkv;
+  long long num_pages;
+  const uint4* rfrag;       // layer base [Hkv][2][4096]
+  const float* clip;        // layer base [2][Hkv][128]
+  int tasks_per_cta;
+  int* err;
+};
+
+__device__ __forceinline__ void load_row64(const uint16_t* row, bool ok, uint32_t (&w)[16]) {
+  if (ok) {
+    const uint4* p = reinterpret_cast<const uint4*>(row);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint4 t = __ldg(p + u);
+      w[4 * u + 0] = t.x; w[4 * u + 1] = t.y; w[4 * u + 2] = t.z; w[4 * u + 3] = t.w;
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < 16; ++u) w[u] = 0u;
+  }
+}
+
+__device__ __forceinline__ void store_words(uint8_t* dst, const uint32_t (&w)[4],
+                                            const uint32_t (&mask)[4], bool full) {
+  uint4* p = reinterpret_cast<uint4*>(dst);
+  if (full) {
+    *p = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+    const uint4 o = *p;
+    *p = make_uint4((o.x & ~mask[0]) | (w[0] & mask[0]), (o.y & ~mask[1]) | (w[1] & mask[1]),
+                    (o.z & ~mask[2]) | (w[2] & mask[2]), (o.w & ~mask[3]) | (w[3] & mask[3]));
+  }
+}
+
+template <int GS>
+__global__ void __launch_bounds__(256, 2) append_kernel(AppendArgs a) {
+  extern __shared__ uint4 sfrag[];                 // 4096 fragments, then clip
+  float* sclip = reinterpret_cast<float*>(sfrag + 4096);
+  const int g = blockIdx.y, tensor = blockIdx.z;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r = lane >> 2, j = lane & 3;
+  constexpr int NG = 128 / GS;
+
+  const uint4* src = a.rfrag + ((size_t)g * 2 + tensor) * 4096;
+  for (int i = threadIdx.x; i < 4096; i += blockDim.x) sfrag[i] = __ldg(src + i);
+  if (threadIdx.x < 128) sclip[threadIdx.x] = a.clip[((size_t)tensor * a.Hkv + g) * 128 + threadIdx.x];
+  __syncthreads();
+
+  const long long total = (long long)a.n_seqs * a.max_tiles;
+  const long long t0 = (long long)blockIdx.x * a.tasks_per_cta;
+  const long long t1 = min(total, t0 + a.tasks_per_cta);
+  for (long long task = t0 + warp; task < t1; task += 8) {
+    const int b = (int)(task / a.max_tiles), lt = (int)(task % a.max_tiles);
+    const int c0 = __ldg(a.cu + b), nb = __ldg(a.cu + b + 1) - c0;
+    const int h0 = __ldg(a.hist_start + b);
+    if (nb <= 0) {
+      if (nb < 0 && lt == 0 && lane == 0) flag_error(a.err, KV_DEVERR_SEQ_RANGE);
+      continue;
+    }
+    if (h0 < 0 || (long long)h0 + nb > (long long)a.max_pages * a.P) {
+      if (lt == 0 && lane == 0) flag_error(a.err, KV_DEVERR_SEQ_RANGE);
+      continue;
+    }
+    const int first = h0 / kTile, last = (h0 + nb - 1) / kTile;
+    if (lt == 0 && last - first + 1 > a.max_tiles && lane == 0) flag_error(a.err, KV_DEVERR_LENGTH);
+    const int tile = first + lt;
+    if (tile > last) continue;
+    const int pid = __ldg(a.pt + (size_t)b * a.max_pages + (tile * kTile) / a.P);
+    if (pid < 0 || pid >= a.num_pages) {
+      if (lane == 0) flag_error(a.err, KV_DEVERR_PAGE_ID);
+      continue;
+    }
+    uint8_t* tb = a.hist + (size_t)pid * a.page_bytes + (size_t)g * a.head_block +
+                  (size_t)((tile * kTile) % a.P / kTile) * a.tile_bytes;
+    const int p0 = max(h0, tile * kTile), p1 = min(h0 + nb, tile * kTile + kTile);
+    const bool full = (p0 == tile * kTile) && (p1 == tile * kTile + kTile);
+    auto row_ok = [&](int row) { const int p = tile * kTile + row; return p >= p0 && p < p1; };
+    auto row_ptr = [&](int row) {
+      const int tok = c0 + (tile * kTile + row - h0);
+      return (tensor == 0 ? a.k : a.v) + ((size_t)tok * a.Hkv + g) * 128 + 32 * j;
+    };
+    uint32_t xr[16], xr8[16];
+    load_row64(row_ptr(r), row_ok(r), xr);
+    load_row64(row_ptr(r + 8), row_ok(r + 8), xr8);
+
+    uint32_t word[4] = {0u, 0u, 0u, 0u}, mask[4] = {0u, 0u, 0u, 0u};
+    if (tensor == 0) {
+      // ---- K: D[token][out channel] = x R_k, tokens as MMA rows ----
+      float acc[16][4];
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc[nt][u] = 0.f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+          const uint4 f = sfrag[(s * 16 + nt) * 32 + lane];
+          mma_bf16(acc[nt], xr[2 * s], xr8[2 * s], xr[2 * s + 1], xr8[2 * s + 1], f.x, f.y);
+          mma_bf16(acc[nt], xr[2 * s], xr8[2 * s], xr[2 * s + 1], xr8[2 * s + 1], f.z, f.w);
+        }
+      }
+      // clip; per row (token) and group min / max
+      float mn[2][NG], mx[2][NG];
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int grp = 0; grp < NG; ++grp) { mn[q][grp] = INFINITY; mx[q][grp] = -INFINITY; }
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        const int grp = (GS == 64) ? (nt >> 3) : 0;
+        const float cl0 = sclip[8 * nt + 2 * j], cl1 = sclip[8 * nt + 2 * j + 1];
+        acc[nt][0] = clip_to(acc[nt][0], cl0);
+        acc[nt][1] = clip_to(acc[nt][1], cl1);
+        acc[nt][2] = clip_to(acc[nt][2], cl0);
+        acc[nt][3] = clip_to(acc[nt][3], cl1);
+        mn[0][grp] = fminf(mn[0][grp], fminf(acc[nt][0], acc[nt][1]));
+        mx[0][grp] = fmaxf(mx[0][grp], fmaxf(acc[nt][0], acc[nt][1]));
+        mn[1][grp] = fminf(mn[1][grp], fminf(acc[nt][2], acc[nt][3]));
+        mx[1][grp] = fmaxf(mx[1][grp], fmaxf(acc[nt][2], acc[nt][3]));
+      }
+      ScaleZero q[2][NG];
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq)
+#pragma unroll
+        for (int grp = 0; grp < NG; ++grp) {
+          float a_ = mn[qq][grp], b_ = mx[qq][grp];
+#pragma unroll
+          for (int o = 1; o < 4; o <<= 1) {
+            a_ = fminf(a_, __shfl_xor_sync(0xffffffffu, a_, o));
+            b_ = fmaxf(b_, __shfl_xor_sync(0xffffffffu, b_, o));
+          }
+          q[qq][grp] = scale_zero(a_, b_);
+        }
+      const bool ok0 = row_ok(r), ok1 = row_ok(r + 8);
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        const int grp = (GS == 64) ? (nt >> 3) : 0;
+        const int w = nt >> 2;
+        const int pi0 = 4 * ((nt >> 1) & 1) + 2 * (nt & 1);   // row r; row r+8 adds 1
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const uint32_t ca = quant_code(acc[nt][e], q[0][grp]);
+          const uint32_t cb = quant_code(acc[nt][2 + e], q[1][grp]);
+          const int bit_a = 16 * e + 2 * pi0, bit_b = 16 * e + 2 * (pi0 + 1);
+          word[w] |= (ca << bit_a) | (cb << bit_b);
+          mask[w] |= (ok0 ? (3u << bit_a) : 0u) | (ok1 ? (3u << bit_b) : 0u);
+        }
+      }
+      store_words(tb + 16 * lane, word, mask, full);
+      if (j == 0) {
+        const int rec = 8 * NG;
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+          if (!(qq ? ok1 : ok0)) continue;
+          const int t = r + 8 * qq;
+          __half2* recp = reinterpret_cast<__half2*>(tb + 1024 + (2 * (t & 7) + (t >> 3)) * rec);
+#pragma unroll
+          for (int grp = 0; grp < NG; ++grp) recp[grp] = __halves2half2(q[qq][grp].sh, q[qq][grp].zh);
+        }
+      }
+    } else {
+      // ---- V: D[out channel][token] = R_v^T x^T, channels as MMA rows ----
+      float acc[8][2][4];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) acc[i][nt][u] = 0.f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 fh = sfrag[((i * 8 + s) * 2 + 0) * 32 + lane];
+          const uint4 fl = sfrag[((i * 8 + s) * 2 + 1) * 32 + lane];
+          mma_bf16(acc[i][0], fh.x, fh.y, fh.z, fh.w, xr[2 * s], xr[2 * s + 1]);
+          mma_bf16(acc[i][0], fl.x, fl.y, fl.z, fl.w, xr[2 * s], xr[2 * s + 1]);
+          mma_bf16(acc[i][1], fh.x, fh.y, fh.z, fh.w, xr8[2 * s], xr8[2 * s + 1]);
+          mma_bf16(acc[i][1], fl.x, fl.y, fl.z, fl.w, xr8[2 * s], xr8[2 * s + 1]);
+        }
+      }
+      // lane holds tokens 8*nt + 2j + e for channels 16i + r (+8)
+      float mn[2][2][NG], mx[2][2][NG];   // [nt][e][grp]
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+          for (int grp = 0; grp < NG; ++grp) { mn[nt][e][grp] = INFINITY; mx[nt][e][grp] = -INFINITY; }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int grp = (GS == 64) ? (i >> 2) : 0;
+        const float cl0 = sclip[16 * i + r], cl1 = sclip[16 * i + r + 8];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            acc[i][nt][e] = clip_to(acc[i][nt][e], cl0);
+            acc[i][nt][2 + e] = clip_to(acc[i][nt][2 + e], cl1);
+            mn[nt][e][grp] = fminf(mn[nt][e][grp], fminf(acc[i][nt][e], acc[i][nt][2 + e]));
+            mx[nt][e][grp] = fmaxf(mx[nt][e][grp], fmaxf(acc[i][nt][e], acc[i][nt][2 + e]));
+          }
+      }
+      ScaleZero q[2][2][NG];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+          for (int grp = 0; grp < NG; ++grp) {
+            float a_ = mn[nt][e][grp], b_ = mx[nt][e][grp];
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+              a_ = fminf(a_, __shfl_xor_sync(0xffffffffu, a_, o));
+              b_ = fmaxf(b_, __shfl_xor_sync(0xffffffffu, b_, o));
+            }
+            q[nt][e][grp] = scale_zero(a_, b_);
+          }
+      bool tok_ok[2][2];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) tok_ok[nt][e] = row_ok(8 * nt + 2 * j + e);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int grp = (GS == 64) ? (i >> 2) : 0;
+        const int w = i >> 1;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int pi0 = 4 * (i & 1) + 2 * nt;               // channel 16i+r; +8 adds 1
+            const uint32_t ca = quant_code(acc[i][nt][e], q[nt][e][grp]);
+            const uint32_t cb = quant_code(acc[i][nt][2 + e], q[nt][e][grp]);
+            const int bit_a = 16 * e + 2 * pi0, bit_b = 16 * e + 2 * (pi0 + 1);
+            word[w] |= (ca << bit_a) | (cb << bit_b);
+            if (tok_ok[nt][e]) mask[w] |= (3u << bit_a) | (3u << bit_b);
+          }
+      }
+      store_words(tb + 512 + 16 * lane, word, mask, full);
+      if (r == 0) {
+        const int rec = 8 * NG;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            if (!tok_ok[nt][e]) continue;
+            const int t = 8 * nt + 2 * j + e;
+            __half2* recp =
+                reinterpret_cast<__half2*>(tb + 1024 + (2 * (t & 7) + (t >> 3)) * rec) + NG;
+#pragma unroll
+            for (int grp = 0; grp < NG; ++grp)
+              recp[grp] = __halves2half2(q[nt][e][grp].sh, q[nt][e][grp].zh);
+          }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// rotation set-up: pool copies of R_k, R_v^T and the bf16 hi/lo MMA fragments
+// ---------------------------------------------------------------------------
+__global__ void rotation_copy_kernel(const float* __restrict__ Rk, const float* __restrict__ Rv,
+                                     float* __restrict__ dRk, float* __restrict__ dRvT, int Hkv) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= Hkv * 128 * 128) return;
+  const int h = idx >> 14, i = (idx >> 7) & 127, c = idx & 127;
+  dRk[idx] = Rk[idx];
+  dRvT[idx] = Rv[((size_t)h * 128 + c) * 128 + i];   // RvT[h][i][c] = Rv[h][c][i]
+}
+
+__device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  const __nv_bfloat16 l = __float2bfloat16_rn(x - __bfloat162float(h));
+  hi = __bfloat16_as_ushort(h);
+  lo = __bfloat16_as_ushort(l);
+}
+
+__device__ __forceinline__ uint32_t pack2(uint16_t a, uint16_t b) { return (uint32_t)a | ((uint32_t)b << 16); }
+
+// Input channel held by fragment k index kappa at k-step s (the lane j of
+// kappa owns input channels 32j .. 32j+31, so x rows load as 64-byte runs).
+__device__ __forceinline__ int in_ch(int s, int kappa) {
+  return 32 * ((kappa & 7) >> 1) + 4 * s + 2 * (kappa >> 3) + (kappa & 1);
+}
+
+__global__ void rotation_frag_kernel(const float* __restrict__ Rk, const float* __restrict__ Rv,
+                                     uint4* __restrict__ frag, int Hkv) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= Hkv * 2 * 4096) return;
+  const int h = idx / 8192, tensor = (idx / 4096) & 1, f = idx & 4095;
+  const int lane = f & 31;
+  const int r = lane >> 2, j = lane & 3;
+  uint4 out;
+  if (tensor == 0) {
+    // B operand of x R_k: element (kappa, n) = R_k[in_ch(s, kappa)][8 nt + n]
+    const int nt = (f >> 5) & 15, s = f >> 9;
+    const float* R = Rk + (size_t)h * 16384;
+    const int col = 8 * nt + r;
+    uint16_t hi[4], lo[4];
+    const int ks[4] = {2 * j, 2 * j + 1, 2 * j + 8, 2 * j + 9};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) split_bf16(R[in_ch(s, ks[u]) * 128 + col], hi[u], lo[u]);
+    out = make_uint4(pack2(hi[0], hi[1]), pack2(hi[2], hi[3]), pack2(lo[0], lo[1]), pack2(lo[2], lo[3]));
+  } else {
+    // A operand of R_v^T x^T: element (row m, kappa) = R_v[in_ch(s, kappa)][16 i + m]
+    const int hl = (f >> 5) & 1, s = (f >> 6) & 7, i = f >> 9;
+    const float* R = Rv + (size_t)h * 16384;
+    const int rows[2] = {16 * i + r, 16 * i + r + 8};
+    const int ks[2][2] = {{2 * j, 2 * j + 1}, {2 * j + 8, 2 * j + 9}};
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {   // a0 (r, k lo), a1 (r+8, k lo), a2 (r, k hi), a3 (r+8, k hi)
+      const int m = rows[q & 1];
+      uint16_t h0, l0, h1, l1;
+      split_bf16(R[in_ch(s, ks[q >> 1][0]) * 128 + m], h0, l0);
+      split_bf16(R[in_ch(s, ks[q >> 1][1]) * 128 + m], h1, l1);
+      w[q] = hl ? pack2(l0, l1) : pack2(h0, h1);
+    }
+    out = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  frag[idx] = out;
+}
+
+// ---------------------------------------------------------------------------
+// BF16 stores: BF16 pool pages and the sink / recent tiers
+// ---------------------------------------------------------------------------
+__global__ void append_bf16_kernel(uint16_t* __restrict__ bk, uint16_t* __restrict__ bv,
+                                   const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+                                   const int32_t* __restrict__ cu, const int32_t* __restrict__ start,
+                                   const int32_t* __restrict__ pt, int max_pages, int max_tokens,
+                                   int n_seqs, int Hkv, int P, long long num_pages, int* err) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long per_tok = (long long)Hkv * 16;
+  const long long total = (long long)n_seqs * max_tokens * per_tok;
+  if (idx >= total) return;
+  const int chunk = (int)(idx % 16);
+  const int g = (int)((idx / 16) % Hkv);
+  const long long vt = idx / per_tok;
+  const int s = (int)(vt / max_tokens), i = (int)(vt % max_tokens);
+  const int c0 = cu[s], n = cu[s + 1] - c0;
+  if (i >= n) return;
+  const int pos = start[s] + i;
+  if (pos < 0 || pos >= max_pages * P) {
+    flag_error(err, KV_DEVERR_SEQ_RANGE);
+    return;
+  }
+  const int pid = pt[(size_t)s * max_pages + pos / P];
+  if (pid < 0 || pid >= num_pages) {
+    flag_error(err, KV_DEVERR_PAGE_ID);
+    return;
+  }
+  const size_t dst = (((size_t)pid * Hkv + g) * P + pos % P) * 128 + chunk * 8;
+  const size_t src = ((size_t)(c0 + i) * Hkv + g) * 128 + chunk * 8;
+  *reinterpret_cast<uint4*>(bk + dst) = *reinterpret_cast<const uint4*>(k + src);
+  *reinterpret_cast<uint4*>(bv + dst) = *reinterpret_cast<const uint4*>(v + src);
+}
+
+__global__ void store_tier_kernel(uint16_t* __restrict__ tk, uint16_t* __restrict__ tv,
+                                  const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+                                  const int32_t* __restrict__ seq, const int32_t* __restrict__ slot,
+                                  int n_rows, int Hkv, int cap, int max_seqs, int* err) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)n_rows * Hkv * 16) return;
+  const int chunk = (int)(idx % 16);
+  const int g = (int)((idx / 16) % Hkv);
+  const int row = (int)(idx / (16 * Hkv));
+  const int sq = seq[row], sl = slot[row];
+  if (sq < 0 || sq >= max_seqs || sl < 0 || sl >= cap) {
+    flag_error(err, KV_DEVERR_LENGTH);
+    return;
+  }
+  const size_t dst = (((size_t)sq * Hkv + g) * cap + sl) * 128 + chunk * 8;
+  const size_t src = ((size_t)row * Hkv + g) * 128 + chunk * 8;
+  *reinterpret_cast<uint4*>(tk + dst) = *reinterpret_cast<const uint4*>(k + src);
+  *reinterpret_cast<uint4*>(tv + dst) = *reinterpret_cast<const uint4*>(v + src);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+cudaError_t launch_rotation_prep(const Pool& p, int layer, const float* Rk, const float* Rv,
+                                 cudaStream_t s) {
+  const int H = p.cfg.num_kv_heads;
+  const size_t mat = (size_t)H * 128 * 128;
+  float* dRk = p.Rk + (size_t)layer * mat;
+  float* dRvT = p.RvT + (size_t)layer * mat;
+  if (Rk != dRk || Rv != dRvT) {
+    rotation_copy_kernel<<<(unsigned)((mat + 255) / 256), 256, 0, s>>>(Rk, Rv, dRk, dRvT, H);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  uint4* frag = p.rfrag + (size_t)layer * H * 2 * rfrag_per_head();
+  const int n = H * 2 * 4096;
+  rotation_frag_kernel<<<(n + 255) / 256, 256, 0, s>>>(Rk, Rv, frag, H);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_store_tier(const Pool& p, int layer, int tier, int n_rows, const void* k,
+                              const void* v, const int32_t* seq, const int32_t* slot,
+                              cudaStream_t s) {
+  if (n_rows == 0) return cudaSuccess;
+  const int H = p.cfg.num_kv_heads;
+  uint16_t* tk = tier == 0 ? p.sink_k + (size_t)layer * p.sink_layer_stride
+                           : p.rec_k + (size_t)layer * p.rec_layer_stride;
+  uint16_t* tv = tier == 0 ? p.sink_v + (size_t)layer * p.sink_layer_stride
+                           : p.rec_v + (size_t)layer * p.rec_layer_stride;
+  const int cap = tier == 0 ? p.cfg.sink_tokens : p.cfg.recent_tokens;
+  const long long n = (long long)n_rows * H * 16;
+  store_tier_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(
+      tk, tv, static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), seq, slot, n_rows,
+      H, cap, p.cfg.max_seqs, p.err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_pack(const Pool& p, int layer, int tensor, int64_t n_rows,
+                                 const float* x, uint8_t* codes, void* sz, cudaStream_t s) {
+  if (n_rows == 0) return cudaSuccess;
+  const int H = p.cfg.num_kv_heads;
+  const long long items = (long long)n_rows * H;
+  const float* clip = p.clip + ((size_t)layer * 2 + tensor) * H * 128;
+  const unsigned blocks = (unsigned)((items + 7) / 8);
+  if (p.cfg.group_size == 64)
+    quantize_pack_kernel<64><<<blocks, 256, 0, s>>>(x, clip, codes, static_cast<__half2*>(sz), items, H);
+  else
+    quantize_pack_kernel<128><<<blocks, 256, 0, s>>>(x, clip, codes, static_cast<__half2*>(sz), items, H);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const Pool& p, int layer, int n_seqs, const void* k, const void* v,
+                          const int32_t* cu, const int32_t* hist_start, const int32_t* pt,
+                          int max_pages, int max_tokens, cudaStream_t s) {
+  if (n_seqs == 0 || max_tokens == 0) return cudaSuccess;
+  const int H = p.cfg.num_kv_heads;
+  AppendArgs a{};
+  a.hist = p.hist + (size_t)layer * p.hist_layer_stride;
+  a.page_bytes = p.page_bytes;
+  a.head_block = p.page_bytes / H;
+  a.tile_bytes = (int)p.tile_bytes;
+  a.tiles_per_page = p.cfg.page_size / kTile;
+  a.P = p.cfg.page_size;
+  a.k = static_cast<const uint16_t*>(k);
+  a.v = static_cast<const uint16_t*>(v);
+  a.cu = cu;
+  a.hist_start = hist_start;
+  a.pt = pt;
+  a.max_pages = max_pages;
+  a.n_seqs = n_seqs;
+  a.max_tiles = (max_tokens + kTile - 1) / kTile + 1;   // +1: an unaligned start spans one more
+  a.Hkv = H;
+  a.num_pages = p.cfg.num_pages;
+  a.rfrag = p.rfrag + (size_t)layer * H * 2 * rfrag_per_head();
+  a.clip = p.clip + (size_t)layer * 2 * H * 128;
+  a.err = p.err;
+  const long long tasks = (long long)n_seqs * a.max_tiles;
+  // CTAs per (head, tensor): enough to fill every SM twice over all heads/tensors
+  long long ctas = (2LL * p.sm_count + 2 * H - 1) / (2 * H);
+  ctas = max(1LL, min(ctas, (tasks + 7) / 8));
+  a.tasks_per_cta = (int)((tasks + ctas - 1) / ctas);
+  ctas = (tasks + a.tasks_per_cta - 1) / a.tasks_per_cta;
+  const size_t smem = 4096 * sizeof(uint4) + 128 * sizeof(float);
+  static bool attr64 = false, attr128 = false;
+  dim3 grid((unsigned)ctas, H, 2);
+  if (p.cfg.group_size == 64) {
+    if (!attr64) {
+      cudaError_t e = cudaFuncSetAttribute(append_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      attr64 = true;
+    }
+    append_kernel<64><<<grid, 256, smem, s>>>(a);
+  } else {
+    if (!attr128) {
+      cudaError_t e = cudaFuncSetAttribute(append_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      attr128 = true;
+    }
+    append_kernel<128><<<grid, 256, smem, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append_bf16(const Pool& p, int layer, int n_seqs, const void* k,
+                               const void* v, const int32_t* cu, const int32_t* start,
+                               const int32_t* pt, int max_pages, int max_tokens,
+                               cudaStream_t s) {
+  if (n_seqs == 0 || max_tokens == 0) return cudaSuccess;
+  const int H = p.cfg.num_kv_heads;
+  const long long n = (long long)n_seqs * max_tokens * H * 16;
+  append_bf16_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(
+      p.bk + (size_t)layer * p.bf16_layer_stride, p.bv + (size_t)layer * p.bf16_layer_stride,
+      static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), cu, start, pt, max_pages,
+      max_tokens, n_seqs, H, p.cfg.page_size, p.cfg.num_pages, p.err);
+  return cudaGetLastError();
+}
+
+}  // namespace kvint2

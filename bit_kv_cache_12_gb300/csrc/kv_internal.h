@@ -1,0 +1,82 @@
+// Internal declarations shared by the translation units of libkvint2.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/kvint2.h"
+
+namespace kvint2 {
+
+constexpr int kHeadDim = 128;
+constexpr int kTile = 16;           // tokens per INT2 history tile
+constexpr int kCodeBlock = 512;     // bytes of K (or V) codes per tile
+
+struct Pool {
+  kv_pool_config_t cfg;
+  int device = 0;
+  int sm_count = 0;
+  int G = 1;                        // q heads per KV head
+
+  // INT2 history: [layer][page][head][tiles_per_page][tile_bytes]
+  uint8_t* hist = nullptr;
+  size_t tile_bytes = 0, page_bytes = 0, hist_layer_stride = 0;
+  // BF16 tiers: [layer][seq][head][cap][128]
+  uint16_t* sink_k = nullptr;
+  uint16_t* sink_v = nullptr;
+  uint16_t* rec_k = nullptr;
+  uint16_t* rec_v = nullptr;
+  size_t sink_layer_stride = 0, rec_layer_stride = 0;   // elements
+  // BF16 pool: [layer][page][head][page_size][128]
+  uint16_t* bk = nullptr;
+  uint16_t* bv = nullptr;
+  size_t bf16_layer_stride = 0;     // elements
+
+  // per layer rotation data
+  float* Rk = nullptr;              // [layer][Hkv][128][128]  x' = x Rk
+  float* RvT = nullptr;             // [layer][Hkv][128][128]  RvT[i][c] = Rv[c][i]
+  float* clip = nullptr;            // [layer][2][Hkv][128]
+  uint4* rfrag = nullptr;           // [layer][Hkv][2][4096] bf16 hi/lo MMA fragments
+  unsigned* tickets = nullptr;      // [layer][max_seqs][Hkv] split-merge counters
+  int* err = nullptr;               // device error word
+};
+
+inline size_t rfrag_per_head() { return 4096; }   // uint4 per (head, tensor)
+
+// ---- launchers (return cudaSuccess or the launch error) --------------------
+cudaError_t launch_rotation_prep(const Pool& p, int layer, const float* Rk, const float* Rv,
+                                 cudaStream_t s);
+cudaError_t launch_store_tier(const Pool& p, int layer, int tier, int n_rows, const void* k,
+                              const void* v, const int32_t* seq, const int32_t* slot,
+                              cudaStream_t s);
+cudaError_t launch_quantize_pack(const Pool& p, int layer, int tensor, int64_t n_rows,
+                                 const float* x, uint8_t* codes, void* sz, cudaStream_t s);
+cudaError_t launch_append(const Pool& p, int layer, int n_seqs, const void* k, const void* v,
+                          const int32_t* cu, const int32_t* hist_start, const int32_t* pt,
+                          int max_pages, int max_tokens, cudaStream_t s);
+cudaError_t launch_append_bf16(const Pool& p, int layer, int n_seqs, const void* k,
+                               const void* v, const int32_t* cu, const int32_t* start,
+                               const int32_t* pt, int max_pages, int max_tokens,
+                               cudaStream_t s);
+
+struct DecodePlan {
+  int n_split = 1;          // history splits per (sequence, KV head)
+  int tiles_per_split = 1;  // INT2: 16-token tiles; BF16: tokens
+  size_t partial_floats = 0;
+  size_t bytes = 0;
+};
+DecodePlan plan_decode_int2(const Pool& p, int B, int max_hist_len);
+DecodePlan plan_decode_bf16(const Pool& p, int B, int max_len);
+
+cudaError_t launch_decode_int2(const Pool& p, int layer, int B, const void* q,
+                               const int32_t* sink_len, const int32_t* hist_len,
+                               const int32_t* rec_len, const int32_t* rec_start,
+                               const int32_t* pt, int max_pages, const DecodePlan& plan,
+                               float scale, float* out, void* ws, cudaStream_t s);
+cudaError_t launch_decode_bf16(const Pool& p, int layer, int B, const void* q,
+                               const int32_t* seq_len, const int32_t* pt, int max_pages,
+                               const DecodePlan& plan, float scale, float* out, void* ws,
+                               cudaStream_t s);
+
+}  // namespace kvint2

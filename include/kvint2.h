@@ -30,7 +30,7 @@
  *     the offending work is skipped; no kernel traps.  Read it with
  *     kv_pool_get_error().
  *   - Supported: head_dim 128, page_size 16 or 32, group_size 64 or 128,
- *     num_q_heads / num_kv_heads in {1, 2, 4, 8, 16}.
+ *     num_q_heads / num_kv_heads in {1, 2, 4, 8}.
  *   - Calls that touch the same pool layer must be ordered on one stream.
  */
 #ifndef KVINT2_H

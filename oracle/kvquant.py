@@ -184,6 +184,22 @@ def _tile_maps():
 _KB, _KS, _VB, _VS = _tile_maps()
 
 
+def _inverse_map(bmap, smap):
+    """For each (byte, 2-bit slot) of a code block, the (token, channel) stored there."""
+    inv_t = np.empty((512, 4), np.int64)
+    inv_c = np.empty((512, 4), np.int64)
+    for t in range(TILE):
+        for c in range(HEAD_DIM):
+            inv_t[bmap[t, c], smap[t, c] // 2] = t
+            inv_c[bmap[t, c], smap[t, c] // 2] = c
+    return inv_t, inv_c
+
+
+_KINV = _inverse_map(_KB, _KS)
+_VINV = _inverse_map(_VB, _VS)
+_SLOT_SHIFT = np.array([0, 2, 4, 6], np.uint16)
+
+
 def tile_bytes(group_size):
     ng = HEAD_DIM // group_size
     return 1024 + TILE * 8 * ng
@@ -212,6 +228,56 @@ def pack_tile(kc, vc, sk, zk, sv, zv, group_size, base=None, valid=None):
         off = 1024 + (2 * (t % 8) + t // 8) * 8 * ng
         out[off:off + 8 * ng] = rec.view(np.uint8)
     return out
+
+
+def pack_tiles_full(kc, vc, sk, zk, sv, zv, group_size):
+    """Vectorised ``pack_tile`` for n complete tiles.
+
+    kc, vc uint8 [n, 16, 128]; s/z fp16 [n, 16, ng] -> uint8 [n, tile_bytes].
+    Each stored byte gathers its four codes through the inverse index map."""
+    n = kc.shape[0]
+    ng = HEAD_DIM // group_size
+    out = np.zeros((n, tile_bytes(group_size)), np.uint8)
+    for blk, codes, (it, ic) in ((0, kc, _KINV), (512, vc, _VINV)):
+        g = codes[:, it, ic].astype(np.uint16) << _SLOT_SHIFT
+        out[:, blk:blk + 512] = g.sum(axis=-1).astype(np.uint8)
+    rec = np.empty((n, TILE, 4 * ng), np.float16)
+    rec[:, :, 0:2 * ng:2] = sk; rec[:, :, 1:2 * ng:2] = zk
+    rec[:, :, 2 * ng::2] = sv; rec[:, :, 2 * ng + 1::2] = zv
+    order = np.array([t for r in range(8) for t in (r, r + 8)])   # record slot -> token
+    out[:, 1024:] = rec[:, order].reshape(n, -1).view(np.uint8)
+    return out
+
+
+def pack_history_full(k_bf16, v_bf16, Rk, Rv, clip_k, clip_v, page_table_row, num_pages,
+                      num_heads, page_size, group_size, pages_buf=None):
+    """Quantize and pack a whole history (positions 0..T-1) of one sequence,
+    all heads, vectorised.  k/v_bf16 [T, Hkv, 128] bf16 bits.  Tokens past T in
+    the last tile are zero codes with zero scale/zero."""
+    T = k_bf16.shape[0]
+    tb = tile_bytes(group_size)
+    tpp = page_size // TILE
+    if pages_buf is None:
+        pages_buf = np.zeros((num_pages, num_heads, tpp * tb), np.uint8)
+    ntiles = (T + TILE - 1) // TILE
+    pad = ntiles * TILE - T
+    ng = HEAD_DIM // group_size
+    for g in range(num_heads):
+        q = quantize_tokens(k_bf16[:, g], v_bf16[:, g], Rk[g], Rv[g], clip_k[g], clip_v[g],
+                            group_size)
+        def tiles(a, dtype):
+            a = np.concatenate([a, np.zeros((pad,) + a.shape[1:], dtype)]) if pad else a
+            return a.reshape((ntiles, TILE) + a.shape[1:])
+        blocks = pack_tiles_full(tiles(q["kc"], np.uint8), tiles(q["vc"], np.uint8),
+                                 tiles(q["sk"], np.float16), tiles(q["zk"], np.float16),
+                                 tiles(q["sv"], np.float16), tiles(q["zv"], np.float16), group_size)
+        ti = np.arange(ntiles)
+        pages = np.asarray(page_table_row)[(ti * TILE) // page_size]
+        within = (ti * TILE % page_size) // TILE
+        for w in range(tpp):
+            sel = within == w
+            pages_buf[pages[sel], g, w * tb:(w + 1) * tb] = blocks[sel]
+    return pages_buf
 
 
 def unpack_tile(buf, group_size):
@@ -272,19 +338,29 @@ def pack_history(pages_buf, page_table_row, hist_start, q, head, num_heads, page
     return pages_buf
 
 
+def unpack_tiles(blocks, group_size):
+    """Vectorised ``unpack_tile`` for blocks uint8 [n, tile_bytes]."""
+    ng = HEAD_DIM // group_size
+    blocks = np.asarray(blocks, dtype=np.uint8)
+    kc = (blocks[:, _KB] >> _KS) & 3
+    vc = (blocks[:, 512 + _VB] >> _VS) & 3
+    order = np.array([2 * (t % 8) + t // 8 for t in range(TILE)])   # token -> record slot
+    recs = np.ascontiguousarray(blocks[:, 1024:]).view(np.float16).reshape(-1, TILE, 4 * ng)[:, order]
+    return (kc.astype(np.uint8), vc.astype(np.uint8), recs[:, :, 0:2 * ng:2], recs[:, :, 1:2 * ng:2],
+            recs[:, :, 2 * ng::2], recs[:, :, 2 * ng + 1::2])
+
+
 def read_history(pages_buf, page_table_row, hist_len, head, page_size, group_size):
     """Decode history tokens 0..hist_len-1 of one head back to codes and s/z."""
     tb = tile_bytes(group_size)
     ng = HEAD_DIM // group_size
-    kc = np.zeros((hist_len, HEAD_DIM), np.uint8); vc = np.zeros_like(kc)
-    sk = np.zeros((hist_len, ng), np.float16); zk = sk.copy(); sv = sk.copy(); zv = sk.copy()
     ntiles = (hist_len + TILE - 1) // TILE
-    for ti in range(ntiles):
-        page = int(page_table_row[(ti * TILE) // page_size])
-        within = (ti * TILE % page_size) // TILE
-        a, b, c, d_, e, f = unpack_tile(pages_buf[page, head, within * tb:(within + 1) * tb],
-                                        group_size)
-        n = min(TILE, hist_len - ti * TILE)
-        sl = slice(ti * TILE, ti * TILE + n)
-        kc[sl] = a[:n]; vc[sl] = b[:n]; sk[sl] = c[:n]; zk[sl] = d_[:n]; sv[sl] = e[:n]; zv[sl] = f[:n]
-    return kc, vc, sk, zk, sv, zv
+    if ntiles == 0:
+        z = np.zeros((0, HEAD_DIM), np.uint8); zs = np.zeros((0, ng), np.float16)
+        return z, z.copy(), zs, zs.copy(), zs.copy(), zs.copy()
+    ti = np.arange(ntiles)
+    pages = np.asarray(page_table_row)[(ti * TILE) // page_size]
+    within = (ti * TILE % page_size) // TILE
+    blocks = np.stack([pages_buf[p, head, w * tb:(w + 1) * tb] for p, w in zip(pages, within)])
+    out = unpack_tiles(blocks, group_size)
+    return tuple(a.reshape((ntiles * TILE,) + a.shape[2:])[:hist_len] for a in out)

@@ -174,3 +174,29 @@ def test_history_pages_roundtrip_across_appends():
         q = q_all[g]
         assert np.array_equal(kc, q["kc"]) and np.array_equal(vc, q["vc"])
         assert np.array_equal(sk, q["sk"]) and np.array_equal(zv, q["zv"])
+
+
+@pytest.mark.parametrize("gs", [64, 128])
+def test_vectorised_tile_packer_matches_per_code_packer(gs):
+    rng = np.random.default_rng(17)
+    ng = 128 // gs
+    n = 3
+    kc = rng.integers(0, 4, (n, 16, 128)).astype(np.uint8); vc = rng.integers(0, 4, (n, 16, 128)).astype(np.uint8)
+    sk, zk, sv, zv = (rng.standard_normal((n, 16, ng)).astype(np.float16) for _ in range(4))
+    fast = kq.pack_tiles_full(kc, vc, sk, zk, sv, zv, gs)
+    for i in range(n):
+        slow = kq.pack_tile(kc[i], vc[i], sk[i], zk[i], sv[i], zv[i], gs)
+        assert np.array_equal(fast[i], slow)
+
+
+def test_pack_history_full_matches_incremental():
+    aw = synth.make_append_workload("t", 4, n_seqs=1, Hkv=2, tokens_per_seq=45, page_size=16,
+                                    group_size=128, kv_kind="normal")
+    a = kq.pack_history_full(aw.k, aw.v, aw.Rk, aw.Rv, aw.clip_k, aw.clip_v, aw.page_table[0],
+                             aw.num_pages, 2, 16, 128)
+    b = np.zeros_like(a)
+    for g in range(2):
+        q = kq.quantize_tokens(aw.k[:, g], aw.v[:, g], aw.Rk[g], aw.Rv[g], aw.clip_k[g],
+                               aw.clip_v[g], 128)
+        kq.pack_history(b, aw.page_table[0], 0, q, g, 2, 16, 128)
+    assert np.array_equal(a, b)
