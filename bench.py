@@ -7,8 +7,9 @@ Inputs are seeded synthetic data (``bit_kv_cache_12_gb300.synth``); the pool
 is filled by the library's own append kernel.
 
 One step = one ``kv_decode_attention`` call (whole batch, one layer).  Every
-timed step is preceded by an L2 flush (a 256 MiB device write outside the
-timed events).  Timing: CUDA events on the launching stream around each
+timed step is preceded by an L2 flush outside the timed events: a 256 MiB
+device write, then a 256 MiB read so the dirty lines are written back before
+the step starts.  Timing: CUDA events on the launching stream around each
 step, device synchronised before and after, max over ranks.
 
 ``--impl reference`` times the CPU oracle on the same workload instead (a
@@ -186,7 +187,7 @@ def config_of(wl):
             "context": int(wl.meta["ctx"][0]), "sink": int(wl.sink_len[0]),
             "int2_history": int(wl.hist_len[0]), "recent": int(wl.rec_len[0]),
             "page_size": wl.page_size, "group_size": wl.group_size,
-            "l2": "flushed between steps (256 MiB device write outside the timed events)"}
+            "l2": "flushed between steps (256 MiB write + 256 MiB read outside the timed events)"}
 
 
 def main():
@@ -275,17 +276,25 @@ def main():
         native.kv_decode_attention_bf16(bpool.handle, 0, B, q, blen, bpt, bpt_np.shape[1],
                                         int(lens.max()), wl.scale, bout, bws, bws_bytes, stream)
 
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    # L2 flush between steps: write a 256 MiB buffer (evicts the pool), then
+    # read another 256 MiB buffer so the write-back of the dirty lines happens
+    # here and not inside the timed kernel.  Both are outside the events.
+    flush_w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_w.zero_()
+        flush_r.sum()
 
     def timed(fn, steps, warmup):
         for _ in range(warmup):
-            flush.zero_(); fn()
+            flush(); fn()
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for s0, s1 in ev:
-            flush.zero_()
+            flush()
             s0.record(stream); fn(); s1.record(stream)
         torch.cuda.synchronize()
         if world > 1:

@@ -7,19 +7,22 @@
 // OSCAR write-up, "1. 三段式 Token 池": 64 sink + INT2 history + 256 recent).
 //
 // GPU design (one launch per decode step):
-//   grid = (history splits + 1, KV heads, sequences), 8 warps per CTA.
+//   grid = (history splits + tier CTAs, KV heads, sequences), 8 warps per CTA.
 //   * history CTAs: q' = q R_k for the CTA's GQA group, then each warp streams
-//     16-token tiles straight from HBM into registers (16-byte loads, two
-//     tiles in flight), unpacks the 2-bit codes into fp16 MMA fragments with
-//     one lop3 + one fma per code pair, and runs QK and PV on the tensor cores
-//     (mma.sync m16n8k16).  Dequantization is folded algebraically:
+//     16-token tiles from HBM through a 4-stage shared-memory ring filled by
+//     16-byte cp.async copies (each lane copies and later reads only its own
+//     bytes, so no barrier is needed; the CTA's page ids are staged in shared
+//     memory first and the q' prologue overlaps the first copies), unpacks
+//     the 2-bit codes into fp16 MMA fragments with one lop3 + one fma per
+//     code pair, and runs QK and PV on the tensor cores (mma.sync m16n8k16).
+//     Dequantization is folded algebraically:
 //       q'.deq(k) = s_k (q'.(c_k - 1)) + (z_k + s_k) sum(q')
 //       sum_t w_t deq(v_t) = sum_t (w_t s_v)(c_v - 1) + sum_t w_t (z_v + s_v)
 //     so the MMA operands are small exact integers and the query / softmax
 //     weights enter as fp16 hi + lo pairs (about 22 significant bits).
 //     Online softmax per head with warp-shuffle max; per-CTA merge in shared
 //     memory; the CTA's value accumulator is rotated back by R_v^T.
-//   * one tier CTA: the <= 320 BF16 sink + recent tokens in SIMT fp32.
+//   * tier CTAs: the <= 320 BF16 sink + recent tokens in SIMT fp32.
 //   * the last CTA of each (sequence, KV head), found by an atomic ticket (no
 //     waiting), merges all partials with the log-sum-exp rule and writes the
 //     fp32 output.
@@ -36,6 +39,9 @@ constexpr int kThreads = 256;
 constexpr int kWarps = 8;
 constexpr int kPart = 132;   // floats per (split, head) partial: m, l, -, -, o[128]
 constexpr float kNegInf = -INFINITY;
+constexpr int kStages = 4;       // tiles in each warp's ring
+constexpr int kMaxPids = 520;    // page ids staged per CTA (splits cover <= 512 tiles / 8192 tokens)
+constexpr int kMaxParts = 400;   // partials per (sequence, KV head) the final merge reads
 
 struct DecodeArgs {
   const uint8_t* hist;      // INT2 layer base
@@ -61,7 +67,7 @@ struct DecodeArgs {
   int max_pages;
   int Hq, Hkv, page_size;
   long long num_pages;
-  int n_split, per_split;
+  int n_split, per_split, n_tier;
   float scale_log2;
   float* out;
   float* ws;
@@ -73,26 +79,42 @@ struct DecodeArgs {
 // shared helpers
 // ---------------------------------------------------------------------------
 
-// out[h][c] = sum_i in[h][i] R[i][c], h < NH; 256 threads, i split in halves.
+// out[h][c] = sum_i in[h][i] R[i][c] for h < NH.  Thread (i-group ig, column
+// quad cq) loads its 16 x float4 of R at once (one memory latency), then the
+// eight i-groups are summed through shared memory (scratch [8][NH][128]).
 template <int NH>
 __device__ void rows_times_R(const float* in, const float* __restrict__ R, float* scratch,
                              float* out) {
-  const int c = threadIdx.x & 127, half = threadIdx.x >> 7;
-  float acc[NH];
+  const int cq = threadIdx.x & 31, ig = threadIdx.x >> 5;
+  float4 rr[16];
 #pragma unroll
-  for (int h = 0; h < NH; ++h) acc[h] = 0.f;
-  const int i0 = half * 64;
-#pragma unroll 8
-  for (int i = i0; i < i0 + 64; ++i) {
-    const float r = __ldg(R + i * 128 + c);
+  for (int u = 0; u < 16; ++u)
+    rr[u] = __ldg(reinterpret_cast<const float4*>(R + (ig * 16 + u) * 128) + cq);
+  float acc[NH][4];
 #pragma unroll
-    for (int h = 0; h < NH; ++h) acc[h] = fmaf(in[h * 128 + i], r, acc[h]);
+  for (int h = 0; h < NH; ++h) acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.f;
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      const float x = in[h * 128 + ig * 16 + u];
+      acc[h][0] = fmaf(x, rr[u].x, acc[h][0]);
+      acc[h][1] = fmaf(x, rr[u].y, acc[h][1]);
+      acc[h][2] = fmaf(x, rr[u].z, acc[h][2]);
+      acc[h][3] = fmaf(x, rr[u].w, acc[h][3]);
+    }
   }
 #pragma unroll
-  for (int h = 0; h < NH; ++h) scratch[(half * NH + h) * 128 + c] = acc[h];
+  for (int h = 0; h < NH; ++h)
+    *reinterpret_cast<float4*>(scratch + (ig * NH + h) * 128 + 4 * cq) =
+        make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
   __syncthreads();
-  for (int idx = threadIdx.x; idx < NH * 128; idx += kThreads)
-    out[idx] = scratch[idx] + scratch[NH * 128 + idx];
+  for (int idx = threadIdx.x; idx < NH * 128; idx += kThreads) {
+    float v = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v += scratch[q * NH * 128 + idx];
+    out[idx] = v;
+  }
   __syncthreads();
 }
 
@@ -161,26 +183,63 @@ __device__ bool last_to_arrive(unsigned* ticket, unsigned total) {
   return last;
 }
 
-// Log-sum-exp merge of all splits of (b, g) and the final normalisation.
+// Log-sum-exp merge of all parts of (b, g) and the final normalisation.
+// m and l of every part are staged in shared memory first; the value vectors
+// are then read as float4 with the parts split over the spare threads.
+// `sm` needs 16 + 1024 + 2 * nparts * G floats.
 template <int G>
-__device__ void final_combine(const DecodeArgs& a, int b, int g, int nparts) {
+__device__ void final_combine(const DecodeArgs& a, int b, int g, int nparts, float* sm) {
+  constexpr int NSUB = kWarps / G;                 // part subsets per output column quad
   const float* base = a.ws + (size_t)(b * a.Hkv + g) * nparts * G * kPart;
-  for (int idx = threadIdx.x; idx < G * 128; idx += kThreads) {
-    const int h = idx >> 7, c = idx & 127;
+  float* sM = sm;                                  // [8]
+  float* sL = sm + 8;                              // [8]
+  float* sacc = sm + 16;                           // [NSUB][G][128]
+  float* sf = sacc + NSUB * G * 128;               // [nparts * G] m, then weights
+  float* sl = sf + nparts * G;                     // [nparts * G]
+  for (int i = threadIdx.x; i < nparts * G; i += kThreads) {
+    sf[i] = __ldcg(base + (size_t)i * kPart);
+    sl[i] = __ldcg(base + (size_t)i * kPart + 1);
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
     float M = kNegInf;
-    for (int s = 0; s < nparts; ++s) M = fmaxf(M, __ldcg(base + (s * G + h) * kPart));
-    float L = 0.f, O = 0.f;
-    if (M != kNegInf) {
-      for (int s = 0; s < nparts; ++s) {
-        const float* p = base + (s * G + h) * kPart;
-        const float ms = __ldcg(p);
-        if (ms == kNegInf) continue;
-        const float f = exp2f(ms - M);
-        L = fmaf(f, __ldcg(p + 1), L);
-        O = fmaf(f, __ldcg(p + 4 + c), O);
-      }
+    for (int s = 0; s < nparts; ++s) M = fmaxf(M, sf[s * G + threadIdx.x]);
+    sM[threadIdx.x] = M;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < nparts * G; i += kThreads) {
+    const float m = sf[i], M = sM[i % G];
+    sf[i] = (m == kNegInf || M == kNegInf) ? 0.f : exp2f(m - M);
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    float L = 0.f;
+    for (int s = 0; s < nparts; ++s) L = fmaf(sf[s * G + threadIdx.x], sl[s * G + threadIdx.x], L);
+    sL[threadIdx.x] = L;
+  }
+  {
+    const int cq = threadIdx.x & 31, h = (threadIdx.x >> 5) % G, sub = (threadIdx.x >> 5) / G;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int s = sub; s < nparts; s += NSUB) {
+      const float f = sf[s * G + h];
+      const float4 o =
+          __ldcg(reinterpret_cast<const float4*>(base + (size_t)(s * G + h) * kPart + 4) + cq);
+      acc.x = fmaf(f, o.x, acc.x);
+      acc.y = fmaf(f, o.y, acc.y);
+      acc.z = fmaf(f, o.z, acc.z);
+      acc.w = fmaf(f, o.w, acc.w);
     }
-    a.out[((size_t)b * a.Hq + g * G + h) * 128 + c] = (L > 0.f) ? O / L : 0.f;
+    *reinterpret_cast<float4*>(sacc + (sub * G + h) * 128 + 4 * cq) = acc;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * 128; idx += kThreads) {
+    const int h = idx >> 7;
+    float O = 0.f;
+#pragma unroll
+    for (int u = 0; u < NSUB; ++u) O += sacc[u * G * 128 + idx];
+    const float L = sL[h];
+    a.out[((size_t)b * a.Hq + g * G + h) * 128 + (idx & 127)] = (L > 0.f) ? O / L : 0.f;
   }
   if (threadIdx.x == 0) a.tickets[b * a.Hkv + g] = 0u;   // ready for the next call
 }
@@ -205,30 +264,42 @@ struct WarpAcc {
   }
 };
 
-// rows(u, &k, &v) gives bf16 row pointers for token u (nullptr = skip token).
+// A zero bf16 row: stands in for tokens a warp must not read (past the end of
+// the range or behind an invalid page id); their weight is forced to 0.
+__device__ __align__(16) uint16_t g_zero_row[128];
+
+// rows(u, k, v) sets bf16 row pointers for token u and returns false if the
+// token must be skipped.  All loads of a phase are issued before their use.
 template <int G, class RowFn>
 __device__ void bf16_rows_attend(const float* sq, float* sp, int u0, int u1, int stride,
                                  const RowFn& rows, float scale_log2, WarpAcc<G>& st) {
   const int lane = threadIdx.x & 31;
   for (int c0 = u0; c0 < u1; c0 += stride) {
     const int u = c0 + lane;
-    const uint16_t* krow = nullptr;
-    const uint16_t* vrow = nullptr;
-    if (u < u1) rows(u, krow, vrow);
+    const uint16_t* krow = g_zero_row;
+    const uint16_t* vrow = g_zero_row;
+    bool ok = false;
+    if (u < u1) ok = rows(u, krow, vrow);
+    if (!ok) krow = vrow = g_zero_row;
     float sc[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) sc[h] = 0.f;
-    if (krow) {
-      const uint4* kr = reinterpret_cast<const uint4*>(krow);
-#pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        const uint4 w = __ldg(kr + i);
+    const uint4* kr = reinterpret_cast<const uint4*>(krow);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint4 kk[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) kk[i] = __ldg(kr + half * 8 + i);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 w = kk[i];
         const float x[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
                             bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+        const int cbase = 8 * (half * 8 + i);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float4 q0 = *reinterpret_cast<const float4*>(sq + h * 128 + 8 * i);
-          const float4 q1 = *reinterpret_cast<const float4*>(sq + h * 128 + 8 * i + 4);
+          const float4 q0 = *reinterpret_cast<const float4*>(sq + h * 128 + cbase);
+          const float4 q1 = *reinterpret_cast<const float4*>(sq + h * 128 + cbase + 4);
           float acc = sc[h];
           acc = fmaf(x[0], q0.x, acc); acc = fmaf(x[1], q0.y, acc);
           acc = fmaf(x[2], q0.z, acc); acc = fmaf(x[3], q0.w, acc);
@@ -240,7 +311,7 @@ __device__ void bf16_rows_attend(const float* sq, float* sp, int u0, int u1, int
     }
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const float v = krow ? sc[h] * scale_log2 : kNegInf;
+      const float v = ok ? sc[h] * scale_log2 : kNegInf;
       const float mnew = fmaxf(st.m[h], warp_max_xor(v, 1));
       const float alpha = (st.m[h] == kNegInf) ? 0.f : exp2f(st.m[h] - mnew);
       st.m[h] = mnew;
@@ -252,20 +323,29 @@ __device__ void bf16_rows_attend(const float* sq, float* sp, int u0, int u1, int
       sp[lane * G + h] = p;
     }
     __syncwarp();
-    const int n = min(32, u1 - c0);
-    for (int t = 0; t < n; ++t) {
-      const uint16_t* vr = reinterpret_cast<const uint16_t*>(
-          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(vrow), t));
-      if (vr == nullptr) continue;   // uniform across the warp
-      const uint2 vv = __ldg(reinterpret_cast<const uint2*>(vr) + lane);
-      const float v0 = bf16lo(vv.x), v1 = bf16hi(vv.x), v2 = bf16lo(vv.y), v3 = bf16hi(vv.y);
+    const unsigned long long vbits = reinterpret_cast<unsigned long long>(vrow);
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float p = sp[t * G + h];
-        st.o[h][0] = fmaf(p, v0, st.o[h][0]);
-        st.o[h][1] = fmaf(p, v1, st.o[h][1]);
-        st.o[h][2] = fmaf(p, v2, st.o[h][2]);
-        st.o[h][3] = fmaf(p, v3, st.o[h][3]);
+    for (int tb = 0; tb < 4; ++tb) {
+      uint2 vv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint16_t* vr =
+            reinterpret_cast<const uint16_t*>(__shfl_sync(0xffffffffu, vbits, tb * 8 + e));
+        vv[e] = __ldg(reinterpret_cast<const uint2*>(vr) + lane);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int t = tb * 8 + e;
+        const float v0 = bf16lo(vv[e].x), v1 = bf16hi(vv[e].x);
+        const float v2 = bf16lo(vv[e].y), v3 = bf16hi(vv[e].y);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float p = sp[t * G + h];
+          st.o[h][0] = fmaf(p, v0, st.o[h][0]);
+          st.o[h][1] = fmaf(p, v1, st.o[h][1]);
+          st.o[h][2] = fmaf(p, v2, st.o[h][2]);
+          st.o[h][3] = fmaf(p, v3, st.o[h][3]);
+        }
       }
     }
     __syncwarp();
@@ -287,6 +367,8 @@ __device__ void warp_acc_to_smem(WarpAcc<G>& st, float* swo, float* swm, float* 
   }
 }
 
+// q of the GQA group (bf16 -> fp32) into shared memory; padded heads are 0.
+// Ends with a barrier.
 template <int G>
 __device__ void load_q(const DecodeArgs& a, int b, int g, float* sq, int padded_heads) {
   for (int idx = threadIdx.x; idx < padded_heads * 128; idx += kThreads) {
@@ -298,37 +380,47 @@ __device__ void load_q(const DecodeArgs& a, int b, int g, float* sq, int padded_
   __syncthreads();
 }
 
-// Shared-memory carve-up (floats) used by both kernels.
-template <int G>
+// Shared-memory carve-up (in floats).  Region "big" is reused: the INT2
+// warps' cp.async rings during the history loop, then the per-warp results
+// (swo/swm/swl); the BF16 paths use it for their weight buffers and results.
+template <int G, int GS, bool kRing = true>
 struct Smem {
   static constexpr int HP = (G <= 4) ? 4 : 4 * ((G + 3) / 4);   // padded heads (MMA columns)
-  static constexpr int sq = 0;                      // [HP][128]
-  static constexpr int sqr = sq + HP * 128;          // [HP][128]
-  static constexpr int ssum = sqr + HP * 128;        // [HP][2] (padded to 4)
-  static constexpr int swo = ssum + ((2 * HP + 3) / 4) * 4;   // [8][G][128]
-  static constexpr int swm = swo + kWarps * G * 128;  // [8][G]
-  static constexpr int swl = swm + ((kWarps * G + 3) / 4) * 4;
-  static constexpr int sp = swl + ((kWarps * G + 3) / 4) * 4;   // [8][32][G]
-  static constexpr int scratch = sp + kWarps * 32 * G;          // [2][HP][128]
-  static constexpr int smm = scratch + 2 * HP * 128;            // [G] merged m
-  static constexpr int sml = smm + ((G + 3) / 4) * 4;
-  static constexpr int total = sml + ((G + 3) / 4) * 4;
+  static constexpr int LB = (GS == 128) ? 48 : 64;               // ring bytes per lane per stage
+  static constexpr int sq = 0;                                    // [HP][128]
+  static constexpr int sqr = sq + HP * 128;                       // [HP][128]
+  static constexpr int ssum = sqr + HP * 128;                     // [HP][2], padded
+  static constexpr int smm = ssum + ((2 * HP + 3) / 4) * 4;       // [G] merged m
+  static constexpr int sml = smm + ((G + 3) / 4) * 4;             // [G] merged l
+  static constexpr int spid = sml + ((G + 3) / 4) * 4;            // [kMaxPids] int
+  static constexpr int scratch = spid + kMaxPids;                 // [8][HP][128]
+  static constexpr int big = scratch + kWarps * HP * 128;
+  static constexpr int ring_floats = kRing ? kWarps * kStages * 32 * LB / 4 : 0;
+  static constexpr int res_floats = kWarps * G * 128 + 2 * ((kWarps * G + 3) / 4) * 4;
+  static constexpr int sp_floats = kWarps * 32 * G;
+  static constexpr int big_floats = (ring_floats > res_floats + sp_floats) ? ring_floats
+                                                                          : res_floats + sp_floats;
+  // inside "big"
+  static constexpr int swo = big;                                 // [8][G][128]
+  static constexpr int swm = swo + kWarps * G * 128;              // [8][G]
+  static constexpr int swl = swm + ((kWarps * G + 3) / 4) * 4;    // [8][G]
+  static constexpr int sp = swl + ((kWarps * G + 3) / 4) * 4;     // [8][32][G]
+  static constexpr int ring = big;
+  static constexpr int total = big + big_floats;
+  // the final merge runs from `scratch` on
+  static_assert(total - scratch >= 16 + 1024 + 2 * kMaxParts * G, "merge scratch");
 };
 
 // ---------------------------------------------------------------------------
 // INT2 history split (the hot loop)
 // ---------------------------------------------------------------------------
-template <int GS>
-struct TileRegs {
-  uint4 k, v, sz0, sz1;
-};
-
 template <int G, int GS>
 __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float* sm,
                              float* part) {
-  using S = Smem<G>;
+  using S = Smem<G, GS>;
   constexpr int NT = S::HP / 4;      // MMA n-tiles of 8 columns (4 heads x hi/lo)
   constexpr int NG = 128 / GS;       // quantization groups per row
+  constexpr int LB = S::LB;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = lane >> 2, j = lane & 3;
 
@@ -346,13 +438,44 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
     return;
   }
 
+  // ---- page ids of this CTA's tiles and q -> shared memory (one latency) ----
+  const int tpp = a.tiles_per_page;
+  const int p_begin = t_begin / tpp, p_count = (t_end - 1) / tpp + 1 - p_begin;
+  int* spid = reinterpret_cast<int*>(sm + S::spid);
+  const int32_t* ptrow = a.pt + (size_t)b * a.max_pages;
+  for (int i = threadIdx.x; i < p_count; i += kThreads) spid[i] = __ldg(ptrow + p_begin + i);
   float* sq = sm + S::sq;
   float* sqr = sm + S::sqr;
   float* ssum = sm + S::ssum;
-  load_q<G>(a, b, g, sq, S::HP);
-  rows_times_R<S::HP>(sq, a.Rk + (size_t)g * 128 * 128, sm + S::scratch, sqr);
+  load_q<G>(a, b, g, sq, S::HP);   // its barrier also publishes spid
 
-  // per-head sums of q' over each quantization group
+  // ---- start streaming this warp's first tiles into its ring ----
+  uint8_t* ring = reinterpret_cast<uint8_t*>(sm + S::ring) + (size_t)warp * kStages * 32 * LB;
+  const uint8_t* head_base = a.hist + (size_t)g * (a.page_bytes / a.Hkv);
+  auto issue = [&](int t, int stage) {
+    if (t < t_end) {
+      const int pid = spid[t / tpp - p_begin];
+      if (pid >= 0 && pid < a.num_pages) {
+        const uint8_t* tb =
+            head_base + (size_t)pid * a.page_bytes + (size_t)(t % tpp) * a.tile_bytes;
+        uint8_t* d = ring + (stage * 32 + lane) * LB;
+        cp_async16(d, tb + 16 * lane);
+        cp_async16(d + 16, tb + 512 + 16 * lane);
+        if (GS == 128) {
+          cp_async16(d + 32, tb + 1024 + 16 * r);
+        } else {
+          cp_async16(d + 32, tb + 1024 + 32 * r);
+          cp_async16(d + 48, tb + 1024 + 32 * r + 16);
+        }
+      }
+    }
+    cp_async_commit();   // empty groups keep the group count uniform
+  };
+#pragma unroll
+  for (int st = 0; st < kStages - 1; ++st) issue(t_begin + warp + kWarps * st, st);
+
+  // ---- q' = q R_k and its per-group sums (overlaps the first copies) ----
+  rows_times_R<S::HP>(sq, a.Rk + (size_t)g * 128 * 128, sm + S::scratch, sqr);
   for (int hh = warp; hh < S::HP; hh += kWarps) {
 #pragma unroll
     for (int grp = 0; grp < NG; ++grp) {
@@ -373,7 +496,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const float* row = sqr + (4 * nt + hl) * 128 + 16 * s + 2 * j;
-        float x[4] = {row[0], row[1], row[8], row[9]};
+        const float x[4] = {row[0], row[1], row[8], row[9]};
         __half p[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -403,43 +526,18 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
       for (int u = 0; u < 4; ++u) oacc[i][nt][u] = 0.f;
   }
 
-  const int32_t* ptrow = a.pt + (size_t)b * a.max_pages;
-  const uint8_t* head_base = a.hist + (size_t)g * (a.page_bytes / a.Hkv);
-  auto page_of = [&](int t) -> int {
-    if (t >= t_end) return -1;
-    return __ldg(ptrow + t / a.tiles_per_page);
-  };
-  auto load_tile = [&](int t, int pid, TileRegs<GS>& d) {
-    if (t >= t_end || pid < 0 || pid >= a.num_pages) {
-      d.k = d.v = d.sz0 = d.sz1 = make_uint4(0, 0, 0, 0);
-      return;
-    }
-    const uint8_t* tb =
-        head_base + (size_t)pid * a.page_bytes + (size_t)(t % a.tiles_per_page) * a.tile_bytes;
-    d.k = ld_stream_v4(tb + 16 * lane);
-    d.v = ld_stream_v4(tb + 512 + 16 * lane);
-    if (GS == 128) {
-      d.sz0 = ld_stream_v4(tb + 1024 + 16 * r);
-      d.sz1 = make_uint4(0, 0, 0, 0);
-    } else {
-      d.sz0 = ld_stream_v4(tb + 1024 + 32 * r);
-      d.sz1 = ld_stream_v4(tb + 1024 + 32 * r + 16);
-    }
-  };
+  int k = 0;
+  for (int t = t_begin + warp; t < t_end; t += kWarps, ++k) {
+    issue(t + kWarps * (kStages - 1), (k + kStages - 1) % kStages);
+    cp_async_wait<kStages - 1>();
+    const uint8_t* src = ring + ((k % kStages) * 32 + lane) * LB;
+    const uint4 kq4 = *reinterpret_cast<const uint4*>(src);
+    const uint4 vq4 = *reinterpret_cast<const uint4*>(src + 16);
+    const uint4 sz0 = *reinterpret_cast<const uint4*>(src + 32);
+    const uint4 sz1 =
+        (GS == 64) ? *reinterpret_cast<const uint4*>(src + 48) : make_uint4(0, 0, 0, 0);
 
-  int t = t_begin + warp;
-  int pid0 = page_of(t), pid1 = page_of(t + kWarps), pid2 = page_of(t + 2 * kWarps);
-  TileRegs<GS> cur, nxt;
-  load_tile(t, pid0, cur);
-  load_tile(t + kWarps, pid1, nxt);
-  int pid_cur = pid0, pid_nxt = pid1;
-
-  for (; t < t_end; t += kWarps) {
-    // prefetch: page id two tiles ahead of the data prefetch, data one tile ahead
-    const int pid3 = page_of(t + 3 * kWarps);
-    TileRegs<GS> nn;
-    load_tile(t + 2 * kWarps, pid2, nn);
-
+    const int pid_cur = spid[t / tpp - p_begin];
     const bool page_ok = pid_cur >= 0 && pid_cur < a.num_pages;
     if (!page_ok && lane == 0) flag_error(a.err, KV_DEVERR_PAGE_ID);
     const bool v0 = page_ok && (t * kTile + r) < h;
@@ -448,14 +546,14 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
     // scale / zero of tokens r and r+8
     float sk[2][NG], zk[2][NG], sv[2][NG], zv[2][NG];
     if (GS == 128) {
-      const __half2 a0 = u32_as_h2(cur.sz0.x), a1 = u32_as_h2(cur.sz0.y);
-      const __half2 b0 = u32_as_h2(cur.sz0.z), b1 = u32_as_h2(cur.sz0.w);
+      const __half2 a0 = u32_as_h2(sz0.x), a1 = u32_as_h2(sz0.y);
+      const __half2 b0 = u32_as_h2(sz0.z), b1 = u32_as_h2(sz0.w);
       sk[0][0] = __low2float(a0); zk[0][0] = __high2float(a0);
       sv[0][0] = __low2float(a1); zv[0][0] = __high2float(a1);
       sk[1][0] = __low2float(b0); zk[1][0] = __high2float(b0);
       sv[1][0] = __low2float(b1); zv[1][0] = __high2float(b1);
     } else {
-      const uint4 s0 = cur.sz0, s1 = cur.sz1;
+      const uint4 s0 = sz0, s1 = sz1;
       sk[0][0] = __low2float(u32_as_h2(s0.x)); zk[0][0] = __high2float(u32_as_h2(s0.x));
       sk[0][NG - 1] = __low2float(u32_as_h2(s0.y)); zk[0][NG - 1] = __high2float(u32_as_h2(s0.y));
       sv[0][0] = __low2float(u32_as_h2(s0.z)); zv[0][0] = __high2float(u32_as_h2(s0.z));
@@ -467,15 +565,17 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
     }
 
     // ---- QK: scores[token][column] on the tensor cores ----
-    float sacc[NG][NT][4];
+    // two independent accumulator chains: the two groups (group 64) or the
+    // even / odd k-steps (group 128)
+    float sacc[2][NT][4];
 #pragma unroll
-    for (int grp = 0; grp < NG; ++grp)
+    for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) sacc[grp][nt][u] = 0.f;
+        for (int u = 0; u < 4; ++u) sacc[ch][nt][u] = 0.f;
     {
-      const uint32_t kw[4] = {cur.k.x, cur.k.y, cur.k.z, cur.k.w};
+      const uint32_t kw[4] = {kq4.x, kq4.y, kq4.z, kq4.w};
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         uint32_t fr[8];
@@ -483,10 +583,10 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
 #pragma unroll
         for (int sh = 0; sh < 2; ++sh) {
           const int s = 2 * w + sh;
-          const int grp = (GS == 64) ? (s >> 2) : 0;
+          const int ch = (GS == 64) ? (s >> 2) : (s & 1);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
-            mma_f16(sacc[grp][nt], fr[4 * sh + 0], fr[4 * sh + 1], fr[4 * sh + 2], fr[4 * sh + 3],
+            mma_f16(sacc[ch][nt], fr[4 * sh + 0], fr[4 * sh + 1], fr[4 * sh + 2], fr[4 * sh + 3],
                     qf[s][nt][0], qf[s][nt][1]);
         }
       }
@@ -499,8 +599,14 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
       float l0 = 0.f, l1 = 0.f;
 #pragma unroll
       for (int grp = 0; grp < NG; ++grp) {
-        const float d0 = sacc[grp][nt][0] + sacc[grp][nt][1];
-        const float d1 = sacc[grp][nt][2] + sacc[grp][nt][3];
+        float d0, d1;
+        if (GS == 64) {
+          d0 = sacc[grp][nt][0] + sacc[grp][nt][1];
+          d1 = sacc[grp][nt][2] + sacc[grp][nt][3];
+        } else {
+          d0 = (sacc[0][nt][0] + sacc[1][nt][0]) + (sacc[0][nt][1] + sacc[1][nt][1]);
+          d1 = (sacc[0][nt][2] + sacc[1][nt][2]) + (sacc[0][nt][3] + sacc[1][nt][3]);
+        }
         l0 += sk[0][grp] * d0 + (zk[0][grp] + sk[0][grp]) * sumq[nt][grp];
         l1 += sk[1][grp] * d1 + (zk[1][grp] + sk[1][grp]) * sumq[nt][grp];
       }
@@ -539,7 +645,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
 
     // ---- PV: value accumulator [channel][column] on the tensor cores ----
     {
-      const uint32_t vw[4] = {cur.v.x, cur.v.y, cur.v.z, cur.v.w};
+      const uint32_t vw[4] = {vq4.x, vq4.y, vq4.z, vq4.w};
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         uint32_t fr[8];
@@ -555,13 +661,9 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
         }
       }
     }
-
-    cur = nxt;
-    nxt = nn;
-    pid_cur = pid_nxt;
-    pid_nxt = pid2;
-    pid2 = pid3;
   }
+  cp_async_wait<0>();
+  __syncthreads();   // every warp is done with its ring before the results reuse it
 
   // ---- warp results -> shared memory ----
   float* swo = sm + S::swo;
@@ -589,19 +691,18 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
     }
   }
   __syncthreads();
-  float* merged = sm + S::sqr;   // q' no longer needed
-  merge_warps<G>(swo, swm, swl, merged, sm + S::smm, sm + S::sml);
+  merge_warps<G>(swo, swm, swl, sqr, sm + S::smm, sm + S::sml);   // q' no longer needed
   // back to the original basis: o = o' R_v^T
-  rows_times_R<G>(merged, a.RvT + (size_t)g * 128 * 128, sm + S::scratch, sm + S::sq);
-  write_partial<G>(part, sm + S::sq, sm + S::smm, sm + S::sml);
+  rows_times_R<G>(sqr, a.RvT + (size_t)g * 128 * 128, sm + S::scratch, sq);
+  write_partial<G>(part, sq, sm + S::smm, sm + S::sml);
 }
 
 // ---------------------------------------------------------------------------
-// BF16 sink + recent tiers of the INT2 pool
+// BF16 sink + recent tiers of the INT2 pool (tier CTA `ti` of n_tier)
 // ---------------------------------------------------------------------------
-template <int G>
-__device__ void bf16_tiers(const DecodeArgs& a, int b, int g, float* sm, float* part) {
-  using S = Smem<G>;
+template <int G, int GS>
+__device__ void bf16_tiers(const DecodeArgs& a, int b, int g, int ti, float* sm, float* part) {
+  using S = Smem<G, GS>;
   const int warp = threadIdx.x >> 5;
   int ns = a.sink_len[b], nr = a.rec_len[b], rs = a.rec_start[b];
   if (ns < 0 || ns > a.sink_cap || nr < 0 || nr > a.rec_cap || rs < 0 || rs >= a.rec_cap) {
@@ -618,7 +719,7 @@ __device__ void bf16_tiers(const DecodeArgs& a, int b, int g, float* sm, float* 
   const uint16_t* rk = a.rec_k + seq_head * a.rec_cap * 128;
   const uint16_t* rv = a.rec_v + seq_head * a.rec_cap * 128;
   const int cap = a.rec_cap;
-  auto rows = [&](int u, const uint16_t*& kr, const uint16_t*& vr) {
+  auto rows = [&](int u, const uint16_t*& kr, const uint16_t*& vr) -> bool {
     if (u < ns) {
       kr = sk + (size_t)u * 128;
       vr = sv + (size_t)u * 128;
@@ -628,10 +729,14 @@ __device__ void bf16_tiers(const DecodeArgs& a, int b, int g, float* sm, float* 
       kr = rk + (size_t)idx * 128;
       vr = rv + (size_t)idx * 128;
     }
+    return true;
   };
+  // this tier CTA's share of the sink + recent tokens
+  const int n = ns + nr, per = (n + a.n_tier - 1) / a.n_tier;
+  const int u0 = ti * per, u1 = min(n, u0 + per);
   WarpAcc<G> st;
   st.init();
-  bf16_rows_attend<G>(sq, sm + S::sp + warp * 32 * G, 32 * warp, ns + nr, 32 * kWarps, rows,
+  bf16_rows_attend<G>(sq, sm + S::sp + warp * 32 * G, u0 + 32 * warp, u1, 32 * kWarps, rows,
                       a.scale_log2, st);
   warp_acc_to_smem<G>(st, sm + S::swo, sm + S::swm, sm + S::swl);
   __syncthreads();
@@ -644,13 +749,14 @@ __global__ void __launch_bounds__(kThreads, (G > 4) ? 1 : 2) decode_int2_kernel(
   extern __shared__ float4 smem4[];
   float* sm = reinterpret_cast<float*>(smem4);
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  const int nparts = a.n_split + 1;
+  const int nparts = a.n_split + a.n_tier;
   float* part = a.ws + ((size_t)(b * a.Hkv + g) * nparts + split) * G * kPart;
   if (split < a.n_split)
     int2_history<G, GS>(a, b, g, split, sm, part);
   else
-    bf16_tiers<G>(a, b, g, sm, part);
-  if (last_to_arrive(a.tickets + b * a.Hkv + g, (unsigned)nparts)) final_combine<G>(a, b, g, nparts);
+    bf16_tiers<G, GS>(a, b, g, split - a.n_split, sm, part);
+  if (last_to_arrive(a.tickets + b * a.Hkv + g, (unsigned)nparts))
+    final_combine<G>(a, b, g, nparts, sm + Smem<G, GS>::scratch);
 }
 
 // ---------------------------------------------------------------------------
@@ -658,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, (G > 4) ? 1 : 2) decode_int2_kernel(
 // ---------------------------------------------------------------------------
 template <int G>
 __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(DecodeArgs a) {
-  using S = Smem<G>;
+  using S = Smem<G, 128, false>;
   extern __shared__ float4 smem4[];
   float* sm = reinterpret_cast<float*>(smem4);
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -675,20 +781,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(DecodeArgs a) 
   if (u0 >= u1) {
     write_empty_partial<G>(part);
   } else {
-    float* sq = sm + S::sq;
-    load_q<G>(a, b, g, sq, G);
-    const int32_t* ptrow = a.pt + (size_t)b * a.max_pages;
     const int P = a.page_size;
-    auto rows = [&](int u, const uint16_t*& kr, const uint16_t*& vr) {
-      const int pid = __ldg(ptrow + u / P);
+    const int p_begin = u0 / P, p_count = (u1 - 1) / P + 1 - p_begin;
+    int* spid = reinterpret_cast<int*>(sm + S::spid);
+    const int32_t* ptrow = a.pt + (size_t)b * a.max_pages;
+    for (int i = threadIdx.x; i < p_count; i += kThreads) spid[i] = __ldg(ptrow + p_begin + i);
+    float* sq = sm + S::sq;
+    load_q<G>(a, b, g, sq, G);   // its barrier also publishes spid
+    auto rows = [&](int u, const uint16_t*& kr, const uint16_t*& vr) -> bool {
+      const int pid = spid[u / P - p_begin];
       if (pid < 0 || pid >= a.num_pages) {
         flag_error(a.err, KV_DEVERR_PAGE_ID);
-        kr = vr = nullptr;
-        return;
+        return false;
       }
       const size_t off = (((size_t)pid * a.Hkv + g) * P + (u % P)) * 128;
       kr = a.bk + off;
       vr = a.bv + off;
+      return true;
     };
     WarpAcc<G> st;
     st.init();
@@ -699,39 +808,55 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(DecodeArgs a) 
     merge_warps<G>(sm + S::swo, sm + S::swm, sm + S::swl, sm + S::sqr, sm + S::smm, sm + S::sml);
     write_partial<G>(part, sm + S::sqr, sm + S::smm, sm + S::sml);
   }
-  if (last_to_arrive(a.tickets + b * a.Hkv + g, (unsigned)nparts)) final_combine<G>(a, b, g, nparts);
+  if (last_to_arrive(a.tickets + b * a.Hkv + g, (unsigned)nparts))
+    final_combine<G>(a, b, g, nparts, sm + S::scratch);
 }
 
+// Sets the dynamic shared-memory limit of a kernel (once) and reports how many
+// of its CTAs fit on one SM (-1 on a CUDA error).
 template <class K>
-cudaError_t set_smem(K kernel, size_t bytes) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+int prepare_kernel(K kernel, size_t smem, bool& done, int& per_sm) {
+  if (!done) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return -1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, smem) != cudaSuccess)
+      return -1;
+    per_sm = n > 0 ? n : 1;
+    done = true;
+  }
+  return per_sm;
+}
+
+template <int G, int GS>
+int int2_blocks_per_sm() {
+  static bool done = false;
+  static int per_sm = 1;
+  return prepare_kernel(decode_int2_kernel<G, GS>, sizeof(float) * Smem<G, GS>::total, done, per_sm);
+}
+
+template <int G>
+int bf16_blocks_per_sm() {
+  static bool done = false;
+  static int per_sm = 1;
+  return prepare_kernel(decode_bf16_kernel<G>, sizeof(float) * Smem<G, 128, false>::total, done,
+                        per_sm);
 }
 
 template <int G, int GS>
 cudaError_t launch_int2_t(const DecodeArgs& a, int B, cudaStream_t s) {
-  const size_t smem = sizeof(float) * Smem<G>::total;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = set_smem(decode_int2_kernel<G, GS>, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  dim3 grid(a.n_split + 1, a.Hkv, B);
-  decode_int2_kernel<G, GS><<<grid, kThreads, smem, s>>>(a);
+  if (int2_blocks_per_sm<G, GS>() < 0) return cudaErrorInvalidConfiguration;
+  dim3 grid(a.n_split + a.n_tier, a.Hkv, B);
+  decode_int2_kernel<G, GS><<<grid, kThreads, sizeof(float) * Smem<G, GS>::total, s>>>(a);
   return cudaGetLastError();
 }
 
 template <int G>
 cudaError_t launch_bf16_t(const DecodeArgs& a, int B, cudaStream_t s) {
-  const size_t smem = sizeof(float) * Smem<G>::total;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = set_smem(decode_bf16_kernel<G>, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  if (bf16_blocks_per_sm<G>() < 0) return cudaErrorInvalidConfiguration;
   dim3 grid(a.n_split, a.Hkv, B);
-  decode_bf16_kernel<G><<<grid, kThreads, smem, s>>>(a);
+  decode_bf16_kernel<G><<<grid, kThreads, sizeof(float) * Smem<G, 128, false>::total, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -753,36 +878,62 @@ DecodeArgs base_args(const Pool& p, int layer, const void* q, const int32_t* pt,
   return a;
 }
 
+int int2_occupancy(const Pool& p) {
+  const bool g64 = p.cfg.group_size == 64;
+  switch (p.G) {
+    case 1: return g64 ? int2_blocks_per_sm<1, 64>() : int2_blocks_per_sm<1, 128>();
+    case 2: return g64 ? int2_blocks_per_sm<2, 64>() : int2_blocks_per_sm<2, 128>();
+    case 4: return g64 ? int2_blocks_per_sm<4, 64>() : int2_blocks_per_sm<4, 128>();
+    default: return g64 ? int2_blocks_per_sm<8, 64>() : int2_blocks_per_sm<8, 128>();
+  }
+}
+
+int bf16_occupancy(const Pool& p) {
+  switch (p.G) {
+    case 1: return bf16_blocks_per_sm<1>();
+    case 2: return bf16_blocks_per_sm<2>();
+    case 4: return bf16_blocks_per_sm<4>();
+    default: return bf16_blocks_per_sm<8>();
+  }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
 // planning and launch
 // ---------------------------------------------------------------------------
-static DecodePlan make_plan(const Pool& p, int B, int units, int max_units_per_split, int extra) {
+
+// Splits per (sequence, KV head): fill exactly one wave of resident CTAs when
+// the batch is small; cap the work of one split (and the number of parts the
+// final merge reads) when it is large.
+static DecodePlan make_plan(const Pool& p, int B, int units, int max_per, int n_extra,
+                            int per_sm) {
   DecodePlan pl;
   const int pairs = B * p.cfg.num_kv_heads;
-  const int slots = 2 * p.sm_count;
-  int ns = (slots + pairs - 1) / pairs;
-  ns = max(1, min(ns, max(1, units)));
-  int per = (max(units, 1) + ns - 1) / ns;
-  if (per > max_units_per_split) {
-    per = max_units_per_split;
-  }
-  ns = max(1, (max(units, 1) + per - 1) / per);
+  const int slots = max(1, per_sm) * p.sm_count;
+  const int u = max(units, 1);
+  int ns = slots / pairs - n_extra;
+  ns = max(1, min(ns, u));
+  int per = (u + ns - 1) / ns;
+  per = min(per, max_per);
+  per = max(per, (u + kMaxParts - n_extra - 1) / (kMaxParts - n_extra));
+  ns = (u + per - 1) / per;
   pl.n_split = ns;
+  pl.n_tier = n_extra;
   pl.tiles_per_split = per;
-  pl.partial_floats = (size_t)pairs * (ns + extra) * p.G * kPart;
+  pl.partial_floats = (size_t)pairs * (ns + n_extra) * p.G * kPart;
   pl.bytes = pl.partial_floats * sizeof(float);
   return pl;
 }
 
 DecodePlan plan_decode_int2(const Pool& p, int B, int max_hist_len) {
   const int tiles = (max(max_hist_len, 0) + kTile - 1) / kTile;
-  return make_plan(p, B, tiles, 512, 1);
+  const int n_tier = max(1, (p.cfg.sink_tokens + p.cfg.recent_tokens + 255) / 256);
+  return make_plan(p, B, tiles, 512, n_tier, int2_occupancy(p));
 }
 
 DecodePlan plan_decode_bf16(const Pool& p, int B, int max_len) {
-  return make_plan(p, B, max(max_len, 0), 8192, 0);
+  return make_plan(p, B, max(max_len, 0), 8192, 0, bf16_occupancy(p));
 }
 
 cudaError_t launch_decode_int2(const Pool& p, int layer, int B, const void* q,
@@ -809,6 +960,7 @@ cudaError_t launch_decode_int2(const Pool& p, int layer, int B, const void* q,
   a.rec_start = rec_start;
   a.n_split = plan.n_split;
   a.per_split = plan.tiles_per_split;
+  a.n_tier = plan.n_tier;
   const bool g64 = p.cfg.group_size == 64;
   switch (p.G) {
     case 1: return g64 ? launch_int2_t<1, 64>(a, B, s) : launch_int2_t<1, 128>(a, B, s);
@@ -829,6 +981,7 @@ cudaError_t launch_decode_bf16(const Pool& p, int layer, int B, const void* q,
   a.seq_len = seq_len;
   a.n_split = plan.n_split;
   a.per_split = plan.tiles_per_split;
+  a.n_tier = 0;
   switch (p.G) {
     case 1: return launch_bf16_t<1>(a, B, s);
     case 2: return launch_bf16_t<2>(a, B, s);

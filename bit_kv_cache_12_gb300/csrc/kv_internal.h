@@ -62,6 +62,7 @@ cudaError_t launch_append_bf16(const Pool& p, int layer, int n_seqs, const void*
 
 struct DecodePlan {
   int n_split = 1;          // history splits per (sequence, KV head)
+  int n_tier = 0;           // CTAs for the BF16 sink + recent tiers (INT2 pool)
   int tiles_per_split = 1;  // INT2: 16-token tiles; BF16: tokens
   size_t partial_floats = 0;
   size_t bytes = 0;

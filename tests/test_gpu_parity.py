@@ -190,12 +190,12 @@ def test_decode_shapes(G, P, gs):
 def test_decode_edge_lengths():
     """Partial tiles, history 0 and 1, short sink and recent tiers."""
     wl = synth.make_decode_workload("edges", 9, B=6, Hq=8, Hkv=2,
-                                    ctx=[1, 64, 65, 321, 337, 64 + 256 + 17], page_size=16)
+                                    ctx=[1, 64, 65, 321, 337, 350], page_size=16)
+    assert list(wl.hist_len) == [0, 0, 0, 1, 17, 30]
     out, ref, err = _decode_case(wl)
     assert err == 0
     ma, rl = gu.metrics(out, ref)
     assert ma <= MAX_ABS and rl <= REL_L2
-    assert list(wl.hist_len) == [0, 0, 0, 1, 17, 17] or True
 
 
 def test_decode_split_count_invariance():
@@ -204,8 +204,9 @@ def test_decode_split_count_invariance():
     pool = gu.make_int2_pool(wl)
     gu.upload_pages(pool, pages)
     a = gu.gpu_decode(pool, wl)
-    b = gu.gpu_decode(pool, wl, max_hist=int(wl.hist_len[0]) * 4 // 4 + 16 * 0)
-    c = gu.gpu_decode(pool, wl, max_hist=wl.page_table.shape[1] * 16)
+    b = gu.gpu_decode(pool, wl)                                   # same plan: deterministic
+    pt2 = np.concatenate([wl.page_table, np.full((1, 300), -1, np.int32)], axis=1)
+    c = gu.gpu_decode(pool, wl, page_table=pt2, max_hist=pt2.shape[1] * 16)   # other split count
     pool.close()
     assert np.array_equal(a, b)
     assert gu.metrics(c, a)[1] <= 1e-6
@@ -295,6 +296,13 @@ def test_decode_bf16_matches_oracle(G, P):
 # ---------------------------------------------------------------------------
 
 def test_end_to_end_append_then_decode():
+    """GPU append + GPU decode against the oracle's own rotate/quantize/attend
+    pipeline.  The stored codes may differ in a handful of rounding-boundary
+    flips (bounded in the append tests); one flipped V code of a token with
+    weight ~1/N moves an output channel by ~s/N, which at N ~ 1e3 is of the
+    order of 1e-3 of the output norm, so this end-to-end check uses the
+    max-abs bound and a 1e-2 rel-L2 bound; the 1e-3 rel-L2 bound applies to
+    identical stored codes (tests above)."""
     wl = synth.make_decode_workload("e2e", 15, B=2, Hq=8, Hkv=2, ctx=[2100, 900], page_size=16,
                                     outliers_per_head=4)
     pool = gu.make_int2_pool(wl)
@@ -305,4 +313,4 @@ def test_end_to_end_append_then_decode():
     ref = gu.oracle_decode(wl, gu.oracle_pages(wl))
     ma, rl = gu.metrics(out, ref)
     print(f"e2e: max_abs {ma:.3e} rel_l2 {rl:.3e}")
-    assert ma <= MAX_ABS and rl <= REL_L2
+    assert ma <= MAX_ABS and rl <= 1e-2
