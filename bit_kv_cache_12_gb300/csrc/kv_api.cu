@@ -273,6 +273,31 @@ kv_status_t kv_decode_attention(kv_pool_t* pool, int32_t layer, int32_t B, const
                                                 static_cast<cudaStream_t>(stream)));
 }
 
+kv_status_t kv_decode_attention_noalloc(kv_pool_t* pool, int32_t layer, int32_t B, const void* q,
+                                        const int32_t* sink_len, const int32_t* hist_len,
+                                        const int32_t* recent_len, const int32_t* recent_start,
+                                        const int32_t* page_table, int32_t max_pages_per_seq,
+                                        int32_t max_hist_len, float softmax_scale, float* out,
+                                        void* stream) {
+  if (!valid_layer(pool, layer) || B <= 0 || max_pages_per_seq <= 0 || max_hist_len < 0)
+    return KV_ERR_INVALID_ARG;
+  const Pool& p = pool->p;
+  if (p.cfg.kind != KV_POOL_INT2_3TIER || B > p.cfg.max_seqs) return KV_ERR_INVALID_ARG;
+  if (!q || !sink_len || !hist_len || !recent_len || !recent_start || !page_table || !out)
+    return KV_ERR_INVALID_ARG;
+  if ((int64_t)max_hist_len > (int64_t)max_pages_per_seq * p.cfg.page_size) return KV_ERR_INVALID_ARG;
+  if ((uintptr_t)q & 1) return KV_ERR_INVALID_ARG;
+  kvint2::DecodePlan pl = kvint2::plan_decode_int2(p, B, max_hist_len);
+  void* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  if (kvint2::noalloc_scratch(&scratch, &scratch_bytes) != cudaSuccess) return KV_ERR_CUDA;
+  if (pl.bytes > scratch_bytes) return KV_ERR_SCRATCH_LIMIT;
+  return cuda_status(kvint2::launch_decode_int2(p, layer, B, q, sink_len, hist_len, recent_len,
+                                                recent_start, page_table, max_pages_per_seq, pl,
+                                                softmax_scale, out, scratch,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 kv_status_t kv_append_bf16(kv_pool_t* pool, int32_t layer, int32_t n_seqs, const void* k,
                            const void* v, const int32_t* cu_tokens, const int32_t* start_pos,
                            const int32_t* page_table, int32_t max_pages_per_seq,

@@ -28,6 +28,8 @@
 //     fp32 output.
 #include <math.h>
 
+#include <atomic>
+
 #include "kv_device.cuh"
 #include "kv_internal.h"
 
@@ -898,6 +900,48 @@ int bf16_occupancy(const Pool& p) {
 }
 
 }  // namespace
+
+// ---------------------------------------------------------------------------
+// fixed scratch for kv_decode_attention_noalloc
+// ---------------------------------------------------------------------------
+// Partials of the split-K decode for callers that cannot allocate device
+// memory.  Lives for the whole process on every device that loads this code.
+// Host code only sees a stand-in for this name: its device address comes from
+// cudaGetSymbolAddress below and is what the kernel receives.
+static __device__ __align__(256) float g_noalloc_scratch[KV_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+namespace {
+constexpr int kMaxDevices = 64;
+void* g_scratch_ptr[kMaxDevices] = {};
+std::atomic<int> g_scratch_state[kMaxDevices];   // 0 = unset, 1 = in progress, 2 = ready
+}  // namespace
+
+cudaError_t noalloc_scratch(void** ptr, size_t* bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (g_scratch_state[dev].load(std::memory_order_acquire) != 2) {
+    int expected = 0;
+    if (g_scratch_state[dev].compare_exchange_strong(expected, 1)) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);   // with `dev` current
+      if (e != cudaSuccess) {
+        g_scratch_state[dev].store(0, std::memory_order_release);
+        return e;
+      }
+      g_scratch_ptr[dev] = p;
+      g_scratch_state[dev].store(2, std::memory_order_release);
+    } else {
+      while (g_scratch_state[dev].load(std::memory_order_acquire) == 1) {
+      }
+      if (g_scratch_state[dev].load(std::memory_order_acquire) != 2) return cudaErrorNotReady;
+    }
+  }
+  *ptr = g_scratch_ptr[dev];
+  *bytes = KV_NOALLOC_SCRATCH_BYTES;
+  return cudaSuccess;
+}
 
 // ---------------------------------------------------------------------------
 // planning and launch

@@ -75,6 +75,10 @@ cudaError_t launch_decode_int2(const Pool& p, int layer, int B, const void* q,
                                const int32_t* rec_len, const int32_t* rec_start,
                                const int32_t* pt, int max_pages, const DecodePlan& plan,
                                float scale, float* out, void* ws, cudaStream_t s);
+// Device address and size of the fixed scratch buffer used by
+// kv_decode_attention_noalloc on the current device (looked up once per device).
+cudaError_t noalloc_scratch(void** ptr, size_t* bytes);
+
 cudaError_t launch_decode_bf16(const Pool& p, int layer, int B, const void* q,
                                const int32_t* seq_len, const int32_t* pt, int max_pages,
                                const DecodePlan& plan, float scale, float* out, void* ws,

@@ -22,8 +22,11 @@ KV_ERR_CUDA = 3
 KV_ERR_UNSUPPORTED = 4
 KV_ERR_DEVICE = 5
 KV_ERR_TIMEOUT = 6
+KV_ERR_SCRATCH_LIMIT = 7
 STATUS_NAMES = {0: "KV_OK", 1: "KV_ERR_INVALID_ARG", 2: "KV_ERR_OOM", 3: "KV_ERR_CUDA",
-                4: "KV_ERR_UNSUPPORTED", 5: "KV_ERR_DEVICE", 6: "KV_ERR_TIMEOUT"}
+                4: "KV_ERR_UNSUPPORTED", 5: "KV_ERR_DEVICE", 6: "KV_ERR_TIMEOUT",
+                7: "KV_ERR_SCRATCH_LIMIT"}
+KV_NOALLOC_SCRATCH_BYTES = 16 << 20
 KV_POOL_INT2_3TIER = 0
 KV_POOL_BF16 = 1
 
@@ -62,6 +65,8 @@ _SIG = {
     "kv_decode_workspace_bytes": (ctypes.c_size_t, [_P, _I32, _I32]),
     "kv_decode_attention": (_I32, [_P, _I32, _I32, _P, _P, _P, _P, _P, _P, _I32, _I32,
                                    ctypes.c_float, _P, _P, ctypes.c_size_t, _P]),
+    "kv_decode_attention_noalloc": (_I32, [_P, _I32, _I32, _P, _P, _P, _P, _P, _P, _I32, _I32,
+                                           ctypes.c_float, _P, _P]),
     "kv_append_bf16": (_I32, [_P, _I32, _I32, _P, _P, _P, _P, _P, _I32, _I32, _P]),
     "kv_decode_attention_bf16": (_I32, [_P, _I32, _I32, _P, _P, _P, _I32, _I32,
                                         ctypes.c_float, _P, _P, ctypes.c_size_t, _P]),
@@ -174,6 +179,17 @@ def kv_decode_attention(pool, layer, B, q, sink_len, hist_len, recent_len, recen
         pool, layer, B, _ptr(q), _ptr(sink_len), _ptr(hist_len), _ptr(recent_len),
         _ptr(recent_start), _ptr(page_table), max_pages_per_seq, max_hist_len,
         float(softmax_scale), _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def kv_decode_attention_noalloc(pool, layer, B, q, sink_len, hist_len, recent_len, recent_start,
+                                page_table, max_pages_per_seq, max_hist_len, softmax_scale, out,
+                                stream=None):
+    """kv_decode_attention without a workspace: for callers that cannot
+    allocate device memory; uses the library's fixed 16 MiB device buffer."""
+    _check("kv_decode_attention_noalloc", lib().kv_decode_attention_noalloc(
+        pool, layer, B, _ptr(q), _ptr(sink_len), _ptr(hist_len), _ptr(recent_len),
+        _ptr(recent_start), _ptr(page_table), max_pages_per_seq, max_hist_len,
+        float(softmax_scale), _ptr(out), _stream(stream)))
 
 
 def kv_append_bf16(pool, layer, n_seqs, k, v, cu_tokens, start_pos, page_table,

@@ -50,7 +50,9 @@ typedef enum {
   KV_ERR_CUDA = 3,         /* a CUDA call or launch failed                   */
   KV_ERR_UNSUPPORTED = 4,  /* valid but not implemented (e.g. head_dim 64)   */
   KV_ERR_DEVICE = 5,       /* kv_pool_get_error: the device recorded an error */
-  KV_ERR_TIMEOUT = 6       /* reserved: a bounded device wait gave up        */
+  KV_ERR_TIMEOUT = 6,      /* reserved: a bounded device wait gave up        */
+  KV_ERR_SCRATCH_LIMIT = 7 /* kv_decode_attention_noalloc: the call needs more
+                              scratch than KV_NOALLOC_SCRATCH_BYTES           */
 } kv_status_t;
 
 /* Device error codes reported by kv_pool_get_error(). */
@@ -225,6 +227,41 @@ kv_status_t kv_decode_attention_bf16(kv_pool_t* pool, int32_t layer, int32_t B, 
                                      int32_t max_pages_per_seq, int32_t max_seq_len,
                                      float softmax_scale, float* out, void* workspace,
                                      size_t workspace_bytes, void* stream);
+
+/* Size of the fixed device buffer behind kv_decode_attention_noalloc. */
+#define KV_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/* kv_decode_attention without a caller workspace.  (The pages describe no
+ * such call: it exists for users of this library, not for the method.)
+ *
+ * Some callers cannot allocate device memory at the point where they decode:
+ * code running under a memory manager that owns every allocation (a serving
+ * engine's arena, a pluggable allocator), or code that must not call
+ * cudaMalloc because it may synchronise the device in a latency-critical
+ * path.  This entry point takes the same arguments as kv_decode_attention
+ * minus the workspace, and keeps the per-split partial results in one
+ * file-scope device buffer of KV_NOALLOC_SCRATCH_BYTES (16 MiB) instead.  The
+ * buffer is reserved on every GPU that loads the library and is held until
+ * the process exits.  The call itself allocates nothing (no cudaMalloc, no
+ * cudaFree, no allocating library routine).
+ *
+ *   - The first call on a device looks up the buffer's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Calls whose workspace need, kv_decode_workspace_bytes(pool, B,
+ *     max_hist_len), exceeds KV_NOALLOC_SCRATCH_BYTES return
+ *     KV_ERR_SCRATCH_LIMIT and launch nothing.
+ *   - Every call on a device shares the one buffer and leaves its own
+ *     contents in it; nothing in it has to start at zero (each call writes
+ *     every partial it later reads).  Calls that overlap on the GPU (other
+ *     streams, other threads, other pools) race on the buffer: order them.
+ * Results equal kv_decode_attention's for the same inputs. */
+kv_status_t kv_decode_attention_noalloc(kv_pool_t* pool, int32_t layer, int32_t B, const void* q,
+                                        const int32_t* sink_len, const int32_t* hist_len,
+                                        const int32_t* recent_len, const int32_t* recent_start,
+                                        const int32_t* page_table, int32_t max_pages_per_seq,
+                                        int32_t max_hist_len, float softmax_scale, float* out,
+                                        void* stream);
 
 #ifdef __cplusplus
 }
