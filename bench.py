@@ -119,45 +119,39 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(wl, max_heads=1):
-    """Time the oracle on a bounded sample: one KV head (its G query heads)
-    over the full context; scaled to one whole step (all KV heads)."""
+def cpu_baseline(wl, min_seconds=10.0, max_seconds=30.0):
+    """Time the oracle on the host cores: whole decode steps (every KV head and
+    query head, full context) repeated until about ``min_seconds`` of CPU work
+    has run; the value is the mean time of one step."""
     from oracle import attention as att
     from oracle import kvquant as kq
     tb = kq.tile_bytes(wl.group_size) * (wl.page_size // 16)
     pages = np.zeros((wl.num_pages, wl.Hkv, tb), np.uint8)
-    for b in range(wl.B):                      # pack the sampled heads (setup, not timed)
-        if wl.hist_len[b] == 0:
-            continue
-        one = kq.pack_history_full(wl.hist_k[b][:, :max_heads], wl.hist_v[b][:, :max_heads],
-                                   wl.Rk, wl.Rv, wl.clip_k, wl.clip_v, wl.page_table[b],
-                                   wl.num_pages, max_heads, wl.page_size, wl.group_size)
-        used = wl.page_table[b][wl.page_table[b] >= 0]
-        pages[used, :max_heads] = one[used]
+    for b in range(wl.B):                      # packing is setup, not timed
+        if wl.hist_len[b]:
+            kq.pack_history_full(wl.hist_k[b], wl.hist_v[b], wl.Rk, wl.Rv, wl.clip_k, wl.clip_v,
+                                 wl.page_table[b], wl.num_pages, wl.Hkv, wl.page_size,
+                                 wl.group_size, pages)
+    hist = lambda b, g: kq.read_history(pages, wl.page_table[b], int(wl.hist_len[b]), g,
+                                        wl.page_size, wl.group_size)
+    steps = 0
     t0 = time.perf_counter()
-    for b in range(wl.B):
-        for g in range(max_heads):
-            kc, vc, sk, zk, sv, zv = kq.read_history(pages, wl.page_table[b], int(wl.hist_len[b]), g,
-                                                     wl.page_size, wl.group_size)
-            kd = kq.dequant(kc, sk, zk, wl.group_size); vd = kq.dequant(vc, sv, zv, wl.group_size)
-            s_ = int(wl.sink_len[b]); r_ = int(wl.rec_len[b])
-            skk = kq.bf16_bits_to_f64(wl.sink_k[b, g, :s_]); svv = kq.bf16_bits_to_f64(wl.sink_v[b, g, :s_])
-            rk = kq.bf16_bits_to_f64(att.ring_order(wl.rec_k[b, g], wl.rec_start[b], r_, wl.rec_k.shape[2]))
-            rv = kq.bf16_bits_to_f64(att.ring_order(wl.rec_v[b, g], wl.rec_start[b], r_, wl.rec_v.shape[2]))
-            for hh in range(wl.G):
-                qf = kq.bf16_bits_to_f64(wl.q[b, g * wl.G + hh])
-                att.three_tier_head(qf, wl.Rk[g].astype(np.float64), wl.Rv[g].astype(np.float64),
-                                    skk, svv, kd, vd, rk, rv, wl.scale)
-    dt = time.perf_counter() - t0
-    step_s = dt * wl.Hkv / max_heads
+    while True:
+        att.decode_three_tier(wl.q, wl.Rk, wl.Rv, wl.sink_k, wl.sink_v, wl.sink_len, hist,
+                              wl.hist_len, wl.rec_k, wl.rec_v, wl.rec_len, wl.rec_start, wl.Hkv,
+                              wl.group_size, wl.scale)
+        steps += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds or dt + dt / steps > max_seconds:
+            break
     try:
         cores = len(os.sched_getaffinity(0))
     except Exception:
         cores = os.cpu_count()
-    return {"value": step_s * 1e6, "unit": "us", "cores": cores, "kind": "oracle",
-            "sample": f"{max_heads} of {wl.Hkv} KV heads ({max_heads * wl.G} of {wl.Hq} query heads) "
-                      f"x full context, numpy fp64 oracle (unpack + dequant + attention), "
-                      f"scaled x{wl.Hkv // max_heads} to one step; measured {dt:.2f} s"}
+    return {"value": dt / steps * 1e6, "unit": "us", "cores": cores, "kind": "oracle",
+            "sample": f"{steps} whole decode steps of the bench workload (all {wl.Hkv} KV heads, "
+                      f"{wl.Hq} query heads, full context) with the numpy fp64 oracle "
+                      f"(unpack, dequantize, three-tier attention) in {dt:.1f} s"}
 
 
 def run_reference(args, rank, world):
@@ -165,11 +159,8 @@ def run_reference(args, rank, world):
         return
     from bit_kv_cache_12_gb300 import synth
     wl = synth.qwen3_4b_decode(ctx=args.ctx)
-    vals = []
-    for _ in range(max(1, min(args.steps, 3))):
-        cb = cpu_baseline(wl)
-        vals.append(cb["value"])
-    cb["value"] = float(np.mean(vals))
+    cb = cpu_baseline(wl, min_seconds=min(60.0, 10.0 * max(1, args.steps) / 10))
+    vals = [cb["value"]]
     line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "us",
             "n_gpus": world, "steps": len(vals), "warmup": 0, "ms_per_step": cb["value"] / 1e3,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",

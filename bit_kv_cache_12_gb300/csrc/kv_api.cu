@@ -103,7 +103,7 @@ kv_status_t kv_pool_create(const kv_pool_config_t* cfg, void* stream, kv_pool_t*
     ok = ok && dev_alloc(&p.Rk, L * H * 128 * 128 * sizeof(float));
     ok = ok && dev_alloc(&p.RvT, L * H * 128 * 128 * sizeof(float));
     ok = ok && dev_alloc(&p.clip, L * 2 * H * 128 * sizeof(float));
-    ok = ok && dev_alloc(&p.rfrag, L * H * 2 * kvint2::rfrag_per_head() * sizeof(uint4));
+    ok = ok && dev_alloc(&p.rfrag, L * H * kvint2::kFragBlocks * kvint2::rfrag_per_head() * sizeof(uint4));
   } else {
     p.bf16_layer_stride = (size_t)c.num_pages * H * c.page_size * 128;
     ok = ok && dev_alloc(&p.bk, L * p.bf16_layer_stride * 2);

@@ -64,7 +64,7 @@ struct AppendArgs {
   const int32_t* pt;
   int max_pages, n_seqs, max_tiles, Hkv;
   long long num_pages;
-  const uint4* rfrag;       // layer base [Hkv][2][4096]
+  const uint4* rfrag;       // layer base [Hkv][kFragBlocks][4096]
   const float* clip;        // layer base [2][Hkv][128]
   int tasks_per_cta;
   int* err;
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(256, 2) append_kernel(AppendArgs a) {
   const int r = lane >> 2, j = lane & 3;
   constexpr int NG = 128 / GS;
 
-  const uint4* src = a.rfrag + ((size_t)g * 2 + tensor) * 4096;
+  const uint4* src = a.rfrag + ((size_t)g * kFragBlocks + tensor) * 4096;
   for (int i = threadIdx.x; i < 4096; i += blockDim.x) sfrag[i] = __ldg(src + i);
   if (threadIdx.x < 128) sclip[threadIdx.x] = a.clip[((size_t)tensor * a.Hkv + g) * 128 + threadIdx.x];
   __syncthreads();
@@ -352,20 +352,32 @@ __device__ __forceinline__ int in_ch(int s, int kappa) {
 __global__ void rotation_frag_kernel(const float* __restrict__ Rk, const float* __restrict__ Rv,
                                      uint4* __restrict__ frag, int Hkv) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= Hkv * 2 * 4096) return;
-  const int h = idx / 8192, tensor = (idx / 4096) & 1, f = idx & 4095;
+  if (idx >= Hkv * kFragBlocks * 4096) return;
+  const int h = idx / (kFragBlocks * 4096), tensor = (idx / 4096) % kFragBlocks, f = idx & 4095;
   const int lane = f & 31;
   const int r = lane >> 2, j = lane & 3;
   uint4 out;
-  if (tensor == 0) {
-    // B operand of x R_k: element (kappa, n) = R_k[in_ch(s, kappa)][8 nt + n]
+  if (tensor != 1) {
+    // B operand of x M: element (kappa, n) = M[in_ch(s, kappa)][8 nt + n], with
+    // M = R_k (blocks 0, 3) or M = R_v^T, M[i][c] = R_v[c][i] (blocks 2, 4);
+    // blocks 3 and 4 hold the third bf16 term of the same elements
     const int nt = (f >> 5) & 15, s = f >> 9;
-    const float* R = Rk + (size_t)h * 16384;
     const int col = 8 * nt + r;
     uint16_t hi[4], lo[4];
     const int ks[4] = {2 * j, 2 * j + 1, 2 * j + 8, 2 * j + 9};
 #pragma unroll
-    for (int u = 0; u < 4; ++u) split_bf16(R[in_ch(s, ks[u]) * 128 + col], hi[u], lo[u]);
+    for (int u = 0; u < 4; ++u) {
+      const int i = in_ch(s, ks[u]);
+      const float m = (tensor == 0 || tensor == 3) ? Rk[(size_t)h * 16384 + i * 128 + col]
+                                                   : Rv[(size_t)h * 16384 + col * 128 + i];
+      split_bf16(m, hi[u], lo[u]);
+      if (tensor >= 3) {   // third term: bf16(m - hi - lo)
+        const float rest = (m - __bfloat162float(__ushort_as_bfloat16(hi[u]))) -
+                           __bfloat162float(__ushort_as_bfloat16(lo[u]));
+        hi[u] = __bfloat16_as_ushort(__float2bfloat16_rn(rest));
+        lo[u] = 0;
+      }
+    }
     out = make_uint4(pack2(hi[0], hi[1]), pack2(hi[2], hi[3]), pack2(lo[0], lo[1]), pack2(lo[2], lo[3]));
   } else {
     // A operand of R_v^T x^T: element (row m, kappa) = R_v[in_ch(s, kappa)][16 i + m]
@@ -457,8 +469,8 @@ cudaError_t launch_rotation_prep(const Pool& p, int layer, const float* Rk, cons
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  uint4* frag = p.rfrag + (size_t)layer * H * 2 * rfrag_per_head();
-  const int n = H * 2 * 4096;
+  uint4* frag = p.rfrag + (size_t)layer * H * kFragBlocks * rfrag_per_head();
+  const int n = H * kFragBlocks * 4096;
   rotation_frag_kernel<<<(n + 255) / 256, 256, 0, s>>>(Rk, Rv, frag, H);
   return cudaGetLastError();
 }
@@ -516,7 +528,7 @@ cudaError_t launch_append(const Pool& p, int layer, int n_seqs, const void* k, c
   a.max_tiles = (max_tokens + kTile - 1) / kTile + 1;   // +1: an unaligned start spans one more
   a.Hkv = H;
   a.num_pages = p.cfg.num_pages;
-  a.rfrag = p.rfrag + (size_t)layer * H * 2 * rfrag_per_head();
+  a.rfrag = p.rfrag + (size_t)layer * H * kFragBlocks * rfrag_per_head();
   a.clip = p.clip + (size_t)layer * 2 * H * 128;
   a.err = p.err;
   const long long tasks = (long long)n_seqs * a.max_tiles;

@@ -44,12 +44,19 @@ constexpr float kNegInf = -INFINITY;
 constexpr int kStages = 4;       // tiles in each warp's ring
 constexpr int kMaxPids = 520;    // page ids staged per CTA (splits cover <= 512 tiles / 8192 tokens)
 constexpr int kMaxParts = 400;   // partials per (sequence, KV head) the final merge reads
+// The history loop keeps each head's exponent reference kSlack (log2 units)
+// above the largest score seen when it was last moved, so weights stay <= 1
+// and the accumulators are rescaled only when a score passes the reference.
+constexpr float kSlack = 4.0f;
+// Sink + recent tokens per tier CTA (staged in the 48 KB "big" region).
+constexpr int kTierTokens = 80;
 
 struct DecodeArgs {
   const uint8_t* hist;      // INT2 layer base
   size_t page_bytes;
   int tile_bytes;
   int tiles_per_page;
+  int tpp_shift;            // log2(tiles_per_page)
   const uint16_t* bk;       // BF16 pool layer base
   const uint16_t* bv;
   const uint16_t* sink_k;   // tier layer bases
@@ -59,6 +66,7 @@ struct DecodeArgs {
   int sink_cap, rec_cap;
   const float* Rk;          // layer base [Hkv][128][128]
   const float* RvT;
+  const uint4* rfrag;       // layer base [Hkv][kFragBlocks][4096] rotation MMA fragments
   const uint16_t* q;
   const int32_t* sink_len;
   const int32_t* hist_len;
@@ -81,41 +89,67 @@ struct DecodeArgs {
 // shared helpers
 // ---------------------------------------------------------------------------
 
-// out[h][c] = sum_i in[h][i] R[i][c] for h < NH.  Thread (i-group ig, column
-// quad cq) loads its 16 x float4 of R at once (one memory latency), then the
-// eight i-groups are summed through shared memory (scratch [8][NH][128]).
-template <int NH>
-__device__ void rows_times_R(const float* in, const float* __restrict__ R, float* scratch,
-                             float* out) {
-  const int cq = threadIdx.x & 31, ig = threadIdx.x >> 5;
-  float4 rr[16];
+// Y[h][c] = sum_i X[h][i] M[i][c] for the first NROWS rows of X (shared,
+// [*][128] fp32), on the tensor cores.  M comes as three bf16 terms
+// (hi + lo from fragment block `b`, the third term from block `b3`), X rows
+// are split into bf16 terms too (three when SPLIT, else X must be exact in
+// bf16); the products above 2^-24 relative are kept, fp32 accumulate.  Warp w
+// produces columns 16w..16w+15; each lane loads its fragments at once.
+template <int NROWS, bool SPLIT>
+__device__ void rot_mma(const float* X, const uint4* __restrict__ frag,
+                        const uint4* __restrict__ frag3, float* Y) {
+  static_assert(NROWS <= 8, "rows");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r = lane >> 2, j = lane & 3;
+  uint4 f[8][2];
+  uint2 f3[8][2];
 #pragma unroll
-  for (int u = 0; u < 16; ++u)
-    rr[u] = __ldg(reinterpret_cast<const float4*>(R + (ig * 16 + u) * 128) + cq);
-  float acc[NH][4];
+  for (int s = 0; s < 8; ++s)
 #pragma unroll
-  for (int h = 0; h < NH; ++h) acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.f;
+    for (int u = 0; u < 2; ++u) {
+      const int idx = (s * 16 + 2 * warp + u) * 32 + lane;
+      f[s][u] = __ldg(frag + idx);
+      const uint4 t = __ldg(frag3 + idx);
+      f3[s][u] = make_uint2(t.x, t.y);
+    }
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  const bool row_ok = r < NROWS;
+  auto bf2 = [](float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  };
+  auto lo2 = [](uint32_t u) { return __uint_as_float(u << 16); };
+  auto hi2 = [](uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); };
 #pragma unroll
-  for (int u = 0; u < 16; ++u) {
+  for (int s = 0; s < 8; ++s) {
+    // A: row r, k index kappa -> input channel 32*(kappa%8/2) + 4s + 2*(kappa/8) + kappa%2
+    const float4 x = row_ok ? *reinterpret_cast<const float4*>(X + r * 128 + 32 * j + 4 * s)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    const uint32_t a0 = bf2(x.x, x.y), a2 = bf2(x.z, x.w);
 #pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      const float x = in[h * 128 + ig * 16 + u];
-      acc[h][0] = fmaf(x, rr[u].x, acc[h][0]);
-      acc[h][1] = fmaf(x, rr[u].y, acc[h][1]);
-      acc[h][2] = fmaf(x, rr[u].z, acc[h][2]);
-      acc[h][3] = fmaf(x, rr[u].w, acc[h][3]);
+    for (int u = 0; u < 2; ++u) {
+      mma_bf16(acc[u], a0, 0u, a2, 0u, f[s][u].x, f[s][u].y);      // hi * hi
+      mma_bf16(acc[u], a0, 0u, a2, 0u, f[s][u].z, f[s][u].w);      // hi * lo
+      mma_bf16(acc[u], a0, 0u, a2, 0u, f3[s][u].x, f3[s][u].y);    // hi * lo2
+    }
+    if (SPLIT) {
+      const float r0 = x.x - lo2(a0), r1 = x.y - hi2(a0), r2 = x.z - lo2(a2), r3 = x.w - hi2(a2);
+      const uint32_t b0 = bf2(r0, r1), b2 = bf2(r2, r3);
+      const uint32_t c0 = bf2(r0 - lo2(b0), r1 - hi2(b0)), c2 = bf2(r2 - lo2(b2), r3 - hi2(b2));
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        mma_bf16(acc[u], b0, 0u, b2, 0u, f[s][u].x, f[s][u].y);    // lo * hi
+        mma_bf16(acc[u], b0, 0u, b2, 0u, f[s][u].z, f[s][u].w);    // lo * lo
+        mma_bf16(acc[u], c0, 0u, c2, 0u, f[s][u].x, f[s][u].y);    // lo2 * hi
+      }
     }
   }
+  __syncthreads();   // everyone has read X
+  if (row_ok) {
 #pragma unroll
-  for (int h = 0; h < NH; ++h)
-    *reinterpret_cast<float4*>(scratch + (ig * NH + h) * 128 + 4 * cq) =
-        make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < NH * 128; idx += kThreads) {
-    float v = 0.f;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) v += scratch[q * NH * 128 + idx];
-    out[idx] = v;
+    for (int u = 0; u < 2; ++u)
+      *reinterpret_cast<float2*>(Y + r * 128 + 16 * warp + 8 * u + 2 * j) =
+          make_float2(acc[u][0], acc[u][1]);
   }
   __syncthreads();
 }
@@ -269,10 +303,19 @@ struct WarpAcc {
 // A zero bf16 row: stands in for tokens a warp must not read (past the end of
 // the range or behind an invalid page id); their weight is forced to 0.
 __device__ __align__(16) uint16_t g_zero_row[128];
+// A zero INT2 tile (largest tile size): copied in place of a tile behind an
+// invalid page id, so every ring slot always holds finite data.
+__device__ __align__(16) uint8_t g_zero_tile[1280];
 
 // rows(u, k, v) sets bf16 row pointers for token u and returns false if the
 // token must be skipped.  All loads of a phase are issued before their use.
-template <int G, class RowFn>
+template <bool kShared, class T>
+__device__ __forceinline__ T load_row(const T* p) {
+  if (kShared) return *p;   // rows staged in shared memory (generic load)
+  return __ldg(p);
+}
+
+template <int G, bool kShared, class RowFn>
 __device__ void bf16_rows_attend(const float* sq, float* sp, int u0, int u1, int stride,
                                  const RowFn& rows, float scale_log2, WarpAcc<G>& st) {
   const int lane = threadIdx.x & 31;
@@ -291,7 +334,7 @@ __device__ void bf16_rows_attend(const float* sq, float* sp, int u0, int u1, int
     for (int half = 0; half < 2; ++half) {
       uint4 kk[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) kk[i] = __ldg(kr + half * 8 + i);
+      for (int i = 0; i < 8; ++i) kk[i] = load_row<kShared>(kr + half * 8 + i);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const uint4 w = kk[i];
@@ -333,7 +376,7 @@ __device__ void bf16_rows_attend(const float* sq, float* sp, int u0, int u1, int
       for (int e = 0; e < 8; ++e) {
         const uint16_t* vr =
             reinterpret_cast<const uint16_t*>(__shfl_sync(0xffffffffu, vbits, tb * 8 + e));
-        vv[e] = __ldg(reinterpret_cast<const uint2*>(vr) + lane);
+        vv[e] = load_row<kShared>(reinterpret_cast<const uint2*>(vr) + lane);
       }
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -411,6 +454,8 @@ struct Smem {
   static constexpr int total = big + big_floats;
   // the final merge runs from `scratch` on
   static_assert(total - scratch >= 16 + 1024 + 2 * kMaxParts * G, "merge scratch");
+  static_assert(!kRing || big_floats * 4 >= kTierTokens * (272 + 256), "tier staging");
+  static_assert(kWarps * HP * 128 >= kWarps * 32 * G, "tier weights in scratch");
 };
 
 // ---------------------------------------------------------------------------
@@ -441,8 +486,8 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
   }
 
   // ---- page ids of this CTA's tiles and q -> shared memory (one latency) ----
-  const int tpp = a.tiles_per_page;
-  const int p_begin = t_begin / tpp, p_count = (t_end - 1) / tpp + 1 - p_begin;
+  const int tsh = a.tpp_shift, tmask = a.tiles_per_page - 1;
+  const int p_begin = t_begin >> tsh, p_count = ((t_end - 1) >> tsh) + 1 - p_begin;
   int* spid = reinterpret_cast<int*>(sm + S::spid);
   const int32_t* ptrow = a.pt + (size_t)b * a.max_pages;
   for (int i = threadIdx.x; i < p_count; i += kThreads) spid[i] = __ldg(ptrow + p_begin + i);
@@ -454,30 +499,29 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
   // ---- start streaming this warp's first tiles into its ring ----
   uint8_t* ring = reinterpret_cast<uint8_t*>(sm + S::ring) + (size_t)warp * kStages * 32 * LB;
   const uint8_t* head_base = a.hist + (size_t)g * (a.page_bytes / a.Hkv);
+  const int lane_k = 16 * lane;
+  const int lane_sz = (GS == 128) ? 1024 + 16 * r : 1024 + 32 * r;
+  uint8_t* ring_lane = ring + lane * LB;
   auto issue = [&](int t, int stage) {
     if (t < t_end) {
-      const int pid = spid[t / tpp - p_begin];
-      if (pid >= 0 && pid < a.num_pages) {
-        const uint8_t* tb =
-            head_base + (size_t)pid * a.page_bytes + (size_t)(t % tpp) * a.tile_bytes;
-        uint8_t* d = ring + (stage * 32 + lane) * LB;
-        cp_async16(d, tb + 16 * lane);
-        cp_async16(d + 16, tb + 512 + 16 * lane);
-        if (GS == 128) {
-          cp_async16(d + 32, tb + 1024 + 16 * r);
-        } else {
-          cp_async16(d + 32, tb + 1024 + 32 * r);
-          cp_async16(d + 48, tb + 1024 + 32 * r + 16);
-        }
-      }
+      const int pid = spid[(t >> tsh) - p_begin];
+      const uint8_t* tb = (pid >= 0 && pid < a.num_pages)
+                              ? head_base + (size_t)pid * a.page_bytes + (t & tmask) * a.tile_bytes
+                              : g_zero_tile;
+      uint8_t* d = ring_lane + stage * (32 * LB);
+      cp_async16(d, tb + lane_k);
+      cp_async16(d + 16, tb + 512 + lane_k);
+      cp_async16(d + 32, tb + lane_sz);
+      if (GS == 64) cp_async16(d + 48, tb + lane_sz + 16);
     }
     cp_async_commit();   // empty groups keep the group count uniform
   };
 #pragma unroll
-  for (int st = 0; st < kStages - 1; ++st) issue(t_begin + warp + kWarps * st, st);
+  for (int st = 0; st < kStages - 1; ++st) issue(t_begin + warp + kWarps * st, st);   // tiles 0..2
 
   // ---- q' = q R_k and its per-group sums (overlaps the first copies) ----
-  rows_times_R<S::HP>(sq, a.Rk + (size_t)g * 128 * 128, sm + S::scratch, sqr);
+  rot_mma<S::HP, false>(sq, a.rfrag + ((size_t)g * kFragBlocks + 0) * 4096,
+                        a.rfrag + ((size_t)g * kFragBlocks + 3) * 4096, sqr);
   for (int hh = warp; hh < S::HP; hh += kWarps) {
 #pragma unroll
     for (int grp = 0; grp < NG; ++grp) {
@@ -528,18 +572,60 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
       for (int u = 0; u < 4; ++u) oacc[i][nt][u] = 0.f;
   }
 
+  // QK of one tile: scores[token][column] on the tensor cores, in two
+  // independent accumulator chains (the two groups for group 64, the even and
+  // odd k-steps for group 128)
+  auto qk_tile = [&](const uint4& kq4, float (&sacc)[2][NT][4]) {
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) sacc[ch][nt][u] = 0.f;
+    const uint32_t kw[4] = {kq4.x, kq4.y, kq4.z, kq4.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t fr[8];
+      unpack_word(kw[w], fr);
+#pragma unroll
+      for (int sh = 0; sh < 2; ++sh) {
+        const int s = 2 * w + sh;
+        const int ch = (GS == 64) ? (s >> 2) : (s & 1);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          mma_f16(sacc[ch][nt], fr[4 * sh + 0], fr[4 * sh + 1], fr[4 * sh + 2], fr[4 * sh + 3],
+                  qf[s][nt][0], qf[s][nt][1]);
+      }
+    }
+  };
+  auto read_slot = [&](int k, uint4& kq4, uint4& vq4, uint4& sz0, uint4& sz1) {
+    const uint8_t* src = ring_lane + (k % kStages) * (32 * LB);
+    kq4 = *reinterpret_cast<const uint4*>(src);
+    vq4 = *reinterpret_cast<const uint4*>(src + 16);
+    sz0 = *reinterpret_cast<const uint4*>(src + 32);
+    sz1 = (GS == 64) ? *reinterpret_cast<const uint4*>(src + 48) : make_uint4(0, 0, 0, 0);
+  };
+
+  // Software pipeline over this warp's tiles: iteration k runs the softmax and
+  // PV of tile k while the QK of tile k+1 is in flight, so the two dependent
+  // chains interleave.  Ring: tile k+4 is copied into tile k's slot.
+  issue(t_begin + warp + kWarps * (kStages - 1), kStages - 1);
+  float sacc[2][NT][4];
+  uint4 vcur = make_uint4(0, 0, 0, 0), szc0 = vcur, szc1 = vcur;
+  if (t_begin + warp < t_end) {
+    uint4 kq4;
+    cp_async_wait<kStages - 1>();
+    read_slot(0, kq4, vcur, szc0, szc1);
+    qk_tile(kq4, sacc);
+  }
   int k = 0;
   for (int t = t_begin + warp; t < t_end; t += kWarps, ++k) {
-    issue(t + kWarps * (kStages - 1), (k + kStages - 1) % kStages);
+    issue(t + kWarps * kStages, k % kStages);
     cp_async_wait<kStages - 1>();
-    const uint8_t* src = ring + ((k % kStages) * 32 + lane) * LB;
-    const uint4 kq4 = *reinterpret_cast<const uint4*>(src);
-    const uint4 vq4 = *reinterpret_cast<const uint4*>(src + 16);
-    const uint4 sz0 = *reinterpret_cast<const uint4*>(src + 32);
-    const uint4 sz1 =
-        (GS == 64) ? *reinterpret_cast<const uint4*>(src + 48) : make_uint4(0, 0, 0, 0);
+    uint4 kn, vn, sn0, sn1;
+    read_slot(k + 1, kn, vn, sn0, sn1);
 
-    const int pid_cur = spid[t / tpp - p_begin];
+    const int pid_cur = spid[(t >> tsh) - p_begin];
     const bool page_ok = pid_cur >= 0 && pid_cur < a.num_pages;
     if (!page_ok && lane == 0) flag_error(a.err, KV_DEVERR_PAGE_ID);
     const bool v0 = page_ok && (t * kTile + r) < h;
@@ -548,14 +634,14 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
     // scale / zero of tokens r and r+8
     float sk[2][NG], zk[2][NG], sv[2][NG], zv[2][NG];
     if (GS == 128) {
-      const __half2 a0 = u32_as_h2(sz0.x), a1 = u32_as_h2(sz0.y);
-      const __half2 b0 = u32_as_h2(sz0.z), b1 = u32_as_h2(sz0.w);
+      const __half2 a0 = u32_as_h2(szc0.x), a1 = u32_as_h2(szc0.y);
+      const __half2 b0 = u32_as_h2(szc0.z), b1 = u32_as_h2(szc0.w);
       sk[0][0] = __low2float(a0); zk[0][0] = __high2float(a0);
       sv[0][0] = __low2float(a1); zv[0][0] = __high2float(a1);
       sk[1][0] = __low2float(b0); zk[1][0] = __high2float(b0);
       sv[1][0] = __low2float(b1); zv[1][0] = __high2float(b1);
     } else {
-      const uint4 s0 = sz0, s1 = sz1;
+      const uint4 s0 = szc0, s1 = szc1;
       sk[0][0] = __low2float(u32_as_h2(s0.x)); zk[0][0] = __high2float(u32_as_h2(s0.x));
       sk[0][NG - 1] = __low2float(u32_as_h2(s0.y)); zk[0][NG - 1] = __high2float(u32_as_h2(s0.y));
       sv[0][0] = __low2float(u32_as_h2(s0.z)); zv[0][0] = __high2float(u32_as_h2(s0.z));
@@ -566,35 +652,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
       sv[1][NG - 1] = __low2float(u32_as_h2(s1.w)); zv[1][NG - 1] = __high2float(u32_as_h2(s1.w));
     }
 
-    // ---- QK: scores[token][column] on the tensor cores ----
-    // two independent accumulator chains: the two groups (group 64) or the
-    // even / odd k-steps (group 128)
-    float sacc[2][NT][4];
-#pragma unroll
-    for (int ch = 0; ch < 2; ++ch)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int u = 0; u < 4; ++u) sacc[ch][nt][u] = 0.f;
-    {
-      const uint32_t kw[4] = {kq4.x, kq4.y, kq4.z, kq4.w};
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        uint32_t fr[8];
-        unpack_word(kw[w], fr);
-#pragma unroll
-        for (int sh = 0; sh < 2; ++sh) {
-          const int s = 2 * w + sh;
-          const int ch = (GS == 64) ? (s >> 2) : (s & 1);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            mma_f16(sacc[ch][nt], fr[4 * sh + 0], fr[4 * sh + 1], fr[4 * sh + 2], fr[4 * sh + 3],
-                    qf[s][nt][0], qf[s][nt][1]);
-        }
-      }
-    }
-
-    // ---- softmax update and PV B fragments ----
+    // ---- softmax update and PV B fragments of tile k ----
     uint32_t bpv[NG][NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -618,10 +676,12 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
       tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
       tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
       tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
-      const float mnew = fmaxf(m_run[nt], tmax);
-      const bool need = mnew > m_run[nt];
+      // m_run is the exponent reference (>= every score seen so far)
+      const bool need = tmax > m_run[nt];
       if (__any_sync(0xffffffffu, need)) {
-        const float alpha = need ? ((m_run[nt] == kNegInf) ? 0.f : exp2f(m_run[nt] - mnew)) : 1.f;
+        const float mnew = need ? tmax + kSlack : m_run[nt];
+        const float alpha = need ? ((m_run[nt] == kNegInf) ? 0.f : exp2_neg(m_run[nt] - mnew)) : 1.f;
+        m_run[nt] = mnew;
         l_run[nt] *= alpha;
 #pragma unroll
         for (int grp = 0; grp < NG; ++grp) zs[nt][grp] *= alpha;
@@ -630,24 +690,27 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
 #pragma unroll
           for (int u = 0; u < 4; ++u) oacc[i][nt][u] *= alpha;
       }
-      m_run[nt] = mnew;
-      const float base = (mnew == kNegInf) ? 0.f : mnew;
-      const float p0 = exp2f(l0 - base), p1 = exp2f(l1 - base);
+      const float base = (m_run[nt] == kNegInf) ? 0.f : m_run[nt];
+      const float p0 = exp2_neg(l0 - base), p1 = exp2_neg(l1 - base);
       l_run[nt] += p0 + p1;
+      // masked tokens have p = 0 and finite (stale or zero) records
 #pragma unroll
       for (int grp = 0; grp < NG; ++grp) {
-        const float w0 = v0 ? p0 * sv[0][grp] : 0.f;
-        const float w1 = v1 ? p1 * sv[1][grp] : 0.f;
-        zs[nt][grp] += (v0 ? p0 * (zv[0][grp] + sv[0][grp]) : 0.f) +
-                       (v1 ? p1 * (zv[1][grp] + sv[1][grp]) : 0.f);
+        const float w0 = p0 * sv[0][grp];
+        const float w1 = p1 * sv[1][grp];
+        zs[nt][grp] = fmaf(p0, zv[0][grp] + sv[0][grp], fmaf(p1, zv[1][grp] + sv[1][grp], zs[nt][grp]));
         bpv[grp][nt][0] = movmatrix_t(split_hi_lo(w0));
         bpv[grp][nt][1] = movmatrix_t(split_hi_lo(w1));
       }
     }
 
-    // ---- PV: value accumulator [channel][column] on the tensor cores ----
+    // ---- QK of tile k+1 (independent of the PV below) ----
+    float snext[2][NT][4];
+    if (t + kWarps < t_end) qk_tile(kn, snext);
+
+    // ---- PV of tile k: value accumulator [channel][column] ----
     {
-      const uint32_t vw[4] = {vq4.x, vq4.y, vq4.z, vq4.w};
+      const uint32_t vw[4] = {vcur.x, vcur.y, vcur.z, vcur.w};
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         uint32_t fr[8];
@@ -663,6 +726,15 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
         }
       }
     }
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) sacc[ch][nt][u] = snext[ch][nt][u];
+    vcur = vn;
+    szc0 = sn0;
+    szc1 = sn1;
   }
   cp_async_wait<0>();
   __syncthreads();   // every warp is done with its ring before the results reuse it
@@ -695,13 +767,17 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
   __syncthreads();
   merge_warps<G>(swo, swm, swl, sqr, sm + S::smm, sm + S::sml);   // q' no longer needed
   // back to the original basis: o = o' R_v^T
-  rows_times_R<G>(sqr, a.RvT + (size_t)g * 128 * 128, sm + S::scratch, sq);
+  rot_mma<G, true>(sqr, a.rfrag + ((size_t)g * kFragBlocks + 2) * 4096,
+                   a.rfrag + ((size_t)g * kFragBlocks + 4) * 4096, sq);
   write_partial<G>(part, sq, sm + S::smm, sm + S::sml);
 }
 
 // ---------------------------------------------------------------------------
 // BF16 sink + recent tiers of the INT2 pool (tier CTA `ti` of n_tier)
 // ---------------------------------------------------------------------------
+constexpr int kTierRowK = 272;   // staged K row stride (bytes): 256 + 16 keeps lane reads conflict-free
+constexpr int kTierRowV = 256;
+
 template <int G, int GS>
 __device__ void bf16_tiers(const DecodeArgs& a, int b, int g, int ti, float* sm, float* part) {
   using S = Smem<G, GS>;
@@ -713,33 +789,46 @@ __device__ void bf16_tiers(const DecodeArgs& a, int b, int g, int ti, float* sm,
     nr = max(0, min(nr, a.rec_cap));
     rs = max(0, min(rs, a.rec_cap - 1));
   }
-  float* sq = sm + S::sq;
-  load_q<G>(a, b, g, sq, G);
+  // this tier CTA's share of the sink + recent tokens
+  const int n = ns + nr, per = (n + a.n_tier - 1) / a.n_tier;
+  const int u0 = min(n, ti * per), u1 = min(n, u0 + per);
   const size_t seq_head = (size_t)b * a.Hkv + g;
   const uint16_t* sk = a.sink_k + seq_head * a.sink_cap * 128;
   const uint16_t* sv = a.sink_v + seq_head * a.sink_cap * 128;
   const uint16_t* rk = a.rec_k + seq_head * a.rec_cap * 128;
   const uint16_t* rv = a.rec_v + seq_head * a.rec_cap * 128;
   const int cap = a.rec_cap;
+  auto src_row = [&](int u, bool key) -> const uint16_t* {
+    if (u < ns) return (key ? sk : sv) + (size_t)u * 128;
+    int idx = rs + (u - ns);
+    idx -= (idx >= cap) ? cap : 0;
+    return (key ? rk : rv) + (size_t)idx * 128;
+  };
+  // stage the K and V rows of [u0, u1) into shared memory with one burst of copies
+  uint8_t* stk = reinterpret_cast<uint8_t*>(sm + S::big);
+  uint8_t* stv = stk + (size_t)per * kTierRowK;
+  const int m = u1 - u0;
+  for (int i = threadIdx.x; i < m * 32; i += kThreads) {
+    const int t = i >> 5, c = i & 31, key = c < 16, ch = c & 15;
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(src_row(u0 + t, key)) + 16 * ch;
+    uint8_t* dst = key ? stk + t * kTierRowK + 16 * ch : stv + t * kTierRowV + 16 * ch;
+    cp_async16(dst, src);
+  }
+  cp_async_commit();
+  float* sq = sm + S::sq;
+  load_q<G>(a, b, g, sq, G);
+  cp_async_wait<0>();
+  __syncthreads();
   auto rows = [&](int u, const uint16_t*& kr, const uint16_t*& vr) -> bool {
-    if (u < ns) {
-      kr = sk + (size_t)u * 128;
-      vr = sv + (size_t)u * 128;
-    } else {
-      int idx = rs + (u - ns);
-      idx -= (idx >= cap) ? cap : 0;
-      kr = rk + (size_t)idx * 128;
-      vr = rv + (size_t)idx * 128;
-    }
+    kr = reinterpret_cast<const uint16_t*>(stk + (u - u0) * kTierRowK);
+    vr = reinterpret_cast<const uint16_t*>(stv + (u - u0) * kTierRowV);
     return true;
   };
-  // this tier CTA's share of the sink + recent tokens
-  const int n = ns + nr, per = (n + a.n_tier - 1) / a.n_tier;
-  const int u0 = ti * per, u1 = min(n, u0 + per);
   WarpAcc<G> st;
   st.init();
-  bf16_rows_attend<G>(sq, sm + S::sp + warp * 32 * G, u0 + 32 * warp, u1, 32 * kWarps, rows,
-                      a.scale_log2, st);
+  bf16_rows_attend<G, true>(sq, sm + S::scratch + warp * 32 * G, u0 + 32 * warp, u1, 32 * kWarps,
+                            rows, a.scale_log2, st);
+  __syncthreads();   // staged rows are dead before the results reuse the region
   warp_acc_to_smem<G>(st, sm + S::swo, sm + S::swm, sm + S::swl);
   __syncthreads();
   merge_warps<G>(sm + S::swo, sm + S::swm, sm + S::swl, sm + S::sqr, sm + S::smm, sm + S::sml);
@@ -803,8 +892,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(DecodeArgs a) 
     };
     WarpAcc<G> st;
     st.init();
-    bf16_rows_attend<G>(sq, sm + S::sp + warp * 32 * G, u0 + 32 * warp, u1, 32 * kWarps, rows,
-                        a.scale_log2, st);
+    bf16_rows_attend<G, false>(sq, sm + S::sp + warp * 32 * G, u0 + 32 * warp, u1, 32 * kWarps,
+                               rows, a.scale_log2, st);
     warp_acc_to_smem<G>(st, sm + S::swo, sm + S::swm, sm + S::swl);
     __syncthreads();
     merge_warps<G>(sm + S::swo, sm + S::swm, sm + S::swl, sm + S::sqr, sm + S::smm, sm + S::sml);
@@ -972,7 +1061,7 @@ static DecodePlan make_plan(const Pool& p, int B, int units, int max_per, int n_
 
 DecodePlan plan_decode_int2(const Pool& p, int B, int max_hist_len) {
   const int tiles = (max(max_hist_len, 0) + kTile - 1) / kTile;
-  const int n_tier = max(1, (p.cfg.sink_tokens + p.cfg.recent_tokens + 255) / 256);
+  const int n_tier = max(1, (p.cfg.sink_tokens + p.cfg.recent_tokens + kTierTokens - 1) / kTierTokens);
   return make_plan(p, B, tiles, 512, n_tier, int2_occupancy(p));
 }
 
@@ -990,6 +1079,7 @@ cudaError_t launch_decode_int2(const Pool& p, int layer, int B, const void* q,
   a.page_bytes = p.page_bytes;
   a.tile_bytes = (int)p.tile_bytes;
   a.tiles_per_page = p.cfg.page_size / kTile;
+  a.tpp_shift = (a.tiles_per_page == 2) ? 1 : 0;
   a.sink_k = p.sink_k + (size_t)layer * p.sink_layer_stride;
   a.sink_v = p.sink_v + (size_t)layer * p.sink_layer_stride;
   a.rec_k = p.rec_k + (size_t)layer * p.rec_layer_stride;
@@ -998,6 +1088,7 @@ cudaError_t launch_decode_int2(const Pool& p, int layer, int B, const void* q,
   a.rec_cap = p.cfg.recent_tokens;
   a.Rk = p.Rk + (size_t)layer * p.cfg.num_kv_heads * 128 * 128;
   a.RvT = p.RvT + (size_t)layer * p.cfg.num_kv_heads * 128 * 128;
+  a.rfrag = p.rfrag + (size_t)layer * p.cfg.num_kv_heads * kFragBlocks * rfrag_per_head();
   a.sink_len = sink_len;
   a.hist_len = hist_len;
   a.rec_len = rec_len;

@@ -37,12 +37,18 @@ struct Pool {
   float* Rk = nullptr;              // [layer][Hkv][128][128]  x' = x Rk
   float* RvT = nullptr;             // [layer][Hkv][128][128]  RvT[i][c] = Rv[c][i]
   float* clip = nullptr;            // [layer][2][Hkv][128]
-  uint4* rfrag = nullptr;           // [layer][Hkv][2][4096] bf16 hi/lo MMA fragments
+  uint4* rfrag = nullptr;           // [layer][Hkv][kFragBlocks][4096] bf16 hi/lo MMA fragments
   unsigned* tickets = nullptr;      // [layer][max_seqs][Hkv] split-merge counters
   int* err = nullptr;               // device error word
 };
 
-inline size_t rfrag_per_head() { return 4096; }   // uint4 per (head, tensor)
+// Rotation fragments per (layer, KV head), 4096 uint4 each (bf16 hi/lo pairs):
+//   block 0: B operand of x . R_k        (append K, decode q' = q R_k)
+//   block 1: A operand of R_v^T . x^T    (append V)
+//   block 2: B operand of y . R_v^T      (decode back-rotation of the values)
+//   block 3, 4: third bf16 term (x - hi - lo) of blocks 0 and 2, in .x/.y
+constexpr int kFragBlocks = 5;
+inline size_t rfrag_per_head() { return 4096; }   // uint4 per (head, block)
 
 // ---- launchers (return cudaSuccess or the launch error) --------------------
 cudaError_t launch_rotation_prep(const Pool& p, int layer, const float* Rk, const float* Rv,
