@@ -358,24 +358,21 @@ __global__ void rotation_frag_kernel(const float* __restrict__ Rk, const float* 
   const int r = lane >> 2, j = lane & 3;
   uint4 out;
   if (tensor != 1) {
-    // B operand of x M: element (kappa, n) = M[in_ch(s, kappa)][8 nt + n], with
-    // M = R_k (blocks 0, 3) or M = R_v^T, M[i][c] = R_v[c][i] (blocks 2, 4);
-    // blocks 3 and 4 hold the third bf16 term of the same elements
+    // B operand of x R_k: element (kappa, n) = R_k[in_ch(s, kappa)][8 nt + n];
+    // block 0 as bf16 hi/lo (append, x in bf16), block 2 as fp16 hi/lo (decode q')
     const int nt = (f >> 5) & 15, s = f >> 9;
     const int col = 8 * nt + r;
     uint16_t hi[4], lo[4];
     const int ks[4] = {2 * j, 2 * j + 1, 2 * j + 8, 2 * j + 9};
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int i = in_ch(s, ks[u]);
-      const float m = (tensor == 0 || tensor == 3) ? Rk[(size_t)h * 16384 + i * 128 + col]
-                                                   : Rv[(size_t)h * 16384 + col * 128 + i];
-      split_bf16(m, hi[u], lo[u]);
-      if (tensor >= 3) {   // third term: bf16(m - hi - lo)
-        const float rest = (m - __bfloat162float(__ushort_as_bfloat16(hi[u]))) -
-                           __bfloat162float(__ushort_as_bfloat16(lo[u]));
-        hi[u] = __bfloat16_as_ushort(__float2bfloat16_rn(rest));
-        lo[u] = 0;
+      const float m = Rk[(size_t)h * 16384 + in_ch(s, ks[u]) * 128 + col];
+      if (tensor == 0) {
+        split_bf16(m, hi[u], lo[u]);
+      } else {
+        const __half hh = __float2half_rn(m);
+        hi[u] = __half_as_ushort(hh);
+        lo[u] = __half_as_ushort(__float2half_rn(m - __half2float(hh)));
       }
     }
     out = make_uint4(pack2(hi[0], hi[1]), pack2(hi[2], hi[3]), pack2(lo[0], lo[1]), pack2(lo[2], lo[3]));

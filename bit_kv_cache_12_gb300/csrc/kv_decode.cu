@@ -7,25 +7,30 @@
 // OSCAR write-up, "1. 三段式 Token 池": 64 sink + INT2 history + 256 recent).
 //
 // GPU design (one launch per decode step):
-//   grid = (history splits + tier CTAs, KV heads, sequences), 8 warps per CTA.
-//   * history CTAs: q' = q R_k for the CTA's GQA group, then each warp streams
-//     16-token tiles from HBM through a 4-stage shared-memory ring filled by
-//     16-byte cp.async copies (each lane copies and later reads only its own
-//     bytes, so no barrier is needed; the CTA's page ids are staged in shared
-//     memory first and the q' prologue overlaps the first copies), unpacks
-//     the 2-bit codes into fp16 MMA fragments with one lop3 + one fma per
-//     code pair, and runs QK and PV on the tensor cores (mma.sync m16n8k16).
-//     Dequantization is folded algebraically:
+//   grid = (history splits + tier CTAs, KV heads, sequences); 16 warps per
+//   CTA and one CTA per SM for GQA <= 4 (8 warps for GQA 8), and the split
+//   count fills one wave when the batch is small.
+//   * history CTAs: one round of loads (page ids of the split, q, length),
+//     then each warp streams 16-token tiles from HBM through a 4-stage
+//     shared-memory ring filled by 16-byte cp.async copies (each lane copies
+//     and later reads only its own bytes, so no barrier is needed) while
+//     q' = q R_k runs on the tensor cores; the 2-bit codes are unpacked into
+//     fp16 MMA fragments with one lop3 + one fma per code pair, and QK and PV
+//     run on the tensor cores (mma.sync m16n8k16).  Dequantization is folded:
 //       q'.deq(k) = s_k (q'.(c_k - 1)) + (z_k + s_k) sum(q')
 //       sum_t w_t deq(v_t) = sum_t (w_t s_v)(c_v - 1) + sum_t w_t (z_v + s_v)
 //     so the MMA operands are small exact integers and the query / softmax
 //     weights enter as fp16 hi + lo pairs (about 22 significant bits).
-//     Online softmax per head with warp-shuffle max; per-CTA merge in shared
-//     memory; the CTA's value accumulator is rotated back by R_v^T.
-//   * tier CTAs: the <= 320 BF16 sink + recent tokens in SIMT fp32.
+//     Online softmax per head with warp-shuffle max and a lazily moved
+//     exponent reference; per-CTA merge in shared memory; the partial stays
+//     in the rotated basis.
+//   * tier CTAs: stage their slice of the BF16 sink + recent storage into
+//     shared memory in the same first round (valid rows are picked once the
+//     lengths arrive; softmax order does not matter) and attend in SIMT fp32.
 //   * the last CTA of each (sequence, KV head), found by an atomic ticket (no
-//     waiting), merges all partials with the log-sum-exp rule and writes the
-//     fp32 output.
+//     waiting), merges all partials with the log-sum-exp rule, rotates the
+//     history sum back by R_v^T once (fp32, R_v^T staged in shared memory in
+//     the same round as the partials' loads) and writes the fp32 output.
 #include <math.h>
 
 #include <atomic>
@@ -37,19 +42,22 @@ namespace kvint2 {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = 8;
-constexpr int kPart = 132;   // floats per (split, head) partial: m, l, -, -, o[128]
+constexpr int kPart = 132;       // floats per (part, head) partial: m, l, -, -, o[128]
 constexpr float kNegInf = -INFINITY;
 constexpr int kStages = 4;       // tiles in each warp's ring
-constexpr int kMaxPids = 520;    // page ids staged per CTA (splits cover <= 512 tiles / 8192 tokens)
 constexpr int kMaxParts = 400;   // partials per (sequence, KV head) the final merge reads
+constexpr int kMaxPids = 1032;   // page ids staged per CTA (a split covers <= 1024 tiles)
+constexpr int kTierRows = 320;   // sink + recent storage rows staged per tier CTA
+constexpr int kTierRowK = 272;   // staged K row stride (bytes): 256 + 16 keeps lane reads conflict-free
+constexpr int kTierRowV = 256;
 // The history loop keeps each head's exponent reference kSlack (log2 units)
 // above the largest score seen when it was last moved, so weights stay <= 1
 // and the accumulators are rescaled only when a score passes the reference.
 constexpr float kSlack = 4.0f;
-// Sink + recent tokens per tier CTA (staged in the 48 KB "big" region).
-constexpr int kTierTokens = 80;
+constexpr int kBf16Warps = 8;
+
+__host__ __device__ constexpr int int2_warps(int G) { return G <= 4 ? 16 : 8; }
+__host__ __device__ constexpr int pad4(int n) { return (n + 3) / 4 * 4; }
 
 struct DecodeArgs {
   const uint8_t* hist;      // INT2 layer base
@@ -64,8 +72,7 @@ struct DecodeArgs {
   const uint16_t* rec_k;
   const uint16_t* rec_v;
   int sink_cap, rec_cap;
-  const float* Rk;          // layer base [Hkv][128][128]
-  const float* RvT;
+  const float* RvT;         // layer base [Hkv][128][128], RvT[i][c] = R_v[c][i]
   const uint4* rfrag;       // layer base [Hkv][kFragBlocks][4096] rotation MMA fragments
   const uint16_t* q;
   const int32_t* sink_len;
@@ -85,89 +92,103 @@ struct DecodeArgs {
   int* err;
 };
 
+// Shared-memory carve-up (in floats) for a CTA of NW warps.  A fixed head
+// (q, q', page ids, merged m/l) is followed by one region reused by phase:
+// the history warps' cp.async rings, or a tier CTA's staged rows and softmax
+// weights, then the per-warp results; the final merge reuses everything.
+template <int G, int GS, int NW, bool kInt2>
+struct Lay {
+  static constexpr int HP = (G <= 4) ? 4 : 4 * ((G + 3) / 4);   // padded heads (MMA columns)
+  static constexpr int LB = (GS == 128) ? 48 : 64;               // ring bytes per lane per stage
+  static constexpr int sq = 0;                                    // [HP][128]
+  static constexpr int sqr = sq + HP * 128;                       // [HP][128]
+  static constexpr int ssum = sqr + HP * 128;                     // [HP][2]
+  static constexpr int smm = ssum + pad4(2 * HP);                 // [G] merged m
+  static constexpr int sml = smm + pad4(G);                       // [G] merged l
+  static constexpr int spid = sml + pad4(G);                      // [kMaxPids] int
+  static constexpr int big = spid + kMaxPids;
+  static constexpr int ring_f = kInt2 ? NW * kStages * 32 * LB / 4 : 0;
+  static constexpr int res_f = NW * G * 128 + 2 * pad4(NW * G);
+  static constexpr int sp_f = NW * 32 * G;
+  static constexpr int stage_f = kInt2 ? kTierRows * (kTierRowK + kTierRowV) / 4 : 0;
+  static constexpr int swo = big;                                 // [NW][G][128]
+  static constexpr int swm = swo + NW * G * 128;                  // [NW][G]
+  static constexpr int swl = swm + pad4(NW * G);                  // [NW][G]
+  static constexpr int ring = big;
+  static constexpr int stage = big;                               // tier rows
+  static constexpr int sp = big + (stage_f > res_f ? stage_f : res_f);   // [NW][32][G]
+  static constexpr int merge_f = (kInt2 ? 16384 : 0) + 16 + 2 * NW * 128 + G * 128 + 2 * kMaxParts * G;
+  static constexpr int phase_end = (big + ring_f > sp + sp_f) ? big + ring_f : sp + sp_f;
+  static constexpr int total = (phase_end > merge_f) ? phase_end : merge_f;
+};
+
 // ---------------------------------------------------------------------------
 // shared helpers
 // ---------------------------------------------------------------------------
 
-// Y[h][c] = sum_i X[h][i] M[i][c] for the first NROWS rows of X (shared,
-// [*][128] fp32), on the tensor cores.  M comes as three bf16 terms
-// (hi + lo from fragment block `b`, the third term from block `b3`), X rows
-// are split into bf16 terms too (three when SPLIT, else X must be exact in
-// bf16); the products above 2^-24 relative are kept, fp32 accumulate.  Warp w
-// produces columns 16w..16w+15; each lane loads its fragments at once.
-template <int NROWS, bool SPLIT>
-__device__ void rot_mma(const float* X, const uint4* __restrict__ frag,
-                        const uint4* __restrict__ frag3, float* Y) {
+// q'[h][c] = sum_i q[h][i] R_k[i][c] for the first NROWS rows of X (shared,
+// [*][128] fp32 holding bf16 values), on the tensor cores: R_k comes as fp16
+// hi + lo B fragments (rotation fragment block 2), q is scaled by 2^-8 (exact)
+// and split into fp16 hi + lo, and the three products above 2^-22 relative are
+// accumulated in fp32.  Warp w of NW produces columns (128/NW)w ..; each lane
+// loads its fragments at once (one memory latency).  Ends with a barrier.
+template <int NROWS, int NW>
+__device__ void rotate_q(const float* X, const uint4* __restrict__ frag, float* Y) {
   static_assert(NROWS <= 8, "rows");
+  constexpr int NTW = 16 / NW;   // 8-column n-tiles per warp
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = lane >> 2, j = lane & 3;
-  uint4 f[8][2];
-  uint2 f3[8][2];
+  uint4 f[8][NTW];
 #pragma unroll
   for (int s = 0; s < 8; ++s)
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int idx = (s * 16 + 2 * warp + u) * 32 + lane;
-      f[s][u] = __ldg(frag + idx);
-      const uint4 t = __ldg(frag3 + idx);
-      f3[s][u] = make_uint2(t.x, t.y);
-    }
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    for (int u = 0; u < NTW; ++u) f[s][u] = __ldg(frag + (s * 16 + NTW * warp + u) * 32 + lane);
+  float acc[NTW][4];
+#pragma unroll
+  for (int u = 0; u < NTW; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
   const bool row_ok = r < NROWS;
-  auto bf2 = [](float a, float b) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<const uint32_t*>(&h);
-  };
-  auto lo2 = [](uint32_t u) { return __uint_as_float(u << 16); };
-  auto hi2 = [](uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); };
+  constexpr float kIn = 1.0f / 256.0f;
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
     // A: row r, k index kappa -> input channel 32*(kappa%8/2) + 4s + 2*(kappa/8) + kappa%2
-    const float4 x = row_ok ? *reinterpret_cast<const float4*>(X + r * 128 + 32 * j + 4 * s)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-    const uint32_t a0 = bf2(x.x, x.y), a2 = bf2(x.z, x.w);
+    float4 x = row_ok ? *reinterpret_cast<const float4*>(X + r * 128 + 32 * j + 4 * s)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    x.x *= kIn; x.y *= kIn; x.z *= kIn; x.w *= kIn;
+    const __half2 h01 = __floats2half2_rn(x.x, x.y), h23 = __floats2half2_rn(x.z, x.w);
+    const __half2 l01 = __floats2half2_rn(x.x - __low2float(h01), x.y - __high2float(h01));
+    const __half2 l23 = __floats2half2_rn(x.z - __low2float(h23), x.w - __high2float(h23));
+    const uint32_t a0 = h2_as_u32(h01), a2 = h2_as_u32(h23);
+    const uint32_t b0 = h2_as_u32(l01), b2 = h2_as_u32(l23);
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      mma_bf16(acc[u], a0, 0u, a2, 0u, f[s][u].x, f[s][u].y);      // hi * hi
-      mma_bf16(acc[u], a0, 0u, a2, 0u, f[s][u].z, f[s][u].w);      // hi * lo
-      mma_bf16(acc[u], a0, 0u, a2, 0u, f3[s][u].x, f3[s][u].y);    // hi * lo2
-    }
-    if (SPLIT) {
-      const float r0 = x.x - lo2(a0), r1 = x.y - hi2(a0), r2 = x.z - lo2(a2), r3 = x.w - hi2(a2);
-      const uint32_t b0 = bf2(r0, r1), b2 = bf2(r2, r3);
-      const uint32_t c0 = bf2(r0 - lo2(b0), r1 - hi2(b0)), c2 = bf2(r2 - lo2(b2), r3 - hi2(b2));
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        mma_bf16(acc[u], b0, 0u, b2, 0u, f[s][u].x, f[s][u].y);    // lo * hi
-        mma_bf16(acc[u], b0, 0u, b2, 0u, f[s][u].z, f[s][u].w);    // lo * lo
-        mma_bf16(acc[u], c0, 0u, c2, 0u, f[s][u].x, f[s][u].y);    // lo2 * hi
-      }
+    for (int u = 0; u < NTW; ++u) {
+      mma_f16(acc[u], a0, 0u, a2, 0u, f[s][u].x, f[s][u].y);   // hi * hi
+      mma_f16(acc[u], a0, 0u, a2, 0u, f[s][u].z, f[s][u].w);   // hi * lo
+      mma_f16(acc[u], b0, 0u, b2, 0u, f[s][u].x, f[s][u].y);   // lo * hi
     }
   }
-  __syncthreads();   // everyone has read X
   if (row_ok) {
 #pragma unroll
-    for (int u = 0; u < 2; ++u)
-      *reinterpret_cast<float2*>(Y + r * 128 + 16 * warp + 8 * u + 2 * j) =
-          make_float2(acc[u][0], acc[u][1]);
+    for (int u = 0; u < NTW; ++u)
+      *reinterpret_cast<float2*>(Y + r * 128 + 8 * (NTW * warp + u) + 2 * j) =
+          make_float2(acc[u][0] * 256.0f, acc[u][1] * 256.0f);
   }
   __syncthreads();
 }
 
-// Merge the 8 warps' (m, l, o) in shared memory into one partial per head.
+// Merge the NW warps' (m, l, o) in shared memory into one partial per head.
 // merged[h][c] receives o; sm_m / sm_l receive m and l.
-template <int G>
+template <int G, int NW>
 __device__ void merge_warps(const float* swo, const float* swm, const float* swl, float* merged,
                             float* sm_m, float* sm_l) {
-  for (int idx = threadIdx.x; idx < G * 128; idx += kThreads) {
+  for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
     const int h = idx >> 7;
     float M = kNegInf;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, swm[w * G + h]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, swm[w * G + h]);
     float L = 0.f, O = 0.f;
     if (M != kNegInf) {
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
+      for (int w = 0; w < NW; ++w) {
         const float mw = swm[w * G + h];
         const float f = (mw == kNegInf) ? 0.f : exp2f(mw - M);
         L = fmaf(f, swl[w * G + h], L);
@@ -183,9 +204,9 @@ __device__ void merge_warps(const float* swo, const float* swm, const float* swl
   __syncthreads();
 }
 
-template <int G>
+template <int G, int NW>
 __device__ void write_partial(float* part, const float* o, const float* sm_m, const float* sm_l) {
-  for (int idx = threadIdx.x; idx < G * 128; idx += kThreads) {
+  for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
     const int h = idx >> 7, c = idx & 127;
     part[h * kPart + 4 + c] = o[idx];
     if (c == 0) {
@@ -195,9 +216,9 @@ __device__ void write_partial(float* part, const float* o, const float* sm_m, co
   }
 }
 
-template <int G>
+template <int G, int NW>
 __device__ void write_empty_partial(float* part) {
-  for (int idx = threadIdx.x; idx < G * 128; idx += kThreads) {
+  for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
     const int h = idx >> 7, c = idx & 127;
     part[h * kPart + 4 + c] = 0.f;
     if (c == 0) {
@@ -220,21 +241,41 @@ __device__ bool last_to_arrive(unsigned* ticket, unsigned total) {
 }
 
 // Log-sum-exp merge of all parts of (b, g) and the final normalisation.
-// m and l of every part are staged in shared memory first; the value vectors
-// are then read as float4 with the parts split over the spare threads.
-// `sm` needs 16 + 1024 + 2 * nparts * G floats.
-template <int G>
-__device__ void final_combine(const DecodeArgs& a, int b, int g, int nparts, float* sm) {
-  constexpr int NSUB = kWarps / G;                 // part subsets per output column quad
+// Parts [0, n_rot) hold value sums in the rotated basis (INT2 history); their
+// merged sum is rotated back by R_v^T once here, then the unrotated parts
+// (BF16 tiers) are added.  One round of loads: R_v^T goes to shared memory by
+// cp.async while every part's m, l and value vector are fetched.
+template <int G, int NW, bool kRot>
+__device__ void final_combine(const DecodeArgs& a, int b, int g, int nparts, int n_rot, float* sm) {
+  constexpr int NSUB = NW / G;       // part subsets per output column quad
+  constexpr int kReg = 8;            // value vectors per thread fetched in the first round
   const float* base = a.ws + (size_t)(b * a.Hkv + g) * nparts * G * kPart;
-  float* sM = sm;                                  // [8]
-  float* sL = sm + 8;                              // [8]
-  float* sacc = sm + 16;                           // [NSUB][G][128]
-  float* sf = sacc + NSUB * G * 128;               // [nparts * G] m, then weights
+  float* sR = sm;                                  // [128][128] R_v^T
+  float* sM = sm + (kRot ? 16384 : 0);             // [8]
+  float* sL = sM + 8;                              // [8]
+  float* sh = sL + 8;                              // [NSUB][G][128] rotated-part sums
+  float* st = sh + NW * 128;                       // [NSUB][G][128] unrotated-part sums
+  float* sO = st + NW * 128;                       // [G][128]
+  float* sf = sO + G * 128;                        // [nparts * G] m, then weights
   float* sl = sf + nparts * G;                     // [nparts * G]
-  for (int i = threadIdx.x; i < nparts * G; i += kThreads) {
+  if (kRot) {
+    const float* R = a.RvT + (size_t)g * 128 * 128;
+    for (int i = threadIdx.x; i < 4096; i += NW * 32) cp_async16(sR + 4 * i, R + 4 * i);
+    cp_async_commit();
+  }
+  for (int i = threadIdx.x; i < nparts * G; i += NW * 32) {
     sf[i] = __ldcg(base + (size_t)i * kPart);
     sl[i] = __ldcg(base + (size_t)i * kPart + 1);
+  }
+  const int cq = threadIdx.x & 31, h = (threadIdx.x >> 5) % G, sub = (threadIdx.x >> 5) / G;
+  auto ovec = [&](int s) {
+    return __ldcg(reinterpret_cast<const float4*>(base + (size_t)(s * G + h) * kPart + 4) + cq);
+  };
+  float4 ov[kReg];
+#pragma unroll
+  for (int u = 0; u < kReg; ++u) {
+    const int s = sub + u * NSUB;
+    ov[u] = (s < nparts) ? ovec(s) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   __syncthreads();
   if (threadIdx.x < G) {
@@ -243,7 +284,7 @@ __device__ void final_combine(const DecodeArgs& a, int b, int g, int nparts, flo
     sM[threadIdx.x] = M;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < nparts * G; i += kThreads) {
+  for (int i = threadIdx.x; i < nparts * G; i += NW * 32) {
     const float m = sf[i], M = sM[i % G];
     sf[i] = (m == kNegInf || M == kNegInf) ? 0.f : exp2f(m - M);
   }
@@ -253,29 +294,54 @@ __device__ void final_combine(const DecodeArgs& a, int b, int g, int nparts, flo
     for (int s = 0; s < nparts; ++s) L = fmaf(sf[s * G + threadIdx.x], sl[s * G + threadIdx.x], L);
     sL[threadIdx.x] = L;
   }
-  {
-    const int cq = threadIdx.x & 31, h = (threadIdx.x >> 5) % G, sub = (threadIdx.x >> 5) / G;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int s = sub; s < nparts; s += NSUB) {
-      const float f = sf[s * G + h];
-      const float4 o =
-          __ldcg(reinterpret_cast<const float4*>(base + (size_t)(s * G + h) * kPart + 4) + cq);
-      acc.x = fmaf(f, o.x, acc.x);
-      acc.y = fmaf(f, o.y, acc.y);
-      acc.z = fmaf(f, o.z, acc.z);
-      acc.w = fmaf(f, o.w, acc.w);
+  float4 ah = make_float4(0.f, 0.f, 0.f, 0.f), at = ah;
+  auto add = [&](int s, const float4& o) {
+    const float f = sf[s * G + h];
+    if (s < n_rot) {
+      ah.x = fmaf(f, o.x, ah.x); ah.y = fmaf(f, o.y, ah.y);
+      ah.z = fmaf(f, o.z, ah.z); ah.w = fmaf(f, o.w, ah.w);
+    } else {
+      at.x = fmaf(f, o.x, at.x); at.y = fmaf(f, o.y, at.y);
+      at.z = fmaf(f, o.z, at.z); at.w = fmaf(f, o.w, at.w);
     }
-    *reinterpret_cast<float4*>(sacc + (sub * G + h) * 128 + 4 * cq) = acc;
+  };
+#pragma unroll
+  for (int u = 0; u < kReg; ++u) {
+    const int s = sub + u * NSUB;
+    if (s < nparts) add(s, ov[u]);
   }
+#pragma unroll 8
+  for (int s = sub + kReg * NSUB; s < nparts; s += NSUB) add(s, ovec(s));
+  *reinterpret_cast<float4*>(sh + (sub * G + h) * 128 + 4 * cq) = ah;
+  *reinterpret_cast<float4*>(st + (sub * G + h) * 128 + 4 * cq) = at;
+  if (kRot) cp_async_wait<0>();
   __syncthreads();
-  for (int idx = threadIdx.x; idx < G * 128; idx += kThreads) {
-    const int h = idx >> 7;
+  if (kRot) {
+    for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
+      float O = 0.f;
+#pragma unroll
+      for (int u = 0; u < NSUB; ++u) O += sh[u * G * 128 + idx];
+      sO[idx] = O;
+    }
+    __syncthreads();
+  }
+  for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
+    const int hh = idx >> 7, c = idx & 127;
     float O = 0.f;
 #pragma unroll
-    for (int u = 0; u < NSUB; ++u) O += sacc[u * G * 128 + idx];
-    const float L = sL[h];
-    a.out[((size_t)b * a.Hq + g * G + h) * 128 + (idx & 127)] = (L > 0.f) ? O / L : 0.f;
+    for (int u = 0; u < NSUB; ++u) O += st[u * G * 128 + idx];
+    if (kRot) {   // o_hist[c] = sum_i o'[i] R_v[c][i] = sum_i o'[i] R_v^T[i][c]
+      const float* o = sO + hh * 128;
+      float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 8
+      for (int i = 0; i < 128; i += 2) {
+        acc0 = fmaf(o[i], sR[i * 128 + c], acc0);
+        acc1 = fmaf(o[i + 1], sR[(i + 1) * 128 + c], acc1);
+      }
+      O += acc0 + acc1;
+    }
+    const float L = sL[hh];
+    a.out[((size_t)b * a.Hq + g * G + hh) * 128 + c] = (L > 0.f) ? O / L : 0.f;
   }
   if (threadIdx.x == 0) a.tickets[b * a.Hkv + g] = 0u;   // ready for the next call
 }
@@ -307,14 +373,14 @@ __device__ __align__(16) uint16_t g_zero_row[128];
 // invalid page id, so every ring slot always holds finite data.
 __device__ __align__(16) uint8_t g_zero_tile[1280];
 
-// rows(u, k, v) sets bf16 row pointers for token u and returns false if the
-// token must be skipped.  All loads of a phase are issued before their use.
 template <bool kShared, class T>
 __device__ __forceinline__ T load_row(const T* p) {
   if (kShared) return *p;   // rows staged in shared memory (generic load)
   return __ldg(p);
 }
 
+// rows(u, k, v) sets bf16 row pointers for token u and returns false if the
+// token must be skipped.  All loads of a phase are issued before their use.
 template <int G, bool kShared, class RowFn>
 __device__ void bf16_rows_attend(const float* sq, float* sp, int u0, int u1, int stride,
                                  const RowFn& rows, float scale_log2, WarpAcc<G>& st) {
@@ -413,50 +479,16 @@ __device__ void warp_acc_to_smem(WarpAcc<G>& st, float* swo, float* swm, float* 
 }
 
 // q of the GQA group (bf16 -> fp32) into shared memory; padded heads are 0.
-// Ends with a barrier.
-template <int G>
+// No barrier.
+template <int G, int NW>
 __device__ void load_q(const DecodeArgs& a, int b, int g, float* sq, int padded_heads) {
-  for (int idx = threadIdx.x; idx < padded_heads * 128; idx += kThreads) {
+  for (int idx = threadIdx.x; idx < padded_heads * 128; idx += NW * 32) {
     const int h = idx >> 7, c = idx & 127;
     float v = 0.f;
     if (h < G) v = __uint_as_float((uint32_t)a.q[((size_t)b * a.Hq + g * G + h) * 128 + c] << 16);
     sq[idx] = v;
   }
-  __syncthreads();
 }
-
-// Shared-memory carve-up (in floats).  Region "big" is reused: the INT2
-// warps' cp.async rings during the history loop, then the per-warp results
-// (swo/swm/swl); the BF16 paths use it for their weight buffers and results.
-template <int G, int GS, bool kRing = true>
-struct Smem {
-  static constexpr int HP = (G <= 4) ? 4 : 4 * ((G + 3) / 4);   // padded heads (MMA columns)
-  static constexpr int LB = (GS == 128) ? 48 : 64;               // ring bytes per lane per stage
-  static constexpr int sq = 0;                                    // [HP][128]
-  static constexpr int sqr = sq + HP * 128;                       // [HP][128]
-  static constexpr int ssum = sqr + HP * 128;                     // [HP][2], padded
-  static constexpr int smm = ssum + ((2 * HP + 3) / 4) * 4;       // [G] merged m
-  static constexpr int sml = smm + ((G + 3) / 4) * 4;             // [G] merged l
-  static constexpr int spid = sml + ((G + 3) / 4) * 4;            // [kMaxPids] int
-  static constexpr int scratch = spid + kMaxPids;                 // [8][HP][128]
-  static constexpr int big = scratch + kWarps * HP * 128;
-  static constexpr int ring_floats = kRing ? kWarps * kStages * 32 * LB / 4 : 0;
-  static constexpr int res_floats = kWarps * G * 128 + 2 * ((kWarps * G + 3) / 4) * 4;
-  static constexpr int sp_floats = kWarps * 32 * G;
-  static constexpr int big_floats = (ring_floats > res_floats + sp_floats) ? ring_floats
-                                                                          : res_floats + sp_floats;
-  // inside "big"
-  static constexpr int swo = big;                                 // [8][G][128]
-  static constexpr int swm = swo + kWarps * G * 128;              // [8][G]
-  static constexpr int swl = swm + ((kWarps * G + 3) / 4) * 4;    // [8][G]
-  static constexpr int sp = swl + ((kWarps * G + 3) / 4) * 4;     // [8][32][G]
-  static constexpr int ring = big;
-  static constexpr int total = big + big_floats;
-  // the final merge runs from `scratch` on
-  static_assert(total - scratch >= 16 + 1024 + 2 * kMaxParts * G, "merge scratch");
-  static_assert(!kRing || big_floats * 4 >= kTierTokens * (272 + 256), "tier staging");
-  static_assert(kWarps * HP * 128 >= kWarps * 32 * G, "tier weights in scratch");
-};
 
 // ---------------------------------------------------------------------------
 // INT2 history split (the hot loop)
@@ -464,37 +496,39 @@ struct Smem {
 template <int G, int GS>
 __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float* sm,
                              float* part) {
-  using S = Smem<G, GS>;
+  constexpr int NW = int2_warps(G);
+  using S = Lay<G, GS, NW, true>;
   constexpr int NT = S::HP / 4;      // MMA n-tiles of 8 columns (4 heads x hi/lo)
   constexpr int NG = 128 / GS;       // quantization groups per row
   constexpr int LB = S::LB;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = lane >> 2, j = lane & 3;
 
-  int h = a.hist_len[b];
+  // ---- one round of loads: page ids of the split's whole range, q, length ----
+  const int tsh = a.tpp_shift, tmask = a.tiles_per_page - 1;
+  const int t_begin = split * a.per_split;
+  const int p_begin = t_begin >> tsh;
+  const int p_all = min(((t_begin + a.per_split - 1) >> tsh) + 1, a.max_pages) - p_begin;
+  int* spid = reinterpret_cast<int*>(sm + S::spid);
+  const int32_t* ptrow = a.pt + (size_t)b * a.max_pages;
+  for (int i = threadIdx.x; i < p_all; i += NW * 32) spid[i] = __ldg(ptrow + p_begin + i);
+  float* sq = sm + S::sq;
+  float* sqr = sm + S::sqr;
+  float* ssum = sm + S::ssum;
+  load_q<G, NW>(a, b, g, sq, S::HP);
+  int h = __ldg(a.hist_len + b);
+  __syncthreads();
   const int cap = a.max_pages * a.page_size;
   if (h < 0 || h > cap) {
     if (threadIdx.x == 0) flag_error(a.err, KV_DEVERR_LENGTH);
     h = max(0, min(h, cap));
   }
   const int ntiles = (h + kTile - 1) / kTile;
-  const int t_begin = split * a.per_split;
   const int t_end = min(ntiles, t_begin + a.per_split);
   if (t_begin >= t_end) {
-    write_empty_partial<G>(part);
+    write_empty_partial<G, NW>(part);
     return;
   }
-
-  // ---- page ids of this CTA's tiles and q -> shared memory (one latency) ----
-  const int tsh = a.tpp_shift, tmask = a.tiles_per_page - 1;
-  const int p_begin = t_begin >> tsh, p_count = ((t_end - 1) >> tsh) + 1 - p_begin;
-  int* spid = reinterpret_cast<int*>(sm + S::spid);
-  const int32_t* ptrow = a.pt + (size_t)b * a.max_pages;
-  for (int i = threadIdx.x; i < p_count; i += kThreads) spid[i] = __ldg(ptrow + p_begin + i);
-  float* sq = sm + S::sq;
-  float* sqr = sm + S::sqr;
-  float* ssum = sm + S::ssum;
-  load_q<G>(a, b, g, sq, S::HP);   // its barrier also publishes spid
 
   // ---- start streaming this warp's first tiles into its ring ----
   uint8_t* ring = reinterpret_cast<uint8_t*>(sm + S::ring) + (size_t)warp * kStages * 32 * LB;
@@ -517,12 +551,11 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
     cp_async_commit();   // empty groups keep the group count uniform
   };
 #pragma unroll
-  for (int st = 0; st < kStages - 1; ++st) issue(t_begin + warp + kWarps * st, st);   // tiles 0..2
+  for (int st = 0; st < kStages - 1; ++st) issue(t_begin + warp + NW * st, st);   // tiles 0..2
 
   // ---- q' = q R_k and its per-group sums (overlaps the first copies) ----
-  rot_mma<S::HP, false>(sq, a.rfrag + ((size_t)g * kFragBlocks + 0) * 4096,
-                        a.rfrag + ((size_t)g * kFragBlocks + 3) * 4096, sqr);
-  for (int hh = warp; hh < S::HP; hh += kWarps) {
+  rotate_q<S::HP, NW>(sq, a.rfrag + ((size_t)g * kFragBlocks + 2) * 4096, sqr);
+  for (int hh = warp; hh < S::HP; hh += NW) {
 #pragma unroll
     for (int grp = 0; grp < NG; ++grp) {
       float v = 0.f;
@@ -572,59 +605,17 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
       for (int u = 0; u < 4; ++u) oacc[i][nt][u] = 0.f;
   }
 
-  // QK of one tile: scores[token][column] on the tensor cores, in two
-  // independent accumulator chains (the two groups for group 64, the even and
-  // odd k-steps for group 128)
-  auto qk_tile = [&](const uint4& kq4, float (&sacc)[2][NT][4]) {
-#pragma unroll
-    for (int ch = 0; ch < 2; ++ch)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int u = 0; u < 4; ++u) sacc[ch][nt][u] = 0.f;
-    const uint32_t kw[4] = {kq4.x, kq4.y, kq4.z, kq4.w};
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      uint32_t fr[8];
-      unpack_word(kw[w], fr);
-#pragma unroll
-      for (int sh = 0; sh < 2; ++sh) {
-        const int s = 2 * w + sh;
-        const int ch = (GS == 64) ? (s >> 2) : (s & 1);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          mma_f16(sacc[ch][nt], fr[4 * sh + 0], fr[4 * sh + 1], fr[4 * sh + 2], fr[4 * sh + 3],
-                  qf[s][nt][0], qf[s][nt][1]);
-      }
-    }
-  };
-  auto read_slot = [&](int k, uint4& kq4, uint4& vq4, uint4& sz0, uint4& sz1) {
-    const uint8_t* src = ring_lane + (k % kStages) * (32 * LB);
-    kq4 = *reinterpret_cast<const uint4*>(src);
-    vq4 = *reinterpret_cast<const uint4*>(src + 16);
-    sz0 = *reinterpret_cast<const uint4*>(src + 32);
-    sz1 = (GS == 64) ? *reinterpret_cast<const uint4*>(src + 48) : make_uint4(0, 0, 0, 0);
-  };
-
-  // Software pipeline over this warp's tiles: iteration k runs the softmax and
-  // PV of tile k while the QK of tile k+1 is in flight, so the two dependent
-  // chains interleave.  Ring: tile k+4 is copied into tile k's slot.
-  issue(t_begin + warp + kWarps * (kStages - 1), kStages - 1);
-  float sacc[2][NT][4];
-  uint4 vcur = make_uint4(0, 0, 0, 0), szc0 = vcur, szc1 = vcur;
-  if (t_begin + warp < t_end) {
-    uint4 kq4;
-    cp_async_wait<kStages - 1>();
-    read_slot(0, kq4, vcur, szc0, szc1);
-    qk_tile(kq4, sacc);
-  }
   int k = 0;
-  for (int t = t_begin + warp; t < t_end; t += kWarps, ++k) {
-    issue(t + kWarps * kStages, k % kStages);
-    cp_async_wait<kStages - 1>();
-    uint4 kn, vn, sn0, sn1;
-    read_slot(k + 1, kn, vn, sn0, sn1);
-
+  for (int t = t_begin + warp; t < t_end; t += NW, ++k) {
+    // tile k+3 goes into the slot read in the previous iteration
+    issue(t + NW * (kStages - 1), (k + kStages - 1) % kStages);
+    cp_async_wait<kStages - 1>();   // tile k landed
+    const uint8_t* src = ring_lane + (k % kStages) * (32 * LB);
+    const uint4 kq4 = *reinterpret_cast<const uint4*>(src);
+    const uint4 vq4 = *reinterpret_cast<const uint4*>(src + 16);
+    const uint4 sz0 = *reinterpret_cast<const uint4*>(src + 32);
+    const uint4 sz1 =
+        (GS == 64) ? *reinterpret_cast<const uint4*>(src + 48) : make_uint4(0, 0, 0, 0);
     const int pid_cur = spid[(t >> tsh) - p_begin];
     const bool page_ok = pid_cur >= 0 && pid_cur < a.num_pages;
     if (!page_ok && lane == 0) flag_error(a.err, KV_DEVERR_PAGE_ID);
@@ -634,14 +625,14 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
     // scale / zero of tokens r and r+8
     float sk[2][NG], zk[2][NG], sv[2][NG], zv[2][NG];
     if (GS == 128) {
-      const __half2 a0 = u32_as_h2(szc0.x), a1 = u32_as_h2(szc0.y);
-      const __half2 b0 = u32_as_h2(szc0.z), b1 = u32_as_h2(szc0.w);
+      const __half2 a0 = u32_as_h2(sz0.x), a1 = u32_as_h2(sz0.y);
+      const __half2 b0 = u32_as_h2(sz0.z), b1 = u32_as_h2(sz0.w);
       sk[0][0] = __low2float(a0); zk[0][0] = __high2float(a0);
       sv[0][0] = __low2float(a1); zv[0][0] = __high2float(a1);
       sk[1][0] = __low2float(b0); zk[1][0] = __high2float(b0);
       sv[1][0] = __low2float(b1); zv[1][0] = __high2float(b1);
     } else {
-      const uint4 s0 = szc0, s1 = szc1;
+      const uint4 s0 = sz0, s1 = sz1;
       sk[0][0] = __low2float(u32_as_h2(s0.x)); zk[0][0] = __high2float(u32_as_h2(s0.x));
       sk[0][NG - 1] = __low2float(u32_as_h2(s0.y)); zk[0][NG - 1] = __high2float(u32_as_h2(s0.y));
       sv[0][0] = __low2float(u32_as_h2(s0.z)); zv[0][0] = __high2float(u32_as_h2(s0.z));
@@ -652,7 +643,35 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
       sv[1][NG - 1] = __low2float(u32_as_h2(s1.w)); zv[1][NG - 1] = __high2float(u32_as_h2(s1.w));
     }
 
-    // ---- softmax update and PV B fragments of tile k ----
+    // ---- QK: scores[token][column] on the tensor cores ----
+    // two independent accumulator chains: the two groups (group 64) or the
+    // even / odd k-steps (group 128)
+    float sacc[2][NT][4];
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) sacc[ch][nt][u] = 0.f;
+    {
+      const uint32_t kw[4] = {kq4.x, kq4.y, kq4.z, kq4.w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint32_t fr[8];
+        unpack_word(kw[w], fr);
+#pragma unroll
+        for (int sh = 0; sh < 2; ++sh) {
+          const int s = 2 * w + sh;
+          const int ch = (GS == 64) ? (s >> 2) : (s & 1);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            mma_f16(sacc[ch][nt], fr[4 * sh + 0], fr[4 * sh + 1], fr[4 * sh + 2], fr[4 * sh + 3],
+                    qf[s][nt][0], qf[s][nt][1]);
+        }
+      }
+    }
+
+    // ---- softmax update and PV B fragments ----
     uint32_t bpv[NG][NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -704,13 +723,9 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
       }
     }
 
-    // ---- QK of tile k+1 (independent of the PV below) ----
-    float snext[2][NT][4];
-    if (t + kWarps < t_end) qk_tile(kn, snext);
-
-    // ---- PV of tile k: value accumulator [channel][column] ----
+    // ---- PV: value accumulator [channel][column] on the tensor cores ----
     {
-      const uint32_t vw[4] = {vcur.x, vcur.y, vcur.z, vcur.w};
+      const uint32_t vw[4] = {vq4.x, vq4.y, vq4.z, vq4.w};
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         uint32_t fr[8];
@@ -726,15 +741,6 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
         }
       }
     }
-#pragma unroll
-    for (int ch = 0; ch < 2; ++ch)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int u = 0; u < 4; ++u) sacc[ch][nt][u] = snext[ch][nt][u];
-    vcur = vn;
-    szc0 = sn0;
-    szc1 = sn1;
   }
   cp_async_wait<0>();
   __syncthreads();   // every warp is done with its ring before the results reuse it
@@ -765,78 +771,76 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
     }
   }
   __syncthreads();
-  merge_warps<G>(swo, swm, swl, sqr, sm + S::smm, sm + S::sml);   // q' no longer needed
-  // back to the original basis: o = o' R_v^T
-  rot_mma<G, true>(sqr, a.rfrag + ((size_t)g * kFragBlocks + 2) * 4096,
-                   a.rfrag + ((size_t)g * kFragBlocks + 4) * 4096, sq);
-  write_partial<G>(part, sq, sm + S::smm, sm + S::sml);
+  merge_warps<G, NW>(swo, swm, swl, sqr, sm + S::smm, sm + S::sml);   // q' no longer needed
+  // the partial stays in the rotated basis; the final merge rotates back once
+  write_partial<G, NW>(part, sqr, sm + S::smm, sm + S::sml);
 }
 
 // ---------------------------------------------------------------------------
-// BF16 sink + recent tiers of the INT2 pool (tier CTA `ti` of n_tier)
+// BF16 sink + recent tiers of the INT2 pool: tier CTA `ti` stages storage
+// rows [ti*kTierRows, ...) of [sink slots | recent ring] before it knows the
+// lengths, then attends over the rows that hold live tokens.
 // ---------------------------------------------------------------------------
-constexpr int kTierRowK = 272;   // staged K row stride (bytes): 256 + 16 keeps lane reads conflict-free
-constexpr int kTierRowV = 256;
-
 template <int G, int GS>
 __device__ void bf16_tiers(const DecodeArgs& a, int b, int g, int ti, float* sm, float* part) {
-  using S = Smem<G, GS>;
+  constexpr int NW = int2_warps(G);
+  using S = Lay<G, GS, NW, true>;
   const int warp = threadIdx.x >> 5;
-  int ns = a.sink_len[b], nr = a.rec_len[b], rs = a.rec_start[b];
-  if (ns < 0 || ns > a.sink_cap || nr < 0 || nr > a.rec_cap || rs < 0 || rs >= a.rec_cap) {
-    if (threadIdx.x == 0) flag_error(a.err, KV_DEVERR_LENGTH);
-    ns = max(0, min(ns, a.sink_cap));
-    nr = max(0, min(nr, a.rec_cap));
-    rs = max(0, min(rs, a.rec_cap - 1));
-  }
-  // this tier CTA's share of the sink + recent tokens
-  const int n = ns + nr, per = (n + a.n_tier - 1) / a.n_tier;
-  const int u0 = min(n, ti * per), u1 = min(n, u0 + per);
+  const int scap = a.sink_cap, rcap = a.rec_cap;
+  const int r0 = min(scap + rcap, ti * kTierRows), r1 = min(scap + rcap, r0 + kTierRows);
   const size_t seq_head = (size_t)b * a.Hkv + g;
-  const uint16_t* sk = a.sink_k + seq_head * a.sink_cap * 128;
-  const uint16_t* sv = a.sink_v + seq_head * a.sink_cap * 128;
-  const uint16_t* rk = a.rec_k + seq_head * a.rec_cap * 128;
-  const uint16_t* rv = a.rec_v + seq_head * a.rec_cap * 128;
-  const int cap = a.rec_cap;
-  auto src_row = [&](int u, bool key) -> const uint16_t* {
-    if (u < ns) return (key ? sk : sv) + (size_t)u * 128;
-    int idx = rs + (u - ns);
-    idx -= (idx >= cap) ? cap : 0;
-    return (key ? rk : rv) + (size_t)idx * 128;
-  };
-  // stage the K and V rows of [u0, u1) into shared memory with one burst of copies
-  uint8_t* stk = reinterpret_cast<uint8_t*>(sm + S::big);
-  uint8_t* stv = stk + (size_t)per * kTierRowK;
-  const int m = u1 - u0;
-  for (int i = threadIdx.x; i < m * 32; i += kThreads) {
-    const int t = i >> 5, c = i & 31, key = c < 16, ch = c & 15;
-    const uint8_t* src = reinterpret_cast<const uint8_t*>(src_row(u0 + t, key)) + 16 * ch;
+  const uint16_t* sk = a.sink_k + seq_head * scap * 128;
+  const uint16_t* sv = a.sink_v + seq_head * scap * 128;
+  const uint16_t* rk = a.rec_k + seq_head * rcap * 128;
+  const uint16_t* rv = a.rec_v + seq_head * rcap * 128;
+  uint8_t* stk = reinterpret_cast<uint8_t*>(sm + S::stage);
+  uint8_t* stv = stk + (size_t)kTierRows * kTierRowK;
+  for (int i = threadIdx.x; i < (r1 - r0) * 32; i += NW * 32) {
+    const int t = i >> 5, c = i & 31, key = c < 16, ch = c & 15, row = r0 + t;
+    const uint16_t* src = (row < scap) ? (key ? sk : sv) + (size_t)row * 128
+                                       : (key ? rk : rv) + (size_t)(row - scap) * 128;
     uint8_t* dst = key ? stk + t * kTierRowK + 16 * ch : stv + t * kTierRowV + 16 * ch;
-    cp_async16(dst, src);
+    cp_async16(dst, reinterpret_cast<const uint8_t*>(src) + 16 * ch);
   }
   cp_async_commit();
   float* sq = sm + S::sq;
-  load_q<G>(a, b, g, sq, G);
+  load_q<G, NW>(a, b, g, sq, G);
+  int ns = __ldg(a.sink_len + b), nr = __ldg(a.rec_len + b), rs = __ldg(a.rec_start + b);
   cp_async_wait<0>();
   __syncthreads();
+  if (ns < 0 || ns > scap || nr < 0 || nr > rcap || rs < 0 || rs >= rcap) {
+    if (threadIdx.x == 0) flag_error(a.err, KV_DEVERR_LENGTH);
+    ns = max(0, min(ns, scap));
+    nr = max(0, min(nr, rcap));
+    rs = max(0, min(rs, rcap - 1));
+  }
   auto rows = [&](int u, const uint16_t*& kr, const uint16_t*& vr) -> bool {
-    kr = reinterpret_cast<const uint16_t*>(stk + (u - u0) * kTierRowK);
-    vr = reinterpret_cast<const uint16_t*>(stv + (u - u0) * kTierRowV);
-    return true;
+    bool live;
+    if (u < scap) {
+      live = u < ns;
+    } else {
+      int d = (u - scap) - rs;
+      d += (d < 0) ? rcap : 0;
+      live = d < nr;
+    }
+    kr = reinterpret_cast<const uint16_t*>(stk + (u - r0) * kTierRowK);
+    vr = reinterpret_cast<const uint16_t*>(stv + (u - r0) * kTierRowV);
+    return live;
   };
   WarpAcc<G> st;
   st.init();
-  bf16_rows_attend<G, true>(sq, sm + S::scratch + warp * 32 * G, u0 + 32 * warp, u1, 32 * kWarps,
-                            rows, a.scale_log2, st);
+  bf16_rows_attend<G, true>(sq, sm + S::sp + warp * 32 * G, r0 + 32 * warp, r1, 32 * NW, rows,
+                            a.scale_log2, st);
   __syncthreads();   // staged rows are dead before the results reuse the region
   warp_acc_to_smem<G>(st, sm + S::swo, sm + S::swm, sm + S::swl);
   __syncthreads();
-  merge_warps<G>(sm + S::swo, sm + S::swm, sm + S::swl, sm + S::sqr, sm + S::smm, sm + S::sml);
-  write_partial<G>(part, sm + S::sqr, sm + S::smm, sm + S::sml);
+  merge_warps<G, NW>(sm + S::swo, sm + S::swm, sm + S::swl, sm + S::sqr, sm + S::smm, sm + S::sml);
+  write_partial<G, NW>(part, sm + S::sqr, sm + S::smm, sm + S::sml);
 }
 
 template <int G, int GS>
-__global__ void __launch_bounds__(kThreads, (G > 4) ? 1 : 2) decode_int2_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(int2_warps(G) * 32, 1) decode_int2_kernel(DecodeArgs a) {
+  constexpr int NW = int2_warps(G);
   extern __shared__ float4 smem4[];
   float* sm = reinterpret_cast<float*>(smem4);
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -847,15 +851,76 @@ __global__ void __launch_bounds__(kThreads, (G > 4) ? 1 : 2) decode_int2_kernel(
   else
     bf16_tiers<G, GS>(a, b, g, split - a.n_split, sm, part);
   if (last_to_arrive(a.tickets + b * a.Hkv + g, (unsigned)nparts))
-    final_combine<G>(a, b, g, nparts, sm + Smem<G, GS>::scratch);
+    final_combine<G, NW, true>(a, b, g, nparts, a.n_split, sm);
 }
 
 // ---------------------------------------------------------------------------
 // All-BF16 paged decode (the baseline)
 // ---------------------------------------------------------------------------
+// Log-sum-exp merge of the BF16 decode's parts (all in the original basis) and
+// the final normalisation: part weights in shared memory, then every warp
+// accumulates a subset of the parts for one head and the subsets are summed.
+template <int G, int NW>
+__device__ void final_combine_plain(const DecodeArgs& a, int b, int g, int nparts, float* sm) {
+  constexpr int NSUB = NW / G;                     // part subsets per output column quad
+  const float* base = a.ws + (size_t)(b * a.Hkv + g) * nparts * G * kPart;
+  float* sM = sm;                                  // [8]
+  float* sL = sm + 8;                              // [8]
+  float* sacc = sm + 16;                           // [NSUB][G][128]
+  float* sf = sacc + NSUB * G * 128;               // [nparts * G] m, then weights
+  float* sl = sf + nparts * G;                     // [nparts * G]
+  for (int i = threadIdx.x; i < nparts * G; i += NW * 32) {
+    sf[i] = __ldcg(base + (size_t)i * kPart);
+    sl[i] = __ldcg(base + (size_t)i * kPart + 1);
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    float M = kNegInf;
+    for (int s = 0; s < nparts; ++s) M = fmaxf(M, sf[s * G + threadIdx.x]);
+    sM[threadIdx.x] = M;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < nparts * G; i += NW * 32) {
+    const float m = sf[i], M = sM[i % G];
+    sf[i] = (m == kNegInf || M == kNegInf) ? 0.f : exp2f(m - M);
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    float L = 0.f;
+    for (int s = 0; s < nparts; ++s) L = fmaf(sf[s * G + threadIdx.x], sl[s * G + threadIdx.x], L);
+    sL[threadIdx.x] = L;
+  }
+  {
+    const int cq = threadIdx.x & 31, h = (threadIdx.x >> 5) % G, sub = (threadIdx.x >> 5) / G;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int s = sub; s < nparts; s += NSUB) {
+      const float f = sf[s * G + h];
+      const float4 o =
+          __ldcg(reinterpret_cast<const float4*>(base + (size_t)(s * G + h) * kPart + 4) + cq);
+      acc.x = fmaf(f, o.x, acc.x);
+      acc.y = fmaf(f, o.y, acc.y);
+      acc.z = fmaf(f, o.z, acc.z);
+      acc.w = fmaf(f, o.w, acc.w);
+    }
+    *reinterpret_cast<float4*>(sacc + (sub * G + h) * 128 + 4 * cq) = acc;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
+    const int h = idx >> 7;
+    float O = 0.f;
+#pragma unroll
+    for (int u = 0; u < NSUB; ++u) O += sacc[u * G * 128 + idx];
+    const float L = sL[h];
+    a.out[((size_t)b * a.Hq + g * G + h) * 128 + (idx & 127)] = (L > 0.f) ? O / L : 0.f;
+  }
+  if (threadIdx.x == 0) a.tickets[b * a.Hkv + g] = 0u;   // ready for the next call
+}
+
 template <int G>
-__global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(DecodeArgs a) {
-  using S = Smem<G, 128, false>;
+__global__ void __launch_bounds__(kBf16Warps * 32, 2) decode_bf16_kernel(DecodeArgs a) {
+  constexpr int NW = kBf16Warps;
+  using S = Lay<G, 128, NW, false>;
   extern __shared__ float4 smem4[];
   float* sm = reinterpret_cast<float*>(smem4);
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -870,15 +935,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(DecodeArgs a) 
   }
   const int u0 = split * a.per_split, u1 = min(n, u0 + a.per_split);
   if (u0 >= u1) {
-    write_empty_partial<G>(part);
+    write_empty_partial<G, NW>(part);
   } else {
     const int P = a.page_size;
     const int p_begin = u0 / P, p_count = (u1 - 1) / P + 1 - p_begin;
     int* spid = reinterpret_cast<int*>(sm + S::spid);
     const int32_t* ptrow = a.pt + (size_t)b * a.max_pages;
-    for (int i = threadIdx.x; i < p_count; i += kThreads) spid[i] = __ldg(ptrow + p_begin + i);
+    for (int i = threadIdx.x; i < p_count; i += NW * 32) spid[i] = __ldg(ptrow + p_begin + i);
     float* sq = sm + S::sq;
-    load_q<G>(a, b, g, sq, G);   // its barrier also publishes spid
+    load_q<G, NW>(a, b, g, sq, G);
+    __syncthreads();   // publishes q and the page ids
     auto rows = [&](int u, const uint16_t*& kr, const uint16_t*& vr) -> bool {
       const int pid = spid[u / P - p_begin];
       if (pid < 0 || pid >= a.num_pages) {
@@ -892,27 +958,27 @@ __global__ void __launch_bounds__(kThreads, 2) decode_bf16_kernel(DecodeArgs a) 
     };
     WarpAcc<G> st;
     st.init();
-    bf16_rows_attend<G, false>(sq, sm + S::sp + warp * 32 * G, u0 + 32 * warp, u1, 32 * kWarps,
-                               rows, a.scale_log2, st);
+    bf16_rows_attend<G, false>(sq, sm + S::sp + warp * 32 * G, u0 + 32 * warp, u1, 32 * NW, rows,
+                               a.scale_log2, st);
     warp_acc_to_smem<G>(st, sm + S::swo, sm + S::swm, sm + S::swl);
     __syncthreads();
-    merge_warps<G>(sm + S::swo, sm + S::swm, sm + S::swl, sm + S::sqr, sm + S::smm, sm + S::sml);
-    write_partial<G>(part, sm + S::sqr, sm + S::smm, sm + S::sml);
+    merge_warps<G, NW>(sm + S::swo, sm + S::swm, sm + S::swl, sm + S::sqr, sm + S::smm, sm + S::sml);
+    write_partial<G, NW>(part, sm + S::sqr, sm + S::smm, sm + S::sml);
   }
   if (last_to_arrive(a.tickets + b * a.Hkv + g, (unsigned)nparts))
-    final_combine<G>(a, b, g, nparts, sm + S::scratch);
+    final_combine_plain<G, NW>(a, b, g, nparts, sm);
 }
 
 // Sets the dynamic shared-memory limit of a kernel (once) and reports how many
 // of its CTAs fit on one SM (-1 on a CUDA error).
 template <class K>
-int prepare_kernel(K kernel, size_t smem, bool& done, int& per_sm) {
+int prepare_kernel(K kernel, int threads, size_t smem, bool& done, int& per_sm) {
   if (!done) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
       return -1;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess)
       return -1;
     per_sm = n > 0 ? n : 1;
     done = true;
@@ -921,25 +987,34 @@ int prepare_kernel(K kernel, size_t smem, bool& done, int& per_sm) {
 }
 
 template <int G, int GS>
+constexpr size_t int2_smem() {
+  return sizeof(float) * Lay<G, GS, int2_warps(G), true>::total;
+}
+template <int G>
+constexpr size_t bf16_smem() {
+  return sizeof(float) * Lay<G, 128, kBf16Warps, false>::total;
+}
+
+template <int G, int GS>
 int int2_blocks_per_sm() {
   static bool done = false;
   static int per_sm = 1;
-  return prepare_kernel(decode_int2_kernel<G, GS>, sizeof(float) * Smem<G, GS>::total, done, per_sm);
+  return prepare_kernel(decode_int2_kernel<G, GS>, int2_warps(G) * 32, int2_smem<G, GS>(), done,
+                        per_sm);
 }
 
 template <int G>
 int bf16_blocks_per_sm() {
   static bool done = false;
   static int per_sm = 1;
-  return prepare_kernel(decode_bf16_kernel<G>, sizeof(float) * Smem<G, 128, false>::total, done,
-                        per_sm);
+  return prepare_kernel(decode_bf16_kernel<G>, kBf16Warps * 32, bf16_smem<G>(), done, per_sm);
 }
 
 template <int G, int GS>
 cudaError_t launch_int2_t(const DecodeArgs& a, int B, cudaStream_t s) {
   if (int2_blocks_per_sm<G, GS>() < 0) return cudaErrorInvalidConfiguration;
   dim3 grid(a.n_split + a.n_tier, a.Hkv, B);
-  decode_int2_kernel<G, GS><<<grid, kThreads, sizeof(float) * Smem<G, GS>::total, s>>>(a);
+  decode_int2_kernel<G, GS><<<grid, int2_warps(G) * 32, int2_smem<G, GS>(), s>>>(a);
   return cudaGetLastError();
 }
 
@@ -947,7 +1022,7 @@ template <int G>
 cudaError_t launch_bf16_t(const DecodeArgs& a, int B, cudaStream_t s) {
   if (bf16_blocks_per_sm<G>() < 0) return cudaErrorInvalidConfiguration;
   dim3 grid(a.n_split, a.Hkv, B);
-  decode_bf16_kernel<G><<<grid, kThreads, sizeof(float) * Smem<G, 128, false>::total, s>>>(a);
+  decode_bf16_kernel<G><<<grid, kBf16Warps * 32, bf16_smem<G>(), s>>>(a);
   return cudaGetLastError();
 }
 
@@ -1061,8 +1136,8 @@ static DecodePlan make_plan(const Pool& p, int B, int units, int max_per, int n_
 
 DecodePlan plan_decode_int2(const Pool& p, int B, int max_hist_len) {
   const int tiles = (max(max_hist_len, 0) + kTile - 1) / kTile;
-  const int n_tier = max(1, (p.cfg.sink_tokens + p.cfg.recent_tokens + kTierTokens - 1) / kTierTokens);
-  return make_plan(p, B, tiles, 512, n_tier, int2_occupancy(p));
+  const int n_tier = max(1, (p.cfg.sink_tokens + p.cfg.recent_tokens + kTierRows - 1) / kTierRows);
+  return make_plan(p, B, tiles, 64 * int2_warps(p.G), n_tier, int2_occupancy(p));
 }
 
 DecodePlan plan_decode_bf16(const Pool& p, int B, int max_len) {
@@ -1086,7 +1161,6 @@ cudaError_t launch_decode_int2(const Pool& p, int layer, int B, const void* q,
   a.rec_v = p.rec_v + (size_t)layer * p.rec_layer_stride;
   a.sink_cap = p.cfg.sink_tokens;
   a.rec_cap = p.cfg.recent_tokens;
-  a.Rk = p.Rk + (size_t)layer * p.cfg.num_kv_heads * 128 * 128;
   a.RvT = p.RvT + (size_t)layer * p.cfg.num_kv_heads * 128 * 128;
   a.rfrag = p.rfrag + (size_t)layer * p.cfg.num_kv_heads * kFragBlocks * rfrag_per_head();
   a.sink_len = sink_len;

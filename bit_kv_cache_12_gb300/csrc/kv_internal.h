@@ -45,9 +45,8 @@ struct Pool {
 // Rotation fragments per (layer, KV head), 4096 uint4 each (bf16 hi/lo pairs):
 //   block 0: B operand of x . R_k        (append K, decode q' = q R_k)
 //   block 1: A operand of R_v^T . x^T    (append V)
-//   block 2: B operand of y . R_v^T      (decode back-rotation of the values)
-//   block 3, 4: third bf16 term (x - hi - lo) of blocks 0 and 2, in .x/.y
-constexpr int kFragBlocks = 5;
+//   block 2: B operand of q . R_k as fp16 hi/lo pairs (decode q' = q R_k)
+constexpr int kFragBlocks = 3;
 inline size_t rfrag_per_head() { return 4096; }   // uint4 per (head, block)
 
 // ---- launchers (return cudaSuccess or the launch error) --------------------
