@@ -52,6 +52,33 @@ def dist_setup(n):
     return rank, world
 
 
+# DRAM traffic of the decode kernel from an ncu capture (profiles/), valid only
+# while the sources it was taken from are unchanged.
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "decode_int2_traffic.json")
+KERNEL_SOURCES = ["bit_kv_cache_12_gb300/csrc/kv_decode.cu", "bit_kv_cache_12_gb300/csrc/kv_device.cuh",
+                  "bit_kv_cache_12_gb300/csrc/kv_internal.h"]
+
+
+def kernel_source_digest():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload):
+    """dram read + write bytes per launch, or None if absent or stale."""
+    try:
+        rec = json.load(open(TRAFFIC_RECORD))
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha256") != kernel_source_digest() or rec.get("workload") != workload:
+        return None
+    return int(rec["dram_bytes_read"]) + int(rec["dram_bytes_write"])
+
+
 def algorithmic_bytes(wl):
     """Bytes the method must move per decode step."""
     ng = 128 // wl.group_size
@@ -343,7 +370,7 @@ def main():
             "data": "synthetic (seeded numpy; pool filled by kv_append_quantize)",
             "config": config_of(wl),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None, "peak_source": peak_src,
+                         "frac": achieved / peak, "traffic": measured_traffic(wl.name), "peak_source": peak_src,
                          "algorithmic_bytes": alg, "bytes_breakdown": parts},
             "us_p10_p50_p90": [float(np.percentile(t_int2, p) * 1e3) for p in (10, 50, 90)],
             "bf16_path": {"us": us_bf16, "bytes": bf16_bytes(wl),

@@ -117,7 +117,8 @@ struct Lay {
   static constexpr int ring = big;
   static constexpr int stage = big;                               // tier rows
   static constexpr int sp = big + (stage_f > res_f ? stage_f : res_f);   // [NW][32][G]
-  static constexpr int merge_f = (kInt2 ? 16384 : 0) + 16 + 2 * NW * 128 + G * 128 + 2 * kMaxParts * G;
+  static constexpr int merge_f = (kInt2 ? 16384 + 128 * ((G + 3) & ~3) + NW * G * 128 : 0) + 16 +
+                                 2 * NW * 128 + 2 * kMaxParts * G;
   static constexpr int phase_end = (big + ring_f > sp + sp_f) ? big + ring_f : sp + sp_f;
   static constexpr int total = (phase_end > merge_f) ? phase_end : merge_f;
 };
@@ -244,19 +245,25 @@ __device__ bool last_to_arrive(unsigned* ticket, unsigned total) {
 // Parts [0, n_rot) hold value sums in the rotated basis (INT2 history); their
 // merged sum is rotated back by R_v^T once here, then the unrotated parts
 // (BF16 tiers) are added.  One round of loads: R_v^T goes to shared memory by
-// cp.async while every part's m, l and value vector are fetched.
+// cp.async while every part's m, l and value vector are fetched.  The
+// back-rotation reads each row of R_v^T once for all G heads: warp w takes
+// rows [w*128/NW, (w+1)*128/NW), lane c takes output columns 4c..4c+3, and
+// the NW row-slice partial sums are added at the end.
 template <int G, int NW, bool kRot>
 __device__ void final_combine(const DecodeArgs& a, int b, int g, int nparts, int n_rot, float* sm) {
   constexpr int NSUB = NW / G;       // part subsets per output column quad
   constexpr int kReg = 8;            // value vectors per thread fetched in the first round
+  constexpr int GP = (G + 3) & ~3;   // heads padded to a multiple of 4
+  constexpr int RPW = 128 / NW;      // rows of R_v^T per warp in the back-rotation
   const float* base = a.ws + (size_t)(b * a.Hkv + g) * nparts * G * kPart;
   float* sR = sm;                                  // [128][128] R_v^T
   float* sM = sm + (kRot ? 16384 : 0);             // [8]
   float* sL = sM + 8;                              // [8]
   float* sh = sL + 8;                              // [NSUB][G][128] rotated-part sums
   float* st = sh + NW * 128;                       // [NSUB][G][128] unrotated-part sums
-  float* sO = st + NW * 128;                       // [G][128]
-  float* sf = sO + G * 128;                        // [nparts * G] m, then weights
+  float* sOt = st + NW * 128;                      // [128][GP] merged rotated sum, transposed
+  float* spr = sOt + 128 * GP;                     // [NW][G][128] back-rotation row-slice sums
+  float* sf = spr + (kRot ? NW * G * 128 : 0);     // [nparts * G] m, then weights
   float* sl = sf + nparts * G;                     // [nparts * G]
   if (kRot) {
     const float* R = a.RvT + (size_t)g * 128 * 128;
@@ -317,12 +324,41 @@ __device__ void final_combine(const DecodeArgs& a, int b, int g, int nparts, int
   if (kRot) cp_async_wait<0>();
   __syncthreads();
   if (kRot) {
-    for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
+    for (int idx = threadIdx.x; idx < GP * 128; idx += NW * 32) {
+      const int hh = idx >> 7, i = idx & 127;
       float O = 0.f;
+      if (hh < G) {
 #pragma unroll
-      for (int u = 0; u < NSUB; ++u) O += sh[u * G * 128 + idx];
-      sO[idx] = O;
+        for (int u = 0; u < NSUB; ++u) O += sh[u * G * 128 + idx];
+      }
+      sOt[i * GP + hh] = O;
     }
+    __syncthreads();
+    // o_hist[h][c] = sum_i o'[h][i] R_v[c][i] = sum_i o'[h][i] R_v^T[i][c]
+    const int warp = threadIdx.x >> 5;
+    float acc[GP][4];
+#pragma unroll
+    for (int hh = 0; hh < GP; ++hh) acc[hh][0] = acc[hh][1] = acc[hh][2] = acc[hh][3] = 0.f;
+#pragma unroll 4
+    for (int ii = 0; ii < RPW; ++ii) {
+      const int i = warp * RPW + ii;
+      const float4 r = *reinterpret_cast<const float4*>(sR + i * 128 + 4 * cq);
+#pragma unroll
+      for (int hq = 0; hq < GP / 4; ++hq) {
+        const float4 o = *reinterpret_cast<const float4*>(sOt + i * GP + 4 * hq);
+        const float ox[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float* d = acc[4 * hq + e];
+          d[0] = fmaf(ox[e], r.x, d[0]); d[1] = fmaf(ox[e], r.y, d[1]);
+          d[2] = fmaf(ox[e], r.z, d[2]); d[3] = fmaf(ox[e], r.w, d[3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh)
+      *reinterpret_cast<float4*>(spr + (warp * G + hh) * 128 + 4 * cq) =
+          make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
     __syncthreads();
   }
   for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
@@ -330,15 +366,11 @@ __device__ void final_combine(const DecodeArgs& a, int b, int g, int nparts, int
     float O = 0.f;
 #pragma unroll
     for (int u = 0; u < NSUB; ++u) O += st[u * G * 128 + idx];
-    if (kRot) {   // o_hist[c] = sum_i o'[i] R_v[c][i] = sum_i o'[i] R_v^T[i][c]
-      const float* o = sO + hh * 128;
-      float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 8
-      for (int i = 0; i < 128; i += 2) {
-        acc0 = fmaf(o[i], sR[i * 128 + c], acc0);
-        acc1 = fmaf(o[i + 1], sR[(i + 1) * 128 + c], acc1);
-      }
-      O += acc0 + acc1;
+    if (kRot) {
+      float Oh = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) Oh += spr[w * G * 128 + idx];
+      O += Oh;
     }
     const float L = sL[hh];
     a.out[((size_t)b * a.Hq + g * G + hh) * 128 + c] = (L > 0.f) ? O / L : 0.f;
@@ -691,13 +723,15 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
       }
       l0 = v0 ? l0 * a.scale_log2 : kNegInf;
       l1 = v1 ? l1 * a.scale_log2 : kNegInf;
-      float tmax = fmaxf(l0, l1);
-      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
-      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
-      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
-      // m_run is the exponent reference (>= every score seen so far)
-      const bool need = tmax > m_run[nt];
-      if (__any_sync(0xffffffffu, need)) {
+      // m_run is the exponent reference (>= every score seen so far); it only
+      // moves when some score of the warp exceeds its head's reference, so the
+      // per-head maximum is formed only then
+      if (__any_sync(0xffffffffu, fmaxf(l0, l1) > m_run[nt])) {
+        float tmax = fmaxf(l0, l1);
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+        const bool need = tmax > m_run[nt];
         const float mnew = need ? tmax + kSlack : m_run[nt];
         const float alpha = need ? ((m_run[nt] == kNegInf) ? 0.f : exp2_neg(m_run[nt] - mnew)) : 1.f;
         m_run[nt] = mnew;
@@ -846,6 +880,10 @@ __global__ void __launch_bounds__(int2_warps(G) * 32, 1) decode_int2_kernel(Deco
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int nparts = a.n_split + a.n_tier;
   float* part = a.ws + ((size_t)(b * a.Hkv + g) * nparts + split) * G * kPart;
+  if (split == 0) {   // R_v^T of this head into L2 for the final merge
+    const char* R = reinterpret_cast<const char*>(a.RvT + (size_t)g * 128 * 128);
+    for (int i = threadIdx.x; i < 512; i += NW * 32) prefetch_l2(R + 128 * i);
+  }
   if (split < a.n_split)
     int2_history<G, GS>(a, b, g, split, sm, part);
   else
