@@ -42,16 +42,6 @@ def parse():
     return ap.parse_args()
 
 
-def dist_setup(n):
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    if world > 1:
-        import torch.distributed as dist
-        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-        dist.init_process_group("nccl")
-    return rank, world
-
-
 # DRAM traffic of the decode kernel from an ncu capture (profiles/), valid only
 # while the sources it was taken from are unchanged.
 TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "decode_int2_traffic.json")
@@ -210,13 +200,16 @@ def config_of(wl):
 
 def main():
     args = parse()
-    rank, world = dist_setup(args.gpus)
+    from bit_kv_cache_12_gb300 import dist as kvdist
     if args.impl == "reference":
+        rank, world, _ = kvdist.rank_world()
         run_reference(args, rank, world)
         return
+    # one replica of the workload per GPU (sequences are independent; no
+    # collective on the data path), timings reduced by max over ranks
+    rank, world, local = kvdist.init("nccl")
     import torch
     from bit_kv_cache_12_gb300 import native, synth
-    local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
@@ -308,15 +301,13 @@ def main():
         for _ in range(warmup):
             flush(); fn()
         torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
+        kvdist.barrier()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for s0, s1 in ev:
             flush()
             s0.record(stream); fn(); s1.record(stream)
         torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
+        kvdist.barrier()
         return np.array([s0.elapsed_time(s1) for s0, s1 in ev])   # ms
 
     with ClockSampler(local) as clk:
@@ -345,12 +336,7 @@ def main():
 
     us = float(np.mean(t_int2) * 1e3)
     us_bf16 = float(np.mean(t_bf16) * 1e3)
-    if world > 1:
-        tt = torch.tensor([us, us_bf16, float(np.mean(t_e2e) * 1e3)], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        us, us_bf16, us_e2e = [float(x) for x in tt.cpu()]
-    else:
-        us_e2e = float(np.mean(t_e2e) * 1e3)
+    us, us_bf16, us_e2e = kvdist.max_over_ranks([us, us_bf16, float(np.mean(t_e2e) * 1e3)], device=dev)
 
     alg, parts = algorithmic_bytes(wl)
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -384,8 +370,7 @@ def main():
         }
         print(json.dumps(line))
     pool.close(); bpool.close()
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    kvdist.shutdown()
 
 
 if __name__ == "__main__":
