@@ -11,6 +11,8 @@ It is a plain, slow restatement of the method, step by step, in numpy:
   the library stores its history in.
 * ``oracle.attention`` fp64 softmax attention over the three-tier token pool
   (BF16 sink, INT2 history, BF16 recent) and over an all-BF16 paged cache.
+* ``oracle.tiers``     where a newly generated token goes: sink, recent ring,
+  or (when the ring is full) eviction of the oldest recent token into history.
 
 Sources: "OSCAR: Offline Spectral Covariance-Aware Rotation for 2-bit KV Cache
 Quantization" (gist.science explainer), section 2.2 B "Online-Betriebsphase";
@@ -22,4 +24,4 @@ come from the oracle itself (closed forms, brute force, hand-worked fixtures
 under ``tests/golden/``).
 """
 
-from . import kvquant, attention  # noqa: F401
+from . import kvquant, attention, tiers  # noqa: F401
