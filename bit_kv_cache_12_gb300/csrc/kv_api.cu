@@ -242,6 +242,23 @@ kv_status_t kv_append_quantize(kv_pool_t* pool, int32_t layer, int32_t n_seqs, c
                                            static_cast<cudaStream_t>(stream)));
 }
 
+kv_status_t kv_append_step(kv_pool_t* pool, int32_t layer, int32_t B, const void* k_new,
+                           const void* v_new, int32_t* sink_len, int32_t* hist_len,
+                           int32_t* recent_len, int32_t* recent_start, const int32_t* page_table,
+                           int32_t max_pages_per_seq, void* stream) {
+  if (!valid_layer(pool, layer) || B < 0 || max_pages_per_seq <= 0) return KV_ERR_INVALID_ARG;
+  const Pool& p = pool->p;
+  if (p.cfg.kind != KV_POOL_INT2_3TIER || B > p.cfg.max_seqs) return KV_ERR_INVALID_ARG;
+  if (B > 0 && (!k_new || !v_new || !sink_len || !hist_len || !recent_len || !recent_start ||
+                !page_table))
+    return KV_ERR_INVALID_ARG;
+  if (((uintptr_t)k_new & 7) || ((uintptr_t)v_new & 7)) return KV_ERR_INVALID_ARG;
+  return cuda_status(kvint2::launch_append_step(p, layer, B, k_new, v_new, sink_len, hist_len,
+                                                recent_len, recent_start, page_table,
+                                                max_pages_per_seq,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 size_t kv_decode_workspace_bytes(const kv_pool_t* pool, int32_t B, int32_t max_len) {
   if (!pool || B <= 0 || max_len < 0 || B > pool->p.cfg.max_seqs) return 0;
   const Pool& p = pool->p;

@@ -96,14 +96,204 @@ __device__ __forceinline__ void store_words(uint8_t* dst, const uint32_t (&w)[4]
   }
 }
 
+// One 16-token tile of one KV head and one tensor (0 = K, 1 = V): the rows
+// with row_ok(row) are rotated (frag: the tensor's bf16 hi + lo rotation
+// fragments), clipped (clip: the tensor's 128 thresholds), quantized and
+// packed into the stored tile at tb; the bits and records of the other rows
+// are kept unless `full`.  row_ptr(row) points at channel 32 * (lane % 4) of
+// the row's bf16 input.  Each output row depends only on its own input row,
+// so a token gets the same codes however many tokens share its tile.
+template <int GS, class RowOk, class RowPtr>
+__device__ __forceinline__ void append_tile(int tensor, const uint4* frag, const float* clip,
+                                            uint8_t* tb, bool full, const RowOk& row_ok,
+                                            const RowPtr& row_ptr) {
+  const int lane = threadIdx.x & 31;
+  const int r = lane >> 2, j = lane & 3;
+  constexpr int NG = 128 / GS;
+  uint32_t xr[16], xr8[16];
+  load_row64(row_ptr(r), row_ok(r), xr);
+  load_row64(row_ptr(r + 8), row_ok(r + 8), xr8);
+
+  uint32_t word[4] = {0u, 0u, 0u, 0u}, mask[4] = {0u, 0u, 0u, 0u};
+  if (tensor == 0) {
+    // ---- K: D[token][out channel] = x R_k, tokens as MMA rows ----
+    float acc[16][4];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) acc[nt][u] = 0.f;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        const uint4 f = frag[(s * 16 + nt) * 32 + lane];
+        mma_bf16(acc[nt], xr[2 * s], xr8[2 * s], xr[2 * s + 1], xr8[2 * s + 1], f.x, f.y);
+        mma_bf16(acc[nt], xr[2 * s], xr8[2 * s], xr[2 * s + 1], xr8[2 * s + 1], f.z, f.w);
+      }
+    }
+    // clip; per row (token) and group min / max
+    float mn[2][NG], mx[2][NG];
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+      for (int grp = 0; grp < NG; ++grp) { mn[q][grp] = INFINITY; mx[q][grp] = -INFINITY; }
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+      const int grp = (GS == 64) ? (nt >> 3) : 0;
+      const float cl0 = clip[8 * nt + 2 * j], cl1 = clip[8 * nt + 2 * j + 1];
+      acc[nt][0] = clip_to(acc[nt][0], cl0);
+      acc[nt][1] = clip_to(acc[nt][1], cl1);
+      acc[nt][2] = clip_to(acc[nt][2], cl0);
+      acc[nt][3] = clip_to(acc[nt][3], cl1);
+      mn[0][grp] = fminf(mn[0][grp], fminf(acc[nt][0], acc[nt][1]));
+      mx[0][grp] = fmaxf(mx[0][grp], fmaxf(acc[nt][0], acc[nt][1]));
+      mn[1][grp] = fminf(mn[1][grp], fminf(acc[nt][2], acc[nt][3]));
+      mx[1][grp] = fmaxf(mx[1][grp], fmaxf(acc[nt][2], acc[nt][3]));
+    }
+    ScaleZero q[2][NG];
+#pragma unroll
+    for (int qq = 0; qq < 2; ++qq)
+#pragma unroll
+      for (int grp = 0; grp < NG; ++grp) {
+        float a_ = mn[qq][grp], b_ = mx[qq][grp];
+#pragma unroll
+        for (int o = 1; o < 4; o <<= 1) {
+          a_ = fminf(a_, __shfl_xor_sync(0xffffffffu, a_, o));
+          b_ = fmaxf(b_, __shfl_xor_sync(0xffffffffu, b_, o));
+        }
+        q[qq][grp] = scale_zero(a_, b_);
+      }
+    const bool ok0 = row_ok(r), ok1 = row_ok(r + 8);
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+      const int grp = (GS == 64) ? (nt >> 3) : 0;
+      const int w = nt >> 2;
+      const int pi0 = 4 * ((nt >> 1) & 1) + 2 * (nt & 1);   // row r; row r+8 adds 1
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const uint32_t ca = quant_code(acc[nt][e], q[0][grp]);
+        const uint32_t cb = quant_code(acc[nt][2 + e], q[1][grp]);
+        const int bit_a = 16 * e + 2 * pi0, bit_b = 16 * e + 2 * (pi0 + 1);
+        word[w] |= (ca << bit_a) | (cb << bit_b);
+        mask[w] |= (ok0 ? (3u << bit_a) : 0u) | (ok1 ? (3u << bit_b) : 0u);
+      }
+    }
+    store_words(tb + 16 * lane, word, mask, full);
+    if (j == 0) {
+      const int rec = 8 * NG;
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) {
+        if (!(qq ? ok1 : ok0)) continue;
+        const int t = r + 8 * qq;
+        __half2* recp = reinterpret_cast<__half2*>(tb + 1024 + (2 * (t & 7) + (t >> 3)) * rec);
+#pragma unroll
+        for (int grp = 0; grp < NG; ++grp) recp[grp] = __halves2half2(q[qq][grp].sh, q[qq][grp].zh);
+      }
+    }
+  } else {
+    // ---- V: D[out channel][token] = R_v^T x^T, channels as MMA rows ----
+    float acc[8][2][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc[i][nt][u] = 0.f;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 fh = frag[((i * 8 + s) * 2 + 0) * 32 + lane];
+        const uint4 fl = frag[((i * 8 + s) * 2 + 1) * 32 + lane];
+        mma_bf16(acc[i][0], fh.x, fh.y, fh.z, fh.w, xr[2 * s], xr[2 * s + 1]);
+        mma_bf16(acc[i][0], fl.x, fl.y, fl.z, fl.w, xr[2 * s], xr[2 * s + 1]);
+        mma_bf16(acc[i][1], fh.x, fh.y, fh.z, fh.w, xr8[2 * s], xr8[2 * s + 1]);
+        mma_bf16(acc[i][1], fl.x, fl.y, fl.z, fl.w, xr8[2 * s], xr8[2 * s + 1]);
+      }
+    }
+    // lane holds tokens 8*nt + 2j + e for channels 16i + r (+8)
+    float mn[2][2][NG], mx[2][2][NG];   // [nt][e][grp]
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int grp = 0; grp < NG; ++grp) { mn[nt][e][grp] = INFINITY; mx[nt][e][grp] = -INFINITY; }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int grp = (GS == 64) ? (i >> 2) : 0;
+      const float cl0 = clip[16 * i + r], cl1 = clip[16 * i + r + 8];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          acc[i][nt][e] = clip_to(acc[i][nt][e], cl0);
+          acc[i][nt][2 + e] = clip_to(acc[i][nt][2 + e], cl1);
+          mn[nt][e][grp] = fminf(mn[nt][e][grp], fminf(acc[i][nt][e], acc[i][nt][2 + e]));
+          mx[nt][e][grp] = fmaxf(mx[nt][e][grp], fmaxf(acc[i][nt][e], acc[i][nt][2 + e]));
+        }
+    }
+    ScaleZero q[2][2][NG];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int grp = 0; grp < NG; ++grp) {
+          float a_ = mn[nt][e][grp], b_ = mx[nt][e][grp];
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            a_ = fminf(a_, __shfl_xor_sync(0xffffffffu, a_, o));
+            b_ = fmaxf(b_, __shfl_xor_sync(0xffffffffu, b_, o));
+          }
+          q[nt][e][grp] = scale_zero(a_, b_);
+        }
+    bool tok_ok[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) tok_ok[nt][e] = row_ok(8 * nt + 2 * j + e);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int grp = (GS == 64) ? (i >> 2) : 0;
+      const int w = i >> 1;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int pi0 = 4 * (i & 1) + 2 * nt;               // channel 16i+r; +8 adds 1
+          const uint32_t ca = quant_code(acc[i][nt][e], q[nt][e][grp]);
+          const uint32_t cb = quant_code(acc[i][nt][2 + e], q[nt][e][grp]);
+          const int bit_a = 16 * e + 2 * pi0, bit_b = 16 * e + 2 * (pi0 + 1);
+          word[w] |= (ca << bit_a) | (cb << bit_b);
+          if (tok_ok[nt][e]) mask[w] |= (3u << bit_a) | (3u << bit_b);
+        }
+    }
+    store_words(tb + 512 + 16 * lane, word, mask, full);
+    if (r == 0) {
+      const int rec = 8 * NG;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          if (!tok_ok[nt][e]) continue;
+          const int t = 8 * nt + 2 * j + e;
+          __half2* recp =
+              reinterpret_cast<__half2*>(tb + 1024 + (2 * (t & 7) + (t >> 3)) * rec) + NG;
+#pragma unroll
+          for (int grp = 0; grp < NG; ++grp)
+            recp[grp] = __halves2half2(q[nt][e][grp].sh, q[nt][e][grp].zh);
+        }
+    }
+  }
+}
+
 template <int GS>
 __global__ void __launch_bounds__(256, 2) append_kernel(AppendArgs a) {
   extern __shared__ uint4 sfrag[];                 // 4096 fragments, then clip
   float* sclip = reinterpret_cast<float*>(sfrag + 4096);
   const int g = blockIdx.y, tensor = blockIdx.z;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int r = lane >> 2, j = lane & 3;
-  constexpr int NG = 128 / GS;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, j = lane & 3;
 
   const uint4* src = a.rfrag + ((size_t)g * kFragBlocks + tensor) * 4096;
   for (int i = threadIdx.x; i < 4096; i += blockDim.x) sfrag[i] = __ldg(src + i);
@@ -143,181 +333,106 @@ __global__ void __launch_bounds__(256, 2) append_kernel(AppendArgs a) {
       const int tok = c0 + (tile * kTile + row - h0);
       return (tensor == 0 ? a.k : a.v) + ((size_t)tok * a.Hkv + g) * 128 + 32 * j;
     };
-    uint32_t xr[16], xr8[16];
-    load_row64(row_ptr(r), row_ok(r), xr);
-    load_row64(row_ptr(r + 8), row_ok(r + 8), xr8);
+    append_tile<GS>(tensor, sfrag, sclip, tb, full, row_ok, row_ptr);
+  }
+}
 
-    uint32_t word[4] = {0u, 0u, 0u, 0u}, mask[4] = {0u, 0u, 0u, 0u};
-    if (tensor == 0) {
-      // ---- K: D[token][out channel] = x R_k, tokens as MMA rows ----
-      float acc[16][4];
-#pragma unroll
-      for (int nt = 0; nt < 16; ++nt)
-#pragma unroll
-        for (int u = 0; u < 4; ++u) acc[nt][u] = 0.f;
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-          const uint4 f = sfrag[(s * 16 + nt) * 32 + lane];
-          mma_bf16(acc[nt], xr[2 * s], xr8[2 * s], xr[2 * s + 1], xr8[2 * s + 1], f.x, f.y);
-          mma_bf16(acc[nt], xr[2 * s], xr8[2 * s], xr[2 * s + 1], xr8[2 * s + 1], f.z, f.w);
-        }
+// ---------------------------------------------------------------------------
+// per-step token placement (yunpan.plus write-up, "2. 在线量化与反量化": a new
+// token is written to the recent tier; when that is full its oldest token is
+// rotated, clipped, quantized and packed into the INT2 history)
+// one CTA per sequence; warps take (KV head, tensor) pairs
+// ---------------------------------------------------------------------------
+struct StepArgs {
+  uint8_t* hist;                  // layer base
+  size_t page_bytes, head_block;
+  int tile_bytes, P;
+  uint16_t* sink_k;               // layer bases [max_seqs][Hkv][cap][128]
+  uint16_t* sink_v;
+  uint16_t* rec_k;
+  uint16_t* rec_v;
+  int sink_cap, rec_cap;
+  const uint16_t* k_new;          // [B][Hkv][128]
+  const uint16_t* v_new;
+  int32_t* sink_len;
+  int32_t* hist_len;
+  int32_t* rec_len;
+  int32_t* rec_start;
+  const int32_t* pt;
+  int max_pages, Hkv;
+  long long num_pages;
+  const uint4* rfrag;             // layer base [Hkv][kFragBlocks][4096]
+  const float* clip;              // layer base [2][Hkv][128]
+  int* err;
+};
+
+template <int GS>
+__global__ void __launch_bounds__(512, 1) append_step_kernel(StepArgs a) {
+  __shared__ int s_mode, s_slot, s_pos;
+  __shared__ long long s_tile;
+  const int b = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  if (threadIdx.x == 0) {
+    const int sl = a.sink_len[b], hl = a.hist_len[b], rl = a.rec_len[b], rs = a.rec_start[b];
+    int mode = -1, slot = 0, pos = 0;
+    long long tile = 0;
+    if (sl < 0 || sl > a.sink_cap || rl < 0 || rl > a.rec_cap || rs < 0 || rs >= a.rec_cap ||
+        hl < 0) {
+      flag_error(a.err, KV_DEVERR_LENGTH);
+    } else if (sl < a.sink_cap) {                    // one of the sequence's first tokens
+      mode = 0;
+      slot = sl;
+    } else if (rl < a.rec_cap) {                     // the recent ring has room
+      mode = 1;
+      slot = (rs + rl) % a.rec_cap;
+    } else {                                         // evict the ring's oldest token
+      const int pidx = hl / a.P;
+      const int pid = (pidx < a.max_pages) ? a.pt[(size_t)b * a.max_pages + pidx] : -1;
+      if (pidx >= a.max_pages) {
+        flag_error(a.err, KV_DEVERR_LENGTH);
+      } else if (pid < 0 || pid >= a.num_pages) {
+        flag_error(a.err, KV_DEVERR_PAGE_ID);
+      } else {
+        mode = 2;
+        slot = rs;
+        pos = hl % kTile;
+        tile = (long long)pid * (long long)a.page_bytes + (long long)((hl % a.P) / kTile) * a.tile_bytes;
       }
-      // clip; per row (token) and group min / max
-      float mn[2][NG], mx[2][NG];
-#pragma unroll
-      for (int q = 0; q < 2; ++q)
-#pragma unroll
-        for (int grp = 0; grp < NG; ++grp) { mn[q][grp] = INFINITY; mx[q][grp] = -INFINITY; }
-#pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        const int grp = (GS == 64) ? (nt >> 3) : 0;
-        const float cl0 = sclip[8 * nt + 2 * j], cl1 = sclip[8 * nt + 2 * j + 1];
-        acc[nt][0] = clip_to(acc[nt][0], cl0);
-        acc[nt][1] = clip_to(acc[nt][1], cl1);
-        acc[nt][2] = clip_to(acc[nt][2], cl0);
-        acc[nt][3] = clip_to(acc[nt][3], cl1);
-        mn[0][grp] = fminf(mn[0][grp], fminf(acc[nt][0], acc[nt][1]));
-        mx[0][grp] = fmaxf(mx[0][grp], fmaxf(acc[nt][0], acc[nt][1]));
-        mn[1][grp] = fminf(mn[1][grp], fminf(acc[nt][2], acc[nt][3]));
-        mx[1][grp] = fmaxf(mx[1][grp], fmaxf(acc[nt][2], acc[nt][3]));
+    }
+    s_mode = mode; s_slot = slot; s_pos = pos; s_tile = tile;
+  }
+  __syncthreads();
+  const int mode = s_mode, slot = s_slot, pos = s_pos;
+  if (mode >= 0) {
+    for (int pair = warp; pair < 2 * a.Hkv; pair += nwarps) {
+      const int g = pair >> 1, tensor = pair & 1;
+      const size_t sh = (size_t)b * a.Hkv + g;
+      const uint16_t* src = (tensor ? a.v_new : a.k_new) + sh * 128;
+      uint16_t* dst = (mode == 0)
+                          ? (tensor ? a.sink_v : a.sink_k) + (sh * a.sink_cap + slot) * 128
+                          : (tensor ? a.rec_v : a.rec_k) + (sh * a.rec_cap + slot) * 128;
+      if (mode == 2) {
+        // the slot's current token goes to history position pos of its tile
+        uint8_t* tb = a.hist + s_tile + (size_t)g * a.head_block;
+        const uint16_t* old = dst;
+        append_tile<GS>(tensor, a.rfrag + ((size_t)g * kFragBlocks + tensor) * 4096,
+                        a.clip + ((size_t)tensor * a.Hkv + g) * 128, tb, false,
+                        [&](int row) { return row == pos; },
+                        [&](int) { return old + 32 * (lane & 3); });
+        __syncwarp();   // every lane has read the old row before it is overwritten
       }
-      ScaleZero q[2][NG];
-#pragma unroll
-      for (int qq = 0; qq < 2; ++qq)
-#pragma unroll
-        for (int grp = 0; grp < NG; ++grp) {
-          float a_ = mn[qq][grp], b_ = mx[qq][grp];
-#pragma unroll
-          for (int o = 1; o < 4; o <<= 1) {
-            a_ = fminf(a_, __shfl_xor_sync(0xffffffffu, a_, o));
-            b_ = fmaxf(b_, __shfl_xor_sync(0xffffffffu, b_, o));
-          }
-          q[qq][grp] = scale_zero(a_, b_);
-        }
-      const bool ok0 = row_ok(r), ok1 = row_ok(r + 8);
-#pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        const int grp = (GS == 64) ? (nt >> 3) : 0;
-        const int w = nt >> 2;
-        const int pi0 = 4 * ((nt >> 1) & 1) + 2 * (nt & 1);   // row r; row r+8 adds 1
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const uint32_t ca = quant_code(acc[nt][e], q[0][grp]);
-          const uint32_t cb = quant_code(acc[nt][2 + e], q[1][grp]);
-          const int bit_a = 16 * e + 2 * pi0, bit_b = 16 * e + 2 * (pi0 + 1);
-          word[w] |= (ca << bit_a) | (cb << bit_b);
-          mask[w] |= (ok0 ? (3u << bit_a) : 0u) | (ok1 ? (3u << bit_b) : 0u);
-        }
-      }
-      store_words(tb + 16 * lane, word, mask, full);
-      if (j == 0) {
-        const int rec = 8 * NG;
-#pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-          if (!(qq ? ok1 : ok0)) continue;
-          const int t = r + 8 * qq;
-          __half2* recp = reinterpret_cast<__half2*>(tb + 1024 + (2 * (t & 7) + (t >> 3)) * rec);
-#pragma unroll
-          for (int grp = 0; grp < NG; ++grp) recp[grp] = __halves2half2(q[qq][grp].sh, q[qq][grp].zh);
-        }
-      }
-    } else {
-      // ---- V: D[out channel][token] = R_v^T x^T, channels as MMA rows ----
-      float acc[8][2][4];
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int u = 0; u < 4; ++u) acc[i][nt][u] = 0.f;
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 fh = sfrag[((i * 8 + s) * 2 + 0) * 32 + lane];
-          const uint4 fl = sfrag[((i * 8 + s) * 2 + 1) * 32 + lane];
-          mma_bf16(acc[i][0], fh.x, fh.y, fh.z, fh.w, xr[2 * s], xr[2 * s + 1]);
-          mma_bf16(acc[i][0], fl.x, fl.y, fl.z, fl.w, xr[2 * s], xr[2 * s + 1]);
-          mma_bf16(acc[i][1], fh.x, fh.y, fh.z, fh.w, xr8[2 * s], xr8[2 * s + 1]);
-          mma_bf16(acc[i][1], fl.x, fl.y, fl.z, fl.w, xr8[2 * s], xr8[2 * s + 1]);
-        }
-      }
-      // lane holds tokens 8*nt + 2j + e for channels 16i + r (+8)
-      float mn[2][2][NG], mx[2][2][NG];   // [nt][e][grp]
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-#pragma unroll
-          for (int grp = 0; grp < NG; ++grp) { mn[nt][e][grp] = INFINITY; mx[nt][e][grp] = -INFINITY; }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int grp = (GS == 64) ? (i >> 2) : 0;
-        const float cl0 = sclip[16 * i + r], cl1 = sclip[16 * i + r + 8];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            acc[i][nt][e] = clip_to(acc[i][nt][e], cl0);
-            acc[i][nt][2 + e] = clip_to(acc[i][nt][2 + e], cl1);
-            mn[nt][e][grp] = fminf(mn[nt][e][grp], fminf(acc[i][nt][e], acc[i][nt][2 + e]));
-            mx[nt][e][grp] = fmaxf(mx[nt][e][grp], fmaxf(acc[i][nt][e], acc[i][nt][2 + e]));
-          }
-      }
-      ScaleZero q[2][2][NG];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-#pragma unroll
-          for (int grp = 0; grp < NG; ++grp) {
-            float a_ = mn[nt][e][grp], b_ = mx[nt][e][grp];
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-              a_ = fminf(a_, __shfl_xor_sync(0xffffffffu, a_, o));
-              b_ = fmaxf(b_, __shfl_xor_sync(0xffffffffu, b_, o));
-            }
-            q[nt][e][grp] = scale_zero(a_, b_);
-          }
-      bool tok_ok[2][2];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) tok_ok[nt][e] = row_ok(8 * nt + 2 * j + e);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int grp = (GS == 64) ? (i >> 2) : 0;
-        const int w = i >> 1;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int pi0 = 4 * (i & 1) + 2 * nt;               // channel 16i+r; +8 adds 1
-            const uint32_t ca = quant_code(acc[i][nt][e], q[nt][e][grp]);
-            const uint32_t cb = quant_code(acc[i][nt][2 + e], q[nt][e][grp]);
-            const int bit_a = 16 * e + 2 * pi0, bit_b = 16 * e + 2 * (pi0 + 1);
-            word[w] |= (ca << bit_a) | (cb << bit_b);
-            if (tok_ok[nt][e]) mask[w] |= (3u << bit_a) | (3u << bit_b);
-          }
-      }
-      store_words(tb + 512 + 16 * lane, word, mask, full);
-      if (r == 0) {
-        const int rec = 8 * NG;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            if (!tok_ok[nt][e]) continue;
-            const int t = 8 * nt + 2 * j + e;
-            __half2* recp =
-                reinterpret_cast<__half2*>(tb + 1024 + (2 * (t & 7) + (t >> 3)) * rec) + NG;
-#pragma unroll
-            for (int grp = 0; grp < NG; ++grp)
-              recp[grp] = __halves2half2(q[nt][e][grp].sh, q[nt][e][grp].zh);
-          }
-      }
+      *reinterpret_cast<uint2*>(dst + 4 * lane) = *reinterpret_cast<const uint2*>(src + 4 * lane);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (mode == 0) {
+      a.sink_len[b] = slot + 1;
+    } else if (mode == 1) {
+      a.rec_len[b] += 1;
+    } else if (mode == 2) {
+      a.hist_len[b] += 1;
+      a.rec_start[b] = (slot + 1) % a.rec_cap;
     }
   }
 }
@@ -552,6 +667,45 @@ cudaError_t launch_append(const Pool& p, int layer, int n_seqs, const void* k, c
     }
     append_kernel<128><<<grid, 256, smem, s>>>(a);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append_step(const Pool& p, int layer, int B, const void* k_new,
+                               const void* v_new, int32_t* sink_len, int32_t* hist_len,
+                               int32_t* rec_len, int32_t* rec_start, const int32_t* pt,
+                               int max_pages, cudaStream_t s) {
+  if (B == 0) return cudaSuccess;
+  const int H = p.cfg.num_kv_heads;
+  StepArgs a{};
+  a.hist = p.hist + (size_t)layer * p.hist_layer_stride;
+  a.page_bytes = p.page_bytes;
+  a.head_block = p.page_bytes / H;
+  a.tile_bytes = (int)p.tile_bytes;
+  a.P = p.cfg.page_size;
+  a.sink_k = p.sink_k + (size_t)layer * p.sink_layer_stride;
+  a.sink_v = p.sink_v + (size_t)layer * p.sink_layer_stride;
+  a.rec_k = p.rec_k + (size_t)layer * p.rec_layer_stride;
+  a.rec_v = p.rec_v + (size_t)layer * p.rec_layer_stride;
+  a.sink_cap = p.cfg.sink_tokens;
+  a.rec_cap = p.cfg.recent_tokens;
+  a.k_new = static_cast<const uint16_t*>(k_new);
+  a.v_new = static_cast<const uint16_t*>(v_new);
+  a.sink_len = sink_len;
+  a.hist_len = hist_len;
+  a.rec_len = rec_len;
+  a.rec_start = rec_start;
+  a.pt = pt;
+  a.max_pages = max_pages;
+  a.Hkv = H;
+  a.num_pages = p.cfg.num_pages;
+  a.rfrag = p.rfrag + (size_t)layer * H * kFragBlocks * rfrag_per_head();
+  a.clip = p.clip + (size_t)layer * 2 * H * 128;
+  a.err = p.err;
+  const int threads = 32 * min(2 * H, 16);
+  if (p.cfg.group_size == 64)
+    append_step_kernel<64><<<B, threads, 0, s>>>(a);
+  else
+    append_step_kernel<128><<<B, threads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

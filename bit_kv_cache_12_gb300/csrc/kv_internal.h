@@ -60,6 +60,10 @@ cudaError_t launch_quantize_pack(const Pool& p, int layer, int tensor, int64_t n
 cudaError_t launch_append(const Pool& p, int layer, int n_seqs, const void* k, const void* v,
                           const int32_t* cu, const int32_t* hist_start, const int32_t* pt,
                           int max_pages, int max_tokens, cudaStream_t s);
+cudaError_t launch_append_step(const Pool& p, int layer, int B, const void* k_new,
+                               const void* v_new, int32_t* sink_len, int32_t* hist_len,
+                               int32_t* rec_len, int32_t* rec_start, const int32_t* pt,
+                               int max_pages, cudaStream_t s);
 cudaError_t launch_append_bf16(const Pool& p, int layer, int n_seqs, const void* k,
                                const void* v, const int32_t* cu, const int32_t* start,
                                const int32_t* pt, int max_pages, int max_tokens,

@@ -62,6 +62,7 @@ _SIG = {
     "kv_store_tier": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
     "kv_quantize_pack_f32": (_I32, [_P, _I32, _I32, _I64, _P, _P, _P, _P]),
     "kv_append_quantize": (_I32, [_P, _I32, _I32, _P, _P, _P, _P, _P, _I32, _I32, _P]),
+    "kv_append_step": (_I32, [_P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _I32, _P]),
     "kv_decode_workspace_bytes": (ctypes.c_size_t, [_P, _I32, _I32]),
     "kv_decode_attention": (_I32, [_P, _I32, _I32, _P, _P, _P, _P, _P, _P, _I32, _I32,
                                    ctypes.c_float, _P, _P, ctypes.c_size_t, _P]),
@@ -166,6 +167,13 @@ def kv_append_quantize(pool, layer, n_seqs, k, v, cu_tokens, hist_start, page_ta
     _check("kv_append_quantize", lib().kv_append_quantize(
         pool, layer, n_seqs, _ptr(k), _ptr(v), _ptr(cu_tokens), _ptr(hist_start),
         _ptr(page_table), max_pages_per_seq, max_tokens_per_seq, _stream(stream)))
+
+
+def kv_append_step(pool, layer, B, k_new, v_new, sink_len, hist_len, recent_len, recent_start,
+                   page_table, max_pages_per_seq, stream=None):
+    _check("kv_append_step", lib().kv_append_step(
+        pool, layer, B, _ptr(k_new), _ptr(v_new), _ptr(sink_len), _ptr(hist_len), _ptr(recent_len),
+        _ptr(recent_start), _ptr(page_table), max_pages_per_seq, _stream(stream)))
 
 
 def kv_decode_workspace_bytes(pool, B, max_len):

@@ -185,6 +185,32 @@ kv_status_t kv_append_quantize(kv_pool_t* pool, int32_t layer, int32_t n_seqs,
                                int32_t max_pages_per_seq, int32_t max_tokens_per_seq,
                                void* stream);
 
+/* One decode step's token placement for B sequences (yunpan.plus write-up,
+ * "1. 三段式 Token 池" and "2. 在线量化与反量化"): the new token of sequence b
+ * (all KV heads) goes to the sink while it holds fewer than sink_tokens
+ * tokens (the sequence's first tokens), else to the recent ring while that
+ * holds fewer than recent_tokens; when the ring is full its oldest token (at
+ * recent_start) is rotated, clipped, quantized and packed into history
+ * position hist_len[b] (the same arithmetic, and so the same codes, as
+ * kv_append_quantize), the new token takes its ring slot and recent_start
+ * advances.  The four length arrays are updated on the device, in stream
+ * order, so consecutive steps and decodes need no host round trip.
+ *   k_new, v_new  device bf16 [B][Hkv][128] (8-byte aligned); sequence b
+ *                 uses pool slot b
+ *   sink_len, hist_len, recent_len, recent_start
+ *                 device int32 [B], read and updated in place
+ *   page_table    device int32 [B][max_pages_per_seq]: the page of history
+ *                 position p is page_table[b][p / page_size]; the caller
+ *                 provides it before the step that needs it
+ * Errors: KV_ERR_INVALID_ARG for bad arguments (nothing launched).  On the
+ * device, lengths out of range set KV_DEVERR_LENGTH and a missing or
+ * out-of-range page id for the eviction sets KV_DEVERR_PAGE_ID; that
+ * sequence's step is then not applied (no tier or length changes). */
+kv_status_t kv_append_step(kv_pool_t* pool, int32_t layer, int32_t B, const void* k_new,
+                           const void* v_new, int32_t* sink_len, int32_t* hist_len,
+                           int32_t* recent_len, int32_t* recent_start,
+                           const int32_t* page_table, int32_t max_pages_per_seq, void* stream);
+
 /* Bytes of device workspace kv_decode_attention / kv_decode_attention_bf16
  * need for a batch of B sequences whose history (INT2 pool) or total length
  * (BF16 pool) is at most max_len tokens.  0 on invalid arguments. */

@@ -25,7 +25,7 @@ def built_lib():
 
 def test_header_declares_the_hot_path_entries():
     names = declared_functions()
-    for required in ["kv_pool_create", "kv_append_quantize", "kv_decode_attention",
+    for required in ["kv_pool_create", "kv_append_quantize", "kv_append_step", "kv_decode_attention",
                      "kv_decode_attention_bf16", "kv_quantize_pack_f32"]:
         assert required in names
 
@@ -59,3 +59,5 @@ def test_invalid_arguments_rejected_without_gpu(built_lib):
     assert L.kv_decode_attention(None, 0, 1, None, None, None, None, None, None, 1, 0,
                                  ctypes.c_float(1.0), None, None, 0, None) == native.KV_ERR_INVALID_ARG
     assert L.kv_decode_workspace_bytes(None, 1, 100) == 0
+    assert L.kv_append_step(None, 0, 1, None, None, None, None, None, None, None, 1,
+                            None) == native.KV_ERR_INVALID_ARG
