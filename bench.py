@@ -331,6 +331,24 @@ def main():
         out_host.copy_(out, non_blocking=True)
 
     t_e2e = timed(e2e_step, args.steps, 3)
+
+    # ---- per-step token placement at batch 64 (every sequence evicts one
+    # recent token into INT2 history per step) ----
+    SB, SH, SP = 64, Hkv, 16
+    spool = native.KVPool(native.KV_POOL_INT2_3TIER, 1, Hq, SH, SP, SB * 4, SB, group_size=wl.group_size)
+    native.kv_pool_set_rotation(spool.handle, 0, Rk, Rv, ck, cv)
+    s_rng = np.random.default_rng(5)
+    s_pt = i32(s_rng.permutation(SB * 4).reshape(SB, 4))
+    s_lens = [i32(np.full(SB, 64)), i32(np.zeros(SB)), i32(np.full(SB, 256)), i32(np.zeros(SB))]
+    s_new = bf16(synth.f32_to_bf16_bits(s_rng.standard_normal((2, SB, SH, 128)).astype(np.float32)))
+
+    def astep():
+        native.kv_append_step(spool.handle, 0, SB, s_new[0], s_new[1], *s_lens, s_pt, 4, stream)
+
+    t_step = timed(astep, 20, 3)
+    if spool.error():
+        raise RuntimeError("device error during the append steps")
+    spool.close()
     h2d = q_host.numel() * 2 + meta_host.numel() * 4
     d2h = out_host.numel() * 4
 
@@ -362,6 +380,10 @@ def main():
             "bf16_path": {"us": us_bf16, "bytes": bf16_bytes(wl),
                           "gbs": bf16_bytes(wl) / (us_bf16 * 1e-6) / 1e9,
                           "speedup_int2_vs_bf16": us_bf16 / us},
+            "append_step": {"us": float(np.mean(t_step) * 1e3), "batch": SB, "kv_heads": SH,
+                            "what": "one kv_append_step launch: each sequence's new token enters the "
+                                    "recent ring and its oldest recent token is rotated, clipped, "
+                                    "quantized and packed into INT2 history"},
             "e2e": {"value": us_e2e, "unit": "us", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h)},
             "gpu_launches": args.steps,

@@ -117,9 +117,15 @@ struct Lay {
   static constexpr int ring = big;
   static constexpr int stage = big;                               // tier rows
   static constexpr int sp = big + (stage_f > res_f ? stage_f : res_f);   // [NW][32][G]
-  static constexpr int merge_f = (kInt2 ? 16384 + 128 * ((G + 3) & ~3) + NW * G * 128 : 0) + 16 +
-                                 2 * NW * 128 + 2 * kMaxParts * G;
-  static constexpr int phase_end = (big + ring_f > sp + sp_f) ? big + ring_f : sp + sp_f;
+  // history CTAs: R_v^T after the ring, and the back-rotation's row-slice sums
+  // inside the ring after the results when they fit, else after R_v^T
+  static constexpr int srv = big + ring_f;                        // [128][128] R_v^T
+  static constexpr int spr_f = NW * G * 128;                      // [NW][G][128]
+  static constexpr int spr = (res_f + spr_f <= ring_f) ? big + res_f : srv + 16384;
+  static constexpr int rot_end = kInt2 ? ((spr + spr_f > srv + 16384) ? spr + spr_f : srv + 16384) : 0;
+  static constexpr int merge_f = 16 + 2 * NW * 128 + 2 * kMaxParts * G;
+  static constexpr int phase_end0 = (big + ring_f > sp + sp_f) ? big + ring_f : sp + sp_f;
+  static constexpr int phase_end = (phase_end0 > rot_end) ? phase_end0 : rot_end;
   static constexpr int total = (phase_end > merge_f) ? phase_end : merge_f;
 };
 
@@ -241,139 +247,111 @@ __device__ bool last_to_arrive(unsigned* ticket, unsigned total) {
   return last;
 }
 
-// Log-sum-exp merge of all parts of (b, g) and the final normalisation.
-// Parts [0, n_rot) hold value sums in the rotated basis (INT2 history); their
-// merged sum is rotated back by R_v^T once here, then the unrotated parts
-// (BF16 tiers) are added.  One round of loads: R_v^T goes to shared memory by
-// cp.async while every part's m, l and value vector are fetched.  The
-// back-rotation reads each row of R_v^T once for all G heads: warp w takes
-// rows [w*128/NW, (w+1)*128/NW), lane c takes output columns 4c..4c+3, and
-// the NW row-slice partial sums are added at the end.
-template <int G, int NW, bool kRot>
-__device__ void final_combine(const DecodeArgs& a, int b, int g, int nparts, int n_rot, float* sm) {
-  constexpr int NSUB = NW / G;       // part subsets per output column quad
-  constexpr int kReg = 8;            // value vectors per thread fetched in the first round
+// Rotate a CTA's merged history value sums back to the original basis:
+// o[h][c] = sum_i o'[h][i] R_v[c][i] = sum_i o'[h][i] R_v^T[i][c].  o' arrives
+// in io [G][128] and the result replaces it.  Each row of R_v^T (shared
+// memory) is read once for all G heads: warp w takes rows
+// [w*128/NW, (w+1)*128/NW), lane c takes columns 4c..4c+3, and the NW
+// row-slice sums (spr) are added at the end.  sOt: [128][GP] scratch.
+template <int G, int NW>
+__device__ void rotate_back(float* io, float* sOt, const float* sR, float* spr) {
   constexpr int GP = (G + 3) & ~3;   // heads padded to a multiple of 4
-  constexpr int RPW = 128 / NW;      // rows of R_v^T per warp in the back-rotation
-  const float* base = a.ws + (size_t)(b * a.Hkv + g) * nparts * G * kPart;
-  float* sR = sm;                                  // [128][128] R_v^T
-  float* sM = sm + (kRot ? 16384 : 0);             // [8]
-  float* sL = sM + 8;                              // [8]
-  float* sh = sL + 8;                              // [NSUB][G][128] rotated-part sums
-  float* st = sh + NW * 128;                       // [NSUB][G][128] unrotated-part sums
-  float* sOt = st + NW * 128;                      // [128][GP] merged rotated sum, transposed
-  float* spr = sOt + 128 * GP;                     // [NW][G][128] back-rotation row-slice sums
-  float* sf = spr + (kRot ? NW * G * 128 : 0);     // [nparts * G] m, then weights
-  float* sl = sf + nparts * G;                     // [nparts * G]
-  if (kRot) {
-    const float* R = a.RvT + (size_t)g * 128 * 128;
-    for (int i = threadIdx.x; i < 4096; i += NW * 32) cp_async16(sR + 4 * i, R + 4 * i);
-    cp_async_commit();
+  constexpr int RPW = 128 / NW;      // rows of R_v^T per warp
+  const int warp = threadIdx.x >> 5, cq = threadIdx.x & 31;
+  for (int idx = threadIdx.x; idx < GP * 128; idx += NW * 32) {
+    const int hh = idx >> 7, i = idx & 127;
+    sOt[i * GP + hh] = (hh < G) ? io[idx] : 0.f;
   }
+  __syncthreads();
+  float acc[GP][4];
+#pragma unroll
+  for (int hh = 0; hh < GP; ++hh) acc[hh][0] = acc[hh][1] = acc[hh][2] = acc[hh][3] = 0.f;
+#pragma unroll 4
+  for (int ii = 0; ii < RPW; ++ii) {
+    const int i = warp * RPW + ii;
+    const float4 r = *reinterpret_cast<const float4*>(sR + i * 128 + 4 * cq);
+#pragma unroll
+    for (int hq = 0; hq < GP / 4; ++hq) {
+      const float4 o = *reinterpret_cast<const float4*>(sOt + i * GP + 4 * hq);
+      const float ox[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float* d = acc[4 * hq + e];
+        d[0] = fmaf(ox[e], r.x, d[0]); d[1] = fmaf(ox[e], r.y, d[1]);
+        d[2] = fmaf(ox[e], r.z, d[2]); d[3] = fmaf(ox[e], r.w, d[3]);
+      }
+    }
+  }
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh)
+    *reinterpret_cast<float4*>(spr + (warp * G + hh) * 128 + 4 * cq) =
+        make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
+    float O = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) O += spr[w * G * 128 + idx];
+    io[idx] = O;
+  }
+  __syncthreads();
+}
+
+// Log-sum-exp merge of all parts of (b, g) (every part in the original basis)
+// and the final normalisation.  Warp h < G forms head h's maximum and weighted
+// sum of l over the parts; then every warp accumulates a subset of the parts'
+// value vectors for one head and the subsets are added.
+template <int G, int NW>
+__device__ void merge_parts(const DecodeArgs& a, int b, int g, int nparts, float* sm) {
+  constexpr int NSUB = NW / G;                     // part subsets per output column quad
+  const float* base = a.ws + (size_t)(b * a.Hkv + g) * nparts * G * kPart;
+  float* sL = sm + 8;                              // [8]
+  float* sacc = sm + 16;                           // [NSUB][G][128]
+  float* sf = sacc + NSUB * G * 128;               // [nparts * G] m, then weights
+  float* sl = sf + nparts * G;                     // [nparts * G]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < nparts * G; i += NW * 32) {
     sf[i] = __ldcg(base + (size_t)i * kPart);
     sl[i] = __ldcg(base + (size_t)i * kPart + 1);
   }
-  const int cq = threadIdx.x & 31, h = (threadIdx.x >> 5) % G, sub = (threadIdx.x >> 5) / G;
-  auto ovec = [&](int s) {
-    return __ldcg(reinterpret_cast<const float4*>(base + (size_t)(s * G + h) * kPart + 4) + cq);
-  };
-  float4 ov[kReg];
-#pragma unroll
-  for (int u = 0; u < kReg; ++u) {
-    const int s = sub + u * NSUB;
-    ov[u] = (s < nparts) ? ovec(s) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
   __syncthreads();
-  if (threadIdx.x < G) {
+  if (warp < G) {
     float M = kNegInf;
-    for (int s = 0; s < nparts; ++s) M = fmaxf(M, sf[s * G + threadIdx.x]);
-    sM[threadIdx.x] = M;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < nparts * G; i += NW * 32) {
-    const float m = sf[i], M = sM[i % G];
-    sf[i] = (m == kNegInf || M == kNegInf) ? 0.f : exp2f(m - M);
-  }
-  __syncthreads();
-  if (threadIdx.x < G) {
+    for (int s = lane; s < nparts; s += 32) M = fmaxf(M, sf[s * G + warp]);
+    M = warp_max_xor(M, 1);
     float L = 0.f;
-    for (int s = 0; s < nparts; ++s) L = fmaf(sf[s * G + threadIdx.x], sl[s * G + threadIdx.x], L);
-    sL[threadIdx.x] = L;
-  }
-  float4 ah = make_float4(0.f, 0.f, 0.f, 0.f), at = ah;
-  auto add = [&](int s, const float4& o) {
-    const float f = sf[s * G + h];
-    if (s < n_rot) {
-      ah.x = fmaf(f, o.x, ah.x); ah.y = fmaf(f, o.y, ah.y);
-      ah.z = fmaf(f, o.z, ah.z); ah.w = fmaf(f, o.w, ah.w);
-    } else {
-      at.x = fmaf(f, o.x, at.x); at.y = fmaf(f, o.y, at.y);
-      at.z = fmaf(f, o.z, at.z); at.w = fmaf(f, o.w, at.w);
+    for (int s = lane; s < nparts; s += 32) {
+      const float m = sf[s * G + warp];
+      const float f = (m == kNegInf || M == kNegInf) ? 0.f : exp2f(m - M);
+      sf[s * G + warp] = f;
+      L = fmaf(f, sl[s * G + warp], L);
     }
-  };
-#pragma unroll
-  for (int u = 0; u < kReg; ++u) {
-    const int s = sub + u * NSUB;
-    if (s < nparts) add(s, ov[u]);
+    L = warp_sum_xor(L, 1);
+    if (lane == 0) sL[warp] = L;
   }
-#pragma unroll 8
-  for (int s = sub + kReg * NSUB; s < nparts; s += NSUB) add(s, ovec(s));
-  *reinterpret_cast<float4*>(sh + (sub * G + h) * 128 + 4 * cq) = ah;
-  *reinterpret_cast<float4*>(st + (sub * G + h) * 128 + 4 * cq) = at;
-  if (kRot) cp_async_wait<0>();
   __syncthreads();
-  if (kRot) {
-    for (int idx = threadIdx.x; idx < GP * 128; idx += NW * 32) {
-      const int hh = idx >> 7, i = idx & 127;
-      float O = 0.f;
-      if (hh < G) {
-#pragma unroll
-        for (int u = 0; u < NSUB; ++u) O += sh[u * G * 128 + idx];
-      }
-      sOt[i * GP + hh] = O;
+  {
+    const int cq = lane, h = warp % G, sub = warp / G;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int s = sub; s < nparts; s += NSUB) {
+      const float f = sf[s * G + h];
+      const float4 o =
+          __ldcg(reinterpret_cast<const float4*>(base + (size_t)(s * G + h) * kPart + 4) + cq);
+      acc.x = fmaf(f, o.x, acc.x);
+      acc.y = fmaf(f, o.y, acc.y);
+      acc.z = fmaf(f, o.z, acc.z);
+      acc.w = fmaf(f, o.w, acc.w);
     }
-    __syncthreads();
-    // o_hist[h][c] = sum_i o'[h][i] R_v[c][i] = sum_i o'[h][i] R_v^T[i][c]
-    const int warp = threadIdx.x >> 5;
-    float acc[GP][4];
-#pragma unroll
-    for (int hh = 0; hh < GP; ++hh) acc[hh][0] = acc[hh][1] = acc[hh][2] = acc[hh][3] = 0.f;
-#pragma unroll 4
-    for (int ii = 0; ii < RPW; ++ii) {
-      const int i = warp * RPW + ii;
-      const float4 r = *reinterpret_cast<const float4*>(sR + i * 128 + 4 * cq);
-#pragma unroll
-      for (int hq = 0; hq < GP / 4; ++hq) {
-        const float4 o = *reinterpret_cast<const float4*>(sOt + i * GP + 4 * hq);
-        const float ox[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float* d = acc[4 * hq + e];
-          d[0] = fmaf(ox[e], r.x, d[0]); d[1] = fmaf(ox[e], r.y, d[1]);
-          d[2] = fmaf(ox[e], r.z, d[2]); d[3] = fmaf(ox[e], r.w, d[3]);
-        }
-      }
-    }
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh)
-      *reinterpret_cast<float4*>(spr + (warp * G + hh) * 128 + 4 * cq) =
-          make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
-    __syncthreads();
+    *reinterpret_cast<float4*>(sacc + (sub * G + h) * 128 + 4 * cq) = acc;
   }
+  __syncthreads();
   for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
-    const int hh = idx >> 7, c = idx & 127;
+    const int hh = idx >> 7;
     float O = 0.f;
 #pragma unroll
-    for (int u = 0; u < NSUB; ++u) O += st[u * G * 128 + idx];
-    if (kRot) {
-      float Oh = 0.f;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) Oh += spr[w * G * 128 + idx];
-      O += Oh;
-    }
+    for (int u = 0; u < NSUB; ++u) O += sacc[u * G * 128 + idx];
     const float L = sL[hh];
-    a.out[((size_t)b * a.Hq + g * G + hh) * 128 + c] = (L > 0.f) ? O / L : 0.f;
+    a.out[((size_t)b * a.Hq + g * G + hh) * 128 + (idx & 127)] = (L > 0.f) ? O / L : 0.f;
   }
   if (threadIdx.x == 0) a.tickets[b * a.Hkv + g] = 0u;   // ready for the next call
 }
@@ -568,7 +546,16 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
   const int lane_k = 16 * lane;
   const int lane_sz = (GS == 128) ? 1024 + 16 * r : 1024 + 32 * r;
   uint8_t* ring_lane = ring + lane * LB;
-  auto issue = [&](int t, int stage) {
+  // R_v^T of this head into shared memory for the back-rotation of the partial
+  // (issued with the first tile the loop requests, so it lands while the
+  // first tiles are processed)
+  float* srv = sm + S::srv;
+  auto issue_rv = [&]() {
+    const float* R = a.RvT + (size_t)g * 128 * 128;
+    for (int i = threadIdx.x; i < 4096; i += NW * 32) cp_async16(srv + 4 * i, R + 4 * i);
+  };
+  auto issue = [&](int t, int stage, bool with_rv) {
+    if (with_rv) issue_rv();
     if (t < t_end) {
       const int pid = spid[(t >> tsh) - p_begin];
       const uint8_t* tb = (pid >= 0 && pid < a.num_pages)
@@ -583,7 +570,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
     cp_async_commit();   // empty groups keep the group count uniform
   };
 #pragma unroll
-  for (int st = 0; st < kStages - 1; ++st) issue(t_begin + warp + NW * st, st);   // tiles 0..2
+  for (int st = 0; st < kStages - 1; ++st) issue(t_begin + warp + NW * st, st, false);   // tiles 0..2
 
   // ---- q' = q R_k and its per-group sums (overlaps the first copies) ----
   rotate_q<S::HP, NW>(sq, a.rfrag + ((size_t)g * kFragBlocks + 2) * 4096, sqr);
@@ -640,7 +627,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
   int k = 0;
   for (int t = t_begin + warp; t < t_end; t += NW, ++k) {
     // tile k+3 goes into the slot read in the previous iteration
-    issue(t + NW * (kStages - 1), (k + kStages - 1) % kStages);
+    issue(t + NW * (kStages - 1), (k + kStages - 1) % kStages, k == 0);
     cp_async_wait<kStages - 1>();   // tile k landed
     const uint8_t* src = ring_lane + (k % kStages) * (32 * LB);
     const uint4 kq4 = *reinterpret_cast<const uint4*>(src);
@@ -776,6 +763,10 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
       }
     }
   }
+  if (k == 0) {   // this warp had no tile: its share of R_v^T is still to be requested
+    issue_rv();
+    cp_async_commit();
+  }
   cp_async_wait<0>();
   __syncthreads();   // every warp is done with its ring before the results reuse it
 
@@ -806,7 +797,8 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
   }
   __syncthreads();
   merge_warps<G, NW>(swo, swm, swl, sqr, sm + S::smm, sm + S::sml);   // q' no longer needed
-  // the partial stays in the rotated basis; the final merge rotates back once
+  // back to the original basis (q is no longer needed either: its slot is scratch)
+  rotate_back<G, NW>(sqr, sq, srv, sm + S::spr);
   write_partial<G, NW>(part, sqr, sm + S::smm, sm + S::sml);
 }
 
@@ -880,16 +872,12 @@ __global__ void __launch_bounds__(int2_warps(G) * 32, 1) decode_int2_kernel(Deco
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int nparts = a.n_split + a.n_tier;
   float* part = a.ws + ((size_t)(b * a.Hkv + g) * nparts + split) * G * kPart;
-  if (split == 0) {   // R_v^T of this head into L2 for the final merge
-    const char* R = reinterpret_cast<const char*>(a.RvT + (size_t)g * 128 * 128);
-    for (int i = threadIdx.x; i < 512; i += NW * 32) prefetch_l2(R + 128 * i);
-  }
   if (split < a.n_split)
     int2_history<G, GS>(a, b, g, split, sm, part);
   else
     bf16_tiers<G, GS>(a, b, g, split - a.n_split, sm, part);
   if (last_to_arrive(a.tickets + b * a.Hkv + g, (unsigned)nparts))
-    final_combine<G, NW, true>(a, b, g, nparts, a.n_split, sm);
+    merge_parts<G, NW>(a, b, g, nparts, sm);
 }
 
 // ---------------------------------------------------------------------------
