@@ -45,6 +45,7 @@ namespace {
 constexpr int kPart = 132;       // floats per (part, head) partial: m, l, -, -, o[128]
 constexpr float kNegInf = -INFINITY;
 constexpr int kStages = 4;       // tiles in each warp's ring
+constexpr int kWaitPolls = 1 << 20;   // bounded mbarrier polls before a copy counts as lost
 constexpr int kMaxParts = 400;   // partials per (sequence, KV head) the final merge reads
 constexpr int kMaxPids = 1032;   // page ids staged per CTA (a split covers <= 1024 tiles)
 constexpr int kTierRows = 320;   // sink + recent storage rows staged per tier CTA
@@ -99,15 +100,16 @@ struct DecodeArgs {
 template <int G, int GS, int NW, bool kInt2>
 struct Lay {
   static constexpr int HP = (G <= 4) ? 4 : 4 * ((G + 3) / 4);   // padded heads (MMA columns)
-  static constexpr int LB = (GS == 128) ? 48 : 64;               // ring bytes per lane per stage
+  static constexpr int TB = 1024 + 16 * 8 * (128 / GS);         // stored tile bytes (one ring stage)
   static constexpr int sq = 0;                                    // [HP][128]
   static constexpr int sqr = sq + HP * 128;                       // [HP][128]
   static constexpr int ssum = sqr + HP * 128;                     // [HP][2]
   static constexpr int smm = ssum + pad4(2 * HP);                 // [G] merged m
   static constexpr int sml = smm + pad4(G);                       // [G] merged l
   static constexpr int spid = sml + pad4(G);                      // [kMaxPids] int
-  static constexpr int big = spid + kMaxPids;
-  static constexpr int ring_f = kInt2 ? NW * kStages * 32 * LB / 4 : 0;
+  static constexpr int smbar = spid + kMaxPids;                   // [NW * kStages + 1] mbarriers
+  static constexpr int big = smbar + (kInt2 ? pad4(2 * (NW * kStages + 1)) : 0);
+  static constexpr int ring_f = kInt2 ? NW * kStages * TB / 4 : 0;
   static constexpr int res_f = NW * G * 128 + 2 * pad4(NW * G);
   static constexpr int sp_f = NW * 32 * G;
   static constexpr int stage_f = kInt2 ? kTierRows * (kTierRowK + kTierRowV) / 4 : 0;
@@ -510,7 +512,6 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
   using S = Lay<G, GS, NW, true>;
   constexpr int NT = S::HP / 4;      // MMA n-tiles of 8 columns (4 heads x hi/lo)
   constexpr int NG = 128 / GS;       // quantization groups per row
-  constexpr int LB = S::LB;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = lane >> 2, j = lane & 3;
 
@@ -541,36 +542,39 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
   }
 
   // ---- start streaming this warp's first tiles into its ring ----
-  uint8_t* ring = reinterpret_cast<uint8_t*>(sm + S::ring) + (size_t)warp * kStages * 32 * LB;
-  const uint8_t* head_base = a.hist + (size_t)g * (a.page_bytes / a.Hkv);
-  const int lane_k = 16 * lane;
-  const int lane_sz = (GS == 128) ? 1024 + 16 * r : 1024 + 32 * r;
-  uint8_t* ring_lane = ring + lane * LB;
-  // R_v^T of this head into shared memory for the back-rotation of the partial
-  // (issued with the first tile the loop requests, so it lands while the
-  // first tiles are processed)
+  // A ring stage holds one whole stored tile, brought in by one bulk copy that
+  // lane 0 issues and that completes on the stage's mbarrier; R_v^T (for the
+  // back-rotation of the partial) comes the same way on its own barrier.
+  constexpr uint32_t TB = S::TB;
+  uint8_t* ring = reinterpret_cast<uint8_t*>(sm + S::ring) + (size_t)warp * kStages * TB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::smbar);
+  uint64_t* wbar = bars + warp * kStages;
+  uint64_t* rbar = bars + NW * kStages;
   float* srv = sm + S::srv;
-  auto issue_rv = [&]() {
-    const float* R = a.RvT + (size_t)g * 128 * 128;
-    for (int i = threadIdx.x; i < 4096; i += NW * 32) cp_async16(srv + 4 * i, R + 4 * i);
-  };
-  auto issue = [&](int t, int stage, bool with_rv) {
-    if (with_rv) issue_rv();
-    if (t < t_end) {
+  if (lane < kStages) mbar_init(wbar + lane, 1);
+  if (threadIdx.x == 0) mbar_init(rbar, 1);
+  mbar_fence_init();
+  __syncthreads();
+  const uint8_t* head_base = a.hist + (size_t)g * (a.page_bytes / a.Hkv);
+  const int lane_sz = (GS == 128) ? 1024 + 16 * r : 1024 + 32 * r;
+  auto issue = [&](int t, int stage) {
+    if (lane == 0 && t < t_end) {
       const int pid = spid[(t >> tsh) - p_begin];
       const uint8_t* tb = (pid >= 0 && pid < a.num_pages)
                               ? head_base + (size_t)pid * a.page_bytes + (t & tmask) * a.tile_bytes
                               : g_zero_tile;
-      uint8_t* d = ring_lane + stage * (32 * LB);
-      cp_async16(d, tb + lane_k);
-      cp_async16(d + 16, tb + 512 + lane_k);
-      cp_async16(d + 32, tb + lane_sz);
-      if (GS == 64) cp_async16(d + 48, tb + lane_sz + 16);
+      mbar_expect_tx(wbar + stage, TB);
+      bulk_g2s(ring + stage * TB, tb, TB, wbar + stage);
     }
-    cp_async_commit();   // empty groups keep the group count uniform
   };
 #pragma unroll
-  for (int st = 0; st < kStages - 1; ++st) issue(t_begin + warp + NW * st, st, false);   // tiles 0..2
+  for (int st = 0; st < kStages - 1; ++st) issue(t_begin + warp + NW * st, st);   // tiles 0..2
+  if (threadIdx.x == 0) {
+    const float* R = a.RvT + (size_t)g * 128 * 128;
+    mbar_expect_tx(rbar, 128 * 128 * 4);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) bulk_g2s(srv + 4096 * c, R + 4096 * c, 16384, rbar);
+  }
 
   // ---- q' = q R_k and its per-group sums (overlaps the first copies) ----
   rotate_q<S::HP, NW>(sq, a.rfrag + ((size_t)g * kFragBlocks + 2) * 4096, sqr);
@@ -625,16 +629,22 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
   }
 
   int k = 0;
+  bool ok = true;
   for (int t = t_begin + warp; t < t_end; t += NW, ++k) {
-    // tile k+3 goes into the slot read in the previous iteration
-    issue(t + NW * (kStages - 1), (k + kStages - 1) % kStages, k == 0);
-    cp_async_wait<kStages - 1>();   // tile k landed
-    const uint8_t* src = ring_lane + (k % kStages) * (32 * LB);
-    const uint4 kq4 = *reinterpret_cast<const uint4*>(src);
-    const uint4 vq4 = *reinterpret_cast<const uint4*>(src + 16);
-    const uint4 sz0 = *reinterpret_cast<const uint4*>(src + 32);
+    __syncwarp();   // every lane is done with the stage refilled next
+    // tile k+3 goes into the stage read in the previous iteration
+    issue(t + NW * (kStages - 1), (k + kStages - 1) % kStages);
+    const int st = k % kStages;
+    if (!__all_sync(0xffffffffu, mbar_wait(wbar + st, (k / kStages) & 1, kWaitPolls))) {
+      ok = false;
+      break;
+    }
+    const uint8_t* src = ring + st * TB;
+    const uint4 kq4 = *reinterpret_cast<const uint4*>(src + 16 * lane);
+    const uint4 vq4 = *reinterpret_cast<const uint4*>(src + 512 + 16 * lane);
+    const uint4 sz0 = *reinterpret_cast<const uint4*>(src + lane_sz);
     const uint4 sz1 =
-        (GS == 64) ? *reinterpret_cast<const uint4*>(src + 48) : make_uint4(0, 0, 0, 0);
+        (GS == 64) ? *reinterpret_cast<const uint4*>(src + lane_sz + 16) : make_uint4(0, 0, 0, 0);
     const int pid_cur = spid[(t >> tsh) - p_begin];
     const bool page_ok = pid_cur >= 0 && pid_cur < a.num_pages;
     if (!page_ok && lane == 0) flag_error(a.err, KV_DEVERR_PAGE_ID);
@@ -763,12 +773,22 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
       }
     }
   }
-  if (k == 0) {   // this warp had no tile: its share of R_v^T is still to be requested
-    issue_rv();
-    cp_async_commit();
+  if (!ok) {   // a copy did not arrive in time: wait (bounded) for the ones in flight
+    if (lane == 0) flag_error(a.err, KV_DEVERR_TIMEOUT);
+    for (int kk = k; kk < k + kStages - 1 && t_begin + warp + NW * kk < t_end; ++kk)
+      mbar_wait(wbar + kk % kStages, (kk / kStages) & 1, kWaitPolls);
   }
-  cp_async_wait<0>();
-  __syncthreads();   // every warp is done with its ring before the results reuse it
+  if (!mbar_wait(rbar, 0, kWaitPolls)) {
+    ok = false;
+    if (threadIdx.x == 0) flag_error(a.err, KV_DEVERR_TIMEOUT);
+  }
+  ok = __syncthreads_and(ok);   // every warp is done with its ring before the results reuse it
+  if (lane < kStages) mbar_inval(wbar + lane);
+  if (threadIdx.x == 0) mbar_inval(rbar);
+  if (!ok) {   // the split's result is skipped
+    write_empty_partial<G, NW>(part);
+    return;
+  }
 
   // ---- warp results -> shared memory ----
   float* swo = sm + S::swo;

@@ -60,7 +60,9 @@ enum {
   KV_DEVERR_NONE = 0,
   KV_DEVERR_PAGE_ID = 1,      /* page table entry outside [0, num_pages)     */
   KV_DEVERR_LENGTH = 2,       /* a length above the tier / table capacity    */
-  KV_DEVERR_SEQ_RANGE = 3     /* cu_tokens not monotone or history overflow  */
+  KV_DEVERR_SEQ_RANGE = 3,    /* cu_tokens not monotone or history overflow  */
+  KV_DEVERR_TIMEOUT = 4       /* a bounded wait for an asynchronous copy ran
+                                 out; the work that needed it was skipped      */
 };
 
 typedef enum { KV_POOL_INT2_3TIER = 0, KV_POOL_BF16 = 1 } kv_pool_kind_t;
