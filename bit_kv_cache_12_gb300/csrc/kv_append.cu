@@ -366,74 +366,96 @@ struct StepArgs {
   int* err;
 };
 
+// The placement of sequence b's new token, from its current lengths:
+// mode 0: sink slot `slot`; 1: recent ring slot `slot`; 2: evict the ring's
+// oldest token (slot `slot`) into history position hist_len, which lands at
+// row `pos` of the tile at byte offset `tile` of the layer's history, then
+// put the new token in that slot; -1: not applied (error code `err`).
+struct StepPlace {
+  int mode, slot, pos, err;
+  long long tile;
+};
+
+__device__ StepPlace step_place(const StepArgs& a, int b) {
+  StepPlace s{-1, 0, 0, 0, 0};
+  const int sl = a.sink_len[b], hl = a.hist_len[b], rl = a.rec_len[b], rs = a.rec_start[b];
+  if (sl < 0 || sl > a.sink_cap || rl < 0 || rl > a.rec_cap || rs < 0 || rs >= a.rec_cap || hl < 0) {
+    s.err = KV_DEVERR_LENGTH;
+  } else if (sl < a.sink_cap) {                    // one of the sequence's first tokens
+    s.mode = 0;
+    s.slot = sl;
+  } else if (rl < a.rec_cap) {                     // the recent ring has room
+    s.mode = 1;
+    s.slot = (rs + rl) % a.rec_cap;
+  } else {                                         // evict the ring's oldest token
+    const int pidx = hl / a.P;
+    const int pid = (pidx < a.max_pages) ? a.pt[(size_t)b * a.max_pages + pidx] : -1;
+    if (pidx >= a.max_pages) {
+      s.err = KV_DEVERR_LENGTH;
+    } else if (pid < 0 || pid >= a.num_pages) {
+      s.err = KV_DEVERR_PAGE_ID;
+    } else {
+      s.mode = 2;
+      s.slot = rs;
+      s.pos = hl % kTile;
+      s.tile = (long long)pid * (long long)a.page_bytes + (long long)((hl % a.P) / kTile) * a.tile_bytes;
+    }
+  }
+  return s;
+}
+
+// Token movement: CTA (sequence chunk, KV head g, tensor); the tensor's
+// rotation fragments and clips of head g go to shared memory once and every
+// warp places the tokens of its sequences.  The lengths are read only; the
+// next kernel updates them.
+constexpr int kStepSeqs = 8;   // sequences per CTA
 template <int GS>
-__global__ void __launch_bounds__(512, 1) append_step_kernel(StepArgs a) {
-  __shared__ int s_mode, s_slot, s_pos;
-  __shared__ long long s_tile;
-  const int b = blockIdx.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  if (threadIdx.x == 0) {
-    const int sl = a.sink_len[b], hl = a.hist_len[b], rl = a.rec_len[b], rs = a.rec_start[b];
-    int mode = -1, slot = 0, pos = 0;
-    long long tile = 0;
-    if (sl < 0 || sl > a.sink_cap || rl < 0 || rl > a.rec_cap || rs < 0 || rs >= a.rec_cap ||
-        hl < 0) {
-      flag_error(a.err, KV_DEVERR_LENGTH);
-    } else if (sl < a.sink_cap) {                    // one of the sequence's first tokens
-      mode = 0;
-      slot = sl;
-    } else if (rl < a.rec_cap) {                     // the recent ring has room
-      mode = 1;
-      slot = (rs + rl) % a.rec_cap;
-    } else {                                         // evict the ring's oldest token
-      const int pidx = hl / a.P;
-      const int pid = (pidx < a.max_pages) ? a.pt[(size_t)b * a.max_pages + pidx] : -1;
-      if (pidx >= a.max_pages) {
-        flag_error(a.err, KV_DEVERR_LENGTH);
-      } else if (pid < 0 || pid >= a.num_pages) {
-        flag_error(a.err, KV_DEVERR_PAGE_ID);
-      } else {
-        mode = 2;
-        slot = rs;
-        pos = hl % kTile;
-        tile = (long long)pid * (long long)a.page_bytes + (long long)((hl % a.P) / kTile) * a.tile_bytes;
-      }
-    }
-    s_mode = mode; s_slot = slot; s_pos = pos; s_tile = tile;
-  }
+__global__ void __launch_bounds__(256, 1) append_step_kernel(StepArgs a, int B) {
+  extern __shared__ uint4 sfrag[];                 // 4096 fragments, then clip
+  float* sclip = reinterpret_cast<float*>(sfrag + 4096);
+  const int g = blockIdx.y, tensor = blockIdx.z;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint4* src_frag = a.rfrag + ((size_t)g * kFragBlocks + tensor) * 4096;
+  for (int i = threadIdx.x; i < 4096; i += blockDim.x) sfrag[i] = __ldg(src_frag + i);
+  if (threadIdx.x < 128) sclip[threadIdx.x] = a.clip[((size_t)tensor * a.Hkv + g) * 128 + threadIdx.x];
   __syncthreads();
-  const int mode = s_mode, slot = s_slot, pos = s_pos;
-  if (mode >= 0) {
-    for (int pair = warp; pair < 2 * a.Hkv; pair += nwarps) {
-      const int g = pair >> 1, tensor = pair & 1;
-      const size_t sh = (size_t)b * a.Hkv + g;
-      const uint16_t* src = (tensor ? a.v_new : a.k_new) + sh * 128;
-      uint16_t* dst = (mode == 0)
-                          ? (tensor ? a.sink_v : a.sink_k) + (sh * a.sink_cap + slot) * 128
-                          : (tensor ? a.rec_v : a.rec_k) + (sh * a.rec_cap + slot) * 128;
-      if (mode == 2) {
-        // the slot's current token goes to history position pos of its tile
-        uint8_t* tb = a.hist + s_tile + (size_t)g * a.head_block;
-        const uint16_t* old = dst;
-        append_tile<GS>(tensor, a.rfrag + ((size_t)g * kFragBlocks + tensor) * 4096,
-                        a.clip + ((size_t)tensor * a.Hkv + g) * 128, tb, false,
-                        [&](int row) { return row == pos; },
-                        [&](int) { return old + 32 * (lane & 3); });
-        __syncwarp();   // every lane has read the old row before it is overwritten
-      }
-      *reinterpret_cast<uint2*>(dst + 4 * lane) = *reinterpret_cast<const uint2*>(src + 4 * lane);
+  const int b0 = blockIdx.x * kStepSeqs;
+  for (int b = b0 + warp; b < min(B, b0 + kStepSeqs); b += blockDim.x >> 5) {
+    const StepPlace pl = step_place(a, b);
+    if (pl.mode < 0) continue;
+    const size_t sh = (size_t)b * a.Hkv + g;
+    const uint16_t* src = (tensor ? a.v_new : a.k_new) + sh * 128;
+    uint16_t* dst = (pl.mode == 0)
+                        ? (tensor ? a.sink_v : a.sink_k) + (sh * a.sink_cap + pl.slot) * 128
+                        : (tensor ? a.rec_v : a.rec_k) + (sh * a.rec_cap + pl.slot) * 128;
+    if (pl.mode == 2) {
+      // the slot's current token goes to history position pos of its tile
+      uint8_t* tb = a.hist + pl.tile + (size_t)g * a.head_block;
+      const uint16_t* old = dst;
+      const int pos = pl.pos;
+      append_tile<GS>(tensor, sfrag, sclip, tb, false, [&](int row) { return row == pos; },
+                      [&](int) { return old + 32 * (lane & 3); });
+      __syncwarp();   // every lane has read the old row before it is overwritten
     }
+    *reinterpret_cast<uint2*>(dst + 4 * lane) = *reinterpret_cast<const uint2*>(src + 4 * lane);
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    if (mode == 0) {
-      a.sink_len[b] = slot + 1;
-    } else if (mode == 1) {
-      a.rec_len[b] += 1;
-    } else if (mode == 2) {
-      a.hist_len[b] += 1;
-      a.rec_start[b] = (slot + 1) % a.rec_cap;
-    }
+}
+
+// Length update after the token movement: one thread per sequence, the same
+// placement decision from the same (not yet updated) lengths.
+__global__ void append_step_lengths_kernel(StepArgs a, int B) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const StepPlace pl = step_place(a, b);
+  if (pl.mode == 0) {
+    a.sink_len[b] = pl.slot + 1;
+  } else if (pl.mode == 1) {
+    a.rec_len[b] += 1;
+  } else if (pl.mode == 2) {
+    a.hist_len[b] += 1;
+    a.rec_start[b] = (pl.slot + 1) % a.rec_cap;
+  } else {
+    flag_error(a.err, pl.err);
   }
 }
 
@@ -701,11 +723,27 @@ cudaError_t launch_append_step(const Pool& p, int layer, int B, const void* k_ne
   a.rfrag = p.rfrag + (size_t)layer * H * kFragBlocks * rfrag_per_head();
   a.clip = p.clip + (size_t)layer * 2 * H * 128;
   a.err = p.err;
-  const int threads = 32 * min(2 * H, 16);
-  if (p.cfg.group_size == 64)
-    append_step_kernel<64><<<B, threads, 0, s>>>(a);
-  else
-    append_step_kernel<128><<<B, threads, 0, s>>>(a);
+  const size_t smem = 4096 * sizeof(uint4) + 128 * sizeof(float);
+  static bool attr64 = false, attr128 = false;
+  dim3 grid((unsigned)((B + kStepSeqs - 1) / kStepSeqs), H, 2);
+  if (p.cfg.group_size == 64) {
+    if (!attr64) {
+      cudaError_t e = cudaFuncSetAttribute(append_step_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      attr64 = true;
+    }
+    append_step_kernel<64><<<grid, 256, smem, s>>>(a, B);
+  } else {
+    if (!attr128) {
+      cudaError_t e = cudaFuncSetAttribute(append_step_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      attr128 = true;
+    }
+    append_step_kernel<128><<<grid, 256, smem, s>>>(a, B);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  append_step_lengths_kernel<<<(B + 127) / 128, 128, 0, s>>>(a, B);
   return cudaGetLastError();
 }
 
