@@ -103,8 +103,8 @@ __device__ __forceinline__ void store_words(uint8_t* dst, const uint32_t (&w)[4]
 // are kept unless `full`.  row_ptr(row) points at channel 32 * (lane % 4) of
 // the row's bf16 input.  Each output row depends only on its own input row,
 // so a token gets the same codes however many tokens share its tile.
-template <int GS, class RowOk, class RowPtr>
-__device__ __forceinline__ void append_tile(int tensor, const uint4* frag, const float* clip,
+template <int GS, int TENSOR, class RowOk, class RowPtr>
+__device__ __forceinline__ void append_tile(const uint4* frag, const float* clip,
                                             uint8_t* tb, bool full, const RowOk& row_ok,
                                             const RowPtr& row_ptr) {
   const int lane = threadIdx.x & 31;
@@ -115,7 +115,7 @@ __device__ __forceinline__ void append_tile(int tensor, const uint4* frag, const
   load_row64(row_ptr(r + 8), row_ok(r + 8), xr8);
 
   uint32_t word[4] = {0u, 0u, 0u, 0u}, mask[4] = {0u, 0u, 0u, 0u};
-  if (tensor == 0) {
+  if constexpr (TENSOR == 0) {
     // ---- K: D[token][out channel] = x R_k, tokens as MMA rows ----
     float acc[16][4];
 #pragma unroll
@@ -288,11 +288,11 @@ __device__ __forceinline__ void append_tile(int tensor, const uint4* frag, const
   }
 }
 
-template <int GS>
+template <int GS, int TENSOR>
 __global__ void __launch_bounds__(256, 2) append_kernel(AppendArgs a) {
   extern __shared__ uint4 sfrag[];                 // 4096 fragments, then clip
   float* sclip = reinterpret_cast<float*>(sfrag + 4096);
-  const int g = blockIdx.y, tensor = blockIdx.z;
+  const int g = blockIdx.y, tensor = TENSOR;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, j = lane & 3;
 
   const uint4* src = a.rfrag + ((size_t)g * kFragBlocks + tensor) * 4096;
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(256, 2) append_kernel(AppendArgs a) {
       const int tok = c0 + (tile * kTile + row - h0);
       return (tensor == 0 ? a.k : a.v) + ((size_t)tok * a.Hkv + g) * 128 + 32 * j;
     };
-    append_tile<GS>(tensor, sfrag, sclip, tb, full, row_ok, row_ptr);
+    append_tile<GS, TENSOR>(sfrag, sclip, tb, full, row_ok, row_ptr);
   }
 }
 
@@ -433,8 +433,12 @@ __global__ void __launch_bounds__(256, 1) append_step_kernel(StepArgs a, int B) 
       uint8_t* tb = a.hist + pl.tile + (size_t)g * a.head_block;
       const uint16_t* old = dst;
       const int pos = pl.pos;
-      append_tile<GS>(tensor, sfrag, sclip, tb, false, [&](int row) { return row == pos; },
-                      [&](int) { return old + 32 * (lane & 3); });
+      auto row_ok = [&](int row) { return row == pos; };
+      auto row_ptr = [&](int) { return old + 32 * (lane & 3); };
+      if (tensor == 0)
+        append_tile<GS, 0>(sfrag, sclip, tb, false, row_ok, row_ptr);
+      else
+        append_tile<GS, 1>(sfrag, sclip, tb, false, row_ok, row_ptr);
       __syncwarp();   // every lane has read the old row before it is overwritten
     }
     *reinterpret_cast<uint2*>(dst + 4 * lane) = *reinterpret_cast<const uint2*>(src + 4 * lane);
@@ -666,30 +670,33 @@ cudaError_t launch_append(const Pool& p, int layer, int n_seqs, const void* k, c
   a.clip = p.clip + (size_t)layer * 2 * H * 128;
   a.err = p.err;
   const long long tasks = (long long)n_seqs * a.max_tiles;
-  // CTAs per (head, tensor): enough to fill every SM twice over all heads/tensors
-  long long ctas = (2LL * p.sm_count + 2 * H - 1) / (2 * H);
+  // CTAs per head in each (one-tensor) launch: enough to fill every SM twice
+  long long ctas = (2LL * p.sm_count + H - 1) / H;
   ctas = max(1LL, min(ctas, (tasks + 7) / 8));
   a.tasks_per_cta = (int)((tasks + ctas - 1) / ctas);
   ctas = (tasks + a.tasks_per_cta - 1) / a.tasks_per_cta;
   const size_t smem = 4096 * sizeof(uint4) + 128 * sizeof(float);
-  static bool attr64 = false, attr128 = false;
-  dim3 grid((unsigned)ctas, H, 2);
+  // K and V as separate launches: each instantiation carries one tensor's code
+  dim3 grid((unsigned)ctas, H, 1);
+  static bool attr[2][2] = {{false, false}, {false, false}};
+  auto go = [&](auto kernel, int gi, int ti) -> cudaError_t {
+    if (!attr[gi][ti]) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      attr[gi][ti] = true;
+    }
+    kernel<<<grid, 256, smem, s>>>(a);
+    return cudaGetLastError();
+  };
+  cudaError_t e;
   if (p.cfg.group_size == 64) {
-    if (!attr64) {
-      cudaError_t e = cudaFuncSetAttribute(append_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      attr64 = true;
-    }
-    append_kernel<64><<<grid, 256, smem, s>>>(a);
+    e = go(append_kernel<64, 0>, 0, 0);
+    if (e == cudaSuccess) e = go(append_kernel<64, 1>, 0, 1);
   } else {
-    if (!attr128) {
-      cudaError_t e = cudaFuncSetAttribute(append_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      attr128 = true;
-    }
-    append_kernel<128><<<grid, 256, smem, s>>>(a);
+    e = go(append_kernel<128, 0>, 1, 0);
+    if (e == cudaSuccess) e = go(append_kernel<128, 1>, 1, 1);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_append_step(const Pool& p, int layer, int B, const void* k_new,

@@ -39,6 +39,7 @@ __device__ __forceinline__ __half f16_sat(float x) {
 struct ScaleZero {
   __half sh, zh;
   float s, z;
+  float rs;   // fl(1 / s) for s > 0
 };
 
 __device__ __forceinline__ ScaleZero scale_zero(float mn, float mx) {
@@ -49,12 +50,21 @@ __device__ __forceinline__ ScaleZero scale_zero(float mn, float mx) {
   r.zh = f16_sat(zf);
   r.s = __half2float(r.sh);
   r.z = __half2float(r.zh);
+  r.rs = (r.s > 0.0f) ? __frcp_rn(r.s) : 0.0f;
   return r;
 }
 
+// code = clamp(rint(fl(fl(y - z) / s)), 0, 3).  The quotient is formed as
+// fl(d * fl(1/s)), which is within 1.5 * 2^-23 * |d / s| of fl(d / s); only a
+// half-integer between the two could change rint, and the relevant quotients
+// are below 3.5, so outside a 2^-18 band around every half-integer the product
+// gives the same code and inside it the IEEE division is taken.
 __device__ __forceinline__ uint32_t quant_code(float y, const ScaleZero& q) {
   if (q.s == 0.0f) return 0u;
-  float t = rintf(__fdiv_rn(__fsub_rn(y, q.z), q.s));
+  const float d = __fsub_rn(y, q.z);
+  float t = __fmul_rn(d, q.rs);
+  if (fabsf(__fsub_rn(t, floorf(t)) - 0.5f) <= 3.814697265625e-6f) t = __fdiv_rn(d, q.s);
+  t = rintf(t);
   t = fminf(fmaxf(t, 0.0f), 3.0f);
   return (uint32_t)t;
 }
