@@ -167,3 +167,49 @@ def test_three_tier_decode_on_tiny_workload_is_sane():
                                 wl.Hkv, 128, wl.scale)
     assert out.shape == (1, 8, 128) and np.all(np.isfinite(out))
     assert np.abs(out).max() < 20
+
+
+def test_log_sum_exp_closed_forms_and_library():
+    """ln sum_t exp(l_t): a single token gives its scaled score; N equal keys
+    give that score + ln N; a small random case equals scipy's logsumexp of
+    scores formed independently (keys rotated back, q not rotated)."""
+    scipy_special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(31)
+    d, tau = 128, 0.11
+    R = synth.haar_orthogonal(rng)
+    e = np.zeros((0, d))
+    q = rng.standard_normal(d)
+    k1 = rng.standard_normal((1, d)); v1 = rng.standard_normal((1, d))
+    _, lse = att.three_tier_head(q, R, R, k1, v1, e, e, e, e, tau, return_lse=True)
+    assert abs(lse - tau * float(q @ k1[0])) <= 1e-12 * max(1.0, abs(lse))
+    kN = np.repeat(k1, 7, axis=0); vN = rng.standard_normal((7, d))
+    _, lse7 = att.three_tier_head(q, R, R, kN, vN, e, e, e, e, tau, return_lse=True)
+    assert abs(lse7 - (tau * float(q @ k1[0]) + np.log(7.0))) <= 1e-12 * max(1.0, abs(lse7))
+    sink = rng.standard_normal((3, d)); hist = rng.standard_normal((5, d)); rec = rng.standard_normal((4, d))
+    vals = rng.standard_normal((12, d))
+    _, lse_r = att.three_tier_head(q, R, R, sink, vals[:3], hist, vals[3:8], rec, vals[8:], tau,
+                                   return_lse=True)
+    keys_orig = np.concatenate([sink, hist @ R.T, rec])       # history keys back in the original basis
+    assert abs(lse_r - scipy_special.logsumexp(tau * keys_orig @ q)) <= 1e-12 * abs(lse_r)
+
+
+def test_multi_query_is_independent_single_queries():
+    wl = synth.make_decode_workload("mq", 32, B=2, Hq=4, Hkv=2, ctx=[400, 700], page_size=16)
+    pages = np.zeros((wl.num_pages, wl.Hkv, kq.tile_bytes(wl.group_size)), np.uint8)
+    for b in range(wl.B):
+        kq.pack_history_full(wl.hist_k[b], wl.hist_v[b], wl.Rk, wl.Rv, wl.clip_k, wl.clip_v, wl.page_table[b],
+                             wl.num_pages, wl.Hkv, wl.page_size, wl.group_size, pages)
+    hist = lambda b, g: kq.read_history(pages, wl.page_table[b], int(wl.hist_len[b]), g, wl.page_size,
+                                        wl.group_size)
+    rng = np.random.default_rng(33)
+    T = 3
+    qm = synth.f32_to_bf16_bits(rng.standard_normal((wl.B, T, wl.Hq, 128)).astype(np.float32))
+    out, lse = att.decode_three_tier_multi(qm, wl.Rk, wl.Rv, wl.sink_k, wl.sink_v, wl.sink_len, hist,
+                                           wl.hist_len, wl.rec_k, wl.rec_v, wl.rec_len, wl.rec_start,
+                                           wl.Hkv, wl.group_size, wl.scale)
+    assert out.shape == (wl.B, T, wl.Hq, 128) and lse.shape == (wl.B, T, wl.Hq)
+    for t in range(T):
+        one = att.decode_three_tier(qm[:, t], wl.Rk, wl.Rv, wl.sink_k, wl.sink_v, wl.sink_len, hist,
+                                    wl.hist_len, wl.rec_k, wl.rec_v, wl.rec_len, wl.rec_start, wl.Hkv,
+                                    wl.group_size, wl.scale)
+        assert np.array_equal(out[:, t], one)
