@@ -1,6 +1,7 @@
 // C ABI of libkvint2: argument checks, pool storage, launches.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <new>
 
 #include "kv_internal.h"
@@ -327,6 +328,40 @@ kv_status_t kv_append_bf16(kv_pool_t* pool, int32_t layer, int32_t n_seqs, const
   return cuda_status(kvint2::launch_append_bf16(pool->p, layer, n_seqs, k, v, cu_tokens, start_pos,
                                                 page_table, max_pages_per_seq, max_tokens_per_seq,
                                                 static_cast<cudaStream_t>(stream)));
+}
+
+size_t kv_decode_multi_workspace_bytes(const kv_pool_t* pool, int32_t B, int32_t T,
+                                       int32_t max_hist_len) {
+  if (!pool || B <= 0 || T <= 0 || max_hist_len < 0 || B > pool->p.cfg.max_seqs) return 0;
+  const Pool& p = pool->p;
+  if (p.cfg.kind != KV_POOL_INT2_3TIER || !is_pow2_in((int)std::min<int64_t>((int64_t)T * p.G, 16), 1, 8))
+    return 0;
+  return kvint2::plan_decode_int2(p, B, max_hist_len, T).bytes;
+}
+
+kv_status_t kv_decode_attention_multi(kv_pool_t* pool, int32_t layer, int32_t B, int32_t T,
+                                      const void* q, const int32_t* sink_len,
+                                      const int32_t* hist_len, const int32_t* recent_len,
+                                      const int32_t* recent_start, const int32_t* page_table,
+                                      int32_t max_pages_per_seq, int32_t max_hist_len,
+                                      float softmax_scale, float* out, float* lse,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (!valid_layer(pool, layer) || B <= 0 || T <= 0 || max_pages_per_seq <= 0 || max_hist_len < 0)
+    return KV_ERR_INVALID_ARG;
+  const Pool& p = pool->p;
+  if (p.cfg.kind != KV_POOL_INT2_3TIER || B > p.cfg.max_seqs) return KV_ERR_INVALID_ARG;
+  if ((int64_t)T * p.G > 8 || !is_pow2_in(T * p.G, 1, 8)) return KV_ERR_UNSUPPORTED;
+  if (!q || !sink_len || !hist_len || !recent_len || !recent_start || !page_table || !out ||
+      !workspace)
+    return KV_ERR_INVALID_ARG;
+  if ((int64_t)max_hist_len > (int64_t)max_pages_per_seq * p.cfg.page_size) return KV_ERR_INVALID_ARG;
+  if (((uintptr_t)workspace & 15) || ((uintptr_t)q & 1) || ((uintptr_t)lse & 3)) return KV_ERR_INVALID_ARG;
+  kvint2::DecodePlan pl = kvint2::plan_decode_int2(p, B, max_hist_len, T);
+  if (workspace_bytes < pl.bytes) return KV_ERR_INVALID_ARG;
+  return cuda_status(kvint2::launch_decode_int2(p, layer, B, q, sink_len, hist_len, recent_len,
+                                                recent_start, page_table, max_pages_per_seq, pl,
+                                                softmax_scale, out, workspace,
+                                                static_cast<cudaStream_t>(stream), T, lse));
 }
 
 kv_status_t kv_decode_attention_bf16(kv_pool_t* pool, int32_t layer, int32_t B, const void* q,

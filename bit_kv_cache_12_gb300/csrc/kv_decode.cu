@@ -86,6 +86,11 @@ struct DecodeArgs {
   int Hq, Hkv, page_size;
   long long num_pages;
   int n_split, per_split, n_tier;
+  // T query positions per sequence: the kernel's G "heads" of a KV head are
+  // (t, h) pairs, t = head / Gq, h = head % Gq (Gq = Hq / Hkv); q and out are
+  // [B][T][Hq][128]; lse (optional) [B][T][Hq]
+  int T, Gq;
+  float* lse;
   float scale_log2;
   float* out;
   float* ws;
@@ -306,6 +311,7 @@ template <int G, int NW>
 __device__ void merge_parts(const DecodeArgs& a, int b, int g, int nparts, float* sm) {
   constexpr int NSUB = NW / G;                     // part subsets per output column quad
   const float* base = a.ws + (size_t)(b * a.Hkv + g) * nparts * G * kPart;
+  float* sM = sm;                                  // [8]
   float* sL = sm + 8;                              // [8]
   float* sacc = sm + 16;                           // [NSUB][G][128]
   float* sf = sacc + NSUB * G * 128;               // [nparts * G] m, then weights
@@ -328,7 +334,10 @@ __device__ void merge_parts(const DecodeArgs& a, int b, int g, int nparts, float
       L = fmaf(f, sl[s * G + warp], L);
     }
     L = warp_sum_xor(L, 1);
-    if (lane == 0) sL[warp] = L;
+    if (lane == 0) {
+      sM[warp] = M;
+      sL[warp] = L;
+    }
   }
   __syncthreads();
   {
@@ -353,7 +362,11 @@ __device__ void merge_parts(const DecodeArgs& a, int b, int g, int nparts, float
 #pragma unroll
     for (int u = 0; u < NSUB; ++u) O += sacc[u * G * 128 + idx];
     const float L = sL[hh];
-    a.out[((size_t)b * a.Hq + g * G + hh) * 128 + (idx & 127)] = (L > 0.f) ? O / L : 0.f;
+    const size_t row = ((size_t)b * a.T + hh / a.Gq) * a.Hq + g * a.Gq + hh % a.Gq;
+    a.out[row * 128 + (idx & 127)] = (L > 0.f) ? O / L : 0.f;
+    // ln sum exp(scaled score) = ln 2 * (M + log2 L), the scores being in log2 units
+    if (a.lse && (idx & 127) == 0)
+      a.lse[row] = (L > 0.f) ? 0.6931471805599453f * (sM[hh] + log2f(L)) : kNegInf;
   }
   if (threadIdx.x == 0) a.tickets[b * a.Hkv + g] = 0u;   // ready for the next call
 }
@@ -497,7 +510,10 @@ __device__ void load_q(const DecodeArgs& a, int b, int g, float* sq, int padded_
   for (int idx = threadIdx.x; idx < padded_heads * 128; idx += NW * 32) {
     const int h = idx >> 7, c = idx & 127;
     float v = 0.f;
-    if (h < G) v = __uint_as_float((uint32_t)a.q[((size_t)b * a.Hq + g * G + h) * 128 + c] << 16);
+    if (h < G) {
+      const size_t row = ((size_t)b * a.T + h / a.Gq) * a.Hq + g * a.Gq + h % a.Gq;
+      v = __uint_as_float((uint32_t)a.q[row * 128 + c] << 16);
+    }
     sq[idx] = v;
   }
 }
@@ -1087,12 +1103,15 @@ DecodeArgs base_args(const Pool& p, int layer, const void* q, const int32_t* pt,
   a.ws = static_cast<float*>(ws);
   a.tickets = p.tickets + (size_t)layer * p.cfg.max_seqs * p.cfg.num_kv_heads;
   a.err = p.err;
+  a.T = 1;
+  a.Gq = p.G;
+  a.lse = nullptr;
   return a;
 }
 
-int int2_occupancy(const Pool& p) {
+int int2_occupancy(const Pool& p, int G) {
   const bool g64 = p.cfg.group_size == 64;
-  switch (p.G) {
+  switch (G) {
     case 1: return g64 ? int2_blocks_per_sm<1, 64>() : int2_blocks_per_sm<1, 128>();
     case 2: return g64 ? int2_blocks_per_sm<2, 64>() : int2_blocks_per_sm<2, 128>();
     case 4: return g64 ? int2_blocks_per_sm<4, 64>() : int2_blocks_per_sm<4, 128>();
@@ -1160,7 +1179,7 @@ cudaError_t noalloc_scratch(void** ptr, size_t* bytes) {
 // Splits per (sequence, KV head): fill exactly one wave of resident CTAs when
 // the batch is small; cap the work of one split (and the number of parts the
 // final merge reads) when it is large.
-static DecodePlan make_plan(const Pool& p, int B, int units, int max_per, int n_extra,
+static DecodePlan make_plan(const Pool& p, int G, int B, int units, int max_per, int n_extra,
                             int per_sm) {
   DecodePlan pl;
   const int pairs = B * p.cfg.num_kv_heads;
@@ -1175,27 +1194,31 @@ static DecodePlan make_plan(const Pool& p, int B, int units, int max_per, int n_
   pl.n_split = ns;
   pl.n_tier = n_extra;
   pl.tiles_per_split = per;
-  pl.partial_floats = (size_t)pairs * (ns + n_extra) * p.G * kPart;
+  pl.partial_floats = (size_t)pairs * (ns + n_extra) * G * kPart;
   pl.bytes = pl.partial_floats * sizeof(float);
   return pl;
 }
 
-DecodePlan plan_decode_int2(const Pool& p, int B, int max_hist_len) {
+DecodePlan plan_decode_int2(const Pool& p, int B, int max_hist_len, int T) {
+  const int G = T * p.G;   // query columns per KV head
   const int tiles = (max(max_hist_len, 0) + kTile - 1) / kTile;
   const int n_tier = max(1, (p.cfg.sink_tokens + p.cfg.recent_tokens + kTierRows - 1) / kTierRows);
-  return make_plan(p, B, tiles, 64 * int2_warps(p.G), n_tier, int2_occupancy(p));
+  return make_plan(p, G, B, tiles, 64 * int2_warps(G), n_tier, int2_occupancy(p, G));
 }
 
 DecodePlan plan_decode_bf16(const Pool& p, int B, int max_len) {
-  return make_plan(p, B, max(max_len, 0), 8192, 0, bf16_occupancy(p));
+  return make_plan(p, p.G, B, max(max_len, 0), 8192, 0, bf16_occupancy(p));
 }
 
 cudaError_t launch_decode_int2(const Pool& p, int layer, int B, const void* q,
                                const int32_t* sink_len, const int32_t* hist_len,
                                const int32_t* rec_len, const int32_t* rec_start,
                                const int32_t* pt, int max_pages, const DecodePlan& plan,
-                               float scale, float* out, void* ws, cudaStream_t s) {
+                               float scale, float* out, void* ws, cudaStream_t s, int T,
+                               float* lse) {
   DecodeArgs a = base_args(p, layer, q, pt, max_pages, scale, out, ws);
+  a.T = T;
+  a.lse = lse;
   a.hist = p.hist + (size_t)layer * p.hist_layer_stride;
   a.page_bytes = p.page_bytes;
   a.tile_bytes = (int)p.tile_bytes;
@@ -1217,7 +1240,7 @@ cudaError_t launch_decode_int2(const Pool& p, int layer, int B, const void* q,
   a.per_split = plan.tiles_per_split;
   a.n_tier = plan.n_tier;
   const bool g64 = p.cfg.group_size == 64;
-  switch (p.G) {
+  switch (T * p.G) {
     case 1: return g64 ? launch_int2_t<1, 64>(a, B, s) : launch_int2_t<1, 128>(a, B, s);
     case 2: return g64 ? launch_int2_t<2, 64>(a, B, s) : launch_int2_t<2, 128>(a, B, s);
     case 4: return g64 ? launch_int2_t<4, 64>(a, B, s) : launch_int2_t<4, 128>(a, B, s);

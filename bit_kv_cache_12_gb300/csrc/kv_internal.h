@@ -76,14 +76,16 @@ struct DecodePlan {
   size_t partial_floats = 0;
   size_t bytes = 0;
 };
-DecodePlan plan_decode_int2(const Pool& p, int B, int max_hist_len);
+// T query positions per sequence (T * G must be 1, 2, 4 or 8)
+DecodePlan plan_decode_int2(const Pool& p, int B, int max_hist_len, int T = 1);
 DecodePlan plan_decode_bf16(const Pool& p, int B, int max_len);
 
 cudaError_t launch_decode_int2(const Pool& p, int layer, int B, const void* q,
                                const int32_t* sink_len, const int32_t* hist_len,
                                const int32_t* rec_len, const int32_t* rec_start,
                                const int32_t* pt, int max_pages, const DecodePlan& plan,
-                               float scale, float* out, void* ws, cudaStream_t s);
+                               float scale, float* out, void* ws, cudaStream_t s, int T = 1,
+                               float* lse = nullptr);
 // Device address and size of the fixed scratch buffer used by
 // kv_decode_attention_noalloc on the current device (looked up once per device).
 cudaError_t noalloc_scratch(void** ptr, size_t* bytes);

@@ -63,6 +63,9 @@ _SIG = {
     "kv_quantize_pack_f32": (_I32, [_P, _I32, _I32, _I64, _P, _P, _P, _P]),
     "kv_append_quantize": (_I32, [_P, _I32, _I32, _P, _P, _P, _P, _P, _I32, _I32, _P]),
     "kv_append_step": (_I32, [_P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _I32, _P]),
+    "kv_decode_multi_workspace_bytes": (ctypes.c_size_t, [_P, _I32, _I32, _I32]),
+    "kv_decode_attention_multi": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _I32, _I32,
+                                         ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]),
     "kv_decode_workspace_bytes": (ctypes.c_size_t, [_P, _I32, _I32]),
     "kv_decode_attention": (_I32, [_P, _I32, _I32, _P, _P, _P, _P, _P, _P, _I32, _I32,
                                    ctypes.c_float, _P, _P, ctypes.c_size_t, _P]),
@@ -174,6 +177,19 @@ def kv_append_step(pool, layer, B, k_new, v_new, sink_len, hist_len, recent_len,
     _check("kv_append_step", lib().kv_append_step(
         pool, layer, B, _ptr(k_new), _ptr(v_new), _ptr(sink_len), _ptr(hist_len), _ptr(recent_len),
         _ptr(recent_start), _ptr(page_table), max_pages_per_seq, _stream(stream)))
+
+
+def kv_decode_multi_workspace_bytes(pool, B, T, max_hist_len):
+    return lib().kv_decode_multi_workspace_bytes(pool, B, T, max_hist_len)
+
+
+def kv_decode_attention_multi(pool, layer, B, T, q, sink_len, hist_len, recent_len, recent_start,
+                              page_table, max_pages_per_seq, max_hist_len, softmax_scale, out,
+                              lse, workspace, workspace_bytes, stream=None):
+    _check("kv_decode_attention_multi", lib().kv_decode_attention_multi(
+        pool, layer, B, T, _ptr(q), _ptr(sink_len), _ptr(hist_len), _ptr(recent_len),
+        _ptr(recent_start), _ptr(page_table), max_pages_per_seq, max_hist_len, softmax_scale,
+        _ptr(out), _ptr(lse), _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def kv_decode_workspace_bytes(pool, B, max_len):

@@ -187,6 +187,33 @@ kv_status_t kv_append_quantize(kv_pool_t* pool, int32_t layer, int32_t n_seqs,
                                int32_t max_pages_per_seq, int32_t max_tokens_per_seq,
                                void* stream);
 
+/* Several query positions per sequence over the same cache: a chunk of
+ * prefill continuing on an INT2 prefix, prefix-cache reuse, or draft tokens
+ * being verified (zingnex.cn forum summary of OSCAR, "与其他优化的协同";
+ * yunpan.plus write-up, "3. 兼容现有架构").  Each of the T queries of
+ * sequence b attends, like kv_decode_attention, over the whole cache of that
+ * sequence (sink, INT2 history, recent); there is no masking among the T
+ * queries.  The caller attends the chunk's own tokens itself and merges the
+ * two by the log-sum-exp rule using `lse`.
+ *   T        query positions per sequence; T * (num_q_heads / num_kv_heads)
+ *            must be 1, 2, 4 or 8 (else KV_ERR_UNSUPPORTED)
+ *   q        device bf16 [B][T][Hq][128]
+ *   out      device fp32 [B][T][Hq][128]
+ *   lse      device fp32 [B][T][Hq] or NULL: ln sum_t exp(softmax_scale * s_t)
+ *            over the cached tokens t (s_t the dot product the attention
+ *            uses); -inf when the sequence caches no token
+ *   other arguments as for kv_decode_attention; the workspace size comes
+ *   from kv_decode_multi_workspace_bytes. */
+size_t kv_decode_multi_workspace_bytes(const kv_pool_t* pool, int32_t B, int32_t T,
+                                       int32_t max_hist_len);
+kv_status_t kv_decode_attention_multi(kv_pool_t* pool, int32_t layer, int32_t B, int32_t T,
+                                      const void* q, const int32_t* sink_len,
+                                      const int32_t* hist_len, const int32_t* recent_len,
+                                      const int32_t* recent_start, const int32_t* page_table,
+                                      int32_t max_pages_per_seq, int32_t max_hist_len,
+                                      float softmax_scale, float* out, float* lse,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
 /* One decode step's token placement for B sequences (yunpan.plus write-up,
  * "1. 三段式 Token 池" and "2. 在线量化与反量化"): the new token of sequence b
  * (all KV heads) goes to the sink while it holds fewer than sink_tokens
