@@ -307,7 +307,7 @@ __device__ void rotate_back(float* io, float* sOt, const float* sR, float* spr) 
 // and the final normalisation.  Warp h < G forms head h's maximum and weighted
 // sum of l over the parts; then every warp accumulates a subset of the parts'
 // value vectors for one head and the subsets are added.
-template <int G, int NW>
+template <int G, int NW, bool kMulti>
 __device__ void merge_parts(const DecodeArgs& a, int b, int g, int nparts, float* sm) {
   constexpr int NSUB = NW / G;                     // part subsets per output column quad
   const float* base = a.ws + (size_t)(b * a.Hkv + g) * nparts * G * kPart;
@@ -362,11 +362,15 @@ __device__ void merge_parts(const DecodeArgs& a, int b, int g, int nparts, float
 #pragma unroll
     for (int u = 0; u < NSUB; ++u) O += sacc[u * G * 128 + idx];
     const float L = sL[hh];
-    const size_t row = ((size_t)b * a.T + hh / a.Gq) * a.Hq + g * a.Gq + hh % a.Gq;
-    a.out[row * 128 + (idx & 127)] = (L > 0.f) ? O / L : 0.f;
-    // ln sum exp(scaled score) = ln 2 * (M + log2 L), the scores being in log2 units
-    if (a.lse && (idx & 127) == 0)
-      a.lse[row] = (L > 0.f) ? 0.6931471805599453f * (sM[hh] + log2f(L)) : kNegInf;
+    if constexpr (kMulti) {
+      const size_t row = ((size_t)b * a.T + hh / a.Gq) * a.Hq + g * a.Gq + hh % a.Gq;
+      a.out[row * 128 + (idx & 127)] = (L > 0.f) ? O / L : 0.f;
+      // ln sum exp(scaled score) = ln 2 * (M + log2 L), the scores being in log2 units
+      if (a.lse && (idx & 127) == 0)
+        a.lse[row] = (L > 0.f) ? 0.6931471805599453f * (sM[hh] + log2f(L)) : kNegInf;
+    } else {
+      a.out[((size_t)b * a.Hq + g * G + hh) * 128 + (idx & 127)] = (L > 0.f) ? O / L : 0.f;
+    }
   }
   if (threadIdx.x == 0) a.tickets[b * a.Hkv + g] = 0u;   // ready for the next call
 }
@@ -505,13 +509,14 @@ __device__ void warp_acc_to_smem(WarpAcc<G>& st, float* swo, float* swm, float* 
 
 // q of the GQA group (bf16 -> fp32) into shared memory; padded heads are 0.
 // No barrier.
-template <int G, int NW>
+template <int G, int NW, bool kMulti = false>
 __device__ void load_q(const DecodeArgs& a, int b, int g, float* sq, int padded_heads) {
   for (int idx = threadIdx.x; idx < padded_heads * 128; idx += NW * 32) {
     const int h = idx >> 7, c = idx & 127;
     float v = 0.f;
     if (h < G) {
-      const size_t row = ((size_t)b * a.T + h / a.Gq) * a.Hq + g * a.Gq + h % a.Gq;
+      const size_t row = kMulti ? ((size_t)b * a.T + h / a.Gq) * a.Hq + g * a.Gq + h % a.Gq
+                                : (size_t)b * a.Hq + g * G + h;
       v = __uint_as_float((uint32_t)a.q[row * 128 + c] << 16);
     }
     sq[idx] = v;
@@ -521,7 +526,7 @@ __device__ void load_q(const DecodeArgs& a, int b, int g, float* sq, int padded_
 // ---------------------------------------------------------------------------
 // INT2 history split (the hot loop)
 // ---------------------------------------------------------------------------
-template <int G, int GS>
+template <int G, int GS, bool kMulti>
 __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float* sm,
                              float* part) {
   constexpr int NW = int2_warps(G);
@@ -542,7 +547,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
   float* sq = sm + S::sq;
   float* sqr = sm + S::sqr;
   float* ssum = sm + S::ssum;
-  load_q<G, NW>(a, b, g, sq, S::HP);
+  load_q<G, NW, kMulti>(a, b, g, sq, S::HP);
   int h = __ldg(a.hist_len + b);
   __syncthreads();
   const int cap = a.max_pages * a.page_size;
@@ -843,7 +848,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
 // rows [ti*kTierRows, ...) of [sink slots | recent ring] before it knows the
 // lengths, then attends over the rows that hold live tokens.
 // ---------------------------------------------------------------------------
-template <int G, int GS>
+template <int G, int GS, bool kMulti>
 __device__ void bf16_tiers(const DecodeArgs& a, int b, int g, int ti, float* sm, float* part) {
   constexpr int NW = int2_warps(G);
   using S = Lay<G, GS, NW, true>;
@@ -866,7 +871,7 @@ __device__ void bf16_tiers(const DecodeArgs& a, int b, int g, int ti, float* sm,
   }
   cp_async_commit();
   float* sq = sm + S::sq;
-  load_q<G, NW>(a, b, g, sq, G);
+  load_q<G, NW, kMulti>(a, b, g, sq, G);
   int ns = __ldg(a.sink_len + b), nr = __ldg(a.rec_len + b), rs = __ldg(a.rec_start + b);
   cp_async_wait<0>();
   __syncthreads();
@@ -900,7 +905,7 @@ __device__ void bf16_tiers(const DecodeArgs& a, int b, int g, int ti, float* sm,
   write_partial<G, NW>(part, sm + S::sqr, sm + S::smm, sm + S::sml);
 }
 
-template <int G, int GS>
+template <int G, int GS, bool kMulti>
 __global__ void __launch_bounds__(int2_warps(G) * 32, 1) decode_int2_kernel(DecodeArgs a) {
   constexpr int NW = int2_warps(G);
   extern __shared__ float4 smem4[];
@@ -909,11 +914,11 @@ __global__ void __launch_bounds__(int2_warps(G) * 32, 1) decode_int2_kernel(Deco
   const int nparts = a.n_split + a.n_tier;
   float* part = a.ws + ((size_t)(b * a.Hkv + g) * nparts + split) * G * kPart;
   if (split < a.n_split)
-    int2_history<G, GS>(a, b, g, split, sm, part);
+    int2_history<G, GS, kMulti>(a, b, g, split, sm, part);
   else
-    bf16_tiers<G, GS>(a, b, g, split - a.n_split, sm, part);
+    bf16_tiers<G, GS, kMulti>(a, b, g, split - a.n_split, sm, part);
   if (last_to_arrive(a.tickets + b * a.Hkv + g, (unsigned)nparts))
-    merge_parts<G, NW>(a, b, g, nparts, sm);
+    merge_parts<G, NW, kMulti>(a, b, g, nparts, sm);
 }
 
 // ---------------------------------------------------------------------------
@@ -1057,11 +1062,11 @@ constexpr size_t bf16_smem() {
   return sizeof(float) * Lay<G, 128, kBf16Warps, false>::total;
 }
 
-template <int G, int GS>
+template <int G, int GS, bool kMulti>
 int int2_blocks_per_sm() {
   static bool done = false;
   static int per_sm = 1;
-  return prepare_kernel(decode_int2_kernel<G, GS>, int2_warps(G) * 32, int2_smem<G, GS>(), done,
+  return prepare_kernel(decode_int2_kernel<G, GS, kMulti>, int2_warps(G) * 32, int2_smem<G, GS>(), done,
                         per_sm);
 }
 
@@ -1072,11 +1077,11 @@ int bf16_blocks_per_sm() {
   return prepare_kernel(decode_bf16_kernel<G>, kBf16Warps * 32, bf16_smem<G>(), done, per_sm);
 }
 
-template <int G, int GS>
+template <int G, int GS, bool kMulti>
 cudaError_t launch_int2_t(const DecodeArgs& a, int B, cudaStream_t s) {
-  if (int2_blocks_per_sm<G, GS>() < 0) return cudaErrorInvalidConfiguration;
+  if (int2_blocks_per_sm<G, GS, kMulti>() < 0) return cudaErrorInvalidConfiguration;
   dim3 grid(a.n_split + a.n_tier, a.Hkv, B);
-  decode_int2_kernel<G, GS><<<grid, int2_warps(G) * 32, int2_smem<G, GS>(), s>>>(a);
+  decode_int2_kernel<G, GS, kMulti><<<grid, int2_warps(G) * 32, int2_smem<G, GS>(), s>>>(a);
   return cudaGetLastError();
 }
 
@@ -1109,13 +1114,14 @@ DecodeArgs base_args(const Pool& p, int layer, const void* q, const int32_t* pt,
   return a;
 }
 
-int int2_occupancy(const Pool& p, int G) {
+template <bool kMulti>
+int int2_occupancy_t(const Pool& p, int G) {
   const bool g64 = p.cfg.group_size == 64;
   switch (G) {
-    case 1: return g64 ? int2_blocks_per_sm<1, 64>() : int2_blocks_per_sm<1, 128>();
-    case 2: return g64 ? int2_blocks_per_sm<2, 64>() : int2_blocks_per_sm<2, 128>();
-    case 4: return g64 ? int2_blocks_per_sm<4, 64>() : int2_blocks_per_sm<4, 128>();
-    default: return g64 ? int2_blocks_per_sm<8, 64>() : int2_blocks_per_sm<8, 128>();
+    case 1: return g64 ? int2_blocks_per_sm<1, 64, kMulti>() : int2_blocks_per_sm<1, 128, kMulti>();
+    case 2: return g64 ? int2_blocks_per_sm<2, 64, kMulti>() : int2_blocks_per_sm<2, 128, kMulti>();
+    case 4: return g64 ? int2_blocks_per_sm<4, 64, kMulti>() : int2_blocks_per_sm<4, 128, kMulti>();
+    default: return g64 ? int2_blocks_per_sm<8, 64, kMulti>() : int2_blocks_per_sm<8, 128, kMulti>();
   }
 }
 
@@ -1203,7 +1209,8 @@ DecodePlan plan_decode_int2(const Pool& p, int B, int max_hist_len, int T) {
   const int G = T * p.G;   // query columns per KV head
   const int tiles = (max(max_hist_len, 0) + kTile - 1) / kTile;
   const int n_tier = max(1, (p.cfg.sink_tokens + p.cfg.recent_tokens + kTierRows - 1) / kTierRows);
-  return make_plan(p, G, B, tiles, 64 * int2_warps(G), n_tier, int2_occupancy(p, G));
+  const int per_sm = (T > 1) ? int2_occupancy_t<true>(p, G) : int2_occupancy_t<false>(p, G);
+  return make_plan(p, G, B, tiles, 64 * int2_warps(G), n_tier, per_sm);
 }
 
 DecodePlan plan_decode_bf16(const Pool& p, int B, int max_len) {
@@ -1240,11 +1247,20 @@ cudaError_t launch_decode_int2(const Pool& p, int layer, int B, const void* q,
   a.per_split = plan.tiles_per_split;
   a.n_tier = plan.n_tier;
   const bool g64 = p.cfg.group_size == 64;
-  switch (T * p.G) {
-    case 1: return g64 ? launch_int2_t<1, 64>(a, B, s) : launch_int2_t<1, 128>(a, B, s);
-    case 2: return g64 ? launch_int2_t<2, 64>(a, B, s) : launch_int2_t<2, 128>(a, B, s);
-    case 4: return g64 ? launch_int2_t<4, 64>(a, B, s) : launch_int2_t<4, 128>(a, B, s);
-    case 8: return g64 ? launch_int2_t<8, 64>(a, B, s) : launch_int2_t<8, 128>(a, B, s);
+  if (T > 1 || lse) {   // several queries per sequence, or the log-sum-exp wanted
+    switch (T * p.G) {
+      case 1: return g64 ? launch_int2_t<1, 64, true>(a, B, s) : launch_int2_t<1, 128, true>(a, B, s);
+      case 2: return g64 ? launch_int2_t<2, 64, true>(a, B, s) : launch_int2_t<2, 128, true>(a, B, s);
+      case 4: return g64 ? launch_int2_t<4, 64, true>(a, B, s) : launch_int2_t<4, 128, true>(a, B, s);
+      case 8: return g64 ? launch_int2_t<8, 64, true>(a, B, s) : launch_int2_t<8, 128, true>(a, B, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  switch (p.G) {
+    case 1: return g64 ? launch_int2_t<1, 64, false>(a, B, s) : launch_int2_t<1, 128, false>(a, B, s);
+    case 2: return g64 ? launch_int2_t<2, 64, false>(a, B, s) : launch_int2_t<2, 128, false>(a, B, s);
+    case 4: return g64 ? launch_int2_t<4, 64, false>(a, B, s) : launch_int2_t<4, 128, false>(a, B, s);
+    case 8: return g64 ? launch_int2_t<8, 64, false>(a, B, s) : launch_int2_t<8, 128, false>(a, B, s);
     default: return cudaErrorInvalidValue;
   }
 }
