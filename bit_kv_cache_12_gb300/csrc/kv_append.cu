@@ -168,7 +168,7 @@ __device__ __forceinline__ void append_tile(const uint4* frag, const float* clip
     for (int nt = 0; nt < 16; ++nt) {
       const int grp = (GS == 64) ? (nt >> 3) : 0;
       const int w = nt >> 2;
-      const int pi0 = 4 * ((nt >> 1) & 1) + 2 * (nt & 1);   // row r; row r+8 adds 1
+      const int pi0 = 2 * ((nt >> 1) & 1) + 4 * (nt & 1);   // row r; row r+8 adds 1
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const uint32_t ca = quant_code(acc[nt][e], q[0][grp]);
@@ -261,7 +261,7 @@ __device__ __forceinline__ void append_tile(const uint4* frag, const float* clip
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int pi0 = 4 * (i & 1) + 2 * nt;               // channel 16i+r; +8 adds 1
+          const int pi0 = 2 * (i & 1) + 4 * nt;               // channel 16i+r; +8 adds 1
           const uint32_t ca = quant_code(acc[i][nt][e], q[nt][e][grp]);
           const uint32_t cb = quant_code(acc[i][nt][2 + e], q[nt][e][grp]);
           const int bit_a = 16 * e + 2 * pi0, bit_b = 16 * e + 2 * (pi0 + 1);

@@ -12,25 +12,27 @@
 //   count fills one wave when the batch is small.
 //   * history CTAs: one round of loads (page ids of the split, q, length),
 //     then each warp streams 16-token tiles from HBM through a 4-stage
-//     shared-memory ring filled by 16-byte cp.async copies (each lane copies
-//     and later reads only its own bytes, so no barrier is needed) while
-//     q' = q R_k runs on the tensor cores; the 2-bit codes are unpacked into
-//     fp16 MMA fragments with one lop3 + one fma per code pair, and QK and PV
-//     run on the tensor cores (mma.sync m16n8k16).  Dequantization is folded:
-//       q'.deq(k) = s_k (q'.(c_k - 1)) + (z_k + s_k) sum(q')
-//       sum_t w_t deq(v_t) = sum_t (w_t s_v)(c_v - 1) + sum_t w_t (z_v + s_v)
-//     so the MMA operands are small exact integers and the query / softmax
-//     weights enter as fp16 hi + lo pairs (about 22 significant bits).
-//     Online softmax per head with warp-shuffle max and a lazily moved
-//     exponent reference; per-CTA merge in shared memory; the partial stays
-//     in the rotated basis.
+//     shared-memory ring, one bulk copy per tile completing on the stage's
+//     mbarrier (bounded waits), while q' = q R_k runs on the tensor cores.
+//     The 2-bit codes become fp16 MMA fragments by masking alone (exact
+//     subnormals, one logic op per code pair) and QK and PV run on the tensor
+//     cores (mma.sync m16n8k16).  Dequantization is folded:
+//       q'.deq(k) = s_k (q'.c_k) + z_k sum(q')
+//       sum_t w_t deq(v_t) = sum_t (w_t s_v) c_v + sum_t w_t z_v
+//     so the MMA operands are exact small integers times powers of two and the
+//     query / softmax weights enter as fp16 hi + lo pairs.  Against subnormal
+//     code operands the tensor cores keep only the upper bits of the lo
+//     products (about 16 significant bits overall; measured output error
+//     about 2e-5 relative to the fp64 oracle at 100k tokens).  Online softmax per head with warp-shuffle max and a
+//     lazily moved exponent reference; per-CTA merge in shared memory; each
+//     CTA rotates its partial back by R_v^T (fp32, bulk-copied to shared
+//     memory at the start).
 //   * tier CTAs: stage their slice of the BF16 sink + recent storage into
 //     shared memory in the same first round (valid rows are picked once the
 //     lengths arrive; softmax order does not matter) and attend in SIMT fp32.
 //   * the last CTA of each (sequence, KV head), found by an atomic ticket (no
-//     waiting), merges all partials with the log-sum-exp rule, rotates the
-//     history sum back by R_v^T once (fp32, R_v^T staged in shared memory in
-//     the same round as the partials' loads) and writes the fp32 output.
+//     waiting), merges all partials with the log-sum-exp rule and writes the
+//     fp32 output (and, for several queries per sequence, the log-sum-exp).
 #include <math.h>
 
 #include <atomic>
@@ -619,7 +621,10 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const float* row = sqr + (4 * nt + hl) * 128 + 16 * s + 2 * j;
-        const float x[4] = {row[0], row[1], row[8], row[9]};
+        // group 64: the odd steps' code factor 16 is cancelled here (a power of 2);
+        // group 128 removes it from the odd steps' accumulator chain instead
+        const float f = (GS == 64 && (s & 1)) ? 0.0625f : 1.0f;
+        const float x[4] = {row[0] * f, row[1] * f, row[8] * f, row[9] * f};
         __half p[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -630,11 +635,13 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
         qf[s][nt][1] = h2_as_u32(__halves2half2(p[2], p[3]));
       }
   }
+  // per-group sums of q' in the units of the score accumulator (2^-24)
   float sumq[NT][NG];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int grp = 0; grp < NG; ++grp) sumq[nt][grp] = ssum[(4 * nt + j) * 2 + grp];
+    for (int grp = 0; grp < NG; ++grp) sumq[nt][grp] = ssum[(4 * nt + j) * 2 + grp] * 5.9604644775390625e-8f;
+  const float sc24 = a.scale_log2 * 16777216.0f;   // 2^24 back on the scores
 
   float m_run[NT], l_run[NT], zs[NT][NG], oacc[8][NT][4];
 #pragma unroll
@@ -692,6 +699,16 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
       sv[1][0] = __low2float(u32_as_h2(s1.z)); zv[1][0] = __high2float(u32_as_h2(s1.z));
       sv[1][NG - 1] = __low2float(u32_as_h2(s1.w)); zv[1][NG - 1] = __high2float(u32_as_h2(s1.w));
     }
+    // token r+8 sits in the score rows with the codes' row factor 4; in PV it
+    // is in the upper k half, whose codes arrive as 3 - c: its weight enters
+    // negated and its zero point becomes z + 3 s, so that
+    //   w (s c + z) = (-w s)(3 - c) + w (z + 3 s)
+#pragma unroll
+    for (int grp = 0; grp < NG; ++grp) {
+      sk[1][grp] *= 0.25f;
+      zv[1][grp] = fmaf(3.0f, sv[1][grp], zv[1][grp]);
+      sv[1][grp] = -sv[1][grp];
+    }
 
     // ---- QK: scores[token][column] on the tensor cores ----
     // two independent accumulator chains: the two groups (group 64) or the
@@ -708,14 +725,14 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         uint32_t fr[8];
-        unpack_word(kw[w], fr);
+        unpack_word<false>(kw[w], fr);
 #pragma unroll
         for (int sh = 0; sh < 2; ++sh) {
           const int s = 2 * w + sh;
           const int ch = (GS == 64) ? (s >> 2) : (s & 1);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
-            mma_f16(sacc[ch][nt], fr[4 * sh + 0], fr[4 * sh + 1], fr[4 * sh + 2], fr[4 * sh + 3],
+            mma_f16(sacc[ch][nt], fr[2 * sh], fr[2 * sh + 1], fr[4 + 2 * sh], fr[5 + 2 * sh],
                     qf[s][nt][0], qf[s][nt][1]);
         }
       }
@@ -733,14 +750,16 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
           d0 = sacc[grp][nt][0] + sacc[grp][nt][1];
           d1 = sacc[grp][nt][2] + sacc[grp][nt][3];
         } else {
-          d0 = (sacc[0][nt][0] + sacc[1][nt][0]) + (sacc[0][nt][1] + sacc[1][nt][1]);
-          d1 = (sacc[0][nt][2] + sacc[1][nt][2]) + (sacc[0][nt][3] + sacc[1][nt][3]);
+          // chain 1 holds the odd steps, whose codes carry the factor 16
+          d0 = fmaf(sacc[1][nt][0] + sacc[1][nt][1], 0.0625f, sacc[0][nt][0] + sacc[0][nt][1]);
+          d1 = fmaf(sacc[1][nt][2] + sacc[1][nt][3], 0.0625f, sacc[0][nt][2] + sacc[0][nt][3]);
         }
-        l0 += sk[0][grp] * d0 + (zk[0][grp] + sk[0][grp]) * sumq[nt][grp];
-        l1 += sk[1][grp] * d1 + (zk[1][grp] + sk[1][grp]) * sumq[nt][grp];
+        // q'.(s c + z) = s (q'.c) + z sum(q')
+        l0 = fmaf(sk[0][grp], d0, fmaf(zk[0][grp], sumq[nt][grp], l0));
+        l1 = fmaf(sk[1][grp], d1, fmaf(zk[1][grp], sumq[nt][grp], l1));
       }
-      l0 = v0 ? l0 * a.scale_log2 : kNegInf;
-      l1 = v1 ? l1 * a.scale_log2 : kNegInf;
+      l0 = v0 ? l0 * sc24 : kNegInf;
+      l1 = v1 ? l1 * sc24 : kNegInf;
       // m_run is the exponent reference (>= every score seen so far); it only
       // moves when some score of the warp exceeds its head's reference, so the
       // per-head maximum is formed only then
@@ -769,7 +788,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
       for (int grp = 0; grp < NG; ++grp) {
         const float w0 = p0 * sv[0][grp];
         const float w1 = p1 * sv[1][grp];
-        zs[nt][grp] = fmaf(p0, zv[0][grp] + sv[0][grp], fmaf(p1, zv[1][grp] + sv[1][grp], zs[nt][grp]));
+        zs[nt][grp] = fmaf(p0, zv[0][grp], fmaf(p1, zv[1][grp], zs[nt][grp]));
         bpv[grp][nt][0] = movmatrix_t(split_hi_lo(w0));
         bpv[grp][nt][1] = movmatrix_t(split_hi_lo(w1));
       }
@@ -781,14 +800,14 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         uint32_t fr[8];
-        unpack_word(vw[w], fr);
+        unpack_word<true>(vw[w], fr);
 #pragma unroll
         for (int sh = 0; sh < 2; ++sh) {
           const int i = 2 * w + sh;
           const int grp = (GS == 64) ? (i >> 2) : 0;
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
-            mma_f16(oacc[i][nt], fr[4 * sh + 0], fr[4 * sh + 1], fr[4 * sh + 2], fr[4 * sh + 3],
+            mma_f16(oacc[i][nt], fr[2 * sh], fr[2 * sh + 1], fr[4 + 2 * sh], fr[5 + 2 * sh],
                     bpv[grp][nt][0], bpv[grp][nt][1]);
         }
       }
@@ -827,8 +846,11 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float zz = z[(GS == 64) ? (i >> 2) : 0];
-        o[16 * i + r] = oacc[i][nt][0] + oacc[i][nt][1] + zz;
-        o[16 * i + r + 8] = oacc[i][nt][2] + oacc[i][nt][3] + zz;
+        // channel rows carry the codes' 2^-24, row factor 4 for r+8 and step
+        // factor 16 for odd i
+        const float u = (i & 1) ? 1048576.0f : 16777216.0f;
+        o[16 * i + r] = fmaf(oacc[i][nt][0] + oacc[i][nt][1], u, zz);
+        o[16 * i + r + 8] = fmaf(oacc[i][nt][2] + oacc[i][nt][3], u * 0.25f, zz);
       }
       if (r == 0) {
         swm[warp * G + hh] = m_run[nt];

@@ -180,41 +180,27 @@ __device__ __forceinline__ uint32_t split_hi_lo(float x) {
   return h2_as_u32(__halves2half2(h, __float2half_rn(r)));
 }
 
-// lop3 (a & b) | c
-__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-
-// Extract the 2-bit codes at bit pair position pi (0..4) of both 16-bit halves
-// of w as (code - 1) in fp16: OR the bits into the mantissa of 1024, then one
-// exact fma removes the 1024 bias and the 4^pi weight.
-template <int PI>
-__device__ __forceinline__ uint32_t codes_m1(uint32_t w) {
-  static_assert(PI >= 0 && PI <= 4, "mantissa position");
-  constexpr uint32_t mask = 0x00030003u << (2 * PI);
-  uint32_t x = and_or(w, mask, 0x64006400u);
-  // constants: 4^-PI and -(1024 * 4^-PI + 1), both exact in fp16
-  constexpr unsigned short kMul[5] = {0x3C00, 0x3400, 0x2C00, 0x2400, 0x1C00};
-  constexpr unsigned short kAdd[5] = {0xE401, 0xDC04, 0xD410, 0xCC40, 0xC500};
-  __half2 m = __halves2half2(__ushort_as_half(kMul[PI]), __ushort_as_half(kMul[PI]));
-  __half2 a = __halves2half2(__ushort_as_half(kAdd[PI]), __ushort_as_half(kAdd[PI]));
-  return h2_as_u32(__hfma2(u32_as_h2(x), m, a));
-}
-
-// All eight f16x2 registers of one 32-bit code word: reg pi holds the codes at
-// bit pairs pi (low half) and 8+pi (high half), as (code - 1).
+// All eight f16x2 MMA registers of one 32-bit code word, as exact fp16
+// subnormals.  Below 2^-14 an fp16 bit pattern read as an integer is the value
+// in units of 2^-24, so masking one 2-bit field of each half is the whole
+// conversion.  Register m (0..3) holds the codes at bit pairs m (low half) and
+// 8+m (high half), register 4+m those at pairs 4+m and 12+m (taken from the
+// word shifted right by 8); both carry the weight 4^m * 2^-24.  The stored
+// order puts the A fragment of an even step at pairs {0, 1, 4, 5} and of an
+// odd step at {2, 3, 6, 7}, so {a0, a1, a2, a3} weigh {1, 4, 1, 4} x 2^-24,
+// times 16 for an odd step: a factor per MMA row half and per step, never
+// per k, which the caller removes outside the MMA.  With kFlipHi the upper
+// k half (a2, a3: registers 4..7) holds 3 - c instead of c, still one logic
+// op (and-not); a caller that negates B's upper k half then accumulates
+// sum_lo c w - sum_hi (3 - c) w, whose terms have no common sign.
+template <bool kFlipHi>
 __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t (&r)[8]) {
-  r[0] = codes_m1<0>(w);
-  r[1] = codes_m1<1>(w);
-  r[2] = codes_m1<2>(w);
-  r[3] = codes_m1<3>(w);
-  r[4] = codes_m1<4>(w);
-  uint32_t w5 = w >> 10;
-  r[5] = codes_m1<0>(w5);
-  r[6] = codes_m1<1>(w5);
-  r[7] = codes_m1<2>(w5);
+  const uint32_t w8 = kFlipHi ? ~(w >> 8) : (w >> 8);
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    r[m] = w & (0x00030003u << (2 * m));
+    r[4 + m] = w8 & (0x00030003u << (2 * m));
+  }
 }
 
 // 2^x for x <= 0 (softmax weights): the hardware approximation, relative

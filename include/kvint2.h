@@ -91,7 +91,7 @@ typedef struct {
  *     per group (s_v, z_v); record slot 2*(t%8) + t/8 holds token t of the tile.
  *     Code bit of (m, k, step) with m, k in [0,16), step in [0,8): 16-byte
  *     lane L = 4*(m%8) + (k%8)/2, 32-bit little-endian word step/2, bit
- *     16*(k%2) + 2*(4*(step%2) + m/8 + 2*(k/8)); K: m = token, k = channel%16,
+ *     16*(k%2) + 2*(2*(step%2) + m/8 + 4*(k/8)); K: m = token, k = channel%16,
  *     step = channel/16; V: m = channel%16, k = token, step = channel/16.
  *   sink_k / sink_v:   bf16 [max_seqs][Hkv][sink_tokens][128]
  *   recent_k/recent_v: bf16 [max_seqs][Hkv][recent_tokens][128] (ring)

@@ -157,7 +157,7 @@ def unpack_canonical(packed):
 # index a 16 x 16 block, step in [0,8) selects one of the eight blocks that
 # tile the 16 x 128 slab.  Its bit lies in the 16-byte group of "lane"
 # L = 4*(m % 8) + (k % 8) // 2, in 32-bit little-endian word w = step // 2,
-# at bit 16*(k % 2) + 2*pi with pi = 4*(step % 2) + (m // 8) + 2*(k // 8).
+# at bit 16*(k % 2) + 2*pi with pi = 2*(step % 2) + (m // 8) + 4*(k // 8).
 #   K tile: m = token, k = channel % 16, step = channel // 16
 #   V tile: m = channel % 16, k = token, step = channel // 16
 
@@ -166,7 +166,7 @@ def tile_code_bit(m, k, step):
     m = np.asarray(m); k = np.asarray(k); step = np.asarray(step)
     lane = 4 * (m % 8) + (k % 8) // 2
     word = step // 2
-    pi = 4 * (step % 2) + (m // 8) + 2 * (k // 8)
+    pi = 2 * (step % 2) + (m // 8) + 4 * (k // 8)
     bit = 16 * (k % 2) + 2 * pi
     byte = 16 * lane + 4 * word + bit // 8
     return byte, bit % 8
