@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "libkvint2.so")
-SOURCES = ["kv_api.cu", "kv_append.cu", "kv_decode.cu"]
+SOURCES = ["kv_api.cu", "kv_append.cu", "kv_append_tc.cu", "kv_decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -5,13 +5,19 @@
 // codes per byte, into the INT2 history); gist.science OSCAR explainer,
 // section 2.2 B (history is stored after the fixed rotation and the clip).
 //
-// GPU design: a warp owns one 16-token tile of one KV head and one tensor.
-// The rotation x' = x R runs on the tensor cores (mma.sync m16n8k16 bf16):
-// x is exact in bf16 and R is split into bf16 hi + lo terms, fp32 accumulate.
-// The MMA accumulator layout is arranged so that each lane ends up owning
-// exactly the 64 codes of its own 16-byte slot of the stored tile (K: x R with
-// tokens as rows; V: R^T x^T with channels as rows), so packing is lane-local
-// and every tile is written with one 16-byte store per lane.
+// This file holds the per-step placement (a new token per sequence into the
+// sink or the recent ring, the evicted token into INT2 history), the parity
+// entry (quantize + canonical pack of rotated fp32 rows), the rotation set-up
+// and the BF16 stores; the bulk append runs on tcgen05 (kv_append_tc.cu).
+//
+// Per-step eviction: a warp owns the one 16-token tile of one KV head and one
+// tensor that the evicted token lands in.  The rotation x' = x R runs on the
+// tensor cores (mma.sync m16n8k16 bf16): x is exact in bf16 and R is split
+// into bf16 hi + lo terms, fp32 accumulate.  The MMA accumulator layout is
+// arranged so that each lane ends up owning exactly the 64 codes of its own
+// 16-byte slot of the stored tile (K: x R with tokens as rows; V: R^T x^T
+// with channels as rows), so packing is lane-local; the bits of the tile's
+// other rows are kept.
 #include "kv_device.cuh"
 #include "kv_internal.h"
 
@@ -53,23 +59,6 @@ __global__ void quantize_pack_kernel(const float* __restrict__ x, const float* _
 // ---------------------------------------------------------------------------
 // fused append
 // ---------------------------------------------------------------------------
-struct AppendArgs {
-  uint8_t* hist;            // layer base
-  size_t page_bytes, head_block;
-  int tile_bytes, tiles_per_page, P;
-  const uint16_t* k;
-  const uint16_t* v;
-  const int32_t* cu;
-  const int32_t* hist_start;
-  const int32_t* pt;
-  int max_pages, n_seqs, max_tiles, Hkv;
-  long long num_pages;
-  const uint4* rfrag;       // layer base [Hkv][kFragBlocks][4096]
-  const float* clip;        // layer base [2][Hkv][128]
-  int tasks_per_cta;
-  int* err;
-};
-
 __device__ __forceinline__ void load_row64(const uint16_t* row, bool ok, uint32_t (&w)[16]) {
   if (ok) {
     const uint4* p = reinterpret_cast<const uint4*>(row);
@@ -288,55 +277,6 @@ __device__ __forceinline__ void append_tile(const uint4* frag, const float* clip
   }
 }
 
-template <int GS, int TENSOR>
-__global__ void __launch_bounds__(256, 2) append_kernel(AppendArgs a) {
-  extern __shared__ uint4 sfrag[];                 // 4096 fragments, then clip
-  float* sclip = reinterpret_cast<float*>(sfrag + 4096);
-  const int g = blockIdx.y, tensor = TENSOR;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, j = lane & 3;
-
-  const uint4* src = a.rfrag + ((size_t)g * kFragBlocks + tensor) * 4096;
-  for (int i = threadIdx.x; i < 4096; i += blockDim.x) sfrag[i] = __ldg(src + i);
-  if (threadIdx.x < 128) sclip[threadIdx.x] = a.clip[((size_t)tensor * a.Hkv + g) * 128 + threadIdx.x];
-  __syncthreads();
-
-  const long long total = (long long)a.n_seqs * a.max_tiles;
-  const long long t0 = (long long)blockIdx.x * a.tasks_per_cta;
-  const long long t1 = min(total, t0 + a.tasks_per_cta);
-  for (long long task = t0 + warp; task < t1; task += 8) {
-    const int b = (int)(task / a.max_tiles), lt = (int)(task % a.max_tiles);
-    const int c0 = __ldg(a.cu + b), nb = __ldg(a.cu + b + 1) - c0;
-    const int h0 = __ldg(a.hist_start + b);
-    if (nb <= 0) {
-      if (nb < 0 && lt == 0 && lane == 0) flag_error(a.err, KV_DEVERR_SEQ_RANGE);
-      continue;
-    }
-    if (h0 < 0 || (long long)h0 + nb > (long long)a.max_pages * a.P) {
-      if (lt == 0 && lane == 0) flag_error(a.err, KV_DEVERR_SEQ_RANGE);
-      continue;
-    }
-    const int first = h0 / kTile, last = (h0 + nb - 1) / kTile;
-    if (lt == 0 && last - first + 1 > a.max_tiles && lane == 0) flag_error(a.err, KV_DEVERR_LENGTH);
-    const int tile = first + lt;
-    if (tile > last) continue;
-    const int pid = __ldg(a.pt + (size_t)b * a.max_pages + (tile * kTile) / a.P);
-    if (pid < 0 || pid >= a.num_pages) {
-      if (lane == 0) flag_error(a.err, KV_DEVERR_PAGE_ID);
-      continue;
-    }
-    uint8_t* tb = a.hist + (size_t)pid * a.page_bytes + (size_t)g * a.head_block +
-                  (size_t)((tile * kTile) % a.P / kTile) * a.tile_bytes;
-    const int p0 = max(h0, tile * kTile), p1 = min(h0 + nb, tile * kTile + kTile);
-    const bool full = (p0 == tile * kTile) && (p1 == tile * kTile + kTile);
-    auto row_ok = [&](int row) { const int p = tile * kTile + row; return p >= p0 && p < p1; };
-    auto row_ptr = [&](int row) {
-      const int tok = c0 + (tile * kTile + row - h0);
-      return (tensor == 0 ? a.k : a.v) + ((size_t)tok * a.Hkv + g) * 128 + 32 * j;
-    };
-    append_tile<GS, TENSOR>(sfrag, sclip, tb, full, row_ok, row_ptr);
-  }
-}
-
 // ---------------------------------------------------------------------------
 // per-step token placement (yunpan.plus write-up, "2. 在线量化与反量化": a new
 // token is written to the recent tier; when that is full its oldest token is
@@ -498,7 +438,23 @@ __global__ void rotation_frag_kernel(const float* __restrict__ Rk, const float* 
   const int lane = f & 31;
   const int r = lane >> 2, j = lane & 3;
   uint4 out;
-  if (tensor != 1) {
+  if (tensor >= 3) {
+    // tcgen05 B operand of x . R (R = R_k or R_v): row n holds R[k][n % 128] for
+    // k = 0..127 as its bf16 hi (n < 128) or lo (n >= 128) term; 128-byte rows,
+    // channels 0-63 in the first 32 KB, 64-127 in the second; the 16-byte chunk c
+    // of row n sits at chunk position c ^ (n % 8) (the 128-byte swizzle)
+    const float* R = (tensor == 3 ? Rk : Rv) + (size_t)h * 16384;
+    const int half = f >> 11, n = (f >> 3) & 255, c = (f & 7) ^ (n & 7);
+    const int k0 = 64 * half + 8 * c, col = n & 127;
+    uint16_t e[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      uint16_t hi, lo;
+      split_bf16(R[(size_t)(k0 + u) * 128 + col], hi, lo);
+      e[u] = (n < 128) ? hi : lo;
+    }
+    out = make_uint4(pack2(e[0], e[1]), pack2(e[2], e[3]), pack2(e[4], e[5]), pack2(e[6], e[7]));
+  } else if (tensor != 1) {
     // B operand of x R_k: element (kappa, n) = R_k[in_ch(s, kappa)][8 nt + n];
     // block 0 as bf16 hi/lo (append, x in bf16), block 2 as fp16 hi/lo (decode q')
     const int nt = (f >> 5) & 15, s = f >> 9;
@@ -648,55 +604,7 @@ cudaError_t launch_append(const Pool& p, int layer, int n_seqs, const void* k, c
                           const int32_t* cu, const int32_t* hist_start, const int32_t* pt,
                           int max_pages, int max_tokens, cudaStream_t s) {
   if (n_seqs == 0 || max_tokens == 0) return cudaSuccess;
-  const int H = p.cfg.num_kv_heads;
-  AppendArgs a{};
-  a.hist = p.hist + (size_t)layer * p.hist_layer_stride;
-  a.page_bytes = p.page_bytes;
-  a.head_block = p.page_bytes / H;
-  a.tile_bytes = (int)p.tile_bytes;
-  a.tiles_per_page = p.cfg.page_size / kTile;
-  a.P = p.cfg.page_size;
-  a.k = static_cast<const uint16_t*>(k);
-  a.v = static_cast<const uint16_t*>(v);
-  a.cu = cu;
-  a.hist_start = hist_start;
-  a.pt = pt;
-  a.max_pages = max_pages;
-  a.n_seqs = n_seqs;
-  a.max_tiles = (max_tokens + kTile - 1) / kTile + 1;   // +1: an unaligned start spans one more
-  a.Hkv = H;
-  a.num_pages = p.cfg.num_pages;
-  a.rfrag = p.rfrag + (size_t)layer * H * kFragBlocks * rfrag_per_head();
-  a.clip = p.clip + (size_t)layer * 2 * H * 128;
-  a.err = p.err;
-  const long long tasks = (long long)n_seqs * a.max_tiles;
-  // CTAs per head in each (one-tensor) launch: enough to fill every SM twice
-  long long ctas = (2LL * p.sm_count + H - 1) / H;
-  ctas = max(1LL, min(ctas, (tasks + 7) / 8));
-  a.tasks_per_cta = (int)((tasks + ctas - 1) / ctas);
-  ctas = (tasks + a.tasks_per_cta - 1) / a.tasks_per_cta;
-  const size_t smem = 4096 * sizeof(uint4) + 128 * sizeof(float);
-  // K and V as separate launches: each instantiation carries one tensor's code
-  dim3 grid((unsigned)ctas, H, 1);
-  static bool attr[2][2] = {{false, false}, {false, false}};
-  auto go = [&](auto kernel, int gi, int ti) -> cudaError_t {
-    if (!attr[gi][ti]) {
-      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      attr[gi][ti] = true;
-    }
-    kernel<<<grid, 256, smem, s>>>(a);
-    return cudaGetLastError();
-  };
-  cudaError_t e;
-  if (p.cfg.group_size == 64) {
-    e = go(append_kernel<64, 0>, 0, 0);
-    if (e == cudaSuccess) e = go(append_kernel<64, 1>, 0, 1);
-  } else {
-    e = go(append_kernel<128, 0>, 1, 0);
-    if (e == cudaSuccess) e = go(append_kernel<128, 1>, 1, 1);
-  }
-  return e;
+  return launch_append_tc(p, layer, n_seqs, k, v, cu, hist_start, pt, max_pages, max_tokens, s);
 }
 
 cudaError_t launch_append_step(const Pool& p, int layer, int B, const void* k_new,

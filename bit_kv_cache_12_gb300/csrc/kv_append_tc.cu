@@ -1,0 +1,520 @@
+// Bulk append on the 5th-generation tensor cores: rotate -> clip -> asymmetric
+// INT2 quantize -> pack into the paged tiles.
+//
+// Method: yunpan.plus OSCAR write-up, "2. 在线量化与反量化" (a token leaving
+// the recent window is rotated, clipped, quantized and packed, four 2-bit
+// codes per byte, into the INT2 history); gist.science OSCAR explainer,
+// section 2.2 B (history is stored after the fixed rotation and the clip).
+//
+// GPU design: the rotation x' = x R of a chunk of 128 tokens of one KV head
+// and one tensor is one dense [128 x 128] . [128 x 256] product: R enters as
+// bf16 hi | lo halves side by side (N = 256), x is exact in bf16.  A CTA of
+// eight warps owns one (KV head, tensor) and walks over 128-token chunks:
+//   * x rows arrive by 16-byte cp.async straight into the 128-byte-swizzled
+//     K-major operand layout (the next chunk's rows while this chunk's
+//     epilogue runs); R^T hi | lo arrives once per CTA, pre-swizzled in global
+//     memory by the rotation set-up, as four bulk copies;
+//   * one thread issues eight tcgen05.mma (kind::f16, M 128, N 256, K 16)
+//     into a 256-column fp32 accumulator in tensor memory and commits them
+//     to an mbarrier;
+//   * every thread then owns one token row and one half of the channels of
+//     the accumulator (tcgen05.ld; warps w and w + 4 share a lane quarter):
+//     x' = hi + lo, clip, per-group min / max (combined across the halves
+//     through shared memory for group 128), s and z, the codes (branch-free,
+//     with a rare exact fix-up); the codes are packed into the tile's storage
+//     order with warp shuffles (partners differ in lane bits 0 and 3) and
+//     written as 8-byte word pairs, merging with the bits of rows outside the
+//     append range where a tile is only partly written.
+// Two CTAs share an SM (256 tensor-memory columns and ~100 KB of shared
+// memory each), so one CTA's MMA overlaps the other's epilogue.
+// Every wait is bounded; a wait that runs out sets KV_DEVERR_TIMEOUT, waits
+// (bounded) for the work in flight, frees the tensor memory and returns.
+#include "kv_device.cuh"
+#include "kv_internal.h"
+
+namespace kvint2 {
+
+namespace {
+
+constexpr int kTcThreads = 256;
+constexpr int kChunk = 128;                  // tokens per MMA (the M of one tcgen05.mma)
+constexpr int kTilesPerChunk = kChunk / kTile;
+constexpr int kTcCols = 256;                 // tensor-memory columns: hi | lo accumulators
+constexpr uint32_t kABytes = kChunk * 256;   // x chunk: 128 rows x 128 bf16
+constexpr uint32_t kBBytes = 256 * 256;      // R^T hi | lo: 256 rows x 128 bf16
+constexpr int kTcPolls = 1 << 20;
+
+// dynamic shared memory carve-up (offsets from a 1024-byte aligned base)
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffB = kOffA + kABytes;
+constexpr uint32_t kOffClip = kOffB + kBBytes;
+constexpr uint32_t kOffStat = kOffClip + 128 * 4;
+constexpr uint32_t kOffBar = kOffStat + 2 * 128 * 8;
+constexpr uint32_t kOffTmem = kOffBar + 16;
+constexpr uint32_t kTcSmem = kOffTmem + 16 + 1024;   // + alignment slack
+
+// ---- tcgen05 / descriptor helpers -------------------------------------------
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte swizzle
+// layout: rows of 128 bytes, 8-row atoms of 1024 bytes (stride-dimension byte
+// offset 1024; the leading-dimension offset is unused for this layout),
+// descriptor version 1, layout type 2 (128-byte swizzle).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
+// N = 256, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(256 >> 3) << 17) |
+                            ((uint32_t)(128 >> 4) << 24);
+
+__device__ __forceinline__ void tc_alloc(uint32_t slot_saddr, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_saddr),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t dtmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(dtmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar_saddr) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar_saddr)
+               : "memory");
+}
+// 16 consecutive fp32 columns of this thread's accumulator row
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+      "[%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tc_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// generic-proxy shared-memory writes -> visible to the tensor cores
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// 16-byte copy global -> shared, zero-filled when !valid (no bytes read)
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+
+// 8-byte store of two words of a stored-tile slot, merged with the existing
+// bits outside `mask` unless every bit is new
+__device__ __forceinline__ void store_merge2(uint8_t* dst, const uint32_t (&w)[2], uint32_t mask) {
+  uint2* p = reinterpret_cast<uint2*>(dst);
+  if (mask == 0xFFFFFFFFu) {
+    *p = make_uint2(w[0], w[1]);
+  } else if (mask != 0u) {
+    const uint2 o = *p;
+    *p = make_uint2((o.x & ~mask) | (w[0] & mask), (o.y & ~mask) | (w[1] & mask));
+  }
+}
+
+struct TcArgs {
+  uint8_t* hist;              // layer base
+  size_t page_bytes, head_block;
+  int tile_bytes, P;
+  const uint16_t* x[2];       // K and V inputs [T][Hkv][128] bf16
+  const int32_t* cu;
+  const int32_t* hist_start;
+  const int32_t* pt;
+  int max_pages, n_seqs, max_chunks, Hkv;
+  long long num_pages;
+  const uint4* rfrag;         // layer base [Hkv][kFragBlocks][4096]
+  const float* clip;          // layer base [2][Hkv][128]
+  int* err;
+  int tasks_per_cta;
+};
+
+// Chunk of one task: 128 consecutive history positions [P0, P0 + 128) of
+// sequence b (P0 a multiple of 16); `live` is false when the task has no work.
+struct Chunk {
+  int b, c0, nb, h0, first, last, P0;
+  bool live;
+};
+
+__device__ __forceinline__ Chunk chunk_of(const TcArgs& a, long long task, bool flag) {
+  Chunk k;
+  k.b = (int)(task / a.max_chunks);
+  const int ci = (int)(task % a.max_chunks);
+  k.c0 = __ldg(a.cu + k.b);
+  k.nb = __ldg(a.cu + k.b + 1) - k.c0;
+  k.h0 = __ldg(a.hist_start + k.b);
+  k.live = false;
+  if (k.nb <= 0) {
+    if (flag && k.nb < 0 && ci == 0) flag_error(a.err, KV_DEVERR_SEQ_RANGE);
+    return k;
+  }
+  if (k.h0 < 0 || (long long)k.h0 + k.nb > (long long)a.max_pages * a.P) {
+    if (flag && ci == 0) flag_error(a.err, KV_DEVERR_SEQ_RANGE);
+    return k;
+  }
+  k.first = k.h0 / kTile;
+  k.last = (k.h0 + k.nb - 1) / kTile;
+  if (flag && ci == 0 && (k.last - k.first) / kTilesPerChunk + 1 > a.max_chunks)
+    flag_error(a.err, KV_DEVERR_LENGTH);
+  k.P0 = (k.first + ci * kTilesPerChunk) * kTile;
+  k.live = k.P0 <= k.last * kTile;
+  return k;
+}
+
+// x rows of a chunk -> the swizzled A operand: thread t copies half a row
+// (row t % 128, channels 64 * (t / 128) ..); rows outside the append range are zero
+__device__ __forceinline__ void load_chunk(const TcArgs& a, const uint16_t* X, int g, const Chunk& k,
+                                           uint32_t sA) {
+  const int row = threadIdx.x & 127, hf = threadIdx.x >> 7;
+  const int pos = k.P0 + row;
+  const bool ok = pos >= k.h0 && pos < k.h0 + k.nb;
+  const uint16_t* src = X + ((size_t)(ok ? k.c0 + (pos - k.h0) : 0) * a.Hkv + g) * 128 + 64 * hf;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    cp_async16_zfill(sA + hf * 16384 + row * 128 + ((c ^ (row & 7)) << 4), src + 8 * c, ok);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int GS>
+__global__ void __launch_bounds__(kTcThreads, 2) append_tc_kernel(TcArgs a) {
+  constexpr int NG = 128 / GS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const uint32_t sA = smem_u32(sm + kOffA), sB = smem_u32(sm + kOffB);
+  float* sclip = reinterpret_cast<float*>(sm + kOffClip);
+  float2* sstat = reinterpret_cast<float2*>(sm + kOffStat);     // [2 halves][128 rows] (min, max)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);   // [0] R copy, [1] MMA done
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kOffTmem);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = blockIdx.y, tensor = blockIdx.z;
+  // warp w reads accumulator rows 32 (w % 4) .. (its tensor-memory lane quarter)
+  // and channels 64 (w / 4) .. 64 (w / 4) + 63
+  const int quarter = warp & 3, hf = warp >> 2;
+  const int m = 32 * quarter + lane;          // this thread's token row of the chunk
+  const int m16 = m & 15;
+
+  if (tid == 0) {
+    mbar_init(bars + 0, 1);
+    mbar_init(bars + 1, 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) tc_alloc(smem_u32(tslot), kTcCols);
+  if (tid < 128) sclip[tid] = a.clip[((size_t)tensor * a.Hkv + g) * 128 + tid];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (tid == 0) {   // R^T hi | lo of this (head, tensor), already in the swizzled operand layout
+    const uint4* src = a.rfrag + ((size_t)g * kFragBlocks + 3 + tensor) * 4096;
+    mbar_expect_tx(bars + 0, kBBytes);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) bulk_g2s(sm + kOffB + 16384 * c, src + 1024 * c, 16384, bars + 0);
+  }
+  const uint16_t* X = tensor ? a.x[1] : a.x[0];
+  const long long total = (long long)a.n_seqs * a.max_chunks;
+  const long long t0 = (long long)blockIdx.x * a.tasks_per_cta;
+  const long long t1 = min(total, t0 + a.tasks_per_cta);
+  auto next_live = [&](long long t) {
+    for (; t < t1; ++t)
+      if (chunk_of(a, t, tid == 0).live) return t;
+    return t1;
+  };
+  long long cur = next_live(t0);
+  if (cur < t1) load_chunk(a, X, g, chunk_of(a, cur, false), sA);
+
+  bool ok = mbar_wait(bars + 0, 0, kTcPolls);   // R is needed before the first MMA
+  if (!__syncthreads_and(ok)) {
+    if (tid == 0) {
+      flag_error(a.err, KV_DEVERR_TIMEOUT);
+      mbar_wait(bars + 0, 0, kTcPolls);         // the copies in flight, bounded
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tc_dealloc(tmem, kTcCols);
+    return;
+  }
+
+  uint32_t phase = 0;
+  const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+  while (cur < t1) {
+    const Chunk k = chunk_of(a, cur, false);
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    fence_async_smem();
+    __syncthreads();
+
+    // ---- x' hi | lo = x . [R_hi | R_lo] on the tensor cores ----
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t koff = (ks & 3) * 32;   // 16 channels = 32 bytes into the swizzled row
+        const uint64_t ad = sw128_desc(sA + (ks >> 2) * 16384 + koff);
+        const uint64_t bd = sw128_desc(sB + (ks >> 2) * 32768 + koff);
+        tc_mma(tmem, ad, bd, kIdesc, ks > 0 ? 1u : 0u);
+      }
+      tc_commit(smem_u32(bars + 1));
+    }
+    ok = mbar_wait(bars + 1, phase, kTcPolls);
+    phase ^= 1;
+    if (!__syncthreads_and(ok)) break;
+    tc_fence_after();
+    // the A buffer is consumed: bring in the next chunk behind this epilogue
+    const long long nxt = next_live(cur + 1);
+    if (nxt < t1) load_chunk(a, X, g, chunk_of(a, nxt, false), sA);
+
+    // ---- this thread's row and channel half: x' = hi + lo, clipped; the
+    // group range first, then the codes (the accumulator is read again rather
+    // than held in registers) ----
+    auto rotated16 = [&](int cb, float (&v)[16]) {
+      uint32_t hi[16], lo[16];
+      tc_ld16(trow + 64 * hf + 16 * cb, hi);
+      tc_ld16(trow + 128 + 64 * hf + 16 * cb, lo);
+      tc_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        v[i] = clip_to(__uint_as_float(hi[i]) + __uint_as_float(lo[i]), sclip[64 * hf + 16 * cb + i]);
+    };
+    float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+      float v[16];
+      rotated16(cb, v);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        mn = fminf(mn, v[i]);
+        mx = fmaxf(mx, v[i]);
+      }
+    }
+    if (GS == 128) {   // the group spans both channel halves: combine with warp w ^ 4
+      sstat[hf * 128 + m] = make_float2(mn, mx);
+      __syncthreads();
+      const float2 o = sstat[(hf ^ 1) * 128 + m];
+      mn = fminf(mn, o.x);
+      mx = fmaxf(mx, o.y);
+    }
+    const ScaleZero q = scale_zero(mn, mx);   // the group of these 64 channels
+
+    // ---- codes: fl(d * fl(1/s)) rounded, unless some quotient is within 2^-18
+    // of a half-integer, where the IEEE division decides (quant_code) ----
+    uint32_t cw[4];   // 16 codes of 2 bits per word, channel order
+    bool fix = false;
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+      float v[16];
+      rotated16(cb, v);
+      uint32_t w = 0u;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float t = __fmul_rn(__fsub_rn(v[i], q.z), q.rs);
+        fix |= fabsf(__fsub_rn(t, floorf(t)) - 0.5f) <= 3.814697265625e-6f;
+        w |= (uint32_t)fminf(fmaxf(rintf(t), 0.0f), 3.0f) << (2 * i);
+      }
+      cw[cb] = w;
+    }
+    // warp-uniform: the re-read is a warp-collective tensor-memory load, and a
+    // lane without a near tie recomputes its own codes unchanged
+    if (__any_sync(0xffffffffu, fix)) {
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) {
+        float v[16];
+        rotated16(cb, v);
+        uint32_t w = 0u;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w |= quant_code(v[i], q) << (2 * i);
+        cw[cb] = w;
+      }
+    }
+    auto code = [&](int i) -> uint32_t { return (cw[i >> 4] >> (2 * (i & 15))) & 3u; };
+
+    // ---- destination tile of this row ----
+    const int pos = k.P0 + m;
+    const bool row_ok = pos >= k.h0 && pos < k.h0 + k.nb;
+    const int tile = pos / kTile;
+    const bool tile_live = tile <= k.last;
+    const int pid_raw = __ldg(a.pt + (size_t)k.b * a.max_pages + min((tile * kTile) / a.P, a.max_pages - 1));
+    const bool pid_ok = pid_raw >= 0 && pid_raw < a.num_pages;
+    if (tile_live && !pid_ok && m16 == 0 && hf == 0) flag_error(a.err, KV_DEVERR_PAGE_ID);
+    const bool write = tile_live && pid_ok;
+    uint8_t* tb = a.hist + (size_t)(pid_ok ? pid_raw : 0) * a.page_bytes + (size_t)g * a.head_block +
+                  (size_t)((tile * kTile) % a.P / kTile) * a.tile_bytes;
+    const unsigned okmask = __ballot_sync(0xffffffffu, row_ok && write);
+
+    if (tensor == 0) {
+      // K: code (token m16, channel c) -> slot 4*(m16%8) + (k%8)/2, word c/32,
+      // bit 16*(k%2) + 2*(2*((c/16)%2) + m16/8 + 4*(k/8)), k = c%16; this half
+      // holds words 2 hf and 2 hf + 1 of every slot
+      uint32_t wd[4][2];
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) wd[jj][0] = wd[jj][1] = 0u;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const int kk = i & 15, s1 = (i >> 4) & 1, lw = i >> 5;
+        wd[(kk & 7) >> 1][lw] |= code(i) << (16 * (kk & 1) + 2 * (2 * s1 + 4 * (kk >> 3)));
+      }
+      const int mh = m16 >> 3;
+      uint32_t out[2][2];
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          const uint32_t lo_w = wd[jj][w] << (2 * mh), hi_w = wd[2 + jj][w] << (2 * mh);
+          const uint32_t recv = __shfl_xor_sync(0xffffffffu, mh ? lo_w : hi_w, 8);
+          out[jj][w] = (mh ? hi_w : lo_w) | recv;
+        }
+      const bool me = (okmask >> lane) & 1u, other = (okmask >> (lane ^ 8)) & 1u;
+      const uint32_t pat_me = mh ? 0xCCCCCCCCu : 0x33333333u;
+      const uint32_t mask = (me ? pat_me : 0u) | (other ? ~pat_me : 0u);
+      if (write) {
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj)
+          store_merge2(tb + 16 * (4 * (m16 & 7) + 2 * mh + jj) + 8 * hf, out[jj], mask);
+      }
+      if (write && row_ok && (GS == 64 || hf == 0)) {
+        __half2* rec = reinterpret_cast<__half2*>(tb + 1024 + (2 * (m16 & 7) + mh) * 8 * NG);
+        rec[GS == 64 ? hf : 0] = __halves2half2(q.sh, q.zh);
+      }
+    } else {
+      // V: code (channel c, token m16) -> slot 4*(c%8) + (m16%8)/2, word c/32,
+      // bit 16*(m16%2) + 2*(2*((c/16)%2) + (c%16)/8 + 4*(m16/8))
+      uint32_t wd[8][2];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) wd[i][0] = wd[i][1] = 0u;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const int mm = i & 15, s1 = (i >> 4) & 1, lw = i >> 5;
+        wd[mm & 7][lw] |= code(i) << (2 * (2 * s1 + (mm >> 3)));
+      }
+      const int ek = m16 & 1, kh = m16 >> 3;
+      const int sh = 16 * ek + 8 * kh;
+      uint32_t r1[4][2];   // partner lane ^ 8: keep slots with m8 / 4 == kh
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          const uint32_t a0 = wd[i][w] << sh, a1 = wd[4 + i][w] << sh;
+          const uint32_t recv = __shfl_xor_sync(0xffffffffu, kh ? a0 : a1, 8);
+          r1[i][w] = (kh ? a1 : a0) | recv;
+        }
+      uint32_t out[2][2];  // partner lane ^ 1: keep m8 % 4 / 2 == ek
+#pragma unroll
+      for (int ii = 0; ii < 2; ++ii)
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          const uint32_t a0 = r1[ii][w], a1 = r1[2 + ii][w];
+          const uint32_t recv = __shfl_xor_sync(0xffffffffu, ek ? a0 : a1, 1);
+          out[ii][w] = (ek ? a1 : a0) | recv;
+        }
+      // bits of the four tokens sharing these words: (ek', kh') -> 0x00FF / 0xFF00 in half ek'
+      const int base = lane & ~9;
+      uint32_t mask = 0u;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int e2 = t & 1, k2 = t >> 1;
+        if ((okmask >> (base | e2 | (k2 << 3))) & 1u) mask |= (k2 ? 0xFF00u : 0x00FFu) << (16 * e2);
+      }
+      const int jk = (m16 & 7) >> 1;
+      if (write) {
+#pragma unroll
+        for (int ii = 0; ii < 2; ++ii)
+          store_merge2(tb + 512 + 16 * (4 * (4 * kh + 2 * ek + ii) + jk) + 8 * hf, out[ii], mask);
+      }
+      if (write && row_ok && (GS == 64 || hf == 0)) {
+        __half2* rec = reinterpret_cast<__half2*>(tb + 1024 + (2 * (m16 & 7) + kh) * 8 * NG) + NG;
+        rec[GS == 64 ? hf : 0] = __halves2half2(q.sh, q.zh);
+      }
+    }
+    tc_fence_before();
+    __syncthreads();   // the accumulator is free for the next chunk
+    cur = nxt;
+  }
+
+  if (!ok) {   // an MMA completion did not arrive in time: wait (bounded) for it
+    if (tid == 0) flag_error(a.err, KV_DEVERR_TIMEOUT);
+    mbar_wait(bars + 1, phase, kTcPolls);
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc_dealloc(tmem, kTcCols);
+  if (tid == 0) {
+    mbar_inval(bars + 0);
+    mbar_inval(bars + 1);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append_tc(const Pool& p, int layer, int n_seqs, const void* k, const void* v,
+                             const int32_t* cu, const int32_t* hist_start, const int32_t* pt,
+                             int max_pages, int max_tokens, cudaStream_t s) {
+  const int H = p.cfg.num_kv_heads;
+  TcArgs a;
+  a.hist = p.hist + (size_t)layer * p.hist_layer_stride;
+  a.page_bytes = p.page_bytes;
+  a.head_block = p.page_bytes / H;
+  a.tile_bytes = (int)p.tile_bytes;
+  a.P = p.cfg.page_size;
+  a.x[0] = static_cast<const uint16_t*>(k);
+  a.x[1] = static_cast<const uint16_t*>(v);
+  a.cu = cu;
+  a.hist_start = hist_start;
+  a.pt = pt;
+  a.max_pages = max_pages;
+  a.n_seqs = n_seqs;
+  const int max_tiles = (max_tokens + kTile - 1) / kTile + 1;   // +1: an unaligned start spans one more
+  a.max_chunks = (max_tiles + kTilesPerChunk - 1) / kTilesPerChunk;
+  a.Hkv = H;
+  a.num_pages = p.cfg.num_pages;
+  a.rfrag = p.rfrag + (size_t)layer * H * kFragBlocks * rfrag_per_head();
+  a.clip = p.clip + (size_t)layer * 2 * H * 128;
+  a.err = p.err;
+  const long long tasks = (long long)n_seqs * a.max_chunks;
+  // two CTAs per SM over all (head, tensor) pairs
+  long long ctas = (2LL * p.sm_count + 2 * H - 1) / (2 * H);
+  ctas = max(1LL, min(ctas, tasks));
+  a.tasks_per_cta = (int)((tasks + ctas - 1) / ctas);
+  ctas = (tasks + a.tasks_per_cta - 1) / a.tasks_per_cta;
+  dim3 grid((unsigned)ctas, H, 2);
+  static bool attr[2] = {false, false};
+  auto go = [&](auto kernel, int gi) -> cudaError_t {
+    if (!attr[gi]) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
+      if (e != cudaSuccess) return e;
+      attr[gi] = true;
+    }
+    kernel<<<grid, kTcThreads, kTcSmem, s>>>(a);
+    return cudaGetLastError();
+  };
+  return p.cfg.group_size == 64 ? go(append_tc_kernel<64>, 0) : go(append_tc_kernel<128>, 1);
+}
+
+}  // namespace kvint2

@@ -43,10 +43,13 @@ struct Pool {
 };
 
 // Rotation fragments per (layer, KV head), 4096 uint4 each (bf16 hi/lo pairs):
-//   block 0: B operand of x . R_k        (append K, decode q' = q R_k)
-//   block 1: A operand of R_v^T . x^T    (append V)
+//   block 0: B operand of x . R_k        (per-step append K, mma.sync fragments)
+//   block 1: A operand of R_v^T . x^T    (per-step append V, mma.sync fragments)
 //   block 2: B operand of q . R_k as fp16 hi/lo pairs (decode q' = q R_k)
-constexpr int kFragBlocks = 3;
+//   block 3: tcgen05 B operand of x . R_k: rows n of [R_k^T hi ; R_k^T lo] (256 x 128
+//            bf16), K-major, 128-byte swizzle, channels 0-63 then 64-127 (bulk append K)
+//   block 4: the same for R_v (bulk append V)
+constexpr int kFragBlocks = 5;
 inline size_t rfrag_per_head() { return 4096; }   // uint4 per (head, block)
 
 // ---- launchers (return cudaSuccess or the launch error) --------------------
@@ -60,6 +63,9 @@ cudaError_t launch_quantize_pack(const Pool& p, int layer, int tensor, int64_t n
 cudaError_t launch_append(const Pool& p, int layer, int n_seqs, const void* k, const void* v,
                           const int32_t* cu, const int32_t* hist_start, const int32_t* pt,
                           int max_pages, int max_tokens, cudaStream_t s);
+cudaError_t launch_append_tc(const Pool& p, int layer, int n_seqs, const void* k, const void* v,
+                             const int32_t* cu, const int32_t* hist_start, const int32_t* pt,
+                             int max_pages, int max_tokens, cudaStream_t s);
 cudaError_t launch_append_step(const Pool& p, int layer, int B, const void* k_new,
                                const void* v_new, int32_t* sink_len, int32_t* hist_len,
                                int32_t* rec_len, int32_t* rec_start, const int32_t* pt,
