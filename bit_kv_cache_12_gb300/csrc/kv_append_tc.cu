@@ -29,6 +29,9 @@
 // memory each), so one CTA's MMA overlaps the other's epilogue.
 // Every wait is bounded; a wait that runs out sets KV_DEVERR_TIMEOUT, waits
 // (bounded) for the work in flight, frees the tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "kv_device.cuh"
 #include "kv_internal.h"
 
@@ -39,7 +42,7 @@ namespace {
 constexpr int kTcThreads = 256;
 constexpr int kChunk = 128;                  // tokens per MMA (the M of one tcgen05.mma)
 constexpr int kTilesPerChunk = kChunk / kTile;
-constexpr int kTcCols = 256;                 // tensor-memory columns: hi | lo accumulators
+constexpr int kTcCols = 128;                 // tensor-memory columns: the fp32 accumulator
 constexpr uint32_t kABytes = kChunk * 256;   // x chunk: 128 rows x 128 bf16
 constexpr uint32_t kBBytes = 256 * 256;      // R^T hi | lo: 256 rows x 128 bf16
 constexpr int kTcPolls = 1 << 20;
@@ -50,7 +53,7 @@ constexpr uint32_t kOffB = kOffA + kABytes;
 constexpr uint32_t kOffClip = kOffB + kBBytes;
 constexpr uint32_t kOffStat = kOffClip + 128 * 4;
 constexpr uint32_t kOffBar = kOffStat + 2 * 128 * 8;
-constexpr uint32_t kOffTmem = kOffBar + 16;
+constexpr uint32_t kOffTmem = kOffBar + 24;
 constexpr uint32_t kTcSmem = kOffTmem + 16 + 1024;   // + alignment slack
 
 // ---- tcgen05 / descriptor helpers -------------------------------------------
@@ -68,8 +71,8 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 }
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
-// N = 256, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(256 >> 3) << 17) |
+// N = 128, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(128 >> 3) << 17) |
                             ((uint32_t)(128 >> 4) << 24);
 
 __device__ __forceinline__ void tc_alloc(uint32_t slot_saddr, uint32_t ncols) {
@@ -104,14 +107,16 @@ __device__ __forceinline__ void tc_commit(uint32_t bar_saddr) {
                    bar_saddr)
                : "memory");
 }
-// 16 consecutive fp32 columns of this thread's accumulator row
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+// 32 consecutive fp32 columns of this thread's accumulator row
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
-      "[%16];"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
       : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
         "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-        "=r"(v[14]), "=r"(v[15])
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]),
+        "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]),
+        "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
       : "r"(taddr)
       : "memory");
 }
@@ -127,6 +132,18 @@ __device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, 
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
                "r"(valid ? 16 : 0)
                : "memory");
+}
+
+// one TMA tile load (box 64 channels x 1 head x 128 rows, 128-byte swizzle)
+// of the x tensor map at (channel c0, head c1, row c2) into shared memory,
+// completing on `bar`; rows outside the map read as zero
+__device__ __forceinline__ void tma_load_x(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                           uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // 8-byte store of two words of a stored-tile slot, merged with the existing
@@ -203,18 +220,17 @@ __device__ __forceinline__ void load_chunk(const TcArgs& a, const uint16_t* X, i
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-template <int GS>
-__global__ void __launch_bounds__(kTcThreads, 2) append_tc_kernel(TcArgs a) {
+template <int GS, int TENSOR>
+__device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap, uint8_t* sm) {
   constexpr int NG = 128 / GS;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sA = smem_u32(sm + kOffA), sB = smem_u32(sm + kOffB);
   float* sclip = reinterpret_cast<float*>(sm + kOffClip);
   float2* sstat = reinterpret_cast<float2*>(sm + kOffStat);     // [2 halves][128 rows] (min, max)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);   // [0] R copy, [1] MMA done
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);   // [0] R copy, [1] MMA done, [2] x by TMA
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kOffTmem);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = blockIdx.y, tensor = blockIdx.z;
+  const int g = blockIdx.y;
+  constexpr int tensor = TENSOR;
   // warp w reads accumulator rows 32 (w % 4) .. (its tensor-memory lane quarter)
   // and channels 64 (w / 4) .. 64 (w / 4) + 63
   const int quarter = warp & 3, hf = warp >> 2;
@@ -224,6 +240,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) append_tc_kernel(TcArgs a) {
   if (tid == 0) {
     mbar_init(bars + 0, 1);
     mbar_init(bars + 1, 1);
+    mbar_init(bars + 2, 1);
     mbar_fence_init();
   }
   if (warp == 0) tc_alloc(smem_u32(tslot), kTcCols);
@@ -247,14 +264,34 @@ __global__ void __launch_bounds__(kTcThreads, 2) append_tc_kernel(TcArgs a) {
       if (chunk_of(a, t, tid == 0).live) return t;
     return t1;
   };
+  // x of a chunk: two TMA tile loads by one thread when all 128 rows lie
+  // below the input's row count T (rows below 0 read as zero); otherwise,
+  // so that nothing past the caller's buffer is read, 16-byte copies by every
+  // thread with rows outside the chunk's append range zero-filled
+  const int T_rows = __ldg(a.cu + a.n_seqs);
+  uint32_t xphase = 0;
+  auto issue_load = [&](const Chunk& k) -> bool {
+    const int r0 = k.c0 + (k.P0 - k.h0);
+    if (r0 + kChunk <= T_rows) {
+      if (tid == 0) {
+        mbar_expect_tx(bars + 2, kABytes);
+        tma_load_x(sA, xmap, 0, g, r0, bars + 2);
+        tma_load_x(sA + 16384, xmap, 64, g, r0, bars + 2);
+      }
+      return true;
+    }
+    load_chunk(a, X, g, k, sA);
+    return false;
+  };
   long long cur = next_live(t0);
-  if (cur < t1) load_chunk(a, X, g, chunk_of(a, cur, false), sA);
+  bool cur_tma = (cur < t1) ? issue_load(chunk_of(a, cur, false)) : false;
 
   bool ok = mbar_wait(bars + 0, 0, kTcPolls);   // R is needed before the first MMA
   if (!__syncthreads_and(ok)) {
     if (tid == 0) {
       flag_error(a.err, KV_DEVERR_TIMEOUT);
       mbar_wait(bars + 0, 0, kTcPolls);         // the copies in flight, bounded
+      if (cur_tma) mbar_wait(bars + 2, 0, kTcPolls);
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     tc_fence_before();
@@ -265,21 +302,33 @@ __global__ void __launch_bounds__(kTcThreads, 2) append_tc_kernel(TcArgs a) {
 
   uint32_t phase = 0;
   const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+  bool x_pending = false;   // a TMA load whose completion has not been waited for
   while (cur < t1) {
     const Chunk k = chunk_of(a, cur, false);
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    fence_async_smem();
-    __syncthreads();
+    if (cur_tma) {
+      ok = mbar_wait(bars + 2, xphase, kTcPolls);
+      xphase ^= 1;
+      if (!__syncthreads_and(ok)) {
+        x_pending = true;
+        break;
+      }
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      fence_async_smem();
+      __syncthreads();
+    }
 
-    // ---- x' hi | lo = x . [R_hi | R_lo] on the tensor cores ----
+    // ---- x' = x . R_hi + x . R_lo on the tensor cores: per 16-channel step
+    // the hi term, then the lo term, into one fp32 accumulator ----
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t koff = (ks & 3) * 32;   // 16 channels = 32 bytes into the swizzled row
         const uint64_t ad = sw128_desc(sA + (ks >> 2) * 16384 + koff);
-        const uint64_t bd = sw128_desc(sB + (ks >> 2) * 32768 + koff);
-        tc_mma(tmem, ad, bd, kIdesc, ks > 0 ? 1u : 0u);
+        const uint32_t bb = sB + (ks >> 2) * 32768 + koff;   // rows 0-127: hi; 128-255: lo
+        tc_mma(tmem, ad, sw128_desc(bb), kIdesc, ks > 0 ? 1u : 0u);
+        tc_mma(tmem, ad, sw128_desc(bb + 16384), kIdesc, 1u);
       }
       tc_commit(smem_u32(bars + 1));
     }
@@ -289,30 +338,34 @@ __global__ void __launch_bounds__(kTcThreads, 2) append_tc_kernel(TcArgs a) {
     tc_fence_after();
     // the A buffer is consumed: bring in the next chunk behind this epilogue
     const long long nxt = next_live(cur + 1);
-    if (nxt < t1) load_chunk(a, X, g, chunk_of(a, nxt, false), sA);
+    const bool nxt_tma = (nxt < t1) ? issue_load(chunk_of(a, nxt, false)) : false;
 
-    // ---- this thread's row and channel half: x' = hi + lo, clipped; the
-    // group range first, then the codes (the accumulator is read again rather
-    // than held in registers) ----
-    auto rotated16 = [&](int cb, float (&v)[16]) {
-      uint32_t hi[16], lo[16];
-      tc_ld16(trow + 64 * hf + 16 * cb, hi);
-      tc_ld16(trow + 128 + 64 * hf + 16 * cb, lo);
+    // ---- this thread's row and channel half: x', clipped; the group range
+    // first, then the codes (the accumulator is read again rather than held in
+    // registers); reductions as trees to keep the dependency chains short ----
+    auto rotated32 = [&](int cb, float (&v)[32]) {
+      uint32_t u[32];
+      tc_ld32(trow + 64 * hf + 32 * cb, u);
       tc_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        v[i] = clip_to(__uint_as_float(hi[i]) + __uint_as_float(lo[i]), sclip[64 * hf + 16 * cb + i]);
+      for (int i = 0; i < 32; ++i) v[i] = clip_to(__uint_as_float(u[i]), sclip[64 * hf + 32 * cb + i]);
     };
     float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
-    for (int cb = 0; cb < 4; ++cb) {
-      float v[16];
-      rotated16(cb, v);
+    for (int cb = 0; cb < 2; ++cb) {
+      float v[32], w[32];
+      rotated32(cb, v);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        mn = fminf(mn, v[i]);
-        mx = fmaxf(mx, v[i]);
-      }
+      for (int i = 0; i < 32; ++i) w[i] = v[i];
+#pragma unroll
+      for (int st = 16; st >= 1; st >>= 1)
+#pragma unroll
+        for (int i = 0; i < st; ++i) {
+          v[i] = fminf(v[i], v[i + st]);
+          w[i] = fmaxf(w[i], w[i + st]);
+        }
+      mn = fminf(mn, v[0]);
+      mx = fmaxf(mx, w[0]);
     }
     if (GS == 128) {   // the group spans both channel halves: combine with warp w ^ 4
       sstat[hf * 128 + m] = make_float2(mn, mx);
@@ -323,37 +376,58 @@ __global__ void __launch_bounds__(kTcThreads, 2) append_tc_kernel(TcArgs a) {
     }
     const ScaleZero q = scale_zero(mn, mx);   // the group of these 64 channels
 
-    // ---- codes: fl(d * fl(1/s)) rounded, unless some quotient is within 2^-18
-    // of a half-integer, where the IEEE division decides (quant_code) ----
-    uint32_t cw[4];   // 16 codes of 2 bits per word, channel order
-    bool fix = false;
+    // ---- codes, straight into this half's storage words (words 2 hf and
+    // 2 hf + 1 of each slot; K: slot (k % 8) / 2 of the token's four, V: slot
+    // c % 8 of the token's eight, k = c % 16) ----
+    constexpr int NS = (TENSOR == 0) ? 4 : 8;
+    uint32_t wd[NS][2];
+    auto clear = [&]() {
 #pragma unroll
-    for (int cb = 0; cb < 4; ++cb) {
-      float v[16];
-      rotated16(cb, v);
-      uint32_t w = 0u;
+      for (int u = 0; u < NS; ++u) wd[u][0] = wd[u][1] = 0u;
+    };
+    auto pack = [&](int i, uint32_t c) {
+      const int kk = i & 15, s1 = (i >> 4) & 1, lw = i >> 5;
+      if (TENSOR == 0)
+        wd[(kk & 7) >> 1][lw] |= c << (16 * (kk & 1) + 2 * (2 * s1 + 4 * (kk >> 3)));
+      else
+        wd[kk & 7][lw] |= c << (2 * (2 * s1 + (kk >> 3)));
+    };
+    // code = rint(clamp(fl(fl(y - z) * fl(1/s)), 0, 3)): the clamped quotient
+    // plus 1.5 * 2^23 holds rint in its low mantissa bits (round to nearest
+    // even); unless some quotient lies within 2^-18 of a half-integer, where
+    // the IEEE division decides (quant_code).  Out of [0, 3] the clamp leaves
+    // an integer, so only ties inside the range can set the fix-up.
+    clear();
+    float emax = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float t = __fmul_rn(__fsub_rn(v[i], q.z), q.rs);
-        fix |= fabsf(__fsub_rn(t, floorf(t)) - 0.5f) <= 3.814697265625e-6f;
-        w |= (uint32_t)fminf(fmaxf(rintf(t), 0.0f), 3.0f) << (2 * i);
+    for (int cb = 0; cb < 2; ++cb) {
+      float v[32];
+      rotated32(cb, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float t = fminf(fmaxf(__fmul_rn(__fsub_rn(v[i], q.z), q.rs), 0.0f), 3.0f);
+        const float rr = __fadd_rn(t, 12582912.0f);
+        pack(32 * cb + i, __float_as_uint(rr) & 3u);
+        v[i] = fabsf(__fsub_rn(t, __fsub_rn(rr, 12582912.0f)));
       }
-      cw[cb] = w;
+#pragma unroll
+      for (int st = 16; st >= 1; st >>= 1)
+#pragma unroll
+        for (int i = 0; i < st; ++i) v[i] = fmaxf(v[i], v[i + st]);
+      emax = fmaxf(emax, v[0]);
     }
     // warp-uniform: the re-read is a warp-collective tensor-memory load, and a
     // lane without a near tie recomputes its own codes unchanged
-    if (__any_sync(0xffffffffu, fix)) {
+    if (__any_sync(0xffffffffu, emax >= 0.499996185302734375f)) {
+      clear();
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        float v[16];
-        rotated16(cb, v);
-        uint32_t w = 0u;
+      for (int cb = 0; cb < 2; ++cb) {
+        float v[32];
+        rotated32(cb, v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) w |= quant_code(v[i], q) << (2 * i);
-        cw[cb] = w;
+        for (int i = 0; i < 32; ++i) pack(32 * cb + i, quant_code(v[i], q));
       }
     }
-    auto code = [&](int i) -> uint32_t { return (cw[i >> 4] >> (2 * (i & 15))) & 3u; };
 
     // ---- destination tile of this row ----
     const int pos = k.P0 + m;
@@ -368,18 +442,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) append_tc_kernel(TcArgs a) {
                   (size_t)((tile * kTile) % a.P / kTile) * a.tile_bytes;
     const unsigned okmask = __ballot_sync(0xffffffffu, row_ok && write);
 
-    if (tensor == 0) {
+    if constexpr (TENSOR == 0) {
       // K: code (token m16, channel c) -> slot 4*(m16%8) + (k%8)/2, word c/32,
       // bit 16*(k%2) + 2*(2*((c/16)%2) + m16/8 + 4*(k/8)), k = c%16; this half
       // holds words 2 hf and 2 hf + 1 of every slot
-      uint32_t wd[4][2];
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) wd[jj][0] = wd[jj][1] = 0u;
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const int kk = i & 15, s1 = (i >> 4) & 1, lw = i >> 5;
-        wd[(kk & 7) >> 1][lw] |= code(i) << (16 * (kk & 1) + 2 * (2 * s1 + 4 * (kk >> 3)));
-      }
       const int mh = m16 >> 3;
       uint32_t out[2][2];
 #pragma unroll
@@ -405,14 +471,6 @@ __global__ void __launch_bounds__(kTcThreads, 2) append_tc_kernel(TcArgs a) {
     } else {
       // V: code (channel c, token m16) -> slot 4*(c%8) + (m16%8)/2, word c/32,
       // bit 16*(m16%2) + 2*(2*((c/16)%2) + (c%16)/8 + 4*(m16/8))
-      uint32_t wd[8][2];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) wd[i][0] = wd[i][1] = 0u;
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const int mm = i & 15, s1 = (i >> 4) & 1, lw = i >> 5;
-        wd[mm & 7][lw] |= code(i) << (2 * (2 * s1 + (mm >> 3)));
-      }
       const int ek = m16 & 1, kh = m16 >> 3;
       const int sh = 16 * ek + 8 * kh;
       uint32_t r1[4][2];   // partner lane ^ 8: keep slots with m8 / 4 == kh
@@ -455,11 +513,13 @@ __global__ void __launch_bounds__(kTcThreads, 2) append_tc_kernel(TcArgs a) {
     tc_fence_before();
     __syncthreads();   // the accumulator is free for the next chunk
     cur = nxt;
+    cur_tma = nxt_tma;
   }
 
-  if (!ok) {   // an MMA completion did not arrive in time: wait (bounded) for it
+  if (!ok) {   // a completion did not arrive in time: wait (bounded) for the work in flight
     if (tid == 0) flag_error(a.err, KV_DEVERR_TIMEOUT);
-    mbar_wait(bars + 1, phase, kTcPolls);
+    if (x_pending) mbar_wait(bars + 2, xphase ^ 1, kTcPolls);
+    else mbar_wait(bars + 1, phase ^ 1, kTcPolls);
   }
   asm volatile("cp.async.wait_group 0;" ::: "memory");
   tc_fence_before();
@@ -468,7 +528,30 @@ __global__ void __launch_bounds__(kTcThreads, 2) append_tc_kernel(TcArgs a) {
   if (tid == 0) {
     mbar_inval(bars + 0);
     mbar_inval(bars + 1);
+    mbar_inval(bars + 2);
   }
+}
+
+template <int GS, int TENSOR>
+__global__ void __launch_bounds__(kTcThreads, 2)
+    append_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap xmap) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  tc_body<GS, TENSOR>(a, &xmap, sm);
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
 }
 
 }  // namespace
@@ -498,23 +581,49 @@ cudaError_t launch_append_tc(const Pool& p, int layer, int n_seqs, const void* k
   a.clip = p.clip + (size_t)layer * 2 * H * 128;
   a.err = p.err;
   const long long tasks = (long long)n_seqs * a.max_chunks;
-  // two CTAs per SM over all (head, tensor) pairs
-  long long ctas = (2LL * p.sm_count + 2 * H - 1) / (2 * H);
+  // x viewed as (128 channels, Hkv heads, rows); the row extent n_seqs * max_tokens
+  // bounds the input's row count T, and the kernel uses the map only for boxes below T
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap maps[2];
+  for (int t = 0; t < 2; ++t) {
+    const cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)n_seqs * (cuuint64_t)max_tokens};
+    const cuuint64_t strides[2] = {256, (cuuint64_t)H * 256};
+    const cuuint32_t box[3] = {64, 1, kChunk};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&maps[t], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(a.x[t]), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  // two CTAs per SM over the KV heads of one tensor; K, then V
+  long long ctas = (2LL * p.sm_count + H - 1) / H;
   ctas = max(1LL, min(ctas, tasks));
   a.tasks_per_cta = (int)((tasks + ctas - 1) / ctas);
   ctas = (tasks + a.tasks_per_cta - 1) / a.tasks_per_cta;
-  dim3 grid((unsigned)ctas, H, 2);
-  static bool attr[2] = {false, false};
-  auto go = [&](auto kernel, int gi) -> cudaError_t {
-    if (!attr[gi]) {
+  dim3 grid((unsigned)ctas, H, 1);
+  static bool attr[2][2] = {{false, false}, {false, false}};
+  auto go = [&](auto kernel, int gi, int t) -> cudaError_t {
+    if (!attr[gi][t]) {
       cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
+      // the whole unified L1 / shared array as shared memory, so that two CTAs fit
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
       if (e != cudaSuccess) return e;
-      attr[gi] = true;
+      attr[gi][t] = true;
     }
-    kernel<<<grid, kTcThreads, kTcSmem, s>>>(a);
+    kernel<<<grid, kTcThreads, kTcSmem, s>>>(a, maps[t]);
     return cudaGetLastError();
   };
-  return p.cfg.group_size == 64 ? go(append_tc_kernel<64>, 0) : go(append_tc_kernel<128>, 1);
+  cudaError_t e;
+  if (p.cfg.group_size == 64) {
+    e = go(append_tc_kernel<64, 0>, 0, 0);
+    if (e == cudaSuccess) e = go(append_tc_kernel<64, 1>, 0, 1);
+  } else {
+    e = go(append_tc_kernel<128, 0>, 1, 0);
+    if (e == cudaSuccess) e = go(append_tc_kernel<128, 1>, 1, 1);
+  }
+  return e;
 }
 
 }  // namespace kvint2
