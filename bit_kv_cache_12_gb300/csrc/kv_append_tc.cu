@@ -1,5 +1,8 @@
-// Bulk append on the 5th-generation tensor cores: rotate -> clip -> asymmetric
-// INT2 quantize -> pack into the paged tiles.
+// INT2 append on the 5th-generation tensor cores, in bulk (kv_append_quantize)
+// and per decode step (kv_append_step): rotate -> clip -> asymmetric INT2
+// quantize -> pack into the paged tiles.  Both run the same MMA and the same
+// epilogue arithmetic (row_codes), so a token gets the same codes on either
+// path.
 //
 // Method: yunpan.plus OSCAR write-up, "2. 在线量化与反量化" (a token leaving
 // the recent window is rotated, clipped, quantized and packed, four 2-bit
@@ -220,6 +223,120 @@ __device__ __forceinline__ void load_chunk(const TcArgs& a, const uint16_t* X, i
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
+// x' = x . R_hi + x . R_lo for a 128-row chunk on the tensor cores: per
+// 16-channel step the hi term, then the lo term, into the 128-column fp32
+// accumulator at tmem; completion arrives on `bar`.  One thread issues.
+__device__ __forceinline__ void issue_rotation(uint32_t tmem, uint32_t sA, uint32_t sB, uint64_t* bar) {
+  tc_fence_after();
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t koff = (ks & 3) * 32;   // 16 channels = 32 bytes into the swizzled row
+    const uint64_t ad = sw128_desc(sA + (ks >> 2) * 16384 + koff);
+    const uint32_t bb = sB + (ks >> 2) * 32768 + koff;   // rows 0-127: hi; 128-255: lo
+    tc_mma(tmem, ad, sw128_desc(bb), kIdesc, ks > 0 ? 1u : 0u);
+    tc_mma(tmem, ad, sw128_desc(bb + 16384), kIdesc, 1u);
+  }
+  tc_commit(smem_u32(bar));
+}
+
+// The codes of one accumulator row (token row m; channels 64 hf .. 64 hf + 63)
+// after clipping, with s and z from the group's range: x' read from tensor
+// memory (lanes of this warp's quarter, address trow), the range first and then
+// the codes (the accumulator is read again rather than held in registers),
+// reductions as trees to keep the dependency chains short.  Codes go into the
+// storage words of this channel half (words 2 hf and 2 hf + 1 of each slot; K:
+// slot (k % 8) / 2 of the token's four, V: slot c % 8 of the token's eight,
+// k = c % 16) at the bit positions of token row 0 of a tile (K) or of tile
+// token 0 (V); the caller shifts them to the row's own positions.  Every
+// thread of the CTA calls this (group 128 combines the two halves through
+// shared memory with a barrier).
+template <int GS, int TENSOR, int NS>
+__device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, const float* sclip, float2* sstat,
+                                               uint32_t (&wd)[NS][2]) {
+  auto rotated32 = [&](int cb, float (&v)[32]) {
+    uint32_t u[32];
+    tc_ld32(trow + 64 * hf + 32 * cb, u);
+    tc_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = clip_to(__uint_as_float(u[i]), sclip[64 * hf + 32 * cb + i]);
+  };
+  float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+  for (int cb = 0; cb < 2; ++cb) {
+    float v[32], w[32];
+    rotated32(cb, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = v[i];
+#pragma unroll
+    for (int st = 16; st >= 1; st >>= 1)
+#pragma unroll
+      for (int i = 0; i < st; ++i) {
+        v[i] = fminf(v[i], v[i + st]);
+        w[i] = fmaxf(w[i], w[i + st]);
+      }
+    mn = fminf(mn, v[0]);
+    mx = fmaxf(mx, w[0]);
+  }
+  if (GS == 128) {   // the group spans both channel halves: combine with warp w ^ 4
+    sstat[hf * 128 + m] = make_float2(mn, mx);
+    __syncthreads();
+    const float2 o = sstat[(hf ^ 1) * 128 + m];
+    mn = fminf(mn, o.x);
+    mx = fmaxf(mx, o.y);
+  }
+  const ScaleZero q = scale_zero(mn, mx);   // the group of these 64 channels
+
+  auto clear = [&]() {
+#pragma unroll
+    for (int u = 0; u < NS; ++u) wd[u][0] = wd[u][1] = 0u;
+  };
+  auto pack = [&](int i, uint32_t c) {
+    const int kk = i & 15, s1 = (i >> 4) & 1, lw = i >> 5;
+    if (TENSOR == 0)
+      wd[(kk & 7) >> 1][lw] |= c << (16 * (kk & 1) + 2 * (2 * s1 + 4 * (kk >> 3)));
+    else
+      wd[kk & 7][lw] |= c << (2 * (2 * s1 + (kk >> 3)));
+  };
+  // code = rint(clamp(fl(fl(y - z) * fl(1/s)), 0, 3)): the clamped quotient
+  // plus 1.5 * 2^23 holds rint in its low mantissa bits (round to nearest
+  // even); unless some quotient lies within 2^-18 of a half-integer, where
+  // the IEEE division decides (quant_code).  Out of [0, 3] the clamp leaves
+  // an integer, so only ties inside the range can set the fix-up.
+  clear();
+  float emax = 0.0f;
+#pragma unroll
+  for (int cb = 0; cb < 2; ++cb) {
+    float v[32];
+    rotated32(cb, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float t = fminf(fmaxf(__fmul_rn(__fsub_rn(v[i], q.z), q.rs), 0.0f), 3.0f);
+      const float rr = __fadd_rn(t, 12582912.0f);
+      pack(32 * cb + i, __float_as_uint(rr) & 3u);
+      v[i] = fabsf(__fsub_rn(t, __fsub_rn(rr, 12582912.0f)));
+    }
+#pragma unroll
+    for (int st = 16; st >= 1; st >>= 1)
+#pragma unroll
+      for (int i = 0; i < st; ++i) v[i] = fmaxf(v[i], v[i + st]);
+    emax = fmaxf(emax, v[0]);
+  }
+  // warp-uniform: the re-read is a warp-collective tensor-memory load, and a
+  // lane without a near tie recomputes its own codes unchanged
+  if (__any_sync(0xffffffffu, emax >= 0.499996185302734375f)) {
+    clear();
+#pragma unroll
+    for (int cb = 0; cb < 2; ++cb) {
+      float v[32];
+      rotated32(cb, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pack(32 * cb + i, quant_code(v[i], q));
+    }
+  }
+
+  return q;
+}
+
 template <int GS, int TENSOR>
 __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap, uint8_t* sm) {
   constexpr int NG = 128 / GS;
@@ -250,7 +367,7 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
   tc_fence_after();
   const uint32_t tmem = *tslot;
   if (tid == 0) {   // R^T hi | lo of this (head, tensor), already in the swizzled operand layout
-    const uint4* src = a.rfrag + ((size_t)g * kFragBlocks + 3 + tensor) * 4096;
+    const uint4* src = a.rfrag + ((size_t)g * kFragBlocks + 1 + tensor) * 4096;
     mbar_expect_tx(bars + 0, kBBytes);
 #pragma unroll
     for (int c = 0; c < 4; ++c) bulk_g2s(sm + kOffB + 16384 * c, src + 1024 * c, 16384, bars + 0);
@@ -318,20 +435,8 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
       __syncthreads();
     }
 
-    // ---- x' = x . R_hi + x . R_lo on the tensor cores: per 16-channel step
-    // the hi term, then the lo term, into one fp32 accumulator ----
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t koff = (ks & 3) * 32;   // 16 channels = 32 bytes into the swizzled row
-        const uint64_t ad = sw128_desc(sA + (ks >> 2) * 16384 + koff);
-        const uint32_t bb = sB + (ks >> 2) * 32768 + koff;   // rows 0-127: hi; 128-255: lo
-        tc_mma(tmem, ad, sw128_desc(bb), kIdesc, ks > 0 ? 1u : 0u);
-        tc_mma(tmem, ad, sw128_desc(bb + 16384), kIdesc, 1u);
-      }
-      tc_commit(smem_u32(bars + 1));
-    }
+    // ---- x' = x . R_hi + x . R_lo on the tensor cores ----
+    if (tid == 0) issue_rotation(tmem, sA, sB, bars + 1);
     ok = mbar_wait(bars + 1, phase, kTcPolls);
     phase ^= 1;
     if (!__syncthreads_and(ok)) break;
@@ -340,94 +445,10 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
     const long long nxt = next_live(cur + 1);
     const bool nxt_tma = (nxt < t1) ? issue_load(chunk_of(a, nxt, false)) : false;
 
-    // ---- this thread's row and channel half: x', clipped; the group range
-    // first, then the codes (the accumulator is read again rather than held in
-    // registers); reductions as trees to keep the dependency chains short ----
-    auto rotated32 = [&](int cb, float (&v)[32]) {
-      uint32_t u[32];
-      tc_ld32(trow + 64 * hf + 32 * cb, u);
-      tc_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = clip_to(__uint_as_float(u[i]), sclip[64 * hf + 32 * cb + i]);
-    };
-    float mn = INFINITY, mx = -INFINITY;
-#pragma unroll
-    for (int cb = 0; cb < 2; ++cb) {
-      float v[32], w[32];
-      rotated32(cb, v);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) w[i] = v[i];
-#pragma unroll
-      for (int st = 16; st >= 1; st >>= 1)
-#pragma unroll
-        for (int i = 0; i < st; ++i) {
-          v[i] = fminf(v[i], v[i + st]);
-          w[i] = fmaxf(w[i], w[i + st]);
-        }
-      mn = fminf(mn, v[0]);
-      mx = fmaxf(mx, w[0]);
-    }
-    if (GS == 128) {   // the group spans both channel halves: combine with warp w ^ 4
-      sstat[hf * 128 + m] = make_float2(mn, mx);
-      __syncthreads();
-      const float2 o = sstat[(hf ^ 1) * 128 + m];
-      mn = fminf(mn, o.x);
-      mx = fmaxf(mx, o.y);
-    }
-    const ScaleZero q = scale_zero(mn, mx);   // the group of these 64 channels
-
-    // ---- codes, straight into this half's storage words (words 2 hf and
-    // 2 hf + 1 of each slot; K: slot (k % 8) / 2 of the token's four, V: slot
-    // c % 8 of the token's eight, k = c % 16) ----
+    // ---- this thread's row and channel half -> s, z and codes ----
     constexpr int NS = (TENSOR == 0) ? 4 : 8;
     uint32_t wd[NS][2];
-    auto clear = [&]() {
-#pragma unroll
-      for (int u = 0; u < NS; ++u) wd[u][0] = wd[u][1] = 0u;
-    };
-    auto pack = [&](int i, uint32_t c) {
-      const int kk = i & 15, s1 = (i >> 4) & 1, lw = i >> 5;
-      if (TENSOR == 0)
-        wd[(kk & 7) >> 1][lw] |= c << (16 * (kk & 1) + 2 * (2 * s1 + 4 * (kk >> 3)));
-      else
-        wd[kk & 7][lw] |= c << (2 * (2 * s1 + (kk >> 3)));
-    };
-    // code = rint(clamp(fl(fl(y - z) * fl(1/s)), 0, 3)): the clamped quotient
-    // plus 1.5 * 2^23 holds rint in its low mantissa bits (round to nearest
-    // even); unless some quotient lies within 2^-18 of a half-integer, where
-    // the IEEE division decides (quant_code).  Out of [0, 3] the clamp leaves
-    // an integer, so only ties inside the range can set the fix-up.
-    clear();
-    float emax = 0.0f;
-#pragma unroll
-    for (int cb = 0; cb < 2; ++cb) {
-      float v[32];
-      rotated32(cb, v);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float t = fminf(fmaxf(__fmul_rn(__fsub_rn(v[i], q.z), q.rs), 0.0f), 3.0f);
-        const float rr = __fadd_rn(t, 12582912.0f);
-        pack(32 * cb + i, __float_as_uint(rr) & 3u);
-        v[i] = fabsf(__fsub_rn(t, __fsub_rn(rr, 12582912.0f)));
-      }
-#pragma unroll
-      for (int st = 16; st >= 1; st >>= 1)
-#pragma unroll
-        for (int i = 0; i < st; ++i) v[i] = fmaxf(v[i], v[i + st]);
-      emax = fmaxf(emax, v[0]);
-    }
-    // warp-uniform: the re-read is a warp-collective tensor-memory load, and a
-    // lane without a near tie recomputes its own codes unchanged
-    if (__any_sync(0xffffffffu, emax >= 0.499996185302734375f)) {
-      clear();
-#pragma unroll
-      for (int cb = 0; cb < 2; ++cb) {
-        float v[32];
-        rotated32(cb, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pack(32 * cb + i, quant_code(v[i], q));
-      }
-    }
+    const ScaleZero q = row_codes<GS, TENSOR>(trow, hf, m, sclip, sstat, wd);
 
     // ---- destination tile of this row ----
     const int pos = k.P0 + m;
@@ -554,6 +575,235 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+
+// ---------------------------------------------------------------------------
+// per-step placement (yunpan.plus write-up, "2. 在线量化与反量化": a new token
+// is written to the recent tier; when that is full its oldest token is
+// rotated, clipped, quantized and packed into the INT2 history)
+// ---------------------------------------------------------------------------
+struct StepArgs {
+  uint8_t* hist;                  // layer base
+  size_t page_bytes, head_block;
+  int tile_bytes, P;
+  uint16_t* sink_k;               // layer bases [max_seqs][Hkv][cap][128]
+  uint16_t* sink_v;
+  uint16_t* rec_k;
+  uint16_t* rec_v;
+  int sink_cap, rec_cap;
+  const uint16_t* k_new;          // [B][Hkv][128]
+  const uint16_t* v_new;
+  int32_t* sink_len;
+  int32_t* hist_len;
+  int32_t* rec_len;
+  int32_t* rec_start;
+  const int32_t* pt;
+  int max_pages, Hkv;
+  long long num_pages;
+  const uint4* rfrag;             // layer base [Hkv][kFragBlocks][4096]
+  const float* clip;              // layer base [2][Hkv][128]
+  int* err;
+};
+
+// The placement of sequence b's new token, from its current lengths:
+// mode 0: sink slot `slot`; 1: recent ring slot `slot`; 2: evict the ring's
+// oldest token (slot `slot`) into history position hist_len, which lands at
+// row `pos` of the tile at byte offset `tile` of the layer's history, then
+// put the new token in that slot; -1: not applied (error code `err`).
+struct StepPlace {
+  int mode, slot, pos, err;
+  long long tile;
+};
+
+__device__ StepPlace step_place(const StepArgs& a, int b) {
+  StepPlace s{-1, 0, 0, 0, 0};
+  const int sl = a.sink_len[b], hl = a.hist_len[b], rl = a.rec_len[b], rs = a.rec_start[b];
+  if (sl < 0 || sl > a.sink_cap || rl < 0 || rl > a.rec_cap || rs < 0 || rs >= a.rec_cap || hl < 0) {
+    s.err = KV_DEVERR_LENGTH;
+  } else if (sl < a.sink_cap) {                    // one of the sequence's first tokens
+    s.mode = 0;
+    s.slot = sl;
+  } else if (rl < a.rec_cap) {                     // the recent ring has room
+    s.mode = 1;
+    s.slot = (rs + rl) % a.rec_cap;
+  } else {                                         // evict the ring's oldest token
+    const int pidx = hl / a.P;
+    const int pid = (pidx < a.max_pages) ? a.pt[(size_t)b * a.max_pages + pidx] : -1;
+    if (pidx >= a.max_pages) {
+      s.err = KV_DEVERR_LENGTH;
+    } else if (pid < 0 || pid >= a.num_pages) {
+      s.err = KV_DEVERR_PAGE_ID;
+    } else {
+      s.mode = 2;
+      s.slot = rs;
+      s.pos = hl % kTile;
+      s.tile = (long long)pid * (long long)a.page_bytes + (long long)((hl % a.P) / kTile) * a.tile_bytes;
+    }
+  }
+  return s;
+}
+
+// Eviction: CTA (128 sequences, KV head g, tensor).  The evicted tokens of
+// the step (the ring's oldest token of every sequence whose ring is full)
+// become the rows of one 128-row chunk, rotated and quantized exactly as the
+// bulk append does it (same MMA, same row_codes); each row then goes into its
+// own tile at its own row, merged with the tile's other rows.  The lengths are
+// read only; the placement kernel that follows moves the new tokens and
+// updates them.
+constexpr uint32_t kOffRows = kOffTmem + 16;
+constexpr uint32_t kEvSmem = kOffRows + 128 * 8 + 128 * 4 + 1024;   // + alignment slack
+
+template <int GS, int TENSOR>
+__device__ __forceinline__ void evict_body(const StepArgs& a, int B, uint8_t* sm) {
+  constexpr int NG = 128 / GS;
+  const uint32_t sA = smem_u32(sm + kOffA), sB = smem_u32(sm + kOffB);
+  float* sclip = reinterpret_cast<float*>(sm + kOffClip);
+  float2* sstat = reinterpret_cast<float2*>(sm + kOffStat);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);   // [0] R copy, [1] MMA done
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kOffTmem);
+  long long* rtile = reinterpret_cast<long long*>(sm + kOffRows);   // byte offset of the row's tile, -1: none
+  int* rpos = reinterpret_cast<int*>(sm + kOffRows + 128 * 8);      // row within the tile
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = blockIdx.y;
+  const int quarter = warp & 3, hf = warp >> 2;
+  const int m = 32 * quarter + lane;
+
+  if (tid == 0) {
+    mbar_init(bars + 0, 1);
+    mbar_init(bars + 1, 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) tc_alloc(smem_u32(tslot), kTcCols);
+  if (tid < 128) sclip[tid] = a.clip[((size_t)TENSOR * a.Hkv + g) * 128 + tid];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (tid == 0) {
+    const uint4* src = a.rfrag + ((size_t)g * kFragBlocks + 1 + TENSOR) * 4096;
+    mbar_expect_tx(bars + 0, kBBytes);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) bulk_g2s(sm + kOffB + 16384 * c, src + 1024 * c, 16384, bars + 0);
+  }
+  {   // the evicted rows -> the swizzled A operand (thread t: row t % 128, channel half t / 128)
+    const int row = tid & 127, hh = tid >> 7;
+    const int b = blockIdx.x * kChunk + row;
+    StepPlace pl{-1, 0, 0, 0, 0};
+    if (b < B) pl = step_place(a, b);
+    const bool ev = pl.mode == 2;
+    if (hh == 0) {
+      rtile[row] = ev ? pl.tile : -1;
+      rpos[row] = pl.pos;
+    }
+    const uint16_t* rec = TENSOR ? a.rec_v : a.rec_k;
+    const uint16_t* src = rec + (ev ? (((size_t)b * a.Hkv + g) * a.rec_cap + pl.slot) * 128 : 0) + 64 * hh;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      cp_async16_zfill(sA + hh * 16384 + row * 128 + ((c ^ (row & 7)) << 4), src + 8 * c, ev);
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+  }
+  fence_async_smem();
+  bool ok = mbar_wait(bars + 0, 0, kTcPolls);
+  if (__syncthreads_and(ok)) {
+    if (tid == 0) issue_rotation(tmem, sA, sB, bars + 1);
+    ok = mbar_wait(bars + 1, 0, kTcPolls);
+    ok = __syncthreads_and(ok);
+    if (!ok && tid == 0) {
+      flag_error(a.err, KV_DEVERR_TIMEOUT);
+      mbar_wait(bars + 1, 0, kTcPolls);   // the MMAs in flight, bounded
+    }
+  } else if (tid == 0) {
+    flag_error(a.err, KV_DEVERR_TIMEOUT);
+    mbar_wait(bars + 0, 0, kTcPolls);     // the copies in flight, bounded
+  }
+  if (ok) {
+    tc_fence_after();
+    constexpr int NS = (TENSOR == 0) ? 4 : 8;
+    uint32_t wd[NS][2];
+    const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+    const ScaleZero q = row_codes<GS, TENSOR>(trow, hf, m, sclip, sstat, wd);
+    const long long tof = rtile[m];
+    if (tof >= 0) {
+      const int pos = rpos[m];
+      uint8_t* tb = a.hist + tof + (size_t)g * a.head_block;
+      if constexpr (TENSOR == 0) {
+        // K: the row's codes at pairs + pos / 8 of its four slots 4 * (pos % 8) + j
+        const int mh = pos >> 3;
+        const uint32_t mask = mh ? 0xCCCCCCCCu : 0x33333333u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t w2[2] = {wd[j][0] << (2 * mh), wd[j][1] << (2 * mh)};
+          store_merge2(tb + 16 * (4 * (pos & 7) + j) + 8 * hf, w2, mask);
+        }
+        if (GS == 64 || hf == 0) {
+          __half2* rec = reinterpret_cast<__half2*>(tb + 1024 + (2 * (pos & 7) + mh) * 8 * NG);
+          rec[GS == 64 ? hf : 0] = __halves2half2(q.sh, q.zh);
+        }
+      } else {
+        // V: the token's codes in byte (pos / 8) of half (pos % 2) of its eight
+        // slots 4 * m8 + (pos % 8) / 2
+        const int ek = pos & 1, kh = pos >> 3, jk = (pos & 7) >> 1, sh = 16 * ek + 8 * kh;
+        const uint32_t mask = (kh ? 0xFF00u : 0x00FFu) << (16 * ek);
+#pragma unroll
+        for (int m8 = 0; m8 < 8; ++m8) {
+          const uint32_t w2[2] = {wd[m8][0] << sh, wd[m8][1] << sh};
+          store_merge2(tb + 512 + 16 * (4 * m8 + jk) + 8 * hf, w2, mask);
+        }
+        if (GS == 64 || hf == 0) {
+          __half2* rec = reinterpret_cast<__half2*>(tb + 1024 + (2 * (pos & 7) + kh) * 8 * NG) + NG;
+          rec[GS == 64 ? hf : 0] = __halves2half2(q.sh, q.zh);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc_dealloc(tmem, kTcCols);
+  if (tid == 0) {
+    mbar_inval(bars + 0);
+    mbar_inval(bars + 1);
+  }
+}
+
+template <int GS>
+__global__ void __launch_bounds__(kTcThreads, 2) evict_tc_kernel(StepArgs a, int B) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  if (blockIdx.z == 0)
+    evict_body<GS, 0>(a, B, sm);
+  else
+    evict_body<GS, 1>(a, B, sm);
+}
+
+// Placement after the eviction: CTA b copies sequence b's new K and V token of
+// every KV head into its sink or ring slot (the evicted slot included), then
+// updates the lengths from the same decision on the unchanged lengths.
+__global__ void step_place_kernel(StepArgs a, int B) {
+  const int b = blockIdx.x;
+  const StepPlace pl = step_place(a, b);
+  if (pl.mode >= 0) {
+    for (int i = threadIdx.x; i < 2 * a.Hkv * 32; i += blockDim.x) {
+      const int t = i / (a.Hkv * 32), g = (i >> 5) % a.Hkv, w = i & 31;
+      const size_t sh = (size_t)b * a.Hkv + g;
+      const uint16_t* src = (t ? a.v_new : a.k_new) + sh * 128;
+      uint16_t* dst = (pl.mode == 0) ? (t ? a.sink_v : a.sink_k) + (sh * a.sink_cap + pl.slot) * 128
+                                     : (t ? a.rec_v : a.rec_k) + (sh * a.rec_cap + pl.slot) * 128;
+      *reinterpret_cast<uint2*>(dst + 4 * w) = *reinterpret_cast<const uint2*>(src + 4 * w);
+    }
+  }
+  __syncthreads();   // every thread has read the lengths
+  if (threadIdx.x == 0) {
+    if (pl.mode == 0) {
+      a.sink_len[b] = pl.slot + 1;
+    } else if (pl.mode == 1) {
+      a.rec_len[b] += 1;
+    } else if (pl.mode == 2) {
+      a.hist_len[b] += 1;
+      a.rec_start[b] = (pl.slot + 1) % a.rec_cap;
+    } else {
+      flag_error(a.err, pl.err);
+    }
+  }
+}
 }  // namespace
 
 cudaError_t launch_append_tc(const Pool& p, int layer, int n_seqs, const void* k, const void* v,
@@ -624,6 +874,55 @@ cudaError_t launch_append_tc(const Pool& p, int layer, int n_seqs, const void* k
     if (e == cudaSuccess) e = go(append_tc_kernel<128, 1>, 1, 1);
   }
   return e;
+}
+
+cudaError_t launch_append_step(const Pool& p, int layer, int B, const void* k_new,
+                               const void* v_new, int32_t* sink_len, int32_t* hist_len,
+                               int32_t* rec_len, int32_t* rec_start, const int32_t* pt,
+                               int max_pages, cudaStream_t s) {
+  if (B == 0) return cudaSuccess;
+  const int H = p.cfg.num_kv_heads;
+  StepArgs a{};
+  a.hist = p.hist + (size_t)layer * p.hist_layer_stride;
+  a.page_bytes = p.page_bytes;
+  a.head_block = p.page_bytes / H;
+  a.tile_bytes = (int)p.tile_bytes;
+  a.P = p.cfg.page_size;
+  a.sink_k = p.sink_k + (size_t)layer * p.sink_layer_stride;
+  a.sink_v = p.sink_v + (size_t)layer * p.sink_layer_stride;
+  a.rec_k = p.rec_k + (size_t)layer * p.rec_layer_stride;
+  a.rec_v = p.rec_v + (size_t)layer * p.rec_layer_stride;
+  a.sink_cap = p.cfg.sink_tokens;
+  a.rec_cap = p.cfg.recent_tokens;
+  a.k_new = static_cast<const uint16_t*>(k_new);
+  a.v_new = static_cast<const uint16_t*>(v_new);
+  a.sink_len = sink_len;
+  a.hist_len = hist_len;
+  a.rec_len = rec_len;
+  a.rec_start = rec_start;
+  a.pt = pt;
+  a.max_pages = max_pages;
+  a.Hkv = H;
+  a.num_pages = p.cfg.num_pages;
+  a.rfrag = p.rfrag + (size_t)layer * H * kFragBlocks * rfrag_per_head();
+  a.clip = p.clip + (size_t)layer * 2 * H * 128;
+  a.err = p.err;
+  static bool attr[2] = {false, false};
+  auto evict = [&](auto kernel, int gi) -> cudaError_t {
+    if (!attr[gi]) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kEvSmem);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      if (e != cudaSuccess) return e;
+      attr[gi] = true;
+    }
+    kernel<<<dim3((unsigned)((B + kChunk - 1) / kChunk), H, 2), kTcThreads, kEvSmem, s>>>(a, B);
+    return cudaGetLastError();
+  };
+  cudaError_t e = (p.cfg.group_size == 64) ? evict(evict_tc_kernel<64>, 0) : evict(evict_tc_kernel<128>, 1);
+  if (e != cudaSuccess) return e;
+  step_place_kernel<<<B, 128, 0, s>>>(a, B);
+  return cudaGetLastError();
 }
 
 }  // namespace kvint2

@@ -600,7 +600,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
   }
 
   // ---- q' = q R_k and its per-group sums (overlaps the first copies) ----
-  rotate_q<S::HP, NW>(sq, a.rfrag + ((size_t)g * kFragBlocks + 2) * 4096, sqr);
+  rotate_q<S::HP, NW>(sq, a.rfrag + ((size_t)g * kFragBlocks + 0) * 4096, sqr);
   for (int hh = warp; hh < S::HP; hh += NW) {
 #pragma unroll
     for (int grp = 0; grp < NG; ++grp) {

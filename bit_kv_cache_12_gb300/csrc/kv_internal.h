@@ -37,19 +37,17 @@ struct Pool {
   float* Rk = nullptr;              // [layer][Hkv][128][128]  x' = x Rk
   float* RvT = nullptr;             // [layer][Hkv][128][128]  RvT[i][c] = Rv[c][i]
   float* clip = nullptr;            // [layer][2][Hkv][128]
-  uint4* rfrag = nullptr;           // [layer][Hkv][kFragBlocks][4096] bf16 hi/lo MMA fragments
+  uint4* rfrag = nullptr;           // [layer][Hkv][kFragBlocks][4096] rotation operands (below)
   unsigned* tickets = nullptr;      // [layer][max_seqs][Hkv] split-merge counters
   int* err = nullptr;               // device error word
 };
 
-// Rotation fragments per (layer, KV head), 4096 uint4 each (bf16 hi/lo pairs):
-//   block 0: B operand of x . R_k        (per-step append K, mma.sync fragments)
-//   block 1: A operand of R_v^T . x^T    (per-step append V, mma.sync fragments)
-//   block 2: B operand of q . R_k as fp16 hi/lo pairs (decode q' = q R_k)
-//   block 3: tcgen05 B operand of x . R_k: rows n of [R_k^T hi ; R_k^T lo] (256 x 128
-//            bf16), K-major, 128-byte swizzle, channels 0-63 then 64-127 (bulk append K)
-//   block 4: the same for R_v (bulk append V)
-constexpr int kFragBlocks = 5;
+// Rotation operands per (layer, KV head), 4096 uint4 (64 KB) each:
+//   block 0: mma.sync B operand of q . R_k as fp16 hi/lo pairs (decode q' = q R_k)
+//   block 1: tcgen05 B operand of x . R_k: rows n of [R_k^T hi ; R_k^T lo] (256 x 128
+//            bf16), K-major, 128-byte swizzle, channels 0-63 then 64-127 (append K)
+//   block 2: the same for R_v (append V)
+constexpr int kFragBlocks = 3;
 inline size_t rfrag_per_head() { return 4096; }   // uint4 per (head, block)
 
 // ---- launchers (return cudaSuccess or the launch error) --------------------
