@@ -473,23 +473,47 @@ def run_decode(args, c, wl, torch, dev, rank, world, local, kvdist):
     if pool.error() or bpool.error():
         raise RuntimeError("device error during the timed steps")
 
-    # ---- end to end through the C ABI with host buffers ----
-    q_host = torch.from_numpy(c.q_np.view(np.int16)).view(torch.bfloat16).pin_memory()
-    meta_host = torch.from_numpy(np.stack([c.sink_len, c.hist_len, c.rec_len, c.rec_start]).astype(np.int32)).pin_memory()
-    meta_dev = torch.empty_like(meta_host, device=dev)
+    # ---- end to end through the C ABI with host buffers: the step's inputs
+    # (q and the four length arrays) in one pinned staging buffer, one copy in,
+    # the output copied back ----
+    q_bytes = B * Hq * 128 * 2
+    meta = np.stack([c.sink_len, c.hist_len, c.rec_len, c.rec_start]).astype(np.int32)
+    stage_host = torch.empty(q_bytes + meta.nbytes, dtype=torch.uint8).pin_memory()
+    stage_host[:q_bytes].copy_(torch.from_numpy(np.ascontiguousarray(c.q_np).view(np.uint8).reshape(-1)))
+    stage_host[q_bytes:].copy_(torch.from_numpy(meta.view(np.uint8).reshape(-1)))
+    stage_dev = torch.empty_like(stage_host, device=dev)
+    q_dev = stage_dev[:q_bytes].view(torch.bfloat16).view(B, Hq, 128)
+    meta_dev = stage_dev[q_bytes:].view(torch.int32).view(4, B)
     out_host = torch.empty((B, Hq, 128), dtype=torch.float32).pin_memory()
 
     def e2e_step():
-        q.copy_(q_host, non_blocking=True)
-        meta_dev.copy_(meta_host, non_blocking=True)
-        native.kv_decode_attention(pool.handle, 0, B, q, meta_dev[0], meta_dev[1], meta_dev[2],
+        stage_dev.copy_(stage_host, non_blocking=True)
+        native.kv_decode_attention(pool.handle, 0, B, q_dev, meta_dev[0], meta_dev[1], meta_dev[2],
                                    meta_dev[3], pt, c.page_table.shape[1], max_hist, c.scale, out,
                                    ws, ws_bytes, stream)
         out_host.copy_(out, non_blocking=True)
 
     t_e2e = timed(e2e_step, args.steps, 3)
-    h2d = q_host.numel() * 2 + meta_host.numel() * 4
+    h2d = stage_host.numel()
     d2h = out_host.numel() * 4
+
+    # ---- several queries per sequence over the same cache (two positions of a
+    # chunk, or a draft and its successor), with the log-sum-exp ----
+    TQ = 2
+    qm = torch.randn(B, TQ, Hq, 128, generator=torch.Generator(device=dev).manual_seed(9),
+                     device=dev).to(torch.bfloat16)
+    m_ws_bytes = native.kv_decode_multi_workspace_bytes(pool.handle, B, TQ, max_hist)
+    m_ws = torch.zeros(m_ws_bytes // 4 + 4, dtype=torch.float32, device=dev)
+    m_out = torch.empty((B, TQ, Hq, 128), dtype=torch.float32, device=dev)
+    m_lse = torch.empty((B, TQ, Hq), dtype=torch.float32, device=dev)
+
+    def mstep():
+        native.kv_decode_attention_multi(pool.handle, 0, B, TQ, qm, sink_len, hist_len, rec_len, rec_start,
+                                         pt, c.page_table.shape[1], max_hist, c.scale, m_out, m_lse, m_ws,
+                                         m_ws_bytes, stream)
+
+    t_multi = (timed(mstep, max(5, args.steps // 2), 3)
+               if TQ * (Hq // Hkv) <= 8 else None)
 
     # ---- per-step token placement at batch 64 (every sequence evicts one
     # recent token into INT2 history per step) ----
@@ -536,11 +560,15 @@ def run_decode(args, c, wl, torch, dev, rank, world, local, kvdist):
                           "gbs": bf16_bytes(c) / (us_bf16 * 1e-6) / 1e9,
                           "speedup_int2_vs_bf16": us_bf16 / us},
             "append_step": {"us": float(np.mean(t_step) * 1e3), "batch": SB, "kv_heads": SH,
-                            "what": "one kv_append_step launch: each sequence's new token enters the "
+                            "what": "one kv_append_step call (eviction and placement launches): each sequence's new token enters the "
                                     "recent ring and its oldest recent token is rotated, clipped, "
                                     "quantized and packed into INT2 history"},
             "e2e": {"value": us_e2e, "unit": "us", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h)},
+            "multi_query": (None if t_multi is None else
+                            {"us": float(np.mean(t_multi) * 1e3), "queries_per_sequence": TQ,
+                             "what": "one kv_decode_attention_multi call over the same cache, "
+                                     "output and log-sum-exp"}),
             "gpu_launches": args.steps,
             "clocks": clk.summary(),
             "cpu_baseline": cb,
