@@ -171,6 +171,7 @@ struct TcArgs {
   const int32_t* pt;
   int max_pages, n_seqs, max_chunks, Hkv;
   long long num_pages;
+  long long map_rows;         // row extent of the x tensor maps (n_seqs * max_tokens)
   const uint4* rfrag;         // layer base [Hkv][kFragBlocks][4096]
   const float* clip;          // layer base [2][Hkv][128]
   int* err;
@@ -184,10 +185,10 @@ struct Chunk {
   bool live;
 };
 
-__device__ __forceinline__ Chunk chunk_of(const TcArgs& a, long long task, bool flag) {
+__device__ __forceinline__ Chunk chunk_of(const TcArgs& a, int task, bool flag) {
   Chunk k;
-  k.b = (int)(task / a.max_chunks);
-  const int ci = (int)(task % a.max_chunks);
+  k.b = task / a.max_chunks;
+  const int ci = task % a.max_chunks;
   k.c0 = __ldg(a.cu + k.b);
   k.nb = __ldg(a.cu + k.b + 1) - k.c0;
   k.h0 = __ldg(a.hist_start + k.b);
@@ -373,23 +374,24 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
     for (int c = 0; c < 4; ++c) bulk_g2s(sm + kOffB + 16384 * c, src + 1024 * c, 16384, bars + 0);
   }
   const uint16_t* X = tensor ? a.x[1] : a.x[0];
-  const long long total = (long long)a.n_seqs * a.max_chunks;
-  const long long t0 = (long long)blockIdx.x * a.tasks_per_cta;
-  const long long t1 = min(total, t0 + a.tasks_per_cta);
-  auto next_live = [&](long long t) {
+  const int total = a.n_seqs * a.max_chunks;
+  const int t0 = blockIdx.x * a.tasks_per_cta;
+  const int t1 = min(total, t0 + a.tasks_per_cta);
+  auto next_live = [&](int t) {
     for (; t < t1; ++t)
       if (chunk_of(a, t, tid == 0).live) return t;
     return t1;
   };
   // x of a chunk: two TMA tile loads by one thread when all 128 rows lie
-  // below the input's row count T (rows below 0 read as zero); otherwise,
-  // so that nothing past the caller's buffer is read, 16-byte copies by every
-  // thread with rows outside the chunk's append range zero-filled
-  const int T_rows = __ldg(a.cu + a.n_seqs);
+  // below the input's row count T and inside the tensor map (rows below 0 read
+  // as zero); otherwise, so that nothing past the caller's buffer is read and
+  // no row of the chunk is lost, 16-byte copies by every thread with rows
+  // outside the chunk's append range zero-filled
+  const int row_lim = (int)min((long long)__ldg(a.cu + a.n_seqs), a.map_rows);
   uint32_t xphase = 0;
   auto issue_load = [&](const Chunk& k) -> bool {
     const int r0 = k.c0 + (k.P0 - k.h0);
-    if (r0 + kChunk <= T_rows) {
+    if (r0 + kChunk <= row_lim) {
       if (tid == 0) {
         mbar_expect_tx(bars + 2, kABytes);
         tma_load_x(sA, xmap, 0, g, r0, bars + 2);
@@ -400,7 +402,7 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
     load_chunk(a, X, g, k, sA);
     return false;
   };
-  long long cur = next_live(t0);
+  int cur = next_live(t0);
   bool cur_tma = (cur < t1) ? issue_load(chunk_of(a, cur, false)) : false;
 
   bool ok = mbar_wait(bars + 0, 0, kTcPolls);   // R is needed before the first MMA
@@ -442,7 +444,7 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
     if (!__syncthreads_and(ok)) break;
     tc_fence_after();
     // the A buffer is consumed: bring in the next chunk behind this epilogue
-    const long long nxt = next_live(cur + 1);
+    const int nxt = next_live(cur + 1);
     const bool nxt_tma = (nxt < t1) ? issue_load(chunk_of(a, nxt, false)) : false;
 
     // ---- this thread's row and channel half -> s, z and codes ----
@@ -827,10 +829,12 @@ cudaError_t launch_append_tc(const Pool& p, int layer, int n_seqs, const void* k
   a.max_chunks = (max_tiles + kTilesPerChunk - 1) / kTilesPerChunk;
   a.Hkv = H;
   a.num_pages = p.cfg.num_pages;
+  a.map_rows = (long long)n_seqs * max_tokens;
   a.rfrag = p.rfrag + (size_t)layer * H * kFragBlocks * rfrag_per_head();
   a.clip = p.clip + (size_t)layer * 2 * H * 128;
   a.err = p.err;
   const long long tasks = (long long)n_seqs * a.max_chunks;
+  if (tasks >= (1LL << 31)) return cudaErrorInvalidValue;   // task indices are 32-bit
   // x viewed as (128 channels, Hkv heads, rows); the row extent n_seqs * max_tokens
   // bounds the input's row count T, and the kernel uses the map only for boxes below T
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();

@@ -102,7 +102,7 @@ struct DecodeArgs {
 
 // Shared-memory carve-up (in floats) for a CTA of NW warps.  A fixed head
 // (q, q', page ids, merged m/l) is followed by one region reused by phase:
-// the history warps' cp.async rings, or a tier CTA's staged rows and softmax
+// the history warps' bulk-copy rings, or a tier CTA's staged rows and softmax
 // weights, then the per-warp results; the final merge reuses everything.
 template <int G, int GS, int NW, bool kInt2>
 struct Lay {

@@ -170,7 +170,8 @@ kv_status_t kv_quantize_pack_f32(kv_pool_t* pool, int32_t layer, int32_t tensor,
 /* Fused append (the eviction step of the yunpan.plus write-up section 2):
  * rotate by R_k / R_v, clip, quantize and pack K and V tokens into the INT2
  * history pages of `layer`.
- *   k, v        device bf16 [T][Hkv][128], T = cu_tokens[n_seqs]
+ *   k, v        device bf16 [T][Hkv][128], T = cu_tokens[n_seqs], 16-byte
+ *               aligned (else KV_ERR_INVALID_ARG)
  *   cu_tokens   device int32 [n_seqs+1], prefix sums of tokens per sequence
  *   hist_start  device int32 [n_seqs]: history position of each sequence's
  *               first appended token (its tokens go to consecutive positions)
@@ -179,8 +180,9 @@ kv_status_t kv_quantize_pack_f32(kv_pool_t* pool, int32_t layer, int32_t tensor,
  *   max_tokens_per_seq  host bound on tokens of any one sequence (sizes the
  *               grid; sequences above it are flagged and truncated)
  * Tiles partly covered keep the other tokens' bits (appends may continue a
- * partly filled page).  Rotation runs on tensor cores with R split into two
- * bf16 terms (about 16 significant bits). */
+ * partly filled page).  Rotation runs on the tcgen05 tensor cores with R split
+ * into two bf16 terms (about 16 significant bits), fp32 accumulation; the
+ * codes equal those of kv_append_step for the same token. */
 kv_status_t kv_append_quantize(kv_pool_t* pool, int32_t layer, int32_t n_seqs,
                                const void* k, const void* v, const int32_t* cu_tokens,
                                const int32_t* hist_start, const int32_t* page_table,
