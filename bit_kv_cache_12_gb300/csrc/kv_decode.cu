@@ -319,6 +319,17 @@ __device__ void merge_parts(const DecodeArgs& a, int b, int g, int nparts, float
   float* sf = sacc + NSUB * G * 128;               // [nparts * G] m, then weights
   float* sl = sf + nparts * G;                     // [nparts * G]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cq = lane, h = warp % G, sub = warp / G;
+  // this warp's first kPre value vectors, loaded in the same round as m and l
+  constexpr int kPre = 8;
+  float4 pre[kPre];
+#pragma unroll
+  for (int u = 0; u < kPre; ++u) {
+    const int s = sub + u * NSUB;
+    pre[u] = (s < nparts)
+                 ? __ldcg(reinterpret_cast<const float4*>(base + (size_t)(s * G + h) * kPart + 4) + cq)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   for (int i = threadIdx.x; i < nparts * G; i += NW * 32) {
     sf[i] = __ldcg(base + (size_t)i * kPart);
     sl[i] = __ldcg(base + (size_t)i * kPart + 1);
@@ -343,10 +354,18 @@ __device__ void merge_parts(const DecodeArgs& a, int b, int g, int nparts, float
   }
   __syncthreads();
   {
-    const int cq = lane, h = warp % G, sub = warp / G;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+      const int s = sub + u * NSUB;
+      const float f = (s < nparts) ? sf[s * G + h] : 0.f;
+      acc.x = fmaf(f, pre[u].x, acc.x);
+      acc.y = fmaf(f, pre[u].y, acc.y);
+      acc.z = fmaf(f, pre[u].z, acc.z);
+      acc.w = fmaf(f, pre[u].w, acc.w);
+    }
 #pragma unroll 8
-    for (int s = sub; s < nparts; s += NSUB) {
+    for (int s = sub + kPre * NSUB; s < nparts; s += NSUB) {
       const float f = sf[s * G + h];
       const float4 o =
           __ldcg(reinterpret_cast<const float4*>(base + (size_t)(s * G + h) * kPart + 4) + cq);
