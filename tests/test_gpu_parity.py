@@ -128,6 +128,60 @@ def test_append_matches_oracle(gs, P):
     pool.close()
 
 
+def _append(aw, page_table, max_tokens):
+    pool = native.KVPool(native.KV_POOL_INT2_3TIER, 1, 2 * aw.Hkv, aw.Hkv, aw.page_size, aw.num_pages,
+                         aw.n_seqs, group_size=aw.group_size)
+    native.kv_pool_set_rotation(pool.handle, 0, gu.f32_dev(aw.Rk), gu.f32_dev(aw.Rv),
+                                gu.f32_dev(aw.clip_k), gu.f32_dev(aw.clip_v))
+    native.kv_append_quantize(pool.handle, 0, aw.n_seqs, gu.bf16_dev(aw.k), gu.bf16_dev(aw.v),
+                              gu.i32_dev(aw.cu_tokens), gu.i32_dev(aw.hist_start), gu.i32_dev(page_table),
+                              page_table.shape[1], max_tokens)
+    torch.cuda.synchronize()
+    err = pool.error()
+    pages = pool.hist_view(0).cpu().numpy()
+    pool.close()
+    return err, pages
+
+
+def _seq_ok(aw, pages, b, n=None):
+    sl = slice(aw.cu_tokens[b], aw.cu_tokens[b + 1])
+    n = int(aw.tokens_per_seq[b]) if n is None else n
+    bad, tot = _compare_codes(pages, aw.k[sl][:n], aw.v[sl][:n], aw, b, int(aw.hist_start[b]), n)
+    assert bad <= max(4, 1e-4 * tot), (b, bad, tot)
+
+
+def test_append_missing_page_and_empty_sequence():
+    """A sequence whose last page id is missing: KV_DEVERR_PAGE_ID, its other
+    pages and every other sequence still hold the oracle's codes; an empty
+    sequence between them is no error."""
+    aw = synth.make_append_workload("apppid", 91, n_seqs=4, Hkv=2, tokens_per_seq=[120, 0, 90, 100],
+                                    hist_start=[0, 0, 0, 5], page_size=16, group_size=128)
+    pt = aw.page_table.copy()
+    pt[2, (90 - 1) // 16] = -1                      # positions 80..89 have no page
+    err, pages = _append(aw, pt, 128)
+    assert err == 1                                 # KV_DEVERR_PAGE_ID
+    _seq_ok(aw, pages, 0)
+    _seq_ok(aw, pages, 3)
+    _seq_ok(aw, pages, 2, n=80)
+
+
+def test_append_over_length_keeps_later_sequences_exact():
+    """A sequence far above max_tokens_per_seq: KV_DEVERR_LENGTH.  The input
+    rows of the valid sequence after it lie beyond n_seqs * max_tokens_per_seq
+    rows, where the tensor-map loads stop; its chunks take the per-thread copies
+    and its codes stay the oracle's."""
+    aw = synth.make_append_workload("applen", 92, n_seqs=4, Hkv=2, tokens_per_seq=[120, 600, 100, 128],
+                                    page_size=16, group_size=64)
+    # sequences 2 and 3: every 128-row chunk lies below T but past the map's 4 * 128 rows
+    assert aw.cu_tokens[2] >= 4 * 128 and aw.cu_tokens[2] + 128 <= aw.cu_tokens[4]
+    err, pages = _append(aw, aw.page_table, 128)
+    assert err == 2                                 # KV_DEVERR_LENGTH
+    _seq_ok(aw, pages, 0)
+    _seq_ok(aw, pages, 2)
+    _seq_ok(aw, pages, 3)
+    _seq_ok(aw, pages, 1, n=256)                    # the chunks the grid covers
+
+
 def test_append_continues_partial_tiles():
     """Two appends into the same pages (unaligned split) equal one append."""
     aw = synth.make_append_workload("cont", 77, n_seqs=1, Hkv=2, tokens_per_seq=45, page_size=32,
