@@ -123,6 +123,20 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&v)[32]) {
       : "r"(taddr)
       : "memory");
 }
+// 32 consecutive fp32 columns of this thread's accumulator row, written back
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tc_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void tc_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -254,18 +268,31 @@ __device__ __forceinline__ void issue_rotation(uint32_t tmem, uint32_t sA, uint3
 template <int GS, int TENSOR, int NS>
 __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, const float* sclip, float2* sstat,
                                                uint32_t (&wd)[NS][2]) {
+  // first pass: x' clipped, written back in place (the second pass reads the
+  // clipped values), and its range
+  auto clipped32 = [&](int cb, float (&v)[32]) {
+    uint32_t u[32];
+    tc_ld32(trow + 64 * hf + 32 * cb, u);
+    tc_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      v[i] = clip_to(__uint_as_float(u[i]), sclip[64 * hf + 32 * cb + i]);
+      u[i] = __float_as_uint(v[i]);
+    }
+    tc_st32(trow + 64 * hf + 32 * cb, u);
+  };
   auto rotated32 = [&](int cb, float (&v)[32]) {
     uint32_t u[32];
     tc_ld32(trow + 64 * hf + 32 * cb, u);
     tc_wait_ld();
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = clip_to(__uint_as_float(u[i]), sclip[64 * hf + 32 * cb + i]);
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(u[i]);
   };
   float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
   for (int cb = 0; cb < 2; ++cb) {
     float v[32], w[32];
-    rotated32(cb, v);
+    clipped32(cb, v);
 #pragma unroll
     for (int i = 0; i < 32; ++i) w[i] = v[i];
 #pragma unroll
@@ -286,6 +313,7 @@ __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, con
     mx = fmaxf(mx, o.y);
   }
   const ScaleZero q = scale_zero(mn, mx);   // the group of these 64 channels
+  tc_wait_st();                             // the clipped values are in place
 
   auto clear = [&]() {
 #pragma unroll
