@@ -319,13 +319,16 @@ __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, con
 #pragma unroll
     for (int u = 0; u < NS; ++u) wd[u][0] = wd[u][1] = 0u;
   };
-  auto pack = [&](int i, uint32_t c) {
-    const int kk = i & 15, s1 = (i >> 4) & 1, lw = i >> 5;
-    if (TENSOR == 0)
-      wd[(kk & 7) >> 1][lw] |= c << (16 * (kk & 1) + 2 * (2 * s1 + 4 * (kk >> 3)));
-    else
-      wd[kk & 7][lw] |= c << (2 * (2 * s1 + (kk >> 3)));
+  // storage word and bit position of channel i of this half
+  auto word_of = [&](int i) -> uint32_t& {
+    const int kk = i & 15, lw = i >> 5;
+    return (TENSOR == 0) ? wd[(kk & 7) >> 1][lw] : wd[kk & 7][lw];
   };
+  auto pos_of = [](int i) -> int {
+    const int kk = i & 15, s1 = (i >> 4) & 1;
+    return (TENSOR == 0) ? 16 * (kk & 1) + 2 * (2 * s1 + 4 * (kk >> 3)) : 2 * (2 * s1 + (kk >> 3));
+  };
+  auto pack = [&](int i, uint32_t c) { word_of(i) |= c << pos_of(i); };
   // code = rint(clamp(fl(fl(y - z) * fl(1/s)), 0, 3)): the clamped quotient
   // plus 1.5 * 2^23 holds rint in its low mantissa bits (round to nearest
   // even); unless some quotient lies within 2^-18 of a half-integer, where
@@ -341,7 +344,11 @@ __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, con
     for (int i = 0; i < 32; ++i) {
       const float t = fminf(fmaxf(__fmul_rn(__fsub_rn(v[i], q.z), q.rs), 0.0f), 3.0f);
       const float rr = __fadd_rn(t, 12582912.0f);
-      pack(32 * cb + i, __float_as_uint(rr) & 3u);
+      // the bits of rr are 0x4B400000 + code: one integer multiply-add places
+      // the code (the constant offsets of a word fold into one; codes do not
+      // overlap, so the sum is the OR)
+      const int pos = pos_of(32 * cb + i);
+      word_of(32 * cb + i) += __float_as_uint(rr) * (1u << pos) - (0x4B400000u << pos);
       v[i] = fabsf(__fsub_rn(t, __fsub_rn(rr, 12582912.0f)));
     }
 #pragma unroll
