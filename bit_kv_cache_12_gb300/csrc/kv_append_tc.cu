@@ -262,9 +262,9 @@ __device__ __forceinline__ void issue_rotation(uint32_t tmem, uint32_t sA, uint3
 // storage words of this channel half (words 2 hf and 2 hf + 1 of each slot; K:
 // slot (k % 8) / 2 of the token's four, V: slot c % 8 of the token's eight,
 // k = c % 16) at the bit positions of token row 0 of a tile (K) or of tile
-// token 0 (V); the caller shifts them to the row's own positions.  Every
-// thread of the CTA calls this (group 128 combines the two halves through
-// shared memory with a barrier).
+// token 0 (V); the caller shifts them to the row's own positions.  Both warps
+// of a lane quarter (w and w + 4) call this together: group 128 combines their
+// two halves through shared memory behind a named barrier of those 64 threads.
 template <int GS, int TENSOR, int NS>
 __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, const float* sclip, float2* sstat,
                                                uint32_t (&wd)[NS][2]) {
@@ -307,7 +307,12 @@ __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, con
   }
   if (GS == 128) {   // the group spans both channel halves: combine with warp w ^ 4
     sstat[hf * 128 + m] = make_float2(mn, mx);
-    __syncthreads();
+    switch (m >> 5) {   // named barrier 1 + quarter: warps m/32 and m/32 + 4 (barrier 0 is the CTA's)
+      case 0: asm volatile("bar.sync 1, 64;" ::: "memory"); break;
+      case 1: asm volatile("bar.sync 2, 64;" ::: "memory"); break;
+      case 2: asm volatile("bar.sync 3, 64;" ::: "memory"); break;
+      default: asm volatile("bar.sync 4, 64;" ::: "memory"); break;
+    }
     const float2 o = sstat[(hf ^ 1) * 128 + m];
     mn = fminf(mn, o.x);
     mx = fmaxf(mx, o.y);
@@ -638,6 +643,7 @@ struct StepArgs {
   long long num_pages;
   const uint4* rfrag;             // layer base [Hkv][kFragBlocks][4096]
   const float* clip;              // layer base [2][Hkv][128]
+  unsigned* tickets;              // layer base [ceil(max_seqs / 128)]
   int* err;
 };
 
@@ -679,15 +685,16 @@ __device__ StepPlace step_place(const StepArgs& a, int b) {
   return s;
 }
 
-// Eviction: CTA (128 sequences, KV head g, tensor).  The evicted tokens of
-// the step (the ring's oldest token of every sequence whose ring is full)
-// become the rows of one 128-row chunk, rotated and quantized exactly as the
-// bulk append does it (same MMA, same row_codes); each row then goes into its
-// own tile at its own row, merged with the tile's other rows.  The lengths are
-// read only; the placement kernel that follows moves the new tokens and
-// updates them.
+// One launch per step: CTA (128 sequences, KV head g, tensor).  The evicted
+// tokens of the step (the ring's oldest token of every sequence whose ring is
+// full) become the rows of one 128-row chunk, rotated and quantized exactly as
+// the bulk append does it (same MMA, same row_codes); each row then goes into
+// its own tile at its own row, merged with the tile's other rows.  Once a
+// thread's copy of the old slot contents has landed it writes the new token's
+// half row into the slot (sink or ring).  The CTAs of a chunk count themselves
+// on a ticket after reading the lengths; the last one updates the lengths.
 constexpr uint32_t kOffRows = kOffTmem + 16;
-constexpr uint32_t kEvSmem = kOffRows + 128 * 8 + 128 * 4 + 1024;   // + alignment slack
+constexpr uint32_t kEvSmem = kOffRows + 128 * 8 + 2 * 128 * 4 + 16 + 1024;   // + alignment slack
 
 template <int GS, int TENSOR>
 __device__ __forceinline__ void evict_body(const StepArgs& a, int B, uint8_t* sm) {
@@ -699,6 +706,8 @@ __device__ __forceinline__ void evict_body(const StepArgs& a, int B, uint8_t* sm
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kOffTmem);
   long long* rtile = reinterpret_cast<long long*>(sm + kOffRows);   // byte offset of the row's tile, -1: none
   int* rpos = reinterpret_cast<int*>(sm + kOffRows + 128 * 8);      // row within the tile
+  int* rplace = rpos + 128;                                         // mode | slot << 2 of the placement, -1: none
+  unsigned* slast = reinterpret_cast<unsigned*>(rplace + 128);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = blockIdx.y;
   const int quarter = warp & 3, hf = warp >> 2;
@@ -731,14 +740,54 @@ __device__ __forceinline__ void evict_body(const StepArgs& a, int B, uint8_t* sm
       rtile[row] = ev ? pl.tile : -1;
       rpos[row] = pl.pos;
     }
-    const uint16_t* rec = TENSOR ? a.rec_v : a.rec_k;
-    const uint16_t* src = rec + (ev ? (((size_t)b * a.Hkv + g) * a.rec_cap + pl.slot) * 128 : 0) + 64 * hh;
+    if (hh == 0) rplace[row] = (pl.mode < 0) ? -1 - pl.err : (pl.mode | (pl.slot << 2));
+    uint16_t* rec = TENSOR ? a.rec_v : a.rec_k;
+    const size_t sh = (size_t)b * a.Hkv + g;
+    const uint16_t* src = rec + (ev ? (sh * a.rec_cap + pl.slot) * 128 : 0) + 64 * hh;
 #pragma unroll
     for (int c = 0; c < 8; ++c)
       cp_async16_zfill(sA + hh * 16384 + row * 128 + ((c ^ (row & 7)) << 4), src + 8 * c, ev);
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    // the old contents of this half row are in shared memory: the new token
+    // takes the slot (the sequence's next sink slot or its ring slot)
+    if (pl.mode >= 0) {
+      const uint16_t* nsrc = (TENSOR ? a.v_new : a.k_new) + sh * 128 + 64 * hh;
+      uint16_t* dst = (pl.mode == 0) ? (TENSOR ? a.sink_v : a.sink_k) + (sh * a.sink_cap + pl.slot) * 128
+                                     : rec + (sh * a.rec_cap + pl.slot) * 128;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        *reinterpret_cast<uint2*>(dst + 64 * hh + 4 * c) = *reinterpret_cast<const uint2*>(nsrc + 4 * c);
+    }
   }
   fence_async_smem();
+  // every thread has read its rows' lengths: count this CTA on the chunk's
+  // ticket; the last CTA of the chunk moves the lengths
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned n = gridDim.y * gridDim.z;
+    *slast = (atomicAdd(a.tickets + blockIdx.x, 1u) == n - 1u) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (*slast != 0u && tid < kChunk) {
+    __threadfence();
+    const int b = blockIdx.x * kChunk + tid;
+    const int pc = rplace[tid];
+    if (b < B) {
+      const int mode = pc & 3, slot = pc >> 2;
+      if (pc < 0) {
+        flag_error(a.err, -1 - pc);
+      } else if (mode == 0) {
+        a.sink_len[b] = slot + 1;
+      } else if (mode == 1) {
+        a.rec_len[b] += 1;
+      } else {
+        a.hist_len[b] += 1;
+        a.rec_start[b] = (slot + 1) % a.rec_cap;
+      }
+    }
+    if (tid == 0) a.tickets[blockIdx.x] = 0u;   // ready for the next step
+  }
   bool ok = mbar_wait(bars + 0, 0, kTcPolls);
   if (__syncthreads_and(ok)) {
     if (tid == 0) issue_rotation(tmem, sA, sB, bars + 1);
@@ -752,7 +801,9 @@ __device__ __forceinline__ void evict_body(const StepArgs& a, int B, uint8_t* sm
     flag_error(a.err, KV_DEVERR_TIMEOUT);
     mbar_wait(bars + 0, 0, kTcPolls);     // the copies in flight, bounded
   }
-  if (ok) {
+  // a lane quarter without an evicted row skips the epilogue (both of its
+  // warps see the same rows, so they skip together)
+  if (ok && __any_sync(0xffffffffu, rtile[m] >= 0)) {
     tc_fence_after();
     constexpr int NS = (TENSOR == 0) ? 4 : 8;
     uint32_t wd[NS][2];
@@ -766,11 +817,18 @@ __device__ __forceinline__ void evict_body(const StepArgs& a, int B, uint8_t* sm
         // K: the row's codes at pairs + pos / 8 of its four slots 4 * (pos % 8) + j
         const int mh = pos >> 3;
         const uint32_t mask = mh ? 0xCCCCCCCCu : 0x33333333u;
+        // every old word first (one round trip), then the merged words
+        uint2* dst[4];
+        uint2 old[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint32_t w2[2] = {wd[j][0] << (2 * mh), wd[j][1] << (2 * mh)};
-          store_merge2(tb + 16 * (4 * (pos & 7) + j) + 8 * hf, w2, mask);
+          dst[j] = reinterpret_cast<uint2*>(tb + 16 * (4 * (pos & 7) + j) + 8 * hf);
+          old[j] = *dst[j];
         }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *dst[j] = make_uint2((old[j].x & ~mask) | ((wd[j][0] << (2 * mh)) & mask),
+                               (old[j].y & ~mask) | ((wd[j][1] << (2 * mh)) & mask));
         if (GS == 64 || hf == 0) {
           __half2* rec = reinterpret_cast<__half2*>(tb + 1024 + (2 * (pos & 7) + mh) * 8 * NG);
           rec[GS == 64 ? hf : 0] = __halves2half2(q.sh, q.zh);
@@ -780,11 +838,18 @@ __device__ __forceinline__ void evict_body(const StepArgs& a, int B, uint8_t* sm
         // slots 4 * m8 + (pos % 8) / 2
         const int ek = pos & 1, kh = pos >> 3, jk = (pos & 7) >> 1, sh = 16 * ek + 8 * kh;
         const uint32_t mask = (kh ? 0xFF00u : 0x00FFu) << (16 * ek);
+        // every old word first (one round trip), then the merged words
+        uint2* dst[8];
+        uint2 old[8];
 #pragma unroll
         for (int m8 = 0; m8 < 8; ++m8) {
-          const uint32_t w2[2] = {wd[m8][0] << sh, wd[m8][1] << sh};
-          store_merge2(tb + 512 + 16 * (4 * m8 + jk) + 8 * hf, w2, mask);
+          dst[m8] = reinterpret_cast<uint2*>(tb + 512 + 16 * (4 * m8 + jk) + 8 * hf);
+          old[m8] = *dst[m8];
         }
+#pragma unroll
+        for (int m8 = 0; m8 < 8; ++m8)
+          *dst[m8] = make_uint2((old[m8].x & ~mask) | ((wd[m8][0] << sh) & mask),
+                                (old[m8].y & ~mask) | ((wd[m8][1] << sh) & mask));
         if (GS == 64 || hf == 0) {
           __half2* rec = reinterpret_cast<__half2*>(tb + 1024 + (2 * (pos & 7) + kh) * 8 * NG) + NG;
           rec[GS == 64 ? hf : 0] = __halves2half2(q.sh, q.zh);
@@ -811,36 +876,6 @@ __global__ void __launch_bounds__(kTcThreads, 2) evict_tc_kernel(StepArgs a, int
     evict_body<GS, 1>(a, B, sm);
 }
 
-// Placement after the eviction: CTA b copies sequence b's new K and V token of
-// every KV head into its sink or ring slot (the evicted slot included), then
-// updates the lengths from the same decision on the unchanged lengths.
-__global__ void step_place_kernel(StepArgs a, int B) {
-  const int b = blockIdx.x;
-  const StepPlace pl = step_place(a, b);
-  if (pl.mode >= 0) {
-    for (int i = threadIdx.x; i < 2 * a.Hkv * 32; i += blockDim.x) {
-      const int t = i / (a.Hkv * 32), g = (i >> 5) % a.Hkv, w = i & 31;
-      const size_t sh = (size_t)b * a.Hkv + g;
-      const uint16_t* src = (t ? a.v_new : a.k_new) + sh * 128;
-      uint16_t* dst = (pl.mode == 0) ? (t ? a.sink_v : a.sink_k) + (sh * a.sink_cap + pl.slot) * 128
-                                     : (t ? a.rec_v : a.rec_k) + (sh * a.rec_cap + pl.slot) * 128;
-      *reinterpret_cast<uint2*>(dst + 4 * w) = *reinterpret_cast<const uint2*>(src + 4 * w);
-    }
-  }
-  __syncthreads();   // every thread has read the lengths
-  if (threadIdx.x == 0) {
-    if (pl.mode == 0) {
-      a.sink_len[b] = pl.slot + 1;
-    } else if (pl.mode == 1) {
-      a.rec_len[b] += 1;
-    } else if (pl.mode == 2) {
-      a.hist_len[b] += 1;
-      a.rec_start[b] = (pl.slot + 1) % a.rec_cap;
-    } else {
-      flag_error(a.err, pl.err);
-    }
-  }
-}
 }  // namespace
 
 cudaError_t launch_append_tc(const Pool& p, int layer, int n_seqs, const void* k, const void* v,
@@ -945,6 +980,7 @@ cudaError_t launch_append_step(const Pool& p, int layer, int B, const void* k_ne
   a.num_pages = p.cfg.num_pages;
   a.rfrag = p.rfrag + (size_t)layer * H * kFragBlocks * rfrag_per_head();
   a.clip = p.clip + (size_t)layer * 2 * H * 128;
+  a.tickets = p.step_tickets + (size_t)layer * ((p.cfg.max_seqs + kChunk - 1) / kChunk);
   a.err = p.err;
   static bool attr[2] = {false, false};
   auto evict = [&](auto kernel, int gi) -> cudaError_t {
@@ -958,10 +994,7 @@ cudaError_t launch_append_step(const Pool& p, int layer, int B, const void* k_ne
     kernel<<<dim3((unsigned)((B + kChunk - 1) / kChunk), H, 2), kTcThreads, kEvSmem, s>>>(a, B);
     return cudaGetLastError();
   };
-  cudaError_t e = (p.cfg.group_size == 64) ? evict(evict_tc_kernel<64>, 0) : evict(evict_tc_kernel<128>, 1);
-  if (e != cudaSuccess) return e;
-  step_place_kernel<<<B, 128, 0, s>>>(a, B);
-  return cudaGetLastError();
+  return (p.cfg.group_size == 64) ? evict(evict_tc_kernel<64>, 0) : evict(evict_tc_kernel<128>, 1);
 }
 
 }  // namespace kvint2

@@ -39,6 +39,7 @@ struct Pool {
   float* clip = nullptr;            // [layer][2][Hkv][128]
   uint4* rfrag = nullptr;           // [layer][Hkv][kFragBlocks][4096] rotation operands (below)
   unsigned* tickets = nullptr;      // [layer][max_seqs][Hkv] split-merge counters
+  unsigned* step_tickets = nullptr; // [layer][ceil(max_seqs / 128)] per-step placement counters
   int* err = nullptr;               // device error word
 };
 
