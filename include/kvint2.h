@@ -225,7 +225,9 @@ kv_status_t kv_decode_attention_multi(kv_pool_t* pool, int32_t layer, int32_t B,
  * position hist_len[b] (the same arithmetic, and so the same codes, as
  * kv_append_quantize), the new token takes its ring slot and recent_start
  * advances.  The four length arrays are updated on the device, in stream
- * order, so consecutive steps and decodes need no host round trip.
+ * order, so consecutive steps and decodes need no host round trip.  One
+ * launch; calls for the same layer must not overlap on the GPU (they share the
+ * layer's completion counters).
  *   k_new, v_new  device bf16 [B][Hkv][128] (8-byte aligned); sequence b
  *                 uses pool slot b
  *   sink_len, hist_len, recent_len, recent_start
