@@ -59,7 +59,7 @@ constexpr int kTierRowV = 256;
 constexpr float kSlack = 4.0f;
 constexpr int kBf16Warps = 8;
 
-__host__ __device__ constexpr int int2_warps(int G) { return G <= 4 ? 16 : 8; }
+__host__ __device__ constexpr int int2_warps(int G) { return G <= 4 ? 16 : 12; }
 __host__ __device__ constexpr int pad4(int n) { return (n + 3) / 4 * 4; }
 
 struct DecodeArgs {
@@ -151,14 +151,16 @@ struct Lay {
 template <int NROWS, int NW>
 __device__ void rotate_q(const float* X, const uint4* __restrict__ frag, float* Y) {
   static_assert(NROWS <= 8, "rows");
-  constexpr int NTW = 16 / NW;   // 8-column n-tiles per warp
+  constexpr int NTW = (16 + NW - 1) / NW;   // 8-column n-tiles per warp: tiles warp, warp + NW, ..
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = lane >> 2, j = lane & 3;
   uint4 f[8][NTW];
 #pragma unroll
   for (int s = 0; s < 8; ++s)
 #pragma unroll
-    for (int u = 0; u < NTW; ++u) f[s][u] = __ldg(frag + (s * 16 + NTW * warp + u) * 32 + lane);
+    for (int u = 0; u < NTW; ++u)
+      f[s][u] = (warp + u * NW < 16) ? __ldg(frag + (s * 16 + warp + u * NW) * 32 + lane)
+                                     : make_uint4(0u, 0u, 0u, 0u);
   float acc[NTW][4];
 #pragma unroll
   for (int u = 0; u < NTW; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
@@ -185,8 +187,9 @@ __device__ void rotate_q(const float* X, const uint4* __restrict__ frag, float* 
   if (row_ok) {
 #pragma unroll
     for (int u = 0; u < NTW; ++u)
-      *reinterpret_cast<float2*>(Y + r * 128 + 8 * (NTW * warp + u) + 2 * j) =
-          make_float2(acc[u][0] * 256.0f, acc[u][1] * 256.0f);
+      if (warp + u * NW < 16)
+        *reinterpret_cast<float2*>(Y + r * 128 + 8 * (warp + u * NW) + 2 * j) =
+            make_float2(acc[u][0] * 256.0f, acc[u][1] * 256.0f);
   }
   __syncthreads();
 }
@@ -259,13 +262,12 @@ __device__ bool last_to_arrive(unsigned* ticket, unsigned total) {
 // Rotate a CTA's merged history value sums back to the original basis:
 // o[h][c] = sum_i o'[h][i] R_v[c][i] = sum_i o'[h][i] R_v^T[i][c].  o' arrives
 // in io [G][128] and the result replaces it.  Each row of R_v^T (shared
-// memory) is read once for all G heads: warp w takes rows
-// [w*128/NW, (w+1)*128/NW), lane c takes columns 4c..4c+3, and the NW
-// row-slice sums (spr) are added at the end.  sOt: [128][GP] scratch.
+// memory) is read once for all G heads: warp w takes rows w, w + NW, ..,
+// lane c takes columns 4c..4c+3, and the NW row-slice sums (spr) are added
+// at the end.  sOt: [128][GP] scratch.
 template <int G, int NW>
 __device__ void rotate_back(float* io, float* sOt, const float* sR, float* spr) {
   constexpr int GP = (G + 3) & ~3;   // heads padded to a multiple of 4
-  constexpr int RPW = 128 / NW;      // rows of R_v^T per warp
   const int warp = threadIdx.x >> 5, cq = threadIdx.x & 31;
   for (int idx = threadIdx.x; idx < GP * 128; idx += NW * 32) {
     const int hh = idx >> 7, i = idx & 127;
@@ -276,8 +278,7 @@ __device__ void rotate_back(float* io, float* sOt, const float* sR, float* spr) 
 #pragma unroll
   for (int hh = 0; hh < GP; ++hh) acc[hh][0] = acc[hh][1] = acc[hh][2] = acc[hh][3] = 0.f;
 #pragma unroll 4
-  for (int ii = 0; ii < RPW; ++ii) {
-    const int i = warp * RPW + ii;
+  for (int i = warp; i < 128; i += NW) {   // rows of R_v^T: warp, warp + NW, ..
     const float4 r = *reinterpret_cast<const float4*>(sR + i * 128 + 4 * cq);
 #pragma unroll
     for (int hq = 0; hq < GP / 4; ++hq) {
@@ -320,13 +321,14 @@ __device__ void merge_parts(const DecodeArgs& a, int b, int g, int nparts, float
   float* sl = sf + nparts * G;                     // [nparts * G]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cq = lane, h = warp % G, sub = warp / G;
+  const bool sums = sub < NSUB;   // warps beyond NSUB * G take no part subset
   // this warp's first kPre value vectors, loaded in the same round as m and l
   constexpr int kPre = 8;
   float4 pre[kPre];
 #pragma unroll
   for (int u = 0; u < kPre; ++u) {
     const int s = sub + u * NSUB;
-    pre[u] = (s < nparts)
+    pre[u] = (sums && s < nparts)
                  ? __ldcg(reinterpret_cast<const float4*>(base + (size_t)(s * G + h) * kPart + 4) + cq)
                  : make_float4(0.f, 0.f, 0.f, 0.f);
   }
@@ -353,7 +355,7 @@ __device__ void merge_parts(const DecodeArgs& a, int b, int g, int nparts, float
     }
   }
   __syncthreads();
-  {
+  if (sums) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int u = 0; u < kPre; ++u) {
