@@ -60,6 +60,10 @@ constexpr float kSlack = 4.0f;
 constexpr int kBf16Warps = 8;
 
 __host__ __device__ constexpr int int2_warps(int G) { return G <= 4 ? 16 : 12; }
+// a split covers at most 64 tiles per warp, and its page ids (one per tile at
+// page 16) are staged in shared memory
+static_assert(64 * int2_warps(1) <= kMaxPids && 64 * int2_warps(8) <= kMaxPids,
+              "a split's page ids must fit the staging array");
 __host__ __device__ constexpr int pad4(int n) { return (n + 3) / 4 * 4; }
 
 struct DecodeArgs {
