@@ -683,6 +683,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
 
   int k = 0;
   bool ok = true;
+#pragma unroll 2   // lets one tile's loads, unpack and QK overlap the previous tile's softmax and PV
   for (int t = t_begin + warp; t < t_end; t += NW, ++k) {
     __syncwarp();   // every lane is done with the stage refilled next
     // tile k+3 goes into the stage read in the previous iteration
