@@ -20,6 +20,15 @@
  *   - Pointers named "device" are CUDA device pointers on the pool's device;
  *     host pointers are named "host".  The caller owns every buffer it
  *     passes; the pool owns its own storage.
+ *   - The decode calls (kv_decode_attention, _noalloc, _multi) also take q,
+ *     the four length arrays, out and lse in mapped page-locked host memory
+ *     whose address is valid on the device under unified addressing
+ *     (cudaHostAlloc memory; for cudaHostRegister memory pass the pointer
+ *     cudaHostGetDevicePointer returns).  The kernel then reads and writes
+ *     them across the CPU-GPU link inside the launch, with no staging
+ *     copies; results are bit-identical to device buffers.  The host must
+ *     not touch them until the stream has passed the call.  The page table,
+ *     workspace and every other buffer stay in device memory.
  *   - Every call is asynchronous on `stream` (a cudaStream_t, NULL = legacy
  *     default stream) unless stated otherwise, and validates its arguments on
  *     the host first: on failure it launches nothing and returns
