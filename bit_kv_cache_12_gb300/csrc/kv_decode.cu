@@ -146,25 +146,36 @@ struct Lay {
 // shared helpers
 // ---------------------------------------------------------------------------
 
+// R_k's MMA fragments for rotate_q, held in registers: warp w of NW produces
+// q' columns (128/NW)w .., and each lane loads all its fragments at once (one
+// memory latency), so the load can be issued early and overlap other loads.
+template <int NW>
+struct RotFrags {
+  static constexpr int NTW = (16 + NW - 1) / NW;   // 8-column n-tiles per warp: warp, warp + NW, ..
+  uint4 f[8][NTW];
+  __device__ __forceinline__ void load(const uint4* __restrict__ frag) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+#pragma unroll
+      for (int u = 0; u < NTW; ++u)
+        f[s][u] = (warp + u * NW < 16) ? __ldg(frag + (s * 16 + warp + u * NW) * 32 + lane)
+                                       : make_uint4(0u, 0u, 0u, 0u);
+  }
+};
+
 // q'[h][c] = sum_i q[h][i] R_k[i][c] for the first NROWS rows of X (shared,
 // [*][128] fp32 holding bf16 values), on the tensor cores: R_k comes as fp16
-// hi + lo B fragments (rotation fragment block 2), q is scaled by 2^-8 (exact)
-// and split into fp16 hi + lo, and the three products above 2^-22 relative are
-// accumulated in fp32.  Warp w of NW produces columns (128/NW)w ..; each lane
-// loads its fragments at once (one memory latency).  Ends with a barrier.
+// hi + lo B fragments (rotation fragment block 0, loaded by RotFrags), q is
+// scaled by 2^-8 (exact) and split into fp16 hi + lo, and the three products
+// above 2^-22 relative are accumulated in fp32.  Ends with a barrier.
 template <int NROWS, int NW>
-__device__ void rotate_q(const float* X, const uint4* __restrict__ frag, float* Y) {
+__device__ void rotate_q(const float* X, const RotFrags<NW>& fr, float* Y) {
   static_assert(NROWS <= 8, "rows");
-  constexpr int NTW = (16 + NW - 1) / NW;   // 8-column n-tiles per warp: tiles warp, warp + NW, ..
+  constexpr int NTW = RotFrags<NW>::NTW;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = lane >> 2, j = lane & 3;
-  uint4 f[8][NTW];
-#pragma unroll
-  for (int s = 0; s < 8; ++s)
-#pragma unroll
-    for (int u = 0; u < NTW; ++u)
-      f[s][u] = (warp + u * NW < 16) ? __ldg(frag + (s * 16 + warp + u * NW) * 32 + lane)
-                                     : make_uint4(0u, 0u, 0u, 0u);
+  const auto& f = fr.f;
   float acc[NTW][4];
 #pragma unroll
   for (int u = 0; u < NTW; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
@@ -227,6 +238,39 @@ __device__ void merge_warps(const float* swo, const float* swm, const float* swl
   __syncthreads();
 }
 
+// merge_warps for the history split, writing the merged o transposed for
+// rotate_back_to_part: oT[c][hh] (GP = heads padded to 4; padded heads 0).
+template <int G, int NW>
+__device__ void merge_warps_t(const float* swo, const float* swm, const float* swl, float* oT,
+                              float* sm_m, float* sm_l) {
+  constexpr int GP = (G + 3) & ~3;
+  for (int idx = threadIdx.x; idx < GP * 128; idx += NW * 32) {
+    const int h = idx >> 7, c = idx & 127;
+    float O = 0.f;
+    if (h < G) {
+      float M = kNegInf;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, swm[w * G + h]);
+      float L = 0.f;
+      if (M != kNegInf) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float mw = swm[w * G + h];
+          const float f = (mw == kNegInf) ? 0.f : exp2f(mw - M);
+          L = fmaf(f, swl[w * G + h], L);
+          O = fmaf(f, swo[(w * G + h) * 128 + c], O);
+        }
+      }
+      if (c == 0) {
+        sm_m[h] = M;
+        sm_l[h] = L;
+      }
+    }
+    oT[c * GP + h] = O;
+  }
+  __syncthreads();
+}
+
 template <int G, int NW>
 __device__ void write_partial(float* part, const float* o, const float* sm_m, const float* sm_l) {
   for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
@@ -252,32 +296,33 @@ __device__ void write_empty_partial(float* part) {
 }
 
 // The last CTA to arrive for a (sequence, KV head) returns true.  No waiting.
+// The barrier orders every thread's partial writes before thread 0's
+// acquire-release increment, which publishes them at GPU scope (release is
+// cumulative); the CTA that takes the last ticket acquires every other CTA's
+// writes, and its second barrier hands them to all of its threads.
 __device__ bool last_to_arrive(unsigned* ticket, unsigned total) {
   __shared__ unsigned s_last;
-  __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(ticket, 1u) == total - 1u) ? 1u : 0u;
-  __syncthreads();
-  const bool last = s_last != 0u;
-  if (last) __threadfence();
-  return last;
-}
-
-// Rotate a CTA's merged history value sums back to the original basis:
-// o[h][c] = sum_i o'[h][i] R_v[c][i] = sum_i o'[h][i] R_v^T[i][c].  o' arrives
-// in io [G][128] and the result replaces it.  Each row of R_v^T (shared
-// memory) is read once for all G heads: warp w takes rows w, w + NW, ..,
-// lane c takes columns 4c..4c+3, and the NW row-slice sums (spr) are added
-// at the end.  sOt: [128][GP] scratch.
-template <int G, int NW>
-__device__ void rotate_back(float* io, float* sOt, const float* sR, float* spr) {
-  constexpr int GP = (G + 3) & ~3;   // heads padded to a multiple of 4
-  const int warp = threadIdx.x >> 5, cq = threadIdx.x & 31;
-  for (int idx = threadIdx.x; idx < GP * 128; idx += NW * 32) {
-    const int hh = idx >> 7, i = idx & 127;
-    sOt[i * GP + hh] = (hh < G) ? io[idx] : 0.f;
+  if (threadIdx.x == 0) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(ticket) : "memory");
+    s_last = (old == total - 1u) ? 1u : 0u;
   }
   __syncthreads();
+  return s_last != 0u;
+}
+
+// Rotate a history split's merged value sums back to the original basis,
+// o[h][c] = sum_i o'[h][i] R_v[c][i] = sum_i o'[h][i] R_v^T[i][c], straight
+// into the split's partial in global memory (with the merged m and l).  o'
+// arrives transposed, oT [128][GP]; each row of R_v^T (shared memory) is read
+// once for all heads: warp w takes rows w, w + NW, .., lane c columns
+// 4c..4c+3, and the NW row-slice sums (spr) are added while storing.
+template <int G, int NW>
+__device__ void rotate_back_to_part(const float* oT, const float* sR, float* spr, float* part,
+                                    const float* sm_m, const float* sm_l) {
+  constexpr int GP = (G + 3) & ~3;
+  const int warp = threadIdx.x >> 5, cq = threadIdx.x & 31;
   float acc[GP][4];
 #pragma unroll
   for (int hh = 0; hh < GP; ++hh) acc[hh][0] = acc[hh][1] = acc[hh][2] = acc[hh][3] = 0.f;
@@ -286,7 +331,7 @@ __device__ void rotate_back(float* io, float* sOt, const float* sR, float* spr) 
     const float4 r = *reinterpret_cast<const float4*>(sR + i * 128 + 4 * cq);
 #pragma unroll
     for (int hq = 0; hq < GP / 4; ++hq) {
-      const float4 o = *reinterpret_cast<const float4*>(sOt + i * GP + 4 * hq);
+      const float4 o = *reinterpret_cast<const float4*>(oT + i * GP + 4 * hq);
       const float ox[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -302,101 +347,68 @@ __device__ void rotate_back(float* io, float* sOt, const float* sR, float* spr) 
         make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
   __syncthreads();
   for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
+    const int h = idx >> 7, c = idx & 127;
     float O = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) O += spr[w * G * 128 + idx];
-    io[idx] = O;
+    part[h * kPart + 4 + c] = O;
+    if (c == 0) {
+      part[h * kPart + 0] = sm_m[h];
+      part[h * kPart + 1] = sm_l[h];
+    }
   }
-  __syncthreads();
 }
 
 // Log-sum-exp merge of all parts of (b, g) (every part in the original basis)
-// and the final normalisation.  Warp h < G forms head h's maximum and weighted
-// sum of l over the parts; then every warp accumulates a subset of the parts'
-// value vectors for one head and the subsets are added.
+// and the final normalisation, in one pass with no barrier: thread (h, c)
+// merges output element c of head h over the parts itself, a batch of
+// kMergeBatch parts per round of loads (m and l of a part are the same for
+// all 128 threads of a head and arrive as broadcasts).  Within a batch the
+// weights are 2^(m_s - M) against the batch's running maximum M; a later batch
+// with a larger maximum rescales what is accumulated so far.
+constexpr int kMergeBatch = 20;
+
 template <int G, int NW, bool kMulti>
 __device__ void merge_parts(const DecodeArgs& a, int b, int g, int nparts, float* sm) {
-  constexpr int NSUB = NW / G;                     // part subsets per output column quad
+  (void)sm;
   const float* base = a.ws + (size_t)(b * a.Hkv + g) * nparts * G * kPart;
-  float* sM = sm;                                  // [8]
-  float* sL = sm + 8;                              // [8]
-  float* sacc = sm + 16;                           // [NSUB][G][128]
-  float* sf = sacc + NSUB * G * 128;               // [nparts * G] m, then weights
-  float* sl = sf + nparts * G;                     // [nparts * G]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int cq = lane, h = warp % G, sub = warp / G;
-  const bool sums = sub < NSUB;   // warps beyond NSUB * G take no part subset
-  // this warp's first kPre value vectors, loaded in the same round as m and l
-  constexpr int kPre = 8;
-  float4 pre[kPre];
-#pragma unroll
-  for (int u = 0; u < kPre; ++u) {
-    const int s = sub + u * NSUB;
-    pre[u] = (sums && s < nparts)
-                 ? __ldcg(reinterpret_cast<const float4*>(base + (size_t)(s * G + h) * kPart + 4) + cq)
-                 : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  for (int i = threadIdx.x; i < nparts * G; i += NW * 32) {
-    sf[i] = __ldcg(base + (size_t)i * kPart);
-    sl[i] = __ldcg(base + (size_t)i * kPart + 1);
-  }
-  __syncthreads();
-  if (warp < G) {
-    float M = kNegInf;
-    for (int s = lane; s < nparts; s += 32) M = fmaxf(M, sf[s * G + warp]);
-    M = warp_max_xor(M, 1);
-    float L = 0.f;
-    for (int s = lane; s < nparts; s += 32) {
-      const float m = sf[s * G + warp];
-      const float f = (m == kNegInf || M == kNegInf) ? 0.f : exp2f(m - M);
-      sf[s * G + warp] = f;
-      L = fmaf(f, sl[s * G + warp], L);
-    }
-    L = warp_sum_xor(L, 1);
-    if (lane == 0) {
-      sM[warp] = M;
-      sL[warp] = L;
-    }
-  }
-  __syncthreads();
-  if (sums) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int u = 0; u < kPre; ++u) {
-      const int s = sub + u * NSUB;
-      const float f = (s < nparts) ? sf[s * G + h] : 0.f;
-      acc.x = fmaf(f, pre[u].x, acc.x);
-      acc.y = fmaf(f, pre[u].y, acc.y);
-      acc.z = fmaf(f, pre[u].z, acc.z);
-      acc.w = fmaf(f, pre[u].w, acc.w);
-    }
-#pragma unroll 8
-    for (int s = sub + kPre * NSUB; s < nparts; s += NSUB) {
-      const float f = sf[s * G + h];
-      const float4 o =
-          __ldcg(reinterpret_cast<const float4*>(base + (size_t)(s * G + h) * kPart + 4) + cq);
-      acc.x = fmaf(f, o.x, acc.x);
-      acc.y = fmaf(f, o.y, acc.y);
-      acc.z = fmaf(f, o.z, acc.z);
-      acc.w = fmaf(f, o.w, acc.w);
-    }
-    *reinterpret_cast<float4*>(sacc + (sub * G + h) * 128 + 4 * cq) = acc;
-  }
-  __syncthreads();
   for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
-    const int hh = idx >> 7;
-    float O = 0.f;
+    const int hh = idx >> 7, c = idx & 127;
+    const float* ph = base + (size_t)hh * kPart;
+    float M = kNegInf, L = 0.f, O = 0.f;
+    for (int s0 = 0; s0 < nparts; s0 += kMergeBatch) {
+      float mv[kMergeBatch], lv[kMergeBatch], ov[kMergeBatch];
 #pragma unroll
-    for (int u = 0; u < NSUB; ++u) O += sacc[u * G * 128 + idx];
-    const float L = sL[hh];
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const int s = s0 + u;
+        const float* pp = ph + (size_t)s * G * kPart;
+        mv[u] = (s < nparts) ? __ldcg(pp) : kNegInf;
+        lv[u] = (s < nparts) ? __ldcg(pp + 1) : 0.f;
+        ov[u] = (s < nparts) ? __ldcg(pp + 4 + c) : 0.f;
+      }
+      float Mb = M;
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) Mb = fmaxf(Mb, mv[u]);
+      if (Mb != kNegInf) {
+        const float alpha = (M == kNegInf) ? 0.f : exp2f(M - Mb);
+        L *= alpha;
+        O *= alpha;
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+          const float f = (mv[u] == kNegInf) ? 0.f : exp2f(mv[u] - Mb);
+          L = fmaf(f, lv[u], L);
+          O = fmaf(f, ov[u], O);
+        }
+        M = Mb;
+      }
+    }
     if constexpr (kMulti) {
       const size_t row = ((size_t)b * a.T + hh / a.Gq) * a.Hq + g * a.Gq + hh % a.Gq;
-      a.out[row * 128 + (idx & 127)] = (L > 0.f) ? O / L : 0.f;
+      a.out[row * 128 + c] = (L > 0.f) ? O / L : 0.f;
       // ln sum exp(scaled score) = ln 2 * (M + log2 L), the scores being in log2 units
-      if (a.lse && (idx & 127) == 0)
-        a.lse[row] = (L > 0.f) ? 0.6931471805599453f * (sM[hh] + log2f(L)) : kNegInf;
+      if (a.lse && c == 0) a.lse[row] = (L > 0.f) ? 0.6931471805599453f * (M + log2f(L)) : kNegInf;
     } else {
-      a.out[((size_t)b * a.Hq + g * G + hh) * 128 + (idx & 127)] = (L > 0.f) ? O / L : 0.f;
+      a.out[((size_t)b * a.Hq + g * G + hh) * 128 + c] = (L > 0.f) ? O / L : 0.f;
     }
   }
   if (threadIdx.x == 0) a.tickets[b * a.Hkv + g] = 0u;   // ready for the next call
@@ -563,33 +575,10 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = lane >> 2, j = lane & 3;
 
-  // ---- one round of loads: page ids of the split's whole range, q, length ----
-  const int tsh = a.tpp_shift, tmask = a.tiles_per_page - 1;
-  const int t_begin = split * a.per_split;
-  const int p_begin = t_begin >> tsh;
-  const int p_all = min(((t_begin + a.per_split - 1) >> tsh) + 1, a.max_pages) - p_begin;
-  int* spid = reinterpret_cast<int*>(sm + S::spid);
-  const int32_t* ptrow = a.pt + (size_t)b * a.max_pages;
-  for (int i = threadIdx.x; i < p_all; i += NW * 32) spid[i] = __ldg(ptrow + p_begin + i);
-  float* sq = sm + S::sq;
-  float* sqr = sm + S::sqr;
-  float* ssum = sm + S::ssum;
-  load_q<G, NW, kMulti>(a, b, g, sq, S::HP);
-  int h = __ldg(a.hist_len + b);
-  __syncthreads();
-  const int cap = a.max_pages * a.page_size;
-  if (h < 0 || h > cap) {
-    if (threadIdx.x == 0) flag_error(a.err, KV_DEVERR_LENGTH);
-    h = max(0, min(h, cap));
-  }
-  const int ntiles = (h + kTile - 1) / kTile;
-  const int t_end = min(ntiles, t_begin + a.per_split);
-  if (t_begin >= t_end) {
-    write_empty_partial<G, NW>(part);
-    return;
-  }
-
-  // ---- start streaming this warp's first tiles into its ring ----
+  // ---- barriers, then one round of independent loads: R_k's fragments, the
+  // split's page ids, q and the length.  Lane 0 of each warp also reads the
+  // page ids of its first tiles itself, so that their copies start as soon as
+  // the page table answers, while q' is still being formed. ----
   // A ring stage holds one whole stored tile, brought in by one bulk copy that
   // lane 0 issues and that completes on the stage's mbarrier; R_v^T (for the
   // back-rotation of the partial) comes the same way on its own barrier.
@@ -602,30 +591,72 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
   if (lane < kStages) mbar_init(wbar + lane, 1);
   if (threadIdx.x == 0) mbar_init(rbar, 1);
   mbar_fence_init();
-  __syncthreads();
+
+  const int tsh = a.tpp_shift, tmask = a.tiles_per_page - 1;
+  const int t_begin = split * a.per_split;
+  const int p_begin = t_begin >> tsh;
+  const int p_all = min(((t_begin + a.per_split - 1) >> tsh) + 1, a.max_pages) - p_begin;
+  const int32_t* ptrow = a.pt + (size_t)b * a.max_pages;
+  int pid_first[kStages - 1];
+  if (lane == 0) {
+#pragma unroll
+    for (int st = 0; st < kStages - 1; ++st) {
+      const int pg = (t_begin + warp + NW * st) >> tsh;
+      pid_first[st] = (pg < a.max_pages) ? __ldg(ptrow + pg) : -1;
+    }
+  }
+  RotFrags<NW> rk;
+  rk.load(a.rfrag + ((size_t)g * kFragBlocks + 0) * 4096);
+  int* spid = reinterpret_cast<int*>(sm + S::spid);
+  for (int i = threadIdx.x; i < p_all; i += NW * 32) spid[i] = __ldg(ptrow + p_begin + i);
+  float* sq = sm + S::sq;
+  float* sqr = sm + S::sqr;
+  float* ssum = sm + S::ssum;
+  load_q<G, NW, kMulti>(a, b, g, sq, S::HP);
+  int h = __ldg(a.hist_len + b);
+  const int cap = a.max_pages * a.page_size;
+  if (h < 0 || h > cap) {
+    if (threadIdx.x == 0) flag_error(a.err, KV_DEVERR_LENGTH);
+    h = max(0, min(h, cap));
+  }
+  const int ntiles = (h + kTile - 1) / kTile;
+  const int t_end = min(ntiles, t_begin + a.per_split);
+  if (t_begin >= t_end) {   // the same for every thread: no copy was started
+    write_empty_partial<G, NW>(part);
+    return;
+  }
+
+  // ---- start streaming this warp's first tiles into its ring ----
   const uint8_t* head_base = a.hist + (size_t)g * (a.page_bytes / a.Hkv);
   const int lane_sz = (GS == 128) ? 1024 + 16 * r : 1024 + 32 * r;
-  auto issue = [&](int t, int stage) {
-    if (lane == 0 && t < t_end) {
-      const int pid = spid[(t >> tsh) - p_begin];
-      const uint8_t* tb = (pid >= 0 && pid < a.num_pages)
-                              ? head_base + (size_t)pid * a.page_bytes + (t & tmask) * a.tile_bytes
-                              : g_zero_tile;
-      mbar_expect_tx(wbar + stage, TB);
-      bulk_g2s(ring + stage * TB, tb, TB, wbar + stage);
-    }
+  auto start_copy = [&](int t, int pid, int stage) {
+    const uint8_t* tb = (pid >= 0 && pid < a.num_pages)
+                            ? head_base + (size_t)pid * a.page_bytes + (t & tmask) * a.tile_bytes
+                            : g_zero_tile;
+    mbar_expect_tx(wbar + stage, TB);
+    bulk_g2s(ring + stage * TB, tb, TB, wbar + stage);
   };
+  auto issue = [&](int t, int stage) {
+    if (lane == 0 && t < t_end) start_copy(t, spid[(t >> tsh) - p_begin], stage);
+  };
+  __syncwarp();   // this warp's barriers are initialised
+  if (lane == 0) {
 #pragma unroll
-  for (int st = 0; st < kStages - 1; ++st) issue(t_begin + warp + NW * st, st);   // tiles 0..2
+    for (int st = 0; st < kStages - 1; ++st) {   // tiles 0..2
+      const int t = t_begin + warp + NW * st;
+      if (t < t_end) start_copy(t, pid_first[st], st);
+    }
+  }
   if (threadIdx.x == 0) {
     const float* R = a.RvT + (size_t)g * 128 * 128;
     mbar_expect_tx(rbar, 128 * 128 * 4);
 #pragma unroll
     for (int c = 0; c < 4; ++c) bulk_g2s(srv + 4096 * c, R + 4096 * c, 16384, rbar);
   }
+  __syncthreads();   // q and the page ids are in shared memory
 
   // ---- q' = q R_k and its per-group sums (overlaps the first copies) ----
-  rotate_q<S::HP, NW>(sq, a.rfrag + ((size_t)g * kFragBlocks + 0) * 4096, sqr);
+  rotate_q<S::HP, NW>(sq, rk, sqr);
   for (int hh = warp; hh < S::HP; hh += NW) {
 #pragma unroll
     for (int grp = 0; grp < NG; ++grp) {
@@ -885,10 +916,10 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
     }
   }
   __syncthreads();
-  merge_warps<G, NW>(swo, swm, swl, sqr, sm + S::smm, sm + S::sml);   // q' no longer needed
-  // back to the original basis (q is no longer needed either: its slot is scratch)
-  rotate_back<G, NW>(sqr, sq, srv, sm + S::spr);
-  write_partial<G, NW>(part, sqr, sm + S::smm, sm + S::sml);
+  // merged sums, transposed for the back-rotation, into q's slot (q and q' are
+  // no longer needed); then back to the original basis, into the partial
+  merge_warps_t<G, NW>(swo, swm, swl, sq, sm + S::smm, sm + S::sml);
+  rotate_back_to_part<G, NW>(sq, srv, sm + S::spr, part, sm + S::smm, sm + S::sml);
 }
 
 // ---------------------------------------------------------------------------
