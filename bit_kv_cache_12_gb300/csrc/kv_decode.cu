@@ -119,7 +119,8 @@ struct Lay {
   static constexpr int sml = smm + pad4(G);                       // [G] merged l
   static constexpr int spid = sml + pad4(G);                      // [kMaxPids] int
   static constexpr int smbar = spid + kMaxPids;                   // [NW * kStages + 1] mbarriers
-  static constexpr int big = smbar + (kInt2 ? pad4(2 * (NW * kStages + 1)) : 0);
+  static constexpr int saddr = smbar + (kInt2 ? pad4(2 * (NW * kStages + 1)) : 0);   // [64 * NW] u64
+  static constexpr int big = saddr + (kInt2 ? 2 * 64 * NW : 0);
   static constexpr int ring_f = kInt2 ? NW * kStages * TB / 4 : 0;
   static constexpr int res_f = NW * G * 128 + 2 * pad4(NW * G);
   static constexpr int sp_f = NW * 32 * G;
@@ -140,6 +141,7 @@ struct Lay {
   static constexpr int phase_end0 = (big + ring_f > sp + sp_f) ? big + ring_f : sp + sp_f;
   static constexpr int phase_end = (phase_end0 > rot_end) ? phase_end0 : rot_end;
   static constexpr int total = (phase_end > merge_f) ? phase_end : merge_f;
+  static_assert(total * 4 <= 227 * 1024, "shared memory of one CTA");
 };
 
 // ---------------------------------------------------------------------------
@@ -240,31 +242,34 @@ __device__ void merge_warps(const float* swo, const float* swm, const float* swl
 
 // merge_warps for the history split, writing the merged o transposed for
 // rotate_back_to_part: oT[c][hh] (GP = heads padded to 4; padded heads 0).
+// The weight of each (warp, head) against the head's maximum is formed once
+// (sf: NW * G floats of scratch), then every output element sums over warps.
 template <int G, int NW>
 __device__ void merge_warps_t(const float* swo, const float* swm, const float* swl, float* oT,
-                              float* sm_m, float* sm_l) {
+                              float* sm_m, float* sm_l, float* sf) {
   constexpr int GP = (G + 3) & ~3;
+  if (threadIdx.x < NW * G) {   // weight of warp w for head h against the head's maximum
+    const int w = threadIdx.x / G, h = threadIdx.x % G;
+    float M = kNegInf;
+#pragma unroll
+    for (int v = 0; v < NW; ++v) M = fmaxf(M, swm[v * G + h]);
+    const float mw = swm[w * G + h];
+    sf[w * G + h] = (mw == kNegInf) ? 0.f : exp2f(mw - M);
+    if (w == 0) sm_m[h] = M;
+  }
+  __syncthreads();
   for (int idx = threadIdx.x; idx < GP * 128; idx += NW * 32) {
     const int h = idx >> 7, c = idx & 127;
     float O = 0.f;
     if (h < G) {
-      float M = kNegInf;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, swm[w * G + h]);
       float L = 0.f;
-      if (M != kNegInf) {
 #pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const float mw = swm[w * G + h];
-          const float f = (mw == kNegInf) ? 0.f : exp2f(mw - M);
-          L = fmaf(f, swl[w * G + h], L);
-          O = fmaf(f, swo[(w * G + h) * 128 + c], O);
-        }
+      for (int w = 0; w < NW; ++w) {
+        const float f = sf[w * G + h];
+        L = fmaf(f, swl[w * G + h], L);
+        O = fmaf(f, swo[(w * G + h) * 128 + c], O);
       }
-      if (c == 0) {
-        sm_m[h] = M;
-        sm_l[h] = L;
-      }
+      if (c == 0) sm_l[h] = L;
     }
     oT[c * GP + h] = O;
   }
@@ -588,6 +593,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
   uint64_t* wbar = bars + warp * kStages;
   uint64_t* rbar = bars + NW * kStages;
   float* srv = sm + S::srv;
+  uint64_t* saddr = reinterpret_cast<uint64_t*>(sm + S::saddr);   // per-tile source addresses
   if (lane < kStages) mbar_init(wbar + lane, 1);
   if (threadIdx.x == 0) mbar_init(rbar, 1);
   mbar_fence_init();
@@ -636,8 +642,12 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
     mbar_expect_tx(wbar + stage, TB);
     bulk_g2s(ring + stage * TB, tb, TB, wbar + stage);
   };
-  auto issue = [&](int t, int stage) {
-    if (lane == 0 && t < t_end) start_copy(t, spid[(t >> tsh) - p_begin], stage);
+  auto issue = [&](int t, int stage) {   // tiles k >= kStages - 1, from the address table
+    if (lane == 0 && t < t_end) {
+      const uint64_t e = saddr[t - t_begin];
+      mbar_expect_tx(wbar + stage, TB);
+      bulk_g2s(ring + stage * TB, reinterpret_cast<const void*>(e & ~1ull), TB, wbar + stage);
+    }
   };
   __syncwarp();   // this warp's barriers are initialised
   if (lane == 0) {
@@ -654,6 +664,21 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
     for (int c = 0; c < 4; ++c) bulk_g2s(srv + 4096 * c, R + 4096 * c, 16384, rbar);
   }
   __syncthreads();   // q and the page ids are in shared memory
+
+  // ---- the source address of every tile of the split, bit 0 set when its
+  // page id is valid (else the copy reads a zero tile and its tokens are
+  // masked); bad page ids are reported here, once per tile ----
+  for (int i = threadIdx.x; i < t_end - t_begin; i += NW * 32) {
+    const int t = t_begin + i;
+    const int pid = spid[(t >> tsh) - p_begin];
+    if (pid >= 0 && pid < a.num_pages) {
+      saddr[i] = reinterpret_cast<uint64_t>(head_base + (size_t)pid * a.page_bytes +
+                                            (t & tmask) * a.tile_bytes) | 1ull;
+    } else {
+      saddr[i] = reinterpret_cast<uint64_t>(g_zero_tile);
+      flag_error(a.err, KV_DEVERR_PAGE_ID);
+    }
+  }
 
   // ---- q' = q R_k and its per-group sums (overlaps the first copies) ----
   rotate_q<S::HP, NW>(sq, rk, sqr);
@@ -699,10 +724,12 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
     for (int grp = 0; grp < NG; ++grp) sumq[nt][grp] = ssum[(4 * nt + j) * 2 + grp] * 5.9604644775390625e-8f;
   const float sc24 = a.scale_log2 * 16777216.0f;   // 2^24 back on the scores
 
-  float m_run[NT], l_run[NT], zs[NT][NG], oacc[8][NT][4];
+  // base: the exponent reference as used (0 while m_run is still -inf)
+  float m_run[NT], base[NT], l_run[NT], zs[NT][NG], oacc[8][NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     m_run[nt] = kNegInf;
+    base[nt] = 0.f;
     l_run[nt] = 0.f;
 #pragma unroll
     for (int grp = 0; grp < NG; ++grp) zs[nt][grp] = 0.f;
@@ -730,9 +757,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
     const uint4 sz0 = *reinterpret_cast<const uint4*>(src + lane_sz);
     const uint4 sz1 =
         (GS == 64) ? *reinterpret_cast<const uint4*>(src + lane_sz + 16) : make_uint4(0, 0, 0, 0);
-    const int pid_cur = spid[(t >> tsh) - p_begin];
-    const bool page_ok = pid_cur >= 0 && pid_cur < a.num_pages;
-    if (!page_ok && lane == 0) flag_error(a.err, KV_DEVERR_PAGE_ID);
+    const bool page_ok = (saddr[t - t_begin] & 1ull) != 0;
     const bool v0 = page_ok && (t * kTile + r) < h;
     const bool v1 = page_ok && (t * kTile + r + 8) < h;
 
@@ -829,6 +854,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
         const float mnew = need ? tmax + kSlack : m_run[nt];
         const float alpha = need ? ((m_run[nt] == kNegInf) ? 0.f : exp2_neg(m_run[nt] - mnew)) : 1.f;
         m_run[nt] = mnew;
+        base[nt] = (mnew == kNegInf) ? 0.f : mnew;
         l_run[nt] *= alpha;
 #pragma unroll
         for (int grp = 0; grp < NG; ++grp) zs[nt][grp] *= alpha;
@@ -837,8 +863,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
 #pragma unroll
           for (int u = 0; u < 4; ++u) oacc[i][nt][u] *= alpha;
       }
-      const float base = (m_run[nt] == kNegInf) ? 0.f : m_run[nt];
-      const float p0 = exp2_neg(l0 - base), p1 = exp2_neg(l1 - base);
+      const float p0 = exp2_neg(l0 - base[nt]), p1 = exp2_neg(l1 - base[nt]);
       l_run[nt] += p0 + p1;
       // masked tokens have p = 0 and finite (stale or zero) records
 #pragma unroll
@@ -918,7 +943,8 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
   __syncthreads();
   // merged sums, transposed for the back-rotation, into q's slot (q and q' are
   // no longer needed); then back to the original basis, into the partial
-  merge_warps_t<G, NW>(swo, swm, swl, sq, sm + S::smm, sm + S::sml);
+  merge_warps_t<G, NW>(swo, swm, swl, sq, sm + S::smm, sm + S::sml,
+                       reinterpret_cast<float*>(spid));   // page ids no longer needed
   rotate_back_to_part<G, NW>(sq, srv, sm + S::spr, part, sm + S::smm, sm + S::sml);
 }
 

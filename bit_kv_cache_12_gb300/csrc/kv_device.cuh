@@ -175,9 +175,8 @@ __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_c
 // (hi, lo) fp16 split of an fp32 value packed as one f16x2 register:
 // low half = fp16(x), high half = fp16(x - fp16(x)).
 __device__ __forceinline__ uint32_t split_hi_lo(float x) {
-  __half h = __float2half_rn(x);
-  float r = x - __half2float(h);
-  return h2_as_u32(__halves2half2(h, __float2half_rn(r)));
+  const float r = x - __half2float(__float2half_rn(x));
+  return h2_as_u32(__floats2half2_rn(x, r));   // one packed convert; x rounds to fp16(x) again
 }
 
 // All eight f16x2 MMA registers of one 32-bit code word, as exact fp16
