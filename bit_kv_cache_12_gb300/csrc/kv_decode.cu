@@ -387,8 +387,10 @@ __device__ void merge_parts(const DecodeArgs& a, int b, int g, int nparts, float
       for (int u = 0; u < kMergeBatch; ++u) {
         const int s = s0 + u;
         const float* pp = ph + (size_t)s * G * kPart;
-        mv[u] = (s < nparts) ? __ldcg(pp) : kNegInf;
-        lv[u] = (s < nparts) ? __ldcg(pp + 1) : 0.f;
+        const float2 ml = (s < nparts) ? __ldcg(reinterpret_cast<const float2*>(pp))
+                                       : make_float2(kNegInf, 0.f);
+        mv[u] = ml.x;
+        lv[u] = ml.y;
         ov[u] = (s < nparts) ? __ldcg(pp + 4 + c) : 0.f;
       }
       float Mb = M;
@@ -757,9 +759,10 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
     const uint4 sz0 = *reinterpret_cast<const uint4*>(src + lane_sz);
     const uint4 sz1 =
         (GS == 64) ? *reinterpret_cast<const uint4*>(src + lane_sz + 16) : make_uint4(0, 0, 0, 0);
-    const bool page_ok = (saddr[t - t_begin] & 1ull) != 0;
-    const bool v0 = page_ok && (t * kTile + r) < h;
-    const bool v1 = page_ok && (t * kTile + r + 8) < h;
+    // tokens of this tile still inside the history (none if its page id is bad)
+    const int lim = ((saddr[t - t_begin] & 1ull) != 0) ? h - t * kTile : 0;
+    const bool v0 = r < lim;
+    const bool v1 = r + 8 < lim;
 
     // scale / zero of tokens r and r+8
     float sk[2][NG], zk[2][NG], sv[2][NG], zv[2][NG];
