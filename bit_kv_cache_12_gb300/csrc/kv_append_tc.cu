@@ -291,19 +291,10 @@ __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, con
   float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
   for (int cb = 0; cb < 2; ++cb) {
-    float v[32], w[32];
+    float v[32];
     clipped32(cb, v);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) w[i] = v[i];
-#pragma unroll
-    for (int st = 16; st >= 1; st >>= 1)
-#pragma unroll
-      for (int i = 0; i < st; ++i) {
-        v[i] = fminf(v[i], v[i + st]);
-        w[i] = fmaxf(w[i], w[i + st]);
-      }
-    mn = fminf(mn, v[0]);
-    mx = fmaxf(mx, w[0]);
+    mn = min_of32(mn, v);
+    mx = max_of32(mx, v);
   }
   if (GS == 128) {   // the group spans both channel halves: combine with warp w ^ 4
     sstat[hf * 128 + m] = make_float2(mn, mx);
@@ -356,11 +347,7 @@ __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, con
       word_of(32 * cb + i) += __float_as_uint(rr) * (1u << pos) - (0x4B400000u << pos);
       v[i] = fabsf(__fsub_rn(t, __fsub_rn(rr, 12582912.0f)));
     }
-#pragma unroll
-    for (int st = 16; st >= 1; st >>= 1)
-#pragma unroll
-      for (int i = 0; i < st; ++i) v[i] = fmaxf(v[i], v[i + st]);
-    emax = fmaxf(emax, v[0]);
+    emax = max_of32(emax, v);
   }
   // warp-uniform: the re-read is a warp-collective tensor-memory load, and a
   // lane without a near tie recomputes its own codes unchanged
