@@ -254,6 +254,41 @@ __device__ __forceinline__ void issue_rotation(uint32_t tmem, uint32_t sA, uint3
   tc_commit(smem_u32(bar));
 }
 
+// Three-input minimum / maximum (one instruction on sm_100 and later); exact,
+// so reductions built from them give the same value in any order (up to the
+// sign of a zero, which the quantizer canonicalises).
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// min / max of acc and 32 values: two independent chains of 3-input steps
+__device__ __forceinline__ float min_of32(float acc, const float (&v)[32]) {
+  float c0 = v[0], c1 = v[1];
+#pragma unroll
+  for (int i = 2; i < 30; i += 4) {
+    c0 = min3f(c0, v[i], v[i + 1]);
+    c1 = min3f(c1, v[i + 2], v[i + 3]);
+  }
+  c0 = min3f(c0, v[30], v[31]);
+  return min3f(acc, c0, c1);
+}
+__device__ __forceinline__ float max_of32(float acc, const float (&v)[32]) {
+  float c0 = v[0], c1 = v[1];
+#pragma unroll
+  for (int i = 2; i < 30; i += 4) {
+    c0 = max3f(c0, v[i], v[i + 1]);
+    c1 = max3f(c1, v[i + 2], v[i + 3]);
+  }
+  c0 = max3f(c0, v[30], v[31]);
+  return max3f(acc, c0, c1);
+}
+
 // The codes of one accumulator row (token row m; channels 64 hf .. 64 hf + 63)
 // after clipping, with s and z from the group's range: x' read from tensor
 // memory (lanes of this warp's quarter, address trow), the range first and then

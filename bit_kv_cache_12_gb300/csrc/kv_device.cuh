@@ -71,41 +71,6 @@ __device__ __forceinline__ uint32_t quant_code(float y, const ScaleZero& q) {
 
 __device__ __forceinline__ float clip_to(float x, float c) { return fminf(fmaxf(x, -c), c); }
 
-// Three-input minimum / maximum (one instruction on sm_100 and later); exact,
-// so reductions built from them give the same value in any order (up to the
-// sign of a zero, which the quantizer canonicalises).
-__device__ __forceinline__ float min3f(float a, float b, float c) {
-  float r;
-  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-__device__ __forceinline__ float max3f(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-// min / max of acc and 32 values: two independent chains of 3-input steps
-__device__ __forceinline__ float min_of32(float acc, const float (&v)[32]) {
-  float c0 = v[0], c1 = v[1];
-#pragma unroll
-  for (int i = 2; i < 30; i += 4) {
-    c0 = min3f(c0, v[i], v[i + 1]);
-    c1 = min3f(c1, v[i + 2], v[i + 3]);
-  }
-  c0 = min3f(c0, v[30], v[31]);
-  return min3f(acc, c0, c1);
-}
-__device__ __forceinline__ float max_of32(float acc, const float (&v)[32]) {
-  float c0 = v[0], c1 = v[1];
-#pragma unroll
-  for (int i = 2; i < 30; i += 4) {
-    c0 = max3f(c0, v[i], v[i + 1]);
-    c1 = max3f(c1, v[i + 2], v[i + 3]);
-  }
-  c0 = max3f(c0, v[30], v[31]);
-  return max3f(acc, c0, c1);
-}
-
 // ---------------------------------------------------------------------------
 // memory
 // ---------------------------------------------------------------------------
