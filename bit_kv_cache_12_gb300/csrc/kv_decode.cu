@@ -105,9 +105,11 @@ struct DecodeArgs {
 };
 
 // Shared-memory carve-up (in floats) for a CTA of NW warps.  A fixed head
-// (q, q', page ids, merged m/l) is followed by one region reused by phase:
-// the history warps' bulk-copy rings, or a tier CTA's staged rows and softmax
-// weights, then the per-warp results; the final merge reuses everything.
+// (q, q', page ids, merged m/l; for INT2 also the ring barriers and the
+// split's per-tile source addresses) is followed by one region reused by
+// phase: the history warps' bulk-copy rings, or a tier CTA's staged rows and
+// softmax weights, then the per-warp results; the BF16 decode's final merge
+// reuses everything (the INT2 final merge reads only global memory).
 template <int G, int GS, int NW, bool kInt2>
 struct Lay {
   static constexpr int HP = (G <= 4) ? 4 : 4 * ((G + 3) / 4);   // padded heads (MMA columns)
