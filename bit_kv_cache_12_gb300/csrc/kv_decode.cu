@@ -1020,8 +1020,21 @@ __global__ void __launch_bounds__(int2_warps(G) * 32, 1) decode_int2_kernel(Deco
   constexpr int NW = int2_warps(G);
   extern __shared__ float4 smem4[];
   float* sm = reinterpret_cast<float*>(smem4);
-  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  // launch order: every history split first ((sequence, KV head) pairs in
+  // turn, their splits together), then every tier CTA, so that on a grid of
+  // several waves the short tier CTAs fill the last wave
   const int nparts = a.n_split + a.n_tier;
+  const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  const int n_hist = a.n_split * gridDim.y * gridDim.z;
+  int split, pair;
+  if (lin < n_hist) {
+    split = lin % a.n_split;
+    pair = lin / a.n_split;
+  } else {
+    split = a.n_split + (lin - n_hist) % a.n_tier;
+    pair = (lin - n_hist) / a.n_tier;
+  }
+  const int g = pair % a.Hkv, b = pair / a.Hkv;
   float* part = a.ws + ((size_t)(b * a.Hkv + g) * nparts + split) * G * kPart;
   if (split < a.n_split)
     int2_history<G, GS, kMulti>(a, b, g, split, sm, part);
