@@ -1,20 +1,26 @@
 """Benchmark: INT2 paged decode-attention step on one GB300.
 
-Default workload (the one the headline number is quoted on): Qwen3-4B-shaped
+Headline workload (the one the metric is quoted on): Qwen3-4B-shaped
 single-layer decode, batch 1, 32 q / 8 KV heads, head_dim 128, context
 100,000 tokens = 64 BF16 sink + 99,680 INT2 history + 256 BF16 recent, page 16
 with a shuffled page table, group 128.  Inputs are seeded synthetic data
 (``bit_kv_cache_12_gb300.synth``, the generator the parity tests use); the pool
 is filled by the library's own append kernel.
 
-``--workload`` selects the other workloads of the same study, generated on the
-device from seeded torch generators with the same shapes and value structure:
+The default run also measures, in the same JSON line under ``workloads``,
+every other workload of the study (``bit_kv_cache_12_gb300.workloads``:
+seeded device generators with the same shapes and value structure):
+  tiny      batch 1, 8 q / 2 KV heads, context 1,024, page 16, group 128
   batch64   Qwen3-8B shape, batch 64, context U[8192, 32768] per sequence,
             page 16, 4 outlier channels per head x10, Haar R, group 128
   long16    Qwen3-32B shape, batch 16, 64 q / 8 KV heads (GQA 8), context
             131,072, page 32, 0.1% token positions x20, Haar R, group 128
   append    64 sequences x 8 KV heads x 4096 tokens evicted in one call,
             Student-t(4) K/V, separate R_k / R_v, clip 0.9, group 64, page 16
+and the online step a server runs (``online_step``): one ``kv_append_step``
+(the new token enters the recent ring and the oldest recent token is rotated,
+quantized and packed into history) followed by the decode, at batch 1 (the
+headline workload) and at batch 64.  ``--workload`` runs one of them alone.
 
 One step = one ``kv_decode_attention`` call (whole batch, one layer), or one
 ``kv_append_quantize`` call for ``append``.  Every timed step is preceded by
@@ -23,7 +29,7 @@ read so the dirty lines are written back before the step starts.  Timing:
 CUDA events on the launching stream around each step, device synchronised
 before and after, max over ranks (one replica of the workload per GPU).
 
-``--impl reference`` times the CPU oracle on the default workload instead:
+``--impl reference`` times the CPU oracle on the headline workload instead:
 W untimed and K timed whole decode steps on the host cores.
 
 Prints exactly one JSON line on rank 0.
@@ -44,6 +50,7 @@ sys.path.insert(0, ROOT)
 METRIC = "INT2 paged decode-attention us/step (HBM GB/s, % of roofline) vs BF16 path"
 APPEND_METRIC = "INT2 append (rotate, clip, quantize, pack) us/call (HBM GB/s, % of roofline)"
 L2_NOTE = "flushed between steps (256 MiB write + 256 MiB read outside the timed events)"
+WORKLOADS = ["all", "qwen3_4b", "tiny", "batch64", "long16", "append"]
 
 
 def parse():
@@ -52,7 +59,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="qwen3_4b", choices=["qwen3_4b", "batch64", "long16", "append"])
+    ap.add_argument("--workload", default="all", choices=WORKLOADS)
     ap.add_argument("--ctx", type=int, default=100_000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -108,6 +115,13 @@ def bf16_bytes(c):
     lens = c.sink_len + c.hist_len + c.rec_len
     pages = int(np.sum((lens + c.P - 1) // c.P))
     return int(np.sum(lens)) * c.Hkv * 512 + pages * 4 * c.Hkv + c.B * c.Hq * 128 * 6
+
+
+def append_bytes_flops(n_rows, GS):
+    """Append: bf16 K and V rows in; codes and (s, z) out; x R for K and V."""
+    alg = n_rows * 256 * 2 + n_rows * (32 + 4 * (128 // GS)) * 2
+    flops = 2.0 * 128 * 128 * n_rows * 2
+    return alg, flops
 
 
 # --------------------------------------------------------------------------
@@ -212,12 +226,43 @@ def cpu_baseline(wl, min_seconds=10.0, max_seconds=30.0):
                       f"(unpack, dequantize, three-tier attention) in {dt:.1f} s"}
 
 
+_SINGLE_CORE_CHILD = r"""
+import json, os, sys, time
+sys.path.insert(0, sys.argv[1])
+os.sched_setaffinity(0, {min(os.sched_getaffinity(0))})
+import bench
+from bit_kv_cache_12_gb300 import synth
+wl = synth.qwen3_4b_decode(ctx=int(sys.argv[2]))
+step = bench._oracle_step_fn(wl)
+t0 = time.perf_counter(); step(); dt = time.perf_counter() - t0
+print(json.dumps({"seconds": dt, "cores": len(os.sched_getaffinity(0))}))
+"""
+
+
+def cpu_baseline_single_core(ctx):
+    """One whole oracle decode step of the headline workload on one host core
+    (a child process pinned to one core, every thread pool of numpy's BLAS
+    limited to one thread before numpy loads)."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = "1"
+    try:
+        r = subprocess.run([sys.executable, "-c", _SINGLE_CORE_CHILD, ROOT, str(ctx)], env=env,
+                           capture_output=True, text=True, timeout=300)
+        res = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:                       # a host without the affinity call, a timeout
+        return {"value": None, "error": str(e)[:200]}
+    return {"value": res["seconds"] * 1e6, "unit": "us", "cores": res["cores"],
+            "sample": "one whole decode step of the bench workload with the numpy fp64 oracle, "
+                      "one process pinned to one core, BLAS threads 1"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    if args.workload != "qwen3_4b":
+    if args.workload not in ("all", "qwen3_4b"):
         print(json.dumps({"impl": "reference", "unavailable":
-                          f"the oracle reference arm covers the default workload only, not {args.workload}"}))
+                          f"the oracle reference arm covers the headline workload only, not {args.workload}"}))
         return
     from bit_kv_cache_12_gb300 import synth
     wl = synth.qwen3_4b_decode(ctx=args.ctx)
@@ -236,123 +281,16 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": us, "unit": "us",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded)", "config": config_of_wl(wl), "cpu_baseline": cb,
+            "data": "synthetic (seeded)", "config": headline_config(wl), "cpu_baseline": cb,
             "e2e": {"value": us, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
 
-def config_of_wl(wl):
+def headline_config(wl):
     return {"workload": wl.name, "batch": wl.B, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": 128,
             "context": int(wl.meta["ctx"][0]), "sink": int(wl.sink_len[0]),
             "int2_history": int(wl.hist_len[0]), "recent": int(wl.rec_len[0]),
             "page_size": wl.page_size, "group_size": wl.group_size, "l2": L2_NOTE}
-
-
-# --------------------------------------------------------------------------
-# decode workloads resident on the device
-# --------------------------------------------------------------------------
-
-class Case:
-    """A three-tier decode workload whose K/V live on the device."""
-
-
-def case_from_synth(wl, torch, dev):
-    def bf16(u16):
-        return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).view(torch.bfloat16).to(dev)
-    c = Case()
-    c.name, c.B, c.Hq, c.Hkv, c.P, c.GS, c.scale = (wl.name, wl.B, wl.Hq, wl.Hkv, wl.page_size,
-                                                    wl.group_size, wl.scale)
-    c.sink_len, c.hist_len = wl.sink_len.astype(np.int32), wl.hist_len.astype(np.int32)
-    c.rec_len, c.rec_start = wl.rec_len.astype(np.int32), wl.rec_start.astype(np.int32)
-    c.page_table, c.num_pages = wl.page_table, wl.num_pages
-    c.Rk, c.Rv, c.clip_k, c.clip_v = wl.Rk, wl.Rv, wl.clip_k, wl.clip_v
-    c.q_np = wl.q
-    c.q = bf16(wl.q)
-    c.hist_k = bf16(np.concatenate(wl.hist_k)); c.hist_v = bf16(np.concatenate(wl.hist_v))
-    c.sink_k, c.sink_v = bf16(wl.sink_k), bf16(wl.sink_v)
-    c.rec_k, c.rec_v = bf16(wl.rec_k), bf16(wl.rec_v)
-    c.config = config_of_wl(wl)
-    return c
-
-
-def _haar(rng, n):
-    from bit_kv_cache_12_gb300 import synth
-    return np.stack([synth.haar_orthogonal(rng) for _ in range(n)]).astype(np.float32)
-
-
-def _clip_from(x, R, ratio, torch):
-    """ratio x per-channel absmax of the rotated rows x [T][Hkv][128] (device)."""
-    Hkv = x.shape[1]
-    out = np.zeros((Hkv, 128), np.float32)
-    for g in range(Hkv):
-        Rg = torch.as_tensor(R[g], device=x.device)
-        m = torch.zeros(128, device=x.device)
-        for s in range(0, x.shape[0], 1 << 18):
-            m = torch.maximum(m, (x[s:s + (1 << 18), g].float() @ Rg).abs().amax(dim=0))
-        out[g] = ratio * m.cpu().numpy()
-    return out
-
-
-def case_generated(kind, torch, dev):
-    """batch64 / long16 workloads generated on the device (seeded)."""
-    S_CAP, W_CAP = 64, 256
-    if kind == "batch64":
-        seed, B, Hq, Hkv, P = 4, 64, 32, 8, 16
-        rng = np.random.default_rng(seed)
-        ctx = rng.integers(8192, 32768 + 1, size=B)
-        name = "qwen3_8b_b64_h32x8_ctx8192-32768"
-    else:
-        seed, B, Hq, Hkv, P = 5, 16, 64, 8, 32
-        rng = np.random.default_rng(seed)
-        ctx = np.full(B, 131072)
-        name = "qwen3_32b_b16_h64x8_ctx131072"
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(seed)
-    c = Case()
-    c.name, c.B, c.Hq, c.Hkv, c.P, c.GS, c.scale = name, B, Hq, Hkv, P, 128, 1.0 / np.sqrt(128.0)
-    c.sink_len = np.minimum(ctx, S_CAP).astype(np.int32)
-    c.rec_len = np.minimum(ctx - c.sink_len, W_CAP).astype(np.int32)
-    c.hist_len = (ctx - c.sink_len - c.rec_len).astype(np.int32)
-    c.rec_start = rng.integers(0, W_CAP, size=B).astype(np.int32)
-    pages_per = (c.hist_len + P - 1) // P
-    c.num_pages = int(pages_per.sum()) + 1
-    perm = rng.permutation(c.num_pages).astype(np.int32)
-    c.page_table = np.full((B, int(pages_per.max())), -1, np.int32)
-    o = 0
-    for b in range(B):
-        c.page_table[b, :pages_per[b]] = perm[o:o + pages_per[b]]; o += pages_per[b]
-    T = int(c.hist_len.sum())
-    scale = torch.ones(Hkv, 128, device=dev)
-    if kind == "batch64":                      # 4 outlier channels per KV head, x10
-        for g in range(Hkv):
-            scale[g, torch.as_tensor(rng.choice(128, 4, replace=False), device=dev)] = 10.0
-
-    def kv(n_rows):
-        return (torch.randn(n_rows, Hkv, 128, generator=gen, device=dev) * scale).to(torch.bfloat16)
-    c.hist_k, c.hist_v = kv(T), kv(T)
-    c.sink_k = kv(B * S_CAP).view(B, S_CAP, Hkv, 128).transpose(1, 2).contiguous()
-    c.sink_v = kv(B * S_CAP).view(B, S_CAP, Hkv, 128).transpose(1, 2).contiguous()
-    c.rec_k = kv(B * W_CAP).view(B, W_CAP, Hkv, 128).transpose(1, 2).contiguous()
-    c.rec_v = kv(B * W_CAP).view(B, W_CAP, Hkv, 128).transpose(1, 2).contiguous()
-    if kind == "long16":                       # 0.1% token positions per sequence, all heads, x20
-        n_out = int(round(0.001 * 131072))
-        cu = np.concatenate([[0], np.cumsum(c.hist_len)])
-        for b in range(B):
-            pos = rng.choice(int(c.hist_len[b]), n_out, replace=False) + cu[b]
-            idx = torch.as_tensor(pos, device=dev)
-            c.hist_k[idx] = (c.hist_k[idx].float() * 20).to(torch.bfloat16)
-            c.hist_v[idx] = (c.hist_v[idx].float() * 20).to(torch.bfloat16)
-    c.Rk, c.Rv = _haar(rng, Hkv), _haar(rng, Hkv)
-    c.clip_k = _clip_from(c.hist_k, c.Rk, 0.95, torch)
-    c.clip_v = _clip_from(c.hist_v, c.Rv, 0.95, torch)
-    c.q = torch.randn(B, Hq, 128, generator=gen, device=dev).to(torch.bfloat16)
-    c.q_np = c.q.view(torch.int16).cpu().numpy().view(np.uint16)
-    c.config = {"workload": name, "batch": B, "q_heads": Hq, "kv_heads": Hkv, "head_dim": 128,
-                "context": [int(ctx.min()), int(ctx.max())], "context_mean": float(ctx.mean()),
-                "sink": S_CAP, "recent": W_CAP, "int2_history_tokens": T, "page_size": P,
-                "group_size": 128, "l2": L2_NOTE,
-                "generation": "seeded torch generator on the device"}
-    return c
 
 
 # --------------------------------------------------------------------------
@@ -393,85 +331,202 @@ def peak_hbm():
     return 6800.0, "fallback 6.8 TB/s"
 
 
+def us_stats(t_ms):
+    return {"us": float(np.mean(t_ms) * 1e3),
+            "us_p10_p50_p90": [float(np.percentile(t_ms, p) * 1e3) for p in (10, 50, 90)]}
+
+
+class Env:
+    """What every measurement needs: torch, device, stream, timer, ranks."""
+
+    def __init__(self, args, torch, dev, rank, world, local, kvdist):
+        self.args, self.torch, self.dev = args, torch, dev
+        self.rank, self.world, self.local, self.kvdist = rank, world, local, kvdist
+        self.stream = torch.cuda.current_stream()
+        self.timed = make_timer(torch, dev, self.stream, kvdist)
+        self.peak, self.peak_src = peak_hbm()
+
+    def i32(self, a):
+        return self.torch.as_tensor(np.ascontiguousarray(np.asarray(a, np.int32))).to(self.dev)
+
+    def max_ranks(self, vals):
+        return self.kvdist.max_over_ranks(vals, device=self.dev)
+
+
 # --------------------------------------------------------------------------
-# decode benchmark
+# decode measurements
 # --------------------------------------------------------------------------
 
-def run_decode(args, c, wl, torch, dev, rank, world, local, kvdist):
-    from bit_kv_cache_12_gb300 import native
-    B, Hq, Hkv = c.B, c.Hq, c.Hkv
-    stream = torch.cuda.current_stream()
-    timed = make_timer(torch, dev, stream, kvdist)
+class DecodeRig:
+    """An INT2 pool filled with case c (the library's append), the decode step
+    over it, and the BF16 pool of the same tokens with its decode step.  With
+    ``spare_steps`` > 0 every sequence gets that many spare history positions
+    (page ids past the case's pages, in the extended table ``pt_ext``) for
+    per-step placement; the decode itself uses the case's own page table."""
 
-    def i32(a):
-        return torch.as_tensor(np.ascontiguousarray(np.asarray(a, np.int32))).to(dev)
+    def __init__(self, env, c, spare_steps=0):
+        from bit_kv_cache_12_gb300 import native
+        torch, dev, i32 = env.torch, env.dev, env.i32
+        self.env, self.c, self.native = env, c, native
+        B, Hq, Hkv = c.B, c.Hq, c.Hkv
+        spare_pages = (spare_steps + c.P - 1) // c.P + 1 if spare_steps else 0
+        pt_np = c.page_table
+        if spare_pages:
+            pages_per = (c.hist_len + c.P - 1) // c.P
+            pt_np = np.full((B, c.page_table.shape[1] + spare_pages), -1, np.int32)
+            for b in range(B):
+                n = int(pages_per[b])
+                pt_np[b, :n] = c.page_table[b, :n]
+                pt_np[b, n:n + spare_pages] = c.num_pages + b * spare_pages + np.arange(spare_pages)
+        self.pt_np, self.pt_ext_np = c.page_table, pt_np
+        self.pool = native.KVPool(native.KV_POOL_INT2_3TIER, 1, Hq, Hkv, c.P,
+                                  c.num_pages + B * spare_pages, B, group_size=c.GS)
+        self.Rk = torch.as_tensor(c.Rk).to(dev); self.Rv = torch.as_tensor(c.Rv).to(dev)
+        self.ck = torch.as_tensor(c.clip_k).to(dev); self.cv = torch.as_tensor(c.clip_v).to(dev)
+        native.kv_pool_set_rotation(self.pool.handle, 0, self.Rk, self.Rv, self.ck, self.cv)
+        sk, sv, rk, rv = self.pool.tier_views(0)
+        sk[:B].copy_(c.sink_k); sv[:B].copy_(c.sink_v)
+        rk[:B].copy_(c.rec_k); rv[:B].copy_(c.rec_v)
+        cu = np.zeros(B + 1, np.int32); cu[1:] = np.cumsum(c.hist_len)
+        self.cu = cu
+        self.pt = i32(c.page_table)
+        self.pt_ext = i32(pt_np)
+        native.kv_append_quantize(self.pool.handle, 0, B, c.hist_k, c.hist_v, i32(cu), i32(np.zeros(B)),
+                                  self.pt, c.page_table.shape[1], int(max(1, c.hist_len.max())))
+        torch.cuda.synchronize()
+        if self.pool.error():
+            raise RuntimeError("device error while filling the pool")
+        self.lens = [i32(c.sink_len), i32(c.hist_len), i32(c.rec_len), i32(c.rec_start)]
+        self.max_hist = int(c.hist_len.max())
+        self.ws_bytes = native.kv_decode_workspace_bytes(self.pool.handle, B, self.max_hist + spare_steps)
+        self.ws = torch.zeros(self.ws_bytes // 4 + 4, dtype=torch.float32, device=dev)
+        self.out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+        self.bpool = None
 
-    # ---- INT2 pool filled by the library's append kernel ----
-    pool = native.KVPool(native.KV_POOL_INT2_3TIER, 1, Hq, Hkv, c.P, c.num_pages, B, group_size=c.GS)
-    Rk = torch.as_tensor(c.Rk).to(dev); Rv = torch.as_tensor(c.Rv).to(dev)
-    ck = torch.as_tensor(c.clip_k).to(dev); cv = torch.as_tensor(c.clip_v).to(dev)
-    native.kv_pool_set_rotation(pool.handle, 0, Rk, Rv, ck, cv)
-    sk, sv, rk, rv = pool.tier_views(0)
-    sk[:B].copy_(c.sink_k); sv[:B].copy_(c.sink_v)
-    rk[:B].copy_(c.rec_k); rv[:B].copy_(c.rec_v)
-    cu = np.zeros(B + 1, np.int32); cu[1:] = np.cumsum(c.hist_len)
-    pt = i32(c.page_table)
-    native.kv_append_quantize(pool.handle, 0, B, c.hist_k, c.hist_v, i32(cu), i32(np.zeros(B)), pt,
-                              c.page_table.shape[1], int(c.hist_len.max()))
-    torch.cuda.synchronize()
-    if pool.error():
-        raise RuntimeError("device error while filling the pool")
+    def decode(self, q=None, lens=None, out=None, max_hist=None, extended=False):
+        c, n = self.c, self.native
+        pt, pt_np = (self.pt_ext, self.pt_ext_np) if extended else (self.pt, self.pt_np)
+        n.kv_decode_attention(self.pool.handle, 0, c.B, c.q if q is None else q,
+                              *(self.lens if lens is None else lens), pt, pt_np.shape[1],
+                              self.max_hist if max_hist is None else max_hist, c.scale,
+                              self.out if out is None else out, self.ws, self.ws_bytes, self.env.stream)
 
-    q = c.q
-    sink_len, hist_len = i32(c.sink_len), i32(c.hist_len)
-    rec_len, rec_start = i32(c.rec_len), i32(c.rec_start)
-    max_hist = int(c.hist_len.max())
-    ws_bytes = native.kv_decode_workspace_bytes(pool.handle, B, max_hist)
-    ws = torch.zeros(ws_bytes // 4 + 4, dtype=torch.float32, device=dev)
-    out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+    def build_bf16(self):
+        """The BF16 pool with the same tokens in logical order (sink, history,
+        ring from its start), shuffled pages."""
+        torch, dev, c, n, i32 = self.env.torch, self.env.dev, self.c, self.native, self.env.i32
+        B = c.B
+        lens = (c.sink_len + c.hist_len + c.rec_len).astype(np.int32)
+        bpages = (lens + c.P - 1) // c.P
+        brng = np.random.default_rng(77)
+        btotal = int(bpages.sum()) + 1
+        bperm = brng.permutation(btotal).astype(np.int32)
+        bpt_np = np.full((B, int(bpages.max())), -1, np.int32)
+        o = 0
+        for b in range(B):
+            bpt_np[b, :bpages[b]] = bperm[o:o + bpages[b]]; o += bpages[b]
+        self.bpool = n.KVPool(n.KV_POOL_BF16, 1, c.Hq, c.Hkv, c.P, btotal, B)
+        W_cap = c.rec_k.shape[2]
+        for b in range(B):
+            s_, r_ = int(c.sink_len[b]), int(c.rec_len[b])
+            ring = torch.as_tensor((c.rec_start[b] + np.arange(r_)) % W_cap, device=dev)
+            kk = torch.cat([c.sink_k[b, :, :s_].transpose(0, 1), c.hist_k[self.cu[b]:self.cu[b + 1]],
+                            c.rec_k[b][:, ring].transpose(0, 1)]).contiguous()
+            vv = torch.cat([c.sink_v[b, :, :s_].transpose(0, 1), c.hist_v[self.cu[b]:self.cu[b + 1]],
+                            c.rec_v[b][:, ring].transpose(0, 1)]).contiguous()
+            n.kv_append_bf16(self.bpool.handle, 0, 1, kk, vv, i32([0, kk.shape[0]]), i32([0]),
+                             i32(bpt_np[b:b + 1]), bpt_np.shape[1], kk.shape[0])
+            del kk, vv
+        torch.cuda.synchronize()
+        self.bpt_np, self.bpt, self.blens = bpt_np, i32(bpt_np), i32(lens)
+        self.bmax = int(lens.max())
+        self.bws_bytes = n.kv_decode_workspace_bytes(self.bpool.handle, B, self.bmax)
+        self.bws = torch.zeros(self.bws_bytes // 4 + 4, dtype=torch.float32, device=dev)
+        self.bout = torch.empty_like(self.out)
+
+    def decode_bf16(self):
+        c = self.c
+        self.native.kv_decode_attention_bf16(self.bpool.handle, 0, c.B, c.q, self.blens, self.bpt,
+                                             self.bpt_np.shape[1], self.bmax, c.scale, self.bout,
+                                             self.bws, self.bws_bytes, self.env.stream)
+
+    def errors(self):
+        return (self.pool.error() if self.pool else 0) or (self.bpool.error() if self.bpool else 0)
+
+    def close(self):
+        for p in (self.pool, self.bpool):
+            if p is not None:
+                p.close()
+        self.pool = self.bpool = None
+
+
+def decode_summary(env, rig, steps, warmup, with_bf16=True):
+    """INT2 and BF16 decode of a rig: times, algorithmic bytes, GB/s, roofline."""
+    c = rig.c
+    t = env.timed(rig.decode, steps, max(3, warmup))
+    res = us_stats(t)
+    res["us"] = env.max_ranks([res["us"]])[0]
+    alg, parts = algorithmic_bytes(c)
+    gbs = alg / (res["us"] * 1e-6) / 1e9
+    res.update({"algorithmic_bytes": alg, "gbs": gbs, "frac_of_measured_peak": gbs / env.peak,
+                "frac_of_8tbs": gbs / 8000.0})
+    if with_bf16:
+        rig.build_bf16()
+        tb = env.timed(rig.decode_bf16, max(5, steps // 2), 3)
+        us_b = env.max_ranks([float(np.mean(tb) * 1e3)])[0]
+        bb = bf16_bytes(c)
+        res["bf16_path"] = {"us": us_b, "bytes": bb, "gbs": bb / (us_b * 1e-6) / 1e9,
+                            "frac_of_measured_peak": bb / (us_b * 1e-6) / 1e9 / env.peak,
+                            "speedup_int2_vs_bf16": us_b / res["us"]}
+    if rig.errors():
+        raise RuntimeError(f"device error during the {c.name} steps")
+    return res, t, parts
+
+
+def online_step(env, rig, steps, warmup, decode_us):
+    """The step a server runs: kv_append_step (every sequence's new token
+    enters its recent ring; the full ring's oldest token is rotated, clipped,
+    quantized and packed into history) then the decode reading the
+    device-updated lengths.  Every timed step grows each history by one."""
+    torch, c, n = env.torch, rig.c, rig.native
+    gen = torch.Generator(device=env.dev)
+    gen.manual_seed(11)
+    new = torch.randn(2, c.B, c.Hkv, 128, generator=gen, device=env.dev).to(torch.bfloat16)
+    lens = [env.i32(c.sink_len), env.i32(c.hist_len), env.i32(c.rec_len), env.i32(c.rec_start)]
+    total = max(3, warmup) + steps
+    max_hist = rig.max_hist + total
+
+    def place():
+        n.kv_append_step(rig.pool.handle, 0, c.B, new[0], new[1], *lens, rig.pt_ext,
+                         rig.pt_ext_np.shape[1], env.stream)
 
     def step():
-        native.kv_decode_attention(pool.handle, 0, B, q, sink_len, hist_len, rec_len, rec_start, pt,
-                                   c.page_table.shape[1], max_hist, c.scale, out, ws, ws_bytes, stream)
+        place()
+        rig.decode(lens=lens, max_hist=max_hist, extended=True)
+    t = env.timed(step, steps, max(3, warmup))
+    if rig.pool.error():
+        raise RuntimeError("device error during the online steps")
+    if not np.all(lens[1].cpu().numpy() == c.hist_len + total):
+        raise RuntimeError("the placement did not evict one token per step")
+    us = env.max_ranks([float(np.mean(t) * 1e3)])[0]
+    return {"us": us, "decode_alone_us": decode_us, "ratio_to_decode_alone": us / decode_us,
+            "batch": c.B, "launches_per_step": 2,
+            "what": "kv_append_step (new token into the recent ring, the oldest recent token rotated, "
+                    "clipped, quantized and packed into INT2 history) then kv_decode_attention "
+                    "over the updated cache, in one timed region"}
 
-    # ---- BF16 pool with the same tokens in logical order ----
-    lens = (c.sink_len + c.hist_len + c.rec_len).astype(np.int32)
-    bpages = (lens + c.P - 1) // c.P
-    brng = np.random.default_rng(77)
-    btotal = int(bpages.sum()) + 1
-    bperm = brng.permutation(btotal).astype(np.int32)
-    bpt_np = np.full((B, int(bpages.max())), -1, np.int32)
-    o = 0
-    for b in range(B):
-        bpt_np[b, :bpages[b]] = bperm[o:o + bpages[b]]; o += bpages[b]
-    bpool = native.KVPool(native.KV_POOL_BF16, 1, Hq, Hkv, c.P, btotal, B)
-    W_cap = c.rec_k.shape[2]
-    for b in range(B):
-        s_, r_ = int(c.sink_len[b]), int(c.rec_len[b])
-        ring = torch.as_tensor((c.rec_start[b] + np.arange(r_)) % W_cap, device=dev)
-        kk = torch.cat([c.sink_k[b, :, :s_].transpose(0, 1), c.hist_k[cu[b]:cu[b + 1]],
-                        c.rec_k[b][:, ring].transpose(0, 1)]).contiguous()
-        vv = torch.cat([c.sink_v[b, :, :s_].transpose(0, 1), c.hist_v[cu[b]:cu[b + 1]],
-                        c.rec_v[b][:, ring].transpose(0, 1)]).contiguous()
-        native.kv_append_bf16(bpool.handle, 0, 1, kk, vv, i32([0, kk.shape[0]]), i32([0]),
-                              i32(bpt_np[b:b + 1]), bpt_np.shape[1], kk.shape[0])
-        del kk, vv
-    torch.cuda.synchronize()
-    bpt = i32(bpt_np)
-    blen = i32(lens)
-    bws_bytes = native.kv_decode_workspace_bytes(bpool.handle, B, int(lens.max()))
-    bws = torch.zeros(bws_bytes // 4 + 4, dtype=torch.float32, device=dev)
-    bout = torch.empty_like(out)
 
-    def bstep():
-        native.kv_decode_attention_bf16(bpool.handle, 0, B, q, blen, bpt, bpt_np.shape[1],
-                                        int(lens.max()), c.scale, bout, bws, bws_bytes, stream)
-
-    with ClockSampler(local) as clk:
-        t_int2 = timed(step, args.steps, max(3, args.warmup))
-    t_bf16 = timed(bstep, max(5, args.steps // 2), 3)
-    if pool.error() or bpool.error():
-        raise RuntimeError("device error during the timed steps")
+def run_headline(env, wl):
+    """The headline workload: decode, BF16 path, end-to-end calls, several
+    queries per sequence, the online step and the oracle on the host."""
+    from bit_kv_cache_12_gb300 import workloads
+    args, torch, dev = env.args, env.torch, env.dev
+    c = workloads.case_from_synth(wl, torch, dev, L2_NOTE)
+    rig = DecodeRig(env, c, spare_steps=max(3, args.warmup) + args.steps + 8)
+    B, Hq = c.B, c.Hq
+    with ClockSampler(env.local) as clk:
+        res, t_int2, parts = decode_summary(env, rig, args.steps, args.warmup)
+    us = res["us"]
 
     # ---- end to end through the C ABI with host buffers: the step's inputs
     # (q and the four length arrays) in one pinned staging buffer, one copy in,
@@ -488,138 +543,107 @@ def run_decode(args, c, wl, torch, dev, rank, world, local, kvdist):
 
     def e2e_step():
         stage_dev.copy_(stage_host, non_blocking=True)
-        native.kv_decode_attention(pool.handle, 0, B, q_dev, meta_dev[0], meta_dev[1], meta_dev[2],
-                                   meta_dev[3], pt, c.page_table.shape[1], max_hist, c.scale, out,
-                                   ws, ws_bytes, stream)
-        out_host.copy_(out, non_blocking=True)
+        rig.decode(q=q_dev, lens=[meta_dev[0], meta_dev[1], meta_dev[2], meta_dev[3]])
+        out_host.copy_(rig.out, non_blocking=True)
 
-    t_e2e = timed(e2e_step, args.steps, 3)
+    t_e2e = env.timed(e2e_step, args.steps, 3)
     h2d = stage_host.numel()
     d2h = out_host.numel() * 4
 
-    # ---- the same call handed the pinned host buffers themselves: the kernel
-    # reads q and the lengths and writes out across the CPU-GPU link ----
+    # ---- the same call handed the pinned host buffers themselves ----
     q_host = stage_host[:q_bytes].view(torch.bfloat16).view(B, Hq, 128)
     meta_host = stage_host[q_bytes:].view(torch.int32).view(4, B)
 
     def mapped_step():
-        native.kv_decode_attention(pool.handle, 0, B, q_host, meta_host[0], meta_host[1], meta_host[2],
-                                   meta_host[3], pt, c.page_table.shape[1], max_hist, c.scale, out_host,
-                                   ws, ws_bytes, stream)
+        rig.decode(q=q_host, lens=[meta_host[0], meta_host[1], meta_host[2], meta_host[3]], out=out_host)
 
-    t_mapped = timed(mapped_step, args.steps, 3)
-    if pool.error():
-        raise RuntimeError("device error during the end-to-end steps")
+    t_mapped = env.timed(mapped_step, args.steps, 3)
 
-    # ---- several queries per sequence over the same cache (two positions of a
-    # chunk, or a draft and its successor), with the log-sum-exp ----
+    # ---- several queries per sequence over the same cache ----
+    from bit_kv_cache_12_gb300 import native
     TQ = 2
     qm = torch.randn(B, TQ, Hq, 128, generator=torch.Generator(device=dev).manual_seed(9),
                      device=dev).to(torch.bfloat16)
-    m_ws_bytes = native.kv_decode_multi_workspace_bytes(pool.handle, B, TQ, max_hist)
+    m_ws_bytes = native.kv_decode_multi_workspace_bytes(rig.pool.handle, B, TQ, rig.max_hist)
     m_ws = torch.zeros(m_ws_bytes // 4 + 4, dtype=torch.float32, device=dev)
     m_out = torch.empty((B, TQ, Hq, 128), dtype=torch.float32, device=dev)
     m_lse = torch.empty((B, TQ, Hq), dtype=torch.float32, device=dev)
 
     def mstep():
-        native.kv_decode_attention_multi(pool.handle, 0, B, TQ, qm, sink_len, hist_len, rec_len, rec_start,
-                                         pt, c.page_table.shape[1], max_hist, c.scale, m_out, m_lse, m_ws,
-                                         m_ws_bytes, stream)
+        native.kv_decode_attention_multi(rig.pool.handle, 0, B, TQ, qm, *rig.lens, rig.pt,
+                                         rig.pt_np.shape[1], rig.max_hist, c.scale, m_out, m_lse, m_ws,
+                                         m_ws_bytes, env.stream)
 
-    t_multi = (timed(mstep, max(5, args.steps // 2), 3)
-               if TQ * (Hq // Hkv) <= 8 else None)
+    t_multi = env.timed(mstep, max(5, args.steps // 2), 3) if TQ * (Hq // c.Hkv) <= 8 else None
+    if rig.pool.error():
+        raise RuntimeError("device error during the end-to-end and multi-query steps")
+    us_e2e, us_mapped = env.max_ranks([float(np.mean(t_e2e) * 1e3), float(np.mean(t_mapped) * 1e3)])
 
-    # ---- per-step token placement at batch 64 (every sequence evicts one
-    # recent token into INT2 history per step) ----
-    SB, SH, SP = 64, Hkv, 16
-    spool = native.KVPool(native.KV_POOL_INT2_3TIER, 1, Hq, SH, SP, SB * 4, SB, group_size=c.GS)
-    native.kv_pool_set_rotation(spool.handle, 0, Rk, Rv, ck, cv)
-    s_rng = np.random.default_rng(5)
-    s_pt = i32(s_rng.permutation(SB * 4).reshape(SB, 4))
-    s_lens = [i32(np.full(SB, 64)), i32(np.zeros(SB)), i32(np.full(SB, 256)), i32(np.zeros(SB))]
-    s_gen = torch.Generator(device=dev)
-    s_gen.manual_seed(5)
-    s_new = torch.randn(2, SB, SH, 128, generator=s_gen, device=dev).to(torch.bfloat16)
+    # ---- the online step at batch 1 (mutates the pool: last) ----
+    online = online_step(env, rig, args.steps, args.warmup, us)
+    rig.close()
 
-    def astep():
-        native.kv_append_step(spool.handle, 0, SB, s_new[0], s_new[1], *s_lens, s_pt, 4, stream)
-
-    t_step = timed(astep, 20, 3)
-    if spool.error():
-        raise RuntimeError("device error during the append steps")
-    spool.close()
-
-    us = float(np.mean(t_int2) * 1e3)
-    us_bf16 = float(np.mean(t_bf16) * 1e3)
-    us, us_bf16, us_e2e, us_mapped = kvdist.max_over_ranks(
-        [us, us_bf16, float(np.mean(t_e2e) * 1e3), float(np.mean(t_mapped) * 1e3)], device=dev)
-
-    alg, parts = algorithmic_bytes(c)
-    peak, peak_src = peak_hbm()
-    achieved = alg / (us * 1e-6) / 1e9
-    if rank == 0:
-        cb = None
-        if wl is not None and not args.no_cpu_baseline:
-            cb = cpu_baseline(wl)
-        line = {
-            "metric": METRIC, "value": us, "unit": "us", "n_gpus": world, "steps": args.steps,
-            "warmup": max(3, args.warmup), "ms_per_step": us / 1e3, "higher_is_better": False,
-            "scaling": "weak", "vs_baseline": None, "dtype": "int2 codes, f16 MMA, f32 accumulate",
-            "data": "synthetic (seeded; pool filled by kv_append_quantize)",
-            "config": c.config,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": measured_traffic(c.name),
-                         "peak_source": peak_src, "algorithmic_bytes": alg, "bytes_breakdown": parts},
-            "us_p10_p50_p90": [float(np.percentile(t_int2, p) * 1e3) for p in (10, 50, 90)],
-            "bf16_path": {"us": us_bf16, "bytes": bf16_bytes(c),
-                          "gbs": bf16_bytes(c) / (us_bf16 * 1e-6) / 1e9,
-                          "speedup_int2_vs_bf16": us_bf16 / us},
-            "append_step": {"us": float(np.mean(t_step) * 1e3), "batch": SB, "kv_heads": SH,
-                            "what": "one kv_append_step call (eviction and placement launches): each sequence's new token enters the "
-                                    "recent ring and its oldest recent token is rotated, clipped, "
-                                    "quantized and packed into INT2 history"},
-            "e2e": {"value": us_e2e, "unit": "us", "h2d_bytes_per_step": int(h2d),
-                    "d2h_bytes_per_step": int(d2h),
-                    "what": "kv_decode_attention with host buffers: one pinned staging copy in (q and "
-                            "the four length arrays), the output copied back, both inside the timed region"},
-            "e2e_host_mapped": {"value": us_mapped, "unit": "us", "h2d_bytes_per_step": int(h2d),
-                                "d2h_bytes_per_step": int(d2h),
-                                "what": "the same call given the pinned host buffers directly: the kernel "
-                                        "reads q and the lengths and writes the output across the CPU-GPU "
-                                        "link inside the timed region (no staging copies)"},
-            "multi_query": (None if t_multi is None else
-                            {"us": float(np.mean(t_multi) * 1e3), "queries_per_sequence": TQ,
-                             "what": "one kv_decode_attention_multi call over the same cache, "
-                                     "output and log-sum-exp"}),
-            "gpu_launches": args.steps,
-            "clocks": clk.summary(),
-            "cpu_baseline": cb,
-        }
-        print(json.dumps(line))
-    pool.close(); bpool.close()
+    achieved = res["algorithmic_bytes"] / (us * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": us, "unit": "us", "n_gpus": env.world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": us / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int2 codes, f16 MMA, f32 accumulate",
+        "data": "synthetic (seeded; pool filled by kv_append_quantize)",
+        "config": headline_config(wl),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": env.peak, "unit": "GB/s",
+                     "frac": achieved / env.peak, "traffic": measured_traffic(c.name),
+                     "peak_source": env.peak_src, "frac_of_8tbs": achieved / 8000.0,
+                     "algorithmic_bytes": res["algorithmic_bytes"], "bytes_breakdown": parts},
+        "us_p10_p50_p90": res["us_p10_p50_p90"],
+        "bf16_path": res["bf16_path"],
+        "online_step": {"batch1": online},
+        "e2e": {"value": us_e2e, "unit": "us", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h),
+                "what": "kv_decode_attention with host buffers: one pinned staging copy in (q and "
+                        "the four length arrays), the output copied back, both inside the timed region"},
+        "e2e_host_mapped": {"value": us_mapped, "unit": "us", "h2d_bytes_per_step": int(h2d),
+                            "d2h_bytes_per_step": int(d2h),
+                            "what": "the same call given the pinned host buffers directly: the kernel "
+                                    "reads q and the lengths and writes the output across the CPU-GPU "
+                                    "link inside the timed region (no staging copies)"},
+        "multi_query": (None if t_multi is None else
+                        {"us": float(np.mean(t_multi) * 1e3), "queries_per_sequence": TQ,
+                         "what": "one kv_decode_attention_multi call over the same cache, "
+                                 "output and log-sum-exp"}),
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    return line
 
 
-# --------------------------------------------------------------------------
-# append benchmark
-# --------------------------------------------------------------------------
+def run_decode_workload(env, c, steps, warmup, online=False):
+    rig = DecodeRig(env, c, spare_steps=(max(3, warmup) + steps + 8) if online else 0)
+    res, _, parts = decode_summary(env, rig, steps, warmup)
+    res["config"] = c.config
+    res["bytes_breakdown"] = parts
+    if online:
+        res["online_step"] = online_step(env, rig, steps, warmup, res["us"])
+    rig.close()
+    return res
 
-def run_append(args, torch, dev, rank, world, local, kvdist):
-    from bit_kv_cache_12_gb300 import native
+
+def run_append(env, steps, warmup):
+    """64 sequences x 8 KV heads x 4096 tokens evicted in one kv_append_quantize."""
+    from bit_kv_cache_12_gb300 import native, workloads
+    torch, dev = env.torch, env.dev
     n_seqs, Hkv, T, P, GS = 64, 8, 4096, 16, 64
     seed = 3
     rng = np.random.default_rng(seed)
     gen = torch.Generator(device=dev)
     gen.manual_seed(seed)
-    stream = torch.cuda.current_stream()
-    timed = make_timer(torch, dev, stream, kvdist)
 
     def student_t4(n):                         # N(0,1) / sqrt(chi2_4 / 4)
         z = torch.randn(n, Hkv, 128, generator=gen, device=dev)
         chi = (torch.randn(4, n, Hkv, 128, generator=gen, device=dev) ** 2).sum(0) / 4.0
         return (z / chi.sqrt()).to(torch.bfloat16)
     k, v = student_t4(n_seqs * T), student_t4(n_seqs * T)
-    Rk, Rv = _haar(rng, Hkv), _haar(rng, Hkv)
-    ck, cv = _clip_from(k, Rk, 0.9, torch), _clip_from(v, Rv, 0.9, torch)
+    Rk, Rv = workloads.haar_stack(rng, Hkv), workloads.haar_stack(rng, Hkv)
+    ck, cv = workloads.clip_from(k, Rk, 0.9, torch), workloads.clip_from(v, Rv, 0.9, torch)
     pages_per = T // P
     num_pages = n_seqs * pages_per
     pt_np = rng.permutation(num_pages).astype(np.int32).reshape(n_seqs, pages_per)
@@ -631,35 +655,22 @@ def run_append(args, torch, dev, rank, world, local, kvdist):
     pt = torch.as_tensor(pt_np, device=dev)
 
     def step():
-        native.kv_append_quantize(pool.handle, 0, n_seqs, k, v, cu, hs, pt, pages_per, T, stream)
+        native.kv_append_quantize(pool.handle, 0, n_seqs, k, v, cu, hs, pt, pages_per, T, env.stream)
 
-    with ClockSampler(local) as clk:
-        t = timed(step, args.steps, max(3, args.warmup))
+    t = env.timed(step, steps, max(3, warmup))
     if pool.error():
         raise RuntimeError("device error during the timed appends")
-    us = kvdist.max_over_ranks([float(np.mean(t) * 1e3)], device=dev)[0]
-    rows = n_seqs * T * Hkv
-    alg = rows * 256 * 2 + rows * (32 + 4 * (128 // GS)) * 2     # bf16 K+V in; codes + s/z out
-    flops = 2.0 * 128 * 128 * rows * 2                           # x R for K and V
-    peak, peak_src = peak_hbm()
-    achieved = alg / (us * 1e-6) / 1e9
-    if rank == 0:
-        line = {
-            "metric": APPEND_METRIC, "value": us, "unit": "us", "n_gpus": world, "steps": args.steps,
-            "warmup": max(3, args.warmup), "ms_per_step": us / 1e3, "higher_is_better": False,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, bf16 hi+lo MMA rotation, f32",
-            "data": "synthetic (seeded torch generator on the device, Student-t(4))",
-            "config": {"workload": "append_64x4096_h8_g64", "sequences": n_seqs, "tokens_per_seq": T,
-                       "kv_heads": Hkv, "page_size": P, "group_size": GS, "l2": L2_NOTE},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None, "peak_source": peak_src,
-                         "algorithmic_bytes": alg},
-            "rotation_tflops": flops / (us * 1e-6) / 1e12,
-            "us_p10_p50_p90": [float(np.percentile(t, p) * 1e3) for p in (10, 50, 90)],
-            "gpu_launches": args.steps, "clocks": clk.summary(), "cpu_baseline": None,
-        }
-        print(json.dumps(line))
     pool.close()
+    res = us_stats(t)
+    res["us"] = env.max_ranks([res["us"]])[0]
+    alg, flops = append_bytes_flops(n_seqs * T * Hkv, GS)
+    gbs = alg / (res["us"] * 1e-6) / 1e9
+    res.update({"algorithmic_bytes": alg, "gbs": gbs, "frac_of_measured_peak": gbs / env.peak,
+                "frac_of_8tbs": gbs / 8000.0, "rotation_tflops": flops / (res["us"] * 1e-6) / 1e12,
+                "launches": 2,
+                "config": {"workload": "append_64x4096_h8_g64", "sequences": n_seqs, "tokens_per_seq": T,
+                           "kv_heads": Hkv, "page_size": P, "group_size": GS, "l2": L2_NOTE}})
+    return res
 
 
 def main():
@@ -673,17 +684,58 @@ def main():
     # collective on the data path), timings reduced by max over ranks
     rank, world, local = kvdist.init("nccl")
     import torch
-    from bit_kv_cache_12_gb300 import synth
+    from bit_kv_cache_12_gb300 import synth, workloads
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if args.workload == "append":
-        run_append(args, torch, dev, rank, world, local, kvdist)
-    elif args.workload == "qwen3_4b":
+    env = Env(args, torch, dev, rank, world, local, kvdist)
+    w = args.workload
+    if w in ("all", "qwen3_4b"):
         wl = synth.qwen3_4b_decode(ctx=args.ctx)
-        run_decode(args, case_from_synth(wl, torch, dev), wl, torch, dev, rank, world, local, kvdist)
+        line = run_headline(env, wl)
+        if w == "all":
+            sub_steps = min(args.steps, 20)
+            nested = {}
+            nested["tiny"] = run_decode_workload(env, workloads.case_from_synth(synth.tiny_decode(), torch,
+                                                                                dev, L2_NOTE),
+                                                 sub_steps, args.warmup)
+            c = workloads.batch64(torch, dev, L2_NOTE)
+            nested["batch64"] = run_decode_workload(env, c, sub_steps, args.warmup, online=True)
+            line["online_step"]["batch64"] = nested["batch64"].pop("online_step")
+            del c
+            torch.cuda.empty_cache()
+            c = workloads.long16(torch, dev, L2_NOTE)
+            nested["long16"] = run_decode_workload(env, c, sub_steps, args.warmup)
+            del c
+            torch.cuda.empty_cache()
+            nested["append"] = run_append(env, sub_steps, args.warmup)
+            line["workloads"] = nested
+        if rank == 0:
+            cb = None
+            if not args.no_cpu_baseline:
+                cb = cpu_baseline(wl)
+                cb["single_core"] = cpu_baseline_single_core(args.ctx)
+            line["cpu_baseline"] = cb
+            print(json.dumps(line))
     else:
-        run_decode(args, case_generated(args.workload, torch, dev), None, torch, dev, rank, world,
-                   local, kvdist)
+        if w == "append":
+            res = run_append(env, args.steps, args.warmup)
+            metric = APPEND_METRIC
+        else:
+            c = (workloads.case_from_synth(synth.tiny_decode(), torch, dev, L2_NOTE) if w == "tiny"
+                 else getattr(workloads, w)(torch, dev, L2_NOTE))
+            res = run_decode_workload(env, c, args.steps, args.warmup, online=(w == "batch64"))
+            metric = METRIC
+        if rank == 0:
+            us = res.pop("us")
+            line = {"metric": metric, "value": us, "unit": "us", "n_gpus": world, "steps": args.steps,
+                    "warmup": max(3, args.warmup), "ms_per_step": us / 1e3, "higher_is_better": False,
+                    "scaling": "weak", "vs_baseline": None, "data": "synthetic (seeded)",
+                    "config": res.pop("config"),
+                    "roofline": {"bound": "hbm", "achieved": res["gbs"], "peak": env.peak, "unit": "GB/s",
+                                 "frac": res["frac_of_measured_peak"], "traffic": None,
+                                 "peak_source": env.peak_src},
+                    "gpu_launches": args.steps * (2 if w == "append" else 1), "cpu_baseline": None, **res}
+            print(json.dumps(line))
     kvdist.shutdown()
 
 

@@ -307,6 +307,10 @@ kv_status_t kv_decode_attention_noalloc(kv_pool_t* pool, int32_t layer, int32_t 
     return KV_ERR_INVALID_ARG;
   if ((int64_t)max_hist_len > (int64_t)max_pages_per_seq * p.cfg.page_size) return KV_ERR_INVALID_ARG;
   if ((uintptr_t)q & 1) return KV_ERR_INVALID_ARG;
+  // the scratch buffer looked up below is the current device's: it must be the pool's
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return KV_ERR_CUDA;
+  if (cur != p.device) return KV_ERR_INVALID_ARG;
   kvint2::DecodePlan pl = kvint2::plan_decode_int2(p, B, max_hist_len);
   void* scratch = nullptr;
   size_t scratch_bytes = 0;
@@ -316,6 +320,13 @@ kv_status_t kv_decode_attention_noalloc(kv_pool_t* pool, int32_t layer, int32_t 
                                                 recent_start, page_table, max_pages_per_seq, pl,
                                                 softmax_scale, out, scratch,
                                                 static_cast<cudaStream_t>(stream)));
+}
+
+kv_status_t kv_debug_stall_first_copy(kv_pool_t* pool, int32_t enable, int32_t max_polls) {
+  if (!pool || max_polls < 0) return KV_ERR_INVALID_ARG;
+  pool->p.test_stall_first_copy = enable ? 1 : 0;
+  pool->p.test_wait_polls = max_polls;
+  return KV_OK;
 }
 
 kv_status_t kv_append_bf16(kv_pool_t* pool, int32_t layer, int32_t n_seqs, const void* k,

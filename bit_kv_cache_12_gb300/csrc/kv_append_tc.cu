@@ -10,25 +10,28 @@
 // section 2.2 B (history is stored after the fixed rotation and the clip).
 //
 // GPU design: the rotation x' = x R of a chunk of 128 tokens of one KV head
-// and one tensor is one dense [128 x 128] . [128 x 256] product: R enters as
-// bf16 hi | lo halves side by side (N = 256), x is exact in bf16.  A CTA of
-// eight warps owns one (KV head, tensor) and walks over 128-token chunks:
-//   * x rows arrive by 16-byte cp.async straight into the 128-byte-swizzled
-//     K-major operand layout (the next chunk's rows while this chunk's
-//     epilogue runs); R^T hi | lo arrives once per CTA, pre-swizzled in global
-//     memory by the rotation set-up, as four bulk copies;
-//   * one thread issues eight tcgen05.mma (kind::f16, M 128, N 256, K 16)
-//     into a 256-column fp32 accumulator in tensor memory and commits them
-//     to an mbarrier;
+// and one tensor is x [128 x 128] . R_hi + x . R_lo, both terms accumulated
+// into one fp32 accumulator (R enters as bf16 hi and lo terms; x is exact in
+// bf16).  A CTA of eight warps owns one (KV head, tensor) and walks over
+// 128-token chunks:
+//   * x rows arrive by two TMA tile loads (128-byte swizzle, the K-major
+//     operand layout) when the whole chunk lies inside the input, else by
+//     16-byte cp.async with rows outside the append range zero-filled; the
+//     next chunk's rows come in while this chunk's epilogue runs.  R^T hi |
+//     lo arrives once per CTA, pre-swizzled in global memory by the rotation
+//     set-up, as four bulk copies;
+//   * one thread issues sixteen tcgen05.mma (kind::f16, M 128, N 128, K 16:
+//     per 16-channel step the hi term, then the lo term) into a 128-column
+//     fp32 accumulator in tensor memory and commits them to an mbarrier;
 //   * every thread then owns one token row and one half of the channels of
 //     the accumulator (tcgen05.ld; warps w and w + 4 share a lane quarter):
-//     x' = hi + lo, clip, per-group min / max (combined across the halves
-//     through shared memory for group 128), s and z, the codes (branch-free,
-//     with a rare exact fix-up); the codes are packed into the tile's storage
-//     order with warp shuffles (partners differ in lane bits 0 and 3) and
-//     written as 8-byte word pairs, merging with the bits of rows outside the
-//     append range where a tile is only partly written.
-// Two CTAs share an SM (256 tensor-memory columns and ~100 KB of shared
+//     clip, per-group min / max (combined across the halves through shared
+//     memory for group 128), s and z, the codes (branch-free, with a rare
+//     exact fix-up); the codes are packed into the tile's storage order with
+//     warp shuffles (partners differ in lane bits 0 and 3) and written as
+//     8-byte word pairs, merging with the bits of rows outside the append
+//     range where a tile is only partly written.
+// Two CTAs share an SM (128 tensor-memory columns and ~100 KB of shared
 // memory each), so one CTA's MMA overlaps the other's epilogue.
 // Every wait is bounded; a wait that runs out sets KV_DEVERR_TIMEOUT, waits
 // (bounded) for the work in flight, frees the tensor memory and returns.

@@ -89,9 +89,12 @@ struct DecodeArgs {
   const int32_t* seq_len;
   const int32_t* pt;
   int max_pages;
+  int max_len;              // host bound on hist_len (INT2) or seq_len (BF16): longer is an error
   int Hq, Hkv, page_size;
   long long num_pages;
   int n_split, per_split, n_tier;
+  int wait_polls;           // polls of a bounded mbarrier wait before it gives up
+  int stall_first_copy;     // test hook: the first tile copy of split 0 is never issued
   // T query positions per sequence: the kernel's G "heads" of a KV head are
   // (t, h) pairs, t = head / Gq, h = head % Gq (Gq = Hq / Hkv); q and out are
   // [B][T][Hq][128]; lse (optional) [B][T][Hq]
@@ -624,7 +627,8 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
   float* ssum = sm + S::ssum;
   load_q<G, NW, kMulti>(a, b, g, sq, S::HP);
   int h = __ldg(a.hist_len + b);
-  const int cap = a.max_pages * a.page_size;
+  // the grid covers max_len history tokens (and the page table max_pages pages)
+  const int cap = min(a.max_pages * a.page_size, a.max_len);
   if (h < 0 || h > cap) {
     if (threadIdx.x == 0) flag_error(a.err, KV_DEVERR_LENGTH);
     h = max(0, min(h, cap));
@@ -658,7 +662,11 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
 #pragma unroll
     for (int st = 0; st < kStages - 1; ++st) {   // tiles 0..2
       const int t = t_begin + warp + NW * st;
-      if (t < t_end) start_copy(t, pid_first[st], st);
+      if (t >= t_end) continue;
+      if (st == 0 && a.stall_first_copy && split == 0 && warp == 0)
+        mbar_expect_tx(wbar, TB);   // test hook: armed for a copy that is never issued
+      else
+        start_copy(t, pid_first[st], st);
     }
   }
   if (threadIdx.x == 0) {
@@ -751,7 +759,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
     // tile k+3 goes into the stage read in the previous iteration
     issue(t + NW * (kStages - 1), (k + kStages - 1) % kStages);
     const int st = k % kStages;
-    if (!__all_sync(0xffffffffu, mbar_wait(wbar + st, (k / kStages) & 1, kWaitPolls))) {
+    if (!__all_sync(0xffffffffu, mbar_wait(wbar + st, (k / kStages) & 1, a.wait_polls))) {
       ok = false;
       break;
     }
@@ -901,11 +909,13 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
     }
   }
   if (!ok) {   // a copy did not arrive in time: wait (bounded) for the ones in flight
+    // iteration k had already issued tile k + kStages - 1, so the copies that
+    // may be in flight are those of tiles k .. k + kStages - 1
     if (lane == 0) flag_error(a.err, KV_DEVERR_TIMEOUT);
-    for (int kk = k; kk < k + kStages - 1 && t_begin + warp + NW * kk < t_end; ++kk)
-      mbar_wait(wbar + kk % kStages, (kk / kStages) & 1, kWaitPolls);
+    for (int kk = k; kk < k + kStages && t_begin + warp + NW * kk < t_end; ++kk)
+      mbar_wait(wbar + kk % kStages, (kk / kStages) & 1, a.wait_polls);
   }
-  if (!mbar_wait(rbar, 0, kWaitPolls)) {
+  if (!mbar_wait(rbar, 0, a.wait_polls)) {
     ok = false;
     if (threadIdx.x == 0) flag_error(a.err, KV_DEVERR_TIMEOUT);
   }
@@ -1118,7 +1128,7 @@ __global__ void __launch_bounds__(kBf16Warps * 32, 2) decode_bf16_kernel(DecodeA
   const int nparts = a.n_split;
   float* part = a.ws + ((size_t)(b * a.Hkv + g) * nparts + split) * G * kPart;
   int n = a.seq_len[b];
-  const int cap = a.max_pages * a.page_size;
+  const int cap = min(a.max_pages * a.page_size, a.max_len);
   if (n < 0 || n > cap) {
     if (threadIdx.x == 0) flag_error(a.err, KV_DEVERR_LENGTH);
     n = max(0, min(n, cap));
@@ -1234,6 +1244,8 @@ DecodeArgs base_args(const Pool& p, int layer, const void* q, const int32_t* pt,
   a.T = 1;
   a.Gq = p.G;
   a.lse = nullptr;
+  a.wait_polls = p.test_wait_polls > 0 ? p.test_wait_polls : kWaitPolls;
+  a.stall_first_copy = p.test_stall_first_copy;
   return a;
 }
 
@@ -1323,6 +1335,7 @@ static DecodePlan make_plan(const Pool& p, int G, int B, int units, int max_per,
   pl.n_split = ns;
   pl.n_tier = n_extra;
   pl.tiles_per_split = per;
+  pl.max_len = 0;
   pl.partial_floats = (size_t)pairs * (ns + n_extra) * G * kPart;
   pl.bytes = pl.partial_floats * sizeof(float);
   return pl;
@@ -1333,11 +1346,15 @@ DecodePlan plan_decode_int2(const Pool& p, int B, int max_hist_len, int T) {
   const int tiles = (max(max_hist_len, 0) + kTile - 1) / kTile;
   const int n_tier = max(1, (p.cfg.sink_tokens + p.cfg.recent_tokens + kTierRows - 1) / kTierRows);
   const int per_sm = (T > 1) ? int2_occupancy_t<true>(p, G) : int2_occupancy_t<false>(p, G);
-  return make_plan(p, G, B, tiles, 64 * int2_warps(G), n_tier, per_sm);
+  DecodePlan pl = make_plan(p, G, B, tiles, 64 * int2_warps(G), n_tier, per_sm);
+  pl.max_len = max(max_hist_len, 0);
+  return pl;
 }
 
 DecodePlan plan_decode_bf16(const Pool& p, int B, int max_len) {
-  return make_plan(p, p.G, B, max(max_len, 0), 8192, 0, bf16_occupancy(p));
+  DecodePlan pl = make_plan(p, p.G, B, max(max_len, 0), 8192, 0, bf16_occupancy(p));
+  pl.max_len = max(max_len, 0);
+  return pl;
 }
 
 cudaError_t launch_decode_int2(const Pool& p, int layer, int B, const void* q,
@@ -1369,6 +1386,7 @@ cudaError_t launch_decode_int2(const Pool& p, int layer, int B, const void* q,
   a.n_split = plan.n_split;
   a.per_split = plan.tiles_per_split;
   a.n_tier = plan.n_tier;
+  a.max_len = plan.max_len;
   const bool g64 = p.cfg.group_size == 64;
   if (T > 1 || lse) {   // several queries per sequence, or the log-sum-exp wanted
     switch (T * p.G) {
@@ -1399,6 +1417,7 @@ cudaError_t launch_decode_bf16(const Pool& p, int layer, int B, const void* q,
   a.n_split = plan.n_split;
   a.per_split = plan.tiles_per_split;
   a.n_tier = 0;
+  a.max_len = plan.max_len;
   switch (p.G) {
     case 1: return launch_bf16_t<1>(a, B, s);
     case 2: return launch_bf16_t<2>(a, B, s);

@@ -41,6 +41,10 @@ struct Pool {
   unsigned* tickets = nullptr;      // [layer][max_seqs][Hkv] split-merge counters
   unsigned* step_tickets = nullptr; // [layer][ceil(max_seqs / 128)] per-step placement counters
   int* err = nullptr;               // device error word
+
+  // test hooks (kv_debug_stall_first_copy): 0 in normal use
+  int test_stall_first_copy = 0;    // decode: the first tile copy of split 0 is never issued
+  int test_wait_polls = 0;          // decode: polls of a bounded wait (0 = the default)
 };
 
 // Rotation operands per (layer, KV head), 4096 uint4 (64 KB) each:
@@ -78,6 +82,7 @@ struct DecodePlan {
   int n_split = 1;          // history splits per (sequence, KV head)
   int n_tier = 0;           // CTAs for the BF16 sink + recent tiers (INT2 pool)
   int tiles_per_split = 1;  // INT2: 16-token tiles; BF16: tokens
+  int max_len = 0;          // history (INT2) or sequence (BF16) tokens the grid covers
   size_t partial_floats = 0;
   size_t bytes = 0;
 };

@@ -71,6 +71,7 @@ _SIG = {
                                    ctypes.c_float, _P, _P, ctypes.c_size_t, _P]),
     "kv_decode_attention_noalloc": (_I32, [_P, _I32, _I32, _P, _P, _P, _P, _P, _P, _I32, _I32,
                                            ctypes.c_float, _P, _P]),
+    "kv_debug_stall_first_copy": (_I32, [_P, _I32, _I32]),
     "kv_append_bf16": (_I32, [_P, _I32, _I32, _P, _P, _P, _P, _P, _I32, _I32, _P]),
     "kv_decode_attention_bf16": (_I32, [_P, _I32, _I32, _P, _P, _P, _I32, _I32,
                                         ctypes.c_float, _P, _P, ctypes.c_size_t, _P]),
@@ -214,6 +215,12 @@ def kv_decode_attention_noalloc(pool, layer, B, q, sink_len, hist_len, recent_le
         pool, layer, B, _ptr(q), _ptr(sink_len), _ptr(hist_len), _ptr(recent_len),
         _ptr(recent_start), _ptr(page_table), max_pages_per_seq, max_hist_len,
         float(softmax_scale), _ptr(out), _stream(stream)))
+
+
+def kv_debug_stall_first_copy(pool, enable, max_polls=0):
+    """Test hook: later decodes of this pool make one bounded wait run out."""
+    _check("kv_debug_stall_first_copy", lib().kv_debug_stall_first_copy(pool, int(enable),
+                                                                         int(max_polls)))
 
 
 def kv_append_bf16(pool, layer, n_seqs, k, v, cu_tokens, start_pos, page_table,

@@ -71,7 +71,13 @@ enum {
   KV_DEVERR_LENGTH = 2,       /* a length above the tier / table capacity    */
   KV_DEVERR_SEQ_RANGE = 3,    /* cu_tokens not monotone or history overflow  */
   KV_DEVERR_TIMEOUT = 4       /* a bounded wait for an asynchronous copy ran
-                                 out; the work that needed it was skipped      */
+                                 out; the work that needed it was skipped.
+                                 The outputs of that call are wrong: discard
+                                 them.  A copy that did not arrive within about
+                                 a second points to a device problem, and the
+                                 library cannot rule out that it lands later;
+                                 do not keep using the pool (or the context)
+                                 after this code except to tear it down. */
 };
 
 typedef enum { KV_POOL_INT2_3TIER = 0, KV_POOL_BF16 = 1 } kv_pool_kind_t;
@@ -265,7 +271,9 @@ size_t kv_decode_workspace_bytes(const kv_pool_t* pool, int32_t B, int32_t max_l
  * R_v^T, and merge everything into fp32 outputs.
  *   q            device bf16 [B][Hq][128]; sequence b uses pool slot b
  *   sink_len     device int32 [B] (<= sink_tokens)
- *   hist_len     device int32 [B] (<= max_hist_len and the page table's span)
+ *   hist_len     device int32 [B] (<= max_hist_len and the page table's span;
+ *                a longer history sets KV_DEVERR_LENGTH and only its first
+ *                min(max_hist_len, span) tokens are attended)
  *   recent_len   device int32 [B] (<= recent_tokens)
  *   recent_start device int32 [B]: ring index of the oldest recent token
  *   page_table   device int32 [B][max_pages_per_seq] (history pages)
@@ -289,7 +297,9 @@ kv_status_t kv_append_bf16(kv_pool_t* pool, int32_t layer, int32_t n_seqs, const
                            int32_t max_tokens_per_seq, void* stream);
 
 /* Decode attention over an all-BF16 paged pool: plain split-K softmax
- * attention of q [B][Hq][128] over seq_len[b] tokens, fp32 out [B][Hq][128]. */
+ * attention of q [B][Hq][128] over seq_len[b] tokens, fp32 out [B][Hq][128].
+ * seq_len[b] above max_seq_len (or the page table's span) sets
+ * KV_DEVERR_LENGTH and only the covered tokens are attended. */
 kv_status_t kv_decode_attention_bf16(kv_pool_t* pool, int32_t layer, int32_t B, const void* q,
                                      const int32_t* seq_len, const int32_t* page_table,
                                      int32_t max_pages_per_seq, int32_t max_seq_len,
@@ -323,13 +333,27 @@ kv_status_t kv_decode_attention_bf16(kv_pool_t* pool, int32_t layer, int32_t B, 
  *     contents in it; nothing in it has to start at zero (each call writes
  *     every partial it later reads).  Calls that overlap on the GPU (other
  *     streams, other threads, other pools) race on the buffer: order them.
- * Results equal kv_decode_attention's for the same inputs. */
+ *   - The current device must be the pool's (the buffer looked up is the
+ *     current device's); otherwise KV_ERR_INVALID_ARG, nothing launched.
+ * Results equal kv_decode_attention's for the same inputs, bit for bit (same
+ * kernel, same split plan, same merge order). */
 kv_status_t kv_decode_attention_noalloc(kv_pool_t* pool, int32_t layer, int32_t B, const void* q,
                                         const int32_t* sink_len, const int32_t* hist_len,
                                         const int32_t* recent_len, const int32_t* recent_start,
                                         const int32_t* page_table, int32_t max_pages_per_seq,
                                         int32_t max_hist_len, float softmax_scale, float* out,
                                         void* stream);
+
+/* Test hook for the bounded waits (no counterpart on the pages).  With
+ * enable != 0, later decode calls of this pool arm the first ring stage of
+ * the first history split for a tile copy that is never issued, so that the
+ * warp's bounded wait runs out: the call sets KV_DEVERR_TIMEOUT, waits
+ * (bounded) for the copies it did issue, skips that split and returns.  No
+ * copy is left in flight, nothing faults and nothing hangs.  max_polls > 0
+ * replaces the default poll limit of those waits (about a second) for the
+ * pool's decode calls; 0 restores it.  enable = 0 restores normal decodes.
+ * Not for production use. */
+kv_status_t kv_debug_stall_first_copy(kv_pool_t* pool, int32_t enable, int32_t max_polls);
 
 #ifdef __cplusplus
 }

@@ -154,3 +154,71 @@ def gpu_decode_bf16(pool, wl, pt, lens, q=None):
                                     ws_bytes)
     torch.cuda.synchronize()
     return out.cpu().numpy()
+
+
+# ---------------------------------------------------------------------------
+# device-resident workloads (bit_kv_cache_12_gb300.workloads): pool fill,
+# one decode in the benchmark's launch configuration, oracle on sampled heads
+# ---------------------------------------------------------------------------
+
+def fill_pool_from_case(c):
+    """An INT2 pool holding case c: tiers copied in, history through the
+    library's own kv_append_quantize (as the benchmark fills it)."""
+    pool = native.KVPool(native.KV_POOL_INT2_3TIER, 1, c.Hq, c.Hkv, c.P, c.num_pages, c.B,
+                         group_size=c.GS)
+    keep = (f32_dev(c.Rk), f32_dev(c.Rv), f32_dev(c.clip_k), f32_dev(c.clip_v))
+    native.kv_pool_set_rotation(pool.handle, 0, *keep)
+    pool._keep = keep
+    sk, sv, rk, rv = pool.tier_views(0)
+    sk[:c.B].copy_(c.sink_k); sv[:c.B].copy_(c.sink_v)
+    rk[:c.B].copy_(c.rec_k); rv[:c.B].copy_(c.rec_v)
+    cu = np.zeros(c.B + 1, np.int32); cu[1:] = np.cumsum(c.hist_len)
+    native.kv_append_quantize(pool.handle, 0, c.B, c.hist_k, c.hist_v, i32_dev(cu),
+                              i32_dev(np.zeros(c.B)), i32_dev(c.page_table), c.page_table.shape[1],
+                              int(max(1, c.hist_len.max())))
+    torch.cuda.synchronize()
+    return pool
+
+
+def decode_case(pool, c, hist_len=None, max_hist=None):
+    """One kv_decode_attention over the whole batch of case c (the benchmark's call)."""
+    hist_len = c.hist_len if hist_len is None else hist_len
+    mh = int(c.hist_len.max()) if max_hist is None else max_hist
+    ws_bytes = native.kv_decode_workspace_bytes(pool.handle, c.B, mh)
+    ws = torch.empty(max(ws_bytes, 16) // 4 + 4, dtype=torch.float32, device="cuda")
+    out = torch.full((c.B, c.Hq, 128), float("nan"), dtype=torch.float32, device="cuda")
+    native.kv_decode_attention(pool.handle, 0, c.B, c.q, i32_dev(c.sink_len), i32_dev(hist_len),
+                               i32_dev(c.rec_len), i32_dev(c.rec_start), i32_dev(c.page_table),
+                               c.page_table.shape[1], mh, c.scale, out, ws, ws_bytes)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def oracle_kv_head(pool, c, b, g, hist_len=None):
+    """Oracle outputs [G, 128] of every query head of KV head g of sequence b,
+    from the codes the pool stores (only that sequence's pages are copied)."""
+    h = int(c.hist_len[b] if hist_len is None else hist_len)
+    npages = (h + c.P - 1) // c.P
+    G = c.Hq // c.Hkv
+    if npages:
+        ids = torch.as_tensor(c.page_table[b, :npages].astype(np.int64), device="cuda")
+        pages = pool.hist_view(0).index_select(0, ids).cpu().numpy()
+        kc, vc, sk, zk, sv, zv = kq.read_history(pages, np.arange(npages), h, g, c.P, c.GS)
+    else:
+        kc = vc = np.zeros((0, 128), np.uint8)
+        sk = zk = sv = zv = np.zeros((0, 128 // c.GS), np.float16)
+    kd = kq.dequant(kc, sk, zk, c.GS)
+    vd = kq.dequant(vc, sv, zv, c.GS)
+    s, r = int(c.sink_len[b]), int(c.rec_len[b])
+    sink_k = kq.bf16_bits_to_f64(_bits(c.sink_k[b, g, :s]))
+    sink_v = kq.bf16_bits_to_f64(_bits(c.sink_v[b, g, :s]))
+    cap = c.rec_k.shape[2]
+    rec_k = kq.bf16_bits_to_f64(att.ring_order(_bits(c.rec_k[b, g]), int(c.rec_start[b]), r, cap))
+    rec_v = kq.bf16_bits_to_f64(att.ring_order(_bits(c.rec_v[b, g]), int(c.rec_start[b]), r, cap))
+    Rk = np.asarray(c.Rk[g], np.float64); Rv = np.asarray(c.Rv[g], np.float64)
+    return np.stack([att.three_tier_head(kq.bf16_bits_to_f64(c.q_np[b, g * G + hh]), Rk, Rv, sink_k,
+                                         sink_v, kd, vd, rec_k, rec_v, c.scale) for hh in range(G)])

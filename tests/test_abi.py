@@ -61,3 +61,9 @@ def test_invalid_arguments_rejected_without_gpu(built_lib):
     assert L.kv_decode_workspace_bytes(None, 1, 100) == 0
     assert L.kv_append_step(None, 0, 1, None, None, None, None, None, None, None, 1,
                             None) == native.KV_ERR_INVALID_ARG
+
+
+def test_binding_has_a_wrapper_for_every_entry():
+    from bit_kv_cache_12_gb300 import native
+    for name in native._SIG:
+        assert callable(getattr(native, name, None)), name

@@ -372,3 +372,44 @@ def test_end_to_end_append_then_decode():
     ma, rl = gu.metrics(out, ref)
     print(f"e2e: max_abs {ma:.3e} rel_l2 {rl:.3e}")
     assert ma <= MAX_ABS and rl <= 1e-2
+
+
+# ---------------------------------------------------------------------------
+# lengths beyond what the call covers
+# ---------------------------------------------------------------------------
+
+def test_decode_history_beyond_max_hist_len_is_flagged():
+    """hist_len[b] above max_hist_len: KV_DEVERR_LENGTH, and the sequence's
+    first max_hist_len history tokens (the ones the grid covers) are attended;
+    the other sequence is unaffected."""
+    wl = synth.make_decode_workload("overlen", 16, B=2, Hq=8, Hkv=2, ctx=[1100, 700], page_size=16)
+    assert list(wl.hist_len) == [780, 380]
+    pages = gu.oracle_pages(wl)
+    pool = gu.make_int2_pool(wl)
+    gu.upload_pages(pool, pages)
+    out = gu.gpu_decode(pool, wl, max_hist=500)
+    assert pool.error() == 2                                   # KV_DEVERR_LENGTH
+    assert np.all(np.isfinite(out))
+    ref = gu.oracle_decode(wl, pages, hist_len=np.array([500, 380]))
+    ma, rl = gu.metrics(out, ref)
+    assert ma <= MAX_ABS and rl <= REL_L2, (ma, rl)
+    pool.close()
+
+
+def test_decode_bf16_length_beyond_max_seq_len_is_flagged():
+    wl = synth.make_decode_workload("overlen_bf", 17, B=2, Hq=8, Hkv=2, ctx=[900, 400], page_size=16)
+    bpool, pt, lens = gu.make_bf16_pool(wl)
+    ws_bytes = native.kv_decode_workspace_bytes(bpool.handle, wl.B, 600)
+    ws = torch.empty(ws_bytes // 4 + 4, dtype=torch.float32, device="cuda")
+    out = torch.full((wl.B, wl.Hq, 128), float("nan"), dtype=torch.float32, device="cuda")
+    native.kv_decode_attention_bf16(bpool.handle, 0, wl.B, gu.bf16_dev(wl.q), gu.i32_dev(lens),
+                                    gu.i32_dev(pt), pt.shape[1], 600, wl.scale, out, ws, ws_bytes)
+    torch.cuda.synchronize()
+    assert bpool.error() == 2                                  # KV_DEVERR_LENGTH
+    kp, vp = bpool.bf16_views(0)
+    kb = kp.view(torch.int16).cpu().numpy().view(np.uint16)
+    vb = vp.view(torch.int16).cpu().numpy().view(np.uint16)
+    bpool.close()
+    ref = att.decode_bf16_paged(wl.q, kb, vb, pt, np.minimum(lens, 600), wl.Hkv, 16, wl.scale)
+    ma, rl = gu.metrics(out.cpu().numpy(), ref)
+    assert ma <= 1e-4 and rl <= 1e-5, (ma, rl)

@@ -213,3 +213,100 @@ def test_multi_query_is_independent_single_queries():
                                     wl.hist_len, wl.rec_k, wl.rec_v, wl.rec_len, wl.rec_start, wl.Hkv,
                                     wl.group_size, wl.scale)
         assert np.array_equal(out[:, t], one)
+
+
+# ---------------------------------------------------------------------------
+# the batch wrapper (decode_three_tier): GQA mapping, per-sequence lengths and
+# ring starts, checked per (sequence, query head) against formulations that
+# share none of its indexing
+# ---------------------------------------------------------------------------
+
+def _ragged_workload(seed, ctx, sink=8, recent=16):
+    return synth.make_decode_workload(f"ragged{seed}", seed, B=len(ctx), Hq=8, Hkv=2, ctx=ctx,
+                                      page_size=16, group_size=64, sink=sink, recent=recent,
+                                      outliers_per_head=2)
+
+
+def _oracle_pages(wl):
+    pages = np.zeros((wl.num_pages, wl.Hkv, kq.tile_bytes(wl.group_size)), np.uint8)
+    for b in range(wl.B):
+        if wl.hist_len[b]:
+            kq.pack_history_full(wl.hist_k[b], wl.hist_v[b], wl.Rk, wl.Rv, wl.clip_k, wl.clip_v,
+                                 wl.page_table[b], wl.num_pages, wl.Hkv, wl.page_size, wl.group_size,
+                                 pages)
+    return pages
+
+
+def test_batch_wrapper_each_head_equals_hand_assembled_brute_force():
+    """Ragged batch (history 0, a partial tile, several tiles; short sink and
+    partly filled rings starting mid-ring): output (b, h) equals the long-double
+    brute force of KV head h // G of sequence b, its tokens gathered here with
+    explicit loops (ring slot (start + t) mod capacity)."""
+    wl = _ragged_workload(41, [5, 30, 61, 19])
+    assert list(wl.hist_len) == [0, 6, 37, 0] and list(wl.rec_len) == [0, 16, 16, 11]
+    pages = _oracle_pages(wl)
+    hist = lambda b, g: kq.read_history(pages, wl.page_table[b], int(wl.hist_len[b]), g,
+                                        wl.page_size, wl.group_size)
+    out = att.decode_three_tier(wl.q, wl.Rk, wl.Rv, wl.sink_k, wl.sink_v, wl.sink_len, hist,
+                                wl.hist_len, wl.rec_k, wl.rec_v, wl.rec_len, wl.rec_start, wl.Hkv,
+                                wl.group_size, wl.scale)
+    G = wl.Hq // wl.Hkv
+    cap = wl.rec_k.shape[2]
+    for b in range(wl.B):
+        for h in range(wl.Hq):
+            g = h // G
+            sk = kq.bf16_bits_to_f64(wl.sink_k[b, g, :wl.sink_len[b]])
+            sv = kq.bf16_bits_to_f64(wl.sink_v[b, g, :wl.sink_len[b]])
+            slots = [(int(wl.rec_start[b]) + t) % cap for t in range(int(wl.rec_len[b]))]
+            rk = kq.bf16_bits_to_f64(np.array([wl.rec_k[b, g, s] for s in slots]).reshape(-1, 128))
+            rv = kq.bf16_bits_to_f64(np.array([wl.rec_v[b, g, s] for s in slots]).reshape(-1, 128))
+            kc, vc, skk, zk, svv, zv = kq.read_history(pages, wl.page_table[b], int(wl.hist_len[b]), g,
+                                                        wl.page_size, wl.group_size)
+            kd = kq.dequant(kc, skk, zk, wl.group_size)
+            vd = kq.dequant(vc, svv, zv, wl.group_size)
+            want = _brute_force_longdouble(kq.bf16_bits_to_f64(wl.q[b, h]), wl.Rk[g].astype(np.float64),
+                                           wl.Rv[g].astype(np.float64), sk, sv, kd, vd, rk, rv, wl.scale)
+            assert np.abs(out[b, h] - want).max() <= 1e-12 * max(1.0, np.abs(want).max()), (b, h)
+
+
+def test_batch_wrapper_without_history_equals_bf16_paged():
+    """History 0 for every sequence: the three-tier wrapper equals the all-BF16
+    paged decode of the same tokens (sink, then the ring from its start) placed
+    in shuffled pages, and each head equals plain attention over the tokens of
+    KV head h // G."""
+    wl = _ragged_workload(42, [3, 8, 20, 24])
+    assert int(wl.hist_len.max()) == 0
+    rng = np.random.default_rng(42)
+    P, cap = 16, wl.rec_k.shape[2]
+    lens = (wl.sink_len + wl.rec_len).astype(int)
+    npg = (lens + P - 1) // P
+    perm = rng.permutation(int(npg.sum()) + 2)
+    kp = np.zeros((len(perm), wl.Hkv, P, 128), np.uint16); vp = kp.copy()
+    pt = np.full((wl.B, int(npg.max())), -1, np.int32)
+    o = 0
+    toks = []
+    for b in range(wl.B):
+        pt[b, :npg[b]] = perm[o:o + npg[b]]; o += npg[b]
+        order = [wl.sink_k[b, :, t] for t in range(wl.sink_len[b])]
+        vorder = [wl.sink_v[b, :, t] for t in range(wl.sink_len[b])]
+        for t in range(int(wl.rec_len[b])):
+            s = (int(wl.rec_start[b]) + t) % cap
+            order.append(wl.rec_k[b, :, s]); vorder.append(wl.rec_v[b, :, s])
+        K = np.array(order).reshape(-1, wl.Hkv, 128); V = np.array(vorder).reshape(-1, wl.Hkv, 128)
+        for t in range(lens[b]):
+            kp[pt[b, t // P], :, t % P] = K[t]; vp[pt[b, t // P], :, t % P] = V[t]
+        toks.append((K, V))
+    empty = lambda b, g: kq.read_history(np.zeros((1, wl.Hkv, kq.tile_bytes(64)), np.uint8),
+                                         np.zeros(1, np.int32), 0, g, P, 64)
+    got = att.decode_three_tier(wl.q, wl.Rk, wl.Rv, wl.sink_k, wl.sink_v, wl.sink_len, empty,
+                                wl.hist_len, wl.rec_k, wl.rec_v, wl.rec_len, wl.rec_start, wl.Hkv,
+                                64, wl.scale)
+    ref = att.decode_bf16_paged(wl.q, kp, vp, pt, lens, wl.Hkv, P, wl.scale)
+    assert np.abs(got - ref).max() <= 1e-13
+    G = wl.Hq // wl.Hkv
+    for b in range(wl.B):
+        K, V = toks[b]
+        for h in range(wl.Hq):
+            want = plain_attention(kq.bf16_bits_to_f64(wl.q[b, h]), kq.bf16_bits_to_f64(K[:, h // G]),
+                                   kq.bf16_bits_to_f64(V[:, h // G]), wl.scale)
+            assert np.abs(got[b, h] - want).max() <= 1e-12, (b, h)
