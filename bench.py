@@ -23,11 +23,19 @@ quantized and packed into history) followed by the decode, at batch 1 (the
 headline workload) and at batch 64.  ``--workload`` runs one of them alone.
 
 One step = one ``kv_decode_attention`` call (whole batch, one layer), or one
-``kv_append_quantize`` call for ``append``.  Every timed step is preceded by
-an L2 flush outside the timed events: a 256 MiB device write, then a 256 MiB
-read so the dirty lines are written back before the step starts.  Timing:
-CUDA events on the launching stream around each step, device synchronised
-before and after, max over ranks (one replica of the workload per GPU).
+``kv_append_quantize`` call for ``append``.  No step finds its data in L2:
+  * the headline workload (60 MB) lives in a pool of 8 layers and step i
+    decodes layer i mod 8, as a server decodes the layers of one token in
+    turn: every step reads its own 60 MB of history, tiers and rotations from
+    HBM, while the kernel's code and the page table (shared by the layers, as
+    in a paged server) stay warm; the same decode after an L2 flush (256 MiB
+    write + 256 MiB read outside the timed events) is reported beside it;
+  * batch64, long16, append and the BF16 comparison pools are each larger
+    than L2 (0.4 to 8.6 GB), so consecutive steps run back to back;
+  * tiny (0.7 MB) is flushed before every step.
+Timing: CUDA events on the launching stream around each step, device
+synchronised before and after, max over ranks (one replica of the workload
+per GPU).
 
 ``--impl reference`` times the CPU oracle on the headline workload instead:
 W untimed and K timed whole decode steps on the host cores.
@@ -49,7 +57,11 @@ sys.path.insert(0, ROOT)
 
 METRIC = "INT2 paged decode-attention us/step (HBM GB/s, % of roofline) vs BF16 path"
 APPEND_METRIC = "INT2 append (rotate, clip, quantize, pack) us/call (HBM GB/s, % of roofline)"
-L2_NOTE = "flushed between steps (256 MiB write + 256 MiB read outside the timed events)"
+L2_FLUSH = "flushed between steps (256 MiB write + 256 MiB read outside the timed events)"
+L2_LARGER = "inputs larger than L2: consecutive steps read disjoint data (no flush)"
+L2_LAYERS = ("inputs larger than L2: the pool holds {n} layers of the workload ({mb:.0f} MB of history) "
+             "and step i decodes layer i mod {n} (no flush; the page table is shared by all layers)")
+HEADLINE_LAYERS = 8
 WORKLOADS = ["all", "qwen3_4b", "tiny", "batch64", "long16", "append"]
 
 
@@ -287,10 +299,12 @@ def run_reference(args, rank, world):
 
 
 def headline_config(wl):
+    hist_mb = HEADLINE_LAYERS * int(np.sum(wl.hist_len)) * wl.Hkv * (64 + 8 * 128 // wl.group_size) / 1e6
     return {"workload": wl.name, "batch": wl.B, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": 128,
             "context": int(wl.meta["ctx"][0]), "sink": int(wl.sink_len[0]),
             "int2_history": int(wl.hist_len[0]), "recent": int(wl.rec_len[0]),
-            "page_size": wl.page_size, "group_size": wl.group_size, "l2": L2_NOTE}
+            "page_size": wl.page_size, "group_size": wl.group_size,
+            "l2": L2_LAYERS.format(n=HEADLINE_LAYERS, mb=hist_mb), "layers_in_pool": HEADLINE_LAYERS}
 
 
 # --------------------------------------------------------------------------
@@ -308,16 +322,20 @@ def make_timer(torch, dev, stream, kvdist):
         flush_w.zero_()
         flush_r.sum()
 
-    def timed(fn, steps, warmup):
-        for _ in range(warmup):
-            flush(); fn()
+    def timed(fn, steps, warmup, flush_l2=False):
+        """fn(i) is step i; warm-up steps are -warmup .. -1."""
+        for i in range(-warmup, 0):
+            if flush_l2:
+                flush()
+            fn(i)
         torch.cuda.synchronize()
         kvdist.barrier()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(steps)]
-        for s0, s1 in ev:
-            flush()
-            s0.record(stream); fn(); s1.record(stream)
+        for i, (s0, s1) in enumerate(ev):
+            if flush_l2:
+                flush()
+            s0.record(stream); fn(i); s1.record(stream)
         torch.cuda.synchronize()
         kvdist.barrier()
         return np.array([s0.elapsed_time(s1) for s0, s1 in ev])   # ms
@@ -358,13 +376,14 @@ class Env:
 # --------------------------------------------------------------------------
 
 class DecodeRig:
-    """An INT2 pool filled with case c (the library's append), the decode step
-    over it, and the BF16 pool of the same tokens with its decode step.  With
-    ``spare_steps`` > 0 every sequence gets that many spare history positions
-    (page ids past the case's pages, in the extended table ``pt_ext``) for
-    per-step placement; the decode itself uses the case's own page table."""
+    """An INT2 pool holding case c in each of ``layers`` layers (the library's
+    append), the decode step over a layer, and the BF16 pool of the same tokens
+    with its decode step.  With ``spare_steps`` > 0 every sequence gets that
+    many spare history positions (page ids past the case's pages, in the
+    extended table ``pt_ext``) for per-step placement; the decode itself uses
+    the case's own page table."""
 
-    def __init__(self, env, c, spare_steps=0):
+    def __init__(self, env, c, spare_steps=0, layers=1):
         from bit_kv_cache_12_gb300 import native
         torch, dev, i32 = env.torch, env.dev, env.i32
         self.env, self.c, self.native = env, c, native
@@ -379,20 +398,23 @@ class DecodeRig:
                 pt_np[b, :n] = c.page_table[b, :n]
                 pt_np[b, n:n + spare_pages] = c.num_pages + b * spare_pages + np.arange(spare_pages)
         self.pt_np, self.pt_ext_np = c.page_table, pt_np
-        self.pool = native.KVPool(native.KV_POOL_INT2_3TIER, 1, Hq, Hkv, c.P,
+        self.layers = layers
+        self.small = False                    # set for workloads that fit in L2
+        self.pool = native.KVPool(native.KV_POOL_INT2_3TIER, layers, Hq, Hkv, c.P,
                                   c.num_pages + B * spare_pages, B, group_size=c.GS)
         self.Rk = torch.as_tensor(c.Rk).to(dev); self.Rv = torch.as_tensor(c.Rv).to(dev)
         self.ck = torch.as_tensor(c.clip_k).to(dev); self.cv = torch.as_tensor(c.clip_v).to(dev)
-        native.kv_pool_set_rotation(self.pool.handle, 0, self.Rk, self.Rv, self.ck, self.cv)
-        sk, sv, rk, rv = self.pool.tier_views(0)
-        sk[:B].copy_(c.sink_k); sv[:B].copy_(c.sink_v)
-        rk[:B].copy_(c.rec_k); rv[:B].copy_(c.rec_v)
         cu = np.zeros(B + 1, np.int32); cu[1:] = np.cumsum(c.hist_len)
         self.cu = cu
         self.pt = i32(c.page_table)
         self.pt_ext = i32(pt_np)
-        native.kv_append_quantize(self.pool.handle, 0, B, c.hist_k, c.hist_v, i32(cu), i32(np.zeros(B)),
-                                  self.pt, c.page_table.shape[1], int(max(1, c.hist_len.max())))
+        for l in range(layers):
+            native.kv_pool_set_rotation(self.pool.handle, l, self.Rk, self.Rv, self.ck, self.cv)
+            sk, sv, rk, rv = self.pool.tier_views(l)
+            sk[:B].copy_(c.sink_k); sv[:B].copy_(c.sink_v)
+            rk[:B].copy_(c.rec_k); rv[:B].copy_(c.rec_v)
+            native.kv_append_quantize(self.pool.handle, l, B, c.hist_k, c.hist_v, i32(cu), i32(np.zeros(B)),
+                                      self.pt, c.page_table.shape[1], int(max(1, c.hist_len.max())))
         torch.cuda.synchronize()
         if self.pool.error():
             raise RuntimeError("device error while filling the pool")
@@ -403,10 +425,11 @@ class DecodeRig:
         self.out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
         self.bpool = None
 
-    def decode(self, q=None, lens=None, out=None, max_hist=None, extended=False):
+    def decode(self, i=0, q=None, lens=None, out=None, max_hist=None, extended=False):
+        """The decode of step i: layer i mod layers."""
         c, n = self.c, self.native
         pt, pt_np = (self.pt_ext, self.pt_ext_np) if extended else (self.pt, self.pt_np)
-        n.kv_decode_attention(self.pool.handle, 0, c.B, c.q if q is None else q,
+        n.kv_decode_attention(self.pool.handle, i % self.layers, c.B, c.q if q is None else q,
                               *(self.lens if lens is None else lens), pt, pt_np.shape[1],
                               self.max_hist if max_hist is None else max_hist, c.scale,
                               self.out if out is None else out, self.ws, self.ws_bytes, self.env.stream)
@@ -444,7 +467,7 @@ class DecodeRig:
         self.bws = torch.zeros(self.bws_bytes // 4 + 4, dtype=torch.float32, device=dev)
         self.bout = torch.empty_like(self.out)
 
-    def decode_bf16(self):
+    def decode_bf16(self, i=0):
         c = self.c
         self.native.kv_decode_attention_bf16(self.bpool.handle, 0, c.B, c.q, self.blens, self.bpt,
                                              self.bpt_np.shape[1], self.bmax, c.scale, self.bout,
@@ -460,10 +483,12 @@ class DecodeRig:
         self.pool = self.bpool = None
 
 
-def decode_summary(env, rig, steps, warmup, with_bf16=True):
-    """INT2 and BF16 decode of a rig: times, algorithmic bytes, GB/s, roofline."""
+def decode_summary(env, rig, steps, warmup, with_bf16=True, flush_l2=False):
+    """INT2 and BF16 decode of a rig: times, algorithmic bytes, GB/s, roofline.
+    The INT2 steps are flushed only with flush_l2; the BF16 pools are larger
+    than L2 except for the tiny workload, which is flushed too."""
     c = rig.c
-    t = env.timed(rig.decode, steps, max(3, warmup))
+    t = env.timed(rig.decode, steps, max(3, warmup), flush_l2=flush_l2)
     res = us_stats(t)
     res["us"] = env.max_ranks([res["us"]])[0]
     alg, parts = algorithmic_bytes(c)
@@ -472,7 +497,7 @@ def decode_summary(env, rig, steps, warmup, with_bf16=True):
                 "frac_of_8tbs": gbs / 8000.0})
     if with_bf16:
         rig.build_bf16()
-        tb = env.timed(rig.decode_bf16, max(5, steps // 2), 3)
+        tb = env.timed(rig.decode_bf16, max(5, steps // 2), 3, flush_l2=flush_l2)
         us_b = env.max_ranks([float(np.mean(tb) * 1e3)])[0]
         bb = bf16_bytes(c)
         res["bf16_path"] = {"us": us_b, "bytes": bb, "gbs": bb / (us_b * 1e-6) / 1e9,
@@ -492,21 +517,22 @@ def online_step(env, rig, steps, warmup, decode_us):
     gen = torch.Generator(device=env.dev)
     gen.manual_seed(11)
     new = torch.randn(2, c.B, c.Hkv, 128, generator=gen, device=env.dev).to(torch.bfloat16)
-    lens = [env.i32(c.sink_len), env.i32(c.hist_len), env.i32(c.rec_len), env.i32(c.rec_start)]
+    L = rig.layers
+    lens = [[env.i32(c.sink_len), env.i32(c.hist_len), env.i32(c.rec_len), env.i32(c.rec_start)]
+            for _ in range(L)]                    # each layer's own lengths
     total = max(3, warmup) + steps
     max_hist = rig.max_hist + total
 
-    def place():
-        n.kv_append_step(rig.pool.handle, 0, c.B, new[0], new[1], *lens, rig.pt_ext,
+    def step(i):                                  # step i places into and decodes layer i mod L
+        l = i % L
+        n.kv_append_step(rig.pool.handle, l, c.B, new[0], new[1], *lens[l], rig.pt_ext,
                          rig.pt_ext_np.shape[1], env.stream)
-
-    def step():
-        place()
-        rig.decode(lens=lens, max_hist=max_hist, extended=True)
-    t = env.timed(step, steps, max(3, warmup))
+        rig.decode(i, lens=lens[l], max_hist=max_hist, extended=True)
+    t = env.timed(step, steps, max(3, warmup), flush_l2=(L == 1 and rig.small))
     if rig.pool.error():
         raise RuntimeError("device error during the online steps")
-    if not np.all(lens[1].cpu().numpy() == c.hist_len + total):
+    placed = sum(int((lens[l][1].cpu().numpy() - c.hist_len).sum()) for l in range(L))
+    if placed != total * c.B:
         raise RuntimeError("the placement did not evict one token per step")
     us = env.max_ranks([float(np.mean(t) * 1e3)])[0]
     return {"us": us, "decode_alone_us": decode_us, "ratio_to_decode_alone": us / decode_us,
@@ -521,12 +547,18 @@ def run_headline(env, wl):
     queries per sequence, the online step and the oracle on the host."""
     from bit_kv_cache_12_gb300 import workloads
     args, torch, dev = env.args, env.torch, env.dev
-    c = workloads.case_from_synth(wl, torch, dev, L2_NOTE)
-    rig = DecodeRig(env, c, spare_steps=max(3, args.warmup) + args.steps + 8)
+    c = workloads.case_from_synth(wl, torch, dev, "")
+    rig = DecodeRig(env, c, spare_steps=max(3, args.warmup) + args.steps + 8, layers=HEADLINE_LAYERS)
     B, Hq = c.B, c.Hq
     with ClockSampler(env.local) as clk:
         res, t_int2, parts = decode_summary(env, rig, args.steps, args.warmup)
     us = res["us"]
+    # the same decode (layer 0) after an L2 flush before every step: code, page
+    # table and rotations are cold as well
+    t_fl = env.timed(lambda i: rig.decode(0), args.steps, max(3, args.warmup), flush_l2=True)
+    flushed = us_stats(t_fl)
+    flushed["what"] = ("the same decode of layer 0 with " + L2_FLUSH + "; the kernel's code, the page "
+                       "table and R come from HBM too")
 
     # ---- end to end through the C ABI with host buffers: the step's inputs
     # (q and the four length arrays) in one pinned staging buffer, one copy in,
@@ -541,9 +573,9 @@ def run_headline(env, wl):
     meta_dev = stage_dev[q_bytes:].view(torch.int32).view(4, B)
     out_host = torch.empty((B, Hq, 128), dtype=torch.float32).pin_memory()
 
-    def e2e_step():
+    def e2e_step(i):
         stage_dev.copy_(stage_host, non_blocking=True)
-        rig.decode(q=q_dev, lens=[meta_dev[0], meta_dev[1], meta_dev[2], meta_dev[3]])
+        rig.decode(i, q=q_dev, lens=[meta_dev[0], meta_dev[1], meta_dev[2], meta_dev[3]])
         out_host.copy_(rig.out, non_blocking=True)
 
     t_e2e = env.timed(e2e_step, args.steps, 3)
@@ -554,8 +586,8 @@ def run_headline(env, wl):
     q_host = stage_host[:q_bytes].view(torch.bfloat16).view(B, Hq, 128)
     meta_host = stage_host[q_bytes:].view(torch.int32).view(4, B)
 
-    def mapped_step():
-        rig.decode(q=q_host, lens=[meta_host[0], meta_host[1], meta_host[2], meta_host[3]], out=out_host)
+    def mapped_step(i):
+        rig.decode(i, q=q_host, lens=[meta_host[0], meta_host[1], meta_host[2], meta_host[3]], out=out_host)
 
     t_mapped = env.timed(mapped_step, args.steps, 3)
 
@@ -569,8 +601,8 @@ def run_headline(env, wl):
     m_out = torch.empty((B, TQ, Hq, 128), dtype=torch.float32, device=dev)
     m_lse = torch.empty((B, TQ, Hq), dtype=torch.float32, device=dev)
 
-    def mstep():
-        native.kv_decode_attention_multi(rig.pool.handle, 0, B, TQ, qm, *rig.lens, rig.pt,
+    def mstep(i):
+        native.kv_decode_attention_multi(rig.pool.handle, i % rig.layers, B, TQ, qm, *rig.lens, rig.pt,
                                          rig.pt_np.shape[1], rig.max_hist, c.scale, m_out, m_lse, m_ws,
                                          m_ws_bytes, env.stream)
 
@@ -584,17 +616,19 @@ def run_headline(env, wl):
     rig.close()
 
     achieved = res["algorithmic_bytes"] / (us * 1e-6) / 1e9
+    config = headline_config(wl)
     line = {
         "metric": METRIC, "value": us, "unit": "us", "n_gpus": env.world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": us / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "int2 codes, f16 MMA, f32 accumulate",
         "data": "synthetic (seeded; pool filled by kv_append_quantize)",
-        "config": headline_config(wl),
+        "config": config,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": env.peak, "unit": "GB/s",
                      "frac": achieved / env.peak, "traffic": measured_traffic(c.name),
                      "peak_source": env.peak_src, "frac_of_8tbs": achieved / 8000.0,
                      "algorithmic_bytes": res["algorithmic_bytes"], "bytes_breakdown": parts},
         "us_p10_p50_p90": res["us_p10_p50_p90"],
+        "flushed_l2": flushed,
         "bf16_path": res["bf16_path"],
         "online_step": {"batch1": online},
         "e2e": {"value": us_e2e, "unit": "us", "h2d_bytes_per_step": int(h2d),
@@ -616,9 +650,12 @@ def run_headline(env, wl):
     return line
 
 
-def run_decode_workload(env, c, steps, warmup, online=False):
+def run_decode_workload(env, c, steps, warmup, online=False, small=False):
+    """small: the workload fits in L2 and every step is flushed."""
     rig = DecodeRig(env, c, spare_steps=(max(3, warmup) + steps + 8) if online else 0)
-    res, _, parts = decode_summary(env, rig, steps, warmup)
+    rig.small = small
+    res, _, parts = decode_summary(env, rig, steps, warmup, flush_l2=small)
+    c.config["l2"] = L2_FLUSH if small else L2_LARGER
     res["config"] = c.config
     res["bytes_breakdown"] = parts
     if online:
@@ -654,7 +691,7 @@ def run_append(env, steps, warmup):
     hs = torch.zeros(n_seqs, dtype=torch.int32, device=dev)
     pt = torch.as_tensor(pt_np, device=dev)
 
-    def step():
+    def step(i):
         native.kv_append_quantize(pool.handle, 0, n_seqs, k, v, cu, hs, pt, pages_per, T, env.stream)
 
     t = env.timed(step, steps, max(3, warmup))
@@ -669,7 +706,7 @@ def run_append(env, steps, warmup):
                 "frac_of_8tbs": gbs / 8000.0, "rotation_tflops": flops / (res["us"] * 1e-6) / 1e12,
                 "launches": 2,
                 "config": {"workload": "append_64x4096_h8_g64", "sequences": n_seqs, "tokens_per_seq": T,
-                           "kv_heads": Hkv, "page_size": P, "group_size": GS, "l2": L2_NOTE}})
+                           "kv_heads": Hkv, "page_size": P, "group_size": GS, "l2": L2_LARGER}})
     return res
 
 
@@ -696,14 +733,14 @@ def main():
             sub_steps = min(args.steps, 20)
             nested = {}
             nested["tiny"] = run_decode_workload(env, workloads.case_from_synth(synth.tiny_decode(), torch,
-                                                                                dev, L2_NOTE),
-                                                 sub_steps, args.warmup)
-            c = workloads.batch64(torch, dev, L2_NOTE)
+                                                                                dev, L2_FLUSH),
+                                                 sub_steps, args.warmup, small=True)
+            c = workloads.batch64(torch, dev, L2_LARGER)
             nested["batch64"] = run_decode_workload(env, c, sub_steps, args.warmup, online=True)
             line["online_step"]["batch64"] = nested["batch64"].pop("online_step")
             del c
             torch.cuda.empty_cache()
-            c = workloads.long16(torch, dev, L2_NOTE)
+            c = workloads.long16(torch, dev, L2_LARGER)
             nested["long16"] = run_decode_workload(env, c, sub_steps, args.warmup)
             del c
             torch.cuda.empty_cache()
@@ -721,9 +758,10 @@ def main():
             res = run_append(env, args.steps, args.warmup)
             metric = APPEND_METRIC
         else:
-            c = (workloads.case_from_synth(synth.tiny_decode(), torch, dev, L2_NOTE) if w == "tiny"
-                 else getattr(workloads, w)(torch, dev, L2_NOTE))
-            res = run_decode_workload(env, c, args.steps, args.warmup, online=(w == "batch64"))
+            c = (workloads.case_from_synth(synth.tiny_decode(), torch, dev, L2_FLUSH) if w == "tiny"
+                 else getattr(workloads, w)(torch, dev, L2_LARGER))
+            res = run_decode_workload(env, c, args.steps, args.warmup, online=(w == "batch64"),
+                                      small=(w == "tiny"))
             metric = METRIC
         if rank == 0:
             us = res.pop("us")

@@ -34,8 +34,8 @@ bool dev_alloc(T** ptr, size_t bytes) {
 }
 
 void free_pool(Pool& p) {
-  void* ptrs[] = {p.hist, p.sink_k, p.sink_v, p.rec_k, p.rec_v, p.bk,     p.bv,
-                  p.Rk,   p.RvT,    p.clip,   p.rfrag, p.tickets, p.step_tickets, p.err};
+  void* ptrs[] = {p.hist, p.sink_k, p.sink_v, p.rec_k,   p.rec_v,        p.bk,  p.bv,  p.Rk,
+                  p.RvT,  p.clip,   p.rfrag,  p.tickets, p.step_tickets, p.arrive, p.err};
   for (void* q : ptrs)
     if (q) cudaFree(q);
 }
@@ -111,6 +111,7 @@ kv_status_t kv_pool_create(const kv_pool_config_t* cfg, void* stream, kv_pool_t*
     ok = ok && dev_alloc(&p.bv, L * p.bf16_layer_stride * 2);
   }
   ok = ok && dev_alloc(&p.tickets, L * c.max_seqs * H * sizeof(unsigned));
+  ok = ok && dev_alloc(&p.arrive, L * c.max_seqs * H * kvint2::kMaskWords * sizeof(unsigned));
   ok = ok && dev_alloc(&p.step_tickets, L * ((c.max_seqs + 127) / 128) * sizeof(unsigned));
   ok = ok && dev_alloc(&p.err, sizeof(int));
   if (!ok) {
@@ -130,6 +131,7 @@ kv_status_t kv_pool_create(const kv_pool_config_t* cfg, void* stream, kv_pool_t*
   zero(p.bk, L * p.bf16_layer_stride * 2);
   zero(p.bv, L * p.bf16_layer_stride * 2);
   zero(p.tickets, L * c.max_seqs * H * sizeof(unsigned));
+  zero(p.arrive, L * c.max_seqs * H * kvint2::kMaskWords * sizeof(unsigned));
   zero(p.step_tickets, L * ((c.max_seqs + 127) / 128) * sizeof(unsigned));
   zero(p.err, sizeof(int));
   if (e == cudaSuccess && c.kind == KV_POOL_INT2_3TIER) {

@@ -6,36 +6,43 @@
 // computes attention, next to the BF16 sink and recent tiers (yunpan.plus
 // OSCAR write-up, "1. 三段式 Token 池": 64 sink + INT2 history + 256 recent).
 //
-// GPU design (one launch per decode step):
-//   grid = (history splits + tier CTAs, KV heads, sequences); 16 warps per
-//   CTA and one CTA per SM for GQA <= 4 (8 warps for GQA 8), and the split
-//   count fills one wave when the batch is small.
-//   * history CTAs: one round of loads (page ids of the split, q, length),
-//     then each warp streams 16-token tiles from HBM through a 4-stage
-//     shared-memory ring, one bulk copy per tile completing on the stage's
-//     mbarrier (bounded waits), while q' = q R_k runs on the tensor cores.
-//     The 2-bit codes become fp16 MMA fragments by masking alone (exact
-//     subnormals, one logic op per code pair) and QK and PV run on the tensor
-//     cores (mma.sync m16n8k16).  Dequantization is folded:
+// GPU design (two launches per decode step):
+//   * a small pre-pass computes q' = q R_k once per (sequence, KV head) on the
+//     tensor cores and writes it as the MMA fragments the history warps use;
+//     the decode kernel is its programmatic dependent, so it launches at once
+//     and its history CTAs wait for q' only after their first tile copies are
+//     in flight.
+//   * decode grid = (history splits + 1 tier CTA, KV heads, sequences); 16
+//     warps per CTA and one CTA per SM for GQA <= 4 (12 warps for GQA 8), and
+//     the split count fills one wave when the batch is small.  Every history
+//     split is launched before every tier CTA.
+//   * history CTAs: each warp streams 16-token tiles from HBM through a
+//     4-stage shared-memory ring, one bulk copy per tile completing on the
+//     stage's mbarrier (bounded waits).  The 2-bit codes become fp16 MMA
+//     fragments by masking alone (exact subnormals, one logic op per code
+//     pair) and QK and PV run on the tensor cores (mma.sync m16n8k16).
+//     Dequantization is folded:
 //       q'.deq(k) = s_k (q'.c_k) + z_k sum(q')
 //       sum_t w_t deq(v_t) = sum_t (w_t s_v) c_v + sum_t w_t z_v
 //     so the MMA operands are exact small integers times powers of two and the
 //     query / softmax weights enter as fp16 hi + lo pairs.  Against subnormal
 //     code operands the tensor cores keep only the upper bits of the lo
 //     products (about 16 significant bits overall; measured output error
-//     about 2e-5 relative to the fp64 oracle at 100k tokens).  Online softmax per head with warp-shuffle max and a
-//     lazily moved exponent reference; per-CTA merge in shared memory; each
-//     CTA rotates its partial back by R_v^T (fp32, bulk-copied to shared
-//     memory at the start).
-//   * tier CTAs: stage their slice of the BF16 sink + recent storage into
-//     shared memory in the same first round (valid rows are picked once the
-//     lengths arrive; softmax order does not matter) and attend in SIMT fp32.
-//   * the last CTA of each (sequence, KV head), found by an atomic ticket (no
-//     waiting), merges all partials with the log-sum-exp rule and writes the
-//     fp32 output (and, for several queries per sequence, the log-sum-exp).
+//     about 2e-5 relative to the fp64 oracle at 100k tokens).  Online softmax
+//     per head with warp-shuffle max and a lazily moved exponent reference;
+//     the warps merge in shared memory and the split writes its partial
+//     (m, l, o') in the rotated basis, then sets its bit in the pair's arrival
+//     mask (release).
+//   * tier CTA: stages the BF16 sink + recent storage into shared memory
+//     before the lengths are known, attends the live rows in SIMT fp32, then
+//     merges the history partials in split order as they arrive (acquire),
+//     rotates the merged history value sum back by R_v^T once and combines it
+//     with its own result into the fp32 output (and, for several queries per
+//     sequence, the log-sum-exp).
 #include <math.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "kv_device.cuh"
 #include "kv_internal.h"
@@ -48,7 +55,8 @@ constexpr int kPart = 132;       // floats per (part, head) partial: m, l, -, -,
 constexpr float kNegInf = -INFINITY;
 constexpr int kStages = 4;       // tiles in each warp's ring
 constexpr int kWaitPolls = 1 << 20;   // bounded mbarrier polls before a copy counts as lost
-constexpr int kMaxParts = 400;   // partials per (sequence, KV head) the final merge reads
+constexpr int kMergePolls = 1 << 21;  // bounded polls of a tier CTA for its history splits
+constexpr int kMaxParts = 400;   // partials per (sequence, KV head) a merge reads
 constexpr int kMaxPids = 1032;   // page ids staged per CTA (a split covers <= 1024 tiles)
 constexpr int kTierRows = 320;   // sink + recent storage rows staged per tier CTA
 constexpr int kTierRowK = 272;   // staged K row stride (bytes): 256 + 16 keeps lane reads conflict-free
@@ -64,6 +72,12 @@ __host__ __device__ constexpr int int2_warps(int G) { return G <= 4 ? 16 : 12; }
 // page 16) are staged in shared memory
 static_assert(64 * int2_warps(1) <= kMaxPids && 64 * int2_warps(8) <= kMaxPids,
               "a split's page ids must fit the staging array");
+static_assert(kMaxParts <= 32 * kMaskWords, "every split has a bit in the arrival mask");
+// Where a history CTA gets q' = q R_k from:
+//   kQLocal  it forms q' itself from R_k's fragments (64 KB per CTA, kept in
+//            L2 across steps by their evict-last priority) - grids of one wave;
+//   kQPre    the batched pre-pass wrote the fragments - grids of several waves.
+constexpr int kQLocal = 0, kQPre = 1;
 __host__ __device__ constexpr int pad4(int n) { return (n + 3) / 4 * 4; }
 
 struct DecodeArgs {
@@ -102,49 +116,32 @@ struct DecodeArgs {
   float* lse;
   float scale_log2;
   float* out;
-  float* ws;
-  unsigned* tickets;
+  float* ws;                // history partials, then (INT2) the q' fragments
+  uint32_t* qfrag;          // INT2: [B][Hkv][32 lanes][qfrag_words] q' fragments in ws
+  unsigned* tickets;        // BF16: split-merge counters
+  unsigned* arrive;         // INT2: [max_seqs][Hkv][kMaskWords] arrival masks of the splits
+  int merge_polls;          // INT2: bounded polls of a tier CTA for its history splits
+  int qmode;                // INT2: where a history CTA gets q' from (kQLocal or kQPre)
   int* err;
 };
 
-// Shared-memory carve-up (in floats) for a CTA of NW warps.  A fixed head
-// (q, q', page ids, merged m/l; for INT2 also the ring barriers and the
-// split's per-tile source addresses) is followed by one region reused by
-// phase: the history warps' bulk-copy rings, or a tier CTA's staged rows and
-// softmax weights, then the per-warp results; the BF16 decode's final merge
-// reuses everything (the INT2 final merge reads only global memory).
-template <int G, int GS, int NW, bool kInt2>
+// Shared-memory carve-up (in floats) of the BF16 decode's CTA of NW warps:
+// q, the split's page ids, merged m / l, then the per-warp softmax weights and
+// results; the final merge reuses everything.
+template <int G, int NW>
 struct Lay {
-  static constexpr int HP = (G <= 4) ? 4 : 4 * ((G + 3) / 4);   // padded heads (MMA columns)
-  static constexpr int TB = 1024 + 16 * 8 * (128 / GS);         // stored tile bytes (one ring stage)
-  static constexpr int sq = 0;                                    // [HP][128]
-  static constexpr int sqr = sq + HP * 128;                       // [HP][128]
-  static constexpr int ssum = sqr + HP * 128;                     // [HP][2]
-  static constexpr int smm = ssum + pad4(2 * HP);                 // [G] merged m
+  static constexpr int sq = 0;                                    // [G][128]
+  static constexpr int sqr = sq + G * 128;                        // [G][128] merged o
+  static constexpr int smm = sqr + G * 128;                       // [G] merged m
   static constexpr int sml = smm + pad4(G);                       // [G] merged l
   static constexpr int spid = sml + pad4(G);                      // [kMaxPids] int
-  static constexpr int smbar = spid + kMaxPids;                   // [NW * kStages + 1] mbarriers
-  static constexpr int saddr = smbar + (kInt2 ? pad4(2 * (NW * kStages + 1)) : 0);   // [64 * NW] u64
-  static constexpr int big = saddr + (kInt2 ? 2 * 64 * NW : 0);
-  static constexpr int ring_f = kInt2 ? NW * kStages * TB / 4 : 0;
-  static constexpr int res_f = NW * G * 128 + 2 * pad4(NW * G);
-  static constexpr int sp_f = NW * 32 * G;
-  static constexpr int stage_f = kInt2 ? kTierRows * (kTierRowK + kTierRowV) / 4 : 0;
+  static constexpr int big = spid + kMaxPids;
   static constexpr int swo = big;                                 // [NW][G][128]
   static constexpr int swm = swo + NW * G * 128;                  // [NW][G]
   static constexpr int swl = swm + pad4(NW * G);                  // [NW][G]
-  static constexpr int ring = big;
-  static constexpr int stage = big;                               // tier rows
-  static constexpr int sp = big + (stage_f > res_f ? stage_f : res_f);   // [NW][32][G]
-  // history CTAs: R_v^T after the ring, and the back-rotation's row-slice sums
-  // inside the ring after the results when they fit, else after R_v^T
-  static constexpr int srv = big + ring_f;                        // [128][128] R_v^T
-  static constexpr int spr_f = NW * G * 128;                      // [NW][G][128]
-  static constexpr int spr = (res_f + spr_f <= ring_f) ? big + res_f : srv + 16384;
-  static constexpr int rot_end = kInt2 ? ((spr + spr_f > srv + 16384) ? spr + spr_f : srv + 16384) : 0;
+  static constexpr int sp = swl + pad4(NW * G);                   // [NW][32][G]
+  static constexpr int phase_end = sp + NW * 32 * G;
   static constexpr int merge_f = 16 + 2 * NW * 128 + 2 * kMaxParts * G;
-  static constexpr int phase_end0 = (big + ring_f > sp + sp_f) ? big + ring_f : sp + sp_f;
-  static constexpr int phase_end = (phase_end0 > rot_end) ? phase_end0 : rot_end;
   static constexpr int total = (phase_end > merge_f) ? phase_end : merge_f;
   static_assert(total * 4 <= 227 * 1024, "shared memory of one CTA");
 };
@@ -153,9 +150,9 @@ struct Lay {
 // shared helpers
 // ---------------------------------------------------------------------------
 
-// R_k's MMA fragments for rotate_q, held in registers: warp w of NW produces
-// q' columns (128/NW)w .., and each lane loads all its fragments at once (one
-// memory latency), so the load can be issued early and overlap other loads.
+// R_k's MMA fragments for the q' pre-pass, held in registers: warp w of NW
+// produces q' columns 8w.., 8(w + NW).., and each lane loads all its fragments
+// at once (one memory latency).
 template <int NW>
 struct RotFrags {
   static constexpr int NTW = (16 + NW - 1) / NW;   // 8-column n-tiles per warp: warp, warp + NW, ..
@@ -173,19 +170,23 @@ struct RotFrags {
 
 // q'[h][c] = sum_i q[h][i] R_k[i][c] for the first NROWS rows of X (shared,
 // [*][128] fp32 holding bf16 values), on the tensor cores: R_k comes as fp16
-// hi + lo B fragments (rotation fragment block 0, loaded by RotFrags), q is
+// hi + lo B fragments (rotation fragment block 0, in shared memory), q is
 // scaled by 2^-8 (exact) and split into fp16 hi + lo, and the three products
-// above 2^-22 relative are accumulated in fp32.  Ends with a barrier.
+// above 2^-22 relative are accumulated in fp32, each in two chains (even and
+// odd k-steps) that are added at the end in a fixed order (the same order as
+// the batched pre-pass).  Warp w produces columns 8w.., 8(w + NW)...  Ends
+// with a barrier.
 template <int NROWS, int NW>
-__device__ void rotate_q(const float* X, const RotFrags<NW>& fr, float* Y) {
+__device__ void rotate_q(const float* X, const uint4* frag, float* Y) {
   static_assert(NROWS <= 8, "rows");
-  constexpr int NTW = RotFrags<NW>::NTW;
+  constexpr int NTW = (16 + NW - 1) / NW;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = lane >> 2, j = lane & 3;
-  const auto& f = fr.f;
-  float acc[NTW][4];
+  float acc[NTW][6][4];
 #pragma unroll
-  for (int u = 0; u < NTW; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
+  for (int u = 0; u < NTW; ++u)
+#pragma unroll
+    for (int c = 0; c < 6; ++c) acc[u][c][0] = acc[u][c][1] = acc[u][c][2] = acc[u][c][3] = 0.f;
   const bool row_ok = r < NROWS;
   constexpr float kIn = 1.0f / 256.0f;
 #pragma unroll
@@ -199,19 +200,27 @@ __device__ void rotate_q(const float* X, const RotFrags<NW>& fr, float* Y) {
     const __half2 l23 = __floats2half2_rn(x.z - __low2float(h23), x.w - __high2float(h23));
     const uint32_t a0 = h2_as_u32(h01), a2 = h2_as_u32(h23);
     const uint32_t b0 = h2_as_u32(l01), b2 = h2_as_u32(l23);
+    const int c = 3 * (s & 1);
 #pragma unroll
     for (int u = 0; u < NTW; ++u) {
-      mma_f16(acc[u], a0, 0u, a2, 0u, f[s][u].x, f[s][u].y);   // hi * hi
-      mma_f16(acc[u], a0, 0u, a2, 0u, f[s][u].z, f[s][u].w);   // hi * lo
-      mma_f16(acc[u], b0, 0u, b2, 0u, f[s][u].x, f[s][u].y);   // lo * hi
+      const int nt = warp + u * NW;
+      const uint4 f = (nt < 16) ? frag[(s * 16 + nt) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+      mma_f16(acc[u][c], a0, 0u, a2, 0u, f.x, f.y);       // hi * hi
+      mma_f16(acc[u][c + 1], a0, 0u, a2, 0u, f.z, f.w);   // hi * lo
+      mma_f16(acc[u][c + 2], b0, 0u, b2, 0u, f.x, f.y);   // lo * hi
     }
   }
   if (row_ok) {
 #pragma unroll
     for (int u = 0; u < NTW; ++u)
-      if (warp + u * NW < 16)
+      if (warp + u * NW < 16) {
+        float y[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          y[e] = ((acc[u][0][e] + acc[u][3][e]) + ((acc[u][1][e] + acc[u][4][e]) + (acc[u][2][e] + acc[u][5][e])));
         *reinterpret_cast<float2*>(Y + r * 128 + 8 * (warp + u * NW) + 2 * j) =
-            make_float2(acc[u][0] * 256.0f, acc[u][1] * 256.0f);
+            make_float2(y[0] * 256.0f, y[1] * 256.0f);
+      }
   }
   __syncthreads();
 }
@@ -241,42 +250,6 @@ __device__ void merge_warps(const float* swo, const float* swm, const float* swl
       sm_m[h] = M;
       sm_l[h] = L;
     }
-  }
-  __syncthreads();
-}
-
-// merge_warps for the history split, writing the merged o transposed for
-// rotate_back_to_part: oT[c][hh] (GP = heads padded to 4; padded heads 0).
-// The weight of each (warp, head) against the head's maximum is formed once
-// (sf: NW * G floats of scratch), then every output element sums over warps.
-template <int G, int NW>
-__device__ void merge_warps_t(const float* swo, const float* swm, const float* swl, float* oT,
-                              float* sm_m, float* sm_l, float* sf) {
-  constexpr int GP = (G + 3) & ~3;
-  if (threadIdx.x < NW * G) {   // weight of warp w for head h against the head's maximum
-    const int w = threadIdx.x / G, h = threadIdx.x % G;
-    float M = kNegInf;
-#pragma unroll
-    for (int v = 0; v < NW; ++v) M = fmaxf(M, swm[v * G + h]);
-    const float mw = swm[w * G + h];
-    sf[w * G + h] = (mw == kNegInf) ? 0.f : exp2f(mw - M);
-    if (w == 0) sm_m[h] = M;
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < GP * 128; idx += NW * 32) {
-    const int h = idx >> 7, c = idx & 127;
-    float O = 0.f;
-    if (h < G) {
-      float L = 0.f;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float f = sf[w * G + h];
-        L = fmaf(f, swl[w * G + h], L);
-        O = fmaf(f, swo[(w * G + h) * 128 + c], O);
-      }
-      if (c == 0) sm_l[h] = L;
-    }
-    oT[c * GP + h] = O;
   }
   __syncthreads();
 }
@@ -322,109 +295,8 @@ __device__ bool last_to_arrive(unsigned* ticket, unsigned total) {
   return s_last != 0u;
 }
 
-// Rotate a history split's merged value sums back to the original basis,
-// o[h][c] = sum_i o'[h][i] R_v[c][i] = sum_i o'[h][i] R_v^T[i][c], straight
-// into the split's partial in global memory (with the merged m and l).  o'
-// arrives transposed, oT [128][GP]; each row of R_v^T (shared memory) is read
-// once for all heads: warp w takes rows w, w + NW, .., lane c columns
-// 4c..4c+3, and the NW row-slice sums (spr) are added while storing.
-template <int G, int NW>
-__device__ void rotate_back_to_part(const float* oT, const float* sR, float* spr, float* part,
-                                    const float* sm_m, const float* sm_l) {
-  constexpr int GP = (G + 3) & ~3;
-  const int warp = threadIdx.x >> 5, cq = threadIdx.x & 31;
-  float acc[GP][4];
-#pragma unroll
-  for (int hh = 0; hh < GP; ++hh) acc[hh][0] = acc[hh][1] = acc[hh][2] = acc[hh][3] = 0.f;
-#pragma unroll 4
-  for (int i = warp; i < 128; i += NW) {   // rows of R_v^T: warp, warp + NW, ..
-    const float4 r = *reinterpret_cast<const float4*>(sR + i * 128 + 4 * cq);
-#pragma unroll
-    for (int hq = 0; hq < GP / 4; ++hq) {
-      const float4 o = *reinterpret_cast<const float4*>(oT + i * GP + 4 * hq);
-      const float ox[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float* d = acc[4 * hq + e];
-        d[0] = fmaf(ox[e], r.x, d[0]); d[1] = fmaf(ox[e], r.y, d[1]);
-        d[2] = fmaf(ox[e], r.z, d[2]); d[3] = fmaf(ox[e], r.w, d[3]);
-      }
-    }
-  }
-#pragma unroll
-  for (int hh = 0; hh < G; ++hh)
-    *reinterpret_cast<float4*>(spr + (warp * G + hh) * 128 + 4 * cq) =
-        make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
-    const int h = idx >> 7, c = idx & 127;
-    float O = 0.f;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) O += spr[w * G * 128 + idx];
-    part[h * kPart + 4 + c] = O;
-    if (c == 0) {
-      part[h * kPart + 0] = sm_m[h];
-      part[h * kPart + 1] = sm_l[h];
-    }
-  }
-}
-
-// Log-sum-exp merge of all parts of (b, g) (every part in the original basis)
-// and the final normalisation, in one pass with no barrier: thread (h, c)
-// merges output element c of head h over the parts itself, a batch of
-// kMergeBatch parts per round of loads (m and l of a part are the same for
-// all 128 threads of a head and arrive as broadcasts).  Within a batch the
-// weights are 2^(m_s - M) against the batch's running maximum M; a later batch
-// with a larger maximum rescales what is accumulated so far.
+// Partials merged per round of loads.
 constexpr int kMergeBatch = 20;
-
-template <int G, int NW, bool kMulti>
-__device__ void merge_parts(const DecodeArgs& a, int b, int g, int nparts, float* sm) {
-  (void)sm;
-  const float* base = a.ws + (size_t)(b * a.Hkv + g) * nparts * G * kPart;
-  for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
-    const int hh = idx >> 7, c = idx & 127;
-    const float* ph = base + (size_t)hh * kPart;
-    float M = kNegInf, L = 0.f, O = 0.f;
-    for (int s0 = 0; s0 < nparts; s0 += kMergeBatch) {
-      float mv[kMergeBatch], lv[kMergeBatch], ov[kMergeBatch];
-#pragma unroll
-      for (int u = 0; u < kMergeBatch; ++u) {
-        const int s = s0 + u;
-        const float* pp = ph + (size_t)s * G * kPart;
-        const float2 ml = (s < nparts) ? __ldcg(reinterpret_cast<const float2*>(pp))
-                                       : make_float2(kNegInf, 0.f);
-        mv[u] = ml.x;
-        lv[u] = ml.y;
-        ov[u] = (s < nparts) ? __ldcg(pp + 4 + c) : 0.f;
-      }
-      float Mb = M;
-#pragma unroll
-      for (int u = 0; u < kMergeBatch; ++u) Mb = fmaxf(Mb, mv[u]);
-      if (Mb != kNegInf) {
-        const float alpha = (M == kNegInf) ? 0.f : exp2f(M - Mb);
-        L *= alpha;
-        O *= alpha;
-#pragma unroll
-        for (int u = 0; u < kMergeBatch; ++u) {
-          const float f = (mv[u] == kNegInf) ? 0.f : exp2f(mv[u] - Mb);
-          L = fmaf(f, lv[u], L);
-          O = fmaf(f, ov[u], O);
-        }
-        M = Mb;
-      }
-    }
-    if constexpr (kMulti) {
-      const size_t row = ((size_t)b * a.T + hh / a.Gq) * a.Hq + g * a.Gq + hh % a.Gq;
-      a.out[row * 128 + c] = (L > 0.f) ? O / L : 0.f;
-      // ln sum exp(scaled score) = ln 2 * (M + log2 L), the scores being in log2 units
-      if (a.lse && c == 0) a.lse[row] = (L > 0.f) ? 0.6931471805599453f * (M + log2f(L)) : kNegInf;
-    } else {
-      a.out[((size_t)b * a.Hq + g * G + hh) * 128 + c] = (L > 0.f) ? O / L : 0.f;
-    }
-  }
-  if (threadIdx.x == 0) a.tickets[b * a.Hkv + g] = 0u;   // ready for the next call
-}
 
 // ---------------------------------------------------------------------------
 // BF16 rows: warp-cooperative SIMT attention over a token range
@@ -575,34 +447,219 @@ __device__ void load_q(const DecodeArgs& a, int b, int g, float* sq, int padded_
 }
 
 // ---------------------------------------------------------------------------
-// INT2 history split (the hot loop)
+// INT2 decode, step 1: q' = q R_k once per (sequence, KV head)
 // ---------------------------------------------------------------------------
+// 32-bit words per (sequence, KV head) and lane of a history warp: the QK B
+// fragments qf[8 steps][NT][2] (fp16 hi / lo of q'), then the per-group sums
+// of q' in the units of the score accumulator (NT * NG <= 4 words).
+template <int G>
+__host__ __device__ constexpr int qfrag_words() { return 16 * ((G <= 4) ? 1 : 2) + 4; }
+
+// q' = q R_k for every (sequence, KV head) of the batch on the tensor cores:
+// q (scaled by 2^-8, exact) split into fp16 hi + lo, R_k as fp16 hi + lo
+// fragments (rotation fragment block 0), the three products above 2^-22
+// relative accumulated in fp32.  A CTA of eight warps takes one KV head and
+// 16 / HP sequences (one 16-row MMA tile of (sequence, head) rows) and writes
+// every history warp's fragments of q' and the per-group sums.  It lets the
+// decode kernel launch at once (programmatic dependent launch); the decode's
+// history CTAs wait for it only when they need q'.
 template <int G, int GS, bool kMulti>
-__device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float* sm,
-                             float* part) {
+__global__ void __launch_bounds__(256) qprep_kernel(DecodeArgs a, int B) {
+  constexpr int HP = (G <= 4) ? 4 : 8;   // MMA columns of a KV head (4 heads x hi / lo)
+  constexpr int NT = HP / 4;
+  constexpr int NG = 128 / GS;
+  constexpr int SPB = 16 / HP;           // sequences per CTA
+  constexpr int QW = qfrag_words<G>();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __shared__ __align__(16) float X[16 * 128];
+  __shared__ __align__(16) float Y[16 * 128];
+  __shared__ float ssum[16 * 2];
+  const int g = blockIdx.x, b0 = blockIdx.y * SPB;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  RotFrags<8> rk;
+  rk.load(a.rfrag + (size_t)g * kFragBlocks * 4096);
+  for (int idx = threadIdx.x; idx < 16 * 128; idx += 256) {   // row = sequence * HP + head
+    const int row = idx >> 7, c = idx & 127, sl = row / HP, hh = row % HP, b = b0 + sl;
+    float v = 0.f;
+    if (hh < G && b < B) {
+      const size_t qrow = kMulti ? ((size_t)b * a.T + hh / a.Gq) * a.Hq + g * a.Gq + hh % a.Gq
+                                 : (size_t)b * a.Hq + g * G + hh;
+      v = __uint_as_float((uint32_t)a.q[qrow * 128 + c] << 16);
+    }
+    X[idx] = v;
+  }
+  __syncthreads();
+  {   // rows r and r + 8 of the A fragment; warp w produces q' columns 8w.. and 8(w + 8)..
+    const int r = lane >> 2, j = lane & 3;
+    float acc[2][6][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int c = 0; c < 6; ++c) acc[u][c][0] = acc[u][c][1] = acc[u][c][2] = acc[u][c][3] = 0.f;
+    constexpr float kIn = 1.0f / 256.0f;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      // A: row r, k index kappa -> input channel 32*(kappa%8/2) + 4s + 2*(kappa/8) + kappa%2
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float4 x = *reinterpret_cast<const float4*>(X + (r + 8 * half) * 128 + 32 * j + 4 * s);
+        x.x *= kIn; x.y *= kIn; x.z *= kIn; x.w *= kIn;
+        const __half2 h01 = __floats2half2_rn(x.x, x.y), h23 = __floats2half2_rn(x.z, x.w);
+        const __half2 l01 = __floats2half2_rn(x.x - __low2float(h01), x.y - __high2float(h01));
+        const __half2 l23 = __floats2half2_rn(x.z - __low2float(h23), x.w - __high2float(h23));
+        hi[half] = h2_as_u32(h01); hi[2 + half] = h2_as_u32(h23);
+        lo[half] = h2_as_u32(l01); lo[2 + half] = h2_as_u32(l23);
+      }
+      const int c = 3 * (s & 1);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint4 f = rk.f[s][u];
+        mma_f16(acc[u][c], hi[0], hi[1], hi[2], hi[3], f.x, f.y);       // hi * hi
+        mma_f16(acc[u][c + 1], hi[0], hi[1], hi[2], hi[3], f.z, f.w);   // hi * lo
+        mma_f16(acc[u][c + 2], lo[0], lo[1], lo[2], lo[3], f.x, f.y);   // lo * hi
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      float y[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        y[e] = ((acc[u][0][e] + acc[u][3][e]) + ((acc[u][1][e] + acc[u][4][e]) + (acc[u][2][e] + acc[u][5][e])));
+      const int col = 8 * (warp + 8 * u) + 2 * j;
+      *reinterpret_cast<float2*>(Y + r * 128 + col) = make_float2(y[0] * 256.0f, y[1] * 256.0f);
+      *reinterpret_cast<float2*>(Y + (r + 8) * 128 + col) = make_float2(y[2] * 256.0f, y[3] * 256.0f);
+    }
+  }
+  __syncthreads();
+  for (int row = warp; row < 16; row += 8) {   // per-group sums of q'
+#pragma unroll
+    for (int grp = 0; grp < NG; ++grp) {
+      float v = 0.f;
+      for (int c = grp * GS + lane; c < (grp + 1) * GS; c += 32) v += Y[row * 128 + c];
+      v = warp_sum_xor(v, 1);
+      if (lane == 0) ssum[row * 2 + grp] = v;
+    }
+  }
+  __syncthreads();
+  // fragments: B column n = lane/4 of n-tile nt -> head 4 nt + n/2, part n%2 (hi / lo)
+  for (int idx = threadIdx.x; idx < SPB * 32 * QW; idx += 256) {
+    const int sl = idx / (32 * QW), ln = (idx / QW) % 32, w = idx % QW;
+    const int b = b0 + sl;
+    if (b >= B) continue;
+    const int r = ln >> 2, j = ln & 3;
+    uint32_t val = 0u;
+    if (w < 16 * NT) {
+      const int reg = w & 1, nt = (w >> 1) % NT, s = (w >> 1) / NT;
+      const float* row = Y + (sl * HP + 4 * nt + (r >> 1)) * 128 + 16 * s + 2 * j + 8 * reg;
+      // group 64: the odd steps' code factor 16 is cancelled here (a power of 2);
+      // group 128 removes it from the odd steps' accumulator chain instead
+      const float f = (GS == 64 && (s & 1)) ? 0.0625f : 1.0f;
+      const float x0 = row[0] * f, x1 = row[1] * f;
+      const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+      const bool lo_part = r & 1;
+      const __half p0 = lo_part ? __float2half_rn(x0 - __half2float(h0)) : h0;
+      const __half p1 = lo_part ? __float2half_rn(x1 - __half2float(h1)) : h1;
+      val = h2_as_u32(__halves2half2(p0, p1));
+    } else if (w - 16 * NT < NT * NG) {
+      const int kk = w - 16 * NT, nt = kk / NG, grp = kk % NG;
+      val = __float_as_uint(ssum[(sl * HP + 4 * nt + j) * 2 + grp] * 5.9604644775390625e-8f);
+    }
+    a.qfrag[((size_t)(b * a.Hkv + g) * 32 + ln) * QW + w] = val;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// INT2 decode, step 2: history splits (the hot loop) and the tier CTA that
+// attends the BF16 rows and merges everything
+// ---------------------------------------------------------------------------
+// Shared memory of a history CTA (byte offsets).  The per-warp results reuse
+// the ring once the loop is done.
+template <int G, int GS>
+struct HistLay {
+  static constexpr int NW = int2_warps(G);
+  static constexpr int TB = 1024 + 16 * 8 * (128 / GS);   // stored tile bytes (one ring stage)
+  static constexpr int ring = 0;                          // [NW][kStages][TB]
+  static constexpr int bars = ring + NW * kStages * TB;   // [NW][kStages] mbarriers
+  static constexpr int saddr = bars + NW * kStages * 8;   // [64 NW] tile source addresses
+  static constexpr int spid = saddr + 64 * NW * 8;        // [kMaxPids] page ids
+  static constexpr int HP = (G <= 4) ? 4 : 8;             // padded heads (MMA columns)
+  static constexpr int sq = spid + kMaxPids * 4;          // [HP][128] q (q' computed in the CTA)
+  static constexpr int sqr = sq + HP * 128 * 4;           // [HP][128] q'
+  static constexpr int ssum = sqr + HP * 128 * 4;         // [HP][2] per-group sums of q'
+  static constexpr int rkbar = (ssum + HP * 2 * 4 + 7) / 8 * 8;   // mbarrier of the R_k fragment copy
+  static constexpr int rfr = (rkbar + 8 + 127) / 128 * 128;      // [4096] uint4 R_k fragments
+  static constexpr int total = rfr + 4096 * 16;
+  static constexpr int swo = 0;                           // [NW][G][128] per-warp o'
+  static constexpr int swm = swo + NW * G * 128 * 4;      // [NW][G] m
+  static constexpr int swl = swm + NW * G * 4;            // [NW][G] l
+  static_assert(swl + NW * G * 4 <= bars, "the warp results fit in the ring");
+};
+
+// Shared memory of a tier CTA (byte offsets).  R_v^T, the warp results and the
+// merged history o' reuse the staging area once the tier rows are attended.
+template <int G>
+struct TierLay {
+  static constexpr int NW = int2_warps(G);
+  static constexpr int sq = 0;                                         // [G][128] q
+  static constexpr int stage = sq + G * 128 * 4;                       // staged sink + recent rows
+  static constexpr int sp = stage + kTierRows * (kTierRowK + kTierRowV);   // [NW][32][G] weights
+  static constexpr int tier_o = sp + NW * 32 * G * 4;                  // [G][128] tier partial o
+  static constexpr int tier_m = tier_o + G * 128 * 4;                  // [G]
+  static constexpr int tier_l = tier_m + G * 4;                        // [G]
+  static constexpr int hist_m = tier_l + G * 4;                        // [G] merged history m
+  static constexpr int hist_l = hist_m + G * 4;                        // [G]
+  static constexpr int bar = (hist_l + G * 4 + 7) / 8 * 8;             // mbarrier of the R_v^T copy
+  static constexpr int ctl = bar + 8;                                  // merge progress
+  static constexpr int total = ctl + 16;
+  static constexpr int swo = stage;                                    // [NW][G][128]
+  static constexpr int swm = swo + NW * G * 128 * 4;                   // [NW][G]
+  static constexpr int swl = swm + NW * G * 4;                         // [NW][G]
+  static constexpr int rv = (swl + NW * G * 4 + 1023) / 1024 * 1024;   // [128][128] R_v^T
+  static constexpr int GP = (G + 3) & ~3;
+  static constexpr int oh = rv + 128 * 128 * 4;                        // [128][GP] merged history o', transposed
+  static constexpr int spr = swo;                                      // [NW][G][128] row-slice sums
+  static_assert(oh + GP * 128 * 4 <= sp, "R_v^T and the merge fit in the staging area");
+};
+
+template <int G, int GS>
+constexpr size_t int2_smem() {
+  return (size_t)(HistLay<G, GS>::total > TierLay<G>::total ? HistLay<G, GS>::total : TierLay<G>::total);
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// One history split of (sequence b, KV head g): stream its 16-token tiles of
+// 2-bit codes and attend them with q' (in the rotated basis), and write the
+// split's partial (m, l, o' unnormalised) to `part`.
+template <int G, int GS, bool kMulti>
+__device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8_t* smb, float* part) {
   constexpr int NW = int2_warps(G);
-  using S = Lay<G, GS, NW, true>;
-  constexpr int NT = S::HP / 4;      // MMA n-tiles of 8 columns (4 heads x hi/lo)
+  using S = HistLay<G, GS>;
+  constexpr int HP = (G <= 4) ? 4 : 4 * ((G + 3) / 4);
+  constexpr int NT = HP / 4;         // MMA n-tiles of 8 columns (4 heads x hi / lo)
   constexpr int NG = 128 / GS;       // quantization groups per row
+  constexpr int QW = qfrag_words<G>();
+  constexpr uint32_t TB = S::TB;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = lane >> 2, j = lane & 3;
 
-  // ---- barriers, then one round of independent loads: R_k's fragments, the
-  // split's page ids, q and the length.  Lane 0 of each warp also reads the
-  // page ids of its first tiles itself, so that their copies start as soon as
-  // the page table answers, while q' is still being formed. ----
+  // ---- barriers, then one round of independent loads: the split's page ids
+  // and the length; lane 0 of each warp also reads the page ids of its first
+  // tiles itself, so that their copies start as soon as the page table answers.
   // A ring stage holds one whole stored tile, brought in by one bulk copy that
-  // lane 0 issues and that completes on the stage's mbarrier; R_v^T (for the
-  // back-rotation of the partial) comes the same way on its own barrier.
-  constexpr uint32_t TB = S::TB;
-  uint8_t* ring = reinterpret_cast<uint8_t*>(sm + S::ring) + (size_t)warp * kStages * TB;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::smbar);
-  uint64_t* wbar = bars + warp * kStages;
-  uint64_t* rbar = bars + NW * kStages;
-  float* srv = sm + S::srv;
-  uint64_t* saddr = reinterpret_cast<uint64_t*>(sm + S::saddr);   // per-tile source addresses
+  // lane 0 issues and that completes on the stage's mbarrier. ----
+  uint8_t* ring = smb + S::ring + (size_t)warp * kStages * TB;
+  uint64_t* wbar = reinterpret_cast<uint64_t*>(smb + S::bars) + warp * kStages;
+  uint64_t* saddr = reinterpret_cast<uint64_t*>(smb + S::saddr);   // per-tile source addresses
+  int* spid = reinterpret_cast<int*>(smb + S::spid);
+  uint64_t* rkbar = reinterpret_cast<uint64_t*>(smb + S::rkbar);
   if (lane < kStages) mbar_init(wbar + lane, 1);
-  if (threadIdx.x == 0) mbar_init(rbar, 1);
+  if (threadIdx.x == 0) mbar_init(rkbar, 1);
   mbar_fence_init();
 
   const int tsh = a.tpp_shift, tmask = a.tiles_per_page - 1;
@@ -618,14 +675,23 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
       pid_first[st] = (pg < a.max_pages) ? __ldg(ptrow + pg) : -1;
     }
   }
-  RotFrags<NW> rk;
-  rk.load(a.rfrag + ((size_t)g * kFragBlocks + 0) * 4096);
-  int* spid = reinterpret_cast<int*>(sm + S::spid);
   for (int i = threadIdx.x; i < p_all; i += NW * 32) spid[i] = __ldg(ptrow + p_begin + i);
-  float* sq = sm + S::sq;
-  float* sqr = sm + S::sqr;
-  float* ssum = sm + S::ssum;
-  load_q<G, NW, kMulti>(a, b, g, sq, S::HP);
+  float* sq = reinterpret_cast<float*>(smb + S::sq);
+  // q' is formed here (kQLocal) or taken from the pre-pass; when formed here,
+  // q and R_k's fragments (64 KB, by bulk copy) are requested behind the loads
+  // above
+  const bool local = a.qmode == kQLocal;
+  uint4* rfr = reinterpret_cast<uint4*>(smb + S::rfr);
+  if (local) {
+    load_q<G, NW, kMulti>(a, b, g, sq, S::HP);
+    if (threadIdx.x == 0) {
+      const uint4* src = a.rfrag + (size_t)g * kFragBlocks * 4096;
+      const uint64_t keep = l2_evict_last_policy();
+      mbar_expect_tx(rkbar, 4096 * 16);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) bulk_g2s_hint(rfr + 1024 * c, src + 1024 * c, 16384, rkbar, keep);
+    }
+  }
   int h = __ldg(a.hist_len + b);
   // the grid covers max_len history tokens (and the page table max_pages pages)
   const int cap = min(a.max_pages * a.page_size, a.max_len);
@@ -635,7 +701,9 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
   }
   const int ntiles = (h + kTile - 1) / kTile;
   const int t_end = min(ntiles, t_begin + a.per_split);
-  if (t_begin >= t_end) {   // the same for every thread: no copy was started
+  if (t_begin >= t_end) {   // the same for every thread: no tile copy was started
+    if (local && !mbar_wait(rkbar, 0, a.wait_polls) && threadIdx.x == 0) flag_error(a.err, KV_DEVERR_TIMEOUT);
+    if (threadIdx.x == 0) mbar_inval(rkbar);
     write_empty_partial<G, NW>(part);
     return;
   }
@@ -643,19 +711,14 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
   // ---- start streaming this warp's first tiles into its ring ----
   const uint8_t* head_base = a.hist + (size_t)g * (a.page_bytes / a.Hkv);
   const int lane_sz = (GS == 128) ? 1024 + 16 * r : 1024 + 32 * r;
+  // the history is read once per step: its lines leave L2 first
+  const uint64_t stream_policy = l2_evict_first_policy();
   auto start_copy = [&](int t, int pid, int stage) {
     const uint8_t* tb = (pid >= 0 && pid < a.num_pages)
                             ? head_base + (size_t)pid * a.page_bytes + (t & tmask) * a.tile_bytes
                             : g_zero_tile;
     mbar_expect_tx(wbar + stage, TB);
-    bulk_g2s(ring + stage * TB, tb, TB, wbar + stage);
-  };
-  auto issue = [&](int t, int stage) {   // tiles k >= kStages - 1, from the address table
-    if (lane == 0 && t < t_end) {
-      const uint64_t e = saddr[t - t_begin];
-      mbar_expect_tx(wbar + stage, TB);
-      bulk_g2s(ring + stage * TB, reinterpret_cast<const void*>(e & ~1ull), TB, wbar + stage);
-    }
+    bulk_g2s_hint(ring + stage * TB, tb, TB, wbar + stage, stream_policy);
   };
   __syncwarp();   // this warp's barriers are initialised
   if (lane == 0) {
@@ -669,17 +732,12 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
         start_copy(t, pid_first[st], st);
     }
   }
-  if (threadIdx.x == 0) {
-    const float* R = a.RvT + (size_t)g * 128 * 128;
-    mbar_expect_tx(rbar, 128 * 128 * 4);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) bulk_g2s(srv + 4096 * c, R + 4096 * c, 16384, rbar);
-  }
-  __syncthreads();   // q and the page ids are in shared memory
+  __syncthreads();   // the page ids (and q) are in shared memory
 
   // ---- the source address of every tile of the split, bit 0 set when its
   // page id is valid (else the copy reads a zero tile and its tokens are
   // masked); bad page ids are reported here, once per tile ----
+  int bad = 0;
   for (int i = threadIdx.x; i < t_end - t_begin; i += NW * 32) {
     const int t = t_begin + i;
     const int pid = spid[(t >> tsh) - p_begin];
@@ -689,25 +747,30 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
     } else {
       saddr[i] = reinterpret_cast<uint64_t>(g_zero_tile);
       flag_error(a.err, KV_DEVERR_PAGE_ID);
+      bad = 1;
     }
   }
+  bad = __syncthreads_or(bad);   // the table is complete; any bad page -> every tile masked
 
-  // ---- q' = q R_k and its per-group sums (overlaps the first copies) ----
-  rotate_q<S::HP, NW>(sq, rk, sqr);
-  for (int hh = warp; hh < S::HP; hh += NW) {
-#pragma unroll
-    for (int grp = 0; grp < NG; ++grp) {
-      float v = 0.f;
-      for (int c = grp * GS + lane; c < (grp + 1) * GS; c += 32) v += sqr[hh * 128 + c];
-      v = warp_sum_xor(v, 1);
-      if (lane == 0) ssum[hh * 2 + grp] = v;
-    }
-  }
-  __syncthreads();
-
-  // QK B fragments: column n = lane/4 -> local head 4*nt + n/2, part n%2 (hi/lo)
   uint32_t qf[8][NT][2];
-  {
+  float sumq[NT][NG];
+  bool ok = true;
+  if (local) {   // ---- q' = q R_k here, then its fragments and per-group sums ----
+    float* sqr = reinterpret_cast<float*>(smb + S::sqr);
+    float* ssum = reinterpret_cast<float*>(smb + S::ssum);
+    ok = __syncthreads_and(mbar_wait(rkbar, 0, a.wait_polls));   // false: the tiles are skipped below
+    rotate_q<S::HP, NW>(sq, rfr, sqr);
+    for (int hh = warp; hh < S::HP; hh += NW) {
+#pragma unroll
+      for (int grp = 0; grp < NG; ++grp) {
+        float v = 0.f;
+        for (int c = grp * GS + lane; c < (grp + 1) * GS; c += 32) v += sqr[hh * 128 + c];
+        v = warp_sum_xor(v, 1);
+        if (lane == 0) ssum[hh * 2 + grp] = v;
+      }
+    }
+    __syncthreads();
+    // QK B fragments: column n = lane/4 -> local head 4*nt + n/2, part n%2 (hi/lo)
     const int hl = r >> 1, e = r & 1;
 #pragma unroll
     for (int s = 0; s < 8; ++s)
@@ -727,13 +790,32 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
         qf[s][nt][0] = h2_as_u32(__halves2half2(p[0], p[1]));
         qf[s][nt][1] = h2_as_u32(__halves2half2(p[2], p[3]));
       }
+    // per-group sums of q' in the units of the score accumulator (2^-24)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int grp = 0; grp < NG; ++grp) sumq[nt][grp] = ssum[(4 * nt + j) * 2 + grp] * 5.9604644775390625e-8f;
+  } else {   // ---- q' fragments and per-group sums from the pre-pass ----
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint4* qp = reinterpret_cast<const uint4*>(a.qfrag + ((size_t)(b * a.Hkv + g) * 32 + lane) * QW);
+    uint32_t w[QW];
+#pragma unroll
+    for (int i = 0; i < QW / 4; ++i) {
+      const uint4 v = __ldcg(qp + i);
+      w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    }
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        qf[s][nt][0] = w[(s * NT + nt) * 2];
+        qf[s][nt][1] = w[(s * NT + nt) * 2 + 1];
+      }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int grp = 0; grp < NG; ++grp) sumq[nt][grp] = __uint_as_float(w[16 * NT + nt * NG + grp]);
   }
-  // per-group sums of q' in the units of the score accumulator (2^-24)
-  float sumq[NT][NG];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int grp = 0; grp < NG; ++grp) sumq[nt][grp] = ssum[(4 * nt + j) * 2 + grp] * 5.9604644775390625e-8f;
   const float sc24 = a.scale_log2 * 16777216.0f;   // 2^24 back on the scores
 
   // base: the exponent reference as used (0 while m_run is still -inf)
@@ -751,28 +833,40 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
       for (int u = 0; u < 4; ++u) oacc[i][nt][u] = 0.f;
   }
 
-  int k = 0;
-  bool ok = true;
-#pragma unroll 2   // lets one tile's loads, unpack and QK overlap the previous tile's softmax and PV
-  for (int t = t_begin + warp; t < t_end; t += NW, ++k) {
+  int k = 0;   // this warp's tile count: ring stage k % kStages, phase k / kStages
+  // tiles of this warp whose copy was issued (the first kStages - 1 above)
+  int issued = min(kStages - 1, (t_end - t_begin - warp + NW - 1) / NW);
+  auto issue = [&](int t, int stage) {   // tiles k >= kStages - 1, from the address table
+    if (t < t_end) ++issued;
+    if (lane == 0 && t < t_end) {
+      const uint64_t e = saddr[t - t_begin];
+      mbar_expect_tx(wbar + stage, TB);
+      bulk_g2s_hint(ring + stage * TB, reinterpret_cast<const void*>(e & ~1ull), TB, wbar + stage, stream_policy);
+    }
+  };
+  // One tile: QK, online softmax and PV.  kMask: the tile may hold tokens past
+  // the history or sit behind a bad page id (only the split's last tile, or
+  // every tile of a split with a bad page); other tiles need no masks.
+  // Returns false if its copy did not arrive in time.
+  auto tile = [&](int t, auto mask_tag) -> bool {
+    constexpr bool kMask = decltype(mask_tag)::value;
     __syncwarp();   // every lane is done with the stage refilled next
     // tile k+3 goes into the stage read in the previous iteration
     issue(t + NW * (kStages - 1), (k + kStages - 1) % kStages);
     const int st = k % kStages;
-    if (!__all_sync(0xffffffffu, mbar_wait(wbar + st, (k / kStages) & 1, a.wait_polls))) {
-      ok = false;
-      break;
-    }
+    if (!__all_sync(0xffffffffu, mbar_wait(wbar + st, (k / kStages) & 1, a.wait_polls))) return false;
     const uint8_t* src = ring + st * TB;
     const uint4 kq4 = *reinterpret_cast<const uint4*>(src + 16 * lane);
     const uint4 vq4 = *reinterpret_cast<const uint4*>(src + 512 + 16 * lane);
     const uint4 sz0 = *reinterpret_cast<const uint4*>(src + lane_sz);
     const uint4 sz1 =
         (GS == 64) ? *reinterpret_cast<const uint4*>(src + lane_sz + 16) : make_uint4(0, 0, 0, 0);
-    // tokens of this tile still inside the history (none if its page id is bad)
-    const int lim = ((saddr[t - t_begin] & 1ull) != 0) ? h - t * kTile : 0;
-    const bool v0 = r < lim;
-    const bool v1 = r + 8 < lim;
+    bool v0 = true, v1 = true;
+    if constexpr (kMask) {   // tokens of this tile still inside the history (none if its page id is bad)
+      const int lim = ((saddr[t - t_begin] & 1ull) != 0) ? h - t * kTile : 0;
+      v0 = r < lim;
+      v1 = r + 8 < lim;
+    }
 
     // scale / zero of tokens r and r+8
     float sk[2][NG], zk[2][NG], sv[2][NG], zv[2][NG];
@@ -853,8 +947,13 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
         l0 = fmaf(sk[0][grp], d0, fmaf(zk[0][grp], sumq[nt][grp], l0));
         l1 = fmaf(sk[1][grp], d1, fmaf(zk[1][grp], sumq[nt][grp], l1));
       }
-      l0 = v0 ? l0 * sc24 : kNegInf;
-      l1 = v1 ? l1 * sc24 : kNegInf;
+      if constexpr (kMask) {
+        l0 = v0 ? l0 * sc24 : kNegInf;
+        l1 = v1 ? l1 * sc24 : kNegInf;
+      } else {
+        l0 *= sc24;
+        l1 *= sc24;
+      }
       // m_run is the exponent reference (>= every score seen so far); it only
       // moves when some score of the warp exceeds its head's reference, so the
       // per-head maximum is formed only then
@@ -907,30 +1006,42 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
         }
       }
     }
-  }
-  if (!ok) {   // a copy did not arrive in time: wait (bounded) for the ones in flight
-    // iteration k had already issued tile k + kStages - 1, so the copies that
-    // may be in flight are those of tiles k .. k + kStages - 1
+    ++k;
+    return true;
+  };
+
+  // tiles below t_full are full and behind valid pages: no masks
+  const int t_full = bad ? t_begin : min(t_end, h / kTile);
+  int t = ok ? t_begin + warp : t_end;   // a lost R_k copy skips the split
+#pragma unroll 2   // lets one tile's loads, unpack and QK overlap the previous tile's softmax and PV
+  for (; t < t_full; t += NW)
+    if (!tile(t, std::false_type{})) {
+      ok = false;
+      break;
+    }
+  if (ok)
+    for (; t < t_end; t += NW)
+      if (!tile(t, std::true_type{})) {
+        ok = false;
+        break;
+      }
+  if (!ok) {   // a copy did not arrive in time: wait (bounded) for the ones in flight,
+    // those of tiles k .. issued - 1 of this warp
     if (lane == 0) flag_error(a.err, KV_DEVERR_TIMEOUT);
-    for (int kk = k; kk < k + kStages && t_begin + warp + NW * kk < t_end; ++kk)
-      mbar_wait(wbar + kk % kStages, (kk / kStages) & 1, a.wait_polls);
-  }
-  if (!mbar_wait(rbar, 0, a.wait_polls)) {
-    ok = false;
-    if (threadIdx.x == 0) flag_error(a.err, KV_DEVERR_TIMEOUT);
+    for (int kk = k; kk < issued; ++kk) mbar_wait(wbar + kk % kStages, (kk / kStages) & 1, a.wait_polls);
   }
   ok = __syncthreads_and(ok);   // every warp is done with its ring before the results reuse it
   if (lane < kStages) mbar_inval(wbar + lane);
-  if (threadIdx.x == 0) mbar_inval(rbar);
+  if (threadIdx.x == 0) mbar_inval(rkbar);
   if (!ok) {   // the split's result is skipped
     write_empty_partial<G, NW>(part);
     return;
   }
 
-  // ---- warp results -> shared memory ----
-  float* swo = sm + S::swo;
-  float* swm = sm + S::swm;
-  float* swl = sm + S::swl;
+  // ---- warp results -> shared memory (over the ring) ----
+  float* swo = reinterpret_cast<float*>(smb + S::swo);
+  float* swm = reinterpret_cast<float*>(smb + S::swm);
+  float* swl = reinterpret_cast<float*>(smb + S::swl);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const float l = warp_sum_xor(l_run[nt], 4);
@@ -956,102 +1067,287 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, float
     }
   }
   __syncthreads();
-  // merged sums, transposed for the back-rotation, into q's slot (q and q' are
-  // no longer needed); then back to the original basis, into the partial
-  merge_warps_t<G, NW>(swo, swm, swl, sq, sm + S::smm, sm + S::sml,
-                       reinterpret_cast<float*>(spid));   // page ids no longer needed
-  rotate_back_to_part<G, NW>(sq, srv, sm + S::spr, part, sm + S::smm, sm + S::sml);
+  // the warps merged with the log-sum-exp rule into the split's partial (rotated basis)
+  for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
+    const int hh = idx >> 7, c = idx & 127;
+    float M = kNegInf;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, swm[w * G + hh]);
+    float L = 0.f, O = 0.f;
+    if (M != kNegInf) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float mw = swm[w * G + hh];
+        const float f = (mw == kNegInf) ? 0.f : exp2f(mw - M);
+        L = fmaf(f, swl[w * G + hh], L);
+        O = fmaf(f, swo[(w * G + hh) * 128 + c], O);
+      }
+    }
+    part[hh * kPart + 4 + c] = O;
+    if (c == 0) {
+      part[hh * kPart + 0] = M;
+      part[hh * kPart + 1] = L;
+    }
+  }
 }
 
-// ---------------------------------------------------------------------------
-// BF16 sink + recent tiers of the INT2 pool: tier CTA `ti` stages storage
-// rows [ti*kTierRows, ...) of [sink slots | recent ring] before it knows the
-// lengths, then attends over the rows that hold live tokens.
-// ---------------------------------------------------------------------------
+// The tier CTA of (sequence b, KV head g), launched after every history
+// split: attends the BF16 sink + recent rows (staged in shared memory, SIMT
+// fp32), then merges the history splits' partials in split order as they
+// arrive (each split sets its bit in the pair's arrival mask with a release
+// reduction after writing its partial), rotates the merged history value sum
+// back by R_v^T once, combines it with the tier result and writes the output.
 template <int G, int GS, bool kMulti>
-__device__ void bf16_tiers(const DecodeArgs& a, int b, int g, int ti, float* sm, float* part) {
+__device__ void tier_merge(const DecodeArgs& a, int b, int g, uint8_t* smb) {
   constexpr int NW = int2_warps(G);
-  using S = Lay<G, GS, NW, true>;
+  using S = TierLay<G>;
   const int warp = threadIdx.x >> 5;
-  const int scap = a.sink_cap, rcap = a.rec_cap;
-  const int r0 = min(scap + rcap, ti * kTierRows), r1 = min(scap + rcap, r0 + kTierRows);
+  const int scap = a.sink_cap, rcap = a.rec_cap, rows = scap + rcap;
   const size_t seq_head = (size_t)b * a.Hkv + g;
   const uint16_t* sk = a.sink_k + seq_head * scap * 128;
   const uint16_t* sv = a.sink_v + seq_head * scap * 128;
   const uint16_t* rk = a.rec_k + seq_head * rcap * 128;
   const uint16_t* rv = a.rec_v + seq_head * rcap * 128;
-  uint8_t* stk = reinterpret_cast<uint8_t*>(sm + S::stage);
+  float* sq = reinterpret_cast<float*>(smb + S::sq);
+  uint8_t* stk = smb + S::stage;
   uint8_t* stv = stk + (size_t)kTierRows * kTierRowK;
-  for (int i = threadIdx.x; i < (r1 - r0) * 32; i += NW * 32) {
-    const int t = i >> 5, c = i & 31, key = c < 16, ch = c & 15, row = r0 + t;
-    const uint16_t* src = (row < scap) ? (key ? sk : sv) + (size_t)row * 128
-                                       : (key ? rk : rv) + (size_t)(row - scap) * 128;
-    uint8_t* dst = key ? stk + t * kTierRowK + 16 * ch : stv + t * kTierRowV + 16 * ch;
-    cp_async16(dst, reinterpret_cast<const uint8_t*>(src) + 16 * ch);
-  }
-  cp_async_commit();
-  float* sq = sm + S::sq;
+  auto stage_rows = [&](int r0, int r1) {   // storage rows [r0, r1) of [sink slots | recent ring]
+    for (int i = threadIdx.x; i < (r1 - r0) * 32; i += NW * 32) {
+      const int t = i >> 5, c = i & 31, key = c < 16, ch = c & 15, row = r0 + t;
+      const uint16_t* src = (row < scap) ? (key ? sk : sv) + (size_t)row * 128
+                                         : (key ? rk : rv) + (size_t)(row - scap) * 128;
+      uint8_t* dst = key ? stk + t * kTierRowK + 16 * ch : stv + t * kTierRowV + 16 * ch;
+      cp_async16(dst, reinterpret_cast<const uint8_t*>(src) + 16 * ch);
+    }
+    cp_async_commit();
+  };
+  stage_rows(0, min(rows, kTierRows));   // before the lengths are known
   load_q<G, NW, kMulti>(a, b, g, sq, G);
   int ns = __ldg(a.sink_len + b), nr = __ldg(a.rec_len + b), rs = __ldg(a.rec_start + b);
-  cp_async_wait<0>();
-  __syncthreads();
   if (ns < 0 || ns > scap || nr < 0 || nr > rcap || rs < 0 || rs >= rcap) {
     if (threadIdx.x == 0) flag_error(a.err, KV_DEVERR_LENGTH);
     ns = max(0, min(ns, scap));
     nr = max(0, min(nr, rcap));
     rs = max(0, min(rs, rcap - 1));
   }
-  auto rows = [&](int u, const uint16_t*& kr, const uint16_t*& vr) -> bool {
-    bool live;
-    if (u < scap) {
-      live = u < ns;
-    } else {
-      int d = (u - scap) - rs;
-      d += (d < 0) ? rcap : 0;
-      live = d < nr;
-    }
-    kr = reinterpret_cast<const uint16_t*>(stk + (u - r0) * kTierRowK);
-    vr = reinterpret_cast<const uint16_t*>(stv + (u - r0) * kTierRowV);
-    return live;
-  };
   WarpAcc<G> st;
   st.init();
-  bf16_rows_attend<G, true>(sq, sm + S::sp + warp * 32 * G, r0 + 32 * warp, r1, 32 * NW, rows,
-                            a.scale_log2, st);
-  __syncthreads();   // staged rows are dead before the results reuse the region
-  warp_acc_to_smem<G>(st, sm + S::swo, sm + S::swm, sm + S::swl);
+  for (int r0 = 0; r0 < rows; r0 += kTierRows) {
+    const int r1 = min(rows, r0 + kTierRows);
+    if (r0 > 0) stage_rows(r0, r1);
+    cp_async_wait<0>();
+    __syncthreads();
+    auto rowfn = [&](int u, const uint16_t*& kr, const uint16_t*& vr) -> bool {
+      bool live;
+      if (u < scap) {
+        live = u < ns;
+      } else {
+        int d = (u - scap) - rs;
+        d += (d < 0) ? rcap : 0;
+        live = d < nr;
+      }
+      kr = reinterpret_cast<const uint16_t*>(stk + (u - r0) * kTierRowK);
+      vr = reinterpret_cast<const uint16_t*>(stv + (u - r0) * kTierRowV);
+      return live;
+    };
+    bf16_rows_attend<G, true>(sq, reinterpret_cast<float*>(smb + S::sp) + warp * 32 * G, r0 + 32 * warp, r1,
+                              32 * NW, rowfn, a.scale_log2, st);
+    __syncthreads();   // the staged rows are dead before they are replaced or reused
+  }
+  float* swo = reinterpret_cast<float*>(smb + S::swo);
+  float* swm = reinterpret_cast<float*>(smb + S::swm);
+  float* swl = reinterpret_cast<float*>(smb + S::swl);
+  float* tier_o = reinterpret_cast<float*>(smb + S::tier_o);
+  float* tier_m = reinterpret_cast<float*>(smb + S::tier_m);
+  float* tier_l = reinterpret_cast<float*>(smb + S::tier_l);
+  warp_acc_to_smem<G>(st, swo, swm, swl);
   __syncthreads();
-  merge_warps<G, NW>(sm + S::swo, sm + S::swm, sm + S::swl, sm + S::sqr, sm + S::smm, sm + S::sml);
-  write_partial<G, NW>(part, sm + S::sqr, sm + S::smm, sm + S::sml);
+  merge_warps<G, NW>(swo, swm, swl, tier_o, tier_m, tier_l);   // ends with a barrier
+
+  // ---- R_v^T (for the one back-rotation) into the staging area, now free ----
+  uint64_t* rbar = reinterpret_cast<uint64_t*>(smb + S::bar);
+  float* srv = reinterpret_cast<float*>(smb + S::rv);
+  if (threadIdx.x == 0) {
+    mbar_init(rbar, 1);
+    mbar_fence_init();
+    const float* R = a.RvT + (size_t)g * 128 * 128;
+    const uint64_t keep = l2_evict_last_policy();
+    mbar_expect_tx(rbar, 128 * 128 * 4);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) bulk_g2s_hint(srv + 4096 * c, R + 4096 * c, 16384, rbar, keep);
+  }
+
+  // ---- merge the history partials, in split order, batch by batch as the
+  // splits of a batch arrive (fixed batches: the arithmetic, and so the
+  // result, does not depend on arrival order) ----
+  constexpr int EPT = (G * 128 + NW * 32 - 1) / (NW * 32);   // output elements per thread
+  float M[EPT], L[EPT], O[EPT];
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    M[e] = kNegInf;
+    L[e] = 0.f;
+    O[e] = 0.f;
+  }
+  int* ctl = reinterpret_cast<int*>(smb + S::ctl);
+  unsigned* mask = a.arrive + seq_head * kMaskWords;
+  const float* pbase = a.ws + seq_head * a.n_split * G * kPart;
+  bool merged_all = true;
+  for (int s0 = 0; s0 < a.n_split; s0 += kMergeBatch) {
+    const int s1 = min(a.n_split, s0 + kMergeBatch);
+    if (threadIdx.x == 0) {   // wait (bounded) until splits s0 .. s1-1 have arrived
+      int done = 0;
+      for (int it = 0; it < a.merge_polls && !done; ++it) {
+        done = 1;
+        for (int s = s0; s < s1 && done; s += 32 - (s & 31)) {
+          const int n = min(s1 - s, 32 - (s & 31));
+          const unsigned want = (n == 32 ? ~0u : ((1u << n) - 1u)) << (s & 31);
+          done = (ld_acquire_u32(mask + (s >> 5)) & want) == want;
+        }
+        if (!done) __nanosleep(64);
+      }
+      ctl[0] = done;
+    }
+    __syncthreads();
+    const bool arrived = ctl[0] != 0;
+    __syncthreads();   // ctl is rewritten for the next batch
+    if (!arrived) {
+      merged_all = false;
+      break;
+    }
+#pragma unroll 1
+    for (int e = 0; e < EPT; ++e) {
+      const int idx = threadIdx.x + e * NW * 32;
+      if (idx >= G * 128) break;
+      const int hh = idx >> 7, c = idx & 127;
+      const float* ph = pbase + (size_t)hh * kPart;
+      float mv[kMergeBatch], lv[kMergeBatch], ov[kMergeBatch];
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const int s = s0 + u;
+        const float* pp = ph + (size_t)s * G * kPart;
+        const float2 ml = (s < s1) ? __ldcg(reinterpret_cast<const float2*>(pp)) : make_float2(kNegInf, 0.f);
+        mv[u] = ml.x;
+        lv[u] = ml.y;
+        ov[u] = (s < s1) ? __ldcg(pp + 4 + c) : 0.f;
+      }
+      float Mb = M[e];
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) Mb = fmaxf(Mb, mv[u]);
+      if (Mb != kNegInf) {
+        const float alpha = (M[e] == kNegInf) ? 0.f : exp2f(M[e] - Mb);
+        float Le = L[e] * alpha, Oe = O[e] * alpha;
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+          const float f = (mv[u] == kNegInf) ? 0.f : exp2f(mv[u] - Mb);
+          Le = fmaf(f, lv[u], Le);
+          Oe = fmaf(f, ov[u], Oe);
+        }
+        M[e] = Mb;
+        L[e] = Le;
+        O[e] = Oe;
+      }
+    }
+  }
+  if (!merged_all && threadIdx.x == 0) flag_error(a.err, KV_DEVERR_TIMEOUT);
+
+  // ---- back to the original basis once: o_hist[h][c] = sum_i o'[h][i] R_v^T[i][c].
+  // o' goes to shared memory transposed ([c][GP]); each row of R_v^T is read
+  // once for all heads: warp w takes rows w, w + NW, .., lane cq columns
+  // 4cq..4cq+3, and the NW row-slice sums are added at the end ----
+  constexpr int GP = S::GP;
+  float* oT = reinterpret_cast<float*>(smb + S::oh);
+  float* spr = reinterpret_cast<float*>(smb + S::spr);
+  float* hist_m = reinterpret_cast<float*>(smb + S::hist_m);
+  float* hist_l = reinterpret_cast<float*>(smb + S::hist_l);
+  for (int idx = threadIdx.x; idx < GP * 128; idx += NW * 32)
+    if ((idx >> 7) >= G) oT[(idx & 127) * GP + (idx >> 7)] = 0.f;   // padded heads
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    const int idx = threadIdx.x + e * NW * 32;
+    if (idx < G * 128) {
+      oT[(idx & 127) * GP + (idx >> 7)] = O[e];
+      if ((idx & 127) == 0) {
+        hist_m[idx >> 7] = M[e];
+        hist_l[idx >> 7] = L[e];
+      }
+    }
+  }
+  if (!mbar_wait(rbar, 0, a.wait_polls) && (threadIdx.x & 31) == 0) flag_error(a.err, KV_DEVERR_TIMEOUT);
+  __syncthreads();
+  {
+    const int cq = threadIdx.x & 31;
+    float acc[GP][4];
+#pragma unroll
+    for (int hh = 0; hh < GP; ++hh) acc[hh][0] = acc[hh][1] = acc[hh][2] = acc[hh][3] = 0.f;
+#pragma unroll 4
+    for (int i = warp; i < 128; i += NW) {   // rows of R_v^T: warp, warp + NW, ..
+      const float4 rr = *reinterpret_cast<const float4*>(srv + i * 128 + 4 * cq);
+#pragma unroll
+      for (int hq = 0; hq < GP / 4; ++hq) {
+        const float4 o = *reinterpret_cast<const float4*>(oT + i * GP + 4 * hq);
+        const float ox[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float* d = acc[4 * hq + e];
+          d[0] = fmaf(ox[e], rr.x, d[0]); d[1] = fmaf(ox[e], rr.y, d[1]);
+          d[2] = fmaf(ox[e], rr.z, d[2]); d[3] = fmaf(ox[e], rr.w, d[3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh)
+      *reinterpret_cast<float4*>(spr + (warp * G + hh) * 128 + 4 * cq) =
+          make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
+    const int hh = idx >> 7, c = idx & 127;
+    float oh = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) oh += spr[w * G * 128 + idx];
+    const float Mh = hist_m[hh], Lh = hist_l[hh], mt = tier_m[hh], lt = tier_l[hh];
+    const float Mx = fmaxf(Mh, mt);
+    const float fh = (Mh == kNegInf) ? 0.f : exp2f(Mh - Mx);
+    const float ft = (mt == kNegInf) ? 0.f : exp2f(mt - Mx);
+    const float Lt = fmaf(Lh, fh, lt * ft);
+    const float val = (Lt > 0.f) ? fmaf(oh, fh, tier_o[idx] * ft) / Lt : 0.f;
+    if constexpr (kMulti) {
+      const size_t row = ((size_t)b * a.T + hh / a.Gq) * a.Hq + g * a.Gq + hh % a.Gq;
+      a.out[row * 128 + c] = val;
+      // ln sum exp(scaled score) = ln 2 * (M + log2 L), the scores being in log2 units
+      if (a.lse && c == 0) a.lse[row] = (Lt > 0.f) ? 0.6931471805599453f * (Mx + log2f(Lt)) : kNegInf;
+    } else {
+      a.out[((size_t)b * a.Hq + g * G + hh) * 128 + c] = val;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < kMaskWords) mask[threadIdx.x] = 0u;   // ready for the next call
+  if (threadIdx.x == 0) mbar_inval(rbar);
 }
 
 template <int G, int GS, bool kMulti>
 __global__ void __launch_bounds__(int2_warps(G) * 32, 1) decode_int2_kernel(DecodeArgs a) {
-  constexpr int NW = int2_warps(G);
   extern __shared__ float4 smem4[];
-  float* sm = reinterpret_cast<float*>(smem4);
+  uint8_t* smb = reinterpret_cast<uint8_t*>(smem4);
   // launch order: every history split first ((sequence, KV head) pairs in
-  // turn, their splits together), then every tier CTA, so that on a grid of
-  // several waves the short tier CTAs fill the last wave
-  const int nparts = a.n_split + a.n_tier;
+  // turn, their splits together), then the tier CTAs, which wait for the
+  // history splits of their pair (earlier in launch order) and merge them
   const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
   const int n_hist = a.n_split * gridDim.y * gridDim.z;
-  int split, pair;
   if (lin < n_hist) {
-    split = lin % a.n_split;
-    pair = lin / a.n_split;
+    const int split = lin % a.n_split, pair = lin / a.n_split;
+    const int g = pair % a.Hkv, b = pair / a.Hkv;
+    float* part = a.ws + ((size_t)pair * a.n_split + split) * G * kPart;
+    int2_history<G, GS, kMulti>(a, b, g, split, smb, part);
+    __syncthreads();   // the partial is written before the release below
+    if (threadIdx.x == 0) {
+      unsigned* m = a.arrive + (size_t)pair * kMaskWords + (split >> 5);
+      asm volatile("red.release.gpu.global.or.b32 [%0], %1;" ::"l"(m), "r"(1u << (split & 31)) : "memory");
+    }
   } else {
-    split = a.n_split + (lin - n_hist) % a.n_tier;
-    pair = (lin - n_hist) / a.n_tier;
+    const int pair = lin - n_hist;
+    tier_merge<G, GS, kMulti>(a, pair / a.Hkv, pair % a.Hkv, smb);
   }
-  const int g = pair % a.Hkv, b = pair / a.Hkv;
-  float* part = a.ws + ((size_t)(b * a.Hkv + g) * nparts + split) * G * kPart;
-  if (split < a.n_split)
-    int2_history<G, GS, kMulti>(a, b, g, split, sm, part);
-  else
-    bf16_tiers<G, GS, kMulti>(a, b, g, split - a.n_split, sm, part);
-  if (last_to_arrive(a.tickets + b * a.Hkv + g, (unsigned)nparts))
-    merge_parts<G, NW, kMulti>(a, b, g, nparts, sm);
 }
 
 // ---------------------------------------------------------------------------
@@ -1120,7 +1416,7 @@ __device__ void final_combine_plain(const DecodeArgs& a, int b, int g, int npart
 template <int G>
 __global__ void __launch_bounds__(kBf16Warps * 32, 2) decode_bf16_kernel(DecodeArgs a) {
   constexpr int NW = kBf16Warps;
-  using S = Lay<G, 128, NW, false>;
+  using S = Lay<G, NW>;
   extern __shared__ float4 smem4[];
   float* sm = reinterpret_cast<float*>(smem4);
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -1186,13 +1482,9 @@ int prepare_kernel(K kernel, int threads, size_t smem, bool& done, int& per_sm) 
   return per_sm;
 }
 
-template <int G, int GS>
-constexpr size_t int2_smem() {
-  return sizeof(float) * Lay<G, GS, int2_warps(G), true>::total;
-}
 template <int G>
 constexpr size_t bf16_smem() {
-  return sizeof(float) * Lay<G, 128, kBf16Warps, false>::total;
+  return sizeof(float) * Lay<G, kBf16Warps>::total;
 }
 
 template <int G, int GS, bool kMulti>
@@ -1210,12 +1502,36 @@ int bf16_blocks_per_sm() {
   return prepare_kernel(decode_bf16_kernel<G>, kBf16Warps * 32, bf16_smem<G>(), done, per_sm);
 }
 
+// A grid of one wave forms q' in every history CTA (one launch); a grid of
+// several waves gets q' from the pre-pass, once per (sequence, KV head), and
+// the decode kernel is launched as its programmatic dependent.
 template <int G, int GS, bool kMulti>
-cudaError_t launch_int2_t(const DecodeArgs& a, int B, cudaStream_t s) {
-  if (int2_blocks_per_sm<G, GS, kMulti>() < 0) return cudaErrorInvalidConfiguration;
-  dim3 grid(a.n_split + a.n_tier, a.Hkv, B);
-  decode_int2_kernel<G, GS, kMulti><<<grid, int2_warps(G) * 32, int2_smem<G, GS>(), s>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_int2_t(DecodeArgs a, int B, int sm_count, cudaStream_t s) {
+  const int per_sm = int2_blocks_per_sm<G, GS, kMulti>();
+  if (per_sm < 0) return cudaErrorInvalidConfiguration;
+  const long long ctas = (long long)(a.n_split + 1) * a.Hkv * B;
+  const bool multi_wave = ctas > (long long)per_sm * sm_count;
+  a.qmode = multi_wave ? kQPre : kQLocal;
+  if (!multi_wave) {
+    decode_int2_kernel<G, GS, kMulti><<<dim3(a.n_split + 1, a.Hkv, B), int2_warps(G) * 32, int2_smem<G, GS>(),
+                                        s>>>(a);
+    return cudaGetLastError();
+  }
+  constexpr int SPB = 16 / ((G <= 4) ? 4 : 8);   // sequences per pre-pass CTA
+  qprep_kernel<G, GS, kMulti><<<dim3(a.Hkv, (B + SPB - 1) / SPB), 256, 0, s>>>(a, B);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_split + 1, a.Hkv, B);
+  cfg.blockDim = dim3(int2_warps(G) * 32);
+  cfg.dynamicSmemBytes = int2_smem<G, GS>();
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_int2_kernel<G, GS, kMulti>, a);
 }
 
 template <int G>
@@ -1245,6 +1561,8 @@ DecodeArgs base_args(const Pool& p, int layer, const void* q, const int32_t* pt,
   a.Gq = p.G;
   a.lse = nullptr;
   a.wait_polls = p.test_wait_polls > 0 ? p.test_wait_polls : kWaitPolls;
+  a.merge_polls = kMergePolls;
+  a.arrive = p.arrive + (size_t)layer * p.cfg.max_seqs * p.cfg.num_kv_heads * kMaskWords;
   a.stall_first_copy = p.test_stall_first_copy;
   return a;
 }
@@ -1344,9 +1662,14 @@ static DecodePlan make_plan(const Pool& p, int G, int B, int units, int max_per,
 DecodePlan plan_decode_int2(const Pool& p, int B, int max_hist_len, int T) {
   const int G = T * p.G;   // query columns per KV head
   const int tiles = (max(max_hist_len, 0) + kTile - 1) / kTile;
-  const int n_tier = max(1, (p.cfg.sink_tokens + p.cfg.recent_tokens + kTierRows - 1) / kTierRows);
   const int per_sm = (T > 1) ? int2_occupancy_t<true>(p, G) : int2_occupancy_t<false>(p, G);
-  DecodePlan pl = make_plan(p, G, B, tiles, 64 * int2_warps(G), n_tier, per_sm);
+  // one tier CTA per (sequence, KV head) beside the history splits; partials
+  // are kept for the history splits only, followed by the q' fragments
+  DecodePlan pl = make_plan(p, G, B, tiles, 64 * int2_warps(G), 1, per_sm);
+  const size_t pairs = (size_t)B * p.cfg.num_kv_heads;
+  pl.partial_floats = pairs * pl.n_split * G * kPart;
+  const size_t qwords = pairs * 32 * (G <= 4 ? qfrag_words<4>() : qfrag_words<8>());
+  pl.bytes = pl.partial_floats * sizeof(float) + qwords * sizeof(uint32_t);
   pl.max_len = max(max_hist_len, 0);
   return pl;
 }
@@ -1387,21 +1710,22 @@ cudaError_t launch_decode_int2(const Pool& p, int layer, int B, const void* q,
   a.per_split = plan.tiles_per_split;
   a.n_tier = plan.n_tier;
   a.max_len = plan.max_len;
+  a.qfrag = reinterpret_cast<uint32_t*>(a.ws + plan.partial_floats);
   const bool g64 = p.cfg.group_size == 64;
   if (T > 1 || lse) {   // several queries per sequence, or the log-sum-exp wanted
     switch (T * p.G) {
-      case 1: return g64 ? launch_int2_t<1, 64, true>(a, B, s) : launch_int2_t<1, 128, true>(a, B, s);
-      case 2: return g64 ? launch_int2_t<2, 64, true>(a, B, s) : launch_int2_t<2, 128, true>(a, B, s);
-      case 4: return g64 ? launch_int2_t<4, 64, true>(a, B, s) : launch_int2_t<4, 128, true>(a, B, s);
-      case 8: return g64 ? launch_int2_t<8, 64, true>(a, B, s) : launch_int2_t<8, 128, true>(a, B, s);
+      case 1: return g64 ? launch_int2_t<1, 64, true>(a, B, p.sm_count, s) : launch_int2_t<1, 128, true>(a, B, p.sm_count, s);
+      case 2: return g64 ? launch_int2_t<2, 64, true>(a, B, p.sm_count, s) : launch_int2_t<2, 128, true>(a, B, p.sm_count, s);
+      case 4: return g64 ? launch_int2_t<4, 64, true>(a, B, p.sm_count, s) : launch_int2_t<4, 128, true>(a, B, p.sm_count, s);
+      case 8: return g64 ? launch_int2_t<8, 64, true>(a, B, p.sm_count, s) : launch_int2_t<8, 128, true>(a, B, p.sm_count, s);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (p.G) {
-    case 1: return g64 ? launch_int2_t<1, 64, false>(a, B, s) : launch_int2_t<1, 128, false>(a, B, s);
-    case 2: return g64 ? launch_int2_t<2, 64, false>(a, B, s) : launch_int2_t<2, 128, false>(a, B, s);
-    case 4: return g64 ? launch_int2_t<4, 64, false>(a, B, s) : launch_int2_t<4, 128, false>(a, B, s);
-    case 8: return g64 ? launch_int2_t<8, 64, false>(a, B, s) : launch_int2_t<8, 128, false>(a, B, s);
+    case 1: return g64 ? launch_int2_t<1, 64, false>(a, B, p.sm_count, s) : launch_int2_t<1, 128, false>(a, B, p.sm_count, s);
+    case 2: return g64 ? launch_int2_t<2, 64, false>(a, B, p.sm_count, s) : launch_int2_t<2, 128, false>(a, B, p.sm_count, s);
+    case 4: return g64 ? launch_int2_t<4, 64, false>(a, B, p.sm_count, s) : launch_int2_t<4, 128, false>(a, B, p.sm_count, s);
+    case 8: return g64 ? launch_int2_t<8, 64, false>(a, B, p.sm_count, s) : launch_int2_t<8, 128, false>(a, B, p.sm_count, s);
     default: return cudaErrorInvalidValue;
   }
 }

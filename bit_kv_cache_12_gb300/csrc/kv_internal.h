@@ -12,6 +12,7 @@ namespace kvint2 {
 constexpr int kHeadDim = 128;
 constexpr int kTile = 16;           // tokens per INT2 history tile
 constexpr int kCodeBlock = 512;     // bytes of K (or V) codes per tile
+constexpr int kMaskWords = 16;      // arrival-mask words per (sequence, KV head): 512 history splits
 
 struct Pool {
   kv_pool_config_t cfg;
@@ -38,7 +39,8 @@ struct Pool {
   float* RvT = nullptr;             // [layer][Hkv][128][128]  RvT[i][c] = Rv[c][i]
   float* clip = nullptr;            // [layer][2][Hkv][128]
   uint4* rfrag = nullptr;           // [layer][Hkv][kFragBlocks][4096] rotation operands (below)
-  unsigned* tickets = nullptr;      // [layer][max_seqs][Hkv] split-merge counters
+  unsigned* tickets = nullptr;      // [layer][max_seqs][Hkv] split-merge counters (BF16 decode)
+  unsigned* arrive = nullptr;       // [layer][max_seqs][Hkv][kMaskWords] arrival masks (INT2 decode)
   unsigned* step_tickets = nullptr; // [layer][ceil(max_seqs / 128)] per-step placement counters
   int* err = nullptr;               // device error word
 

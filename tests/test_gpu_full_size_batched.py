@@ -74,6 +74,8 @@ def test_split_bound_multi_wave(G, P, B, lo, hi):
     pool = native.KVPool(native.KV_POOL_INT2_3TIER, 1, c.Hq, Hkv, P, 4, B)
     per_part = ws(pool.handle, B, int(c.hist_len.max()))
     pool.close()
-    # 2 history splits + 1 tier CTA per (sequence, KV head): the first split holds 64 tiles per warp
-    assert per_part == B * Hkv * 3 * G * 132 * 4
+    # 2 history splits per (sequence, KV head), the first with 64 tiles per warp:
+    # their partials (132 floats per query head), then the q' fragments
+    qwords = 32 * (16 * (1 if G <= 4 else 2) + 4)
+    assert per_part == B * Hkv * (2 * G * 132 * 4 + qwords * 4)
     _check(c, [(0, 0), (B // 2, 1), (B - 1, 0), (B - 1, 1), (int(np.argmax(c.hist_len)), 1)])
