@@ -265,7 +265,7 @@ kv_status_t kv_append_step(kv_pool_t* pool, int32_t layer, int32_t B, const void
 }
 
 size_t kv_decode_workspace_bytes(const kv_pool_t* pool, int32_t B, int32_t max_len) {
-  if (!pool || B <= 0 || max_len < 0 || B > pool->p.cfg.max_seqs) return 0;
+  if (!pool || B <= 0 || max_len < 0 || max_len > kvint2::kMaxDecodeLen || B > pool->p.cfg.max_seqs) return 0;
   const Pool& p = pool->p;
   kvint2::DecodePlan pl = p.cfg.kind == KV_POOL_INT2_3TIER ? kvint2::plan_decode_int2(p, B, max_len)
                                                            : kvint2::plan_decode_bf16(p, B, max_len);
@@ -285,7 +285,8 @@ kv_status_t kv_decode_attention(kv_pool_t* pool, int32_t layer, int32_t B, const
   if (!q || !sink_len || !hist_len || !recent_len || !recent_start || !page_table || !out ||
       !workspace)
     return KV_ERR_INVALID_ARG;
-  if ((int64_t)max_hist_len > (int64_t)max_pages_per_seq * p.cfg.page_size) return KV_ERR_INVALID_ARG;
+  if ((int64_t)max_hist_len > (int64_t)max_pages_per_seq * p.cfg.page_size || max_hist_len > kvint2::kMaxDecodeLen)
+    return KV_ERR_INVALID_ARG;
   if (((uintptr_t)workspace & 15) || ((uintptr_t)q & 1)) return KV_ERR_INVALID_ARG;
   kvint2::DecodePlan pl = kvint2::plan_decode_int2(p, B, max_hist_len);
   if (workspace_bytes < pl.bytes) return KV_ERR_INVALID_ARG;
@@ -307,7 +308,8 @@ kv_status_t kv_decode_attention_noalloc(kv_pool_t* pool, int32_t layer, int32_t 
   if (p.cfg.kind != KV_POOL_INT2_3TIER || B > p.cfg.max_seqs) return KV_ERR_INVALID_ARG;
   if (!q || !sink_len || !hist_len || !recent_len || !recent_start || !page_table || !out)
     return KV_ERR_INVALID_ARG;
-  if ((int64_t)max_hist_len > (int64_t)max_pages_per_seq * p.cfg.page_size) return KV_ERR_INVALID_ARG;
+  if ((int64_t)max_hist_len > (int64_t)max_pages_per_seq * p.cfg.page_size || max_hist_len > kvint2::kMaxDecodeLen)
+    return KV_ERR_INVALID_ARG;
   if ((uintptr_t)q & 1) return KV_ERR_INVALID_ARG;
   // the scratch buffer looked up below is the current device's: it must be the pool's
   int cur = -1;
@@ -369,7 +371,8 @@ kv_status_t kv_decode_attention_multi(kv_pool_t* pool, int32_t layer, int32_t B,
   if (!q || !sink_len || !hist_len || !recent_len || !recent_start || !page_table || !out ||
       !workspace)
     return KV_ERR_INVALID_ARG;
-  if ((int64_t)max_hist_len > (int64_t)max_pages_per_seq * p.cfg.page_size) return KV_ERR_INVALID_ARG;
+  if ((int64_t)max_hist_len > (int64_t)max_pages_per_seq * p.cfg.page_size || max_hist_len > kvint2::kMaxDecodeLen)
+    return KV_ERR_INVALID_ARG;
   if (((uintptr_t)workspace & 15) || ((uintptr_t)q & 1) || ((uintptr_t)lse & 3)) return KV_ERR_INVALID_ARG;
   kvint2::DecodePlan pl = kvint2::plan_decode_int2(p, B, max_hist_len, T);
   if (workspace_bytes < pl.bytes) return KV_ERR_INVALID_ARG;
@@ -378,6 +381,8 @@ kv_status_t kv_decode_attention_multi(kv_pool_t* pool, int32_t layer, int32_t B,
                                                 softmax_scale, out, workspace,
                                                 static_cast<cudaStream_t>(stream), T, lse));
 }
+
+static_assert(kvint2::kMaxDecodeLen == KV_MAX_DECODE_LEN, "one decode length bound");
 
 kv_status_t kv_decode_attention_bf16(kv_pool_t* pool, int32_t layer, int32_t B, const void* q,
                                      const int32_t* seq_len, const int32_t* page_table,
@@ -389,7 +394,8 @@ kv_status_t kv_decode_attention_bf16(kv_pool_t* pool, int32_t layer, int32_t B, 
   const Pool& p = pool->p;
   if (p.cfg.kind != KV_POOL_BF16 || B > p.cfg.max_seqs) return KV_ERR_INVALID_ARG;
   if (!q || !seq_len || !page_table || !out || !workspace) return KV_ERR_INVALID_ARG;
-  if ((int64_t)max_seq_len > (int64_t)max_pages_per_seq * p.cfg.page_size) return KV_ERR_INVALID_ARG;
+  if ((int64_t)max_seq_len > (int64_t)max_pages_per_seq * p.cfg.page_size || max_seq_len > kvint2::kMaxDecodeLen)
+    return KV_ERR_INVALID_ARG;
   if (((uintptr_t)workspace & 15) || ((uintptr_t)q & 1)) return KV_ERR_INVALID_ARG;
   kvint2::DecodePlan pl = kvint2::plan_decode_bf16(p, B, max_seq_len);
   if (workspace_bytes < pl.bytes) return KV_ERR_INVALID_ARG;

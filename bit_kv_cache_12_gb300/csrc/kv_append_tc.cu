@@ -628,18 +628,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   tc_body<GS, TENSOR>(a, &xmap, sm);
 }
 
-// cuTensorMapEncodeTiled from the driver, looked up once
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      f = nullptr;
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }();
-  return fn;
+  return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
 }
 
 
@@ -902,6 +892,20 @@ __global__ void __launch_bounds__(kTcThreads, 2) evict_tc_kernel(StepArgs a, int
 }
 
 }  // namespace
+
+// cuTensorMapEncodeTiled from the driver, looked up once
+void* tensor_map_encode_fn() {
+  static void* fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return f;
+  }();
+  return fn;
+}
 
 cudaError_t launch_append_tc(const Pool& p, int layer, int n_seqs, const void* k, const void* v,
                              const int32_t* cu, const int32_t* hist_start, const int32_t* pt,

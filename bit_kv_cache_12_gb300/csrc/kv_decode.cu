@@ -41,6 +41,9 @@
 //     sequence, the log-sum-exp).
 #include <math.h>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <atomic>
 #include <type_traits>
 
@@ -70,6 +73,8 @@ constexpr int kBf16Warps = 8;
 __host__ __device__ constexpr int int2_warps(int G) { return G <= 4 ? 16 : 12; }
 // a split covers at most 64 tiles per warp, and its page ids (one per tile at
 // page 16) are staged in shared memory
+static_assert((long long)kMaxParts * (kMaxPids - 8) * kTile >= kMaxDecodeLen,
+              "a decode of the longest length stages at most kMaxPids - 8 page ids per split");
 static_assert(64 * int2_warps(1) <= kMaxPids && 64 * int2_warps(8) <= kMaxPids,
               "a split's page ids must fit the staging array");
 static_assert(kMaxParts <= 32 * kMaskWords, "every split has a bit in the arrival mask");
@@ -1413,14 +1418,74 @@ __device__ void final_combine_plain(const DecodeArgs& a, int b, int g, int npart
   if (threadIdx.x == 0) a.tickets[b * a.Hkv + g] = 0u;   // ready for the next call
 }
 
+// A warp's ring stage holds one 16-token tile of K and of V: four TMA boxes of
+// 16 rows x 64 channels (2 KB each, 128-byte swizzle: the 16-byte chunk c of
+// row r sits at chunk position c ^ (r % 8), so the ldmatrix reads below are
+// conflict-free): [K 0-63][K 64-127][V 0-63][V 64-127].
+constexpr int kBfStages = 3;
+constexpr int kBfStage = 8192;
+
 template <int G>
-__global__ void __launch_bounds__(kBf16Warps * 32, 2) decode_bf16_kernel(DecodeArgs a) {
+struct BfLay {
+  static constexpr int NW = kBf16Warps;
+  static constexpr int ring = 0;                                  // [NW][kBfStages][kBfStage]
+  static constexpr int bars = ring + NW * kBfStages * kBfStage;   // [NW][kBfStages] mbarriers
+  static constexpr int spid = bars + NW * kBfStages * 8;          // [kMaxPids] page ids
+  static constexpr int total = spid + kMaxPids * 4 + 1024;        // + slack to align the ring to 1 KB
+  // after the loop, over the ring: per-warp results, then the final merge
+  static constexpr int swo = 0;                                   // [NW][G][128]
+  static constexpr int swm = swo + NW * G * 128 * 4;              // [NW][G]
+  static constexpr int swl = swm + NW * G * 4;                    // [NW][G]
+  static_assert(swl + NW * G * 4 <= bars, "warp results fit in the ring");
+  static_assert((16 + 2 * NW * 128 + 2 * kMaxParts * G) * 4 <= bars, "the final merge fits in the ring");
+};
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// one 2D TMA box (x = channel, y = row) of `map` into shared memory, completing on `bar`
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+// (hi, lo) bf16 split of an fp32 weight as one bf16x2 register: low half
+// bf16(x), high half bf16(x - bf16(x))
+__device__ __forceinline__ uint32_t split_hi_lo_bf16(float x) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+  return (uint32_t)__bfloat16_as_ushort(hi) | ((uint32_t)__bfloat16_as_ushort(lo) << 16);
+}
+
+// Plain split-K attention over the all-BF16 pool.  Each warp streams its
+// 16-token tiles of K and V by TMA through a ring in shared memory; QK runs
+// on the tensor cores with q exact in bf16 (B column 2h holds head h, column
+// 2h + 1 is zero), PV with the softmax weights as bf16 hi + lo (about 16
+// significant bits) in columns 2h and 2h + 1; online softmax per head as in
+// the INT2 loop.  The splits merge with the log-sum-exp rule in the CTA that
+// takes the last ticket.
+template <int G>
+__global__ void __launch_bounds__(kBf16Warps * 32, 1)
+    decode_bf16_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
+                       const __grid_constant__ CUtensorMap vmap) {
   constexpr int NW = kBf16Warps;
-  using S = Lay<G, NW>;
-  extern __shared__ float4 smem4[];
-  float* sm = reinterpret_cast<float*>(smem4);
+  constexpr int NT = (G <= 4) ? 1 : 2;   // 8-column n-tiles: 4 heads each
+  using S = BfLay<G>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smb = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  float* sm = reinterpret_cast<float*>(smb);
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r = lane >> 2, j = lane & 3;
   const int nparts = a.n_split;
   float* part = a.ws + ((size_t)(b * a.Hkv + g) * nparts + split) * G * kPart;
   int n = a.seq_len[b];
@@ -1429,37 +1494,203 @@ __global__ void __launch_bounds__(kBf16Warps * 32, 2) decode_bf16_kernel(DecodeA
     if (threadIdx.x == 0) flag_error(a.err, KV_DEVERR_LENGTH);
     n = max(0, min(n, cap));
   }
-  const int u0 = split * a.per_split, u1 = min(n, u0 + a.per_split);
-  if (u0 >= u1) {
+  const int ntiles = (n + kTile - 1) / kTile;
+  const int t_begin = split * a.per_split, t_end = min(ntiles, t_begin + a.per_split);
+  if (t_begin >= t_end) {
     write_empty_partial<G, NW>(part);
   } else {
-    const int P = a.page_size;
-    const int p_begin = u0 / P, p_count = (u1 - 1) / P + 1 - p_begin;
-    int* spid = reinterpret_cast<int*>(sm + S::spid);
+    uint8_t* ring = smb + S::ring + (size_t)warp * kBfStages * kBfStage;
+    uint64_t* wbar = reinterpret_cast<uint64_t*>(smb + S::bars) + warp * kBfStages;
+    int* spid = reinterpret_cast<int*>(smb + S::spid);
+    if (lane < kBfStages) mbar_init(wbar + lane, 1);
+    mbar_fence_init();
+    const int tpp = a.page_size / kTile;   // tiles per page
+    const int p_begin = t_begin / tpp, p_count = (t_end - 1) / tpp + 1 - p_begin;
     const int32_t* ptrow = a.pt + (size_t)b * a.max_pages;
     for (int i = threadIdx.x; i < p_count; i += NW * 32) spid[i] = __ldg(ptrow + p_begin + i);
-    float* sq = sm + S::sq;
-    load_q<G, NW>(a, b, g, sq, G);
-    __syncthreads();   // publishes q and the page ids
-    auto rows = [&](int u, const uint16_t*& kr, const uint16_t*& vr) -> bool {
-      const int pid = spid[u / P - p_begin];
-      if (pid < 0 || pid >= a.num_pages) {
-        flag_error(a.err, KV_DEVERR_PAGE_ID);
-        return false;
+    // QK B fragments straight from q (bf16 bits): column n = r of n-tile u is head 4u + r/2 when r is even
+    uint32_t qf[8][NT][2];
+    {
+      const int hh = r >> 1;
+#pragma unroll
+      for (int u = 0; u < NT; ++u) {
+        const int head = 4 * u + hh;
+        const bool live = !(r & 1) && head < G;
+        const uint32_t* qrow =
+            reinterpret_cast<const uint32_t*>(a.q + ((size_t)b * a.Hq + g * G + (live ? head : 0)) * 128);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          qf[s][u][0] = live ? __ldg(qrow + 8 * s + j) : 0u;       // channels 16s + 2j, +1
+          qf[s][u][1] = live ? __ldg(qrow + 8 * s + 4 + j) : 0u;   // channels 16s + 2j + 8, +9
+        }
       }
-      const size_t off = (((size_t)pid * a.Hkv + g) * P + (u % P)) * 128;
-      kr = a.bk + off;
-      vr = a.bv + off;
-      return true;
+    }
+    __syncthreads();   // page ids in shared memory, barriers initialised
+    // tile t -> its 16 rows of the pool, viewed as [num_pages * Hkv * page_size][128];
+    // a bad page id reads page 0 and its tokens are masked
+    auto tile_row = [&](int t, bool& valid) -> int {
+      const int pid = spid[t / tpp - p_begin];
+      valid = pid >= 0 && pid < a.num_pages;
+      return (int)(((long long)(valid ? pid : 0) * a.Hkv + g) * a.page_size + (t % tpp) * kTile);
     };
-    WarpAcc<G> st;
-    st.init();
-    bf16_rows_attend<G, false>(sq, sm + S::sp + warp * 32 * G, u0 + 32 * warp, u1, 32 * NW, rows,
-                               a.scale_log2, st);
-    warp_acc_to_smem<G>(st, sm + S::swo, sm + S::swm, sm + S::swl);
-    __syncthreads();
-    merge_warps<G, NW>(sm + S::swo, sm + S::swm, sm + S::swl, sm + S::sqr, sm + S::smm, sm + S::sml);
-    write_partial<G, NW>(part, sm + S::sqr, sm + S::smm, sm + S::sml);
+    auto issue = [&](int t, int st) {
+      if (t < t_end && lane == 0) {
+        bool valid;
+        const int row = tile_row(t, valid);
+        const uint32_t dst = smem_u32(ring + st * kBfStage);
+        mbar_expect_tx(wbar + st, kBfStage);
+        tma_load_2d(dst, &kmap, 0, row, wbar + st);
+        tma_load_2d(dst + 2048, &kmap, 64, row, wbar + st);
+        tma_load_2d(dst + 4096, &vmap, 0, row, wbar + st);
+        tma_load_2d(dst + 6144, &vmap, 64, row, wbar + st);
+      }
+    };
+#pragma unroll
+    for (int st = 0; st < kBfStages - 1; ++st) issue(t_begin + warp + NW * st, st);
+    int issued = min(kBfStages - 1, (t_end - t_begin - warp + NW - 1) / NW);
+
+    float m_run[NT], base[NT], l_run[NT], oacc[8][NT][4];
+#pragma unroll
+    for (int u = 0; u < NT; ++u) {
+      m_run[u] = kNegInf;
+      base[u] = 0.f;
+      l_run[u] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) oacc[i][u][0] = oacc[i][u][1] = oacc[i][u][2] = oacc[i][u][3] = 0.f;
+    }
+    // ldmatrix row / chunk of this lane: K (A of QK): row lane%16, chunk + lane/16;
+    // V (A of PV, transposed): row lane%8 + 8 (lane/16), chunk + (lane/8)%2
+    const int krow = lane & 15, kc = lane >> 4;
+    const int vrow = (lane & 7) + 8 * (lane >> 4), vc = (lane >> 3) & 1;
+    int k = 0;
+    bool ok = true;
+    for (int t = t_begin + warp; t < t_end; t += NW, ++k) {
+      __syncwarp();   // every lane is done with the stage refilled next
+      issue(t + NW * (kBfStages - 1), (k + kBfStages - 1) % kBfStages);
+      if (t + NW * (kBfStages - 1) < t_end) ++issued;
+      const int st = k % kBfStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(wbar + st, (k / kBfStages) & 1, a.wait_polls))) {
+        ok = false;
+        break;
+      }
+      const uint32_t sbase = smem_u32(ring + st * kBfStage);
+      bool valid;
+      tile_row(t, valid);
+      const int lim = valid ? n - t * kTile : 0;
+      const bool v0 = r < lim, v1 = r + 8 < lim;
+      if (lim < kTile) {
+        // V rows past the sequence (or of a bad page) are zeroed, so that a weight of
+        // zero never meets a stale non-finite value; the fence orders these writes
+        // before the stage's next copy
+        for (int idx = lane + 16 * max(lim, 0); idx < 16 * kTile; idx += 32) {
+          const int row = idx >> 4, c = idx & 15;
+          *reinterpret_cast<uint4*>(ring + st * kBfStage + 4096 + (c >> 3) * 2048 + row * 128 + (c & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+      }
+      // ---- QK ----
+      float sacc[NT][4];
+#pragma unroll
+      for (int u = 0; u < NT; ++u) sacc[u][0] = sacc[u][1] = sacc[u][2] = sacc[u][3] = 0.f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const int c = 2 * (s & 3) + kc;
+        uint32_t fa[4];
+        ldmatrix_x4(sbase + (s >> 2) * 2048 + krow * 128 + ((c ^ (krow & 7)) << 4), fa);
+#pragma unroll
+        for (int u = 0; u < NT; ++u) mma_bf16(sacc[u], fa[0], fa[1], fa[2], fa[3], qf[s][u][0], qf[s][u][1]);
+      }
+      // ---- softmax (column 2j: head 4u + j; column 2j + 1 is zero) and PV B fragments ----
+      uint32_t bpv[NT][2];
+#pragma unroll
+      for (int u = 0; u < NT; ++u) {
+        const float l0 = v0 ? sacc[u][0] * a.scale_log2 : kNegInf;
+        const float l1 = v1 ? sacc[u][2] * a.scale_log2 : kNegInf;
+        if (__any_sync(0xffffffffu, fmaxf(l0, l1) > m_run[u])) {
+          float tmax = fmaxf(l0, l1);
+          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+          const bool need = tmax > m_run[u];
+          const float mnew = need ? tmax + kSlack : m_run[u];
+          const float alpha = need ? ((m_run[u] == kNegInf) ? 0.f : exp2_neg(m_run[u] - mnew)) : 1.f;
+          m_run[u] = mnew;
+          base[u] = (mnew == kNegInf) ? 0.f : mnew;
+          l_run[u] *= alpha;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) oacc[i][u][e] *= alpha;
+        }
+        const float p0 = exp2_neg(l0 - base[u]), p1 = exp2_neg(l1 - base[u]);
+        l_run[u] += p0 + p1;
+        bpv[u][0] = movmatrix_t(split_hi_lo_bf16(p0));
+        bpv[u][1] = movmatrix_t(split_hi_lo_bf16(p1));
+      }
+      // ---- PV: value accumulator [channel][column] ----
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = 2 * (i & 3) + vc;
+        uint32_t fa[4];
+        ldmatrix_x4_t(sbase + 4096 + (i >> 2) * 2048 + vrow * 128 + ((c ^ (vrow & 7)) << 4), fa);
+#pragma unroll
+        for (int u = 0; u < NT; ++u) mma_bf16(oacc[i][u], fa[0], fa[1], fa[2], fa[3], bpv[u][0], bpv[u][1]);
+      }
+    }
+    if (!ok) {   // a copy did not arrive in time: wait (bounded) for the ones in flight
+      if (lane == 0) flag_error(a.err, KV_DEVERR_TIMEOUT);
+      for (int kk = k; kk < issued; ++kk) mbar_wait(wbar + kk % kBfStages, (kk / kBfStages) & 1, a.wait_polls);
+    }
+    ok = __syncthreads_and(ok);   // the ring is free before the results reuse it
+    if (lane < kBfStages) mbar_inval(wbar + lane);
+    if (!ok) {
+      write_empty_partial<G, NW>(part);
+    } else {
+      float* swo = reinterpret_cast<float*>(smb + S::swo);
+      float* swm = reinterpret_cast<float*>(smb + S::swm);
+      float* swl = reinterpret_cast<float*>(smb + S::swl);
+#pragma unroll
+      for (int u = 0; u < NT; ++u) {
+        const float l = warp_sum_xor(l_run[u], 4);
+        const int hh = 4 * u + j;
+        if (hh < G) {
+          float* o = swo + (warp * G + hh) * 128;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            o[16 * i + r] = oacc[i][u][0] + oacc[i][u][1];          // hi + lo columns
+            o[16 * i + r + 8] = oacc[i][u][2] + oacc[i][u][3];
+          }
+          if (r == 0) {
+            swm[warp * G + hh] = m_run[u];
+            swl[warp * G + hh] = l;
+          }
+        }
+      }
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
+        const int hh = idx >> 7, c = idx & 127;
+        float M = kNegInf;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, swm[w * G + hh]);
+        float L = 0.f, O = 0.f;
+        if (M != kNegInf) {
+#pragma unroll
+          for (int w = 0; w < NW; ++w) {
+            const float mw = swm[w * G + hh];
+            const float f = (mw == kNegInf) ? 0.f : exp2f(mw - M);
+            L = fmaf(f, swl[w * G + hh], L);
+            O = fmaf(f, swo[(w * G + hh) * 128 + c], O);
+          }
+        }
+        part[hh * kPart + 4 + c] = O;
+        if (c == 0) {
+          part[hh * kPart + 0] = M;
+          part[hh * kPart + 1] = L;
+        }
+      }
+    }
   }
   if (last_to_arrive(a.tickets + b * a.Hkv + g, (unsigned)nparts))
     final_combine_plain<G, NW>(a, b, g, nparts, sm);
@@ -1484,7 +1715,7 @@ int prepare_kernel(K kernel, int threads, size_t smem, bool& done, int& per_sm) 
 
 template <int G>
 constexpr size_t bf16_smem() {
-  return sizeof(float) * Lay<G, kBf16Warps>::total;
+  return BfLay<G>::total;
 }
 
 template <int G, int GS, bool kMulti>
@@ -1535,10 +1766,11 @@ cudaError_t launch_int2_t(DecodeArgs a, int B, int sm_count, cudaStream_t s) {
 }
 
 template <int G>
-cudaError_t launch_bf16_t(const DecodeArgs& a, int B, cudaStream_t s) {
+cudaError_t launch_bf16_t(const DecodeArgs& a, int B, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          cudaStream_t s) {
   if (bf16_blocks_per_sm<G>() < 0) return cudaErrorInvalidConfiguration;
   dim3 grid(a.n_split, a.Hkv, B);
-  decode_bf16_kernel<G><<<grid, kBf16Warps * 32, bf16_smem<G>(), s>>>(a);
+  decode_bf16_kernel<G><<<grid, kBf16Warps * 32, bf16_smem<G>(), s>>>(a, kmap, vmap);
   return cudaGetLastError();
 }
 
@@ -1675,7 +1907,9 @@ DecodePlan plan_decode_int2(const Pool& p, int B, int max_hist_len, int T) {
 }
 
 DecodePlan plan_decode_bf16(const Pool& p, int B, int max_len) {
-  DecodePlan pl = make_plan(p, p.G, B, max(max_len, 0), 8192, 0, bf16_occupancy(p));
+  // splits in 16-token tiles, at most 64 tiles per warp
+  const int tiles = (max(max_len, 0) + kTile - 1) / kTile;
+  DecodePlan pl = make_plan(p, p.G, B, tiles, 64 * kBf16Warps, 0, bf16_occupancy(p));
   pl.max_len = max(max_len, 0);
   return pl;
 }
@@ -1711,6 +1945,7 @@ cudaError_t launch_decode_int2(const Pool& p, int layer, int B, const void* q,
   a.n_tier = plan.n_tier;
   a.max_len = plan.max_len;
   a.qfrag = reinterpret_cast<uint32_t*>(a.ws + plan.partial_floats);
+  if (plan.tiles_per_split > kMaxPids - 8) return cudaErrorInvalidValue;   // page ids staged per CTA
   const bool g64 = p.cfg.group_size == 64;
   if (T > 1 || lse) {   // several queries per sequence, or the log-sum-exp wanted
     switch (T * p.G) {
@@ -1742,11 +1977,30 @@ cudaError_t launch_decode_bf16(const Pool& p, int layer, int B, const void* q,
   a.per_split = plan.tiles_per_split;
   a.n_tier = 0;
   a.max_len = plan.max_len;
+  if (plan.tiles_per_split > kMaxPids - 8) return cudaErrorInvalidValue;   // page ids staged per CTA
+  // K and V of the layer viewed as [num_pages * Hkv * page_size rows][128] bf16,
+  // boxes of 16 rows x 64 channels with the 128-byte swizzle
+  auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
+  if (!encode) return cudaErrorNotSupported;
+  const unsigned long long rows = (unsigned long long)p.cfg.num_pages * p.cfg.num_kv_heads * p.cfg.page_size;
+  if (rows >= (1ull << 31)) return cudaErrorInvalidValue;   // row coordinates are 32-bit
+  CUtensorMap maps[2];
+  const uint16_t* bases[2] = {a.bk, a.bv};
+  for (int t = 0; t < 2; ++t) {
+    const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {256};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kTile};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&maps[t], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(bases[t]), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   switch (p.G) {
-    case 1: return launch_bf16_t<1>(a, B, s);
-    case 2: return launch_bf16_t<2>(a, B, s);
-    case 4: return launch_bf16_t<4>(a, B, s);
-    case 8: return launch_bf16_t<8>(a, B, s);
+    case 1: return launch_bf16_t<1>(a, B, maps[0], maps[1], s);
+    case 2: return launch_bf16_t<2>(a, B, maps[0], maps[1], s);
+    case 4: return launch_bf16_t<4>(a, B, maps[0], maps[1], s);
+    case 8: return launch_bf16_t<8>(a, B, maps[0], maps[1], s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -12,6 +12,7 @@ namespace kvint2 {
 constexpr int kHeadDim = 128;
 constexpr int kTile = 16;           // tokens per INT2 history tile
 constexpr int kCodeBlock = 512;     // bytes of K (or V) codes per tile
+constexpr int kMaxDecodeLen = 6553600;   // longest history (INT2) or sequence (BF16) one decode covers
 constexpr int kMaskWords = 16;      // arrival-mask words per (sequence, KV head): 512 history splits
 
 struct Pool {
@@ -79,6 +80,9 @@ cudaError_t launch_append_bf16(const Pool& p, int layer, int n_seqs, const void*
                                const void* v, const int32_t* cu, const int32_t* start,
                                const int32_t* pt, int max_pages, int max_tokens,
                                cudaStream_t s);
+
+// cuTensorMapEncodeTiled (driver entry point, looked up once; NULL if absent)
+void* tensor_map_encode_fn();
 
 struct DecodePlan {
   int n_split = 1;          // history splits per (sequence, KV head)

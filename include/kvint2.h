@@ -261,7 +261,10 @@ kv_status_t kv_append_step(kv_pool_t* pool, int32_t layer, int32_t B, const void
 
 /* Bytes of device workspace kv_decode_attention / kv_decode_attention_bf16
  * need for a batch of B sequences whose history (INT2 pool) or total length
- * (BF16 pool) is at most max_len tokens.  0 on invalid arguments. */
+ * (BF16 pool) is at most max_len tokens.  0 on invalid arguments.  Every
+ * decode call takes max_hist_len / max_seq_len <= KV_MAX_DECODE_LEN
+ * (else KV_ERR_INVALID_ARG). */
+#define KV_MAX_DECODE_LEN 6553600
 size_t kv_decode_workspace_bytes(const kv_pool_t* pool, int32_t B, int32_t max_len);
 
 /* One decode step of one layer for B sequences over the three-tier pool

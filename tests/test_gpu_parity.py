@@ -286,6 +286,10 @@ def test_decode_page_permutation_is_bit_identical():
 
 
 def test_decode_hist0_equals_bf16_path():
+    """With no history the INT2 decode is plain attention over BF16 tokens, as is
+    the BF16 decode.  The BF16 decode applies each softmax weight as a bf16
+    hi + lo pair on the tensor cores (relative error <= 2^-16 per weight), so
+    the two agree to 1e-5 rel-L2, not to fp32 rounding."""
     wl = synth.make_decode_workload("h0", 12, B=3, Hq=8, Hkv=2, ctx=[70, 320, 200], page_size=16)
     assert int(wl.hist_len.max()) == 0
     pool = gu.make_int2_pool(wl)
@@ -294,7 +298,9 @@ def test_decode_hist0_equals_bf16_path():
     bpool, pt, lens = gu.make_bf16_pool(wl)
     ref = gu.gpu_decode_bf16(bpool, wl, pt, lens)
     bpool.close()
-    assert gu.metrics(out, ref)[1] <= 1e-6
+    ma, rl = gu.metrics(out, ref)
+    print(f"hist0 vs bf16: max_abs {ma:.3e} rel_l2 {rl:.3e}")
+    assert rl <= 1e-5
 
 
 def test_decode_grid_exact_equals_bf16_path():
@@ -346,6 +352,7 @@ def test_decode_bf16_matches_oracle(G, P):
     bpool.close()
     ref = att.decode_bf16_paged(wl.q, kb, vb, pt, lens, wl.Hkv, P, wl.scale)
     ma, rl = gu.metrics(out, ref)
+    print(f"bf16 G={G} P={P}: max_abs {ma:.3e} rel_l2 {rl:.3e}")
     assert ma <= 1e-4 and rl <= 1e-5
 
 
