@@ -322,24 +322,75 @@ def make_timer(torch, dev, stream, kvdist):
         flush_w.zero_()
         flush_r.sum()
 
-    def timed(fn, steps, warmup, flush_l2=False):
-        """fn(i) is step i; warm-up steps are -warmup .. -1."""
+    def timed(fn, steps, warmup, flush_l2=False, per_step_pass=True):
+        """fn(i) is step i; warm-up steps are -warmup .. -1.  With a flush each
+        step is timed alone between its own events.  Without one the K steps run
+        back to back between two region events, every step queued before the
+        first starts (the mean is region / K: launch latency overlapped as in a
+        serving loop); a second pass of the same steps with per-step events
+        gives the distribution (skipped for steps that change the pool)."""
+        t0 = time.perf_counter()
         for i in range(-warmup, 0):
             if flush_l2:
                 flush()
             fn(i)
+        host_per_step = (time.perf_counter() - t0) / max(warmup, 1)
         torch.cuda.synchronize()
         kvdist.barrier()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(steps)]
-        for i, (s0, s1) in enumerate(ev):
-            if flush_l2:
-                flush()
-            s0.record(stream); fn(i); s1.record(stream)
+
+        def per_step():
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(steps)]
+            for i, (s0, s1) in enumerate(ev):
+                if flush_l2:
+                    flush()
+                s0.record(stream); fn(i); s1.record(stream)
+            torch.cuda.synchronize()
+            return np.array([s0.elapsed_time(s1) for s0, s1 in ev])   # ms
+
+        if flush_l2:
+            per = per_step()
+            kvdist.barrier()
+            return Timing(per, None)
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # hold the stream (a bounded spin kernel) while the host queues every step
+        hold_s = max(0.02, 3.0 * host_per_step * steps)
+        torch.cuda._sleep(int(hold_s * SPIN_CYCLES_PER_S))
+        r0.record(stream)
+        t1 = time.perf_counter()
+        for i in range(steps):
+            fn(i)
+        r1.record(stream)
+        queued_s = time.perf_counter() - t1
         torch.cuda.synchronize()
+        region = r0.elapsed_time(r1)
+        per = per_step() if per_step_pass else None
         kvdist.barrier()
-        return np.array([s0.elapsed_time(s1) for s0, s1 in ev])   # ms
+        if queued_s >= hold_s and per is not None:   # the GPU may have waited for the host
+            return Timing(per, None)
+        return Timing(per, region, steps, host_bound=queued_s >= hold_s)
     return timed
+
+
+class Timing:
+    """Per-step event times (ms) and, for back-to-back steps, the region time."""
+
+    def __init__(self, per_step_ms, region_ms, steps=None, host_bound=False):
+        self.per_step = per_step_ms
+        self.region_ms = region_ms
+        self.steps = steps if steps is not None else len(per_step_ms)
+        self.host_bound = host_bound   # the region may include waits for the host
+
+    @property
+    def mean_ms(self):
+        if self.region_ms is not None:
+            return self.region_ms / self.steps
+        return float(np.mean(self.per_step))
+
+
+# cycles of torch's spin kernel per second (the SM clock is at most 2.07 GHz,
+# so the hold lasts at least the time asked for)
+SPIN_CYCLES_PER_S = 2.1e9
 
 
 def peak_hbm():
@@ -349,9 +400,20 @@ def peak_hbm():
     return 6800.0, "fallback 6.8 TB/s"
 
 
-def us_stats(t_ms):
-    return {"us": float(np.mean(t_ms) * 1e3),
-            "us_p10_p50_p90": [float(np.percentile(t_ms, p) * 1e3) for p in (10, 50, 90)]}
+def us_stats(t):
+    out = {"us": float(t.mean_ms * 1e3)}
+    if t.per_step is not None:
+        out["us_p10_p50_p90"] = [float(np.percentile(t.per_step, p) * 1e3) for p in (10, 50, 90)]
+    if t.region_ms is not None:
+        out["timing"] = ("region of the back-to-back steps (all queued before the first starts) / steps; "
+                         "percentiles from a second pass with per-step events")
+        if t.per_step is not None:
+            out["us_per_step_events"] = float(np.mean(t.per_step) * 1e3)
+        if t.host_bound:
+            out["timing"] += " (the host queued slower than the hold: an upper bound)"
+    else:
+        out["timing"] = "mean of per-step events"
+    return out
 
 
 class Env:
@@ -498,7 +560,7 @@ def decode_summary(env, rig, steps, warmup, with_bf16=True, flush_l2=False):
     if with_bf16:
         rig.build_bf16()
         tb = env.timed(rig.decode_bf16, max(5, steps // 2), 3, flush_l2=flush_l2)
-        us_b = env.max_ranks([float(np.mean(tb) * 1e3)])[0]
+        us_b = env.max_ranks([float(tb.mean_ms * 1e3)])[0]
         bb = bf16_bytes(c)
         res["bf16_path"] = {"us": us_b, "bytes": bb, "gbs": bb / (us_b * 1e-6) / 1e9,
                             "frac_of_measured_peak": bb / (us_b * 1e-6) / 1e9 / env.peak,
@@ -528,14 +590,15 @@ def online_step(env, rig, steps, warmup, decode_us):
         n.kv_append_step(rig.pool.handle, l, c.B, new[0], new[1], *lens[l], rig.pt_ext,
                          rig.pt_ext_np.shape[1], env.stream)
         rig.decode(i, lens=lens[l], max_hist=max_hist, extended=True)
-    t = env.timed(step, steps, max(3, warmup), flush_l2=(L == 1 and rig.small))
+    t = env.timed(step, steps, max(3, warmup), flush_l2=(L == 1 and rig.small), per_step_pass=False)
     if rig.pool.error():
         raise RuntimeError("device error during the online steps")
     placed = sum(int((lens[l][1].cpu().numpy() - c.hist_len).sum()) for l in range(L))
     if placed != total * c.B:
         raise RuntimeError("the placement did not evict one token per step")
-    us = env.max_ranks([float(np.mean(t) * 1e3)])[0]
-    return {"us": us, "decode_alone_us": decode_us, "ratio_to_decode_alone": us / decode_us,
+    us = env.max_ranks([float(t.mean_ms * 1e3)])[0]
+    return {"us": us, "timing": us_stats(t)["timing"], "decode_alone_us": decode_us,
+            "ratio_to_decode_alone": us / decode_us,
             "batch": c.B, "launches_per_step": 2,
             "what": "kv_append_step (new token into the recent ring, the oldest recent token rotated, "
                     "clipped, quantized and packed into INT2 history) then kv_decode_attention "
@@ -609,7 +672,7 @@ def run_headline(env, wl):
     t_multi = env.timed(mstep, max(5, args.steps // 2), 3) if TQ * (Hq // c.Hkv) <= 8 else None
     if rig.pool.error():
         raise RuntimeError("device error during the end-to-end and multi-query steps")
-    us_e2e, us_mapped = env.max_ranks([float(np.mean(t_e2e) * 1e3), float(np.mean(t_mapped) * 1e3)])
+    us_e2e, us_mapped = env.max_ranks([float(t_e2e.mean_ms * 1e3), float(t_mapped.mean_ms * 1e3)])
 
     # ---- the online step at batch 1 (mutates the pool: last) ----
     online = online_step(env, rig, args.steps, args.warmup, us)
@@ -641,7 +704,7 @@ def run_headline(env, wl):
                                     "reads q and the lengths and writes the output across the CPU-GPU "
                                     "link inside the timed region (no staging copies)"},
         "multi_query": (None if t_multi is None else
-                        {"us": float(np.mean(t_multi) * 1e3), "queries_per_sequence": TQ,
+                        {"us": float(t_multi.mean_ms * 1e3), "queries_per_sequence": TQ,
                          "what": "one kv_decode_attention_multi call over the same cache, "
                                  "output and log-sum-exp"}),
         "gpu_launches": args.steps,

@@ -174,6 +174,9 @@ kv_status_t kv_pool_set_rotation(kv_pool_t* pool, int32_t layer, const float* R_
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(cl + H * 128, clip_v, H * 128 * sizeof(float), cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess) e = kvint2::launch_rotation_prep(p, layer, R_k, R_v, s);
+  // decodes read the rotation before they wait for the kernel ahead of them:
+  // the set-up is complete before this call returns
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   return cuda_status(e);
 }
 

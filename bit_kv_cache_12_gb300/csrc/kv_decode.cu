@@ -83,7 +83,6 @@ static_assert(kMaxParts <= 32 * kMaskWords, "every split has a bit in the arriva
 //            L2 across steps by their evict-last priority) - grids of one wave;
 //   kQPre    the batched pre-pass wrote the fragments - grids of several waves.
 constexpr int kQLocal = 0, kQPre = 1;
-__host__ __device__ constexpr int pad4(int n) { return (n + 3) / 4 * 4; }
 
 struct DecodeArgs {
   const uint8_t* hist;      // INT2 layer base
@@ -128,27 +127,6 @@ struct DecodeArgs {
   int merge_polls;          // INT2: bounded polls of a tier CTA for its history splits
   int qmode;                // INT2: where a history CTA gets q' from (kQLocal or kQPre)
   int* err;
-};
-
-// Shared-memory carve-up (in floats) of the BF16 decode's CTA of NW warps:
-// q, the split's page ids, merged m / l, then the per-warp softmax weights and
-// results; the final merge reuses everything.
-template <int G, int NW>
-struct Lay {
-  static constexpr int sq = 0;                                    // [G][128]
-  static constexpr int sqr = sq + G * 128;                        // [G][128] merged o
-  static constexpr int smm = sqr + G * 128;                       // [G] merged m
-  static constexpr int sml = smm + pad4(G);                       // [G] merged l
-  static constexpr int spid = sml + pad4(G);                      // [kMaxPids] int
-  static constexpr int big = spid + kMaxPids;
-  static constexpr int swo = big;                                 // [NW][G][128]
-  static constexpr int swm = swo + NW * G * 128;                  // [NW][G]
-  static constexpr int swl = swm + pad4(NW * G);                  // [NW][G]
-  static constexpr int sp = swl + pad4(NW * G);                   // [NW][32][G]
-  static constexpr int phase_end = sp + NW * 32 * G;
-  static constexpr int merge_f = 16 + 2 * NW * 128 + 2 * kMaxParts * G;
-  static constexpr int total = (phase_end > merge_f) ? phase_end : merge_f;
-  static_assert(total * 4 <= 227 * 1024, "shared memory of one CTA");
 };
 
 // ---------------------------------------------------------------------------
@@ -666,6 +644,22 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
   if (lane < kStages) mbar_init(wbar + lane, 1);
   if (threadIdx.x == 0) mbar_init(rkbar, 1);
   mbar_fence_init();
+  // q' is formed here (kQLocal) or taken from the pre-pass.  When formed here,
+  // R_k's fragments (64 KB, a pool constant) are requested before the wait for
+  // the preceding kernel, which this launch may overlap; every buffer the
+  // caller passes is read after it
+  const bool local = a.qmode == kQLocal;
+  uint4* rfr = reinterpret_cast<uint4*>(smb + S::rfr);
+  if (local) {
+    if (threadIdx.x == 0) {
+      const uint4* src = a.rfrag + (size_t)g * kFragBlocks * 4096;
+      const uint64_t keep = l2_evict_last_policy();
+      mbar_expect_tx(rkbar, 4096 * 16);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) bulk_g2s_hint(rfr + 1024 * c, src + 1024 * c, 16384, rkbar, keep);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+  }
 
   const int tsh = a.tpp_shift, tmask = a.tiles_per_page - 1;
   const int t_begin = split * a.per_split;
@@ -682,21 +676,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
   }
   for (int i = threadIdx.x; i < p_all; i += NW * 32) spid[i] = __ldg(ptrow + p_begin + i);
   float* sq = reinterpret_cast<float*>(smb + S::sq);
-  // q' is formed here (kQLocal) or taken from the pre-pass; when formed here,
-  // q and R_k's fragments (64 KB, by bulk copy) are requested behind the loads
-  // above
-  const bool local = a.qmode == kQLocal;
-  uint4* rfr = reinterpret_cast<uint4*>(smb + S::rfr);
-  if (local) {
-    load_q<G, NW, kMulti>(a, b, g, sq, S::HP);
-    if (threadIdx.x == 0) {
-      const uint4* src = a.rfrag + (size_t)g * kFragBlocks * 4096;
-      const uint64_t keep = l2_evict_last_policy();
-      mbar_expect_tx(rkbar, 4096 * 16);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) bulk_g2s_hint(rfr + 1024 * c, src + 1024 * c, 16384, rkbar, keep);
-    }
-  }
+  if (local) load_q<G, NW, kMulti>(a, b, g, sq, S::HP);
   int h = __ldg(a.hist_len + b);
   // the grid covers max_len history tokens (and the page table max_pages pages)
   const int cap = min(a.max_pages * a.page_size, a.max_len);
@@ -1116,6 +1096,8 @@ __device__ void tier_merge(const DecodeArgs& a, int b, int g, uint8_t* smb) {
   float* sq = reinterpret_cast<float*>(smb + S::sq);
   uint8_t* stk = smb + S::stage;
   uint8_t* stv = stk + (size_t)kTierRows * kTierRowK;
+  // every input of the tier CTA comes from the caller: after the preceding kernel
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   auto stage_rows = [&](int r0, int r1) {   // storage rows [r0, r1) of [sink slots | recent ring]
     for (int i = threadIdx.x; i < (r1 - r0) * 32; i += NW * 32) {
       const int t = i >> 5, c = i & 31, key = c < 16, ch = c & 15, row = r0 + t;
@@ -1339,6 +1321,9 @@ __global__ void __launch_bounds__(int2_warps(G) * 32, 1) decode_int2_kernel(Deco
   // history splits of their pair (earlier in launch order) and merge them
   const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
   const int n_hist = a.n_split * gridDim.y * gridDim.z;
+  // the next kernel may start its own prologue as SMs free up; it waits for
+  // this grid before it reads anything this grid writes
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (lin < n_hist) {
     const int split = lin % a.n_split, pair = lin / a.n_split;
     const int g = pair % a.Hkv, b = pair / a.Hkv;
@@ -1488,6 +1473,10 @@ __global__ void __launch_bounds__(kBf16Warps * 32, 1)
   const int r = lane >> 2, j = lane & 3;
   const int nparts = a.n_split;
   float* part = a.ws + ((size_t)(b * a.Hkv + g) * nparts + split) * G * kPart;
+  // programmatic dependent launch: let the next kernel start its prologue, and
+  // wait for the preceding one before reading any input
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   int n = a.seq_len[b];
   const int cap = min(a.max_pages * a.page_size, a.max_len);
   if (n < 0 || n > cap) {
@@ -1743,15 +1732,15 @@ cudaError_t launch_int2_t(DecodeArgs a, int B, int sm_count, cudaStream_t s) {
   const long long ctas = (long long)(a.n_split + 1) * a.Hkv * B;
   const bool multi_wave = ctas > (long long)per_sm * sm_count;
   a.qmode = multi_wave ? kQPre : kQLocal;
-  if (!multi_wave) {
-    decode_int2_kernel<G, GS, kMulti><<<dim3(a.n_split + 1, a.Hkv, B), int2_warps(G) * 32, int2_smem<G, GS>(),
-                                        s>>>(a);
-    return cudaGetLastError();
+  if (multi_wave) {   // the pre-pass starts after the preceding kernel; the decode overlaps it
+    constexpr int SPB = 16 / ((G <= 4) ? 4 : 8);   // sequences per pre-pass CTA
+    qprep_kernel<G, GS, kMulti><<<dim3(a.Hkv, (B + SPB - 1) / SPB), 256, 0, s>>>(a, B);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
   }
-  constexpr int SPB = 16 / ((G <= 4) ? 4 : 8);   // sequences per pre-pass CTA
-  qprep_kernel<G, GS, kMulti><<<dim3(a.Hkv, (B + SPB - 1) / SPB), 256, 0, s>>>(a, B);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  // programmatic dependent launch: the CTAs may start while the preceding
+  // kernel finishes; they wait for it (griddepcontrol.wait) before reading
+  // any input the caller passes
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_split + 1, a.Hkv, B);
   cfg.blockDim = dim3(int2_warps(G) * 32);
@@ -1769,9 +1758,17 @@ template <int G>
 cudaError_t launch_bf16_t(const DecodeArgs& a, int B, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t s) {
   if (bf16_blocks_per_sm<G>() < 0) return cudaErrorInvalidConfiguration;
-  dim3 grid(a.n_split, a.Hkv, B);
-  decode_bf16_kernel<G><<<grid, kBf16Warps * 32, bf16_smem<G>(), s>>>(a, kmap, vmap);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_split, a.Hkv, B);
+  cfg.blockDim = dim3(kBf16Warps * 32);
+  cfg.dynamicSmemBytes = bf16_smem<G>();
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_bf16_kernel<G>, a, kmap, vmap);
 }
 
 DecodeArgs base_args(const Pool& p, int layer, const void* q, const int32_t* pt, int max_pages,

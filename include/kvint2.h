@@ -34,6 +34,10 @@
  *     the host first: on failure it launches nothing and returns
  *     KV_ERR_INVALID_ARG or KV_ERR_UNSUPPORTED.  A failed launch returns
  *     KV_ERR_CUDA.
+ *   - The decode calls launch with programmatic dependent launch: their CTAs
+ *     may start (and fetch the pool's rotation) while the kernel ahead of them
+ *     on `stream` finishes, and read no buffer the caller passes before that
+ *     kernel has completed.
  *   - Problems only the GPU can see (a page id outside [0, num_pages), a
  *     length above capacity) are recorded in the pool's device error word and
  *     the offending work is skipped; no kernel traps.  Read it with
@@ -144,8 +148,10 @@ kv_status_t kv_pool_destroy(kv_pool_t* pool);
  *              Must be orthogonal (R R^T = I); the decode uses R^T as inverse.
  *   clip_k/v   device fp32 [Hkv][128] thresholds c_j > 0 on rotated channels,
  *              y = min(max(x', -c), c); +inf disables clipping.
- * The values are copied into the pool (asynchronously on `stream`; the
- * inputs may be freed once the stream reaches this point). */
+ * The values are copied into the pool on `stream`, and the call returns once
+ * the copy is complete (it synchronises `stream`): decode launches read the
+ * rotation while the kernel ahead of them may still run (programmatic
+ * dependent launch), so it must be in place before they are issued. */
 kv_status_t kv_pool_set_rotation(kv_pool_t* pool, int32_t layer, const float* R_k,
                                  const float* R_v, const float* clip_k, const float* clip_v,
                                  void* stream);
