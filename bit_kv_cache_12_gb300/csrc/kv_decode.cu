@@ -558,6 +558,13 @@ __global__ void __launch_bounds__(256) qprep_kernel(DecodeArgs a, int B) {
 // ---------------------------------------------------------------------------
 // Shared memory of a history CTA (byte offsets).  The per-warp results reuse
 // the ring once the loop is done.
+// A ring stage known at compile time (the steady-state loop) or at run time.
+template <int V>
+struct RingStage {};
+template <int V>
+__device__ __forceinline__ constexpr int stage_index(RingStage<V>) { return V; }
+__device__ __forceinline__ int stage_index(int v) { return v; }
+
 template <int G, int GS>
 struct HistLay {
   static constexpr int NW = int2_warps(G);
@@ -819,10 +826,8 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
   }
 
   int k = 0;   // this warp's tile count: ring stage k % kStages, phase k / kStages
-  // tiles of this warp whose copy was issued (the first kStages - 1 above)
-  int issued = min(kStages - 1, (t_end - t_begin - warp + NW - 1) / NW);
+  const int n_warp = max(0, (t_end - t_begin - warp + NW - 1) / NW);   // tiles of this warp
   auto issue = [&](int t, int stage) {   // tiles k >= kStages - 1, from the address table
-    if (t < t_end) ++issued;
     if (lane == 0 && t < t_end) {
       const uint64_t e = saddr[t - t_begin];
       mbar_expect_tx(wbar + stage, TB);
@@ -833,13 +838,15 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
   // the history or sit behind a bad page id (only the split's last tile, or
   // every tile of a split with a bad page); other tiles need no masks.
   // Returns false if its copy did not arrive in time.
-  auto tile = [&](int t, auto mask_tag) -> bool {
+  // st / par: the ring stage and the phase parity of tile k (compile-time
+  // stages in the steady-state loop below).
+  auto tile = [&](int t, auto mask_tag, auto stage, uint32_t par) -> bool {
     constexpr bool kMask = decltype(mask_tag)::value;
+    const int st = stage_index(stage);
     __syncwarp();   // every lane is done with the stage refilled next
     // tile k+3 goes into the stage read in the previous iteration
-    issue(t + NW * (kStages - 1), (k + kStages - 1) % kStages);
-    const int st = k % kStages;
-    if (!__all_sync(0xffffffffu, mbar_wait(wbar + st, (k / kStages) & 1, a.wait_polls))) return false;
+    issue(t + NW * (kStages - 1), (st + kStages - 1) % kStages);
+    if (!__all_sync(0xffffffffu, mbar_wait(wbar + st, par, a.wait_polls))) return false;
     const uint8_t* src = ring + st * TB;
     const uint4 kq4 = *reinterpret_cast<const uint4*>(src + 16 * lane);
     const uint4 vq4 = *reinterpret_cast<const uint4*>(src + 512 + 16 * lane);
@@ -997,22 +1004,28 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
 
   // tiles below t_full are full and behind valid pages: no masks
   const int t_full = bad ? t_begin : min(t_end, h / kTile);
+  const bool started = ok;
   int t = ok ? t_begin + warp : t_end;   // a lost R_k copy skips the split
-#pragma unroll 2   // lets one tile's loads, unpack and QK overlap the previous tile's softmax and PV
-  for (; t < t_full; t += NW)
-    if (!tile(t, std::false_type{})) {
-      ok = false;
-      break;
-    }
-  if (ok)
-    for (; t < t_end; t += NW)
-      if (!tile(t, std::true_type{})) {
-        ok = false;
-        break;
-      }
+  // steady state: kStages unmasked tiles per pass, one per ring stage, so that
+  // stage offsets and barrier addresses are constants (k is a multiple of
+  // kStages here); the phase parity flips once per pass
+  uint32_t ph = 0;
+  for (; ok && t + NW * (kStages - 1) < t_full; t += NW * kStages, ph ^= 1u) {
+    ok = tile(t, std::false_type{}, RingStage<0>{}, ph) &&
+         tile(t + NW, std::false_type{}, RingStage<1>{}, ph) &&
+         tile(t + 2 * NW, std::false_type{}, RingStage<2>{}, ph) &&
+         tile(t + 3 * NW, std::false_type{}, RingStage<3>{}, ph);
+    if (!ok) t = t_end;   // k counts the tiles done
+  }
+  static_assert(kStages == 4, "the steady-state pass above takes one tile per stage");
+  // the rest (fewer than kStages full tiles, then the tail) through the masked body
+  for (; ok && t < t_end; t += NW)
+    ok = tile(t, std::true_type{}, k % kStages, (uint32_t)(k / kStages) & 1u);
   if (!ok) {   // a copy did not arrive in time: wait (bounded) for the ones in flight,
-    // those of tiles k .. issued - 1 of this warp
+    // those of tiles k .. issued - 1 of this warp (tile k issued tile k + kStages - 1
+    // before its wait ran out; a split that never started issued the first kStages - 1)
     if (lane == 0) flag_error(a.err, KV_DEVERR_TIMEOUT);
+    const int issued = started ? min(k + kStages, n_warp) : min(kStages - 1, n_warp);
     for (int kk = k; kk < issued; ++kk) mbar_wait(wbar + kk % kStages, (kk / kStages) & 1, a.wait_polls);
   }
   ok = __syncthreads_and(ok);   // every warp is done with its ring before the results reuse it
