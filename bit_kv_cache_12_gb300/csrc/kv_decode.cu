@@ -238,18 +238,6 @@ __device__ void merge_warps(const float* swo, const float* swm, const float* swl
 }
 
 template <int G, int NW>
-__device__ void write_partial(float* part, const float* o, const float* sm_m, const float* sm_l) {
-  for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
-    const int h = idx >> 7, c = idx & 127;
-    part[h * kPart + 4 + c] = o[idx];
-    if (c == 0) {
-      part[h * kPart + 0] = sm_m[h];
-      part[h * kPart + 1] = sm_l[h];
-    }
-  }
-}
-
-template <int G, int NW>
 __device__ void write_empty_partial(float* part) {
   for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
     const int h = idx >> 7, c = idx & 127;
