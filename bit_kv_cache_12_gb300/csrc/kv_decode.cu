@@ -63,7 +63,7 @@ constexpr int kMaxParts = 400;   // partials per (sequence, KV head) a merge rea
 constexpr int kMaxPids = 1032;   // page ids staged per CTA (a split covers <= 1024 tiles)
 constexpr int kTierRows = 320;   // sink + recent storage rows staged per tier CTA
 constexpr int kTierRowK = 272;   // staged K row stride (bytes): 256 + 16 keeps lane reads conflict-free
-constexpr int kTierRowV = 256;
+constexpr int kTierRowV = 272;   // staged V row stride: the transposed ldmatrix reads are conflict-free too
 // The history loop keeps each head's exponent reference kSlack (log2 units)
 // above the largest score seen when it was last moved, so weights stay <= 1
 // and the accumulators are rescaled only when a score passes the reference.
@@ -273,132 +273,34 @@ constexpr int kMergeBatch = 20;
 // BF16 rows: warp-cooperative SIMT attention over a token range
 // (QK with one token per lane, PV with four channels per lane)
 // ---------------------------------------------------------------------------
-template <int G>
-struct WarpAcc {
-  float m[G];      // running max (log2 units), uniform across the warp
-  float l[G];      // lane-partial sum of weights
-  float o[G][4];   // channels 4*lane .. 4*lane+3
-  __device__ void init() {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      m[h] = kNegInf;
-      l[h] = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[h][e] = 0.f;
-    }
-  }
-};
-
-// A zero bf16 row: stands in for tokens a warp must not read (past the end of
-// the range or behind an invalid page id); their weight is forced to 0.
-__device__ __align__(16) uint16_t g_zero_row[128];
 // A zero INT2 tile (largest tile size): copied in place of a tile behind an
 // invalid page id, so every ring slot always holds finite data.
 __device__ __align__(16) uint8_t g_zero_tile[1280];
 
-template <bool kShared, class T>
-__device__ __forceinline__ T load_row(const T* p) {
-  if (kShared) return *p;   // rows staged in shared memory (generic load)
-  return __ldg(p);
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
 }
-
-// rows(u, k, v) sets bf16 row pointers for token u and returns false if the
-// token must be skipped.  All loads of a phase are issued before their use.
-template <int G, bool kShared, class RowFn>
-__device__ void bf16_rows_attend(const float* sq, float* sp, int u0, int u1, int stride,
-                                 const RowFn& rows, float scale_log2, WarpAcc<G>& st) {
-  const int lane = threadIdx.x & 31;
-  for (int c0 = u0; c0 < u1; c0 += stride) {
-    const int u = c0 + lane;
-    const uint16_t* krow = g_zero_row;
-    const uint16_t* vrow = g_zero_row;
-    bool ok = false;
-    if (u < u1) ok = rows(u, krow, vrow);
-    if (!ok) krow = vrow = g_zero_row;
-    float sc[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) sc[h] = 0.f;
-    const uint4* kr = reinterpret_cast<const uint4*>(krow);
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint4 kk[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) kk[i] = load_row<kShared>(kr + half * 8 + i);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint4 w = kk[i];
-        const float x[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
-                            bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
-        const int cbase = 8 * (half * 8 + i);
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float4 q0 = *reinterpret_cast<const float4*>(sq + h * 128 + cbase);
-          const float4 q1 = *reinterpret_cast<const float4*>(sq + h * 128 + cbase + 4);
-          float acc = sc[h];
-          acc = fmaf(x[0], q0.x, acc); acc = fmaf(x[1], q0.y, acc);
-          acc = fmaf(x[2], q0.z, acc); acc = fmaf(x[3], q0.w, acc);
-          acc = fmaf(x[4], q1.x, acc); acc = fmaf(x[5], q1.y, acc);
-          acc = fmaf(x[6], q1.z, acc); acc = fmaf(x[7], q1.w, acc);
-          sc[h] = acc;
-        }
-      }
-    }
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float v = ok ? sc[h] * scale_log2 : kNegInf;
-      const float mnew = fmaxf(st.m[h], warp_max_xor(v, 1));
-      const float alpha = (st.m[h] == kNegInf) ? 0.f : exp2f(st.m[h] - mnew);
-      st.m[h] = mnew;
-      st.l[h] *= alpha;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) st.o[h][e] *= alpha;
-      const float p = exp2f(v - ((mnew == kNegInf) ? 0.f : mnew));
-      st.l[h] += p;
-      sp[lane * G + h] = p;
-    }
-    __syncwarp();
-    const unsigned long long vbits = reinterpret_cast<unsigned long long>(vrow);
-#pragma unroll
-    for (int tb = 0; tb < 4; ++tb) {
-      uint2 vv[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint16_t* vr =
-            reinterpret_cast<const uint16_t*>(__shfl_sync(0xffffffffu, vbits, tb * 8 + e));
-        vv[e] = load_row<kShared>(reinterpret_cast<const uint2*>(vr) + lane);
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int t = tb * 8 + e;
-        const float v0 = bf16lo(vv[e].x), v1 = bf16hi(vv[e].x);
-        const float v2 = bf16lo(vv[e].y), v3 = bf16hi(vv[e].y);
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float p = sp[t * G + h];
-          st.o[h][0] = fmaf(p, v0, st.o[h][0]);
-          st.o[h][1] = fmaf(p, v1, st.o[h][1]);
-          st.o[h][2] = fmaf(p, v2, st.o[h][2]);
-          st.o[h][3] = fmaf(p, v3, st.o[h][3]);
-        }
-      }
-    }
-    __syncwarp();
-  }
+__device__ __forceinline__ void ldmatrix_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
 }
-
-template <int G>
-__device__ void warp_acc_to_smem(WarpAcc<G>& st, float* swo, float* swm, float* swl) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const float l = warp_sum_xor(st.l[h], 1);
-    *reinterpret_cast<float4*>(swo + (warp * G + h) * 128 + 4 * lane) =
-        make_float4(st.o[h][0], st.o[h][1], st.o[h][2], st.o[h][3]);
-    if (lane == 0) {
-      swm[warp * G + h] = st.m[h];
-      swl[warp * G + h] = l;
-    }
-  }
+// one 2D TMA box (x = channel, y = row) of `map` into shared memory, completing on `bar`
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+// (hi, lo) bf16 split of an fp32 weight as one bf16x2 register: low half
+// bf16(x), high half bf16(x - bf16(x))
+__device__ __forceinline__ uint32_t split_hi_lo_bf16(float x) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+  return (uint32_t)__bfloat16_as_ushort(hi) | ((uint32_t)__bfloat16_as_ushort(lo) << 16);
 }
 
 // q of the GQA group (bf16 -> fp32) into shared memory; padded heads are 0.
@@ -581,8 +483,7 @@ struct TierLay {
   static constexpr int NW = int2_warps(G);
   static constexpr int sq = 0;                                         // [G][128] q
   static constexpr int stage = sq + G * 128 * 4;                       // staged sink + recent rows
-  static constexpr int sp = stage + kTierRows * (kTierRowK + kTierRowV);   // [NW][32][G] weights
-  static constexpr int tier_o = sp + NW * 32 * G * 4;                  // [G][128] tier partial o
+  static constexpr int tier_o = stage + kTierRows * (kTierRowK + kTierRowV);   // [G][128] tier partial o
   static constexpr int tier_m = tier_o + G * 128 * 4;                  // [G]
   static constexpr int tier_l = tier_m + G * 4;                        // [G]
   static constexpr int hist_m = tier_l + G * 4;                        // [G] merged history m
@@ -597,7 +498,7 @@ struct TierLay {
   static constexpr int GP = (G + 3) & ~3;
   static constexpr int oh = rv + 128 * 128 * 4;                        // [128][GP] merged history o', transposed
   static constexpr int spr = swo;                                      // [NW][G][128] row-slice sums
-  static_assert(oh + GP * 128 * 4 <= sp, "R_v^T and the merge fit in the staging area");
+  static_assert(oh + GP * 128 * 4 <= tier_o, "R_v^T and the merge fit in the staging area");
 };
 
 template <int G, int GS>
@@ -1118,28 +1019,108 @@ __device__ void tier_merge(const DecodeArgs& a, int b, int g, uint8_t* smb) {
     nr = max(0, min(nr, rcap));
     rs = max(0, min(rs, rcap - 1));
   }
-  WarpAcc<G> st;
-  st.init();
+  // ---- the tier rows on the tensor cores: warp w takes the 16-row tiles w,
+  // w + NW, .. of each staged pass; q exact in bf16 as the QK B operand (column
+  // 2h: head h, 2h + 1: zero), the softmax weights as bf16 hi + lo for PV, the
+  // online softmax with the lazy reference of the history loop ----
+  constexpr int NT = (G <= 4) ? 1 : 2;
+  const int lane = threadIdx.x & 31, r = lane >> 2, j = lane & 3;
+  auto live_row = [&](int u) -> bool {   // storage row u holds a token of the sequence
+    if (u < scap) return u < ns;
+    int d = (u - scap) - rs;
+    d += (d < 0) ? rcap : 0;
+    return d < nr;
+  };
+  uint32_t qf[8][NT][2];
+  float m_run[NT], base[NT], l_run[NT], oacc[8][NT][4];
+#pragma unroll
+  for (int u = 0; u < NT; ++u) {
+    m_run[u] = kNegInf;
+    base[u] = 0.f;
+    l_run[u] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) oacc[i][u][0] = oacc[i][u][1] = oacc[i][u][2] = oacc[i][u][3] = 0.f;
+  }
+  const uint32_t sk_base = smem_u32(stk), sv_base = smem_u32(stv);
+  const int krow = lane & 15, kc = lane >> 4;
+  const int vrow = (lane & 7) + 8 * (lane >> 4), vc = (lane >> 3) & 1;
   for (int r0 = 0; r0 < rows; r0 += kTierRows) {
     const int r1 = min(rows, r0 + kTierRows);
     if (r0 > 0) stage_rows(r0, r1);
     cp_async_wait<0>();
     __syncthreads();
-    auto rowfn = [&](int u, const uint16_t*& kr, const uint16_t*& vr) -> bool {
-      bool live;
-      if (u < scap) {
-        live = u < ns;
-      } else {
-        int d = (u - scap) - rs;
-        d += (d < 0) ? rcap : 0;
-        live = d < nr;
+    if (r0 == 0) {   // q (in shared memory since the barrier) -> B fragments
+      const int hh = r >> 1;
+#pragma unroll
+      for (int u = 0; u < NT; ++u) {
+        const int head = 4 * u + hh;
+        const bool on = !(r & 1) && head < G;
+        const float* qrow = sq + (on ? head : 0) * 128;
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2) {
+          const int c = 16 * s2 + 2 * j;
+          qf[s2][u][0] = on ? ((__float_as_uint(qrow[c]) >> 16) | (__float_as_uint(qrow[c + 1]) & 0xFFFF0000u)) : 0u;
+          qf[s2][u][1] = on ? ((__float_as_uint(qrow[c + 8]) >> 16) | (__float_as_uint(qrow[c + 9]) & 0xFFFF0000u)) : 0u;
+        }
       }
-      kr = reinterpret_cast<const uint16_t*>(stk + (u - r0) * kTierRowK);
-      vr = reinterpret_cast<const uint16_t*>(stv + (u - r0) * kTierRowV);
-      return live;
-    };
-    bf16_rows_attend<G, true>(sq, reinterpret_cast<float*>(smb + S::sp) + warp * 32 * G, r0 + 32 * warp, r1,
-                              32 * NW, rowfn, a.scale_log2, st);
+    }
+    const int nrow = r1 - r0, ntile = (nrow + 15) / 16;
+    for (int tt = warp; tt < ntile; tt += NW) {
+      const int t0 = 16 * tt;
+      // a dead row's V (or a row past the pass) is zeroed, so that its zero
+      // weight never meets a stale value
+      if (lane < 16 && !(t0 + lane < nrow && live_row(r0 + t0 + lane))) {
+        uint4* vz = reinterpret_cast<uint4*>(stv + (size_t)(t0 + lane) * kTierRowV);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) vz[c] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncwarp();
+      const bool v0 = t0 + r < nrow && live_row(r0 + t0 + r);
+      const bool v1 = t0 + r + 8 < nrow && live_row(r0 + t0 + r + 8);
+      float sacc[NT][4];
+#pragma unroll
+      for (int u = 0; u < NT; ++u) sacc[u][0] = sacc[u][1] = sacc[u][2] = sacc[u][3] = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < 8; ++s2) {
+        uint32_t fa[4];
+        ldmatrix_x4(sk_base + (t0 + krow) * kTierRowK + (2 * s2 + kc) * 16, fa);
+#pragma unroll
+        for (int u = 0; u < NT; ++u) mma_bf16(sacc[u], fa[0], fa[1], fa[2], fa[3], qf[s2][u][0], qf[s2][u][1]);
+      }
+      uint32_t bpv[NT][2];
+#pragma unroll
+      for (int u = 0; u < NT; ++u) {
+        const float l0 = v0 ? sacc[u][0] * a.scale_log2 : kNegInf;
+        const float l1 = v1 ? sacc[u][2] * a.scale_log2 : kNegInf;
+        if (__any_sync(0xffffffffu, fmaxf(l0, l1) > m_run[u])) {
+          float tmax = fmaxf(l0, l1);
+          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+          const bool need = tmax > m_run[u];
+          const float mnew = need ? tmax + kSlack : m_run[u];
+          const float alpha = need ? ((m_run[u] == kNegInf) ? 0.f : exp2_neg(m_run[u] - mnew)) : 1.f;
+          m_run[u] = mnew;
+          base[u] = (mnew == kNegInf) ? 0.f : mnew;
+          l_run[u] *= alpha;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) oacc[i][u][e] *= alpha;
+        }
+        const float p0 = exp2_neg(l0 - base[u]), p1 = exp2_neg(l1 - base[u]);
+        l_run[u] += p0 + p1;
+        bpv[u][0] = movmatrix_t(split_hi_lo_bf16(p0));
+        bpv[u][1] = movmatrix_t(split_hi_lo_bf16(p1));
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t fa[4];
+        ldmatrix_x4_t(sv_base + (t0 + vrow) * kTierRowV + (2 * i + vc) * 16, fa);
+#pragma unroll
+        for (int u = 0; u < NT; ++u) mma_bf16(oacc[i][u], fa[0], fa[1], fa[2], fa[3], bpv[u][0], bpv[u][1]);
+      }
+    }
     __syncthreads();   // the staged rows are dead before they are replaced or reused
   }
   float* swo = reinterpret_cast<float*>(smb + S::swo);
@@ -1148,7 +1129,23 @@ __device__ void tier_merge(const DecodeArgs& a, int b, int g, uint8_t* smb) {
   float* tier_o = reinterpret_cast<float*>(smb + S::tier_o);
   float* tier_m = reinterpret_cast<float*>(smb + S::tier_m);
   float* tier_l = reinterpret_cast<float*>(smb + S::tier_l);
-  warp_acc_to_smem<G>(st, swo, swm, swl);
+#pragma unroll
+  for (int u = 0; u < NT; ++u) {   // warp results (hi + lo columns summed) -> shared memory
+    const float l = warp_sum_xor(l_run[u], 4);
+    const int hh = 4 * u + j;
+    if (hh < G) {
+      float* o = swo + (warp * G + hh) * 128;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        o[16 * i + r] = oacc[i][u][0] + oacc[i][u][1];
+        o[16 * i + r + 8] = oacc[i][u][2] + oacc[i][u][3];
+      }
+      if (r == 0) {
+        swm[warp * G + hh] = m_run[u];
+        swl[warp * G + hh] = l;
+      }
+    }
+  }
   __syncthreads();
   merge_warps<G, NW>(swo, swm, swl, tier_o, tier_m, tier_l);   // ends with a barrier
 
@@ -1425,32 +1422,6 @@ struct BfLay {
   static_assert(swl + NW * G * 4 <= bars, "warp results fit in the ring");
   static_assert((16 + 2 * NW * 128 + 2 * kMaxParts * G) * 4 <= bars, "the final merge fits in the ring");
 };
-
-__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldmatrix_x4_t(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-// one 2D TMA box (x = channel, y = row) of `map` into shared memory, completing on `bar`
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-      "[%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-// (hi, lo) bf16 split of an fp32 weight as one bf16x2 register: low half
-// bf16(x), high half bf16(x - bf16(x))
-__device__ __forceinline__ uint32_t split_hi_lo_bf16(float x) {
-  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-  const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
-  return (uint32_t)__bfloat16_as_ushort(hi) | ((uint32_t)__bfloat16_as_ushort(lo) << 16);
-}
 
 // Plain split-K attention over the all-BF16 pool.  Each warp streams its
 // 16-token tiles of K and V by TMA through a ring in shared memory; QK runs

@@ -62,10 +62,13 @@ def test_multi_query_matches_oracle(G, T, gs):
     ma, rl = gu.metrics(out, ref)
     assert ma <= MAX_ABS and rl <= REL_L2, (ma, rl)
     assert np.abs(lse - ref_lse).max() <= 1e-4 * max(1.0, np.abs(ref_lse).max())
-    # every query position equals the single-query decode of that query
+    # every query position equals the single-query decode of that query, up to
+    # the rounding of the BF16 tier rows: their softmax weights enter the tensor
+    # cores as bf16 hi + lo pairs (relative error <= 2^-16 each), and the
+    # multi-query kernel spreads the rows over a different number of warps
     for t in range(T):
         one = gu.gpu_decode(pool, wl, q=np.ascontiguousarray(qm[:, t]))
-        assert gu.metrics(out[:, t], one)[1] <= 1e-6
+        assert gu.metrics(out[:, t], one)[1] <= 1e-5
     out2, _ = _multi(pool, wl, qm, with_lse=False)       # lse is optional
     assert np.array_equal(out2, out)
     pool.close()
