@@ -735,7 +735,17 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
     __syncwarp();   // every lane is done with the stage refilled next
     // tile k+3 goes into the stage read in the previous iteration
     issue(t + NW * (kStages - 1), (st + kStages - 1) % kStages);
-    if (!__all_sync(0xffffffffu, mbar_wait(wbar + st, par, a.wait_polls))) return false;
+    {   // one poll first (the copy is usually in); the bounded loop only if it is not
+      uint32_t ready;
+      asm volatile(
+          "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+          : "=r"(ready)
+          : "r"(smem_u32(wbar + st)), "r"(par)
+          : "memory");
+      if (!__all_sync(0xffffffffu, ready != 0u) &&
+          !__all_sync(0xffffffffu, mbar_wait(wbar + st, par, a.wait_polls)))
+        return false;
+    }
     const uint8_t* src = ring + st * TB;
     const uint4 kq4 = *reinterpret_cast<const uint4*>(src + 16 * lane);
     const uint4 vq4 = *reinterpret_cast<const uint4*>(src + 512 + 16 * lane);
