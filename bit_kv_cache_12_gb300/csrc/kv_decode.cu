@@ -133,9 +133,9 @@ struct DecodeArgs {
 // shared helpers
 // ---------------------------------------------------------------------------
 
-// R_k's MMA fragments for the q' pre-pass, held in registers: warp w of NW
-// produces q' columns 8w.., 8(w + NW).., and each lane loads all its fragments
-// at once (one memory latency).
+// R_k's MMA fragments held in registers (the q' pre-pass and the history CTAs
+// that form q' themselves): warp w of NW produces q' columns 8w.., 8(w + NW)..,
+// and each lane loads all its fragments at once (one memory latency).
 template <int NW>
 struct RotFrags {
   static constexpr int NTW = (16 + NW - 1) / NW;   // 8-column n-tiles per warp: warp, warp + NW, ..
@@ -153,14 +153,14 @@ struct RotFrags {
 
 // q'[h][c] = sum_i q[h][i] R_k[i][c] for the first NROWS rows of X (shared,
 // [*][128] fp32 holding bf16 values), on the tensor cores: R_k comes as fp16
-// hi + lo B fragments (rotation fragment block 0, in shared memory), q is
+// hi + lo B fragments (rotation fragment block 0, this warp's in registers), q is
 // scaled by 2^-8 (exact) and split into fp16 hi + lo, and the three products
 // above 2^-22 relative are accumulated in fp32, each in two chains (even and
 // odd k-steps) that are added at the end in a fixed order (the same order as
 // the batched pre-pass).  Warp w produces columns 8w.., 8(w + NW)...  Ends
 // with a barrier.
 template <int NROWS, int NW>
-__device__ void rotate_q(const float* X, const uint4* frag, float* Y) {
+__device__ void rotate_q(const float* X, const RotFrags<NW>& rkf, float* Y) {
   static_assert(NROWS <= 8, "rows");
   constexpr int NTW = (16 + NW - 1) / NW;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -186,8 +186,7 @@ __device__ void rotate_q(const float* X, const uint4* frag, float* Y) {
     const int c = 3 * (s & 1);
 #pragma unroll
     for (int u = 0; u < NTW; ++u) {
-      const int nt = warp + u * NW;
-      const uint4 f = (nt < 16) ? frag[(s * 16 + nt) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+      const uint4 f = rkf.f[s][u];   // zero past the 16 n-tiles
       mma_f16(acc[u][c], a0, 0u, a2, 0u, f.x, f.y);       // hi * hi
       mma_f16(acc[u][c + 1], a0, 0u, a2, 0u, f.z, f.w);   // hi * lo
       mma_f16(acc[u][c + 2], b0, 0u, b2, 0u, f.x, f.y);   // lo * hi
@@ -467,9 +466,7 @@ struct HistLay {
   static constexpr int sq = spid + kMaxPids * 4;          // [HP][128] q (q' computed in the CTA)
   static constexpr int sqr = sq + HP * 128 * 4;           // [HP][128] q'
   static constexpr int ssum = sqr + HP * 128 * 4;         // [HP][2] per-group sums of q'
-  static constexpr int rkbar = (ssum + HP * 2 * 4 + 7) / 8 * 8;   // mbarrier of the R_k fragment copy
-  static constexpr int rfr = (rkbar + 8 + 127) / 128 * 128;      // [4096] uint4 R_k fragments
-  static constexpr int total = rfr + 4096 * 16;
+  static constexpr int total = ssum + HP * 2 * 4;
   static constexpr int swo = 0;                           // [NW][G][128] per-warp o'
   static constexpr int swm = swo + NW * G * 128 * 4;      // [NW][G] m
   static constexpr int swl = swm + NW * G * 4;            // [NW][G] l
@@ -536,24 +533,16 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
   uint64_t* wbar = reinterpret_cast<uint64_t*>(smb + S::bars) + warp * kStages;
   uint64_t* saddr = reinterpret_cast<uint64_t*>(smb + S::saddr);   // per-tile source addresses
   int* spid = reinterpret_cast<int*>(smb + S::spid);
-  uint64_t* rkbar = reinterpret_cast<uint64_t*>(smb + S::rkbar);
   if (lane < kStages) mbar_init(wbar + lane, 1);
-  if (threadIdx.x == 0) mbar_init(rkbar, 1);
   mbar_fence_init();
   // q' is formed here (kQLocal) or taken from the pre-pass.  When formed here,
-  // R_k's fragments (64 KB, a pool constant) are requested before the wait for
-  // the preceding kernel, which this launch may overlap; every buffer the
-  // caller passes is read after it
+  // each warp loads its own R_k fragments (4 KB, a pool constant) into
+  // registers before the wait for the preceding kernel, which this launch may
+  // overlap; every buffer the caller passes is read after it
   const bool local = a.qmode == kQLocal;
-  uint4* rfr = reinterpret_cast<uint4*>(smb + S::rfr);
+  RotFrags<NW> rkf;
   if (local) {
-    if (threadIdx.x == 0) {
-      const uint4* src = a.rfrag + (size_t)g * kFragBlocks * 4096;
-      const uint64_t keep = l2_evict_last_policy();
-      mbar_expect_tx(rkbar, 4096 * 16);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) bulk_g2s_hint(rfr + 1024 * c, src + 1024 * c, 16384, rkbar, keep);
-    }
+    rkf.load(a.rfrag + (size_t)g * kFragBlocks * 4096);
     asm volatile("griddepcontrol.wait;" ::: "memory");
   }
 
@@ -583,8 +572,6 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
   const int ntiles = (h + kTile - 1) / kTile;
   const int t_end = min(ntiles, t_begin + a.per_split);
   if (t_begin >= t_end) {   // the same for every thread: no tile copy was started
-    if (local && !mbar_wait(rkbar, 0, a.wait_polls) && threadIdx.x == 0) flag_error(a.err, KV_DEVERR_TIMEOUT);
-    if (threadIdx.x == 0) mbar_inval(rkbar);
     write_empty_partial<G, NW>(part);
     return;
   }
@@ -639,8 +626,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
   if (local) {   // ---- q' = q R_k here, then its fragments and per-group sums ----
     float* sqr = reinterpret_cast<float*>(smb + S::sqr);
     float* ssum = reinterpret_cast<float*>(smb + S::ssum);
-    ok = __syncthreads_and(mbar_wait(rkbar, 0, a.wait_polls));   // false: the tiles are skipped below
-    rotate_q<S::HP, NW>(sq, rfr, sqr);
+    rotate_q<S::HP, NW>(sq, rkf, sqr);
     for (int hh = warp; hh < S::HP; hh += NW) {
 #pragma unroll
       for (int grp = 0; grp < NG; ++grp) {
@@ -929,7 +915,6 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
   }
   ok = __syncthreads_and(ok);   // every warp is done with its ring before the results reuse it
   if (lane < kStages) mbar_inval(wbar + lane);
-  if (threadIdx.x == 0) mbar_inval(rkbar);
   if (!ok) {   // the split's result is skipped
     write_empty_partial<G, NW>(part);
     return;
