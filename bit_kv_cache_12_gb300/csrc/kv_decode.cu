@@ -64,6 +64,11 @@ constexpr int kMaxPids = 1032;   // page ids staged per CTA (a split covers <= 1
 constexpr int kTierRows = 320;   // sink + recent storage rows staged per tier CTA
 constexpr int kTierRowK = 272;   // staged K row stride (bytes): 256 + 16 keeps lane reads conflict-free
 constexpr int kTierRowV = 272;   // staged V row stride: the transposed ldmatrix reads are conflict-free too
+// q rows staged for rotate_q: channel c of row h at h * kQStride + c + 4 (c / 32),
+// so that the rotation's float4 reads (row r, channels 32 j + 4 s ..) spread over
+// all banks; q' rows are kQrStride apart for the same reason in the fragment build.
+constexpr int kQStride = 168;
+constexpr int kQrStride = 136;
 // The history loop keeps each head's exponent reference kSlack (log2 units)
 // above the largest score seen when it was last moved, so weights stay <= 1
 // and the accumulators are rescaled only when a score passes the reference.
@@ -152,7 +157,8 @@ struct RotFrags {
 };
 
 // q'[h][c] = sum_i q[h][i] R_k[i][c] for the first NROWS rows of X (shared,
-// [*][128] fp32 holding bf16 values), on the tensor cores: R_k comes as fp16
+// fp32 holding bf16 values, rows kQStride apart with 4 floats of padding after
+// every 32 channels) into Y (rows kQrStride apart), on the tensor cores: R_k comes as fp16
 // hi + lo B fragments (rotation fragment block 0, this warp's in registers), q is
 // scaled by 2^-8 (exact) and split into fp16 hi + lo, and the three products
 // above 2^-22 relative are accumulated in fp32, each in two chains (even and
@@ -175,7 +181,7 @@ __device__ void rotate_q(const float* X, const RotFrags<NW>& rkf, float* Y) {
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
     // A: row r, k index kappa -> input channel 32*(kappa%8/2) + 4s + 2*(kappa/8) + kappa%2
-    float4 x = row_ok ? *reinterpret_cast<const float4*>(X + r * 128 + 32 * j + 4 * s)
+    float4 x = row_ok ? *reinterpret_cast<const float4*>(X + r * kQStride + 36 * j + 4 * s)
                       : make_float4(0.f, 0.f, 0.f, 0.f);
     x.x *= kIn; x.y *= kIn; x.z *= kIn; x.w *= kIn;
     const __half2 h01 = __floats2half2_rn(x.x, x.y), h23 = __floats2half2_rn(x.z, x.w);
@@ -200,7 +206,7 @@ __device__ void rotate_q(const float* X, const RotFrags<NW>& rkf, float* Y) {
 #pragma unroll
         for (int e = 0; e < 2; ++e)
           y[e] = ((acc[u][0][e] + acc[u][3][e]) + ((acc[u][1][e] + acc[u][4][e]) + (acc[u][2][e] + acc[u][5][e])));
-        *reinterpret_cast<float2*>(Y + r * 128 + 8 * (warp + u * NW) + 2 * j) =
+        *reinterpret_cast<float2*>(Y + r * kQrStride + 8 * (warp + u * NW) + 2 * j) =
             make_float2(y[0] * 256.0f, y[1] * 256.0f);
       }
   }
@@ -304,7 +310,7 @@ __device__ __forceinline__ uint32_t split_hi_lo_bf16(float x) {
 
 // q of the GQA group (bf16 -> fp32) into shared memory; padded heads are 0.
 // No barrier.
-template <int G, int NW, bool kMulti = false>
+template <int G, int NW, bool kMulti = false, bool kPad = false>
 __device__ void load_q(const DecodeArgs& a, int b, int g, float* sq, int padded_heads) {
   for (int idx = threadIdx.x; idx < padded_heads * 128; idx += NW * 32) {
     const int h = idx >> 7, c = idx & 127;
@@ -314,7 +320,7 @@ __device__ void load_q(const DecodeArgs& a, int b, int g, float* sq, int padded_
                                 : (size_t)b * a.Hq + g * G + h;
       v = __uint_as_float((uint32_t)a.q[row * 128 + c] << 16);
     }
-    sq[idx] = v;
+    sq[kPad ? h * kQStride + c + 4 * (c >> 5) : idx] = v;
   }
 }
 
@@ -463,9 +469,9 @@ struct HistLay {
   static constexpr int saddr = bars + NW * kStages * 8;   // [64 NW] tile source addresses
   static constexpr int spid = saddr + 64 * NW * 8;        // [kMaxPids] page ids
   static constexpr int HP = (G <= 4) ? 4 : 8;             // padded heads (MMA columns)
-  static constexpr int sq = spid + kMaxPids * 4;          // [HP][128] q (q' computed in the CTA)
-  static constexpr int sqr = sq + HP * 128 * 4;           // [HP][128] q'
-  static constexpr int ssum = sqr + HP * 128 * 4;         // [HP][2] per-group sums of q'
+  static constexpr int sq = spid + kMaxPids * 4;          // [HP][kQStride] q (q' computed in the CTA)
+  static constexpr int sqr = sq + HP * kQStride * 4;      // [HP][kQrStride] q'
+  static constexpr int ssum = sqr + HP * kQrStride * 4;   // [HP][2] per-group sums of q'
   static constexpr int total = ssum + HP * 2 * 4;
   static constexpr int swo = 0;                           // [NW][G][128] per-warp o'
   static constexpr int swm = swo + NW * G * 128 * 4;      // [NW][G] m
@@ -561,7 +567,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
   }
   for (int i = threadIdx.x; i < p_all; i += NW * 32) spid[i] = __ldg(ptrow + p_begin + i);
   float* sq = reinterpret_cast<float*>(smb + S::sq);
-  if (local) load_q<G, NW, kMulti>(a, b, g, sq, S::HP);
+  if (local) load_q<G, NW, kMulti, true>(a, b, g, sq, S::HP);
   int h = __ldg(a.hist_len + b);
   // the grid covers max_len history tokens (and the page table max_pages pages)
   const int cap = min(a.max_pages * a.page_size, a.max_len);
@@ -631,7 +637,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
 #pragma unroll
       for (int grp = 0; grp < NG; ++grp) {
         float v = 0.f;
-        for (int c = grp * GS + lane; c < (grp + 1) * GS; c += 32) v += sqr[hh * 128 + c];
+        for (int c = grp * GS + lane; c < (grp + 1) * GS; c += 32) v += sqr[hh * kQrStride + c];
         v = warp_sum_xor(v, 1);
         if (lane == 0) ssum[hh * 2 + grp] = v;
       }
@@ -643,7 +649,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
     for (int s = 0; s < 8; ++s)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const float* row = sqr + (4 * nt + hl) * 128 + 16 * s + 2 * j;
+        const float* row = sqr + (4 * nt + hl) * kQrStride + 16 * s + 2 * j;
         // group 64: the odd steps' code factor 16 is cancelled here (a power of 2);
         // group 128 removes it from the odd steps' accumulator chain instead
         const float f = (GS == 64 && (s & 1)) ? 0.0625f : 1.0f;
