@@ -79,7 +79,7 @@ __global__ void rotation_frag_kernel(const float* __restrict__ Rk, const float* 
   if (idx >= Hkv * kFragBlocks * 4096) return;
   const int h = idx / (kFragBlocks * 4096), block = (idx / 4096) % kFragBlocks, f = idx & 4095;
   uint4 out;
-  if (block >= 1) {
+  if (block == 1 || block == 2) {
     // tcgen05 B operand of x . R (block 1: R_k, block 2: R_v): row n holds
     // R[k][n % 128] for k = 0..127 as its bf16 hi (n < 128) or lo (n >= 128)
     // term; 128-byte rows, channels 0-63 in the first 32 KB, 64-127 in the
@@ -97,10 +97,12 @@ __global__ void rotation_frag_kernel(const float* __restrict__ Rk, const float* 
     }
     out = make_uint4(pack2(e[0], e[1]), pack2(e[2], e[3]), pack2(e[4], e[5]), pack2(e[6], e[7]));
   } else {
-    // mma.sync B operand of q . R_k as fp16 hi / lo pairs (decode q' = q R_k):
+    // mma.sync B operand of q . R_k (block 0, decode q' = q R_k) or of
+    // o' . R_v^T (block 3, the decode's back-rotation) as fp16 hi / lo pairs:
     // fragment f = (k-step s, n-tile nt, lane); element (kappa, n) =
-    // R_k[in_ch(s, kappa)][8 nt + n], lane (r, j) holding kappa = 2j, 2j+1,
-    // 2j+8, 2j+9 (the decode loads q with the same channel order)
+    // M[in_ch(s, kappa)][8 nt + n] for M = R_k or R_v^T, lane (r, j) holding
+    // kappa = 2j, 2j+1, 2j+8, 2j+9 (the decode stages its rows in the same
+    // channel order)
     const int lane = f & 31, r = lane >> 2, j = lane & 3;
     const int nt = (f >> 5) & 15, s = f >> 9;
     const int col = 8 * nt + r;
@@ -108,7 +110,9 @@ __global__ void rotation_frag_kernel(const float* __restrict__ Rk, const float* 
     const int ks[4] = {2 * j, 2 * j + 1, 2 * j + 8, 2 * j + 9};
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const float m = Rk[(size_t)h * 16384 + in_ch(s, ks[u]) * 128 + col];
+      const int in = in_ch(s, ks[u]);
+      const float m = (block == 0) ? Rk[(size_t)h * 16384 + in * 128 + col]
+                                   : Rv[(size_t)h * 16384 + col * 128 + in];   // R_v^T[in][col]
       const __half hh = __float2half_rn(m);
       hi[u] = __half_as_ushort(hh);
       lo[u] = __half_as_ushort(__float2half_rn(m - __half2float(hh)));

@@ -501,7 +501,15 @@ struct TierLay {
   static constexpr int GP = (G + 3) & ~3;
   static constexpr int oh = rv + 128 * 128 * 4;                        // [128][GP] merged history o', transposed
   static constexpr int spr = swo;                                      // [NW][G][128] row-slice sums
-  static_assert(oh + GP * 128 * 4 <= tier_o, "R_v^T and the merge fit in the staging area");
+  static_assert(oh + GP * 128 * 4 <= tier_o && spr + NW * G * 128 * 4 <= rv,
+                "R_v^T, the row-slice sums and the merge fit in the staging area");
+  // the tensor-core back-rotation (more than 4 query columns) instead of rv / oh / spr
+  static constexpr int HP = (G <= 4) ? 4 : 8;                          // rows of the back-rotation
+  static constexpr int sx = (swl + NW * G * 4 + 15) / 16 * 16;         // [HP][kQStride] scaled o'/L
+  static constexpr int sy = sx + HP * kQStride * 4;                    // [HP][kQrStride] rotated
+  static constexpr int smax = sy + HP * kQrStride * 4;                 // [HP] max |o'/L| (bits)
+  static constexpr int sinv = smax + HP * 4;                           // [HP] 1 / scale
+  static_assert(sinv + HP * 4 <= tier_o, "the back-rotation fits in the staging area");
 };
 
 template <int G, int GS>
@@ -1150,10 +1158,14 @@ __device__ void tier_merge(const DecodeArgs& a, int b, int g, uint8_t* smb) {
   __syncthreads();
   merge_warps<G, NW>(swo, swm, swl, tier_o, tier_m, tier_l);   // ends with a barrier
 
-  // ---- R_v^T (for the one back-rotation) into the staging area, now free ----
+  // ---- R_v^T for the one back-rotation: up to 4 query columns as fp32 into the
+  // staging area, now free (SIMT rotation); more as MMA fragments in registers
+  // (tensor-core rotation), both while the history splits finish ----
   uint64_t* rbar = reinterpret_cast<uint64_t*>(smb + S::bar);
   float* srv = reinterpret_cast<float*>(smb + S::rv);
-  if (threadIdx.x == 0) {
+  RotFrags<NW> rvf;
+  if constexpr (G > 4) rvf.load(a.rfrag + ((size_t)g * kFragBlocks + 3) * 4096);
+  if (G <= 4 && threadIdx.x == 0) {
     mbar_init(rbar, 1);
     mbar_fence_init();
     const float* R = a.RvT + (size_t)g * 128 * 128;
@@ -1236,6 +1248,7 @@ __device__ void tier_merge(const DecodeArgs& a, int b, int g, uint8_t* smb) {
   }
   if (!merged_all && threadIdx.x == 0) flag_error(a.err, KV_DEVERR_TIMEOUT);
 
+  if constexpr (G <= 4) {
   // ---- back to the original basis once: o_hist[h][c] = sum_i o'[h][i] R_v^T[i][c].
   // o' goes to shared memory transposed ([c][GP]); each row of R_v^T is read
   // once for all heads: warp w takes rows w, w + NW, .., lane cq columns
@@ -1306,9 +1319,75 @@ __device__ void tier_merge(const DecodeArgs& a, int b, int g, uint8_t* smb) {
       a.out[((size_t)b * a.Hq + g * G + hh) * 128 + c] = val;
     }
   }
+  } else {
+  // ---- back to the original basis once, on the tensor cores:
+  // o_hist[h][c] = sum_i o'[h][i] R_v^T[i][c].  Each head's merged o' is
+  // normalised by its l and scaled by a power of two that puts its largest
+  // component near 2^10, so that the fp16 hi + lo terms of rotate_q keep about
+  // 22 bits of every component; the scale is taken out afterwards ----
+  constexpr int HP = S::HP;
+  float* sx = reinterpret_cast<float*>(smb + S::sx);
+  float* sy = reinterpret_cast<float*>(smb + S::sy);
+  unsigned* smax = reinterpret_cast<unsigned*>(smb + S::smax);
+  float* sinv = reinterpret_cast<float*>(smb + S::sinv);
+  float* hist_m = reinterpret_cast<float*>(smb + S::hist_m);
+  float* hist_l = reinterpret_cast<float*>(smb + S::hist_l);
+  if (threadIdx.x < HP) smax[threadIdx.x] = 0u;
+  for (int idx = G * 128 + threadIdx.x; idx < HP * 128; idx += NW * 32)   // padded rows
+    sx[(idx >> 7) * kQStride + (idx & 127) + 4 * ((idx & 127) >> 5)] = 0.f;
+  __syncthreads();
+  float ov[EPT];
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    const int idx = threadIdx.x + e * NW * 32;
+    ov[e] = 0.f;
+    if (idx < G * 128) {
+      ov[e] = (L[e] > 0.f) ? O[e] / L[e] : 0.f;
+      atomicMax(smax + (idx >> 7), __float_as_uint(fabsf(ov[e])));   // order-free: a maximum
+      if ((idx & 127) == 0) {
+        hist_m[idx >> 7] = M[e];
+        hist_l[idx >> 7] = L[e];
+      }
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    const int idx = threadIdx.x + e * NW * 32;
+    if (idx < G * 128) {
+      const int hh = idx >> 7, c = idx & 127;
+      const uint32_t mb = smax[hh];
+      // 2^(10 - exponent of the largest component); 1 for an all-zero (or non-finite) row
+      const int ex = (int)((mb >> 23) & 0xFFu) - 127;
+      const float scale = (mb == 0u || ex > 127) ? 1.0f : ldexpf(1.0f, 10 - max(ex, -100));
+      sx[hh * kQStride + c + 4 * (c >> 5)] = ov[e] * scale;
+      if (c == 0) sinv[hh] = 1.0f / scale;
+    }
+  }
+  __syncthreads();
+  rotate_q<HP, NW>(sx, rvf, sy);   // ends with a barrier
+  for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
+    const int hh = idx >> 7, c = idx & 127;
+    const float Mh = hist_m[hh], Lh = hist_l[hh], mt = tier_m[hh], lt = tier_l[hh];
+    const float oh = sy[hh * kQrStride + c] * sinv[hh] * Lh;   // the unnormalised rotated sum
+    const float Mx = fmaxf(Mh, mt);
+    const float fh = (Mh == kNegInf) ? 0.f : exp2f(Mh - Mx);
+    const float ft = (mt == kNegInf) ? 0.f : exp2f(mt - Mx);
+    const float Lt = fmaf(Lh, fh, lt * ft);
+    const float val = (Lt > 0.f) ? fmaf(oh, fh, tier_o[idx] * ft) / Lt : 0.f;
+    if constexpr (kMulti) {
+      const size_t row = ((size_t)b * a.T + hh / a.Gq) * a.Hq + g * a.Gq + hh % a.Gq;
+      a.out[row * 128 + c] = val;
+      // ln sum exp(scaled score) = ln 2 * (M + log2 L), the scores being in log2 units
+      if (a.lse && c == 0) a.lse[row] = (Lt > 0.f) ? 0.6931471805599453f * (Mx + log2f(Lt)) : kNegInf;
+    } else {
+      a.out[((size_t)b * a.Hq + g * G + hh) * 128 + c] = val;
+    }
+  }
+  }
   __syncthreads();
   if (threadIdx.x < kMaskWords) mask[threadIdx.x] = 0u;   // ready for the next call
-  if (threadIdx.x == 0) mbar_inval(rbar);
+  if (G <= 4 && threadIdx.x == 0) mbar_inval(rbar);
 }
 
 template <int G, int GS, bool kMulti>

@@ -55,7 +55,8 @@ struct Pool {
 //   block 1: tcgen05 B operand of x . R_k: rows n of [R_k^T hi ; R_k^T lo] (256 x 128
 //            bf16), K-major, 128-byte swizzle, channels 0-63 then 64-127 (append K)
 //   block 2: the same for R_v (append V)
-constexpr int kFragBlocks = 3;
+//   block 3: mma.sync B operand of o' . R_v^T, laid out as block 0 (decode back-rotation)
+constexpr int kFragBlocks = 4;
 inline size_t rfrag_per_head() { return 4096; }   // uint4 per (head, block)
 
 // ---- launchers (return cudaSuccess or the launch error) --------------------
