@@ -202,30 +202,65 @@ struct Chunk {
   bool live;
 };
 
-__device__ __forceinline__ Chunk chunk_of(const TcArgs& a, int task, bool flag) {
-  Chunk k;
-  k.b = task / a.max_chunks;
-  const int ci = task % a.max_chunks;
-  k.c0 = __ldg(a.cu + k.b);
-  k.nb = __ldg(a.cu + k.b + 1) - k.c0;
-  k.h0 = __ldg(a.hist_start + k.b);
-  k.live = false;
-  if (k.nb <= 0) {
-    if (flag && k.nb < 0 && ci == 0) flag_error(a.err, KV_DEVERR_SEQ_RANGE);
+// Walks the tasks [t, t1) of a CTA in order without divisions: the sequence
+// index and the chunk index within it advance together, and a sequence's
+// range (cu, hist_start) is read once, when the walk enters it.  Errors of a
+// sequence (a negative or out-of-range span, more chunks than the grid covers)
+// are reported by the thread that walks into its first chunk with `flag` set.
+struct TaskCursor {
+  int t, t1, b, ci;
+  int c0, nb, h0, first, last;
+  bool seq_ok;
+  __device__ void enter(const TcArgs& a, bool flag) {   // the sequence of task t
+    c0 = __ldg(a.cu + b);
+    nb = __ldg(a.cu + b + 1) - c0;
+    h0 = __ldg(a.hist_start + b);
+    seq_ok = false;
+    if (nb <= 0) {
+      if (flag && nb < 0 && ci == 0) flag_error(a.err, KV_DEVERR_SEQ_RANGE);
+      return;
+    }
+    if (h0 < 0 || (long long)h0 + nb > (long long)a.max_pages * a.P) {
+      if (flag && ci == 0) flag_error(a.err, KV_DEVERR_SEQ_RANGE);
+      return;
+    }
+    first = h0 / kTile;
+    last = (h0 + nb - 1) / kTile;
+    if (flag && ci == 0 && (last - first) / kTilesPerChunk + 1 > a.max_chunks) flag_error(a.err, KV_DEVERR_LENGTH);
+    seq_ok = true;
+  }
+  __device__ void start(const TcArgs& a, int t0, int t_end, bool flag) {
+    t = t0;
+    t1 = t_end;
+    b = t0 / a.max_chunks;
+    ci = t0 - b * a.max_chunks;
+    if (t < t1) enter(a, flag);
+  }
+  __device__ bool live() const { return seq_ok && (first + ci * kTilesPerChunk) <= last; }
+  __device__ void step(const TcArgs& a, bool flag) {
+    ++t;
+    if (++ci == a.max_chunks) {
+      ci = 0;
+      ++b;
+      if (t < t1) enter(a, flag);
+    }
+  }
+  __device__ void next_live(const TcArgs& a, bool flag) {   // from the current task on
+    while (t < t1 && !live()) step(a, flag);
+  }
+  __device__ Chunk chunk() const {
+    Chunk k;
+    k.b = b;
+    k.c0 = c0;
+    k.nb = nb;
+    k.h0 = h0;
+    k.first = first;
+    k.last = last;
+    k.P0 = (first + ci * kTilesPerChunk) * kTile;
+    k.live = live();
     return k;
   }
-  if (k.h0 < 0 || (long long)k.h0 + k.nb > (long long)a.max_pages * a.P) {
-    if (flag && ci == 0) flag_error(a.err, KV_DEVERR_SEQ_RANGE);
-    return k;
-  }
-  k.first = k.h0 / kTile;
-  k.last = (k.h0 + k.nb - 1) / kTile;
-  if (flag && ci == 0 && (k.last - k.first) / kTilesPerChunk + 1 > a.max_chunks)
-    flag_error(a.err, KV_DEVERR_LENGTH);
-  k.P0 = (k.first + ci * kTilesPerChunk) * kTile;
-  k.live = k.P0 <= k.last * kTile;
-  return k;
-}
+};
 
 // x rows of a chunk -> the swizzled A operand: thread t copies half a row
 // (row t % 128, channels 64 * (t / 128) ..); rows outside the append range are zero
@@ -442,11 +477,9 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
   const int total = a.n_seqs * a.max_chunks;
   const int t0 = blockIdx.x * a.tasks_per_cta;
   const int t1 = min(total, t0 + a.tasks_per_cta);
-  auto next_live = [&](int t) {
-    for (; t < t1; ++t)
-      if (chunk_of(a, t, tid == 0).live) return t;
-    return t1;
-  };
+  // the walk over this CTA's tasks (every thread holds the same cursor)
+  TaskCursor tc;
+  tc.start(a, t0, t1, tid == 0);
   // x of a chunk: two TMA tile loads by one thread when all 128 rows lie
   // below the input's row count T and inside the tensor map (rows below 0 read
   // as zero); otherwise, so that nothing past the caller's buffer is read and
@@ -467,8 +500,10 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
     load_chunk(a, X, g, k, sA);
     return false;
   };
-  int cur = next_live(t0);
-  bool cur_tma = (cur < t1) ? issue_load(chunk_of(a, cur, false)) : false;
+  tc.next_live(a, tid == 0);
+  int cur = tc.t;
+  Chunk kc = tc.chunk();
+  bool cur_tma = (cur < t1) ? issue_load(kc) : false;
 
   bool ok = mbar_wait(bars + 0, 0, kTcPolls);   // R is needed before the first MMA
   if (!__syncthreads_and(ok)) {
@@ -488,7 +523,7 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
   const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
   bool x_pending = false;   // a TMA load whose completion has not been waited for
   while (cur < t1) {
-    const Chunk k = chunk_of(a, cur, false);
+    const Chunk k = kc;
     if (cur_tma) {
       ok = mbar_wait(bars + 2, xphase, kTcPolls);
       xphase ^= 1;
@@ -509,8 +544,11 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
     if (!__syncthreads_and(ok)) break;
     tc_fence_after();
     // the A buffer is consumed: bring in the next chunk behind this epilogue
-    const int nxt = next_live(cur + 1);
-    const bool nxt_tma = (nxt < t1) ? issue_load(chunk_of(a, nxt, false)) : false;
+    tc.step(a, tid == 0);
+    tc.next_live(a, tid == 0);
+    const int nxt = tc.t;
+    const Chunk kn = tc.chunk();
+    const bool nxt_tma = (nxt < t1) ? issue_load(kn) : false;
 
     // ---- this thread's row and channel half -> s, z and codes ----
     constexpr int NS = (TENSOR == 0) ? 4 : 8;
@@ -601,6 +639,7 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
     tc_fence_before();
     __syncthreads();   // the accumulator is free for the next chunk
     cur = nxt;
+    kc = kn;
     cur_tma = nxt_tma;
   }
 
