@@ -398,20 +398,26 @@ __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, con
     return (TENSOR == 0) ? 16 * (kk & 1) + 2 * (2 * s1 + 4 * (kk >> 3)) : 2 * (2 * s1 + (kk >> 3));
   };
   auto pack = [&](int i, uint32_t c) { word_of(i) |= c << pos_of(i); };
-  // code = rint(clamp(fl(fl(y - z) * fl(1/s)), 0, 3)): the clamped quotient
-  // plus 1.5 * 2^23 holds rint in its low mantissa bits (round to nearest
-  // even); unless some quotient lies within 2^-18 of a half-integer, where
-  // the IEEE division decides (quant_code).  Out of [0, 3] the clamp leaves
-  // an integer, so only ties inside the range can set the fix-up.
+  // code = rint(clamp(fl(fl(y - z) / s), 0, 3)).  The clamped quotient is
+  // formed as 3 * sat(fl(y - z) * fl(fl(1/s) / 3)) (the saturating multiply
+  // clamps to [0, 1] for free; the result lies within 1e-6 of fl(fl(y - z) /
+  // s) clamped); plus 1.5 * 2^23 it holds rint in its low mantissa bits (round
+  // to nearest even), unless some quotient lies within 2^-18 of a
+  // half-integer, where the IEEE division decides (quant_code).  Out of
+  // [0, 3] the clamp leaves an integer, so only ties inside the range can set
+  // the fix-up.
   clear();
   float emax = 0.0f;
+  const float rs3 = __fmul_rn(q.rs, 0.3333333432674408f);   // the quotient / 3, saturated to [0, 1]
 #pragma unroll
   for (int cb = 0; cb < 2; ++cb) {
     float v[32];
     rotated32(cb, v);
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const float t = fminf(fmaxf(__fmul_rn(__fsub_rn(v[i], q.z), q.rs), 0.0f), 3.0f);
+      float u;
+      asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(u) : "f"(__fsub_rn(v[i], q.z)), "f"(rs3));
+      const float t = __fmul_rn(u, 3.0f);
       const float rr = __fadd_rn(t, 12582912.0f);
       // the bits of rr are 0x4B400000 + code: one integer multiply-add places
       // the code (the constant offsets of a word fold into one; codes do not
@@ -524,24 +530,27 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
   bool x_pending = false;   // a TMA load whose completion has not been waited for
   while (cur < t1) {
     const Chunk k = kc;
+    // x of the chunk: thread 0 alone waits for a TMA load (it issues the MMA);
+    // 16-byte copies are every thread's and end with the CTA's barrier
+    bool xok = true;
     if (cur_tma) {
-      ok = mbar_wait(bars + 2, xphase, kTcPolls);
+      if (tid == 0) xok = mbar_wait(bars + 2, xphase, kTcPolls);
       xphase ^= 1;
-      if (!__syncthreads_and(ok)) {
-        x_pending = true;
-        break;
-      }
     } else {
       asm volatile("cp.async.wait_group 0;" ::: "memory");
       fence_async_smem();
       __syncthreads();
     }
 
-    // ---- x' = x . R_hi + x . R_lo on the tensor cores ----
-    if (tid == 0) issue_rotation(tmem, sA, sB, bars + 1);
+    // ---- x' = x . R_hi + x . R_lo on the tensor cores (not issued if x did
+    // not arrive: every thread's wait below then runs out) ----
+    if (tid == 0 && xok) issue_rotation(tmem, sA, sB, bars + 1);
     ok = mbar_wait(bars + 1, phase, kTcPolls);
     phase ^= 1;
-    if (!__syncthreads_and(ok)) break;
+    if (!__syncthreads_and(ok)) {
+      x_pending = !xok;
+      break;
+    }
     tc_fence_after();
     // the A buffer is consumed: bring in the next chunk behind this epilogue
     tc.step(a, tid == 0);
@@ -550,17 +559,17 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
     const Chunk kn = tc.chunk();
     const bool nxt_tma = (nxt < t1) ? issue_load(kn) : false;
 
-    // ---- this thread's row and channel half -> s, z and codes ----
-    constexpr int NS = (TENSOR == 0) ? 4 : 8;
-    uint32_t wd[NS][2];
-    const ScaleZero q = row_codes<GS, TENSOR>(trow, hf, m, sclip, sstat, wd);
-
-    // ---- destination tile of this row ----
+    // ---- destination tile of this row (its page id read before the epilogue) ----
     const int pos = k.P0 + m;
     const bool row_ok = pos >= k.h0 && pos < k.h0 + k.nb;
     const int tile = pos / kTile;
     const bool tile_live = tile <= k.last;
     const int pid_raw = __ldg(a.pt + (size_t)k.b * a.max_pages + min((tile * kTile) / a.P, a.max_pages - 1));
+
+    // ---- this thread's row and channel half -> s, z and codes ----
+    constexpr int NS = (TENSOR == 0) ? 4 : 8;
+    uint32_t wd[NS][2];
+    const ScaleZero q = row_codes<GS, TENSOR>(trow, hf, m, sclip, sstat, wd);
     const bool pid_ok = pid_raw >= 0 && pid_raw < a.num_pages;
     if (tile_live && !pid_ok && m16 == 0 && hf == 0) flag_error(a.err, KV_DEVERR_PAGE_ID);
     const bool write = tile_live && pid_ok;
