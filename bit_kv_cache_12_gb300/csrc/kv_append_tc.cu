@@ -399,13 +399,13 @@ __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, con
   };
   auto pack = [&](int i, uint32_t c) { word_of(i) |= c << pos_of(i); };
   // code = rint(clamp(fl(fl(y - z) / s), 0, 3)).  The clamped quotient is
-  // formed as 3 * sat(fl(y - z) * fl(fl(1/s) / 3)) (the saturating multiply
-  // clamps to [0, 1] for free; the result lies within 1e-6 of fl(fl(y - z) /
-  // s) clamped); plus 1.5 * 2^23 it holds rint in its low mantissa bits (round
-  // to nearest even), unless some quotient lies within 2^-18 of a
-  // half-integer, where the IEEE division decides (quant_code).  Out of
-  // [0, 3] the clamp leaves an integer, so only ties inside the range can set
-  // the fix-up.
+  // 3 u with u = sat(fl(y - z) * fl(fl(1/s) / 3)) (the saturating multiply
+  // clamps to [0, 1] for free; 3 u lies within 1e-6 of fl(fl(y - z) / s)
+  // clamped); 3 u + 1.5 * 2^23, rounded once, holds rint(3 u) in its low
+  // mantissa bits (round to nearest even), unless some quotient lies within
+  // 2^-18 of a half-integer, where the IEEE division decides (quant_code).
+  // Out of [0, 3] the clamp leaves an integer, so only ties inside the range
+  // can set the fix-up.
   clear();
   float emax = 0.0f;
   const float rs3 = __fmul_rn(q.rs, 0.3333333432674408f);   // the quotient / 3, saturated to [0, 1]
@@ -417,14 +417,13 @@ __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, con
     for (int i = 0; i < 32; ++i) {
       float u;
       asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(u) : "f"(__fsub_rn(v[i], q.z)), "f"(rs3));
-      const float t = __fmul_rn(u, 3.0f);
-      const float rr = __fadd_rn(t, 12582912.0f);
-      // the bits of rr are 0x4B400000 + code: one integer multiply-add places
-      // the code (the constant offsets of a word fold into one; codes do not
-      // overlap, so the sum is the OR)
+      // rr = 3 u + 1.5 * 2^23 rounded once: its bits are 0x4B400000 + code
+      const float rr = __fmaf_rn(u, 3.0f, 12582912.0f);
+      // one integer multiply-add places the code (the constant offsets of a
+      // word fold into one; codes do not overlap, so the sum is the OR)
       const int pos = pos_of(32 * cb + i);
       word_of(32 * cb + i) += __float_as_uint(rr) * (1u << pos) - (0x4B400000u << pos);
-      v[i] = fabsf(__fsub_rn(t, __fsub_rn(rr, 12582912.0f)));
+      v[i] = fabsf(__fmaf_rn(u, 3.0f, -__fsub_rn(rr, 12582912.0f)));   // distance to the code
     }
     emax = max_of32(emax, v);
   }
