@@ -476,7 +476,7 @@ struct HistLay {
   static constexpr int swo = 0;                           // [NW][G][128] per-warp o'
   static constexpr int swm = swo + NW * G * 128 * 4;      // [NW][G] m
   static constexpr int swl = swm + NW * G * 4;            // [NW][G] l
-  static_assert(swl + NW * G * 4 <= bars, "the warp results fit in the ring");
+  static_assert(swl + NW * G * 4 + G * 4 <= bars, "the warp results fit in the ring");
 };
 
 // Shared memory of a tier CTA (byte offsets).  R_v^T, the warp results and the
@@ -963,25 +963,33 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
     }
   }
   __syncthreads();
-  // the warps merged with the log-sum-exp rule into the split's partial (rotated basis)
-  for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
-    const int hh = idx >> 7, c = idx & 127;
+  // the warps merged with the log-sum-exp rule into the split's partial (rotated
+  // basis): each head's maximum, then every warp's weight exp2(m_w - M) once,
+  // then every output element a sum of NW products
+  float* sM = swl + NW * G;   // [G]
+  if (threadIdx.x < G) {
     float M = kNegInf;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, swm[w * G + hh]);
-    float L = 0.f, O = 0.f;
-    if (M != kNegInf) {
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, swm[w * G + threadIdx.x]);
+    sM[threadIdx.x] = M;
+  }
+  __syncthreads();
+  if (threadIdx.x < NW * G) {   // swm becomes the warps' weights
+    const float mw = swm[threadIdx.x], M = sM[threadIdx.x % G];
+    swm[threadIdx.x] = (mw == kNegInf || M == kNegInf) ? 0.f : exp2f(mw - M);
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
+    const int hh = idx >> 7, c = idx & 127;
+    float O = 0.f;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float mw = swm[w * G + hh];
-        const float f = (mw == kNegInf) ? 0.f : exp2f(mw - M);
-        L = fmaf(f, swl[w * G + hh], L);
-        O = fmaf(f, swo[(w * G + hh) * 128 + c], O);
-      }
-    }
+    for (int w = 0; w < NW; ++w) O = fmaf(swm[w * G + hh], swo[(w * G + hh) * 128 + c], O);
     part[hh * kPart + 4 + c] = O;
     if (c == 0) {
-      part[hh * kPart + 0] = M;
+      float L = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) L = fmaf(swm[w * G + hh], swl[w * G + hh], L);
+      part[hh * kPart + 0] = sM[hh];
       part[hh * kPart + 1] = L;
     }
   }
