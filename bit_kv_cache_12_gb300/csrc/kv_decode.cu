@@ -1198,6 +1198,102 @@ __device__ void tier_merge(const DecodeArgs& a, int b, int g, uint8_t* smb) {
   unsigned* mask = a.arrive + seq_head * kMaskWords;
   const float* pbase = a.ws + seq_head * a.n_split * G * kPart;
   bool merged_all = true;
+  if constexpr (G > 4) {
+  // 8 query columns: per-head maxima and weights computed once per batch
+  // (fewer exponentials than per element, which pays off at this width; with
+  // fewer columns the extra barriers cost more than they save); per-head state
+  // and the batch's weights in the (dead) tier warp results
+  float* sml = reinterpret_cast<float*>(smb + S::swo);   // [kMergeBatch][G] (m, l)
+  float* sf = sml + 2 * kMergeBatch * G;                  // [kMergeBatch][G] weights
+  float* sMh = sf + kMergeBatch * G;                      // [G] running m
+  float* sLh = sMh + G;                                   // [G] running l
+  float* sal = sLh + G;                                   // [G] rescale of the running sums
+  if (threadIdx.x < G) {
+    sMh[threadIdx.x] = kNegInf;
+    sLh[threadIdx.x] = 0.f;
+  }
+  for (int s0 = 0; s0 < a.n_split; s0 += kMergeBatch) {
+    const int s1 = min(a.n_split, s0 + kMergeBatch);
+    if (threadIdx.x == 0) {   // wait (bounded) until splits s0 .. s1-1 have arrived
+      int done = 0;
+      for (int it = 0; it < a.merge_polls && !done; ++it) {
+        done = 1;
+        for (int s = s0; s < s1 && done; s += 32 - (s & 31)) {
+          const int n = min(s1 - s, 32 - (s & 31));
+          const unsigned want = (n == 32 ? ~0u : ((1u << n) - 1u)) << (s & 31);
+          done = (ld_acquire_u32(mask + (s >> 5)) & want) == want;
+        }
+        if (!done) __nanosleep(64);
+      }
+      ctl[0] = done;
+    }
+    __syncthreads();
+    const bool arrived = ctl[0] != 0;
+    __syncthreads();   // ctl is rewritten for the next batch
+    if (!arrived) {
+      merged_all = false;
+      break;
+    }
+    // one round of loads: every thread its o values of the batch, the first
+    // threads the (m, l) of every (split, head)
+    const int nb = s1 - s0;
+    float ov[EPT][kMergeBatch];
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      const int idx = threadIdx.x + e * NW * 32;
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u)
+        ov[e][u] = (idx < G * 128 && u < nb)
+                       ? __ldcg(pbase + ((size_t)(s0 + u) * G + (idx >> 7)) * kPart + 4 + (idx & 127))
+                       : 0.f;
+    }
+    for (int i = threadIdx.x; i < nb * G; i += NW * 32) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(pbase + ((size_t)s0 * G + i) * kPart));
+      sml[2 * i] = ml.x;
+      sml[2 * i + 1] = ml.y;
+    }
+    __syncthreads();
+    if (threadIdx.x < G) {   // each head's new maximum and the rescale of its running sums
+      const int hh = threadIdx.x;
+      float Mb = sMh[hh];
+      for (int u = 0; u < nb; ++u) Mb = fmaxf(Mb, sml[2 * (u * G + hh)]);
+      sal[hh] = (sMh[hh] == kNegInf || Mb == kNegInf) ? 0.f : exp2f(sMh[hh] - Mb);
+      sMh[hh] = Mb;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < nb * G; i += NW * 32) {   // every (split, head)'s weight
+      const float mv = sml[2 * i], Mb = sMh[i % G];
+      sf[i] = (mv == kNegInf || Mb == kNegInf) ? 0.f : exp2f(mv - Mb);
+    }
+    __syncthreads();
+    if (threadIdx.x < G) {
+      const int hh = threadIdx.x;
+      float Le = sLh[hh] * sal[hh];
+      for (int u = 0; u < nb; ++u) Le = fmaf(sf[u * G + hh], sml[2 * (u * G + hh) + 1], Le);
+      sLh[hh] = Le;
+    }
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      const int idx = threadIdx.x + e * NW * 32;
+      if (idx < G * 128) {
+        const int hh = idx >> 7;
+        float Oe = O[e] * sal[hh];
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) Oe = fmaf(u < nb ? sf[u * G + hh] : 0.f, ov[e][u], Oe);
+        O[e] = Oe;
+      }
+    }
+    __syncthreads();   // sml / sf / sal are rewritten by the next batch
+  }
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {   // the per-head m and l of each element's head
+    const int idx = threadIdx.x + e * NW * 32;
+    if (idx < G * 128) {
+      M[e] = sMh[idx >> 7];
+      L[e] = sLh[idx >> 7];
+    }
+  }
+  } else {
   for (int s0 = 0; s0 < a.n_split; s0 += kMergeBatch) {
     const int s1 = min(a.n_split, s0 + kMergeBatch);
     if (threadIdx.x == 0) {   // wait (bounded) until splits s0 .. s1-1 have arrived
@@ -1253,6 +1349,7 @@ __device__ void tier_merge(const DecodeArgs& a, int b, int g, uint8_t* smb) {
         O[e] = Oe;
       }
     }
+  }
   }
   if (!merged_all && threadIdx.x == 0) flag_error(a.err, KV_DEVERR_TIMEOUT);
 
