@@ -2025,7 +2025,7 @@ cudaError_t noalloc_scratch(void** ptr, size_t* bytes) {
 // the batch is small; cap the work of one split (and the number of parts the
 // final merge reads) when it is large.
 static DecodePlan make_plan(const Pool& p, int G, int B, int units, int max_per, int n_extra,
-                            int per_sm) {
+                            int per_sm, int min_per = 1) {
   DecodePlan pl;
   const int pairs = B * p.cfg.num_kv_heads;
   const int slots = max(1, per_sm) * p.sm_count;
@@ -2033,6 +2033,7 @@ static DecodePlan make_plan(const Pool& p, int G, int B, int units, int max_per,
   int ns = slots / pairs - n_extra;
   ns = max(1, min(ns, u));
   int per = (u + ns - 1) / ns;
+  per = max(per, min_per);   // short histories: fewer, fuller splits (less to merge)
   per = min(per, max_per);
   per = max(per, (u + kMaxParts - n_extra - 1) / (kMaxParts - n_extra));
   ns = (u + per - 1) / per;
@@ -2051,7 +2052,7 @@ DecodePlan plan_decode_int2(const Pool& p, int B, int max_hist_len, int T) {
   const int per_sm = (T > 1) ? int2_occupancy_t<true>(p, G) : int2_occupancy_t<false>(p, G);
   // one tier CTA per (sequence, KV head) beside the history splits; partials
   // are kept for the history splits only, followed by the q' fragments
-  DecodePlan pl = make_plan(p, G, B, tiles, 64 * int2_warps(G), 1, per_sm);
+  DecodePlan pl = make_plan(p, G, B, tiles, 64 * int2_warps(G), 1, per_sm, int2_warps(G));
   const size_t pairs = (size_t)B * p.cfg.num_kv_heads;
   pl.partial_floats = pairs * pl.n_split * G * kPart;
   const size_t qwords = pairs * 32 * (G <= 4 ? qfrag_words<4>() : qfrag_words<8>());
