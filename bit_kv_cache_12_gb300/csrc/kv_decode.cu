@@ -158,57 +158,79 @@ struct RotFrags {
 
 // q'[h][c] = sum_i q[h][i] R_k[i][c] for the first NROWS rows of X (shared,
 // fp32 holding bf16 values, rows kQStride apart with 4 floats of padding after
-// every 32 channels) into Y (rows kQrStride apart), on the tensor cores: R_k comes as fp16
-// hi + lo B fragments (rotation fragment block 0, this warp's in registers), q is
-// scaled by 2^-8 (exact) and split into fp16 hi + lo, and the three products
-// above 2^-22 relative are accumulated in fp32, each in two chains (even and
-// odd k-steps) that are added at the end in a fixed order (the same order as
-// the batched pre-pass).  Warp w produces columns 8w.., 8(w + NW)...  Ends
-// with a barrier.
-template <int NROWS, int NW>
-__device__ void rotate_q(const float* X, const RotFrags<NW>& rkf, float* Y) {
+// every 32 channels) into Y (rows kQrStride apart), on the tensor cores: R_k
+// comes as fp16 hi + lo B fragments (rotation fragment block 0, this warp's in
+// registers), q is scaled by 2^-8 (exact) and split into fp16 hi + lo, which
+// enter as separate MMA rows (hi in rows 0..7, lo in rows 8..15, or hi in
+// rows 0..3 and lo in rows 4..7 for up to 4 rows), so that two products per
+// k-step (rows x R_hi, rows x R_lo) give the three terms above 2^-22
+// relative, accumulated in fp32 in two chains (even and odd k-steps).  Warp w
+// produces columns 8w.., 8(w + NW)...  With kSums, each 8-column n-tile's
+// partial row sums go to P[n-tile][row] (for the per-group sums of q').
+// Ends with a barrier.
+template <int NROWS, int NW, bool kSums = false>
+__device__ void rotate_q(const float* X, const RotFrags<NW>& rkf, float* Y, float* P = nullptr) {
   static_assert(NROWS <= 8, "rows");
   constexpr int NTW = (16 + NW - 1) / NW;
+  constexpr bool kSplitRows = NROWS <= 4;   // hi rows 0..3, lo rows 4..7 (else 0..7 / 8..15)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = lane >> 2, j = lane & 3;
-  float acc[NTW][6][4];
+  float acc[NTW][4][4];   // [n-tile][R_hi even, R_hi odd, R_lo even, R_lo odd][fragment]
 #pragma unroll
   for (int u = 0; u < NTW; ++u)
 #pragma unroll
-    for (int c = 0; c < 6; ++c) acc[u][c][0] = acc[u][c][1] = acc[u][c][2] = acc[u][c][3] = 0.f;
-  const bool row_ok = r < NROWS;
+    for (int c = 0; c < 4; ++c) acc[u][c][0] = acc[u][c][1] = acc[u][c][2] = acc[u][c][3] = 0.f;
+  const int xrow = kSplitRows ? (r & 3) : r;
+  const bool row_ok = xrow < NROWS;
+  const bool lo_lane = kSplitRows && r >= 4;   // this lane's row holds the lo terms
   constexpr float kIn = 1.0f / 256.0f;
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
     // A: row r, k index kappa -> input channel 32*(kappa%8/2) + 4s + 2*(kappa/8) + kappa%2
-    float4 x = row_ok ? *reinterpret_cast<const float4*>(X + r * kQStride + 36 * j + 4 * s)
+    float4 x = row_ok ? *reinterpret_cast<const float4*>(X + xrow * kQStride + 36 * j + 4 * s)
                       : make_float4(0.f, 0.f, 0.f, 0.f);
     x.x *= kIn; x.y *= kIn; x.z *= kIn; x.w *= kIn;
     const __half2 h01 = __floats2half2_rn(x.x, x.y), h23 = __floats2half2_rn(x.z, x.w);
     const __half2 l01 = __floats2half2_rn(x.x - __low2float(h01), x.y - __high2float(h01));
     const __half2 l23 = __floats2half2_rn(x.z - __low2float(h23), x.w - __high2float(h23));
-    const uint32_t a0 = h2_as_u32(h01), a2 = h2_as_u32(h23);
-    const uint32_t b0 = h2_as_u32(l01), b2 = h2_as_u32(l23);
-    const int c = 3 * (s & 1);
+    uint32_t a0, a1, a2, a3;
+    if (kSplitRows) {
+      a0 = lo_lane ? h2_as_u32(l01) : h2_as_u32(h01);
+      a2 = lo_lane ? h2_as_u32(l23) : h2_as_u32(h23);
+      a1 = a3 = 0u;
+    } else {
+      a0 = h2_as_u32(h01); a2 = h2_as_u32(h23);
+      a1 = h2_as_u32(l01); a3 = h2_as_u32(l23);
+    }
 #pragma unroll
     for (int u = 0; u < NTW; ++u) {
       const uint4 f = rkf.f[s][u];   // zero past the 16 n-tiles
-      mma_f16(acc[u][c], a0, 0u, a2, 0u, f.x, f.y);       // hi * hi
-      mma_f16(acc[u][c + 1], a0, 0u, a2, 0u, f.z, f.w);   // hi * lo
-      mma_f16(acc[u][c + 2], b0, 0u, b2, 0u, f.x, f.y);   // lo * hi
+      mma_f16(acc[u][s & 1], a0, a1, a2, a3, f.x, f.y);         // rows x R_hi
+      mma_f16(acc[u][2 + (s & 1)], a0, a1, a2, a3, f.z, f.w);   // rows x R_lo
     }
   }
-  if (row_ok) {
 #pragma unroll
-    for (int u = 0; u < NTW; ++u)
-      if (warp + u * NW < 16) {
-        float y[2];
+  for (int u = 0; u < NTW; ++u) {
+    const int nt = warp + u * NW;
+    // hi.R_hi + hi.R_lo + lo.R_hi for this lane's hi row
+    float y[2];
 #pragma unroll
-        for (int e = 0; e < 2; ++e)
-          y[e] = ((acc[u][0][e] + acc[u][3][e]) + ((acc[u][1][e] + acc[u][4][e]) + (acc[u][2][e] + acc[u][5][e])));
-        *reinterpret_cast<float2*>(Y + r * kQrStride + 8 * (warp + u * NW) + 2 * j) =
-            make_float2(y[0] * 256.0f, y[1] * 256.0f);
-      }
+    for (int e = 0; e < 2; ++e) {
+      const float hh = acc[u][0][e] + acc[u][1][e], hl = acc[u][2][e] + acc[u][3][e];
+      float lh;
+      if (kSplitRows) lh = __shfl_xor_sync(0xffffffffu, hh, 16);   // row r + 4: lo x R_hi
+      else lh = acc[u][0][2 + e] + acc[u][1][2 + e];                // row r + 8: lo x R_hi
+      y[e] = (hh + hl) + lh;
+    }
+    const bool out_row = row_ok && !lo_lane && nt < 16;
+    if (out_row)
+      *reinterpret_cast<float2*>(Y + xrow * kQrStride + 8 * nt + 2 * j) = make_float2(y[0] * 256.0f, y[1] * 256.0f);
+    if constexpr (kSums) {   // this n-tile's 8 columns of row xrow, summed over the 4 lanes of the row
+      float part = (y[0] + y[1]) * 256.0f;
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      if (out_row && j == 0) P[nt * 8 + xrow] = part;
+    }
   }
   __syncthreads();
 }
@@ -471,8 +493,8 @@ struct HistLay {
   static constexpr int HP = (G <= 4) ? 4 : 8;             // padded heads (MMA columns)
   static constexpr int sq = spid + kMaxPids * 4;          // [HP][kQStride] q (q' computed in the CTA)
   static constexpr int sqr = sq + HP * kQStride * 4;      // [HP][kQrStride] q'
-  static constexpr int ssum = sqr + HP * kQrStride * 4;   // [HP][2] per-group sums of q'
-  static constexpr int total = ssum + HP * 2 * 4;
+  static constexpr int spart = sqr + HP * kQrStride * 4; // [16 n-tiles][8] partial row sums of q'
+  static constexpr int total = spart + 16 * 8 * 4;
   static constexpr int swo = 0;                           // [NW][G][128] per-warp o'
   static constexpr int swm = swo + NW * G * 128 * 4;      // [NW][G] m
   static constexpr int swl = swm + NW * G * 4;            // [NW][G] l
@@ -639,18 +661,8 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
   bool ok = true;
   if (local) {   // ---- q' = q R_k here, then its fragments and per-group sums ----
     float* sqr = reinterpret_cast<float*>(smb + S::sqr);
-    float* ssum = reinterpret_cast<float*>(smb + S::ssum);
-    rotate_q<S::HP, NW>(sq, rkf, sqr);
-    for (int hh = warp; hh < S::HP; hh += NW) {
-#pragma unroll
-      for (int grp = 0; grp < NG; ++grp) {
-        float v = 0.f;
-        for (int c = grp * GS + lane; c < (grp + 1) * GS; c += 32) v += sqr[hh * kQrStride + c];
-        v = warp_sum_xor(v, 1);
-        if (lane == 0) ssum[hh * 2 + grp] = v;
-      }
-    }
-    __syncthreads();
+    float* spart = reinterpret_cast<float*>(smb + S::spart);
+    rotate_q<S::HP, NW, true>(sq, rkf, sqr, spart);   // ends with a barrier
     // QK B fragments: column n = lane/4 -> local head 4*nt + n/2, part n%2 (hi/lo)
     const int hl = r >> 1, e = r & 1;
 #pragma unroll
@@ -671,11 +683,17 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
         qf[s][nt][0] = h2_as_u32(__halves2half2(p[0], p[1]));
         qf[s][nt][1] = h2_as_u32(__halves2half2(p[2], p[3]));
       }
-    // per-group sums of q' in the units of the score accumulator (2^-24)
+    // per-group sums of q' (over the group's 8-column n-tiles) in the units of
+    // the score accumulator (2^-24)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int grp = 0; grp < NG; ++grp) sumq[nt][grp] = ssum[(4 * nt + j) * 2 + grp] * 5.9604644775390625e-8f;
+      for (int grp = 0; grp < NG; ++grp) {
+        float v = 0.f;
+#pragma unroll
+        for (int t = grp * (GS / 8); t < (grp + 1) * (GS / 8); ++t) v += spart[t * 8 + 4 * nt + j];
+        sumq[nt][grp] = v * 5.9604644775390625e-8f;
+      }
   } else {   // ---- q' fragments and per-group sums from the pre-pass ----
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint4* qp = reinterpret_cast<const uint4*>(a.qfrag + ((size_t)(b * a.Hkv + g) * 32 + lane) * QW);
