@@ -60,7 +60,8 @@ constexpr int kStages = 4;       // tiles in each warp's ring
 constexpr int kWaitPolls = 1 << 20;   // bounded mbarrier polls before a copy counts as lost
 constexpr int kMergePolls = 1 << 21;  // bounded polls of a tier CTA for its history splits
 constexpr int kMaxParts = 400;   // partials per (sequence, KV head) a merge reads
-constexpr int kMaxPids = 1032;   // page ids staged per CTA (a split covers <= 1024 tiles)
+constexpr int kMaxTilesPerWarp = 128;   // longest INT2 history split, in tiles per warp
+constexpr int kMaxPids = 16 * kMaxTilesPerWarp + 8;   // page ids staged per CTA
 constexpr int kTierRows = 320;   // sink + recent storage rows staged per tier CTA
 constexpr int kTierRowK = 272;   // staged K row stride (bytes): 256 + 16 keeps lane reads conflict-free
 constexpr int kTierRowV = 272;   // staged V row stride: the transposed ldmatrix reads are conflict-free too
@@ -76,16 +77,22 @@ constexpr float kSlack = 4.0f;
 constexpr int kBf16Warps = 8;
 
 __host__ __device__ constexpr int int2_warps(int G) { return G <= 4 ? 16 : 12; }
-// a split covers at most 64 tiles per warp, and its page ids (one per tile at
-// page 16) are staged in shared memory
+// Longest history split, in tiles per warp, of a grid: grids of several waves
+// run fewer CTAs (fewer prologues and ramps) with longer splits; measured on
+// the batched workloads, 128 suits up to 4 query columns per KV head (batch 64:
+// 244 -> 229 us against 64) and 96 suits 8 (16 x 131k: 472 -> 453 us; 128 gave
+// 471).  A split's page ids (one per tile at page 16) are staged in shared memory.
+__host__ __device__ constexpr int int2_max_tiles_per_warp(int G) { return G <= 4 ? 128 : 96; }
 static_assert((long long)kMaxParts * (kMaxPids - 8) * kTile >= kMaxDecodeLen,
               "a decode of the longest length stages at most kMaxPids - 8 page ids per split");
-static_assert(64 * int2_warps(1) <= kMaxPids && 64 * int2_warps(8) <= kMaxPids,
+static_assert(int2_max_tiles_per_warp(1) * int2_warps(1) <= kMaxPids &&
+                  int2_max_tiles_per_warp(8) * int2_warps(8) <= kMaxPids &&
+                  int2_max_tiles_per_warp(1) <= kMaxTilesPerWarp && int2_max_tiles_per_warp(8) <= kMaxTilesPerWarp,
               "a split's page ids must fit the staging array");
 static_assert(kMaxParts <= 32 * kMaskWords, "every split has a bit in the arrival mask");
 // Where a history CTA gets q' = q R_k from:
-//   kQLocal  it forms q' itself from R_k's fragments (64 KB per CTA, kept in
-//            L2 across steps by their evict-last priority) - grids of one wave;
+//   kQLocal  it forms q' itself, each warp from its own 4 KB of R_k's
+//            fragments held in registers - grids of one wave;
 //   kQPre    the batched pre-pass wrote the fragments - grids of several waves.
 constexpr int kQLocal = 0, kQPre = 1;
 
@@ -488,8 +495,8 @@ struct HistLay {
   static constexpr int TB = 1024 + 16 * 8 * (128 / GS);   // stored tile bytes (one ring stage)
   static constexpr int ring = 0;                          // [NW][kStages][TB]
   static constexpr int bars = ring + NW * kStages * TB;   // [NW][kStages] mbarriers
-  static constexpr int saddr = bars + NW * kStages * 8;   // [64 NW] tile source addresses
-  static constexpr int spid = saddr + 64 * NW * 8;        // [kMaxPids] page ids
+  static constexpr int saddr = bars + NW * kStages * 8;   // [kMaxTilesPerWarp NW] tile source addresses
+  static constexpr int spid = saddr + kMaxTilesPerWarp * NW * 8;   // [kMaxPids] page ids
   static constexpr int HP = (G <= 4) ? 4 : 8;             // padded heads (MMA columns)
   static constexpr int sq = spid + kMaxPids * 4;          // [HP][kQStride] q (q' computed in the CTA)
   static constexpr int sqr = sq + HP * kQStride * 4;      // [HP][kQrStride] q'
@@ -1517,16 +1524,18 @@ template <int G, int GS, bool kMulti>
 __global__ void __launch_bounds__(int2_warps(G) * 32, 1) decode_int2_kernel(DecodeArgs a) {
   extern __shared__ float4 smem4[];
   uint8_t* smb = reinterpret_cast<uint8_t*>(smem4);
-  // launch order: every history split first ((sequence, KV head) pairs in
-  // turn, their splits together), then the tier CTAs, which wait for the
-  // history splits of their pair (earlier in launch order) and merge them
+  // launch order: every history split first, split-major (every pair's first
+  // split, then every pair's second, ..: the longest work goes first on grids
+  // of several waves), then the tier CTAs, which wait for the history splits of
+  // their pair (earlier in launch order) and merge them
   const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
   const int n_hist = a.n_split * gridDim.y * gridDim.z;
   // the next kernel may start its own prologue as SMs free up; it waits for
   // this grid before it reads anything this grid writes
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (lin < n_hist) {
-    const int split = lin % a.n_split, pair = lin / a.n_split;
+    const int n_pairs = gridDim.y * gridDim.z;
+    const int split = lin / n_pairs, pair = lin % n_pairs;   // split-major: every pair's first split first
     const int g = pair % a.Hkv, b = pair / a.Hkv;
     float* part = a.ws + ((size_t)pair * a.n_split + split) * G * kPart;
     int2_history<G, GS, kMulti>(a, b, g, split, smb, part);
@@ -2070,7 +2079,7 @@ DecodePlan plan_decode_int2(const Pool& p, int B, int max_hist_len, int T) {
   const int per_sm = (T > 1) ? int2_occupancy_t<true>(p, G) : int2_occupancy_t<false>(p, G);
   // one tier CTA per (sequence, KV head) beside the history splits; partials
   // are kept for the history splits only, followed by the q' fragments
-  DecodePlan pl = make_plan(p, G, B, tiles, 64 * int2_warps(G), 1, per_sm, int2_warps(G));
+  DecodePlan pl = make_plan(p, G, B, tiles, int2_max_tiles_per_warp(G) * int2_warps(G), 1, per_sm, int2_warps(G));
   const size_t pairs = (size_t)B * p.cfg.num_kv_heads;
   pl.partial_floats = pairs * pl.n_split * G * kPart;
   const size_t qwords = pairs * 32 * (G <= 4 ? qfrag_words<4>() : qfrag_words<8>());

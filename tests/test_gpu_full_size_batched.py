@@ -10,10 +10,10 @@ recomputes sampled KV heads (every query head of each) from the codes the
 pool stores, including the last (sequence, KV head) pair, whose history splits
 run in the grid's last wave; every output is finite.
 
-Two smaller cases force what the batched shapes reach only at size: a split
-of 64 tiles per warp (the bound of one split: 768 tiles at GQA 8 with 12
-warps, 1,024 page ids at GQA 4 with 16 warps, the staging limit being 1,032)
-on grids of several waves with ragged lengths.  The gist.science OSCAR
+Smaller cases force what the batched shapes reach only at size: the longest
+split (128 tiles per warp at GQA 4 with 16 warps = 2,048 page ids, the staging
+limit being 2,056; 96 per warp at GQA 8 with 12 warps = 1,152) and a second,
+shorter split per pair, on grids of several waves with ragged lengths.  The gist.science OSCAR
 explainer, section 4 (system results), reports the method at large batch."""
 
 import numpy as np
@@ -64,8 +64,8 @@ def test_long16_full_size():
     _check(c, [(0, 0), (7, 3), (c.B - 1, c.Hkv - 1)])
 
 
-@pytest.mark.parametrize("G,P,B,lo,hi", [(8, 16, 64, 12700, 13120), (4, 16, 40, 17000, 17920),
-                                         (8, 32, 64, 12700, 13120)])
+@pytest.mark.parametrize("G,P,B,lo,hi", [(8, 16, 64, 18800, 19400), (4, 16, 40, 33000, 33900),
+                                         (8, 32, 64, 18800, 19400)])
 def test_split_bound_multi_wave(G, P, B, lo, hi):
     Hkv = 2
     c = workloads.generate(torch, torch.device("cuda"), f"wave_g{G}_p{P}", 90 + G + P, B, G * Hkv,
@@ -74,8 +74,9 @@ def test_split_bound_multi_wave(G, P, B, lo, hi):
     pool = native.KVPool(native.KV_POOL_INT2_3TIER, 1, c.Hq, Hkv, P, 4, B)
     per_part = ws(pool.handle, B, int(c.hist_len.max()))
     pool.close()
-    # 2 history splits per (sequence, KV head), the first with 64 tiles per warp:
-    # their partials (132 floats per query head), then the q' fragments
+    # 2 history splits per (sequence, KV head), the first with the longest split
+    # (128 tiles per warp of 16 at 4 query columns, 96 of 12 at 8): their
+    # partials (132 floats per query head), then the q' fragments
     qwords = 32 * (16 * (1 if G <= 4 else 2) + 4)
     assert per_part == B * Hkv * (2 * G * 132 * 4 + qwords * 4)
     _check(c, [(0, 0), (B // 2, 1), (B - 1, 0), (B - 1, 1), (int(np.argmax(c.hist_len)), 1)])
