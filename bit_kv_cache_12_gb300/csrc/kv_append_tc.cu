@@ -599,7 +599,7 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
           store_merge2(tb + 16 * (4 * (m16 & 7) + 2 * mh + jj) + 8 * hf, out[jj], mask);
       }
       if (write && row_ok && (GS == 64 || hf == 0)) {
-        __half2* rec = reinterpret_cast<__half2*>(tb + 1024 + (2 * (m16 & 7) + mh) * 8 * NG);
+        __half2* rec = reinterpret_cast<__half2*>(tb + 1024 + (2 * (m16 & 7) + mh) * 4 * NG);
         rec[GS == 64 ? hf : 0] = __halves2half2(q.sh, q.zh);
       }
     } else {
@@ -640,7 +640,7 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
           store_merge2(tb + 512 + 16 * (4 * (4 * kh + 2 * ek + ii) + jk) + 8 * hf, out[ii], mask);
       }
       if (write && row_ok && (GS == 64 || hf == 0)) {
-        __half2* rec = reinterpret_cast<__half2*>(tb + 1024 + (2 * (m16 & 7) + kh) * 8 * NG) + NG;
+        __half2* rec = reinterpret_cast<__half2*>(tb + 1024 + 64 * NG + (2 * (m16 & 7) + kh) * 4 * NG);
         rec[GS == 64 ? hf : 0] = __halves2half2(q.sh, q.zh);
       }
     }
@@ -892,7 +892,7 @@ __device__ __forceinline__ void evict_body(const StepArgs& a, int B, uint8_t* sm
           *dst[j] = make_uint2((old[j].x & ~mask) | ((wd[j][0] << (2 * mh)) & mask),
                                (old[j].y & ~mask) | ((wd[j][1] << (2 * mh)) & mask));
         if (GS == 64 || hf == 0) {
-          __half2* rec = reinterpret_cast<__half2*>(tb + 1024 + (2 * (pos & 7) + mh) * 8 * NG);
+          __half2* rec = reinterpret_cast<__half2*>(tb + 1024 + (2 * (pos & 7) + mh) * 4 * NG);
           rec[GS == 64 ? hf : 0] = __halves2half2(q.sh, q.zh);
         }
       } else {
@@ -913,7 +913,7 @@ __device__ __forceinline__ void evict_body(const StepArgs& a, int B, uint8_t* sm
           *dst[m8] = make_uint2((old[m8].x & ~mask) | ((wd[m8][0] << sh) & mask),
                                 (old[m8].y & ~mask) | ((wd[m8][1] << sh) & mask));
         if (GS == 64 || hf == 0) {
-          __half2* rec = reinterpret_cast<__half2*>(tb + 1024 + (2 * (pos & 7) + kh) * 8 * NG) + NG;
+          __half2* rec = reinterpret_cast<__half2*>(tb + 1024 + 64 * NG + (2 * (pos & 7) + kh) * 4 * NG);
           rec[GS == 64 ? hf : 0] = __halves2half2(q.sh, q.zh);
         }
       }

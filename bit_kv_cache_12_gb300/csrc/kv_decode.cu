@@ -621,7 +621,9 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
 
   // ---- start streaming this warp's first tiles into its ring ----
   const uint8_t* head_base = a.hist + (size_t)g * (a.page_bytes / a.Hkv);
-  const int lane_sz = (GS == 128) ? 1024 + 16 * r : 1024 + 32 * r;
+  // s/z records of tokens r and r + 8 (record slots 2r, 2r + 1): K block at
+  // 1024, V block 16 slots of 4 NG bytes later
+  const int lane_szk = 1024 + 8 * NG * r, lane_szv = lane_szk + 64 * NG;
   // the history is read once per step: its lines leave L2 first
   const uint64_t stream_policy = l2_evict_first_policy();
   auto start_copy = [&](int t, int pid, int stage) {
@@ -774,9 +776,16 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
     const uint8_t* src = ring + st * TB;
     const uint4 kq4 = *reinterpret_cast<const uint4*>(src + 16 * lane);
     const uint4 vq4 = *reinterpret_cast<const uint4*>(src + 512 + 16 * lane);
-    const uint4 sz0 = *reinterpret_cast<const uint4*>(src + lane_sz);
-    const uint4 sz1 =
-        (GS == 64) ? *reinterpret_cast<const uint4*>(src + lane_sz + 16) : make_uint4(0, 0, 0, 0);
+    uint4 szk, szv;   // group 128: (x, y) = tokens r, r + 8; group 64: (x, y) token r, (z, w) token r + 8
+    if (GS == 128) {
+      const uint2 k2 = *reinterpret_cast<const uint2*>(src + lane_szk);
+      const uint2 v2 = *reinterpret_cast<const uint2*>(src + lane_szv);
+      szk = make_uint4(k2.x, k2.y, 0u, 0u);
+      szv = make_uint4(v2.x, v2.y, 0u, 0u);
+    } else {
+      szk = *reinterpret_cast<const uint4*>(src + lane_szk);
+      szv = *reinterpret_cast<const uint4*>(src + lane_szv);
+    }
     bool v0 = true, v1 = true;
     if constexpr (kMask) {   // tokens of this tile still inside the history (none if its page id is bad)
       const int lim = ((saddr[t - t_begin] & 1ull) != 0) ? h - t * kTile : 0;
@@ -787,22 +796,19 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
     // scale / zero of tokens r and r+8
     float sk[2][NG], zk[2][NG], sv[2][NG], zv[2][NG];
     if (GS == 128) {
-      const __half2 a0 = u32_as_h2(sz0.x), a1 = u32_as_h2(sz0.y);
-      const __half2 b0 = u32_as_h2(sz0.z), b1 = u32_as_h2(sz0.w);
-      sk[0][0] = __low2float(a0); zk[0][0] = __high2float(a0);
-      sv[0][0] = __low2float(a1); zv[0][0] = __high2float(a1);
-      sk[1][0] = __low2float(b0); zk[1][0] = __high2float(b0);
-      sv[1][0] = __low2float(b1); zv[1][0] = __high2float(b1);
+      sk[0][0] = __low2float(u32_as_h2(szk.x)); zk[0][0] = __high2float(u32_as_h2(szk.x));
+      sk[1][0] = __low2float(u32_as_h2(szk.y)); zk[1][0] = __high2float(u32_as_h2(szk.y));
+      sv[0][0] = __low2float(u32_as_h2(szv.x)); zv[0][0] = __high2float(u32_as_h2(szv.x));
+      sv[1][0] = __low2float(u32_as_h2(szv.y)); zv[1][0] = __high2float(u32_as_h2(szv.y));
     } else {
-      const uint4 s0 = sz0, s1 = sz1;
-      sk[0][0] = __low2float(u32_as_h2(s0.x)); zk[0][0] = __high2float(u32_as_h2(s0.x));
-      sk[0][NG - 1] = __low2float(u32_as_h2(s0.y)); zk[0][NG - 1] = __high2float(u32_as_h2(s0.y));
-      sv[0][0] = __low2float(u32_as_h2(s0.z)); zv[0][0] = __high2float(u32_as_h2(s0.z));
-      sv[0][NG - 1] = __low2float(u32_as_h2(s0.w)); zv[0][NG - 1] = __high2float(u32_as_h2(s0.w));
-      sk[1][0] = __low2float(u32_as_h2(s1.x)); zk[1][0] = __high2float(u32_as_h2(s1.x));
-      sk[1][NG - 1] = __low2float(u32_as_h2(s1.y)); zk[1][NG - 1] = __high2float(u32_as_h2(s1.y));
-      sv[1][0] = __low2float(u32_as_h2(s1.z)); zv[1][0] = __high2float(u32_as_h2(s1.z));
-      sv[1][NG - 1] = __low2float(u32_as_h2(s1.w)); zv[1][NG - 1] = __high2float(u32_as_h2(s1.w));
+      sk[0][0] = __low2float(u32_as_h2(szk.x)); zk[0][0] = __high2float(u32_as_h2(szk.x));
+      sk[0][NG - 1] = __low2float(u32_as_h2(szk.y)); zk[0][NG - 1] = __high2float(u32_as_h2(szk.y));
+      sk[1][0] = __low2float(u32_as_h2(szk.z)); zk[1][0] = __high2float(u32_as_h2(szk.z));
+      sk[1][NG - 1] = __low2float(u32_as_h2(szk.w)); zk[1][NG - 1] = __high2float(u32_as_h2(szk.w));
+      sv[0][0] = __low2float(u32_as_h2(szv.x)); zv[0][0] = __high2float(u32_as_h2(szv.x));
+      sv[0][NG - 1] = __low2float(u32_as_h2(szv.y)); zv[0][NG - 1] = __high2float(u32_as_h2(szv.y));
+      sv[1][0] = __low2float(u32_as_h2(szv.z)); zv[1][0] = __high2float(u32_as_h2(szv.z));
+      sv[1][NG - 1] = __low2float(u32_as_h2(szv.w)); zv[1][NG - 1] = __high2float(u32_as_h2(szv.w));
     }
     // token r+8 sits in the score rows with the codes' row factor 4; in PV it
     // is in the upper k half, whose codes arrive as 3 - c: its weight enters

@@ -105,9 +105,11 @@ typedef struct {
  *   INT2 history block of (page p, KV head g):
  *       hist + l*hist_layer_stride + p*hist_page_stride + g*hist_head_stride
  *     = page_size/16 tiles of tile_bytes each; a tile is
- *       [K codes 512 B][V codes 512 B][scale/zero records 16 * rec_bytes B]
- *     rec_bytes = 8 * 128/group_size: per group (s_k, z_k) fp16 pairs, then
- *     per group (s_v, z_v); record slot 2*(t%8) + t/8 holds token t of the tile.
+ *       [K codes 512 B][V codes 512 B][K records 16 * rec_bytes B][V records 16 * rec_bytes B]
+ *     rec_bytes = 4 * 128/group_size: per group the (s, z) fp16 pair of the
+ *     tensor; record slot 2*(t%8) + t/8 of each block holds token t of the tile
+ *     (K and V records in separate 32-byte sectors, so each tensor's writes
+ *     cover whole sectors).
  *     Code bit of (m, k, step) with m, k in [0,16), step in [0,8): 16-byte
  *     lane L = 4*(m%8) + (k%8)/2, 32-bit little-endian word step/2, bit
  *     16*(k%2) + 2*(2*(step%2) + m/8 + 4*(k/8)); K: m = token, k = channel%16,

@@ -148,10 +148,10 @@ def unpack_canonical(packed):
 # --------------------------------------------------------------------------
 #
 # A page of P tokens (P = 16 or 32) of one KV head is P/16 tiles.  Each tile:
-#   [ K codes 512 B ][ V codes 512 B ][ scale/zero records 16 * rec B ]
-# rec = 4 halves per group: (s_k, z_k) for each group, then (s_v, z_v) for
-# each group; Gs=128 -> 8 B per token, Gs=64 -> 16 B per token.  Records are
-# stored by token pairs: pair r (r = 0..7) holds token r then token r + 8.
+#   [ K codes 512 B ][ V codes 512 B ][ K records 16 * rec B ][ V records 16 * rec B ]
+# rec = 2 halves per group, (s, z) for each group of the tensor; Gs=128 -> 4 B
+# per token and tensor, Gs=64 -> 8 B.  Records are stored by token pairs:
+# slot 2r holds token r, slot 2r + 1 token r + 8 (r = 0..7).
 #
 # Code bits.  A code is addressed by (m, k, step): m in [0,16) and k in [0,16)
 # index a 16 x 16 block, step in [0,8) selects one of the eight blocks that
@@ -222,11 +222,12 @@ def pack_tile(kc, vc, sk, zk, sv, zv, group_size, base=None, valid=None):
             for (blk, bmap, smap, code) in ((0, _KB, _KS, kc), (512, _VB, _VS, vc)):
                 byte = blk + int(bmap[t, c]); sh = int(smap[t, c])
                 out[byte] = (out[byte] & ~np.uint8(3 << sh)) | np.uint8((int(code[t, c]) & 3) << sh)
-        rec = np.empty(4 * ng, np.float16)
-        rec[0:2 * ng:2] = sk[t]; rec[1:2 * ng:2] = zk[t]
-        rec[2 * ng::2] = sv[t]; rec[2 * ng + 1::2] = zv[t]
-        off = 1024 + (2 * (t % 8) + t // 8) * 8 * ng
-        out[off:off + 8 * ng] = rec.view(np.uint8)
+        slot = 2 * (t % 8) + t // 8
+        for blk, s_, z_ in ((1024, sk, zk), (1024 + TILE * 4 * ng, sv, zv)):
+            rec = np.empty(2 * ng, np.float16)
+            rec[0::2] = s_[t]; rec[1::2] = z_[t]
+            off = blk + slot * 4 * ng
+            out[off:off + 4 * ng] = rec.view(np.uint8)
     return out
 
 
@@ -241,11 +242,11 @@ def pack_tiles_full(kc, vc, sk, zk, sv, zv, group_size):
     for blk, codes, (it, ic) in ((0, kc, _KINV), (512, vc, _VINV)):
         g = codes[:, it, ic].astype(np.uint16) << _SLOT_SHIFT
         out[:, blk:blk + 512] = g.sum(axis=-1).astype(np.uint8)
-    rec = np.empty((n, TILE, 4 * ng), np.float16)
-    rec[:, :, 0:2 * ng:2] = sk; rec[:, :, 1:2 * ng:2] = zk
-    rec[:, :, 2 * ng::2] = sv; rec[:, :, 2 * ng + 1::2] = zv
     order = np.array([t for r in range(8) for t in (r, r + 8)])   # record slot -> token
-    out[:, 1024:] = rec[:, order].reshape(n, -1).view(np.uint8)
+    for blk, s_, z_ in ((1024, sk, zk), (1024 + TILE * 4 * ng, sv, zv)):
+        rec = np.empty((n, TILE, 2 * ng), np.float16)
+        rec[:, :, 0::2] = s_; rec[:, :, 1::2] = z_
+        out[:, blk:blk + TILE * 4 * ng] = rec[:, order].reshape(n, -1).view(np.uint8)
     return out
 
 
@@ -286,12 +287,15 @@ def unpack_tile(buf, group_size):
     buf = np.asarray(buf, dtype=np.uint8)
     kc = (buf[_KB] >> _KS) & 3
     vc = (buf[512 + _VB] >> _VS) & 3
-    recs = np.empty((TILE, 4 * ng), np.float16)
+    rk = np.empty((TILE, 2 * ng), np.float16)
+    rv = np.empty((TILE, 2 * ng), np.float16)
     for t in range(TILE):
-        off = 1024 + (2 * (t % 8) + t // 8) * 8 * ng
-        recs[t] = buf[off:off + 8 * ng].view(np.float16)
-    sk = recs[:, 0:2 * ng:2]; zk = recs[:, 1:2 * ng:2]
-    sv = recs[:, 2 * ng::2]; zv = recs[:, 2 * ng + 1::2]
+        slot = 2 * (t % 8) + t // 8
+        rk[t] = buf[1024 + slot * 4 * ng:1024 + (slot + 1) * 4 * ng].view(np.float16)
+        off = 1024 + TILE * 4 * ng + slot * 4 * ng
+        rv[t] = buf[off:off + 4 * ng].view(np.float16)
+    sk = rk[:, 0::2]; zk = rk[:, 1::2]
+    sv = rv[:, 0::2]; zv = rv[:, 1::2]
     return kc.astype(np.uint8), vc.astype(np.uint8), sk, zk, sv, zv
 
 
@@ -345,9 +349,9 @@ def unpack_tiles(blocks, group_size):
     kc = (blocks[:, _KB] >> _KS) & 3
     vc = (blocks[:, 512 + _VB] >> _VS) & 3
     order = np.array([2 * (t % 8) + t // 8 for t in range(TILE)])   # token -> record slot
-    recs = np.ascontiguousarray(blocks[:, 1024:]).view(np.float16).reshape(-1, TILE, 4 * ng)[:, order]
-    return (kc.astype(np.uint8), vc.astype(np.uint8), recs[:, :, 0:2 * ng:2], recs[:, :, 1:2 * ng:2],
-            recs[:, :, 2 * ng::2], recs[:, :, 2 * ng + 1::2])
+    rk = np.ascontiguousarray(blocks[:, 1024:1024 + TILE * 4 * ng]).view(np.float16).reshape(-1, TILE, 2 * ng)[:, order]
+    rv = np.ascontiguousarray(blocks[:, 1024 + TILE * 4 * ng:]).view(np.float16).reshape(-1, TILE, 2 * ng)[:, order]
+    return (kc.astype(np.uint8), vc.astype(np.uint8), rk[:, :, 0::2], rk[:, :, 1::2], rv[:, :, 0::2], rv[:, :, 1::2])
 
 
 def read_history(pages_buf, page_table_row, hist_len, head, page_size, group_size):

@@ -136,6 +136,34 @@ def test_tile_layout_is_a_bijection(tensor):
 
 
 @pytest.mark.parametrize("gs", [64, 128])
+def test_tile_record_positions(gs):
+    """Byte positions of the s/z records, worked by hand from the documented
+    layout: after the 1024 code bytes, 16 K slots of 4 * (128 / gs) bytes, then
+    16 V slots; slot 2 (t % 8) + t / 8 holds token t as (s, z) fp16 per group."""
+    ng = 128 // gs
+    sk = np.zeros((16, ng), np.float16); zk = np.zeros((16, ng), np.float16)
+    sv = np.zeros((16, ng), np.float16); zv = np.zeros((16, ng), np.float16)
+    sk[0, 0], zk[0, 0] = 1.5, -2.0       # token 0: slot 0
+    sk[8, 0], zk[8, 0] = 3.0, 0.25       # token 8: slot 1
+    sk[1, ng - 1] = 6.0                  # token 1: slot 2, last group
+    sv[0, 0], zv[0, 0] = 0.5, -1.0       # V block, token 0
+    sv[15, ng - 1] = 7.0                 # V block, token 15: slot 15, last group
+    z = np.zeros((16, 128), np.uint8)
+    tile = kq.pack_tile(z, z, sk, zk, sv, zv, gs)
+    f16 = lambda off: float(tile[off:off + 2].view(np.float16)[0])
+    kb, vb = 1024, 1024 + 16 * 4 * ng
+    assert (f16(kb), f16(kb + 2)) == (1.5, -2.0)
+    assert (f16(kb + 4 * ng), f16(kb + 4 * ng + 2)) == (3.0, 0.25)
+    assert f16(kb + 2 * 4 * ng + 4 * (ng - 1)) == 6.0
+    assert (f16(vb), f16(vb + 2)) == (0.5, -1.0)
+    assert f16(vb + 15 * 4 * ng + 4 * (ng - 1)) == 7.0
+    assert len(tile) == 1024 + 2 * 16 * 4 * ng
+    back = kq.unpack_tile(tile, gs)
+    for got, want in zip(back[2:], (sk, zk, sv, zv)):
+        assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("gs", [64, 128])
 def test_tile_pack_roundtrip_and_partial_merge(gs):
     rng = np.random.default_rng(9)
     ng = 128 // gs
