@@ -12,27 +12,29 @@
 // GPU design: the rotation x' = x R of a chunk of 128 tokens of one KV head
 // and one tensor is x [128 x 128] . R_hi + x . R_lo, both terms accumulated
 // into one fp32 accumulator (R enters as bf16 hi and lo terms; x is exact in
-// bf16).  A CTA of eight warps owns one (KV head, tensor) and walks over
-// 128-token chunks:
+// bf16).  The bulk append runs one CTA per SM on one (KV head, tensor): two
+// teams of eight warps take the CTA's 128-token chunks in turn:
 //   * x rows arrive by two TMA tile loads (128-byte swizzle, the K-major
 //     operand layout) when the whole chunk lies inside the input, else by
-//     16-byte cp.async with rows outside the append range zero-filled; the
-//     next chunk's rows come in while this chunk's epilogue runs.  R^T hi |
-//     lo arrives once per CTA, pre-swizzled in global memory by the rotation
+//     16-byte cp.async with rows outside the append range zero-filled, into
+//     one of four buffers, two chunks ahead of the epilogue.  R^T hi | lo
+//     arrives once per CTA, pre-swizzled in global memory by the rotation
 //     set-up, as four bulk copies;
-//   * one thread issues sixteen tcgen05.mma (kind::f16, M 128, N 128, K 16:
-//     per 16-channel step the hi term, then the lo term) into a 128-column
-//     fp32 accumulator in tensor memory and commits them to an mbarrier;
-//   * every thread then owns one token row and one half of the channels of
-//     the accumulator (tcgen05.ld; warps w and w + 4 share a lane quarter):
-//     clip, per-group min / max (combined across the halves through shared
-//     memory for group 128), s and z, the codes (branch-free, with a rare
-//     exact fix-up); the codes are packed into the tile's storage order with
-//     warp shuffles (partners differ in lane bits 0 and 3) and written as
-//     8-byte word pairs, merging with the bits of rows outside the append
-//     range where a tile is only partly written.
-// Two CTAs share an SM (128 tensor-memory columns and ~100 KB of shared
-// memory each), so one CTA's MMA overlaps the other's epilogue.
+//   * a team's leader thread issues sixteen tcgen05.mma (kind::f16, M 128,
+//     N 128, K 16: per 16-channel step the hi term, then the lo term) into
+//     one of four 128-column fp32 accumulators in tensor memory (all 512
+//     columns), one chunk ahead of the team's epilogue, and commits them to
+//     an mbarrier;
+//   * every thread of a team owns one token row and one half of the channels
+//     of the accumulator (tcgen05.ld; warps w and w + 4 of a team share a
+//     lane quarter): clip, per-group min / max (combined across the halves
+//     through shared memory for group 128), s and z, the codes (branch-free,
+//     with a rare exact fix-up); the codes are packed into the tile's storage
+//     order with warp shuffles (partners differ in lane bits 0 and 3) and
+//     written as 8-byte word pairs, merging with the bits of rows outside the
+//     append range where a tile is only partly written.
+// The per-step eviction runs the same product and epilogue on one chunk per
+// CTA, two CTAs per SM.
 // Every wait is bounded; a wait that runs out sets KV_DEVERR_TIMEOUT, waits
 // (bounded) for the work in flight, frees the tensor memory and returns.
 #include <cuda.h>
@@ -60,7 +62,6 @@ constexpr uint32_t kOffClip = kOffB + kBBytes;
 constexpr uint32_t kOffStat = kOffClip + 128 * 4;
 constexpr uint32_t kOffBar = kOffStat + 2 * 128 * 8;
 constexpr uint32_t kOffTmem = kOffBar + 24;
-constexpr uint32_t kTcSmem = kOffTmem + 16 + 1024;   // + alignment slack
 
 // ---- tcgen05 / descriptor helpers -------------------------------------------
 // Shared-memory matrix descriptor of a K-major operand in the 128-byte swizzle
@@ -262,11 +263,11 @@ struct TaskCursor {
   }
 };
 
-// x rows of a chunk -> the swizzled A operand: thread t copies half a row
-// (row t % 128, channels 64 * (t / 128) ..); rows outside the append range are zero
+// x rows of a chunk -> the swizzled A operand: thread t (0 .. 255) copies half a
+// row (row t % 128, channels 64 * (t / 128) ..); rows outside the append range are zero
 __device__ __forceinline__ void load_chunk(const TcArgs& a, const uint16_t* X, int g, const Chunk& k,
-                                           uint32_t sA) {
-  const int row = threadIdx.x & 127, hf = threadIdx.x >> 7;
+                                           uint32_t sA, int t) {
+  const int row = t & 127, hf = t >> 7;
   const int pos = k.P0 + row;
   const bool ok = pos >= k.h0 && pos < k.h0 + k.nb;
   const uint16_t* src = X + ((size_t)(ok ? k.c0 + (pos - k.h0) : 0) * a.Hkv + g) * 128 + 64 * hf;
@@ -292,6 +293,27 @@ __device__ __forceinline__ void issue_rotation(uint32_t tmem, uint32_t sA, uint3
   tc_commit(smem_u32(bar));
 }
 
+// Pairs of fp32 values in one 64-bit register for the paired fp32 arithmetic
+// of sm_100 and later (add / sub / fma .f32x2: one instruction for two
+// values, each rounded exactly as the scalar instruction rounds it).
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
 // Three-input minimum / maximum (one instruction on sm_100 and later); exact,
 // so reductions built from them give the same value in any order (up to the
 // sign of a zero, which the quantizer canonicalises).
@@ -337,10 +359,11 @@ __device__ __forceinline__ float max_of32(float acc, const float (&v)[32]) {
 // k = c % 16) at the bit positions of token row 0 of a tile (K) or of tile
 // token 0 (V); the caller shifts them to the row's own positions.  Both warps
 // of a lane quarter (w and w + 4) call this together: group 128 combines their
-// two halves through shared memory behind a named barrier of those 64 threads.
+// two halves through shared memory behind named barrier `qbar`, of those 64
+// threads.
 template <int GS, int TENSOR, int NS>
 __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, const float* sclip, float2* sstat,
-                                               uint32_t (&wd)[NS][2]) {
+                                               uint32_t (&wd)[NS][2], int qbar) {
   // first pass: x' clipped, written back in place (the second pass reads the
   // clipped values), and its range
   auto clipped32 = [&](int cb, float (&v)[32]) {
@@ -371,12 +394,7 @@ __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, con
   }
   if (GS == 128) {   // the group spans both channel halves: combine with warp w ^ 4
     sstat[hf * 128 + m] = make_float2(mn, mx);
-    switch (m >> 5) {   // named barrier 1 + quarter: warps m/32 and m/32 + 4 (barrier 0 is the CTA's)
-      case 0: asm volatile("bar.sync 1, 64;" ::: "memory"); break;
-      case 1: asm volatile("bar.sync 2, 64;" ::: "memory"); break;
-      case 2: asm volatile("bar.sync 3, 64;" ::: "memory"); break;
-      default: asm volatile("bar.sync 4, 64;" ::: "memory"); break;
-    }
+    asm volatile("bar.sync %0, 64;" ::"r"(qbar) : "memory");
     const float2 o = sstat[(hf ^ 1) * 128 + m];
     mn = fminf(mn, o.x);
     mx = fmaxf(mx, o.y);
@@ -413,17 +431,26 @@ __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, con
   for (int cb = 0; cb < 2; ++cb) {
     float v[32];
     rotated32(cb, v);
+    const uint64_t zz = f2pack(q.z, q.z), three = f2pack(3.0f, 3.0f), mag = f2pack(12582912.0f, 12582912.0f);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      float u;
-      asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(u) : "f"(__fsub_rn(v[i], q.z)), "f"(rs3));
+    for (int i = 0; i < 32; i += 2) {   // channels i and i + 1 as one pair
+      float d0, d1, u0, u1, r0, r1, e0, e1;
+      f2unpack(f2sub(f2pack(v[i], v[i + 1]), zz), d0, d1);
+      asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(u0) : "f"(d0), "f"(rs3));
+      asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(u1) : "f"(d1), "f"(rs3));
+      const uint64_t up = f2pack(u0, u1);
       // rr = 3 u + 1.5 * 2^23 rounded once: its bits are 0x4B400000 + code
-      const float rr = __fmaf_rn(u, 3.0f, 12582912.0f);
-      // one integer multiply-add places the code (the constant offsets of a
+      const uint64_t rr = f2fma(up, three, mag);
+      f2unpack(rr, r0, r1);
+      // one integer multiply-add places a code (the constant offsets of a
       // word fold into one; codes do not overlap, so the sum is the OR)
-      const int pos = pos_of(32 * cb + i);
-      word_of(32 * cb + i) += __float_as_uint(rr) * (1u << pos) - (0x4B400000u << pos);
-      v[i] = fabsf(__fmaf_rn(u, 3.0f, -__fsub_rn(rr, 12582912.0f)));   // distance to the code
+      const int pos0 = pos_of(32 * cb + i), pos1 = pos_of(32 * cb + i + 1);
+      word_of(32 * cb + i) += __float_as_uint(r0) * (1u << pos0) - (0x4B400000u << pos0);
+      word_of(32 * cb + i + 1) += __float_as_uint(r1) * (1u << pos1) - (0x4B400000u << pos1);
+      // distance to the code: 3 u - code, the code being exactly 1.5 * 2^23 - rr negated
+      f2unpack(f2fma(up, three, f2sub(mag, rr)), e0, e1);
+      v[i] = fabsf(e0);
+      v[i + 1] = fabsf(e1);
     }
     emax = max_of32(emax, v);
   }
@@ -443,120 +470,216 @@ __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, con
   return q;
 }
 
+// ---- bulk append: one CTA per SM, two teams of eight warps ----------------
+// The CTA's live chunks j = 0, 1, 2, ... alternate between the teams (team
+// j % 2).  Chunk j's x lands in buffer j % 4 and its product in accumulator
+// j % 4 (tensor-memory columns 128 (j % 4)), so every buffer and accumulator
+// belongs to one team.  At the start of its chunk j a team's leader issues the
+// product of the team's next chunk j + 2, whose x has been loading for a
+// whole chunk, into the accumulator that chunk j - 2 left; once chunk j's own
+// product has been read the leader starts the x load of chunk j + 4 into the
+// buffer chunk j's product has released.  The epilogue of a chunk thus never
+// waits for the tensor cores, and the two teams keep sixteen warps issuing.
+constexpr int kBkThreads = 512;
+constexpr int kBkCols = 512;                 // four 128-column fp32 accumulators
+constexpr uint32_t kBkOffB = 0;              // R^T hi | lo
+constexpr uint32_t kBkOffA = kBkOffB + kBBytes;             // four x buffers
+constexpr uint32_t kBkOffClip = kBkOffA + 4 * kABytes;
+constexpr uint32_t kBkOffStat = kBkOffClip + 128 * 4;       // [team][half][128 rows] (min, max)
+constexpr uint32_t kBkOffInfo = kBkOffStat + 2 * 2 * 128 * 8;   // [8] chunk records of 8 ints
+constexpr uint32_t kBkOffBar = kBkOffInfo + 8 * 32;        // [0] R, [1 + b] x in buffer b, [5 + b] product b
+constexpr uint32_t kBkOffMisc = kBkOffBar + 9 * 8;         // tensor-memory address, abort flag
+constexpr uint32_t kBkSmem = kBkOffMisc + 16 + 1024;       // + alignment slack
+
+// chunk record fields (record j % 8 describes chunk j)
+enum { kRecB = 0, kRecC0, kRecNb, kRecH0, kRecLast, kRecP0, kRecState };
+enum { kChunkNone = 0, kChunkTma = 1, kChunkCopy = 2 };   // record state: no chunk, x by TMA, x by copies
+
+__device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// barrier `id` of the 256 threads of a team
+__device__ __forceinline__ void team_sync(int id) {
+  asm volatile("bar.sync %0, 256;" ::"r"(id) : "memory");
+}
+// the same barrier, returning whether `p` holds in every thread of the team
+__device__ __forceinline__ bool team_and(int id, bool p) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred pi, po;\n"
+      "setp.ne.u32 pi, %1, 0;\n"
+      "bar.red.and.pred po, %2, 256, pi;\n"
+      "selp.u32 %0, 1, 0, po; }"
+      : "=r"(r)
+      : "r"((uint32_t)p), "r"(id)
+      : "memory");
+  return r != 0u;
+}
+
 template <int GS, int TENSOR>
 __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap, uint8_t* sm) {
   constexpr int NG = 128 / GS;
-  const uint32_t sA = smem_u32(sm + kOffA), sB = smem_u32(sm + kOffB);
-  float* sclip = reinterpret_cast<float*>(sm + kOffClip);
-  float2* sstat = reinterpret_cast<float2*>(sm + kOffStat);     // [2 halves][128 rows] (min, max)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);   // [0] R copy, [1] MMA done, [2] x by TMA
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kOffTmem);
+  const uint32_t sA0 = smem_u32(sm + kBkOffA), sB = smem_u32(sm + kBkOffB);
+  float* sclip = reinterpret_cast<float*>(sm + kBkOffClip);
+  int* info = reinterpret_cast<int*>(sm + kBkOffInfo);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBkOffBar);
+  uint64_t* xfull = bars + 1;   // x of chunk j in buffer j % 4
+  uint64_t* mdone = bars + 5;   // product of chunk j in accumulator j % 4
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kBkOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kBkOffMisc + 4);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = blockIdx.y;
-  constexpr int tensor = TENSOR;
-  // warp w reads accumulator rows 32 (w % 4) .. (its tensor-memory lane quarter)
-  // and channels 64 (w / 4) .. 64 (w / 4) + 63
-  const int quarter = warp & 3, hf = warp >> 2;
-  const int m = 32 * quarter + lane;          // this thread's token row of the chunk
+  const int team = warp >> 3, ltid = tid & 255, lwarp = warp & 7;
+  const bool leader = ltid == 0;
+  const int tbar = 1 + team;   // named barrier of the team (0 is the CTA's)
+  // warp w of a team reads accumulator rows 32 (w % 4) .. (its tensor-memory
+  // lane quarter) and channels 64 (w / 4) .. 64 (w / 4) + 63
+  const int quarter = lwarp & 3, hf = lwarp >> 2;
+  const int qbar = 3 + 4 * team + quarter;   // the quarter's two warps (group 128)
+  const int m = 32 * quarter + lane;         // this thread's token row of a chunk
   const int m16 = m & 15;
+  float2* sstat = reinterpret_cast<float2*>(sm + kBkOffStat) + 256 * team;
+  const int g = blockIdx.y;
 
   if (tid == 0) {
-    mbar_init(bars + 0, 1);
-    mbar_init(bars + 1, 1);
-    mbar_init(bars + 2, 1);
+    for (int i = 0; i < 9; ++i) mbar_init(bars + i, 1);
+    *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 0) tc_alloc(smem_u32(tslot), kTcCols);
-  if (tid < 128) sclip[tid] = a.clip[((size_t)tensor * a.Hkv + g) * 128 + tid];
+  if (warp == 0) tc_alloc(smem_u32(tslot), kBkCols);
+  if (tid < 128) sclip[tid] = a.clip[((size_t)TENSOR * a.Hkv + g) * 128 + tid];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
   if (tid == 0) {   // R^T hi | lo of this (head, tensor), already in the swizzled operand layout
-    const uint4* src = a.rfrag + ((size_t)g * kFragBlocks + 1 + tensor) * 4096;
+    const uint4* src = a.rfrag + ((size_t)g * kFragBlocks + 1 + TENSOR) * 4096;
     mbar_expect_tx(bars + 0, kBBytes);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) bulk_g2s(sm + kOffB + 16384 * c, src + 1024 * c, 16384, bars + 0);
+    for (int c = 0; c < 4; ++c) bulk_g2s(sm + kBkOffB + 16384 * c, src + 1024 * c, 16384, bars + 0);
   }
-  const uint16_t* X = tensor ? a.x[1] : a.x[0];
+  const uint16_t* X = TENSOR ? a.x[1] : a.x[0];
   const int total = a.n_seqs * a.max_chunks;
   const int t0 = blockIdx.x * a.tasks_per_cta;
   const int t1 = min(total, t0 + a.tasks_per_cta);
-  // the walk over this CTA's tasks (every thread holds the same cursor)
-  TaskCursor tc;
-  tc.start(a, t0, t1, tid == 0);
-  // x of a chunk: two TMA tile loads by one thread when all 128 rows lie
-  // below the input's row count T and inside the tensor map (rows below 0 read
-  // as zero); otherwise, so that nothing past the caller's buffer is read and
-  // no row of the chunk is lost, 16-byte copies by every thread with rows
-  // outside the chunk's append range zero-filled
+  // x of a chunk: two TMA tile loads when all 128 rows lie below the input's
+  // row count T and inside the tensor map (rows below 0 read as zero);
+  // otherwise, so that nothing past the caller's buffer is read, 16-byte
+  // copies by the team's threads with rows outside the append range zero-filled
   const int row_lim = (int)min((long long)__ldg(a.cu + a.n_seqs), a.map_rows);
-  uint32_t xphase = 0;
-  auto issue_load = [&](const Chunk& k) -> bool {
-    const int r0 = k.c0 + (k.P0 - k.h0);
-    if (r0 + kChunk <= row_lim) {
-      if (tid == 0) {
-        mbar_expect_tx(bars + 2, kABytes);
-        tma_load_x(sA, xmap, 0, g, r0, bars + 2);
-        tma_load_x(sA + 16384, xmap, 64, g, r0, bars + 2);
-      }
-      return true;
-    }
-    load_chunk(a, X, g, k, sA);
-    return false;
-  };
-  tc.next_live(a, tid == 0);
-  int cur = tc.t;
-  Chunk kc = tc.chunk();
-  bool cur_tma = (cur < t1) ? issue_load(kc) : false;
 
-  bool ok = mbar_wait(bars + 0, 0, kTcPolls);   // R is needed before the first MMA
-  if (!__syncthreads_and(ok)) {
-    if (tid == 0) {
-      flag_error(a.err, KV_DEVERR_TIMEOUT);
-      mbar_wait(bars + 0, 0, kTcPolls);         // the copies in flight, bounded
-      if (cur_tma) mbar_wait(bars + 2, 0, kTcPolls);
+  // The leader's walk over the CTA's live chunks, positioned at the team's
+  // next chunk to load (the walk steps over the other team's chunks).
+  TaskCursor tc;
+  int jm = team - 2, jl = team - 2;   // leader: last chunk whose product / TMA load it issued
+  if (leader) {
+    tc.start(a, t0, t1, tid == 0);
+    tc.next_live(a, tid == 0);
+    if (team == 1 && tc.t < t1) {
+      tc.step(a, false);
+      tc.next_live(a, false);
     }
+  }
+  // leader: record chunk J (the team's next) and start its x load
+  auto load_next = [&](int J) {
+    int* r = info + 8 * (J & 7);
+    if (tc.t >= t1) {
+      r[kRecState] = kChunkNone;
+      return;
+    }
+    const Chunk k = tc.chunk();
+    const int r0 = k.c0 + (k.P0 - k.h0);
+    const bool tma = r0 + kChunk <= row_lim;
+    r[kRecB] = k.b;
+    r[kRecC0] = k.c0;
+    r[kRecNb] = k.nb;
+    r[kRecH0] = k.h0;
+    r[kRecLast] = k.last;
+    r[kRecP0] = k.P0;
+    r[kRecState] = tma ? kChunkTma : kChunkCopy;
+    if (tma) {
+      const uint32_t dst = sA0 + (uint32_t)(J & 3) * kABytes;
+      mbar_expect_tx(xfull + (J & 3), kABytes);
+      tma_load_x(dst, xmap, 0, g, r0, xfull + (J & 3));
+      tma_load_x(dst + 16384, xmap, 64, g, r0, xfull + (J & 3));
+      jl = J;
+    }
+    for (int s2 = 0; s2 < 2 && tc.t < t1; ++s2) {   // past the other team's chunk to this team's next
+      tc.step(a, tid == 0);
+      tc.next_live(a, tid == 0);
+    }
+  };
+  // every thread of the team, after the barrier that published record J:
+  // x of chunk J by 16-byte copies, then the leader's arrival on its buffer
+  auto copy_chunk = [&](int J) {
+    const int* r = info + 8 * (J & 7);
+    Chunk k;
+    k.b = r[kRecB];
+    k.c0 = r[kRecC0];
+    k.nb = r[kRecNb];
+    k.h0 = r[kRecH0];
+    k.last = r[kRecLast];
+    k.P0 = r[kRecP0];
+    load_chunk(a, X, g, k, sA0 + (uint32_t)(J & 3) * kABytes, ltid);
     asm volatile("cp.async.wait_group 0;" ::: "memory");
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tc_dealloc(tmem, kTcCols);
-    return;
+    fence_async_smem();
+    team_sync(tbar);
+    if (leader) mbar_arrive1(xfull + (J & 3));
+  };
+  // leader: the product of chunk J into accumulator J % 4 once its x is in
+  auto issue_product = [&](int J) -> bool {
+    if (!mbar_wait(xfull + (J & 3), (uint32_t)(J >> 2) & 1u, kTcPolls)) return false;
+    issue_rotation(tmem + 128u * (uint32_t)(J & 3), sA0 + (uint32_t)(J & 3) * kABytes, sB, mdone + (J & 3));
+    jm = J;
+    return true;
+  };
+
+  // ---- prologue: the team's first two chunks loading, the first product issued ----
+  if (leader) {
+    load_next(team);
+    load_next(team + 2);
+  }
+  team_sync(tbar);
+  if (info[8 * team + kRecState] == kChunkCopy) copy_chunk(team);
+  if (info[8 * (team + 2) + kRecState] == kChunkCopy) copy_chunk(team + 2);
+  bool r_ok = true;
+  if (leader) {
+    r_ok = mbar_wait(bars + 0, 0, kTcPolls);   // R is needed before the first product
+    bool ok = r_ok;
+    if (ok && info[8 * team + kRecState] != kChunkNone) ok = issue_product(team);
+    if (!ok) {
+      flag_error(a.err, KV_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+    }
   }
 
-  uint32_t phase = 0;
-  const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-  bool x_pending = false;   // a TMA load whose completion has not been waited for
-  while (cur < t1) {
-    const Chunk k = kc;
-    // x of the chunk: thread 0 alone waits for a TMA load (it issues the MMA);
-    // 16-byte copies are every thread's and end with the CTA's barrier
-    bool xok = true;
-    if (cur_tma) {
-      if (tid == 0) xok = mbar_wait(bars + 2, xphase, kTcPolls);
-      xphase ^= 1;
-    } else {
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-      fence_async_smem();
-      __syncthreads();
+  int jw = team - 2;   // last chunk whose product the team has waited for
+  for (int j = team;; j += 2) {
+    const int* r = info + 8 * (j & 7);
+    if (r[kRecState] == kChunkNone) break;
+    // product j complete: the leader waits, the team follows
+    bool ok = true;
+    if (leader) {
+      ok = *abort_flag == 0 && mbar_wait(mdone + (j & 3), (uint32_t)(j >> 2) & 1u, kTcPolls);
+      if (!ok) {
+        flag_error(a.err, KV_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
     }
-
-    // ---- x' = x . R_hi + x . R_lo on the tensor cores (not issued if x did
-    // not arrive: every thread's wait below then runs out) ----
-    if (tid == 0 && xok) issue_rotation(tmem, sA, sB, bars + 1);
-    ok = mbar_wait(bars + 1, phase, kTcPolls);
-    phase ^= 1;
-    if (!__syncthreads_and(ok)) {
-      x_pending = !xok;
-      break;
-    }
+    if (!team_and(tbar, ok)) break;
     tc_fence_after();
-    // the A buffer is consumed: bring in the next chunk behind this epilogue
-    tc.step(a, tid == 0);
-    tc.next_live(a, tid == 0);
-    const int nxt = tc.t;
-    const Chunk kn = tc.chunk();
-    const bool nxt_tma = (nxt < t1) ? issue_load(kn) : false;
+    jw = j;
+    Chunk k;
+    k.b = r[kRecB];
+    k.h0 = r[kRecH0];
+    k.nb = r[kRecNb];
+    k.last = r[kRecLast];
+    k.P0 = r[kRecP0];
+    // the team's next product (its x has been loading for a whole chunk) into
+    // the accumulator chunk j - 2 left
+    if (leader && info[8 * ((j + 2) & 7) + kRecState] != kChunkNone && !issue_product(j + 2)) {
+      flag_error(a.err, KV_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+    }
 
     // ---- destination tile of this row (its page id read before the epilogue) ----
     const int pos = k.P0 + m;
@@ -568,7 +691,8 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
     // ---- this thread's row and channel half -> s, z and codes ----
     constexpr int NS = (TENSOR == 0) ? 4 : 8;
     uint32_t wd[NS][2];
-    const ScaleZero q = row_codes<GS, TENSOR>(trow, hf, m, sclip, sstat, wd);
+    const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16) + 128u * (uint32_t)(j & 3);
+    const ScaleZero q = row_codes<GS, TENSOR>(trow, hf, m, sclip, sstat, wd, qbar);
     const bool pid_ok = pid_raw >= 0 && pid_raw < a.num_pages;
     if (tile_live && !pid_ok && m16 == 0 && hf == 0) flag_error(a.err, KV_DEVERR_PAGE_ID);
     const bool write = tile_live && pid_ok;
@@ -644,31 +768,31 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
         rec[GS == 64 ? hf : 0] = __halves2half2(q.sh, q.zh);
       }
     }
+    // the x of the team's chunk j + 4 into the buffer product j has released
+    if (leader) load_next(j + 4);
     tc_fence_before();
-    __syncthreads();   // the accumulator is free for the next chunk
-    cur = nxt;
-    kc = kn;
-    cur_tma = nxt_tma;
+    team_sync(tbar);   // accumulator j % 4 is free for product j + 4; record j + 4 is published
+    if (info[8 * ((j + 4) & 7) + kRecState] == kChunkCopy) copy_chunk(j + 4);
   }
 
-  if (!ok) {   // a completion did not arrive in time: wait (bounded) for the work in flight
-    if (tid == 0) flag_error(a.err, KV_DEVERR_TIMEOUT);
-    if (x_pending) mbar_wait(bars + 2, xphase ^ 1, kTcPolls);
-    else mbar_wait(bars + 1, phase ^ 1, kTcPolls);
+  // leader: wait (bounded) for what is still in flight after an early exit:
+  // products issued but not waited for, then TMA loads no product consumed
+  if (leader) {
+    if (!r_ok) mbar_wait(bars + 0, 0, kTcPolls);
+    for (int J = jw + 2; J <= jm; J += 2) mbar_wait(mdone + (J & 3), (uint32_t)(J >> 2) & 1u, kTcPolls);
+    for (int J = jm + 2; J <= jl; J += 2)
+      if (info[8 * (J & 7) + kRecState] == kChunkTma) mbar_wait(xfull + (J & 3), (uint32_t)(J >> 2) & 1u, kTcPolls);
   }
   asm volatile("cp.async.wait_group 0;" ::: "memory");
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tc_dealloc(tmem, kTcCols);
-  if (tid == 0) {
-    mbar_inval(bars + 0);
-    mbar_inval(bars + 1);
-    mbar_inval(bars + 2);
-  }
+  if (warp == 0) tc_dealloc(tmem, kBkCols);
+  if (tid == 0)
+    for (int i = 0; i < 9; ++i) mbar_inval(bars + i);
 }
 
 template <int GS, int TENSOR>
-__global__ void __launch_bounds__(kTcThreads, 2)
+__global__ void __launch_bounds__(kBkThreads, 1)
     append_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap xmap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -870,7 +994,7 @@ __device__ __forceinline__ void evict_body(const StepArgs& a, int B, uint8_t* sm
     constexpr int NS = (TENSOR == 0) ? 4 : 8;
     uint32_t wd[NS][2];
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-    const ScaleZero q = row_codes<GS, TENSOR>(trow, hf, m, sclip, sstat, wd);
+    const ScaleZero q = row_codes<GS, TENSOR>(trow, hf, m, sclip, sstat, wd, 1 + quarter);
     const long long tof = rtile[m];
     if (tof >= 0) {
       const int pos = rpos[m];
@@ -996,8 +1120,8 @@ cudaError_t launch_append_tc(const Pool& p, int layer, int n_seqs, const void* k
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  // two CTAs per SM over the KV heads of one tensor; K, then V
-  long long ctas = (2LL * p.sm_count + H - 1) / H;
+  // one CTA per SM over the KV heads of one tensor; K, then V
+  long long ctas = ((long long)p.sm_count + H - 1) / H;
   ctas = max(1LL, min(ctas, tasks));
   a.tasks_per_cta = (int)((tasks + ctas - 1) / ctas);
   ctas = (tasks + a.tasks_per_cta - 1) / a.tasks_per_cta;
@@ -1005,14 +1129,14 @@ cudaError_t launch_append_tc(const Pool& p, int layer, int n_seqs, const void* k
   static bool attr[2][2] = {{false, false}, {false, false}};
   auto go = [&](auto kernel, int gi, int t) -> cudaError_t {
     if (!attr[gi][t]) {
-      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
-      // the whole unified L1 / shared array as shared memory, so that two CTAs fit
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBkSmem);
+      // the whole unified L1 / shared array as shared memory
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
       if (e != cudaSuccess) return e;
       attr[gi][t] = true;
     }
-    kernel<<<grid, kTcThreads, kTcSmem, s>>>(a, maps[t]);
+    kernel<<<grid, kBkThreads, kBkSmem, s>>>(a, maps[t]);
     return cudaGetLastError();
   };
   cudaError_t e;
