@@ -282,13 +282,17 @@ __device__ __forceinline__ void load_chunk(const TcArgs& a, const uint16_t* X, i
 // accumulator at tmem; completion arrives on `bar`.  One thread issues.
 __device__ __forceinline__ void issue_rotation(uint32_t tmem, uint32_t sA, uint32_t sB, uint64_t* bar) {
   tc_fence_after();
+  // descriptors of the later steps: the start-address field (address / 16,
+  // 14 bits) of the first plus the step's byte offset / 16 (the operands lie
+  // below 256 KB, so the field does not carry)
+  const uint64_t ad0 = sw128_desc(sA), bd0 = sw128_desc(sB);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const uint32_t koff = (ks & 3) * 32;   // 16 channels = 32 bytes into the swizzled row
-    const uint64_t ad = sw128_desc(sA + (ks >> 2) * 16384 + koff);
-    const uint32_t bb = sB + (ks >> 2) * 32768 + koff;   // rows 0-127: hi; 128-255: lo
-    tc_mma(tmem, ad, sw128_desc(bb), kIdesc, ks > 0 ? 1u : 0u);
-    tc_mma(tmem, ad, sw128_desc(bb + 16384), kIdesc, 1u);
+    const uint64_t ad = ad0 + (((ks >> 2) * 16384 + koff) >> 4);
+    const uint64_t bd = bd0 + (((ks >> 2) * 32768 + koff) >> 4);   // rows 0-127: hi; 128-255: lo
+    tc_mma(tmem, ad, bd, kIdesc, ks > 0 ? 1u : 0u);
+    tc_mma(tmem, ad, bd + (16384 >> 4), kIdesc, 1u);
   }
   tc_commit(smem_u32(bar));
 }
@@ -474,12 +478,13 @@ __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, con
 // The CTA's live chunks j = 0, 1, 2, ... alternate between the teams (team
 // j % 2).  Chunk j's x lands in buffer j % 4 and its product in accumulator
 // j % 4 (tensor-memory columns 128 (j % 4)), so every buffer and accumulator
-// belongs to one team.  At the start of its chunk j a team's leader issues the
-// product of the team's next chunk j + 2, whose x has been loading for a
-// whole chunk, into the accumulator that chunk j - 2 left; once chunk j's own
-// product has been read the leader starts the x load of chunk j + 4 into the
-// buffer chunk j's product has released.  The epilogue of a chunk thus never
-// waits for the tensor cores, and the two teams keep sixteen warps issuing.
+// belongs to one team.  At the start of its chunk j, once product j is
+// complete, a team's leader thread issues the product of the team's next chunk
+// j + 2 (its x has been loading for a whole chunk) into the accumulator that
+// chunk j - 2 left, and its loader thread (in another warp) starts the x load
+// of chunk j + 4 into the buffer product j has released.  The epilogue of a
+// chunk thus never waits for the tensor cores, and the two teams keep sixteen
+// warps issuing.
 constexpr int kBkThreads = 512;
 constexpr int kBkCols = 512;                 // four 128-column fp32 accumulators
 constexpr uint32_t kBkOffB = 0;              // R^T hi | lo
@@ -529,7 +534,8 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kBkOffMisc + 4);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int team = warp >> 3, ltid = tid & 255, lwarp = warp & 7;
-  const bool leader = ltid == 0;
+  const bool leader = ltid == 0;        // waits for and issues the team's products
+  const bool loader = ltid == 32;       // walks the tasks and starts the team's x loads
   const int tbar = 1 + team;   // named barrier of the team (0 is the CTA's)
   // warp w of a team reads accumulator rows 32 (w % 4) .. (its tensor-memory
   // lane quarter) and channels 64 (w / 4) .. 64 (w / 4) + 63
@@ -567,19 +573,21 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
   // copies by the team's threads with rows outside the append range zero-filled
   const int row_lim = (int)min((long long)__ldg(a.cu + a.n_seqs), a.map_rows);
 
-  // The leader's walk over the CTA's live chunks, positioned at the team's
-  // next chunk to load (the walk steps over the other team's chunks).
+  // The loader's walk over the CTA's live chunks, positioned at the team's
+  // next chunk to load (the walk steps over the other team's chunks); team
+  // 0's loader reports the errors of the sequences it walks into.
   TaskCursor tc;
-  int jm = team - 2, jl = team - 2;   // leader: last chunk whose product / TMA load it issued
-  if (leader) {
-    tc.start(a, t0, t1, tid == 0);
-    tc.next_live(a, tid == 0);
+  int jm = team - 2;   // leader: last chunk whose product it issued
+  int jl = team - 2;   // loader: last chunk whose x it loaded by TMA
+  if (loader) {
+    tc.start(a, t0, t1, team == 0);
+    tc.next_live(a, team == 0);
     if (team == 1 && tc.t < t1) {
       tc.step(a, false);
       tc.next_live(a, false);
     }
   }
-  // leader: record chunk J (the team's next) and start its x load
+  // loader: record chunk J (the team's next) and start its x load
   auto load_next = [&](int J) {
     int* r = info + 8 * (J & 7);
     if (tc.t >= t1) {
@@ -604,12 +612,12 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
       jl = J;
     }
     for (int s2 = 0; s2 < 2 && tc.t < t1; ++s2) {   // past the other team's chunk to this team's next
-      tc.step(a, tid == 0);
-      tc.next_live(a, tid == 0);
+      tc.step(a, team == 0);
+      tc.next_live(a, team == 0);
     }
   };
   // every thread of the team, after the barrier that published record J:
-  // x of chunk J by 16-byte copies, then the leader's arrival on its buffer
+  // x of chunk J by 16-byte copies, then the loader's arrival on its buffer
   auto copy_chunk = [&](int J) {
     const int* r = info + 8 * (J & 7);
     Chunk k;
@@ -623,7 +631,7 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     fence_async_smem();
     team_sync(tbar);
-    if (leader) mbar_arrive1(xfull + (J & 3));
+    if (loader) mbar_arrive1(xfull + (J & 3));
   };
   // leader: the product of chunk J into accumulator J % 4 once its x is in
   auto issue_product = [&](int J) -> bool {
@@ -634,7 +642,7 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
   };
 
   // ---- prologue: the team's first two chunks loading, the first product issued ----
-  if (leader) {
+  if (loader) {
     load_next(team);
     load_next(team + 2);
   }
@@ -680,6 +688,8 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
       flag_error(a.err, KV_DEVERR_TIMEOUT);
       *abort_flag = 1;
     }
+    // the x of the team's chunk j + 4 into the buffer product j has released
+    if (loader) load_next(j + 4);
 
     // ---- destination tile of this row (its page id read before the epilogue) ----
     const int pos = k.P0 + m;
@@ -768,21 +778,21 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
         rec[GS == 64 ? hf : 0] = __halves2half2(q.sh, q.zh);
       }
     }
-    // the x of the team's chunk j + 4 into the buffer product j has released
-    if (leader) load_next(j + 4);
     tc_fence_before();
     team_sync(tbar);   // accumulator j % 4 is free for product j + 4; record j + 4 is published
     if (info[8 * ((j + 4) & 7) + kRecState] == kChunkCopy) copy_chunk(j + 4);
   }
 
-  // leader: wait (bounded) for what is still in flight after an early exit:
-  // products issued but not waited for, then TMA loads no product consumed
+  // wait (bounded) for what is still in flight after an early exit: the
+  // leader for products issued but not waited for, the loader for TMA loads
+  // of chunks the team did not reach (a load a product consumed has completed)
   if (leader) {
     if (!r_ok) mbar_wait(bars + 0, 0, kTcPolls);
     for (int J = jw + 2; J <= jm; J += 2) mbar_wait(mdone + (J & 3), (uint32_t)(J >> 2) & 1u, kTcPolls);
-    for (int J = jm + 2; J <= jl; J += 2)
-      if (info[8 * (J & 7) + kRecState] == kChunkTma) mbar_wait(xfull + (J & 3), (uint32_t)(J >> 2) & 1u, kTcPolls);
   }
+  if (loader)
+    for (int J = jw + 2; J <= jl; J += 2)
+      if (info[8 * (J & 7) + kRecState] == kChunkTma) mbar_wait(xfull + (J & 3), (uint32_t)(J >> 2) & 1u, kTcPolls);
   asm volatile("cp.async.wait_group 0;" ::: "memory");
   tc_fence_before();
   __syncthreads();
