@@ -13,18 +13,19 @@
 // and one tensor is x [128 x 128] . R_hi + x . R_lo, both terms accumulated
 // into one fp32 accumulator (R enters as bf16 hi and lo terms; x is exact in
 // bf16).  The bulk append runs one CTA per SM on one (KV head, tensor): two
-// teams of eight warps take the CTA's 128-token chunks in turn:
-//   * x rows arrive by two TMA tile loads (128-byte swizzle, the K-major
-//     operand layout) when the whole chunk lies inside the input, else by
-//     16-byte cp.async with rows outside the append range zero-filled, into
-//     one of four buffers, two chunks ahead of the epilogue.  R^T hi | lo
-//     arrives once per CTA, pre-swizzled in global memory by the rotation
-//     set-up, as four bulk copies;
-//   * a team's leader thread issues sixteen tcgen05.mma (kind::f16, M 128,
+// teams of eight epilogue warps take the CTA's 128-token chunks in turn, and
+// four serving warps feed them:
+//   * per team a loader thread walks the tasks and starts each chunk's x load
+//     as soon as one of four buffers is free: two TMA tile loads (128-byte
+//     swizzle, the K-major operand layout) when the whole chunk lies inside
+//     the input, else 16-byte cp.async by the loader's warp with rows outside
+//     the append range zero-filled.  R^T hi | lo arrives once per CTA,
+//     pre-swizzled in global memory by the rotation set-up, as four bulk
+//     copies;
+//   * per team an issuer thread starts sixteen tcgen05.mma (kind::f16, M 128,
 //     N 128, K 16: per 16-channel step the hi term, then the lo term) into
 //     one of four 128-column fp32 accumulators in tensor memory (all 512
-//     columns), one chunk ahead of the team's epilogue, and commits them to
-//     an mbarrier;
+//     columns) and commits them to an mbarrier;
 //   * every thread of a team owns one token row and one half of the channels
 //     of the accumulator (tcgen05.ld; warps w and w + 4 of a team share a
 //     lane quarter): clip, per-group min / max (combined across the halves
@@ -474,27 +475,32 @@ __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, con
   return q;
 }
 
-// ---- bulk append: one CTA per SM, two teams of eight warps ----------------
-// The CTA's live chunks j = 0, 1, 2, ... alternate between the teams (team
-// j % 2).  Chunk j's x lands in buffer j % 4 and its product in accumulator
-// j % 4 (tensor-memory columns 128 (j % 4)), so every buffer and accumulator
-// belongs to one team.  At the start of its chunk j, once product j is
-// complete, a team's leader thread issues the product of the team's next chunk
-// j + 2 (its x has been loading for a whole chunk) into the accumulator that
-// chunk j - 2 left, and its loader thread (in another warp) starts the x load
-// of chunk j + 4 into the buffer product j has released.  The epilogue of a
-// chunk thus never waits for the tensor cores, and the two teams keep sixteen
-// warps issuing.
-constexpr int kBkThreads = 512;
+// ---- bulk append: one CTA per SM, warp-specialised ---------------------------
+// The CTA's live chunks j = 0, 1, 2, ... alternate between two teams of eight
+// epilogue warps (team j % 2).  Chunk j's x lands in buffer j % 4 and its
+// product in accumulator j % 4 (tensor-memory columns 128 (j % 4)), so every
+// buffer and accumulator belongs to one team.  Four more warps serve the
+// teams, one thread each: per team a loader walks the tasks, publishes each
+// chunk's record and starts its x load as soon as the buffer is free (product
+// j - 4 complete), and an issuer starts product j once its x is in and the
+// team has read accumulator j % 4 for chunk j - 4.  Nothing waits on a CTA
+// barrier inside the loop: records, x, products and accumulators are handed
+// over through mbarriers, and an issuer thread that stalls while the tensor
+// cores take its sixteen MMAs holds up no epilogue warp.
+constexpr int kBkWarps = 20;                 // 16 epilogue + 4 serving warps
+constexpr int kBkThreads = 32 * kBkWarps;
 constexpr int kBkCols = 512;                 // four 128-column fp32 accumulators
 constexpr uint32_t kBkOffB = 0;              // R^T hi | lo
 constexpr uint32_t kBkOffA = kBkOffB + kBBytes;             // four x buffers
 constexpr uint32_t kBkOffClip = kBkOffA + 4 * kABytes;
-constexpr uint32_t kBkOffStat = kBkOffClip + 128 * 4;       // [team][half][128 rows] (min, max)
-constexpr uint32_t kBkOffInfo = kBkOffStat + 2 * 2 * 128 * 8;   // [8] chunk records of 8 ints
-constexpr uint32_t kBkOffBar = kBkOffInfo + 8 * 32;        // [0] R, [1 + b] x in buffer b, [5 + b] product b
-constexpr uint32_t kBkOffMisc = kBkOffBar + 9 * 8;         // tensor-memory address, abort flag
-constexpr uint32_t kBkSmem = kBkOffMisc + 16 + 1024;       // + alignment slack
+constexpr uint32_t kBkOffStat = kBkOffClip + 128 * 4;       // [team][chunk parity][half][128 rows] (min, max)
+constexpr uint32_t kBkOffInfo = kBkOffStat + 2 * 2 * 2 * 128 * 8;   // [8] chunk records of 8 ints
+// mbarriers: [0] R; [1 + b] x in buffer b; [5 + b] product b done; [9 + b]
+// accumulator b read (eight warps); [13 + s] record s published
+constexpr int kBkBars = 21;
+constexpr uint32_t kBkOffBar = kBkOffInfo + 8 * 32;
+constexpr uint32_t kBkOffMisc = kBkOffBar + kBkBars * 8;     // tensor-memory address, abort flag, last load / product per buffer
+constexpr uint32_t kBkSmem = kBkOffMisc + 48 + 1024;        // + alignment slack
 
 // chunk record fields (record j % 8 describes chunk j)
 enum { kRecB = 0, kRecC0, kRecNb, kRecH0, kRecLast, kRecP0, kRecState };
@@ -503,17 +509,16 @@ enum { kChunkNone = 0, kChunkTma = 1, kChunkCopy = 2 };   // record state: no ch
 __device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-// barrier `id` of the 256 threads of a team
-__device__ __forceinline__ void team_sync(int id) {
-  asm volatile("bar.sync %0, 256;" ::"r"(id) : "memory");
-}
-// the same barrier, returning whether `p` holds in every thread of the team
-__device__ __forceinline__ bool team_and(int id, bool p) {
+__device__ __forceinline__ uint32_t par(int j, int shift) { return (uint32_t)(j >> shift) & 1u; }
+// whether `p` holds in all 64 threads of named barrier `id` (both warps of a
+// lane quarter), so that the two take the same branch before the barrier
+// they share in the epilogue of group 128
+__device__ __forceinline__ bool pair_and(int id, bool p) {
   uint32_t r;
   asm volatile(
       "{ .reg .pred pi, po;\n"
       "setp.ne.u32 pi, %1, 0;\n"
-      "bar.red.and.pred po, %2, 256, pi;\n"
+      "bar.red.and.pred po, %2, 64, pi;\n"
       "selp.u32 %0, 1, 0, po; }"
       : "=r"(r)
       : "r"((uint32_t)p), "r"(id)
@@ -528,26 +533,27 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
   float* sclip = reinterpret_cast<float*>(sm + kBkOffClip);
   int* info = reinterpret_cast<int*>(sm + kBkOffInfo);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBkOffBar);
-  uint64_t* xfull = bars + 1;   // x of chunk j in buffer j % 4
-  uint64_t* mdone = bars + 5;   // product of chunk j in accumulator j % 4
+  uint64_t* xfull = bars + 1;     // x of chunk j in buffer j % 4
+  uint64_t* mdone = bars + 5;     // product of chunk j in accumulator j % 4
+  uint64_t* accfree = bars + 9;   // accumulator j % 4 read by the team's eight warps
+  uint64_t* recready = bars + 13; // record j % 8 published
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kBkOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kBkOffMisc + 4);
+  int* last_load = reinterpret_cast<int*>(sm + kBkOffMisc + 8);   // [4] last chunk loaded by TMA per buffer
+  int* last_prod = last_load + 4;                                  // [4] last product issued per accumulator
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int team = warp >> 3, ltid = tid & 255, lwarp = warp & 7;
-  const bool leader = ltid == 0;        // waits for and issues the team's products
-  const bool loader = ltid == 32;       // walks the tasks and starts the team's x loads
-  const int tbar = 1 + team;   // named barrier of the team (0 is the CTA's)
-  // warp w of a team reads accumulator rows 32 (w % 4) .. (its tensor-memory
-  // lane quarter) and channels 64 (w / 4) .. 64 (w / 4) + 63
-  const int quarter = lwarp & 3, hf = lwarp >> 2;
-  const int qbar = 3 + 4 * team + quarter;   // the quarter's two warps (group 128)
-  const int m = 32 * quarter + lane;         // this thread's token row of a chunk
-  const int m16 = m & 15;
-  float2* sstat = reinterpret_cast<float2*>(sm + kBkOffStat) + 256 * team;
   const int g = blockIdx.y;
 
   if (tid == 0) {
-    for (int i = 0; i < 9; ++i) mbar_init(bars + i, 1);
+    mbar_init(bars + 0, 1);
+    for (int b = 0; b < 4; ++b) {
+      mbar_init(xfull + b, 1);
+      mbar_init(mdone + b, 1);
+      mbar_init(accfree + b, 8);
+      last_load[b] = -1;
+      last_prod[b] = -1;
+    }
+    for (int s2 = 0; s2 < 8; ++s2) mbar_init(recready + s2, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -563,242 +569,250 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
 #pragma unroll
     for (int c = 0; c < 4; ++c) bulk_g2s(sm + kBkOffB + 16384 * c, src + 1024 * c, 16384, bars + 0);
   }
-  const uint16_t* X = TENSOR ? a.x[1] : a.x[0];
-  const int total = a.n_seqs * a.max_chunks;
-  const int t0 = blockIdx.x * a.tasks_per_cta;
-  const int t1 = min(total, t0 + a.tasks_per_cta);
-  // x of a chunk: two TMA tile loads when all 128 rows lie below the input's
-  // row count T and inside the tensor map (rows below 0 read as zero);
-  // otherwise, so that nothing past the caller's buffer is read, 16-byte
-  // copies by the team's threads with rows outside the append range zero-filled
-  const int row_lim = (int)min((long long)__ldg(a.cu + a.n_seqs), a.map_rows);
-
-  // The loader's walk over the CTA's live chunks, positioned at the team's
-  // next chunk to load (the walk steps over the other team's chunks); team
-  // 0's loader reports the errors of the sequences it walks into.
-  TaskCursor tc;
-  int jm = team - 2;   // leader: last chunk whose product it issued
-  int jl = team - 2;   // loader: last chunk whose x it loaded by TMA
-  if (loader) {
-    tc.start(a, t0, t1, team == 0);
-    tc.next_live(a, team == 0);
-    if (team == 1 && tc.t < t1) {
-      tc.step(a, false);
-      tc.next_live(a, false);
-    }
-  }
-  // loader: record chunk J (the team's next) and start its x load
-  auto load_next = [&](int J) {
-    int* r = info + 8 * (J & 7);
-    if (tc.t >= t1) {
-      r[kRecState] = kChunkNone;
-      return;
-    }
-    const Chunk k = tc.chunk();
-    const int r0 = k.c0 + (k.P0 - k.h0);
-    const bool tma = r0 + kChunk <= row_lim;
-    r[kRecB] = k.b;
-    r[kRecC0] = k.c0;
-    r[kRecNb] = k.nb;
-    r[kRecH0] = k.h0;
-    r[kRecLast] = k.last;
-    r[kRecP0] = k.P0;
-    r[kRecState] = tma ? kChunkTma : kChunkCopy;
-    if (tma) {
-      const uint32_t dst = sA0 + (uint32_t)(J & 3) * kABytes;
-      mbar_expect_tx(xfull + (J & 3), kABytes);
-      tma_load_x(dst, xmap, 0, g, r0, xfull + (J & 3));
-      tma_load_x(dst + 16384, xmap, 64, g, r0, xfull + (J & 3));
-      jl = J;
-    }
-    for (int s2 = 0; s2 < 2 && tc.t < t1; ++s2) {   // past the other team's chunk to this team's next
-      tc.step(a, team == 0);
-      tc.next_live(a, team == 0);
-    }
-  };
-  // every thread of the team, after the barrier that published record J:
-  // x of chunk J by 16-byte copies, then the loader's arrival on its buffer
-  auto copy_chunk = [&](int J) {
-    const int* r = info + 8 * (J & 7);
-    Chunk k;
-    k.b = r[kRecB];
-    k.c0 = r[kRecC0];
-    k.nb = r[kRecNb];
-    k.h0 = r[kRecH0];
-    k.last = r[kRecLast];
-    k.P0 = r[kRecP0];
-    load_chunk(a, X, g, k, sA0 + (uint32_t)(J & 3) * kABytes, ltid);
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    fence_async_smem();
-    team_sync(tbar);
-    if (loader) mbar_arrive1(xfull + (J & 3));
-  };
-  // leader: the product of chunk J into accumulator J % 4 once its x is in
-  auto issue_product = [&](int J) -> bool {
-    if (!mbar_wait(xfull + (J & 3), (uint32_t)(J >> 2) & 1u, kTcPolls)) return false;
-    issue_rotation(tmem + 128u * (uint32_t)(J & 3), sA0 + (uint32_t)(J & 3) * kABytes, sB, mdone + (J & 3));
-    jm = J;
-    return true;
+  auto fail = [&]() {
+    flag_error(a.err, KV_DEVERR_TIMEOUT);
+    *abort_flag = 1;
   };
 
-  // ---- prologue: the team's first two chunks loading, the first product issued ----
-  if (loader) {
-    load_next(team);
-    load_next(team + 2);
-  }
-  team_sync(tbar);
-  if (info[8 * team + kRecState] == kChunkCopy) copy_chunk(team);
-  if (info[8 * (team + 2) + kRecState] == kChunkCopy) copy_chunk(team + 2);
-  bool r_ok = true;
-  if (leader) {
-    r_ok = mbar_wait(bars + 0, 0, kTcPolls);   // R is needed before the first product
-    bool ok = r_ok;
-    if (ok && info[8 * team + kRecState] != kChunkNone) ok = issue_product(team);
-    if (!ok) {
-      flag_error(a.err, KV_DEVERR_TIMEOUT);
-      *abort_flag = 1;
+  if (warp >= 16) {
+    // ---- serving warps: 16 + t loads for team t, 18 + t issues its products ----
+    const int team = warp & 1;
+    if (warp < 18) {
+      const uint16_t* X = TENSOR ? a.x[1] : a.x[0];
+      const int total = a.n_seqs * a.max_chunks;
+      const int t0 = blockIdx.x * a.tasks_per_cta;
+      const int t1 = min(total, t0 + a.tasks_per_cta);
+      // x of a chunk: two TMA tile loads when all 128 rows lie below the
+      // input's row count T and inside the tensor map (rows below 0 read as
+      // zero); otherwise, so that nothing past the caller's buffer is read,
+      // 16-byte copies by the loader's warp with rows outside the append range
+      // zero-filled
+      const int row_lim = (int)min((long long)__ldg(a.cu + a.n_seqs), a.map_rows);
+      // the walk over the CTA's live chunks, at the team's next chunk (it
+      // steps over the other team's); team 0's loader reports the errors of
+      // the sequences it walks into
+      TaskCursor tc;
+      const bool report = team == 0 && lane == 0;
+      tc.start(a, t0, t1, report);
+      tc.next_live(a, report);
+      if (team == 1 && tc.t < t1) {
+        tc.step(a, false);
+        tc.next_live(a, false);
+      }
+      for (int J = team;; J += 2) {
+        // buffer J % 4 is free once product J - 4 is complete; record J % 8
+        // was read by the team before it released accumulator (J - 8) % 4,
+        // which came before product J - 4
+        if (J >= 4) {
+          bool ok = *abort_flag == 0;
+          if (ok && lane == 0) ok = mbar_wait(mdone + (J & 3), par(J - 4, 2), kTcPolls);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) {
+            if (lane == 0) fail();
+            break;
+          }
+        }
+        int* r = info + 8 * (J & 7);
+        const bool have = tc.t < t1;
+        Chunk k = tc.chunk();
+        const int r0 = k.c0 + (k.P0 - k.h0);
+        const bool tma = have && r0 + kChunk <= row_lim;
+        if (lane == 0) {
+          r[kRecB] = k.b;
+          r[kRecC0] = k.c0;
+          r[kRecNb] = k.nb;
+          r[kRecH0] = k.h0;
+          r[kRecLast] = k.last;
+          r[kRecP0] = k.P0;
+          r[kRecState] = !have ? kChunkNone : tma ? kChunkTma : kChunkCopy;
+          if (tma) {
+            const uint32_t dst = sA0 + (uint32_t)(J & 3) * kABytes;
+            mbar_expect_tx(xfull + (J & 3), kABytes);
+            tma_load_x(dst, xmap, 0, g, r0, xfull + (J & 3));
+            tma_load_x(dst + 16384, xmap, 64, g, r0, xfull + (J & 3));
+            last_load[J & 3] = J;
+          }
+          mbar_arrive1(recready + (J & 7));   // release: the record is visible to its waiters
+        }
+        if (!have) break;
+        if (!tma) {   // the warp's 32 lanes copy the 128 half rows x 2 of the chunk
+          for (int i = 0; i < 8; ++i) load_chunk(a, X, g, k, sA0 + (uint32_t)(J & 3) * kABytes, lane + 32 * i);
+          asm volatile("cp.async.wait_group 0;" ::: "memory");
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive1(xfull + (J & 3));
+        }
+        for (int s2 = 0; s2 < 2 && tc.t < t1; ++s2) {   // past the other team's chunk to this team's next
+          tc.step(a, report);
+          tc.next_live(a, report);
+        }
+      }
+    } else if (lane == 0) {
+      bool ok = mbar_wait(bars + 0, 0, kTcPolls);   // R is needed before the first product
+      if (!ok) fail();
+      for (int J = team; ok; J += 2) {
+        ok = *abort_flag == 0 && mbar_wait(recready + (J & 7), par(J, 3), kTcPolls);
+        if (!ok) {
+          fail();
+          break;
+        }
+        if (info[8 * (J & 7) + kRecState] == kChunkNone) break;
+        // x in, and accumulator J % 4 read by the team for chunk J - 4
+        ok = mbar_wait(xfull + (J & 3), par(J, 2), kTcPolls) &&
+             (J < 4 || mbar_wait(accfree + (J & 3), par(J - 4, 2), kTcPolls));
+        if (!ok) {
+          fail();
+          break;
+        }
+        issue_rotation(tmem + 128u * (uint32_t)(J & 3), sA0 + (uint32_t)(J & 3) * kABytes, sB, mdone + (J & 3));
+        last_prod[J & 3] = J;
+      }
     }
-  }
-
-  int jw = team - 2;   // last chunk whose product the team has waited for
-  for (int j = team;; j += 2) {
-    const int* r = info + 8 * (j & 7);
-    if (r[kRecState] == kChunkNone) break;
-    // product j complete: the leader waits, the team follows
-    bool ok = true;
-    if (leader) {
-      ok = *abort_flag == 0 && mbar_wait(mdone + (j & 3), (uint32_t)(j >> 2) & 1u, kTcPolls);
+    __syncwarp();
+  } else {
+    // ---- epilogue warps ----
+    const int team = warp >> 3, lwarp = warp & 7;
+    // warp w of a team reads accumulator rows 32 (w % 4) .. (its tensor-memory
+    // lane quarter) and channels 64 (w / 4) .. 64 (w / 4) + 63
+    const int quarter = lwarp & 3, hf = lwarp >> 2;
+    const int qbar = 1 + 4 * team + quarter;   // the quarter's two warps (group 128)
+    const int m = 32 * quarter + lane;         // this thread's token row of a chunk
+    const int m16 = m & 15;
+    for (int j = team;; j += 2) {
+      // the chunk's record, then its product (at group 128 the two warps of a
+      // quarter decide together: they meet at a barrier in the epilogue)
+      bool ok = __all_sync(0xffffffffu, *abort_flag == 0 && mbar_wait(recready + (j & 7), par(j, 3), kTcPolls));
+      if (GS == 128) ok = pair_and(qbar, ok);
+      const int* r = info + 8 * (j & 7);
+      if (ok && r[kRecState] == kChunkNone) break;
+      if (ok) {
+        ok = __all_sync(0xffffffffu, mbar_wait(mdone + (j & 3), par(j, 2), kTcPolls));
+        if (GS == 128) ok = pair_and(qbar, ok);
+      }
       if (!ok) {
-        flag_error(a.err, KV_DEVERR_TIMEOUT);
-        *abort_flag = 1;
+        if (lane == 0) fail();
+        break;
       }
-    }
-    if (!team_and(tbar, ok)) break;
-    tc_fence_after();
-    jw = j;
-    Chunk k;
-    k.b = r[kRecB];
-    k.h0 = r[kRecH0];
-    k.nb = r[kRecNb];
-    k.last = r[kRecLast];
-    k.P0 = r[kRecP0];
-    // the team's next product (its x has been loading for a whole chunk) into
-    // the accumulator chunk j - 2 left
-    if (leader && info[8 * ((j + 2) & 7) + kRecState] != kChunkNone && !issue_product(j + 2)) {
-      flag_error(a.err, KV_DEVERR_TIMEOUT);
-      *abort_flag = 1;
-    }
-    // the x of the team's chunk j + 4 into the buffer product j has released
-    if (loader) load_next(j + 4);
+      tc_fence_after();
+      Chunk k;
+      k.b = r[kRecB];
+      k.h0 = r[kRecH0];
+      k.nb = r[kRecNb];
+      k.last = r[kRecLast];
+      k.P0 = r[kRecP0];
 
-    // ---- destination tile of this row (its page id read before the epilogue) ----
-    const int pos = k.P0 + m;
-    const bool row_ok = pos >= k.h0 && pos < k.h0 + k.nb;
-    const int tile = pos / kTile;
-    const bool tile_live = tile <= k.last;
-    const int pid_raw = __ldg(a.pt + (size_t)k.b * a.max_pages + min((tile * kTile) / a.P, a.max_pages - 1));
+      // ---- destination tile of this row (its page id read before the epilogue) ----
+      const int pos = k.P0 + m;
+      const bool row_ok = pos >= k.h0 && pos < k.h0 + k.nb;
+      const int tile = pos / kTile;
+      const bool tile_live = tile <= k.last;
+      const int pid_raw = __ldg(a.pt + (size_t)k.b * a.max_pages + min((tile * kTile) / a.P, a.max_pages - 1));
 
-    // ---- this thread's row and channel half -> s, z and codes ----
-    constexpr int NS = (TENSOR == 0) ? 4 : 8;
-    uint32_t wd[NS][2];
-    const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16) + 128u * (uint32_t)(j & 3);
-    const ScaleZero q = row_codes<GS, TENSOR>(trow, hf, m, sclip, sstat, wd, qbar);
-    const bool pid_ok = pid_raw >= 0 && pid_raw < a.num_pages;
-    if (tile_live && !pid_ok && m16 == 0 && hf == 0) flag_error(a.err, KV_DEVERR_PAGE_ID);
-    const bool write = tile_live && pid_ok;
-    uint8_t* tb = a.hist + (size_t)(pid_ok ? pid_raw : 0) * a.page_bytes + (size_t)g * a.head_block +
-                  (size_t)((tile * kTile) % a.P / kTile) * a.tile_bytes;
-    const unsigned okmask = __ballot_sync(0xffffffffu, row_ok && write);
+      // ---- this thread's row and channel half -> s, z and codes ----
+      constexpr int NS = (TENSOR == 0) ? 4 : 8;
+      uint32_t wd[NS][2];
+      const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16) + 128u * (uint32_t)(j & 3);
+      float2* sstat = reinterpret_cast<float2*>(sm + kBkOffStat) + 256 * (2 * team + ((j >> 1) & 1));
+      const ScaleZero q = row_codes<GS, TENSOR>(trow, hf, m, sclip, sstat, wd, qbar);
+      // the accumulator is read: release it to the team's issuer
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(accfree + (j & 3));
+      const bool pid_ok = pid_raw >= 0 && pid_raw < a.num_pages;
+      if (tile_live && !pid_ok && m16 == 0 && hf == 0) flag_error(a.err, KV_DEVERR_PAGE_ID);
+      const bool write = tile_live && pid_ok;
+      uint8_t* tb = a.hist + (size_t)(pid_ok ? pid_raw : 0) * a.page_bytes + (size_t)g * a.head_block +
+                    (size_t)((tile * kTile) % a.P / kTile) * a.tile_bytes;
+      const unsigned okmask = __ballot_sync(0xffffffffu, row_ok && write);
 
-    if constexpr (TENSOR == 0) {
-      // K: code (token m16, channel c) -> slot 4*(m16%8) + (k%8)/2, word c/32,
-      // bit 16*(k%2) + 2*(2*((c/16)%2) + m16/8 + 4*(k/8)), k = c%16; this half
-      // holds words 2 hf and 2 hf + 1 of every slot
-      const int mh = m16 >> 3;
-      uint32_t out[2][2];
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj)
-#pragma unroll
-        for (int w = 0; w < 2; ++w) {
-          const uint32_t lo_w = wd[jj][w] << (2 * mh), hi_w = wd[2 + jj][w] << (2 * mh);
-          const uint32_t recv = __shfl_xor_sync(0xffffffffu, mh ? lo_w : hi_w, 8);
-          out[jj][w] = (mh ? hi_w : lo_w) | recv;
-        }
-      const bool me = (okmask >> lane) & 1u, other = (okmask >> (lane ^ 8)) & 1u;
-      const uint32_t pat_me = mh ? 0xCCCCCCCCu : 0x33333333u;
-      const uint32_t mask = (me ? pat_me : 0u) | (other ? ~pat_me : 0u);
-      if (write) {
-#pragma unroll
+      if constexpr (TENSOR == 0) {
+        // K: code (token m16, channel c) -> slot 4*(m16%8) + (k%8)/2, word c/32,
+        // bit 16*(k%2) + 2*(2*((c/16)%2) + m16/8 + 4*(k/8)), k = c%16; this half
+        // holds words 2 hf and 2 hf + 1 of every slot
+        const int mh = m16 >> 3;
+        uint32_t out[2][2];
+  #pragma unroll
         for (int jj = 0; jj < 2; ++jj)
-          store_merge2(tb + 16 * (4 * (m16 & 7) + 2 * mh + jj) + 8 * hf, out[jj], mask);
-      }
-      if (write && row_ok && (GS == 64 || hf == 0)) {
-        __half2* rec = reinterpret_cast<__half2*>(tb + 1024 + (2 * (m16 & 7) + mh) * 4 * NG);
-        rec[GS == 64 ? hf : 0] = __halves2half2(q.sh, q.zh);
-      }
-    } else {
-      // V: code (channel c, token m16) -> slot 4*(c%8) + (m16%8)/2, word c/32,
-      // bit 16*(m16%2) + 2*(2*((c/16)%2) + (c%16)/8 + 4*(m16/8))
-      const int ek = m16 & 1, kh = m16 >> 3;
-      const int sh = 16 * ek + 8 * kh;
-      uint32_t r1[4][2];   // partner lane ^ 8: keep slots with m8 / 4 == kh
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int w = 0; w < 2; ++w) {
-          const uint32_t a0 = wd[i][w] << sh, a1 = wd[4 + i][w] << sh;
-          const uint32_t recv = __shfl_xor_sync(0xffffffffu, kh ? a0 : a1, 8);
-          r1[i][w] = (kh ? a1 : a0) | recv;
+  #pragma unroll
+          for (int w = 0; w < 2; ++w) {
+            const uint32_t lo_w = wd[jj][w] << (2 * mh), hi_w = wd[2 + jj][w] << (2 * mh);
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, mh ? lo_w : hi_w, 8);
+            out[jj][w] = (mh ? hi_w : lo_w) | recv;
+          }
+        const bool me = (okmask >> lane) & 1u, other = (okmask >> (lane ^ 8)) & 1u;
+        const uint32_t pat_me = mh ? 0xCCCCCCCCu : 0x33333333u;
+        const uint32_t mask = (me ? pat_me : 0u) | (other ? ~pat_me : 0u);
+        if (write) {
+  #pragma unroll
+          for (int jj = 0; jj < 2; ++jj)
+            store_merge2(tb + 16 * (4 * (m16 & 7) + 2 * mh + jj) + 8 * hf, out[jj], mask);
         }
-      uint32_t out[2][2];  // partner lane ^ 1: keep m8 % 4 / 2 == ek
-#pragma unroll
-      for (int ii = 0; ii < 2; ++ii)
-#pragma unroll
-        for (int w = 0; w < 2; ++w) {
-          const uint32_t a0 = r1[ii][w], a1 = r1[2 + ii][w];
-          const uint32_t recv = __shfl_xor_sync(0xffffffffu, ek ? a0 : a1, 1);
-          out[ii][w] = (ek ? a1 : a0) | recv;
+        if (write && row_ok && (GS == 64 || hf == 0)) {
+          __half2* rec = reinterpret_cast<__half2*>(tb + 1024 + (2 * (m16 & 7) + mh) * 4 * NG);
+          rec[GS == 64 ? hf : 0] = __halves2half2(q.sh, q.zh);
         }
-      // bits of the four tokens sharing these words: (ek', kh') -> 0x00FF / 0xFF00 in half ek'
-      const int base = lane & ~9;
-      uint32_t mask = 0u;
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int e2 = t & 1, k2 = t >> 1;
-        if ((okmask >> (base | e2 | (k2 << 3))) & 1u) mask |= (k2 ? 0xFF00u : 0x00FFu) << (16 * e2);
-      }
-      const int jk = (m16 & 7) >> 1;
-      if (write) {
-#pragma unroll
+      } else {
+        // V: code (channel c, token m16) -> slot 4*(c%8) + (m16%8)/2, word c/32,
+        // bit 16*(m16%2) + 2*(2*((c/16)%2) + (c%16)/8 + 4*(m16/8))
+        const int ek = m16 & 1, kh = m16 >> 3;
+        const int sh = 16 * ek + 8 * kh;
+        uint32_t r1[4][2];   // partner lane ^ 8: keep slots with m8 / 4 == kh
+  #pragma unroll
+        for (int i = 0; i < 4; ++i)
+  #pragma unroll
+          for (int w = 0; w < 2; ++w) {
+            const uint32_t a0 = wd[i][w] << sh, a1 = wd[4 + i][w] << sh;
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, kh ? a0 : a1, 8);
+            r1[i][w] = (kh ? a1 : a0) | recv;
+          }
+        uint32_t out[2][2];  // partner lane ^ 1: keep m8 % 4 / 2 == ek
+  #pragma unroll
         for (int ii = 0; ii < 2; ++ii)
-          store_merge2(tb + 512 + 16 * (4 * (4 * kh + 2 * ek + ii) + jk) + 8 * hf, out[ii], mask);
-      }
-      if (write && row_ok && (GS == 64 || hf == 0)) {
-        __half2* rec = reinterpret_cast<__half2*>(tb + 1024 + 64 * NG + (2 * (m16 & 7) + kh) * 4 * NG);
-        rec[GS == 64 ? hf : 0] = __halves2half2(q.sh, q.zh);
+  #pragma unroll
+          for (int w = 0; w < 2; ++w) {
+            const uint32_t a0 = r1[ii][w], a1 = r1[2 + ii][w];
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, ek ? a0 : a1, 1);
+            out[ii][w] = (ek ? a1 : a0) | recv;
+          }
+        // bits of the four tokens sharing these words: (ek', kh') -> 0x00FF / 0xFF00 in half ek'
+        const int base = lane & ~9;
+        uint32_t mask = 0u;
+  #pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int e2 = t & 1, k2 = t >> 1;
+          if ((okmask >> (base | e2 | (k2 << 3))) & 1u) mask |= (k2 ? 0xFF00u : 0x00FFu) << (16 * e2);
+        }
+        const int jk = (m16 & 7) >> 1;
+        if (write) {
+  #pragma unroll
+          for (int ii = 0; ii < 2; ++ii)
+            store_merge2(tb + 512 + 16 * (4 * (4 * kh + 2 * ek + ii) + jk) + 8 * hf, out[ii], mask);
+        }
+        if (write && row_ok && (GS == 64 || hf == 0)) {
+          __half2* rec = reinterpret_cast<__half2*>(tb + 1024 + 64 * NG + (2 * (m16 & 7) + kh) * 4 * NG);
+          rec[GS == 64 ? hf : 0] = __halves2half2(q.sh, q.zh);
+        }
       }
     }
-    tc_fence_before();
-    team_sync(tbar);   // accumulator j % 4 is free for product j + 4; record j + 4 is published
-    if (info[8 * ((j + 4) & 7) + kRecState] == kChunkCopy) copy_chunk(j + 4);
   }
 
-  // wait (bounded) for what is still in flight after an early exit: the
-  // leader for products issued but not waited for, the loader for TMA loads
-  // of chunks the team did not reach (a load a product consumed has completed)
-  if (leader) {
-    if (!r_ok) mbar_wait(bars + 0, 0, kTcPolls);
-    for (int J = jw + 2; J <= jm; J += 2) mbar_wait(mdone + (J & 3), (uint32_t)(J >> 2) & 1u, kTcPolls);
+  // every role is done; after an early exit, wait (bounded) for what is still
+  // in flight: the last TMA load and the last product of each buffer (the
+  // phases of a barrier complete in order)
+  __syncthreads();
+  if (tid == 0) {
+    mbar_wait(bars + 0, 0, kTcPolls);
+    for (int b = 0; b < 4; ++b) {
+      if (last_load[b] >= 0) mbar_wait(xfull + b, par(last_load[b], 2), kTcPolls);
+      if (last_prod[b] >= 0) mbar_wait(mdone + b, par(last_prod[b], 2), kTcPolls);
+    }
   }
-  if (loader)
-    for (int J = jw + 2; J <= jl; J += 2)
-      if (info[8 * (J & 7) + kRecState] == kChunkTma) mbar_wait(xfull + (J & 3), (uint32_t)(J >> 2) & 1u, kTcPolls);
   asm volatile("cp.async.wait_group 0;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tc_dealloc(tmem, kBkCols);
   if (tid == 0)
-    for (int i = 0; i < 9; ++i) mbar_inval(bars + i);
+    for (int i = 0; i < kBkBars; ++i) mbar_inval(bars + i);
 }
 
 template <int GS, int TENSOR>
