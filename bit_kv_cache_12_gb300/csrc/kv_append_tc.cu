@@ -319,6 +319,9 @@ __device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
   return r;
 }
+// the exact code of one value (the rare fix-up path; kept out of line)
+__device__ __noinline__ uint32_t quant_code_exact(float y, ScaleZero q) { return quant_code(y, q); }
+
 // Three-input minimum / maximum (one instruction on sm_100 and later); exact,
 // so reductions built from them give the same value in any order (up to the
 // sign of a zero, which the quantizer canonicalises).
@@ -420,55 +423,66 @@ __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, con
     const int kk = i & 15, s1 = (i >> 4) & 1;
     return (TENSOR == 0) ? 16 * (kk & 1) + 2 * (2 * s1 + 4 * (kk >> 3)) : 2 * (2 * s1 + (kk >> 3));
   };
-  auto pack = [&](int i, uint32_t c) { word_of(i) |= c << pos_of(i); };
   // code = rint(clamp(fl(fl(y - z) / s), 0, 3)).  The clamped quotient is
   // 3 u with u = sat(fl(y - z) * fl(fl(1/s) / 3)) (the saturating multiply
   // clamps to [0, 1] for free; 3 u lies within 1e-6 of fl(fl(y - z) / s)
   // clamped); 3 u + 1.5 * 2^23, rounded once, holds rint(3 u) in its low
-  // mantissa bits (round to nearest even), unless some quotient lies within
+  // mantissa bits (round to nearest even), unless the quotient lies within
   // 2^-18 of a half-integer, where the IEEE division decides (quant_code).
   // Out of [0, 3] the clamp leaves an integer, so only ties inside the range
-  // can set the fix-up.
+  // can need the exact path.
   clear();
-  float emax = 0.0f;
   const float rs3 = __fmul_rn(q.rs, 0.3333333432674408f);   // the quotient / 3, saturated to [0, 1]
+  const uint64_t zz = f2pack(q.z, q.z), three = f2pack(3.0f, 3.0f), mag = f2pack(12582912.0f, 12582912.0f);
+  // channels i and i + 1 as one pair: rr = 3 u + 1.5 * 2^23 rounded once
+  // (its bits are 0x4B400000 + code) and e = 3 u - code
+  auto fast_pair = [&](float y0, float y1, float& r0, float& r1, float& e0, float& e1) {
+    float d0, d1, u0, u1;
+    f2unpack(f2sub(f2pack(y0, y1), zz), d0, d1);
+    asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(u0) : "f"(d0), "f"(rs3));
+    asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(u1) : "f"(d1), "f"(rs3));
+    const uint64_t up = f2pack(u0, u1);
+    const uint64_t rr = f2fma(up, three, mag);
+    f2unpack(rr, r0, r1);
+    f2unpack(f2fma(up, three, f2sub(mag, rr)), e0, e1);   // the code is exactly 1.5 * 2^23 - rr, negated
+  };
+  constexpr float kTieBand = 0.499996185302734375f;   // 1/2 - 2^-18
+  float emx[2];   // largest distance to the code per 32-channel block
 #pragma unroll
   for (int cb = 0; cb < 2; ++cb) {
     float v[32];
     rotated32(cb, v);
-    const uint64_t zz = f2pack(q.z, q.z), three = f2pack(3.0f, 3.0f), mag = f2pack(12582912.0f, 12582912.0f);
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) {   // channels i and i + 1 as one pair
-      float d0, d1, u0, u1, r0, r1, e0, e1;
-      f2unpack(f2sub(f2pack(v[i], v[i + 1]), zz), d0, d1);
-      asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(u0) : "f"(d0), "f"(rs3));
-      asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(u1) : "f"(d1), "f"(rs3));
-      const uint64_t up = f2pack(u0, u1);
-      // rr = 3 u + 1.5 * 2^23 rounded once: its bits are 0x4B400000 + code
-      const uint64_t rr = f2fma(up, three, mag);
-      f2unpack(rr, r0, r1);
+    for (int i = 0; i < 32; i += 2) {
+      float r0, r1, e0, e1;
+      fast_pair(v[i], v[i + 1], r0, r1, e0, e1);
       // one integer multiply-add places a code (the constant offsets of a
       // word fold into one; codes do not overlap, so the sum is the OR)
       const int pos0 = pos_of(32 * cb + i), pos1 = pos_of(32 * cb + i + 1);
       word_of(32 * cb + i) += __float_as_uint(r0) * (1u << pos0) - (0x4B400000u << pos0);
       word_of(32 * cb + i + 1) += __float_as_uint(r1) * (1u << pos1) - (0x4B400000u << pos1);
-      // distance to the code: 3 u - code, the code being exactly 1.5 * 2^23 - rr negated
-      f2unpack(f2fma(up, three, f2sub(mag, rr)), e0, e1);
       v[i] = fabsf(e0);
       v[i + 1] = fabsf(e1);
     }
-    emax = max_of32(emax, v);
+    emx[cb] = max_of32(0.0f, v);
   }
-  // warp-uniform: the re-read is a warp-collective tensor-memory load, and a
-  // lane without a near tie recomputes its own codes unchanged
-  if (__any_sync(0xffffffffu, emax >= 0.499996185302734375f)) {
-    clear();
+  // a block with a near tie in some lane is read again (a warp-collective
+  // tensor-memory load); only the values within the band get the exact code,
+  // patched into their 2-bit fields
 #pragma unroll
-    for (int cb = 0; cb < 2; ++cb) {
-      float v[32];
-      rotated32(cb, v);
+  for (int cb = 0; cb < 2; ++cb) {
+    if (!__any_sync(0xffffffffu, emx[cb] >= kTieBand)) continue;
+    float v[32];
+    rotated32(cb, v);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) pack(32 * cb + i, quant_code(v[i], q));
+    for (int i = 0; i < 32; ++i) {
+      float r0, r1, e0, e1;
+      if ((i & 1) == 0) fast_pair(v[i], v[i + 1], r0, r1, e0, e1);
+      const float r = (i & 1) ? r1 : r0, e = (i & 1) ? e1 : e0;
+      if (fabsf(e) >= kTieBand) {
+        const uint32_t fast = __float_as_uint(r) - 0x4B400000u;
+        word_of(32 * cb + i) ^= ((fast ^ quant_code_exact(v[i], q)) & 3u) << pos_of(32 * cb + i);
+      }
     }
   }
 
