@@ -524,6 +524,22 @@ __device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ uint32_t par(int j, int shift) { return (uint32_t)(j >> shift) & 1u; }
+// mbar_wait for the serving warps: each poll may suspend the thread until the
+// phase completes or about 1 us passes, so that a waiting server takes no
+// issue slots from the epilogue warps
+__device__ __forceinline__ bool mbar_wait_idle(uint64_t* bar, uint32_t parity, int limit) {
+  const uint32_t a = smem_u32(bar);
+  for (int it = 0; it < limit; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(a), "r"(parity), "r"(1000u)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
 // whether `p` holds in all 64 threads of named barrier `id` (both warps of a
 // lane quarter), so that the two take the same branch before the barrier
 // they share in the epilogue of group 128
@@ -619,7 +635,7 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
         // which came before product J - 4
         if (J >= 4) {
           bool ok = *abort_flag == 0;
-          if (ok && lane == 0) ok = mbar_wait(mdone + (J & 3), par(J - 4, 2), kTcPolls);
+          if (ok && lane == 0) ok = mbar_wait_idle(mdone + (J & 3), par(J - 4, 2), kTcPolls);
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) {
             if (lane == 0) fail();
@@ -662,18 +678,18 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
         }
       }
     } else if (lane == 0) {
-      bool ok = mbar_wait(bars + 0, 0, kTcPolls);   // R is needed before the first product
+      bool ok = mbar_wait_idle(bars + 0, 0, kTcPolls);   // R is needed before the first product
       if (!ok) fail();
       for (int J = team; ok; J += 2) {
-        ok = *abort_flag == 0 && mbar_wait(recready + (J & 7), par(J, 3), kTcPolls);
+        ok = *abort_flag == 0 && mbar_wait_idle(recready + (J & 7), par(J, 3), kTcPolls);
         if (!ok) {
           fail();
           break;
         }
         if (info[8 * (J & 7) + kRecState] == kChunkNone) break;
         // x in, and accumulator J % 4 read by the team for chunk J - 4
-        ok = mbar_wait(xfull + (J & 3), par(J, 2), kTcPolls) &&
-             (J < 4 || mbar_wait(accfree + (J & 3), par(J - 4, 2), kTcPolls));
+        ok = mbar_wait_idle(xfull + (J & 3), par(J, 2), kTcPolls) &&
+             (J < 4 || mbar_wait_idle(accfree + (J & 3), par(J - 4, 2), kTcPolls));
         if (!ok) {
           fail();
           break;
@@ -833,7 +849,9 @@ template <int GS, int TENSOR>
 __global__ void __launch_bounds__(kBkThreads, 1)
     append_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap xmap) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  // 1024-byte aligned (the swizzled operands), by an offset into the shared
+  // array so that the compiler keeps the accesses in the shared space
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   tc_body<GS, TENSOR>(a, &xmap, sm);
 }
 
