@@ -578,7 +578,7 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
     mbar_init(bars + 0, 1);
     for (int b = 0; b < 4; ++b) {
       mbar_init(xfull + b, 1);
-      mbar_init(mdone + b, 1);
+      mbar_init(mdone + b, 2);   // the product's commit and the issuer's arrival
       mbar_init(accfree + b, 8);
       last_load[b] = -1;
       last_prod[b] = -1;
@@ -686,7 +686,11 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
           fail();
           break;
         }
-        if (info[8 * (J & 7) + kRecState] == kChunkNone) break;
+        if (info[8 * (J & 7) + kRecState] == kChunkNone) {   // the team's end: its warps read the record
+          mbar_arrive1(mdone + (J & 3));
+          mbar_arrive1(mdone + (J & 3));
+          break;
+        }
         // x in, and accumulator J % 4 read by the team for chunk J - 4
         ok = mbar_wait_idle(xfull + (J & 3), par(J, 2), kTcPolls) &&
              (J < 4 || mbar_wait_idle(accfree + (J & 3), par(J - 4, 2), kTcPolls));
@@ -695,6 +699,9 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
           break;
         }
         issue_rotation(tmem + 128u * (uint32_t)(J & 3), sA0 + (uint32_t)(J & 3) * kABytes, sB, mdone + (J & 3));
+        // the second arrival (a release after this thread acquired the record):
+        // a warp that sees product J complete also sees record J
+        mbar_arrive1(mdone + (J & 3));
         last_prod[J & 3] = J;
       }
     }
@@ -709,20 +716,18 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
     const int m = 32 * quarter + lane;         // this thread's token row of a chunk
     const int m16 = m & 15;
     for (int j = team;; j += 2) {
-      // the chunk's record, then its product (at group 128 the two warps of a
-      // quarter decide together: they meet at a barrier in the epilogue)
-      bool ok = __all_sync(0xffffffffu, *abort_flag == 0 && mbar_wait(recready + (j & 7), par(j, 3), kTcPolls));
+      // product j complete, which also publishes record j (the issuer arrives
+      // once it has read the record; at the team's end it arrives twice with
+      // no product); at group 128 the two warps of a quarter decide together:
+      // they meet at a barrier in the epilogue
+      bool ok = __all_sync(0xffffffffu, *abort_flag == 0 && mbar_wait(mdone + (j & 3), par(j, 2), kTcPolls));
       if (GS == 128) ok = pair_and(qbar, ok);
-      const int* r = info + 8 * (j & 7);
-      if (ok && r[kRecState] == kChunkNone) break;
-      if (ok) {
-        ok = __all_sync(0xffffffffu, mbar_wait(mdone + (j & 3), par(j, 2), kTcPolls));
-        if (GS == 128) ok = pair_and(qbar, ok);
-      }
       if (!ok) {
         if (lane == 0) fail();
         break;
       }
+      const int* r = info + 8 * (j & 7);
+      if (r[kRecState] == kChunkNone) break;
       tc_fence_after();
       Chunk k;
       k.b = r[kRecB];
@@ -826,11 +831,12 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
     }
   }
 
-  // every role is done; after an early exit, wait (bounded) for what is still
-  // in flight: the last TMA load and the last product of each buffer (the
-  // phases of a barrier complete in order)
+  // every role is done.  On the normal path every load fed a product and
+  // every product was read by its team; after an early exit, wait (bounded)
+  // for what may still be in flight: the last TMA load and the last product
+  // of each buffer (the phases of a barrier complete in order)
   __syncthreads();
-  if (tid == 0) {
+  if (tid == 0 && *abort_flag != 0) {
     mbar_wait(bars + 0, 0, kTcPolls);
     for (int b = 0; b < 4; ++b) {
       if (last_load[b] >= 0) mbar_wait(xfull + b, par(last_load[b], 2), kTcPolls);
