@@ -195,6 +195,8 @@ struct TcArgs {
   const float* clip;          // layer base [2][Hkv][128]
   int* err;
   int tasks_per_cta;
+  int wait_polls;             // bound of the bulk append's waits between its warps
+  int stall_first_load;       // test hook: CTA (0, 0) never starts the x load of its first chunk
 };
 
 // Chunk of one task: 128 consecutive history positions [P0, P0 + 128) of
@@ -635,7 +637,7 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
         // which came before product J - 4
         if (J >= 4) {
           bool ok = *abort_flag == 0;
-          if (ok && lane == 0) ok = mbar_wait_idle(mdone + (J & 3), par(J - 4, 2), kTcPolls);
+          if (ok && lane == 0) ok = mbar_wait_idle(mdone + (J & 3), par(J - 4, 2), a.wait_polls);
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) {
             if (lane == 0) fail();
@@ -647,6 +649,8 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
         Chunk k = tc.chunk();
         const int r0 = k.c0 + (k.P0 - k.h0);
         const bool tma = have && r0 + kChunk <= row_lim;
+        // test hook: this chunk's x is never loaded, so its issuer's bounded wait runs out
+        const bool withhold = have && a.stall_first_load && J == 0 && blockIdx.x == 0 && blockIdx.y == 0;
         if (lane == 0) {
           r[kRecB] = k.b;
           r[kRecC0] = k.c0;
@@ -655,7 +659,7 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
           r[kRecLast] = k.last;
           r[kRecP0] = k.P0;
           r[kRecState] = !have ? kChunkNone : tma ? kChunkTma : kChunkCopy;
-          if (tma) {
+          if (tma && !withhold) {
             const uint32_t dst = sA0 + (uint32_t)(J & 3) * kABytes;
             mbar_expect_tx(xfull + (J & 3), kABytes);
             tma_load_x(dst, xmap, 0, g, r0, xfull + (J & 3));
@@ -665,7 +669,7 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
           mbar_arrive1(recready + (J & 7));   // release: the record is visible to its waiters
         }
         if (!have) break;
-        if (!tma) {   // the warp's 32 lanes copy the 128 half rows x 2 of the chunk
+        if (!tma && !withhold) {   // the warp's 32 lanes copy the 128 half rows x 2 of the chunk
           for (int i = 0; i < 8; ++i) load_chunk(a, X, g, k, sA0 + (uint32_t)(J & 3) * kABytes, lane + 32 * i);
           asm volatile("cp.async.wait_group 0;" ::: "memory");
           fence_async_smem();
@@ -678,10 +682,10 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
         }
       }
     } else if (lane == 0) {
-      bool ok = mbar_wait_idle(bars + 0, 0, kTcPolls);   // R is needed before the first product
+      bool ok = mbar_wait_idle(bars + 0, 0, a.wait_polls);   // R is needed before the first product
       if (!ok) fail();
       for (int J = team; ok; J += 2) {
-        ok = *abort_flag == 0 && mbar_wait_idle(recready + (J & 7), par(J, 3), kTcPolls);
+        ok = *abort_flag == 0 && mbar_wait_idle(recready + (J & 7), par(J, 3), a.wait_polls);
         if (!ok) {
           fail();
           break;
@@ -692,8 +696,8 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
           break;
         }
         // x in, and accumulator J % 4 read by the team for chunk J - 4
-        ok = mbar_wait_idle(xfull + (J & 3), par(J, 2), kTcPolls) &&
-             (J < 4 || mbar_wait_idle(accfree + (J & 3), par(J - 4, 2), kTcPolls));
+        ok = mbar_wait_idle(xfull + (J & 3), par(J, 2), a.wait_polls) &&
+             (J < 4 || mbar_wait_idle(accfree + (J & 3), par(J - 4, 2), a.wait_polls));
         if (!ok) {
           fail();
           break;
@@ -720,7 +724,7 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
       // once it has read the record; at the team's end it arrives twice with
       // no product); at group 128 the two warps of a quarter decide together:
       // they meet at a barrier in the epilogue
-      bool ok = __all_sync(0xffffffffu, *abort_flag == 0 && mbar_wait(mdone + (j & 3), par(j, 2), kTcPolls));
+      bool ok = __all_sync(0xffffffffu, *abort_flag == 0 && mbar_wait(mdone + (j & 3), par(j, 2), a.wait_polls));
       if (GS == 128) ok = pair_and(qbar, ok);
       if (!ok) {
         if (lane == 0) fail();
@@ -1162,6 +1166,8 @@ cudaError_t launch_append_tc(const Pool& p, int layer, int n_seqs, const void* k
   a.Hkv = H;
   a.num_pages = p.cfg.num_pages;
   a.map_rows = (long long)n_seqs * max_tokens;
+  a.wait_polls = p.test_wait_polls > 0 ? p.test_wait_polls : kTcPolls;
+  a.stall_first_load = p.test_stall_first_copy;
   a.rfrag = p.rfrag + (size_t)layer * H * kFragBlocks * rfrag_per_head();
   a.clip = p.clip + (size_t)layer * 2 * H * 128;
   a.err = p.err;

@@ -46,8 +46,9 @@ struct Pool {
   int* err = nullptr;               // device error word
 
   // test hooks (kv_debug_stall_first_copy): 0 in normal use
-  int test_stall_first_copy = 0;    // decode: the first tile copy of split 0 is never issued
-  int test_wait_polls = 0;          // decode: polls of a bounded wait (0 = the default)
+  int test_stall_first_copy = 0;    // decode: the first tile copy of split 0 is never issued;
+                                    // bulk append: the first x load of CTA (0, 0) is never started
+  int test_wait_polls = 0;          // decode and bulk append: polls of a bounded wait (0 = the default)
 };
 
 // Rotation operands per (layer, KV head), 4096 uint4 (64 KB) each:

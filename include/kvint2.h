@@ -359,11 +359,16 @@ kv_status_t kv_decode_attention_noalloc(kv_pool_t* pool, int32_t layer, int32_t 
  * enable != 0, later decode calls of this pool arm the first ring stage of
  * the first history split for a tile copy that is never issued, so that the
  * warp's bounded wait runs out: the call sets KV_DEVERR_TIMEOUT, waits
- * (bounded) for the copies it did issue, skips that split and returns.  No
- * copy is left in flight, nothing faults and nothing hangs.  max_polls > 0
- * replaces the default poll limit of those waits (about a second) for the
- * pool's decode calls; 0 restores it.  enable = 0 restores normal decodes.
- * Not for production use. */
+ * (bounded) for the copies it did issue, skips that split and returns; and
+ * later kv_append_quantize calls never start the x load of the first chunk
+ * of the first CTA, so that the wait for it runs out: the call sets
+ * KV_DEVERR_TIMEOUT, every warp of that CTA leaves its loop, the CTA waits
+ * (bounded) for the loads and products it did start and returns (the
+ * history it was to write is left incomplete).  No copy is left in flight,
+ * nothing faults and nothing hangs.  max_polls > 0 replaces the default poll
+ * limit of those waits (about a second) for the pool's decode and bulk
+ * append calls; 0 restores it.  enable = 0 restores normal calls.  Not for
+ * production use. */
 kv_status_t kv_debug_stall_first_copy(kv_pool_t* pool, int32_t enable, int32_t max_polls);
 
 #ifdef __cplusplus
