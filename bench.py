@@ -731,22 +731,10 @@ def run_append(env, steps, warmup):
     """64 sequences x 8 KV heads x 4096 tokens evicted in one kv_append_quantize."""
     from bit_kv_cache_12_gb300 import native, workloads
     torch, dev = env.torch, env.dev
-    n_seqs, Hkv, T, P, GS = 64, 8, 4096, 16, 64
-    seed = 3
-    rng = np.random.default_rng(seed)
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(seed)
-
-    def student_t4(n):                         # N(0,1) / sqrt(chi2_4 / 4)
-        z = torch.randn(n, Hkv, 128, generator=gen, device=dev)
-        chi = (torch.randn(4, n, Hkv, 128, generator=gen, device=dev) ** 2).sum(0) / 4.0
-        return (z / chi.sqrt()).to(torch.bfloat16)
-    k, v = student_t4(n_seqs * T), student_t4(n_seqs * T)
-    Rk, Rv = workloads.haar_stack(rng, Hkv), workloads.haar_stack(rng, Hkv)
-    ck, cv = workloads.clip_from(k, Rk, 0.9, torch), workloads.clip_from(v, Rv, 0.9, torch)
-    pages_per = T // P
-    num_pages = n_seqs * pages_per
-    pt_np = rng.permutation(num_pages).astype(np.int32).reshape(n_seqs, pages_per)
+    w = workloads.append_workload(torch, dev)
+    n_seqs, Hkv, T, P, GS = w["n_seqs"], w["Hkv"], w["T"], w["page_size"], w["group_size"]
+    k, v, Rk, Rv, ck, cv = w["k"], w["v"], w["Rk"], w["Rv"], w["clip_k"], w["clip_v"]
+    pages_per, num_pages, pt_np = w["pages_per_seq"], w["num_pages"], w["page_table"]
     pool = native.KVPool(native.KV_POOL_INT2_3TIER, 1, Hkv, Hkv, P, num_pages, n_seqs, group_size=GS)
     native.kv_pool_set_rotation(pool.handle, 0, torch.as_tensor(Rk).to(dev), torch.as_tensor(Rv).to(dev),
                                 torch.as_tensor(ck).to(dev), torch.as_tensor(cv).to(dev))

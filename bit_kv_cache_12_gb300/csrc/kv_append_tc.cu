@@ -691,6 +691,13 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
           break;
         }
         if (info[8 * (J & 7) + kRecState] == kChunkNone) {   // the team's end: its warps read the record
+          // first every warp has taken product J - 4 from this barrier (and
+          // released its accumulator): completing the next phase earlier would
+          // hide product J - 4's phase from a warp still waiting for it
+          if (J >= 4 && !mbar_wait_idle(accfree + (J & 3), par(J - 4, 2), a.wait_polls)) {
+            fail();
+            break;
+          }
           mbar_arrive1(mdone + (J & 3));
           mbar_arrive1(mdone + (J & 3));
           break;

@@ -65,6 +65,30 @@ def case_from_synth(wl, torch, dev, l2_note=""):
     return c
 
 
+def append_workload(torch, dev, seed=3, n_seqs=64, Hkv=8, T=4096, P=16, GS=64, clip_ratio=0.9):
+    """The bulk-append workload: n_seqs sequences x Hkv KV heads x T tokens of
+    Student-t(4) K and V rows (bf16, on the device), per-head Haar R_k and R_v,
+    clips at clip_ratio x the rotated per-channel absmax, a shuffled page
+    table.  Returns a dict of the device inputs and their host copies."""
+    rng = np.random.default_rng(seed)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+
+    def student_t4(n):                         # N(0,1) / sqrt(chi2_4 / 4)
+        z = torch.randn(n, Hkv, 128, generator=gen, device=dev)
+        chi = (torch.randn(4, n, Hkv, 128, generator=gen, device=dev) ** 2).sum(0) / 4.0
+        return (z / chi.sqrt()).to(torch.bfloat16)
+    k, v = student_t4(n_seqs * T), student_t4(n_seqs * T)
+    Rk, Rv = haar_stack(rng, Hkv), haar_stack(rng, Hkv)
+    ck, cv = clip_from(k, Rk, clip_ratio, torch), clip_from(v, Rv, clip_ratio, torch)
+    pages_per = T // P
+    num_pages = n_seqs * pages_per
+    pt_np = rng.permutation(num_pages).astype(np.int32).reshape(n_seqs, pages_per)
+    return {"k": k, "v": v, "Rk": Rk, "Rv": Rv, "clip_k": ck, "clip_v": cv, "page_table": pt_np,
+            "n_seqs": n_seqs, "Hkv": Hkv, "T": T, "page_size": P, "group_size": GS,
+            "num_pages": num_pages, "pages_per_seq": pages_per}
+
+
 def haar_stack(rng, n):
     from bit_kv_cache_12_gb300 import synth
     return np.stack([synth.haar_orthogonal(rng) for _ in range(n)]).astype(np.float32)

@@ -1,0 +1,41 @@
+"""The bulk append repeated on one large group-128 input: no device error and
+the same stored bytes every time.
+
+The input (the batched workload generator: 64 sequences of 18,800 - 19,400
+history tokens, 2 KV heads, page 32, group 128) gives every CTA about 120
+chunks and ragged ends, so each CTA's two teams reach the end of their chunks
+at different times while some of their warps are still on the exact tie
+fix-up.  A team's end is signalled through the same product barrier as its
+chunks; before that signal every warp must have taken the previous product
+from that barrier, else a slow warp waits for a phase the barrier has already
+passed (its bounded wait then reports KV_DEVERR_TIMEOUT).  Repeating the call
+makes such a timing-dependent hand-over show; the stored bytes must not
+depend on timing.  The yunpan.plus OSCAR write-up, section
+"2. 在线量化与反量化", describes the step (rotate, clip, quantize, pack)."""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from bit_kv_cache_12_gb300 import native, workloads
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+def test_append_repeated_is_error_free_and_deterministic():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    c = workloads.generate(torch, torch.device("cuda"), "repeat_g8_p32", 130, 64, 16, 2, 32,
+                           ctx_range=(18800, 19400), outlier_channels=4)
+    ref = None
+    for _ in range(6):
+        pool = gu.fill_pool_from_case(c)
+        assert pool.error() == 0
+        pages = pool.hist_view(0).cpu().numpy()
+        pool.close()
+        if ref is None:
+            ref = pages.copy()
+        else:
+            assert np.array_equal(pages, ref)
