@@ -10,7 +10,8 @@ chunks; before that signal every warp must have taken the previous product
 from that barrier, else a slow warp waits for a phase the barrier has already
 passed (its bounded wait then reports KV_DEVERR_TIMEOUT).  Repeating the call
 makes such a timing-dependent hand-over show; the stored bytes must not
-depend on timing.  The yunpan.plus OSCAR write-up, section
+depend on timing, and sampled chunks (group 128) must agree with the oracle's
+fp64 rotation and scalar quantizer as in the full-size append test.  The yunpan.plus OSCAR write-up, section
 "2. 在线量化与反量化", describes the step (rotate, clip, quantize, pack)."""
 
 import numpy as np
@@ -18,8 +19,11 @@ import pytest
 
 torch = pytest.importorskip("torch")
 
+import types
+
 from bit_kv_cache_12_gb300 import native, workloads
 from tests import gpu_util as gu
+from tests.test_gpu_parity import _compare_codes
 
 pytestmark = pytest.mark.gpu
 
@@ -39,3 +43,16 @@ def test_append_repeated_is_error_free_and_deterministic():
             ref = pages.copy()
         else:
             assert np.array_equal(pages, ref)
+    aw = types.SimpleNamespace(group_size=c.GS, Hkv=c.Hkv, page_table=c.page_table, page_size=c.P,
+                               Rk=c.Rk, Rv=c.Rv, clip_k=c.clip_k, clip_v=c.clip_v)
+    cu = np.zeros(c.B + 1, np.int64)
+    cu[1:] = np.cumsum(c.hist_len)
+    for b in (0, 31, 63):
+        n = int(c.hist_len[b])
+        for p0 in (0, (n // 2) // 16 * 16, max(0, n - 128) // 16 * 16):
+            m = min(128, n - p0)
+            rows = slice(int(cu[b]) + p0, int(cu[b]) + p0 + m)
+            kb = c.hist_k[rows].cpu().view(torch.int16).numpy().view(np.uint16)
+            vb = c.hist_v[rows].cpu().view(torch.int16).numpy().view(np.uint16)
+            bad, tot = _compare_codes(ref, kb, vb, aw, b, p0, m)
+            assert bad <= max(4, 1e-4 * tot), (b, p0, bad, tot)
