@@ -869,7 +869,11 @@ __global__ void __launch_bounds__(kBkThreads, 1)
   // 1024-byte aligned (the swizzled operands), by an offset into the shared
   // array so that the compiler keeps the accesses in the shared space
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  // K: the V launch may start as this grid's CTAs leave; V: this grid ends
+  // only after the K grid (a later kernel of the stream waits for both)
+  if (TENSOR == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   tc_body<GS, TENSOR>(a, &xmap, sm);
+  if (TENSOR == 1 && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -1211,8 +1215,20 @@ cudaError_t launch_append_tc(const Pool& p, int layer, int n_seqs, const void* k
       if (e != cudaSuccess) return e;
       attr[gi][t] = true;
     }
-    kernel<<<grid, kBkThreads, kBkSmem, s>>>(a, maps[t]);
-    return cudaGetLastError();
+    // the V launch is the K launch's programmatic dependent: its CTAs take SMs
+    // as K's CTAs leave (the two write disjoint bytes of the tiles), and each
+    // waits for the K grid before it exits, so that the V grid ends after it
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kBkThreads, 1, 1);
+    cfg.dynamicSmemBytes = kBkSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute lattr[1];
+    lattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    lattr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = lattr;
+    cfg.numAttrs = (t == 1) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, a, maps[t]);
   };
   cudaError_t e;
   if (p.cfg.group_size == 64) {
