@@ -499,10 +499,15 @@ __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, con
 // teams, one thread each: per team a loader walks the tasks, publishes each
 // chunk's record and starts its x load as soon as the buffer is free (product
 // j - 4 complete), and an issuer starts product j once its x is in and the
-// team has read accumulator j % 4 for chunk j - 4.  Nothing waits on a CTA
-// barrier inside the loop: records, x, products and accumulators are handed
-// over through mbarriers, and an issuer thread that stalls while the tensor
-// cores take its sixteen MMAs holds up no epilogue warp.
+// team has read accumulator j % 4 for chunk j - 4; the product barrier also
+// takes the issuer's own arrival after it read the record, so a warp that sees
+// the product also sees its record.  A team's end is a record with no chunk,
+// signalled on the product barrier the same way once every warp has released
+// chunk j - 4 (an earlier signal would complete a phase past one a slow warp
+// still waits for).  Nothing waits on a CTA barrier inside the loop: records,
+// x, products and accumulators are handed over through mbarriers, and an
+// issuer thread that stalls while the tensor cores take its sixteen MMAs holds
+// up no epilogue warp.
 constexpr int kBkWarps = 20;                 // 16 epilogue + 4 serving warps
 constexpr int kBkThreads = 32 * kBkWarps;
 constexpr int kBkCols = 512;                 // four 128-column fp32 accumulators
@@ -511,8 +516,9 @@ constexpr uint32_t kBkOffA = kBkOffB + kBBytes;             // four x buffers
 constexpr uint32_t kBkOffClip = kBkOffA + 4 * kABytes;
 constexpr uint32_t kBkOffStat = kBkOffClip + 128 * 4;       // [team][chunk parity][half][128 rows] (min, max)
 constexpr uint32_t kBkOffInfo = kBkOffStat + 2 * 2 * 2 * 128 * 8;   // [8] chunk records of 8 ints
-// mbarriers: [0] R; [1 + b] x in buffer b; [5 + b] product b done; [9 + b]
-// accumulator b read (eight warps); [13 + s] record s published
+// mbarriers: [0] R; [1 + b] x in buffer b; [5 + b] product b done (its commit
+// and the issuer's arrival); [9 + b] accumulator b read (eight warps);
+// [13 + s] record s published (to the issuer)
 constexpr int kBkBars = 21;
 constexpr uint32_t kBkOffBar = kBkOffInfo + 8 * 32;
 constexpr uint32_t kBkOffMisc = kBkOffBar + kBkBars * 8;     // tensor-memory address, abort flag, last load / product per buffer
