@@ -372,21 +372,16 @@ __device__ __forceinline__ float max_of32(float acc, const float (&v)[32]) {
 // two halves through shared memory behind named barrier `qbar`, of those 64
 // threads.
 template <int GS, int TENSOR, int NS>
-__device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, const float* sclip, float2* sstat,
-                                               uint32_t (&wd)[NS][2], int qbar) {
-  // first pass: x' clipped, written back in place (the second pass reads the
-  // clipped values), and its range
-  auto clipped32 = [&](int cb, float (&v)[32]) {
-    uint32_t u[32];
-    tc_ld32(trow + 64 * hf + 32 * cb, u);
-    tc_wait_ld();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      v[i] = clip_to(__uint_as_float(u[i]), sclip[64 * hf + 32 * cb + i]);
-      u[i] = __float_as_uint(v[i]);
-    }
-    tc_st32(trow + 64 * hf + 32 * cb, u);
-  };
+__device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, const float* sclip,
+                                               const float* sclipmin, float2* sstat, uint32_t (&wd)[NS][2],
+                                               int qbar) {
+  // first pass: x' clipped and its range, per block of 32 channels.  The
+  // block's range is taken on x' first: when no lane of the warp has a value
+  // of magnitude above the block's smallest clip (sclipmin, null: always
+  // clip), no value of the block is clipped, x' in tensor memory already is
+  // the clipped value and that range is the clipped range; otherwise the
+  // block is clipped, written back in place (the second pass reads the
+  // clipped values) and its range taken again
   auto rotated32 = [&](int cb, float (&v)[32]) {
     uint32_t u[32];
     tc_ld32(trow + 64 * hf + 32 * cb, u);
@@ -398,9 +393,22 @@ __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, con
 #pragma unroll
   for (int cb = 0; cb < 2; ++cb) {
     float v[32];
-    clipped32(cb, v);
-    mn = min_of32(mn, v);
-    mx = max_of32(mx, v);
+    rotated32(cb, v);
+    float bmn = min_of32(INFINITY, v), bmx = max_of32(-INFINITY, v);
+    const float cmin = sclipmin ? sclipmin[2 * hf + cb] : -1.0f;
+    if (__any_sync(0xffffffffu, !(fmaxf(bmx, -bmn) <= cmin))) {   // warp-uniform: the store is collective
+      uint32_t u[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        v[i] = clip_to(v[i], sclip[64 * hf + 32 * cb + i]);
+        u[i] = __float_as_uint(v[i]);
+      }
+      tc_st32(trow + 64 * hf + 32 * cb, u);
+      bmn = min_of32(INFINITY, v);
+      bmx = max_of32(-INFINITY, v);
+    }
+    mn = fminf(mn, bmn);
+    mx = fmaxf(mx, bmx);
   }
   if (GS == 128) {   // the group spans both channel halves: combine with warp w ^ 4
     sstat[hf * 128 + m] = make_float2(mn, mx);
@@ -410,7 +418,7 @@ __device__ __forceinline__ ScaleZero row_codes(uint32_t trow, int hf, int m, con
     mx = fmaxf(mx, o.y);
   }
   const ScaleZero q = scale_zero(mn, mx);   // the group of these 64 channels
-  tc_wait_st();                             // the clipped values are in place
+  tc_wait_st();                             // any clipped values are in place
 
   auto clear = [&]() {
 #pragma unroll
@@ -514,7 +522,8 @@ constexpr int kBkCols = 512;                 // four 128-column fp32 accumulator
 constexpr uint32_t kBkOffB = 0;              // R^T hi | lo
 constexpr uint32_t kBkOffA = kBkOffB + kBBytes;             // four x buffers
 constexpr uint32_t kBkOffClip = kBkOffA + 4 * kABytes;
-constexpr uint32_t kBkOffStat = kBkOffClip + 128 * 4;       // [team][chunk parity][half][128 rows] (min, max)
+constexpr uint32_t kBkOffClipMin = kBkOffClip + 128 * 4;   // [4] smallest clip of each 32-channel block
+constexpr uint32_t kBkOffStat = kBkOffClipMin + 16;        // [team][chunk parity][half][128 rows] (min, max)
 constexpr uint32_t kBkOffInfo = kBkOffStat + 2 * 2 * 2 * 128 * 8;   // [8] chunk records of 8 ints
 // mbarriers: [0] R; [1 + b] x in buffer b; [5 + b] product b done (its commit
 // and the issuer's arrival); [9 + b] accumulator b read (eight warps);
@@ -569,6 +578,7 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
   constexpr int NG = 128 / GS;
   const uint32_t sA0 = smem_u32(sm + kBkOffA), sB = smem_u32(sm + kBkOffB);
   float* sclip = reinterpret_cast<float*>(sm + kBkOffClip);
+  float* sclipmin = reinterpret_cast<float*>(sm + kBkOffClipMin);
   int* info = reinterpret_cast<int*>(sm + kBkOffInfo);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBkOffBar);
   uint64_t* xfull = bars + 1;     // x of chunk j in buffer j % 4
@@ -597,6 +607,12 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
   }
   if (warp == 0) tc_alloc(smem_u32(tslot), kBkCols);
   if (tid < 128) sclip[tid] = a.clip[((size_t)TENSOR * a.Hkv + g) * 128 + tid];
+  if (tid >= 128 && tid < 132) {   // the smallest clip of channels 32 (tid - 128) ..
+    const float* c = a.clip + ((size_t)TENSOR * a.Hkv + g) * 128 + 32 * (tid - 128);
+    float v = c[0];
+    for (int i = 1; i < 32; ++i) v = fminf(v, c[i]);
+    sclipmin[tid - 128] = v;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -765,7 +781,7 @@ __device__ __forceinline__ void tc_body(const TcArgs& a, const CUtensorMap* xmap
       uint32_t wd[NS][2];
       const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16) + 128u * (uint32_t)(j & 3);
       float2* sstat = reinterpret_cast<float2*>(sm + kBkOffStat) + 256 * (2 * team + ((j >> 1) & 1));
-      const ScaleZero q = row_codes<GS, TENSOR>(trow, hf, m, sclip, sstat, wd, qbar);
+      const ScaleZero q = row_codes<GS, TENSOR>(trow, hf, m, sclip, sclipmin, sstat, wd, qbar);
       // the accumulator is read: release it to the team's issuer
       tc_fence_before();
       __syncwarp();
@@ -1077,7 +1093,7 @@ __device__ __forceinline__ void evict_body(const StepArgs& a, int B, uint8_t* sm
     constexpr int NS = (TENSOR == 0) ? 4 : 8;
     uint32_t wd[NS][2];
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-    const ScaleZero q = row_codes<GS, TENSOR>(trow, hf, m, sclip, sstat, wd, 1 + quarter);
+    const ScaleZero q = row_codes<GS, TENSOR>(trow, hf, m, sclip, nullptr, sstat, wd, 1 + quarter);
     const long long tof = rtile[m];
     if (tof >= 0) {
       const int pos = rpos[m];
