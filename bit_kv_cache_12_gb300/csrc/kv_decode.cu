@@ -501,7 +501,9 @@ struct HistLay {
   static constexpr int sq = spid + kMaxPids * 4;          // [HP][kQStride] q (q' computed in the CTA)
   static constexpr int sqr = sq + HP * kQStride * 4;      // [HP][kQrStride] q'
   static constexpr int spart = sqr + HP * kQrStride * 4; // [16 n-tiles][8] partial row sums of q'
-  static constexpr int total = spart + 16 * 8 * 4;
+  static constexpr int sqf = spart + 16 * 8 * 4;         // [8 k-steps][NT][32 lanes][2] QK B fragments
+  static constexpr int ssum = sqf + 8 * (HP / 4) * 32 * 2 * 4;   // [NT][NG][4] per-group sums of q'
+  static constexpr int total = ssum + 2 * 2 * 4 * 4;
   static constexpr int swo = 0;                           // [NW][G][128] per-warp o'
   static constexpr int swm = swo + NW * G * 128 * 4;      // [NW][G] m
   static constexpr int swl = swm + NW * G * 4;            // [NW][G] l
@@ -672,37 +674,52 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
     float* sqr = reinterpret_cast<float*>(smb + S::sqr);
     float* spart = reinterpret_cast<float*>(smb + S::spart);
     rotate_q<S::HP, NW, true>(sq, rkf, sqr, spart);   // ends with a barrier
-    // QK B fragments: column n = lane/4 -> local head 4*nt + n/2, part n%2 (hi/lo)
-    const int hl = r >> 1, e = r & 1;
-#pragma unroll
-    for (int s = 0; s < 8; ++s)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
+    // The QK B fragments and the per-group sums are the same in every warp:
+    // work item p < 8 NT (k-step p / NT, n-tile p % NT) builds one fragment
+    // pair for all 32 lanes, item 8 NT the sums; the warps take the items in
+    // turn, and every warp then loads its copy from shared memory.
+    uint32_t* sqf = reinterpret_cast<uint32_t*>(smb + S::sqf);
+    float* ssum = reinterpret_cast<float*>(smb + S::ssum);
+    for (int p = warp; p <= 8 * NT; p += NW) {
+      if (p < 8 * NT) {
+        const int s = p / NT, nt = p % NT;
+        // QK B fragments: column n = lane/4 -> local head 4*nt + n/2, part n%2 (hi/lo)
+        const int hl = r >> 1, e = r & 1;
         const float* row = sqr + (4 * nt + hl) * kQrStride + 16 * s + 2 * j;
         // group 64: the odd steps' code factor 16 is cancelled here (a power of 2);
         // group 128 removes it from the odd steps' accumulator chain instead
         const float f = (GS == 64 && (s & 1)) ? 0.0625f : 1.0f;
         const float x[4] = {row[0] * f, row[1] * f, row[8] * f, row[9] * f};
-        __half p[4];
+        __half hp[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const __half hi = __float2half_rn(x[u]);
-          p[u] = e ? __float2half_rn(x[u] - __half2float(hi)) : hi;
+          hp[u] = e ? __float2half_rn(x[u] - __half2float(hi)) : hi;
         }
-        qf[s][nt][0] = h2_as_u32(__halves2half2(p[0], p[1]));
-        qf[s][nt][1] = h2_as_u32(__halves2half2(p[2], p[3]));
+        *reinterpret_cast<uint2*>(sqf + (p * 32 + lane) * 2) =
+            make_uint2(h2_as_u32(__halves2half2(hp[0], hp[1])), h2_as_u32(__halves2half2(hp[2], hp[3])));
+      } else if (lane < 4 * NT * NG) {
+        // per-group sums of q' (over the group's 8-column n-tiles) in the units
+        // of the score accumulator (2^-24): lane = (n-tile, group, column pair)
+        const int jj = lane & 3, grp = (lane >> 2) % NG, nt = (lane >> 2) / NG;
+        float v = 0.f;
+        for (int t = grp * (GS / 8); t < (grp + 1) * (GS / 8); ++t) v += spart[t * 8 + 4 * nt + jj];
+        ssum[(nt * NG + grp) * 4 + jj] = v * 5.9604644775390625e-8f;
       }
-    // per-group sums of q' (over the group's 8-column n-tiles) in the units of
-    // the score accumulator (2^-24)
+    }
+    __syncthreads();
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint2 w = *reinterpret_cast<const uint2*>(sqf + ((s * NT + nt) * 32 + lane) * 2);
+        qf[s][nt][0] = w.x;
+        qf[s][nt][1] = w.y;
+      }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int grp = 0; grp < NG; ++grp) {
-        float v = 0.f;
-#pragma unroll
-        for (int t = grp * (GS / 8); t < (grp + 1) * (GS / 8); ++t) v += spart[t * 8 + 4 * nt + j];
-        sumq[nt][grp] = v * 5.9604644775390625e-8f;
-      }
+      for (int grp = 0; grp < NG; ++grp) sumq[nt][grp] = ssum[(nt * NG + grp) * 4 + j];
   } else {   // ---- q' fragments and per-group sums from the pre-pass ----
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint4* qp = reinterpret_cast<const uint4*>(a.qfrag + ((size_t)(b * a.Hkv + g) * 32 + lane) * QW);
