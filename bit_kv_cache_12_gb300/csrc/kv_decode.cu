@@ -176,7 +176,8 @@ struct RotFrags {
 // partial row sums go to P[n-tile][row] (for the per-group sums of q').
 // Ends with a barrier.
 template <int NROWS, int NW, bool kSums = false>
-__device__ void rotate_q(const float* X, const RotFrags<NW>& rkf, float* Y, float* P = nullptr) {
+__device__ void rotate_q(const float* X, const RotFrags<NW>& rkf, float* Y, float* P = nullptr,
+                         uint32_t* SA = nullptr) {
   static_assert(NROWS <= 8, "rows");
   constexpr int NTW = (16 + NW - 1) / NW;
   constexpr bool kSplitRows = NROWS <= 4;   // hi rows 0..3, lo rows 4..7 (else 0..7 / 8..15)
@@ -191,8 +192,8 @@ __device__ void rotate_q(const float* X, const RotFrags<NW>& rkf, float* Y, floa
   const bool row_ok = xrow < NROWS;
   const bool lo_lane = kSplitRows && r >= 4;   // this lane's row holds the lo terms
   constexpr float kIn = 1.0f / 256.0f;
-#pragma unroll
-  for (int s = 0; s < 8; ++s) {
+  // the A fragments of k-step s (the same in every warp)
+  auto afrag = [&](int s, uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
     // A: row r, k index kappa -> input channel 32*(kappa%8/2) + 4s + 2*(kappa/8) + kappa%2
     float4 x = row_ok ? *reinterpret_cast<const float4*>(X + xrow * kQStride + 36 * j + 4 * s)
                       : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -200,7 +201,6 @@ __device__ void rotate_q(const float* X, const RotFrags<NW>& rkf, float* Y, floa
     const __half2 h01 = __floats2half2_rn(x.x, x.y), h23 = __floats2half2_rn(x.z, x.w);
     const __half2 l01 = __floats2half2_rn(x.x - __low2float(h01), x.y - __high2float(h01));
     const __half2 l23 = __floats2half2_rn(x.z - __low2float(h23), x.w - __high2float(h23));
-    uint32_t a0, a1, a2, a3;
     if (kSplitRows) {
       a0 = lo_lane ? h2_as_u32(l01) : h2_as_u32(h01);
       a2 = lo_lane ? h2_as_u32(l23) : h2_as_u32(h23);
@@ -208,6 +208,26 @@ __device__ void rotate_q(const float* X, const RotFrags<NW>& rkf, float* Y, floa
     } else {
       a0 = h2_as_u32(h01); a2 = h2_as_u32(h23);
       a1 = h2_as_u32(l01); a3 = h2_as_u32(l23);
+    }
+  };
+  // with SA (8 k-steps x 32 lanes x 4 words of shared memory), warp w < 8
+  // builds k-step w for every lane and the others load them
+  if (SA) {
+    if (warp < 8) {
+      uint32_t a0, a1, a2, a3;
+      afrag(warp, a0, a1, a2, a3);
+      *reinterpret_cast<uint4*>(SA + (warp * 32 + lane) * 4) = make_uint4(a0, a1, a2, a3);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    uint32_t a0, a1, a2, a3;
+    if (SA) {
+      const uint4 w = *reinterpret_cast<const uint4*>(SA + (s * 32 + lane) * 4);
+      a0 = w.x; a1 = w.y; a2 = w.z; a3 = w.w;
+    } else {
+      afrag(s, a0, a1, a2, a3);
     }
 #pragma unroll
     for (int u = 0; u < NTW; ++u) {
@@ -502,7 +522,8 @@ struct HistLay {
   static constexpr int sqr = sq + HP * kQStride * 4;      // [HP][kQrStride] q'
   static constexpr int spart = sqr + HP * kQrStride * 4; // [16 n-tiles][8] partial row sums of q'
   static constexpr int sqf = spart + 16 * 8 * 4;         // [8 k-steps][NT][32 lanes][2] QK B fragments
-  static constexpr int ssum = sqf + 8 * (HP / 4) * 32 * 2 * 4;   // [NT][NG][4] per-group sums of q'
+                                                         // (first the A fragments of q: [8][32][4])
+  static constexpr int ssum = sqf + 8 * 32 * 4 * 4;      // [NT][NG][4] per-group sums of q'
   static constexpr int total = ssum + 2 * 2 * 4 * 4;
   static constexpr int swo = 0;                           // [NW][G][128] per-warp o'
   static constexpr int swm = swo + NW * G * 128 * 4;      // [NW][G] m
@@ -673,7 +694,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
   if (local) {   // ---- q' = q R_k here, then its fragments and per-group sums ----
     float* sqr = reinterpret_cast<float*>(smb + S::sqr);
     float* spart = reinterpret_cast<float*>(smb + S::spart);
-    rotate_q<S::HP, NW, true>(sq, rkf, sqr, spart);   // ends with a barrier
+    rotate_q<S::HP, NW, true>(sq, rkf, sqr, spart, reinterpret_cast<uint32_t*>(smb + S::sqf));   // ends with a barrier
     // The QK B fragments and the per-group sums are the same in every warp:
     // work item p < 8 NT (k-step p / NT, n-tile p % NT) builds one fragment
     // pair for all 32 lanes, item 8 NT the sums; the warps take the items in
