@@ -215,7 +215,7 @@ def test_crafted_rows_reach_every_branch():
         sf = s.astype(np.float64)[..., None]; zf = z.astype(np.float64)[..., None]
         with np.errstate(divide="ignore", invalid="ignore"):
             qv = (y.astype(np.float64) - zf) / sf
-        frac = np.abs(qv - np.floor(qv) - 0.5)
+            frac = np.abs(qv - np.floor(qv) - 0.5)   # nan where s = 0: not live below
         live = np.isfinite(qv) & (qv >= 0) & (qv <= 3)
         assert np.any(live & (frac == 0)), "exact ties"
         assert np.any(live & (frac > 0) & (frac < 2.0 ** -18)), "near ties"
