@@ -645,6 +645,19 @@ def run_headline(env, wl):
     h2d = stage_host.numel()
     d2h = out_host.numel() * 4
 
+    # where the staged step's time goes: each copy alone, and the input copy
+    # followed by the decode (every copy-engine <-> kernel hand-over on the
+    # stream waits for the previous operation to finish)
+    def h2d_then_decode(i):
+        stage_dev.copy_(stage_host, non_blocking=True)
+        rig.decode(i, q=q_dev, lens=[meta_dev[0], meta_dev[1], meta_dev[2], meta_dev[3]])
+
+    t_parts = [env.timed(lambda i: stage_dev.copy_(stage_host, non_blocking=True), args.steps, 3,
+                         per_step_pass=False),
+               env.timed(lambda i: out_host.copy_(rig.out, non_blocking=True), args.steps, 3,
+                         per_step_pass=False),
+               env.timed(h2d_then_decode, args.steps, 3, per_step_pass=False)]
+
     # ---- the same call handed the pinned host buffers themselves ----
     q_host = stage_host[:q_bytes].view(torch.bfloat16).view(B, Hq, 128)
     meta_host = stage_host[q_bytes:].view(torch.int32).view(4, B)
@@ -673,6 +686,7 @@ def run_headline(env, wl):
     if rig.pool.error():
         raise RuntimeError("device error during the end-to-end and multi-query steps")
     us_e2e, us_mapped = env.max_ranks([float(t_e2e.mean_ms * 1e3), float(t_mapped.mean_ms * 1e3)])
+    us_h2d, us_d2h, us_h2d_dec = env.max_ranks([float(t.mean_ms * 1e3) for t in t_parts])
 
     # ---- the online step at batch 1 (mutates the pool: last) ----
     online = online_step(env, rig, args.steps, args.warmup, us)
@@ -697,7 +711,13 @@ def run_headline(env, wl):
         "e2e": {"value": us_e2e, "unit": "us", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
                 "what": "kv_decode_attention with host buffers: one pinned staging copy in (q and "
-                        "the four length arrays), the output copied back, both inside the timed region"},
+                        "the four length arrays), the output copied back, both inside the timed region",
+                "breakdown_us": {"h2d_copy_alone": us_h2d, "d2h_copy_alone": us_d2h,
+                                 "h2d_copy_then_decode": us_h2d_dec, "decode_alone": us,
+                                 "what": "back-to-back steps of each part alone; the copies take about "
+                                         "2 us each on their own, the rest of the staged step is the "
+                                         "hand-over between the copy engine and the kernels on one "
+                                         "stream (the decode cannot start its prologue under a copy)"}},
         "e2e_host_mapped": {"value": us_mapped, "unit": "us", "h2d_bytes_per_step": int(h2d),
                             "d2h_bytes_per_step": int(d2h),
                             "what": "the same call given the pinned host buffers directly: the kernel "
