@@ -524,11 +524,16 @@ struct HistLay {
   static constexpr int sqf = spart + 16 * 8 * 4;         // [8 k-steps][NT][32 lanes][2] QK B fragments
                                                          // (first the A fragments of q: [8][32][4])
   static constexpr int ssum = sqf + 8 * 32 * 4 * 4;      // [NT][NG][4] per-group sums of q'
-  static constexpr int total = ssum + 2 * 2 * 4 * 4;
-  static constexpr int swo = 0;                           // [NW][G][128] per-warp o'
-  static constexpr int swm = swo + NW * G * 128 * 4;      // [NW][G] m
-  static constexpr int swl = swm + NW * G * 4;            // [NW][G] l
-  static_assert(swl + NW * G * 4 + G * 4 <= bars, "the warp results fit in the ring");
+  // the warps' results, written by each warp as its loop ends (not over the
+  // ring, which other warps may still be reading); rows of kWoStride floats
+  // put the four heads a lane row writes in different banks
+  static constexpr int kWoStride = 136;
+  static constexpr int swo = (ssum + 2 * 2 * 4 * 4 + 15) / 16 * 16;   // [NW][G][kWoStride] per-warp o'
+  static constexpr int swm = swo + NW * G * kWoStride * 4;             // [NW][G] m
+  static constexpr int swl = swm + NW * G * 4;                         // [NW][G] l
+  static constexpr int swt = swl + NW * G * 4;                         // [NW][G] the warps' weights
+  static constexpr int sM = swt + NW * G * 4;                          // [G] each head's maximum
+  static constexpr int total = sM + G * 4;
 };
 
 // Shared memory of a tier CTA (byte offsets).  R_v^T, the warp results and the
@@ -996,17 +1001,13 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
     const int issued = started ? min(k + kStages, n_warp) : min(kStages - 1, n_warp);
     for (int kk = k; kk < issued; ++kk) mbar_wait(wbar + kk % kStages, (kk / kStages) & 1, a.wait_polls);
   }
-  ok = __syncthreads_and(ok);   // every warp is done with its ring before the results reuse it
-  if (lane < kStages) mbar_inval(wbar + lane);
-  if (!ok) {   // the split's result is skipped
-    write_empty_partial<G, NW>(part);
-    return;
-  }
+  if (lane < kStages) mbar_inval(wbar + lane);   // this warp's copies are all in (or given up on)
 
-  // ---- warp results -> shared memory (over the ring) ----
+  // ---- this warp's results -> shared memory, as soon as its loop ends ----
   float* swo = reinterpret_cast<float*>(smb + S::swo);
   float* swm = reinterpret_cast<float*>(smb + S::swm);
   float* swl = reinterpret_cast<float*>(smb + S::swl);
+  constexpr int WS = S::kWoStride;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const float l = warp_sum_xor(l_run[nt], 4);
@@ -1015,7 +1016,7 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
     for (int grp = 0; grp < NG; ++grp) z[grp] = warp_sum_xor(zs[nt][grp], 4);
     const int hh = 4 * nt + j;
     if (hh < G) {
-      float* o = swo + (warp * G + hh) * 128;
+      float* o = swo + (warp * G + hh) * WS;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float zz = z[(GS == 64) ? (i >> 2) : 0];
@@ -1031,33 +1032,36 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
       }
     }
   }
-  __syncthreads();
+  ok = __syncthreads_and(ok);   // every warp's results are in
+  if (!ok) {   // the split's result is skipped
+    write_empty_partial<G, NW>(part);
+    return;
+  }
   // the warps merged with the log-sum-exp rule into the split's partial (rotated
-  // basis): each head's maximum, then every warp's weight exp2(m_w - M) once,
-  // then every output element a sum of NW products
-  float* sM = swl + NW * G;   // [G]
-  if (threadIdx.x < G) {
+  // basis): for each (warp, head) its head's maximum and the warp's weight
+  // exp2(m_w - M), then every output element a sum of NW products
+  float* swt = reinterpret_cast<float*>(smb + S::swt);
+  float* sM = reinterpret_cast<float*>(smb + S::sM);
+  if (threadIdx.x < NW * G) {
+    const int hh = threadIdx.x % G;
     float M = kNegInf;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, swm[w * G + threadIdx.x]);
-    sM[threadIdx.x] = M;
-  }
-  __syncthreads();
-  if (threadIdx.x < NW * G) {   // swm becomes the warps' weights
-    const float mw = swm[threadIdx.x], M = sM[threadIdx.x % G];
-    swm[threadIdx.x] = (mw == kNegInf || M == kNegInf) ? 0.f : exp2f(mw - M);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, swm[w * G + hh]);
+    const float mw = swm[threadIdx.x];
+    swt[threadIdx.x] = (mw == kNegInf || M == kNegInf) ? 0.f : exp2f(mw - M);
+    if (threadIdx.x < G) sM[threadIdx.x] = M;
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
     const int hh = idx >> 7, c = idx & 127;
     float O = 0.f;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) O = fmaf(swm[w * G + hh], swo[(w * G + hh) * 128 + c], O);
+    for (int w = 0; w < NW; ++w) O = fmaf(swt[w * G + hh], swo[(w * G + hh) * WS + c], O);
     part[hh * kPart + 4 + c] = O;
     if (c == 0) {
       float L = 0.f;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) L = fmaf(swm[w * G + hh], swl[w * G + hh], L);
+      for (int w = 0; w < NW; ++w) L = fmaf(swt[w * G + hh], swl[w * G + hh], L);
       part[hh * kPart + 0] = sM[hh];
       part[hh * kPart + 1] = L;
     }
