@@ -1296,7 +1296,7 @@ __device__ void tier_merge(const DecodeArgs& a, int b, int g, uint8_t* smb) {
           const unsigned want = (n == 32 ? ~0u : ((1u << n) - 1u)) << (s & 31);
           done = (ld_acquire_u32(mask + (s >> 5)) & want) == want;
         }
-        if (!done) __nanosleep(64);
+        if (!done) __nanosleep(16);
       }
       ctl[0] = done;
     }
@@ -1378,7 +1378,7 @@ __device__ void tier_merge(const DecodeArgs& a, int b, int g, uint8_t* smb) {
           const unsigned want = (n == 32 ? ~0u : ((1u << n) - 1u)) << (s & 31);
           done = (ld_acquire_u32(mask + (s >> 5)) & want) == want;
         }
-        if (!done) __nanosleep(64);
+        if (!done) __nanosleep(16);
       }
       ctl[0] = done;
     }
