@@ -264,7 +264,7 @@ __device__ void rotate_q(const float* X, const RotFrags<NW>& rkf, float* Y, floa
 
 // Merge the NW warps' (m, l, o) in shared memory into one partial per head.
 // merged[h][c] receives o; sm_m / sm_l receive m and l.
-template <int G, int NW>
+template <int G, int NW, int WS>
 __device__ void merge_warps(const float* swo, const float* swm, const float* swl, float* merged,
                             float* sm_m, float* sm_l) {
   for (int idx = threadIdx.x; idx < G * 128; idx += NW * 32) {
@@ -279,7 +279,7 @@ __device__ void merge_warps(const float* swo, const float* swm, const float* swl
         const float mw = swm[w * G + h];
         const float f = (mw == kNegInf) ? 0.f : exp2f(mw - M);
         L = fmaf(f, swl[w * G + h], L);
-        O = fmaf(f, swo[(w * G + h) * 128 + (idx & 127)], O);
+        O = fmaf(f, swo[(w * G + h) * WS + (idx & 127)], O);
       }
     }
     merged[idx] = O;
@@ -551,8 +551,9 @@ struct TierLay {
   static constexpr int bar = (hist_l + G * 4 + 7) / 8 * 8;             // mbarrier of the R_v^T copy
   static constexpr int ctl = bar + 8;                                  // merge progress
   static constexpr int total = ctl + 16;
-  static constexpr int swo = stage;                                    // [NW][G][128]
-  static constexpr int swm = swo + NW * G * 128 * 4;                   // [NW][G]
+  static constexpr int kWoStride = 136;   // warp result rows: 128 + 8 keeps the stores conflict-free
+  static constexpr int swo = stage;                                    // [NW][G][kWoStride]
+  static constexpr int swm = swo + NW * G * kWoStride * 4;             // [NW][G]
   static constexpr int swl = swm + NW * G * 4;                         // [NW][G]
   static constexpr int rv = (swl + NW * G * 4 + 1023) / 1024 * 1024;   // [128][128] R_v^T
   static constexpr int GP = (G + 3) & ~3;
@@ -1224,7 +1225,7 @@ __device__ void tier_merge(const DecodeArgs& a, int b, int g, uint8_t* smb) {
     const float l = warp_sum_xor(l_run[u], 4);
     const int hh = 4 * u + j;
     if (hh < G) {
-      float* o = swo + (warp * G + hh) * 128;
+      float* o = swo + (warp * G + hh) * S::kWoStride;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         o[16 * i + r] = oacc[i][u][0] + oacc[i][u][1];
@@ -1237,7 +1238,7 @@ __device__ void tier_merge(const DecodeArgs& a, int b, int g, uint8_t* smb) {
     }
   }
   __syncthreads();
-  merge_warps<G, NW>(swo, swm, swl, tier_o, tier_m, tier_l);   // ends with a barrier
+  merge_warps<G, NW, S::kWoStride>(swo, swm, swl, tier_o, tier_m, tier_l);   // ends with a barrier
 
   // ---- R_v^T for the one back-rotation: up to 4 query columns as fp32 into the
   // staging area, now free (SIMT rotation); more as MMA fragments in registers
