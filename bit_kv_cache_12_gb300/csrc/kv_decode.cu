@@ -30,11 +30,12 @@
 //     products (about 16 significant bits overall; measured output error
 //     about 2e-5 relative to the fp64 oracle at 100k tokens).  Online softmax
 //     per head with warp-shuffle max and a lazily moved exponent reference;
-//     the warps merge in shared memory and the split writes its partial
-//     (m, l, o') in the rotated basis, then sets its bit in the pair's arrival
-//     mask (release).
+//     each warp puts its result in shared memory as its loop ends, the warps
+//     merge there and the split writes its partial (m, l, o') in the rotated
+//     basis, then sets its bit in the pair's arrival mask (release).
 //   * tier CTA: stages the BF16 sink + recent storage into shared memory
-//     before the lengths are known, attends the live rows in SIMT fp32, then
+//     before the lengths are known, attends the live rows on the tensor cores
+//     (bf16 MMA, the softmax weights as bf16 hi + lo), then
 //     merges the history partials in split order as they arrive (acquire),
 //     rotates the merged history value sum back by R_v^T once and combines it
 //     with its own result into the fp32 output (and, for several queries per
@@ -324,8 +325,7 @@ __device__ bool last_to_arrive(unsigned* ticket, unsigned total) {
 constexpr int kMergeBatch = 20;
 
 // ---------------------------------------------------------------------------
-// BF16 rows: warp-cooperative SIMT attention over a token range
-// (QK with one token per lane, PV with four channels per lane)
+// shared helpers: the zero tile, ldmatrix
 // ---------------------------------------------------------------------------
 // A zero INT2 tile (largest tile size): copied in place of a tile behind an
 // invalid page id, so every ring slot always holds finite data.
@@ -1070,8 +1070,8 @@ __device__ void int2_history(const DecodeArgs& a, int b, int g, int split, uint8
 }
 
 // The tier CTA of (sequence b, KV head g), launched after every history
-// split: attends the BF16 sink + recent rows (staged in shared memory, SIMT
-// fp32), then merges the history splits' partials in split order as they
+// split: attends the BF16 sink + recent rows (staged in shared memory, on the
+// tensor cores), then merges the history splits' partials in split order as they
 // arrive (each split sets its bit in the pair's arrival mask with a release
 // reduction after writing its partial), rotates the merged history value sum
 // back by R_v^T once, combines it with the tier result and writes the output.
