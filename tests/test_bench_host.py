@@ -70,3 +70,16 @@ def test_traffic_record_counts_only_for_its_sources(tmp_path):
     assert b.measured_traffic("w") is None
     b.TRAFFIC_RECORD = str(tmp_path / "missing.json")
     assert b.measured_traffic("w") is None
+
+
+def test_append_bytes_and_flops_of_the_append_workload():
+    """64 sequences x 4096 tokens x 8 KV heads: K and V rows in (bf16, 256 B
+    each), and out per token the K and V share of a stored page tile (1,280 B
+    per 16 tokens at group 64, 1,152 B at group 128); the rotation is one
+    128 x 128 product per row and tensor."""
+    b = _bench()
+    n = 64 * 4096 * 8
+    alg, flops = b.append_bytes_flops(n, 64)
+    assert alg == n * (2 * 256 + 1280 // 16) == 1_241_513_984
+    assert b.append_bytes_flops(n, 128)[0] == n * (2 * 256 + 1152 // 16)
+    assert flops == 2 * 2 * 128 * 128 * n
